@@ -1,0 +1,392 @@
+"""Benchmark of the DoRA norm + compose hot path on GB300.
+
+One step = the whole path on one module of the 8192-wide rank-384 workload
+(out = in = 8192, r = 384, T = 15360 tokens = batch 3 x seq 5120, bf16
+activations, fp32 weights): factored norm -> compose forward -> compose
+backward, through the C ABI.  Prints ONE JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the fp64 CPU oracle (the method's plain definition) on
+a bounded sample of the same workload, on the host cores.
+
+Multi-GPU: one process per GPU under torchrun; every rank runs an independent
+replica on its own seeded inputs (the path has no exchange step), timing is
+the max over ranks, and the value is the aggregate over ranks ("weak").
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")   # the CPU baseline runs single-threaded
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from parameter_efficient_fine_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "fused DoRA compose fwd+bwd HBM GB/s (% of GB300 peak); factored-norm µs/module"
+WORKLOAD = "high_rank"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def algorithmic(sh) -> dict:
+    """Bytes each kernel must move at minimum (each input read once, each output
+    written once) and the norm's algorithmic flops (single pass, no TF32 split)."""
+    e = sh.act_bytes
+    T, out, inp, r = sh.T, sh.out, sh.inp, sh.r
+    return {
+        "fwd_bytes": 3 * T * out * e + 4 * out,                # base, lora -> y ; g
+        "bwd_bytes": 5 * T * out * e + 3 * 4 * out,            # dy, base, lora -> d_base, d_lora ; g, n, d_mag
+        "norm_bytes": 4 * (out * inp + r * inp + out * r + 3 * out),
+        "norm_flops": 2 * out * inp * r + 2 * r * r * inp + 2 * out * r * r,
+    }
+
+
+def peaks() -> dict:
+    p = {"hbm_gbs": FALLBACK_HBM_GBS, "bf16_tflops": FALLBACK_BF16_TFLOPS, "source": "fallback"}
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            m = json.load(f)
+        p = {"hbm_gbs": float(m["hbm_gbs"]), "bf16_tflops": float(m["bf16_tflops"]),
+             "bf16_tflops_sustained": float(m.get("bf16_tflops_sustained", m["bf16_tflops"])), "source": "measured"}
+    except Exception:
+        pass
+    return p
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for nm, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(nm)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle arm (also the cpu_baseline leg of our own line)
+# ---------------------------------------------------------------------------
+def oracle_sample(sh, d, tokens: int, rows: int) -> dict:
+    """Times the fp64 oracle on a bounded sample: compose fwd + bwd on the first
+    `tokens` tokens (all columns), and the dense norm on the first `rows` rows."""
+    import oracle
+    s = d["s"]
+    base = oracle.bf16_bits_to_f64(d["base"][:tokens])
+    lora = oracle.bf16_bits_to_f64(d["lora"][:tokens])
+    dy = oracle.bf16_bits_to_f64(d["dy"][:tokens])
+    t0 = time.perf_counter()
+    n, g = oracle.weight_norm(d["W0"][:rows], d["A"], d["B"][:rows], d["m"][:rows], s)
+    t1 = time.perf_counter()
+    g_full = np.ones(sh.out)
+    g_full[:rows] = g
+    n_full = np.ones(sh.out)
+    n_full[:rows] = n
+    y = oracle.compose_fwd(base, lora, g_full, s)
+    t2 = time.perf_counter()
+    oracle.compose_bwd(dy, base, lora, g_full, n_full, s)
+    t3 = time.perf_counter()
+    sub = wl.ModuleShape(sh.name, sh.out, sh.inp, sh.r, tokens, sh.act, sh.sigma_B, sh.sigma_m, True, False)
+    a = algorithmic(sub)
+    del y
+    return {"compose_s": (t3 - t1), "norm_s": (t1 - t0), "compose_bytes": a["fwd_bytes"] + a["bwd_bytes"],
+            "norm_us_per_module": (t1 - t0) * 1e6 * sh.out / rows, "tokens": tokens, "rows": rows}
+
+
+def cpu_baseline(sh, d, tokens=4096, rows=1024, budget_s=10.0, max_reps=8) -> dict:
+    """The oracle as it stands, single-threaded, repeated on the same bounded
+    sample until about `budget_s` seconds of CPU work have been timed."""
+    cb = cs = ns = 0.0
+    reps = 0
+    t0 = time.perf_counter()
+    while reps < max_reps and (reps == 0 or time.perf_counter() - t0 < budget_s):
+        r = oracle_sample(sh, d, tokens, rows)
+        cb += r["compose_bytes"]
+        cs += r["compose_s"]
+        ns += r["norm_s"]
+        reps += 1
+    return {"value": cb / cs / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"fp64 numpy oracle, 1 thread, {reps} repetitions: compose fwd+bwd on {tokens} of {sh.T} "
+                      f"tokens x {sh.out} columns; dense norm on {rows} of {sh.out} rows",
+            "norm_us_per_module": ns / reps * 1e6 * sh.out / rows}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    sh = wl.shape(WORKLOAD)
+    d = wl.make_module(sh, wl.seed_for(WORKLOAD))
+    tokens, rows = 768, 256
+    for _ in range(args.warmup):
+        oracle_sample(sh, d, tokens, rows)
+    times, vals, norm_us = [], [], []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        r = oracle_sample(sh, d, tokens, rows)
+        times.append(time.perf_counter() - t0)
+        vals.append(r["compose_bytes"] / r["compose_s"] / 1e9)
+        norm_us.append(r["norm_us_per_module"])
+    value = statistics.mean(vals)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * statistics.mean(times),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{WORKLOAD}: out=in={sh.out}, r={sh.r}, T={sh.T} bf16 activations, fp32 weights",
+                   "sample_per_step": f"compose fwd+bwd on {tokens} tokens, dense norm on {rows} rows"},
+        "norm_us_per_module": statistics.mean(norm_us),
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{tokens} tokens x {sh.out} columns compose fwd+bwd; {rows} norm rows"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import parameter_efficient_fine_gb300 as dora
+    from parameter_efficient_fine_gb300 import build as dbuild
+
+    dbuild.build()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    sh = wl.shape(WORKLOAD)
+    d = wl.make_module(sh, wl.seed_for(WORKLOAD, rank))
+    s = d["s"]
+    alg = algorithmic(sh)
+
+    def f32(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+    def bf16(a):
+        return torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16)
+
+    W0, A, B, m = (f32(d[k]) for k in ("W0", "A", "B", "m"))
+    base, lora, dy = (bf16(d[k]) for k in ("base", "lora", "dy"))
+    norm = torch.empty(sh.out, device=dev)
+    g = torch.empty(sh.out, device=dev)
+    y = torch.empty_like(base)
+    db = torch.empty_like(base)
+    dl = torch.empty_like(base)
+    dm = torch.empty(sh.out, device=dev)
+    ws_n = torch.empty(dora.dora_norm_factored_workspace(sh.out, sh.inp, sh.r), dtype=torch.uint8, device=dev)
+    ws_b = torch.empty(dora.dora_compose_bwd_workspace(sh.T, sh.out), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        dora.dora_norm_factored(W0, A, B, m, s, norm, g, ws_n, stream)
+        if ev is not None:
+            ev[1].record(stream)
+        dora.dora_compose_fwd(base, lora, g, s, y, stream)
+        if ev is not None:
+            ev[2].record(stream)
+        dora.dora_compose_bwd(dy, base, lora, g, norm, s, db, dl, dm, ws_b, stream)
+        if ev is not None:
+            ev[3].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if dora.dora_device_error() != 0:
+        raise RuntimeError("a kernel wait gave up during warm-up")
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    try:
+        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        gpu_id = str(local_rank)
+    clocks = ClockSampler(gpu_id)
+    clocks.start()
+    launches0 = dora.dora_kernel_launches()
+    barrier()
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for k in range(args.steps):
+        step(evs[k])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    launches = dora.dora_kernel_launches() - launches0
+    clk = clocks.stop()
+    if dora.dora_device_error() != 0:
+        raise RuntimeError("a kernel wait gave up during the timed steps")
+
+    total_ms = t_start.elapsed_time(t_end)
+    norm_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    fwd_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    bwd_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
+    if dist is not None:
+        t = torch.tensor([total_ms, norm_ms, fwd_ms, bwd_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms, norm_ms, fwd_ms, bwd_ms = t.tolist()
+
+    compose_bytes = alg["fwd_bytes"] + alg["bwd_bytes"]
+    value = world * compose_bytes / ((fwd_ms + bwd_ms) * 1e-3) / 1e9
+    pk = peaks()
+
+    # ---- end to end through the public API, host buffers, copies timed
+    e2e = None
+    if not args.no_e2e:
+        host_in = {k: v.cpu().pin_memory() for k, v in
+                   (("W0", W0), ("A", A), ("B", B), ("m", m), ("base", base), ("lora", lora), ("dy", dy))}
+        host_out = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in
+                    (("y", y), ("db", db), ("dl", dl), ("dm", dm), ("norm", norm), ("g", g))}
+        dev_in = {"W0": W0, "A": A, "B": B, "m": m, "base": base, "lora": lora, "dy": dy}
+        dev_out = {"y": y, "db": db, "dl": dl, "dm": dm, "norm": norm, "g": g}
+        h2d = sum(v.numel() * v.element_size() for v in host_in.values())
+        d2h = sum(v.numel() * v.element_size() for v in host_out.values())
+
+        def e2e_step():
+            for k, v in host_in.items():
+                dev_in[k].copy_(v, non_blocking=True)
+            step()
+            for k, v in host_out.items():
+                v.copy_(dev_out[k], non_blocking=True)
+
+        for _ in range(max(1, args.warmup)):
+            e2e_step()
+        torch.cuda.synchronize()
+        barrier()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        e2e_ms = a.elapsed_time(b) / args.steps
+        if dist is not None:
+            t = torch.tensor([e2e_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms = t.item()
+        e2e = {"value": world * compose_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+
+    bwd_gbs = alg["bwd_bytes"] / (bwd_ms * 1e-3) / 1e9
+    fwd_gbs = alg["fwd_bytes"] / (fwd_ms * 1e-3) / 1e9
+    norm_us = norm_ms * 1e3
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{WORKLOAD}: DoRA module out=in={sh.out}, r={sh.r} (s=32/sqrt(r)), "
+                               f"T={sh.T} tokens (batch 3 x seq 5120), bf16 activations, fp32 weights; "
+                               "step = factored norm + compose fwd + compose bwd",
+                   "l2": "inputs larger than L2 (W0 268 MB; each activation 252 MB)",
+                   "parallelism": "replicas" if world > 1 else "single"},
+        "pct_of_hbm_peak": 100.0 * value / world / pk["hbm_gbs"],
+        "norm_us_per_module": norm_us,
+        "breakdown": {"norm_us": norm_us, "fwd_us": fwd_ms * 1e3, "bwd_us": bwd_ms * 1e3,
+                      "fwd_gbs": fwd_gbs, "bwd_gbs": bwd_gbs,
+                      "norm_tflops_algorithmic": alg["norm_flops"] / (norm_ms * 1e-3) / 1e12,
+                      "norm_tflops_issued_3xtf32": 3 * alg["norm_flops"] / (norm_ms * 1e-3) / 1e12},
+        "roofline": {"bound": "hbm", "kernel": "compose_bwd", "achieved": bwd_gbs, "peak": pk["hbm_gbs"],
+                     "unit": "GB/s", "frac": bwd_gbs / pk["hbm_gbs"], "traffic": None,
+                     "peak_source": pk["source"]},
+        "gpu_launches": launches,
+        "clocks": clk,
+    }
+    if e2e is not None:
+        line["e2e"] = e2e
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(sh, d)
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_ours(args, rank, world, local_rank)
+
+
+if __name__ == "__main__":
+    main()

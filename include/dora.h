@@ -1,0 +1,187 @@
+/*
+ * dora.h -- C ABI of libdora: the DoRA weight-norm and compose hot path on
+ * GB300 (sm_103a).
+ *
+ * Method source (cited below as "P1 ¶<opening words>"):
+ *   P1 = web page "人工智能训练新突破：Anthropic团队破解大模型微调内存瓶颈难题"
+ *        (techwalker.com, 2026-04-01), summarising arXiv:2603.22276.
+ *
+ * Notation: W0[out,in] frozen base weight, A[r,in] and B[out,r] the low-rank
+ * adapter, s its scale, m[out] the DoRA magnitude; activations base = x W0^T
+ * and lora = x A^T B^T (NOT pre-scaled by s) are [T,out].
+ *
+ *   n_i  = || W0_i + s (B A)_i ||                       (per output row)
+ *   g_i  = m_i / n_i
+ *   y    = base + (g-1)*base + g*s*lora                 (g broadcast over T)
+ *   d_base = g*dy,  d_lora = s*g*dy,
+ *   d_mag_j = sum_t dy[t,j] * (base[t,j] + s*lora[t,j]) / n_j   (n held constant)
+ *
+ * Conventions shared by every entry point:
+ *   - Every data pointer is a DEVICE pointer owned by the caller.  The library
+ *     never allocates, frees or synchronises; every call is asynchronous on
+ *     `stream` (NULL = the legacy default stream).
+ *   - Arrays are dense and row-major with the shapes given; no aliasing
+ *     between any input and any output.
+ *   - Argument errors are detected on the host before anything is launched and
+ *     return a status with no side effect.  A failed launch returns
+ *     DORA_ERR_CUDA.  Kernels that wait on on-chip barriers give up after a
+ *     bounded time and record it in a device word read by dora_device_error().
+ *   - Results are bitwise reproducible for a given shape on a given device.
+ *   - Only sm_103 devices are accepted (DORA_ERR_ARCH otherwise).
+ */
+#ifndef DORA_H
+#define DORA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t / CUstream. */
+typedef struct CUstream_st *dora_stream_t;
+
+typedef enum {
+  DORA_OK = 0,
+  DORA_ERR_NULL = 1,       /* a required pointer is NULL                          */
+  DORA_ERR_SHAPE = 2,      /* a size is negative, zero where not allowed, or too large */
+  DORA_ERR_ALIGN = 3,      /* a pointer or row stride breaks an alignment rule    */
+  DORA_ERR_DTYPE = 4,      /* unknown activation dtype                            */
+  DORA_ERR_WORKSPACE = 5,  /* workspace NULL, misaligned or smaller than required */
+  DORA_ERR_ARCH = 6,       /* current device is not sm_103                        */
+  DORA_ERR_CUDA = 7,       /* a CUDA runtime/driver call or launch failed         */
+  DORA_ERR_DEVICE = 8      /* a kernel's bounded on-chip wait gave up (see dora_device_error) */
+} dora_status;
+
+typedef enum {
+  DORA_F32 = 0,            /* activations and their gradients are float32  */
+  DORA_BF16 = 1            /* activations and their gradients are bfloat16 */
+} dora_dtype;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *dora_status_str(dora_status st);
+
+/* ------------------------------------------------------------------------ */
+/* (a) factored per-output-row weight norm                                   */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Bytes of device workspace dora_norm_factored needs for this shape.  Pure
+ * host arithmetic (no CUDA call); an upper bound valid on any device.  It grows
+ * as O((out + in)*r + r^2) -- rank-dependent factors only, never out*in
+ * (P1 ¶第一个创新是"因式分解规范化"技术: memory O(out*in) -> O(out*r + r^2)).
+ * Returns 0 for an invalid shape.
+ */
+size_t dora_norm_factored_workspace(int64_t out, int64_t in, int64_t r);
+
+/*
+ * norm[i] = || W0_i + s (B A)_i ||,  g[i] = m[i] / norm[i]   for i < out.
+ *
+ * P1 ¶第一个创新是"因式分解规范化"技术: the squared norm is evaluated as a base
+ * term, a cross term and a Gram term,
+ *     n_i^2 = ||W0_i||^2 + 2 s <U_i, B_i> + s^2 B_i G B_i^T,
+ *     U = W0 A^T [out,r],  G = A A^T [r,r],
+ * so the out x in adapted weight is never formed.  The contractions run on the
+ * tensor cores in a 3-pass TF32 split (hi*hi + hi*lo + lo*hi) with fp32
+ * accumulation; n^2 is clamped at 0 before the square root; g is an IEEE
+ * division with no epsilon (n = 0 gives inf/NaN).
+ *
+ *   W0    float32 [out, in]    16-byte aligned, in % 4 == 0
+ *   A     float32 [r, in]      16-byte aligned
+ *   B     float32 [out, r]     16-byte aligned (any r >= 1)
+ *   m     float32 [out]        4-byte aligned
+ *   s     adapter scale (e.g. alpha/sqrt(r))
+ *   norm  float32 [out]  out
+ *   g     float32 [out]  out
+ *   workspace  >= dora_norm_factored_workspace(out,in,r) bytes, 256-byte
+ *              aligned, caller-owned scratch; contents on entry are ignored
+ *   Sizes: out >= 0 (0 is a no-op), in >= 1, r >= 1, r <= 1024,
+ *          out, in < 2^31.
+ */
+dora_status dora_norm_factored(const float *W0, const float *A, const float *B,
+                               const float *m, float s,
+                               int64_t out, int64_t in, int64_t r,
+                               float *norm, float *g,
+                               void *workspace, size_t workspace_bytes,
+                               dora_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* (b) fused compose, forward                                                */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * y = base + (g-1)*base + g*s*lora, one pass over [T,out].
+ *
+ * P1 ¶第二个创新是"融合Triton内核"技术 (four elementwise kernels fused into one)
+ * and ¶从技术架构角度来看 / ¶他们在一个Qwen2-VL-7B适配器上的测量 (stable form with
+ * the correction (g-1) kept explicit, fp32 intermediates).  Every element is
+ * computed in fp32 and rounded once (nearest even) to the activation dtype.
+ *
+ *   act   DORA_F32 or DORA_BF16: dtype of base, lora and y
+ *   base, lora  [T, out] of `act`
+ *   g     float32 [out]
+ *   y     [T, out] of `act`
+ *   Sizes: T >= 0, out >= 0 (either 0 is a no-op).  Any out and any element
+ *   alignment are accepted; the 128-bit path is taken when out is a multiple
+ *   of 16/sizeof(act) and base, lora and y are 16-byte aligned.
+ */
+dora_status dora_compose_fwd(dora_dtype act, const void *base, const void *lora,
+                             const float *g, float s, int64_t T, int64_t out,
+                             void *y, dora_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* (b) fused compose, backward                                               */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Bytes of device workspace dora_compose_bwd needs (fp32 partial column sums
+ * of d_mag).  Pure host arithmetic; an upper bound valid on any device.
+ */
+size_t dora_compose_bwd_workspace(int64_t T, int64_t out);
+
+/*
+ * d_base = g*dy,  d_lora = s*g*dy,
+ * d_mag[j] = (sum_t dy[t,j]*(base[t,j] + s*lora[t,j])) / norm[j].
+ *
+ * P1 ¶研究团队还设计了一个智能的三层调度系统 (fused backward in training) and
+ * ¶研究团队还进行了广泛的收敛等价性验证 (d_mag reduction order).  The row norm is
+ * treated as a constant (no gradient into A or B).  d_base and d_lora are
+ * rounded once to `act`; d_mag is float32, summed in a fixed order (per-thread
+ * token runs, then a fixed-order sum of the per-run partials), so it is
+ * bitwise reproducible.  d_mag is overwritten, not accumulated.
+ *
+ *   act        dtype of grad_out, base, lora, d_base, d_lora
+ *   grad_out, base, lora   [T, out] of `act`
+ *   g, norm    float32 [out]
+ *   d_base, d_lora  [T, out] of `act`
+ *   d_mag      float32 [out]
+ *   workspace  >= dora_compose_bwd_workspace(T,out) bytes, 256-byte aligned
+ *   Sizes: T >= 0, out >= 0 (out == 0 is a no-op; T == 0 gives d_mag = 0).
+ */
+dora_status dora_compose_bwd(dora_dtype act, const void *grad_out, const void *base,
+                             const void *lora, const float *g, const float *norm,
+                             float s, int64_t T, int64_t out,
+                             void *d_base, void *d_lora, float *d_mag,
+                             void *workspace, size_t workspace_bytes,
+                             dora_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* diagnostics                                                               */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Reads (synchronously: waits for the device) and clears the current device's
+ * error word.  *code = 0 when no kernel gave up waiting; otherwise a nonzero
+ * code naming the wait that timed out.  Returns DORA_ERR_DEVICE in that case.
+ */
+dora_status dora_device_error(int *code);
+
+/* Number of kernels this process has launched through the library. */
+uint64_t dora_kernel_launches(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DORA_H */

@@ -1,0 +1,160 @@
+"""DoRA weight-norm and compose hot path for GB300 (sm_103a).
+
+Thin ctypes binding over libdora.so (include/dora.h).  Every function here only
+marshals arguments -- shapes from tensor sizes, raw device pointers, the
+current torch stream -- and calls the C entry point of the same name; all
+arithmetic runs in the library's CUDA kernels.  There is no fallback: if the
+library is missing or a call fails, an exception is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+__all__ = [
+    "DoraError",
+    "load_library",
+    "library_path",
+    "dora_status_str",
+    "dora_norm_factored_workspace",
+    "dora_norm_factored",
+    "dora_compose_fwd",
+    "dora_compose_bwd_workspace",
+    "dora_compose_bwd",
+    "dora_device_error",
+    "dora_kernel_launches",
+    "DORA_F32",
+    "DORA_BF16",
+]
+
+DORA_F32 = 0
+DORA_BF16 = 1
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_PKG, "lib", "libdora.so")
+_lib = None
+
+_vp = ctypes.c_void_p
+_i64 = ctypes.c_int64
+_sz = ctypes.c_size_t
+_f32 = ctypes.c_float
+_int = ctypes.c_int
+
+_SIGNATURES = {
+    "dora_status_str": (ctypes.c_char_p, [_int]),
+    "dora_norm_factored_workspace": (_sz, [_i64, _i64, _i64]),
+    "dora_norm_factored": (_int, [_vp, _vp, _vp, _vp, _f32, _i64, _i64, _i64, _vp, _vp, _vp, _sz, _vp]),
+    "dora_compose_fwd": (_int, [_int, _vp, _vp, _vp, _f32, _i64, _i64, _vp, _vp]),
+    "dora_compose_bwd_workspace": (_sz, [_i64, _i64]),
+    "dora_compose_bwd": (_int, [_int, _vp, _vp, _vp, _vp, _vp, _f32, _i64, _i64, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "dora_device_error": (_int, [ctypes.POINTER(_int)]),
+    "dora_kernel_launches": (ctypes.c_uint64, []),
+}
+
+
+class DoraError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn}: {load_library().dora_status_str(status).decode()}")
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load_library():
+    """Load libdora.so (built by __graft_entry__.build()); raises if absent."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(f"libdora.so not built ({_LIB_PATH}); run __graft_entry__.build() first")
+        lib = ctypes.CDLL(_LIB_PATH)
+        for name, (res, args) in _SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+    return _lib
+
+
+def _ptr(x) -> int:
+    if x is None:
+        return 0
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(stream) -> int:
+    if stream is not None:
+        return stream if isinstance(stream, int) else stream.cuda_stream
+    import torch
+    return torch.cuda.current_stream().cuda_stream
+
+
+def _act(t) -> int:
+    import torch
+    if t.dtype == torch.float32:
+        return DORA_F32
+    if t.dtype == torch.bfloat16:
+        return DORA_BF16
+    raise TypeError(f"activation dtype {t.dtype} not supported (float32 or bfloat16)")
+
+
+def _check(name: str, st: int) -> None:
+    if st != 0:
+        raise DoraError(name, st)
+
+
+def dora_status_str(status: int) -> str:
+    return load_library().dora_status_str(status).decode()
+
+
+def dora_norm_factored_workspace(out: int, inp: int, r: int) -> int:
+    return int(load_library().dora_norm_factored_workspace(out, inp, r))
+
+
+def dora_compose_bwd_workspace(T: int, out: int) -> int:
+    return int(load_library().dora_compose_bwd_workspace(T, out))
+
+
+def dora_norm_factored(W0, A, B, m, s: float, norm, g, workspace, stream=None) -> None:
+    """norm[i] = ||W0_i + s (B A)_i||, g = m / norm (see include/dora.h)."""
+    out, inp = W0.shape
+    r = A.shape[0]
+    st = load_library().dora_norm_factored(
+        _ptr(W0), _ptr(A), _ptr(B), _ptr(m), float(s), out, inp, r, _ptr(norm), _ptr(g),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
+    _check("dora_norm_factored", st)
+
+
+def dora_compose_fwd(base, lora, g, s: float, y, stream=None) -> None:
+    """y = base + (g-1)*base + g*s*lora (see include/dora.h)."""
+    T, out = base.shape
+    st = load_library().dora_compose_fwd(_act(base), _ptr(base), _ptr(lora), _ptr(g), float(s), T, out,
+                                         _ptr(y), _stream(stream))
+    _check("dora_compose_fwd", st)
+
+
+def dora_compose_bwd(grad_out, base, lora, g, norm, s: float, d_base, d_lora, d_mag, workspace,
+                     stream=None) -> None:
+    """d_base = g*dy, d_lora = s*g*dy, d_mag = sum_t dy*(base+s*lora)/norm (see include/dora.h)."""
+    T, out = grad_out.shape
+    st = load_library().dora_compose_bwd(
+        _act(grad_out), _ptr(grad_out), _ptr(base), _ptr(lora), _ptr(g), _ptr(norm), float(s), T, out,
+        _ptr(d_base), _ptr(d_lora), _ptr(d_mag), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream))
+    _check("dora_compose_bwd", st)
+
+
+def dora_device_error() -> int:
+    """Reads and clears the device error word (synchronises the device)."""
+    code = _int(0)
+    st = load_library().dora_device_error(ctypes.byref(code))
+    if st not in (0, 8):
+        raise DoraError("dora_device_error", st)
+    return int(code.value)
+
+
+def dora_kernel_launches() -> int:
+    return int(load_library().dora_kernel_launches())

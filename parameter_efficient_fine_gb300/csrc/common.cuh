@@ -1,0 +1,37 @@
+// Host-side helpers shared by the libdora translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+
+#include "../../include/dora.h"
+
+namespace dora {
+
+// Kernel launches issued by this process through the library.
+extern std::atomic<uint64_t> g_launches;
+
+inline void count_launches(uint64_t n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+
+// Per-device facts, read once per device.
+struct DeviceInfo {
+  int ok_arch;    // 1 when the device is sm_103
+  int sms;        // streaming multiprocessors
+};
+
+// Returns DORA_OK and fills *info for the current device; DORA_ERR_ARCH when the
+// device is not sm_103; DORA_ERR_CUDA when the runtime cannot answer.
+dora_status current_device(DeviceInfo *info, int *device);
+
+inline bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+inline dora_status launch_status() {
+  return cudaGetLastError() == cudaSuccess ? DORA_OK : DORA_ERR_CUDA;
+}
+
+inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+inline int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
+
+}  // namespace dora

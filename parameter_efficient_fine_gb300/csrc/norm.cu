@@ -1,0 +1,898 @@
+// Factored DoRA row norm on GB300 (sm_103a): tcgen05 tensor-core GEMMs fed by
+// TMA, accumulating in tensor memory.
+//
+// Method source: web page "人工智能训练新突破：Anthropic团队破解大模型微调内存瓶颈难题"
+// (techwalker.com), paragraph on factored normalisation: the row norm of
+// W0 + s B A splits into a base, a cross and a Gram term, so memory falls from
+// O(out*in) to O(out*r + r^2).  Written out,
+//     n_i^2 = ||W0_i||^2 + 2 s <U_i, B_i> + s^2 B_i G B_i^T,  U = W0 A^T,  G = A A^T.
+// The cross and Gram terms are folded into ONE accumulator per output row:
+//     D_i = W0_i A^T + B_i (s/2 G)            (K = in + r)
+//     n_i^2 = ||W0_i||^2 + 2 s <B_i, D_i>
+// so U never reaches global memory; only G (r x r) does.
+//
+// Launch sequence of dora_norm_factored:
+//   1. split_kernel      A -> (A_hi, A_lo), the 3-pass TF32 split of the N operand
+//   2. tc_gemm (GRAM)    partial tiles of G = A A^T, stream-K over K = in
+//   3. gram_reduce       fixed-order sum of the partial tiles, scaled by s/2, split hi/lo
+//   4. tc_gemm (NORM)    [W0 | B] x [A | sG/2]^T, stream-K; per segment the epilogue
+//                        reduces each row to (sum W0_i^2 over its K range, <B_i, D_i>)
+//   5. norm_finalize     fixed-order sum of the segments, n = sqrt(max(0, n^2)), g = m/n
+//
+// Precision: fp32 inputs are split x = hi + lo with hi, lo TF32 (round to
+// nearest, ties away); each product is hi*hi + hi*lo + lo*hi (the dropped
+// lo*lo is ~2^-22 relative), accumulated in fp32 in tensor memory.  The
+// M-side operand (W0 or B) is split in shared memory by converter warps, which
+// also accumulate ||W0_i||^2 on the way; the N-side operand is split once in
+// global memory (it is re-read by every M tile).
+//
+// tc_gemm structure (one CTA per SM, persistent, 192 threads):
+//   warp 0      TMA producer: loads the M-side box [128 x 16 fp32] and the
+//               N-side hi/lo boxes of each K block into a ring of stages
+//   warp 1      allocates tensor memory; one lane issues tcgen05.mma
+//   warps 2..5  converters (hi/lo split of the M-side box, row sums of W0^2),
+//               then the epilogue for their 32 tensor-memory lanes each
+// Operand tiles are K-major with the 64-byte swizzle (16 fp32 per row).  The
+// work is the list of (M tile, N chunk, K block) units, split evenly over the
+// CTAs; a CTA's range crosses at most a few tile boundaries, and each piece
+// ("segment") leaves one partial result.  All partial sums are combined in a
+// fixed order, so results are bitwise reproducible.
+//
+// Every wait on a shared-memory barrier is bounded (kWaitLimitNs).  A wait that
+// gives up sets a CTA abort flag, records a code in a device error word and
+// makes all roles leave their loops; the producer then waits (bounded) for its
+// copies in flight, the MMA lane for its issued MMAs, and tensor memory is
+// freed before the CTA exits.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstring>
+#include <mutex>
+
+#include "common.cuh"
+
+namespace {
+
+constexpr int kBM = 128;            // rows per M tile (= tensor-memory lanes)
+constexpr int kBK = 16;             // fp32 per K block (64 bytes, one swizzle row)
+constexpr int kRowBytes = kBK * 4;  // 64
+constexpr int kThreads = 192;
+constexpr int kMaxChunkN = 384;     // largest N handled by one CTA pass
+constexpr int kMaxR = 1024;
+constexpr int kMaxCtas = 256;       // workspace bound: any device up to this size
+constexpr int kMinUnitsNorm = 4;
+constexpr int kMinUnitsGram = 16;
+constexpr int kSmemBudget = 200 * 1024;
+constexpr int kMaxStages = 6;
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
+
+enum Mode : int { kGram = 0, kNorm = 1 };
+
+// device error word: 0 = fine; otherwise the code of the wait that gave up
+__device__ int g_dora_err = 0;
+
+struct TcParams {
+  int mode;
+  int M;            // valid M-side rows (out, or r for the Gram pass)
+  int kb1;          // K blocks in segment 1 (W0 or A columns)
+  int kbtot;        // K blocks in total (segment 2 = B / Gs columns)
+  int nchunks;      // N chunks per M tile
+  int NC;           // N per chunk (multiple of 16, <= kMaxChunkN)
+  int nbox;         // rows per N-side TMA box
+  int nloads;       // N-side boxes per stage (per hi / lo)
+  int NT;           // N-side rows in shared memory per stage (nloads * nbox)
+  int nmma0, nmma1; // N of the first / second MMA instruction of a chunk
+  int tmem_cols;
+  int stages;
+  int tiles;        // M tiles * nchunks
+  long long units;  // tiles * kbtot
+  int ctas;
+  int maxseg;
+  unsigned stage_bytes;
+  unsigned tx_bytes;
+  float *part;      // GRAM: [tiles][maxseg][128][NC]; NORM: [tiles][maxseg][128][2]
+  const float *B;   // NORM epilogue: B [M, r]
+  int r;
+  int *err;
+};
+
+// ---------------------------------------------------------------------------
+// PTX wrappers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ unsigned long long globaltimer() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void prefetch_map(const CUtensorMap *map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void mma_tf32(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc)
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
+}
+// 32 consecutive fp32 columns of this thread's tensor-memory lane
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ uint32_t tf32_rna(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  return r;
+}
+
+// Shared-memory matrix descriptor: K-major operand, 64-byte swizzle, rows of
+// 64 bytes, 8-row groups 512 bytes apart.
+__device__ __forceinline__ uint64_t sdesc_sw64(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);   // start address >> 4      [0,14)
+  d |= static_cast<uint64_t>(1) << 16;                   // leading offset (unused)  [16,30)
+  d |= static_cast<uint64_t>(512 >> 4) << 32;            // stride offset 512 B      [32,46)
+  d |= static_cast<uint64_t>(1) << 46;                   // descriptor version       [46,48)
+  d |= static_cast<uint64_t>(4) << 61;                   // swizzle: 64 bytes        [61,64)
+  return d;
+}
+// Instruction descriptor: kind::tf32, fp32 accumulator, both operands K-major,
+// M = 128, N = n.
+__host__ __device__ __forceinline__ uint32_t idesc_tf32(int n) {
+  return (1u << 4)                                  // D format: f32
+         | (2u << 7)                                // A format: tf32
+         | (2u << 10)                               // B format: tf32
+         | (static_cast<uint32_t>(n >> 3) << 17)    // N >> 3
+         | (static_cast<uint32_t>(kBM >> 4) << 24); // M >> 4
+}
+
+// CTA that owns work unit u when `units` are split evenly over `ctas`.
+__host__ __device__ __forceinline__ long long unit_begin(long long c, long long units, long long ctas) {
+  return c * units / ctas;
+}
+__host__ __device__ __forceinline__ int cta_of(long long u, long long units, int ctas) {
+  long long c = (u * ctas) / units;
+  if (c >= ctas) c = ctas - 1;
+  while (c + 1 < ctas && unit_begin(c + 1, units, ctas) <= u) ++c;
+  while (c > 0 && unit_begin(c, units, ctas) > u) --c;
+  return static_cast<int>(c);
+}
+
+struct SharedCtl {
+  volatile int abort;
+  uint32_t tmem_base;
+};
+
+__device__ bool wait_bounded(uint32_t bar, uint32_t parity, SharedCtl *ctl, int *err, int code) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (ctl->abort) return false;
+    if ((i & 63u) == 0 && globaltimer() - t0 > kWaitLimitNs) {
+      ctl->abort = 1;
+      atomicCAS(err, 0, code);
+      return false;
+    }
+  }
+}
+
+// wait used while leaving after an abort: ignores the abort flag
+__device__ void wait_drain(uint32_t bar, uint32_t parity) {
+  const unsigned long long t0 = globaltimer();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer() - t0 > kWaitLimitNs) return;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// the tensor-core GEMM (GRAM or NORM mode)
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kThreads, 1)
+tc_gemm_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ CUtensorMap mX2,
+               const __grid_constant__ CUtensorMap mY1h, const __grid_constant__ CUtensorMap mY1l,
+               const __grid_constant__ CUtensorMap mY2h, const __grid_constant__ CUtensorMap mY2l,
+               const TcParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int S = p.stages;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + static_cast<size_t>(S) * p.stage_bytes);
+  // barrier layout: full[S], conv[S], empty[S], accf, acce, fin
+  SharedCtl *ctl = reinterpret_cast<SharedCtl *>(bars + 3 * S + 3);
+  const uint32_t full0 = smem_u32(bars);
+  const uint32_t conv0 = full0 + 8u * S;
+  const uint32_t empty0 = conv0 + 8u * S;
+  const uint32_t accf = empty0 + 8u * S;
+  const uint32_t acce = accf + 8;
+  const uint32_t fin = acce + 8;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full0 + 8u * s, 1);
+      mbar_init(conv0 + 8u * s, 128);
+      mbar_init(empty0 + 8u * s, 1);
+    }
+    mbar_init(accf, 1);
+    mbar_init(acce, 128);
+    mbar_init(fin, 1);
+    ctl->abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_map(&mX1);
+    prefetch_map(&mY1h);
+    prefetch_map(&mY1l);
+    if (p.kbtot > p.kb1) {
+      prefetch_map(&mX2);
+      prefetch_map(&mY2h);
+      prefetch_map(&mY2l);
+    }
+  }
+  if (warp == 1) {
+    __syncwarp();
+    tmem_alloc(smem_u32(&ctl->tmem_base), static_cast<uint32_t>(p.tmem_cols));
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl->tmem_base;
+
+  const long long u_begin = unit_begin(blockIdx.x, p.units, p.ctas);
+  const long long u_end = unit_begin(blockIdx.x + 1, p.units, p.ctas);
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ producer
+      int stage = 0;
+      uint32_t phase = 0;
+      int issued = 0;  // loads issued in total (to drain on abort)
+      bool ok = true;
+      for (long long u = u_begin; u < u_end && ok;) {
+        const int t = static_cast<int>(u / p.kbtot);
+        const int kb0 = static_cast<int>(u - static_cast<long long>(t) * p.kbtot);
+        const int kbe = static_cast<int>(min(static_cast<long long>(p.kbtot), kb0 + (u_end - u)));
+        const int mt = t / p.nchunks;
+        const int nc = t - mt * p.nchunks;
+        for (int kb = kb0; kb < kbe; ++kb) {
+          if (!wait_bounded(empty0 + 8u * stage, phase ^ 1u, ctl, p.err, 1)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = full0 + 8u * stage;
+          mbar_expect_tx(fb, p.tx_bytes);
+          const uint32_t xs = smem_u32(smem + static_cast<size_t>(stage) * p.stage_bytes);
+          const uint32_t yh = xs + 2u * kBM * kRowBytes;
+          const uint32_t yl = yh + static_cast<uint32_t>(p.NT) * kRowBytes;
+          const bool seg1 = kb < p.kb1;
+          const int kx = (seg1 ? kb : kb - p.kb1) * kBK;
+          tma_load_2d(xs, seg1 ? &mX1 : &mX2, kx, mt * kBM, fb);
+          for (int i = 0; i < p.nloads; ++i) {
+            const int ny = nc * p.NC + i * p.nbox;
+            const uint32_t off = static_cast<uint32_t>(i * p.nbox * kRowBytes);
+            tma_load_2d(yh + off, seg1 ? &mY1h : &mY2h, kx, ny, fb);
+            tma_load_2d(yl + off, seg1 ? &mY1l : &mY2l, kx, ny, fb);
+          }
+          ++issued;
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        u += kbe - kb0;
+      }
+      if (!ok) {
+        // drain: the last min(issued, S) stages may still have copies in flight
+        int st = stage;
+        uint32_t ph = phase;
+        for (int k = 0; k < S && k < issued; ++k) {
+          if (--st < 0) {
+            st = S - 1;
+            ph ^= 1u;
+          }
+          wait_drain(full0 + 8u * st, ph);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ MMA issuer
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t aphase = 0;
+      bool ok = true;
+      const uint32_t id0 = idesc_tf32(p.nmma0);
+      const uint32_t id1 = p.nmma1 > 0 ? idesc_tf32(p.nmma1) : 0u;
+      for (long long u = u_begin; u < u_end && ok;) {
+        const int t = static_cast<int>(u / p.kbtot);
+        const int kb0 = static_cast<int>(u - static_cast<long long>(t) * p.kbtot);
+        const int kbe = static_cast<int>(min(static_cast<long long>(p.kbtot), kb0 + (u_end - u)));
+        if (!wait_bounded(acce, aphase ^ 1u, ctl, p.err, 3)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        for (int kb = kb0; kb < kbe; ++kb) {
+          if (!wait_bounded(conv0 + 8u * stage, phase, ctl, p.err, 2)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t xh = smem_u32(smem + static_cast<size_t>(stage) * p.stage_bytes);
+          const uint32_t xl = xh + kBM * kRowBytes;
+          const uint32_t yh = xl + kBM * kRowBytes;
+          const uint32_t yl = yh + static_cast<uint32_t>(p.NT) * kRowBytes;
+#pragma unroll
+          for (int k = 0; k < kBK / 8; ++k) {
+            const uint32_t acc0 = (kb != kb0 || k != 0) ? 1u : 0u;
+            const uint32_t ko = static_cast<uint32_t>(k) * 32u;  // 8 tf32 = 32 bytes
+            const uint64_t ah = sdesc_sw64(xh + ko), al = sdesc_sw64(xl + ko);
+            {
+              const uint64_t bh = sdesc_sw64(yh + ko), bl = sdesc_sw64(yl + ko);
+              mma_tf32(tmem, al, bh, id0, acc0);
+              mma_tf32(tmem, ah, bl, id0, 1u);
+              mma_tf32(tmem, ah, bh, id0, 1u);
+            }
+            if (p.nmma1 > 0) {
+              const uint32_t no = 256u * kRowBytes;
+              const uint64_t bh = sdesc_sw64(yh + no + ko), bl = sdesc_sw64(yl + no + ko);
+              mma_tf32(tmem + 256u, al, bh, id1, acc0);
+              mma_tf32(tmem + 256u, ah, bl, id1, 1u);
+              mma_tf32(tmem + 256u, ah, bh, id1, 1u);
+            }
+          }
+          mma_commit(empty0 + 8u * stage);
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        mma_commit(accf);
+        aphase ^= 1u;
+        u += kbe - kb0;
+      }
+      // all issued MMAs must finish before tensor memory is released
+      mma_commit(fin);
+      wait_drain(fin, 0);
+    }
+  } else {
+    // -------------------------------------------------------- converters + epilogue
+    const int quad = warp & 3;            // tensor-memory lane group of this warp
+    const int row = quad * 32 + lane;     // row within the M tile
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+    const int swz = (row >> 1) & 3;       // 64-byte swizzle: chunk c lives at c ^ swz
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t aphase = 0;
+    bool ok = true;
+    for (long long u = u_begin; u < u_end && ok;) {
+      const int t = static_cast<int>(u / p.kbtot);
+      const int kb0 = static_cast<int>(u - static_cast<long long>(t) * p.kbtot);
+      const int kbe = static_cast<int>(min(static_cast<long long>(p.kbtot), kb0 + (u_end - u)));
+      const int mt = t / p.nchunks;
+      const int nc = t - mt * p.nchunks;
+      float n0 = 0.0f;  // sum of W0_i^2 over this segment's K range
+      for (int kb = kb0; kb < kbe; ++kb) {
+        // every lane waits; the decision to go on is taken warp-wide so that
+        // the warp stays converged for the tcgen05.ld of the epilogue
+        const bool got = wait_bounded(full0 + 8u * stage, phase, ctl, p.err, 4);
+        if (!__all_sync(0xffffffffu, got)) {
+          ok = false;
+          break;
+        }
+        float4 *xh = reinterpret_cast<float4 *>(smem + static_cast<size_t>(stage) * p.stage_bytes + row * kRowBytes);
+        float4 *xl = reinterpret_cast<float4 *>(reinterpret_cast<uint8_t *>(xh) + kBM * kRowBytes);
+        float blk = 0.0f;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int ph = c ^ swz;
+          const float4 v = xh[ph];
+          float4 h, l;
+          h.x = __uint_as_float(tf32_rna(v.x));
+          h.y = __uint_as_float(tf32_rna(v.y));
+          h.z = __uint_as_float(tf32_rna(v.z));
+          h.w = __uint_as_float(tf32_rna(v.w));
+          l.x = __uint_as_float(tf32_rna(v.x - h.x));
+          l.y = __uint_as_float(tf32_rna(v.y - h.y));
+          l.z = __uint_as_float(tf32_rna(v.z - h.z));
+          l.w = __uint_as_float(tf32_rna(v.w - h.w));
+          xh[ph] = h;
+          xl[ph] = l;
+          blk = fmaf(v.x, v.x, blk);
+          blk = fmaf(v.y, v.y, blk);
+          blk = fmaf(v.z, v.z, blk);
+          blk = fmaf(v.w, v.w, blk);
+        }
+        if (kb < p.kb1) n0 += blk;
+        fence_proxy_async();
+        mbar_arrive(conv0 + 8u * stage);
+        if (++stage == S) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (!ok) break;
+      // ---- epilogue of this segment
+      const bool got = wait_bounded(accf, aphase, ctl, p.err, 5);
+      if (!__all_sync(0xffffffffu, got)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const int grow = mt * kBM + row;
+      const bool valid = grow < p.M;
+      const int seg = static_cast<int>(blockIdx.x) - cta_of(static_cast<long long>(t) * p.kbtot, p.units, p.ctas);
+      if (p.mode == kNorm) {
+        float dot = 0.0f;
+        const float *Brow = p.B + static_cast<size_t>(valid ? grow : 0) * p.r;
+        for (int c = 0; c < p.NC; c += 32) {
+          float v[32];
+          tmem_ld32(lane_addr + static_cast<uint32_t>(c), v);
+          const int n0c = nc * p.NC + c;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            if (valid && c + j < p.NC && n0c + j < p.r) dot = fmaf(__ldg(Brow + n0c + j), v[j], dot);
+          }
+        }
+        if (valid) {
+          float2 *dst = reinterpret_cast<float2 *>(p.part) + (static_cast<size_t>(t) * p.maxseg + seg) * kBM + row;
+          *dst = make_float2(n0, dot);
+        }
+      } else {
+        float *dst = p.part + ((static_cast<size_t>(t) * p.maxseg + seg) * kBM + row) * p.NC;
+        for (int c = 0; c < p.NC; c += 32) {
+          float v[32];
+          tmem_ld32(lane_addr + static_cast<uint32_t>(c), v);
+          if (valid) {
+#pragma unroll
+            for (int j = 0; j < 32; j += 4) {
+              if (c + j < p.NC) *reinterpret_cast<float4 *>(dst + c + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(acce);
+      aphase ^= 1u;
+      u += kbe - kb0;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) {
+    __syncwarp();
+    tmem_dealloc(tmem, static_cast<uint32_t>(p.tmem_cols));
+  }
+}
+
+// ---------------------------------------------------------------------------
+// elementwise helpers
+// ---------------------------------------------------------------------------
+
+// x -> (hi, lo) TF32 split, count elements (multiple of 4, 16-byte aligned)
+__global__ void __launch_bounds__(256) split_kernel(const float *__restrict__ x, long long n4,
+                                                    float *__restrict__ hi, float *__restrict__ lo) {
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += (long long)gridDim.x * blockDim.x) {
+    const float4 v = __ldg(reinterpret_cast<const float4 *>(x) + i);
+    float4 h, l;
+    h.x = __uint_as_float(tf32_rna(v.x));
+    h.y = __uint_as_float(tf32_rna(v.y));
+    h.z = __uint_as_float(tf32_rna(v.z));
+    h.w = __uint_as_float(tf32_rna(v.w));
+    l.x = __uint_as_float(tf32_rna(v.x - h.x));
+    l.y = __uint_as_float(tf32_rna(v.y - h.y));
+    l.z = __uint_as_float(tf32_rna(v.z - h.z));
+    l.w = __uint_as_float(tf32_rna(v.w - h.w));
+    reinterpret_cast<float4 *>(hi)[i] = h;
+    reinterpret_cast<float4 *>(lo)[i] = l;
+  }
+}
+
+// B [out, r] -> Bp [out, rp] with zero columns r..rp-1 (rp = r rounded up to 4)
+__global__ void __launch_bounds__(256) pad_cols_kernel(const float *__restrict__ B, long long rows, int r, int rp,
+                                                       float *__restrict__ Bp) {
+  const long long n = rows * rp;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
+    const long long row = i / rp;
+    const int c = static_cast<int>(i - row * rp);
+    Bp[i] = c < r ? B[row * r + c] : 0.0f;
+  }
+}
+
+struct StreamK {
+  long long units;
+  int ctas, kbtot, maxseg;
+};
+
+// Gs[k][l] = (s/2) * G[k][l] for k, l < r (zero-padded to npad), split hi/lo
+__global__ void __launch_bounds__(256) gram_reduce_kernel(const float *__restrict__ part, StreamK sk, int nchunks,
+                                                          int NC, int r, int npad, float half_s,
+                                                          float *__restrict__ gh, float *__restrict__ gl) {
+  const long long n = static_cast<long long>(npad) * npad;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
+    const int k = static_cast<int>(i / npad);
+    const int l = static_cast<int>(i - static_cast<long long>(k) * npad);
+    float v = 0.0f;
+    if (k < r && l < r) {
+      const int mt = k / kBM, row = k - mt * kBM;
+      const int nc = l / NC, col = l - nc * NC;
+      const int t = mt * nchunks + nc;
+      const long long ub = static_cast<long long>(t) * sk.kbtot;
+      const int c0 = cta_of(ub, sk.units, sk.ctas);
+      const int c1 = cta_of(ub + sk.kbtot - 1, sk.units, sk.ctas);
+      float sum = 0.0f;
+      for (int j = 0; j <= c1 - c0; ++j) sum += part[((static_cast<size_t>(t) * sk.maxseg + j) * kBM + row) * NC + col];
+      v = half_s * sum;
+    }
+    const float h = __uint_as_float(tf32_rna(v));
+    gh[i] = h;
+    gl[i] = __uint_as_float(tf32_rna(v - h));
+  }
+}
+
+// n_i = sqrt(max(0, sum n0 + 2 s sum dot)), g_i = m_i / n_i
+__global__ void __launch_bounds__(256) norm_finalize_kernel(const float2 *__restrict__ part, StreamK sk, int nchunks,
+                                                            int out, const float *__restrict__ m, float two_s,
+                                                            float *__restrict__ norm, float *__restrict__ g) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= out) return;
+  const int mt = i / kBM, row = i - mt * kBM;
+  float n0 = 0.0f, dot = 0.0f;
+  for (int nc = 0; nc < nchunks; ++nc) {
+    const int t = mt * nchunks + nc;
+    const long long ub = static_cast<long long>(t) * sk.kbtot;
+    const int c0 = cta_of(ub, sk.units, sk.ctas);
+    const int c1 = cta_of(ub + sk.kbtot - 1, sk.units, sk.ctas);
+    for (int j = 0; j <= c1 - c0; ++j) {
+      const float2 v = part[(static_cast<size_t>(t) * sk.maxseg + j) * kBM + row];
+      if (nc == 0) n0 += v.x;
+      dot += v.y;
+    }
+  }
+  const float n2 = fmaf(two_s, dot, n0);
+  const float n = sqrtf(fmaxf(n2, 0.0f));
+  norm[i] = n;
+  g[i] = m[i] / n;
+}
+
+// ---------------------------------------------------------------------------
+// host planning
+// ---------------------------------------------------------------------------
+struct GemmPlan {
+  TcParams p;
+  size_t smem_bytes;
+  size_t part_bytes;
+};
+
+int seg_bound(long long units, int ctas, int kbtot) {
+  const long long per = units / ctas;  // >= 1 since ctas <= units
+  return static_cast<int>((kbtot - 1) / per + 2);
+}
+
+// N layout shared by both passes: npad = r rounded to 16, split into equal
+// chunks of at most kMaxChunkN.
+void plan_n(int r, int *npad, int *nchunks, int *NC) {
+  *npad = static_cast<int>(dora::round_up(r, 16));
+  *nchunks = static_cast<int>(dora::ceil_div(*npad, kMaxChunkN));
+  *NC = static_cast<int>(dora::round_up(dora::ceil_div(*npad, *nchunks), 16));
+}
+
+bool plan_gemm(int mode, int M, int kb1, int kb2, int r, int sms, GemmPlan *gp) {
+  TcParams &p = gp->p;
+  std::memset(&p, 0, sizeof(p));
+  p.mode = mode;
+  p.M = M;
+  p.kb1 = kb1;
+  p.kbtot = kb1 + kb2;
+  int npad;
+  plan_n(r, &npad, &p.nchunks, &p.NC);
+  p.nbox = p.NC <= 128 ? p.NC : 128;
+  p.nloads = static_cast<int>(dora::ceil_div(p.NC, p.nbox));
+  p.NT = p.nloads * p.nbox;
+  p.nmma0 = p.NC <= 256 ? p.NC : 256;
+  p.nmma1 = p.NC - p.nmma0;
+  int cols = 32;
+  while (cols < p.NC) cols *= 2;
+  p.tmem_cols = cols;
+  p.stage_bytes = static_cast<unsigned>(2 * kBM * kRowBytes + 2 * p.NT * kRowBytes);
+  p.tx_bytes = static_cast<unsigned>(kBM * kRowBytes + 2 * p.NT * kRowBytes);
+  p.stages = static_cast<int>((kSmemBudget - 2048) / p.stage_bytes);
+  if (p.stages > kMaxStages) p.stages = kMaxStages;
+  if (p.stages < 2) return false;
+  const int mtiles = static_cast<int>(dora::ceil_div(M, kBM));
+  p.tiles = mtiles * p.nchunks;
+  p.units = static_cast<long long>(p.tiles) * p.kbtot;
+  const int min_units = mode == kGram ? kMinUnitsGram : kMinUnitsNorm;
+  long long ctas = dora::ceil_div(p.units, min_units);
+  if (ctas > sms) ctas = sms;
+  if (ctas < 1) ctas = 1;
+  p.ctas = static_cast<int>(ctas);
+  p.maxseg = seg_bound(p.units, p.ctas, p.kbtot);
+  p.r = r;
+  const size_t per_row = mode == kGram ? static_cast<size_t>(p.NC) : 2;
+  gp->part_bytes = static_cast<size_t>(p.tiles) * p.maxseg * kBM * per_row * sizeof(float);
+  gp->smem_bytes = static_cast<size_t>(p.stages) * p.stage_bytes + 1024 /*align*/ + 8 * (3 * p.stages + 3) + 64;
+  // tensor memory: a CTA holding 512 columns must be alone on its SM
+  if (p.tmem_cols > 256 && gp->smem_bytes < 116 * 1024) gp->smem_bytes = 116 * 1024;
+  return true;
+}
+
+struct Layout {
+  size_t a_hi, a_lo, g_hi, g_lo, part_g, part_n, b_pad, total;
+};
+
+size_t al256(size_t x) { return (x + 255) & ~size_t(255); }
+
+bool plan_layout(int64_t out, int64_t in, int64_t r, int sms, GemmPlan *gg, GemmPlan *gn, Layout *L) {
+  const int kb1 = static_cast<int>(dora::ceil_div(in, kBK));
+  const int kb2 = static_cast<int>(dora::ceil_div(r, kBK));
+  if (!plan_gemm(kGram, static_cast<int>(r), kb1, 0, static_cast<int>(r), sms, gg)) return false;
+  if (!plan_gemm(kNorm, static_cast<int>(out), kb1, kb2, static_cast<int>(r), sms, gn)) return false;
+  int npad, nchunks, NC;
+  plan_n(static_cast<int>(r), &npad, &nchunks, &NC);
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off += al256(bytes);
+    return o;
+  };
+  L->a_hi = take(static_cast<size_t>(r) * in * 4);
+  L->a_lo = take(static_cast<size_t>(r) * in * 4);
+  L->g_hi = take(static_cast<size_t>(npad) * npad * 4);
+  L->g_lo = take(static_cast<size_t>(npad) * npad * 4);
+  L->part_g = take(gg->part_bytes);
+  L->part_n = take(gn->part_bytes);
+  L->b_pad = (r % 4) ? take(static_cast<size_t>(out) * dora::round_up(r, 4) * 4) : 0;
+  L->total = off;
+  return true;
+}
+
+bool shape_ok(int64_t out, int64_t in, int64_t r) {
+  return out >= 0 && in >= 1 && r >= 1 && r <= kMaxR && out < (1ll << 31) && in < (1ll << 31) &&
+         in * r < (1ll << 40);
+}
+
+// ---- tensor maps (driver entry point fetched through the runtime)
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static std::once_flag once;
+  static EncodeTiledFn fn = nullptr;
+  std::call_once(once, [] {
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  return fn;
+}
+
+// 2-D fp32 matrix [rows, cols] with row stride ld (elements), box [box_rows, 16]
+bool make_map(CUtensorMap *map, const float *base, int64_t rows, int64_t cols, int64_t ld, int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 4};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int grid_for(long long n, int sms) {
+  long long b = dora::ceil_div(n, 256);
+  const long long cap = static_cast<long long>(sms) * 8;
+  if (b > cap) b = cap;
+  if (b < 1) b = 1;
+  return static_cast<int>(b);
+}
+
+}  // namespace
+
+extern "C" size_t dora_norm_factored_workspace(int64_t out, int64_t in, int64_t r) {
+  if (!shape_ok(out, in, r)) return 0;
+  GemmPlan gg, gn;
+  Layout L;
+  if (!plan_layout(out > 0 ? out : 1, in, r, kMaxCtas, &gg, &gn, &L)) return 0;
+  return L.total;
+}
+
+extern "C" dora_status dora_device_error(int *code) {
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_dora_err, sizeof(int)) != cudaSuccess) return DORA_ERR_CUDA;
+  if (code) *code = v;
+  if (v != 0) {
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(g_dora_err, &zero, sizeof(int)) != cudaSuccess) return DORA_ERR_CUDA;
+    return DORA_ERR_DEVICE;
+  }
+  return DORA_OK;
+}
+
+extern "C" dora_status dora_norm_factored(const float *W0, const float *A, const float *B, const float *m, float s,
+                                          int64_t out, int64_t in, int64_t r, float *norm, float *g,
+                                          void *workspace, size_t workspace_bytes, dora_stream_t stream) {
+  if (!shape_ok(out, in, r)) return DORA_ERR_SHAPE;
+  if (out == 0) return DORA_OK;
+  if (!W0 || !A || !B || !m || !norm || !g) return DORA_ERR_NULL;
+  if (!workspace) return DORA_ERR_WORKSPACE;
+  if (in % 4 != 0) return DORA_ERR_ALIGN;
+  if (!dora::aligned(W0, 16) || !dora::aligned(A, 16) || !dora::aligned(B, 16) || !dora::aligned(m, 4) ||
+      !dora::aligned(norm, 4) || !dora::aligned(g, 4))
+    return DORA_ERR_ALIGN;
+  if (!dora::aligned(workspace, 256) || workspace_bytes < dora_norm_factored_workspace(out, in, r))
+    return DORA_ERR_WORKSPACE;
+
+  dora::DeviceInfo info;
+  int device = 0;
+  dora_status st = dora::current_device(&info, &device);
+  if (st != DORA_OK) return st;
+  const int sms = info.sms < kMaxCtas ? info.sms : kMaxCtas;
+
+  GemmPlan gg, gn;
+  Layout L;
+  if (!plan_layout(out, in, r, sms, &gg, &gn, &L)) return DORA_ERR_SHAPE;
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  float *a_hi = reinterpret_cast<float *>(ws + L.a_hi);
+  float *a_lo = reinterpret_cast<float *>(ws + L.a_lo);
+  float *g_hi = reinterpret_cast<float *>(ws + L.g_hi);
+  float *g_lo = reinterpret_cast<float *>(ws + L.g_lo);
+  float *part_g = reinterpret_cast<float *>(ws + L.part_g);
+  float *part_n = reinterpret_cast<float *>(ws + L.part_n);
+  const float *Bk = B;
+  int64_t ldb = r;
+  int npad, nchunks, NC;
+  plan_n(static_cast<int>(r), &npad, &nchunks, &NC);
+
+  // device error word, passed to the kernels by address
+  static std::mutex err_mu;
+  static int *err_ptr[64] = {};
+  int *errp = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(err_mu);
+    if (device >= 64) return DORA_ERR_CUDA;
+    if (!err_ptr[device]) {
+      void *ptr = nullptr;
+      if (cudaGetSymbolAddress(&ptr, g_dora_err) != cudaSuccess) return DORA_ERR_CUDA;
+      if (cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget + 2048) !=
+          cudaSuccess)
+        return DORA_ERR_CUDA;
+      err_ptr[device] = static_cast<int *>(ptr);
+    }
+    errp = err_ptr[device];
+  }
+
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  uint64_t launches = 0;
+
+  // 1. N-side split of A; B padded to a TMA-legal row stride when r % 4 != 0
+  const long long a4 = r * in / 4;
+  split_kernel<<<grid_for(a4, sms), 256, 0, cs>>>(A, a4, a_hi, a_lo);
+  ++launches;
+  if (r % 4) {
+    const int rp = static_cast<int>(dora::round_up(r, 4));
+    float *bp = reinterpret_cast<float *>(ws + L.b_pad);
+    pad_cols_kernel<<<grid_for(out * rp, sms), 256, 0, cs>>>(B, out, static_cast<int>(r), rp, bp);
+    ++launches;
+    Bk = bp;
+    ldb = rp;
+  }
+
+  // tensor maps
+  CUtensorMap mA, mAh_n, mAl_n, mW0, mB, mGh, mGl;
+  const int nbox = gn.p.nbox;
+  bool ok = make_map(&mA, A, r, in, in, kBM) && make_map(&mAh_n, a_hi, r, in, in, nbox) &&
+            make_map(&mAl_n, a_lo, r, in, in, nbox) && make_map(&mW0, W0, out, in, in, kBM) &&
+            make_map(&mB, Bk, out, ldb, ldb, kBM) && make_map(&mGh, g_hi, npad, npad, npad, nbox) &&
+            make_map(&mGl, g_lo, npad, npad, npad, nbox);
+  if (!ok) {
+    dora::count_launches(launches);
+    return DORA_ERR_CUDA;
+  }
+
+  // 2. Gram partial tiles
+  gg.p.part = part_g;
+  gg.p.err = errp;
+  tc_gemm_kernel<<<gg.p.ctas, kThreads, gg.smem_bytes, cs>>>(mA, mA, mAh_n, mAl_n, mAh_n, mAl_n, gg.p);
+  ++launches;
+
+  // 3. Gs = (s/2) G, split hi/lo
+  StreamK skg{gg.p.units, gg.p.ctas, gg.p.kbtot, gg.p.maxseg};
+  gram_reduce_kernel<<<grid_for(static_cast<long long>(npad) * npad, sms), 256, 0, cs>>>(
+      part_g, skg, gg.p.nchunks, gg.p.NC, static_cast<int>(r), npad, 0.5f * s, g_hi, g_lo);
+  ++launches;
+
+  // 4. [W0 | B] x [A | Gs]^T with per-segment row reductions
+  gn.p.part = part_n;
+  gn.p.err = errp;
+  gn.p.B = B;
+  tc_gemm_kernel<<<gn.p.ctas, kThreads, gn.smem_bytes, cs>>>(mW0, mB, mAh_n, mAl_n, mGh, mGl, gn.p);
+  ++launches;
+
+  // 5. n and g
+  StreamK skn{gn.p.units, gn.p.ctas, gn.p.kbtot, gn.p.maxseg};
+  norm_finalize_kernel<<<static_cast<unsigned>(dora::ceil_div(out, 256)), 256, 0, cs>>>(
+      reinterpret_cast<const float2 *>(part_n), skn, gn.p.nchunks, static_cast<int>(out), m, 2.0f * s, norm, g);
+  ++launches;
+  dora::count_launches(launches);
+  return dora::launch_status();
+}

@@ -1,0 +1,219 @@
+"""GPU parity: the CUDA library (called through its C ABI) against the fp64
+oracle on the same seeded inputs, at sizes the oracle finishes in seconds
+that still span several tiles and ragged tails, plus edge and degenerate
+cases.  Tolerances are stated in tests/gpu_util.py."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from parameter_efficient_fine_gb300 import workloads as wl
+
+from gpu_util import (DEV, act_to_dev, act_to_f64, assert_no_device_error, check_bf16_rule, check_bound,
+                      check_rel, dmag_bound, f32_dev, run_bwd, run_fwd, run_norm, to_f64)
+
+pytestmark = pytest.mark.gpu
+
+
+def _weights_dev(d):
+    return tuple(f32_dev(d[k]) for k in ("W0", "A", "B", "m"))
+
+
+def _full_check(sh, seed, bwd=True):
+    """Norm, forward and (optionally) backward of one module, all elements."""
+    d = wl.make_module(sh, seed)
+    s = d["s"]
+    W0, A, B, m = _weights_dev(d)
+    norm, g = run_norm(W0, A, B, m, s)
+    n_ref, g_ref = oracle.weight_norm(d["W0"], d["A"], d["B"], d["m"], s)
+    check_rel("norm", to_f64(norm), n_ref)
+    check_rel("g", to_f64(g), g_ref)
+
+    base, lora, dy = (act_to_dev(d[k]) for k in ("base", "lora", "dy"))
+    b64, l64, d64 = (act_to_f64(d[k]) for k in ("base", "lora", "dy"))
+    y = run_fwd(base, lora, g, s)
+    y_ref = oracle.compose_fwd(b64, l64, g_ref, s)
+    if sh.act == "bf16":
+        check_bf16_rule("y", to_f64(y), y_ref)
+    else:
+        bound = 2.0 ** -21 * (np.abs(b64) + np.abs(g_ref) * s * np.abs(l64)) + 1.1e-5 * np.abs(y_ref)
+        check_bound("y", to_f64(y), y_ref, bound)
+    if bwd:
+        db, dl, dm = run_bwd(dy, base, lora, g, norm, s)
+        db_ref, dl_ref, dm_ref = oracle.compose_bwd(d64, b64, l64, g_ref, n_ref, s)
+        if sh.act == "bf16":
+            check_bf16_rule("d_base", to_f64(db), db_ref)
+            check_bf16_rule("d_lora", to_f64(dl), dl_ref)
+        else:
+            gb = np.abs(g_ref)[None, :] * np.abs(d64)
+            check_bound("d_base", to_f64(db), db_ref, 2.0 ** -22 * gb + 1.1e-5 * np.abs(db_ref))
+            check_bound("d_lora", to_f64(dl), dl_ref, 2.0 ** -22 * gb * (1 + s) + 1.1e-5 * np.abs(dl_ref))
+        check_bf16_rule("d_mag", to_f64(dm), dm_ref)
+        check_bound("d_mag", to_f64(dm), dm_ref, dmag_bound(d64, b64, l64, n_ref, s) + 1.1e-5 * np.abs(dm_ref))
+    assert_no_device_error()
+
+
+def test_tiny_workload_all_elements():
+    _full_check(wl.shape("tiny"), wl.seed_for("tiny"))
+
+
+def test_attention_projection_reduced_tokens():
+    # full 4096 x 4096 r=64 weights, forward + norm (the inference path), T cut to 512
+    _full_check(wl.shape("attn_proj", T=512), wl.seed_for("attn_proj"), bwd=False)
+
+
+@pytest.mark.parametrize("out,inp,r,T", [
+    (1000, 1040, 384, 777),    # ragged M tile, ragged K block, N = 256 + 128 MMAs
+    (300, 256, 1, 65),         # r = 1 (N padded to 16), B padded to a 16-byte row
+    (257, 512, 17, 33),        # r not a multiple of 4 or 16
+    (384, 256, 272, 40),       # one N chunk of 272 = 256 + 16
+    (200, 128, 400, 24),       # two N chunks of 208
+    (130, 64, 768, 16),        # two N chunks of 384 (the largest rank swept)
+    (8, 4, 5, 3),              # one K block, mostly out of bounds
+    (1, 16, 2, 1),             # a single output row, a single token
+])
+def test_shapes_span_tiles_and_ragged_tails(out, inp, r, T):
+    sh = wl.shape("high_rank", out=out, inp=inp, r=r, T=T)
+    _full_check(sh, 7000 + out + r)
+
+
+def test_mlp_shapes_reduced():
+    # rectangular gate/up and down shapes (in != out), tokens cut down
+    _full_check(wl.shape("mlp_gate_up", out=1792, inp=512, T=64), 4000)
+    _full_check(wl.shape("mlp_down", out=512, inp=1792, T=64), 4001)
+
+
+def test_bitwise_determinism():
+    sh = wl.shape("high_rank", out=640, inp=1024, r=96, T=300)
+    d = wl.make_module(sh, 99)
+    s = d["s"]
+    W0, A, B, m = _weights_dev(d)
+    base, lora, dy = (act_to_dev(d[k]) for k in ("base", "lora", "dy"))
+    outs = []
+    for _ in range(2):
+        norm, g = run_norm(W0, A, B, m, s)
+        y = run_fwd(base, lora, g, s)
+        db, dl, dm = run_bwd(dy, base, lora, g, norm, s)
+        outs.append([t.clone() for t in (norm, g, y, db, dl, dm)])
+    for a, b in zip(*outs):
+        assert torch.equal(a.view(torch.uint8) if a.dtype != torch.uint8 else a,
+                           b.view(torch.uint8) if b.dtype != torch.uint8 else b)
+    assert_no_device_error()
+
+
+def test_zero_adapter_gives_identity():
+    # B = 0 and m = ||W0_i||: g = 1 up to fp32 rounding of the row norm, and in
+    # bf16 the correction vanishes exactly: y == base, d_base == dy bitwise
+    sh = wl.shape("high_rank", out=512, inp=768, r=32, T=128)
+    d = wl.make_module(sh, 5)
+    d["B"] = np.zeros_like(d["B"])
+    d["m"] = np.linalg.norm(d["W0"].astype(np.float64), axis=1).astype(np.float32)
+    W0, A, B, m = _weights_dev(d)
+    norm, g = run_norm(W0, A, B, m, d["s"])
+    gg = to_f64(g)
+    assert np.max(np.abs(gg - 1.0)) <= 4e-6
+    base = act_to_dev(d["base"])
+    y = run_fwd(base, torch.zeros_like(base), g, d["s"])
+    assert torch.equal(y.view(torch.int16), base.view(torch.int16))
+    dy = act_to_dev(d["dy"])
+    db, dl, dm = run_bwd(dy, base, torch.zeros_like(base), g, norm, d["s"])
+    assert torch.equal(db.view(torch.int16), dy.view(torch.int16))
+    assert_no_device_error()
+
+
+def test_empty_and_degenerate_token_counts():
+    out = 64
+    g = torch.ones(out, device=DEV)
+    norm = torch.full((out,), 2.0, device=DEV)
+    e = torch.empty(0, out, device=DEV, dtype=torch.bfloat16)
+    y = run_fwd(e, e, g, 1.0)
+    assert y.numel() == 0
+    db, dl, dm = run_bwd(e, e, e, g, norm, 1.0)
+    assert torch.equal(dm, torch.zeros(out, device=DEV))
+    assert_no_device_error()
+
+
+@pytest.mark.parametrize("act", ["bf16", "f32"])
+@pytest.mark.parametrize("out,off", [(101, 0), (101, 1), (104, 1), (104, 0)])
+def test_vector_and_scalar_paths(act, out, off):
+    # out not a multiple of the vector width, or rows that start off a 16-byte
+    # boundary, take the scalar path; both paths must give the same numbers
+    T, s = 37, 1.7
+    rng = np.random.default_rng(3 + out + off)
+    f = {k: rng.standard_normal((T, out)).astype(np.float32) for k in ("base", "lora", "dy")}
+    if act == "bf16":
+        f = {k: wl.f32_to_bf16_bits(v) for k, v in f.items()}
+    g = (1 + rng.uniform(-0.05, 0.05, out)).astype(np.float32)
+    n = rng.uniform(0.5, 2, out).astype(np.float32)
+    views = {}
+    for k, v in f.items():
+        src = act_to_dev(v)
+        buf = torch.empty(T * out + 8, device=DEV, dtype=src.dtype)
+        buf[off:off + T * out].copy_(src.reshape(-1))
+        views[k] = buf[off:off + T * out].view(T, out)
+    gd, nd = f32_dev(g), f32_dev(n)
+    y = run_fwd(views["base"], views["lora"], gd, s)
+    db, dl, dm = run_bwd(views["dy"], views["base"], views["lora"], gd, nd, s)
+    b64, l64, d64 = (act_to_f64(f[k]) for k in ("base", "lora", "dy"))
+    g64, n64 = g.astype(np.float64), n.astype(np.float64)
+    y_ref = oracle.compose_fwd(b64, l64, g64, s)
+    db_ref, dl_ref, dm_ref = oracle.compose_bwd(d64, b64, l64, g64, n64, s)
+    if act == "bf16":
+        check_bf16_rule("y", to_f64(y), y_ref)
+        check_bf16_rule("d_base", to_f64(db), db_ref)
+        check_bf16_rule("d_lora", to_f64(dl), dl_ref)
+    else:
+        check_bound("y", to_f64(y), y_ref, 2.0 ** -21 * (np.abs(b64) + np.abs(g64) * s * np.abs(l64)))
+        check_bound("d_base", to_f64(db), db_ref, 2.0 ** -22 * np.abs(g64) * np.abs(d64))
+        check_bound("d_lora", to_f64(dl), dl_ref, 2.0 ** -22 * np.abs(g64) * (1 + s) * np.abs(d64))
+    check_bound("d_mag", to_f64(dm), dm_ref, dmag_bound(d64, b64, l64, n64, s))
+    assert_no_device_error()
+
+
+def test_compose_same_g_fp32_exactness():
+    # with both sides given the same fp32 g, the bf16 compose must be the
+    # correctly rounded fp64 result except where the exact value is within
+    # fp32 noise of a rounding midpoint
+    T, out, s = 512, 1024, 32 / 384 ** 0.5
+    rng = np.random.default_rng(11)
+    base = wl.f32_to_bf16_bits(rng.standard_normal((T, out)).astype(np.float32))
+    lora = wl.f32_to_bf16_bits((rng.standard_normal((T, out)) * 0.196).astype(np.float32))
+    g = (1 + rng.uniform(-2 ** -9, 2 ** -9, out)).astype(np.float32)
+    y = run_fwd(act_to_dev(base), act_to_dev(lora), f32_dev(g), s)
+    exact = oracle.compose_fwd(act_to_f64(base), act_to_f64(lora), g.astype(np.float64), s)
+    rn = oracle.f64_to_bf16_bits(exact)
+    got = y.view(torch.int16).cpu().numpy().view(np.uint16)
+    frac = float(np.mean(got == rn))
+    assert frac >= 0.999, frac
+    assert_no_device_error()
+
+
+def test_g_near_one_stress_keeps_base_correction():
+    # m = n_fp64 * (1 + U(-2^-9, 2^-9)): g - 1 lies in the bf16 collapse region
+    # (a naive bf16 path rounds g to 1 and loses the correction).  The fused
+    # stable path must stay within the tolerance everywhere and match the
+    # correctly rounded result on >= 99.9% of elements.
+    sh = wl.shape("high_rank", out=1024, inp=1024, r=384, T=1024)
+    d = wl.make_module(sh, 2024)
+    s = d["s"]
+    n_ref = oracle.adapted_row_norm(d["W0"], d["A"], d["B"], s)
+    rng = np.random.default_rng(77)
+    d["m"] = (n_ref * (1 + rng.uniform(-2 ** -9, 2 ** -9, sh.out))).astype(np.float32)
+    W0, A, B, m = _weights_dev(d)
+    norm, g = run_norm(W0, A, B, m, s)
+    n_ref, g_ref = oracle.weight_norm(d["W0"], d["A"], d["B"], d["m"], s)
+    check_rel("g", to_f64(g), g_ref)
+    assert np.all(np.abs(g_ref - 1) <= 2 ** -9 * 1.01)
+    base, lora = act_to_dev(d["base"]), act_to_dev(d["lora"])
+    y = run_fwd(base, lora, g, s)
+    y_ref = oracle.compose_fwd(act_to_f64(d["base"]), act_to_f64(d["lora"]), g_ref, s)
+    check_bf16_rule("y", to_f64(y), y_ref)
+    rn = oracle.f64_to_bf16_bits(y_ref)
+    got = y.view(torch.int16).cpu().numpy().view(np.uint16)
+    stable_frac = float(np.mean(got == rn))
+    naive = oracle.compose_fwd_naive_bf16(d["base"], d["lora"], g_ref, s)
+    naive_frac = float(np.mean(naive == rn))
+    print(f"g~1 stress: correctly rounded match stable={stable_frac:.5f} naive={naive_frac:.5f}")
+    assert stable_frac >= 0.999
+    assert naive_frac < stable_frac
+    assert_no_device_error()

@@ -1,0 +1,98 @@
+"""GPU parity at the workloads' full sizes, in the launch configuration the
+benchmark times (the same library calls on the same shapes).  The oracle
+checks sampled outputs it can compute one by one -- whole rows of the norm,
+single elements of the compose, whole columns of d_mag -- and every output is
+checked for properties that hold at any size (finite, bitwise reproducible)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from parameter_efficient_fine_gb300 import workloads as wl
+
+from gpu_util import (act_to_dev, act_to_f64, assert_no_device_error, check_bf16_rule, check_bound, check_rel,
+                      dmag_bound, f32_dev, run_bwd, run_fwd, run_norm, to_f64)
+
+pytestmark = pytest.mark.gpu
+
+
+def _sampled_check(sh, seed, bwd=True, n_rows=384, n_elems=200_000, n_cols=48):
+    d = wl.make_module(sh, seed)
+    s = d["s"]
+    W0, A, B, m = (f32_dev(d[k]) for k in ("W0", "A", "B", "m"))
+    norm, g = run_norm(W0, A, B, m, s)
+    rng = np.random.default_rng(seed + 17)
+    rows = np.unique(np.concatenate([rng.choice(sh.out, n_rows, replace=False), [0, sh.out - 1]]))
+    n_ref, g_ref = oracle.weight_norm(d["W0"][rows], d["A"], d["B"][rows], d["m"][rows], s)
+    norm_h, g_h = to_f64(norm), to_f64(g)
+    check_rel("norm", norm_h[rows], n_ref)
+    check_rel("g", g_h[rows], g_ref)
+    assert np.all(np.isfinite(norm_h)) and np.all(norm_h > 0) and np.all(np.isfinite(g_h))
+
+    base, lora = act_to_dev(d["base"]), act_to_dev(d["lora"])
+    y = run_fwd(base, lora, g, s)
+    # single elements (t, j) with j among the rows whose g the oracle knows
+    pos = rng.integers(0, len(rows), n_elems)
+    tt = rng.integers(0, sh.T, n_elems)
+    jj = rows[pos]
+    b64 = act_to_f64(d["base"][tt, jj])
+    l64 = act_to_f64(d["lora"][tt, jj])
+    y_ref = oracle.compose_fwd(b64[None, :], l64[None, :], g_ref[pos], s)[0]
+    y_h = to_f64(y[torch.from_numpy(tt).cuda(), torch.from_numpy(jj).cuda()])
+    check_bf16_rule("y", y_h, y_ref)
+    assert bool(torch.isfinite(y.float()).all())
+    if bwd:
+        dy = act_to_dev(d["dy"])
+        db, dl, dm = run_bwd(dy, base, lora, g, norm, s)
+        d64 = act_to_f64(d["dy"][tt, jj])
+        db_ref, dl_ref, _ = oracle.compose_bwd(d64[None, :], b64[None, :], l64[None, :], g_ref[pos], n_ref[pos], s)
+        ti, ji = torch.from_numpy(tt).cuda(), torch.from_numpy(jj).cuda()
+        check_bf16_rule("d_base", to_f64(db[ti, ji]), db_ref[0])
+        check_bf16_rule("d_lora", to_f64(dl[ti, ji]), dl_ref[0])
+        # whole columns of d_mag
+        cpos = rng.choice(len(rows), min(n_cols, len(rows)), replace=False)
+        cols = rows[cpos]
+        dcol, bcol, lcol = (act_to_f64(d[k][:, cols]) for k in ("dy", "base", "lora"))
+        _, _, dm_ref = oracle.compose_bwd(dcol, bcol, lcol, g_ref[cpos], n_ref[cpos], s)
+        dm_h = to_f64(dm)[cols]
+        check_bf16_rule("d_mag", dm_h, dm_ref)
+        check_bound("d_mag", dm_h, dm_ref, dmag_bound(dcol, bcol, lcol, n_ref[cpos], s) + 1.1e-5 * np.abs(dm_ref))
+        assert bool(torch.isfinite(dm).all())
+        # the full-size backward is bitwise reproducible
+        db2, dl2, dm2 = run_bwd(dy, base, lora, g, norm, s)
+        assert torch.equal(dm.view(torch.int32), dm2.view(torch.int32))
+        assert torch.equal(db.view(torch.int16), db2.view(torch.int16))
+    norm2, g2 = run_norm(W0, A, B, m, s)
+    assert torch.equal(norm.view(torch.int32), norm2.view(torch.int32))
+    assert_no_device_error()
+
+
+def test_high_rank_training_step_full_size():
+    # out = in = 8192, r = 384, T = 15360: the benchmarked step
+    _sampled_check(wl.shape("high_rank"), wl.seed_for("high_rank"))
+
+
+def test_attention_projection_inference_full_size():
+    _sampled_check(wl.shape("attn_proj"), wl.seed_for("attn_proj"), bwd=False)
+
+
+@pytest.mark.parametrize("k,r", list(enumerate(wl.RANK_SWEEP)))
+def test_rank_sweep_norm_full_size(k, r):
+    # norm at every swept rank on the 8192-wide module (activations are the
+    # same kernels as the high-rank step and are not regenerated here)
+    sh = wl.shape("rank_sweep", r=r)
+    seed = wl.seed_for("rank_sweep", k)
+    w = wl.make_weights(sh, seed)
+    W0, A, B, m = (f32_dev(w[key]) for key in ("W0", "A", "B", "m"))
+    norm, g = run_norm(W0, A, B, m, w["s"])
+    rng = np.random.default_rng(seed)
+    rows = np.unique(np.concatenate([rng.choice(sh.out, 256, replace=False), [0, sh.out - 1]]))
+    n_ref, g_ref = oracle.weight_norm(w["W0"][rows], w["A"], w["B"][rows], w["m"][rows], w["s"])
+    check_rel("norm", to_f64(norm)[rows], n_ref)
+    check_rel("g", to_f64(g)[rows], g_ref)
+    assert_no_device_error()
+
+
+@pytest.mark.parametrize("name", ["mlp_gate_up", "mlp_down"])
+def test_mlp_modules_full_size(name):
+    _sampled_check(wl.shape(name), wl.seed_for(name), n_elems=100_000, n_cols=32)

@@ -103,7 +103,8 @@ def test_bitwise_determinism():
 
 def test_zero_adapter_gives_identity():
     # B = 0 and m = ||W0_i||: g = 1 up to fp32 rounding of the row norm, and in
-    # bf16 the correction vanishes exactly: y == base, d_base == dy bitwise
+    # bf16 the correction vanishes exactly: y == base, d_base == dy as values
+    # (IEEE gives -0 + (+0) = +0, so a -0.0 input may come back as +0.0)
     sh = wl.shape("high_rank", out=512, inp=768, r=32, T=128)
     d = wl.make_module(sh, 5)
     d["B"] = np.zeros_like(d["B"])
@@ -114,10 +115,10 @@ def test_zero_adapter_gives_identity():
     assert np.max(np.abs(gg - 1.0)) <= 4e-6
     base = act_to_dev(d["base"])
     y = run_fwd(base, torch.zeros_like(base), g, d["s"])
-    assert torch.equal(y.view(torch.int16), base.view(torch.int16))
+    assert torch.equal(y.float(), base.float())
     dy = act_to_dev(d["dy"])
     db, dl, dm = run_bwd(dy, base, torch.zeros_like(base), g, norm, d["s"])
-    assert torch.equal(db.view(torch.int16), dy.view(torch.int16))
+    assert torch.equal(db.float(), dy.float())
     assert_no_device_error()
 
 

@@ -12,19 +12,29 @@
 // so U never reaches global memory; only G (r x r) does.
 //
 // Launch sequence of dora_norm_factored:
-//   1. split_kernel      A -> (A_hi, A_lo), the 3-pass TF32 split of the N operand
+//   1. split_n_kernel    A -> (A_hi, A_c), the split N operand (see Precision)
 //   2. tc_gemm (GRAM)    partial tiles of G = A A^T, stream-K over K = in
-//   3. gram_reduce       fixed-order sum of the partial tiles, scaled by s/2, split hi/lo
+//   3. gram_reduce       fixed-order sum of the partial tiles, scaled by s/2, split
 //   4. tc_gemm (NORM)    [W0 | B] x [A | sG/2]^T, stream-K; per segment the epilogue
 //                        reduces each row to (sum W0_i^2 over its K range, <B_i, D_i>)
 //   5. norm_finalize     fixed-order sum of the segments, n = sqrt(max(0, n^2)), g = m/n
 //
-// Precision: fp32 inputs are split x = hi + lo with hi, lo TF32 (round to
-// nearest, ties away); each product is hi*hi + hi*lo + lo*hi (the dropped
-// lo*lo is ~2^-22 relative), accumulated in fp32 in tensor memory.  The
-// M-side operand (W0 or B) is split in shared memory by converter warps, which
-// also accumulate ||W0_i||^2 on the way; the N-side operand is split once in
-// global memory (it is re-read by every M tile).
+// Precision: every fp32 operand is split x = hi + lo, hi = x rounded to TF32
+// (nearest, ties away), lo = x - hi exactly, |lo| <= 2^-11 |x|.  Each product
+// is evaluated as
+//     x*y ~ hi_x*hi_y            one kind::tf32 MMA (exact products)
+//         + lo_x*hi_y + hi_x*lo_y  one kind::f16 MMA on bf16 operands, the two
+//                                  terms side by side along K (K = 16 = 8 + 8)
+// with fp32 accumulation in tensor memory.  The correction terms are ~2^-11 of
+// the product, so their bf16 rounding costs <= 2^-19 of it; lo*lo (2^-22) is
+// dropped.  Against three TF32 passes this issues 2/3 of the tensor work and
+// reads 2/3 of the operand bytes from shared memory per K step.
+// The M-side operand (W0 or B) is split in shared memory by converter warps,
+// which also accumulate ||W0_i||^2 on the way; the N-side operand is split once
+// in global memory (it is re-read by every M tile) into a TF32 matrix and a
+// bf16 matrix holding, per group of 8 K indices, 8 hi values then 8 lo values.
+// The M-side correction tile holds lo then hi per group, so the K-concatenated
+// bf16 MMA yields lo_x*hi_y + hi_x*lo_y.
 //
 // tc_gemm structure (one CTA per SM, persistent, 192 threads):
 //   warp 0      TMA producer: loads the M-side box [128 x 16 fp32] and the
@@ -44,6 +54,7 @@
 // copies in flight, the MMA lane for its issued MMAs, and tensor memory is
 // freed before the CTA exits.
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include <cstring>
@@ -62,7 +73,9 @@ constexpr int kMaxR = 1024;
 constexpr int kMaxCtas = 256;       // workspace bound: any device up to this size
 constexpr int kMinUnitsNorm = 4;
 constexpr int kMinUnitsGram = 16;
-constexpr int kSmemBudget = 200 * 1024;
+constexpr int kSmemMax = 232448;           // 227 KB: the opt-in maximum per CTA
+constexpr int kEpiBoxBytes = 32 * 32 * 4;   // epilogue B box: 32 rows x 32 fp32 (128-byte swizzle)
+constexpr int kEpiBytes = 4 * 2 * kEpiBoxBytes;  // 4 epilogue warps x 2 buffers
 constexpr int kMaxStages = 6;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
 
@@ -91,7 +104,6 @@ struct TcParams {
   unsigned stage_bytes;
   unsigned tx_bytes;
   float *part;      // GRAM: [tiles][maxseg][128][NC]; NORM: [tiles][maxseg][128][2]
-  const float *B;   // NORM epilogue: B [M, r]
   int r;
   int *err;
 };
@@ -167,6 +179,14 @@ __device__ __forceinline__ void mma_tf32(uint32_t d, uint64_t adesc, uint64_t bd
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc)
       : "memory");
 }
+__device__ __forceinline__ void mma_bf16(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc)
+      : "memory");
+}
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
                : "memory");
@@ -192,6 +212,11 @@ __device__ __forceinline__ uint32_t tf32_rna(float x) {
   asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
   return r;
 }
+// two floats -> two bf16 (nearest even), a in the low half
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t *>(&h);
+}
 
 // Shared-memory matrix descriptor: K-major operand, 64-byte swizzle, rows of
 // 64 bytes, 8-row groups 512 bytes apart.
@@ -210,6 +235,15 @@ __host__ __device__ __forceinline__ uint32_t idesc_tf32(int n) {
   return (1u << 4)                                  // D format: f32
          | (2u << 7)                                // A format: tf32
          | (2u << 10)                               // B format: tf32
+         | (static_cast<uint32_t>(n >> 3) << 17)    // N >> 3
+         | (static_cast<uint32_t>(kBM >> 4) << 24); // M >> 4
+}
+// Instruction descriptor: kind::f16 with bf16 operands, fp32 accumulator,
+// both K-major, M = 128, N = n.
+__host__ __device__ __forceinline__ uint32_t idesc_bf16(int n) {
+  return (1u << 4)                                  // D format: f32
+         | (1u << 7)                                // A format: bf16
+         | (1u << 10)                               // B format: bf16
          | (static_cast<uint32_t>(n >> 3) << 17)    // N >> 3
          | (static_cast<uint32_t>(kBM >> 4) << 24); // M >> 4
 }
@@ -258,21 +292,23 @@ __device__ void wait_drain(uint32_t bar, uint32_t parity) {
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kThreads, 1)
 tc_gemm_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ CUtensorMap mX2,
-               const __grid_constant__ CUtensorMap mY1h, const __grid_constant__ CUtensorMap mY1l,
-               const __grid_constant__ CUtensorMap mY2h, const __grid_constant__ CUtensorMap mY2l,
-               const TcParams p) {
+               const __grid_constant__ CUtensorMap mY1h, const __grid_constant__ CUtensorMap mY1c,
+               const __grid_constant__ CUtensorMap mY2h, const __grid_constant__ CUtensorMap mY2c,
+               const __grid_constant__ CUtensorMap mBe, const TcParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int S = p.stages;
-  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + static_cast<size_t>(S) * p.stage_bytes);
-  // barrier layout: full[S], conv[S], empty[S], accf, acce, fin
-  SharedCtl *ctl = reinterpret_cast<SharedCtl *>(bars + 3 * S + 3);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + static_cast<size_t>(S) * p.stage_bytes +
+                                               (p.mode == kNorm ? kEpiBytes : 0));
+  // barrier layout: full[S], conv[S], empty[S], accf, acce, fin, epi[8]
+  SharedCtl *ctl = reinterpret_cast<SharedCtl *>(bars + 3 * S + 3 + 8);
   const uint32_t full0 = smem_u32(bars);
   const uint32_t conv0 = full0 + 8u * S;
   const uint32_t empty0 = conv0 + 8u * S;
   const uint32_t accf = empty0 + 8u * S;
   const uint32_t acce = accf + 8;
   const uint32_t fin = acce + 8;
+  const uint32_t epib0 = fin + 8;   // epilogue B buffers: barrier of warp quadrant q, buffer b at epib0 + 8*(2q+b)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -286,17 +322,19 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ 
     mbar_init(accf, 1);
     mbar_init(acce, 128);
     mbar_init(fin, 1);
+    for (int e = 0; e < 8; ++e) mbar_init(epib0 + 8u * e, 1);
     ctl->abort = 0;
     fence_barrier_init();
   }
   if (warp == 0 && lane == 0) {
     prefetch_map(&mX1);
     prefetch_map(&mY1h);
-    prefetch_map(&mY1l);
+    prefetch_map(&mY1c);
+    if (p.mode == kNorm) prefetch_map(&mBe);
     if (p.kbtot > p.kb1) {
       prefetch_map(&mX2);
       prefetch_map(&mY2h);
-      prefetch_map(&mY2l);
+      prefetch_map(&mY2c);
     }
   }
   if (warp == 1) {
@@ -334,15 +372,15 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ 
           mbar_expect_tx(fb, p.tx_bytes);
           const uint32_t xs = smem_u32(smem + static_cast<size_t>(stage) * p.stage_bytes);
           const uint32_t yh = xs + 2u * kBM * kRowBytes;
-          const uint32_t yl = yh + static_cast<uint32_t>(p.NT) * kRowBytes;
+          const uint32_t yc = yh + static_cast<uint32_t>(p.NT) * kRowBytes;
           const bool seg1 = kb < p.kb1;
-          const int kx = (seg1 ? kb : kb - p.kb1) * kBK;
+          const int kx = (seg1 ? kb : kb - p.kb1) * kBK;   // fp32 column of the hi operands
           tma_load_2d(xs, seg1 ? &mX1 : &mX2, kx, mt * kBM, fb);
           for (int i = 0; i < p.nloads; ++i) {
             const int ny = nc * p.NC + i * p.nbox;
             const uint32_t off = static_cast<uint32_t>(i * p.nbox * kRowBytes);
             tma_load_2d(yh + off, seg1 ? &mY1h : &mY2h, kx, ny, fb);
-            tma_load_2d(yl + off, seg1 ? &mY1l : &mY2l, kx, ny, fb);
+            tma_load_2d(yc + off, seg1 ? &mY1c : &mY2c, 2 * kx, ny, fb);   // bf16 column
           }
           ++issued;
           if (++stage == S) {
@@ -374,6 +412,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ 
       bool ok = true;
       const uint32_t id0 = idesc_tf32(p.nmma0);
       const uint32_t id1 = p.nmma1 > 0 ? idesc_tf32(p.nmma1) : 0u;
+      const uint32_t ic0 = idesc_bf16(p.nmma0);
+      const uint32_t ic1 = p.nmma1 > 0 ? idesc_bf16(p.nmma1) : 0u;
       for (long long u = u_begin; u < u_end && ok;) {
         const int t = static_cast<int>(u / p.kbtot);
         const int kb0 = static_cast<int>(u - static_cast<long long>(t) * p.kbtot);
@@ -390,25 +430,25 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ 
           }
           tc_fence_after();
           const uint32_t xh = smem_u32(smem + static_cast<size_t>(stage) * p.stage_bytes);
-          const uint32_t xl = xh + kBM * kRowBytes;
-          const uint32_t yh = xl + kBM * kRowBytes;
-          const uint32_t yl = yh + static_cast<uint32_t>(p.NT) * kRowBytes;
+          const uint32_t xc = xh + kBM * kRowBytes;
+          const uint32_t yh = xc + kBM * kRowBytes;
+          const uint32_t yc = yh + static_cast<uint32_t>(p.NT) * kRowBytes;
 #pragma unroll
           for (int k = 0; k < kBK / 8; ++k) {
             const uint32_t acc0 = (kb != kb0 || k != 0) ? 1u : 0u;
-            const uint32_t ko = static_cast<uint32_t>(k) * 32u;  // 8 tf32 = 32 bytes
-            const uint64_t ah = sdesc_sw64(xh + ko), al = sdesc_sw64(xl + ko);
+            // K step k: 8 tf32 (32 bytes) of the hi tiles, 16 bf16 (32 bytes)
+            // of the correction tiles
+            const uint32_t ko = static_cast<uint32_t>(k) * 32u;
+            const uint64_t ah = sdesc_sw64(xh + ko), ac = sdesc_sw64(xc + ko);
             {
-              const uint64_t bh = sdesc_sw64(yh + ko), bl = sdesc_sw64(yl + ko);
-              mma_tf32(tmem, al, bh, id0, acc0);
-              mma_tf32(tmem, ah, bl, id0, 1u);
+              const uint64_t bh = sdesc_sw64(yh + ko), bc = sdesc_sw64(yc + ko);
+              mma_bf16(tmem, ac, bc, ic0, acc0);
               mma_tf32(tmem, ah, bh, id0, 1u);
             }
             if (p.nmma1 > 0) {
               const uint32_t no = 256u * kRowBytes;
-              const uint64_t bh = sdesc_sw64(yh + no + ko), bl = sdesc_sw64(yl + no + ko);
-              mma_tf32(tmem + 256u, al, bh, id1, acc0);
-              mma_tf32(tmem + 256u, ah, bl, id1, 1u);
+              const uint64_t bh = sdesc_sw64(yh + no + ko), bc = sdesc_sw64(yc + no + ko);
+              mma_bf16(tmem + 256u, ac, bc, ic1, acc0);
               mma_tf32(tmem + 256u, ah, bh, id1, 1u);
             }
           }
@@ -433,6 +473,11 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ 
     const int row = quad * 32 + lane;     // row within the M tile
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quad * 32) << 16);
     const int swz = (row >> 1) & 3;       // 64-byte swizzle: chunk c lives at c ^ swz
+    // epilogue B buffers of this warp (NORM): two 32 x 32 fp32 boxes
+    uint8_t *ebuf = smem + static_cast<size_t>(S) * p.stage_bytes + quad * 2 * kEpiBoxBytes;
+    const uint32_t eb_bar = epib0 + 16u * quad;
+    uint32_t eph = 0u;    // bit b: phase parity of buffer b's barrier
+    uint32_t epend = 0u;  // bit b: a copy into buffer b is in flight
     int stage = 0;
     uint32_t phase = 0;
     uint32_t aphase = 0;
@@ -452,28 +497,37 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ 
           ok = false;
           break;
         }
+        // this thread's row: 16 fp32 in four 16-byte chunks; logical chunk c
+        // sits at physical chunk c ^ swz in both the fp32 and the bf16 tile
         float4 *xh = reinterpret_cast<float4 *>(smem + static_cast<size_t>(stage) * p.stage_bytes + row * kRowBytes);
-        float4 *xl = reinterpret_cast<float4 *>(reinterpret_cast<uint8_t *>(xh) + kBM * kRowBytes);
-        float blk = 0.0f;
+        uint4 *xc = reinterpret_cast<uint4 *>(reinterpret_cast<uint8_t *>(xh) + kBM * kRowBytes);
+        float v[16], h[16], l[16];
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-          const int ph = c ^ swz;
-          const float4 v = xh[ph];
-          float4 h, l;
-          h.x = __uint_as_float(tf32_rna(v.x));
-          h.y = __uint_as_float(tf32_rna(v.y));
-          h.z = __uint_as_float(tf32_rna(v.z));
-          h.w = __uint_as_float(tf32_rna(v.w));
-          l.x = __uint_as_float(tf32_rna(v.x - h.x));
-          l.y = __uint_as_float(tf32_rna(v.y - h.y));
-          l.z = __uint_as_float(tf32_rna(v.z - h.z));
-          l.w = __uint_as_float(tf32_rna(v.w - h.w));
-          xh[ph] = h;
-          xl[ph] = l;
-          blk = fmaf(v.x, v.x, blk);
-          blk = fmaf(v.y, v.y, blk);
-          blk = fmaf(v.z, v.z, blk);
-          blk = fmaf(v.w, v.w, blk);
+          const float4 q = xh[c ^ swz];
+          v[4 * c] = q.x;
+          v[4 * c + 1] = q.y;
+          v[4 * c + 2] = q.z;
+          v[4 * c + 3] = q.w;
+        }
+        float blk = 0.0f;
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          h[e] = __uint_as_float(tf32_rna(v[e]));
+          l[e] = v[e] - h[e];
+          blk = fmaf(v[e], v[e], blk);
+        }
+#pragma unroll
+        for (int c = 0; c < 4; ++c) xh[c ^ swz] = make_float4(h[4 * c], h[4 * c + 1], h[4 * c + 2], h[4 * c + 3]);
+        // correction tile, per group of 8 K indices: 8 lo then 8 hi (bf16)
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          const float *lq = l + 8 * q;
+          const float *hq = h + 8 * q;
+          xc[(2 * q) ^ swz] = make_uint4(pack_bf16x2(lq[0], lq[1]), pack_bf16x2(lq[2], lq[3]),
+                                         pack_bf16x2(lq[4], lq[5]), pack_bf16x2(lq[6], lq[7]));
+          xc[(2 * q + 1) ^ swz] = make_uint4(pack_bf16x2(hq[0], hq[1]), pack_bf16x2(hq[2], hq[3]),
+                                             pack_bf16x2(hq[4], hq[5]), pack_bf16x2(hq[6], hq[7]));
         }
         if (kb < p.kb1) n0 += blk;
         fence_proxy_async();
@@ -495,16 +549,57 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ 
       const bool valid = grow < p.M;
       const int seg = static_cast<int>(blockIdx.x) - cta_of(static_cast<long long>(t) * p.kbtot, p.units, p.ctas);
       if (p.mode == kNorm) {
+        // <B_i, D_i>: the warp's 32 rows of B arrive as 32 x 32 boxes by TMA,
+        // two in flight; lane i reads row i (128-byte swizzle: chunk q at q ^ (i & 7))
         float dot = 0.0f;
-        const float *Brow = p.B + static_cast<size_t>(valid ? grow : 0) * p.r;
-        for (int c = 0; c < p.NC; c += 32) {
-          float v[32];
-          tmem_ld32(lane_addr + static_cast<uint32_t>(c), v);
-          const int n0c = nc * p.NC + c;
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            if (valid && c + j < p.NC && n0c + j < p.r) dot = fmaf(__ldg(Brow + n0c + j), v[j], dot);
+        const int nchk = (p.NC + 31) >> 5;
+        const int ybase = mt * kBM + quad * 32;
+        if (lane == 0) {
+          for (int b = 0; b < 2 && b < nchk; ++b) {
+            mbar_expect_tx(eb_bar + 8u * b, kEpiBoxBytes);
+            tma_load_2d(smem_u32(ebuf + b * kEpiBoxBytes), &mBe, nc * p.NC + 32 * b, ybase, eb_bar + 8u * b);
+            epend |= 1u << b;
           }
+        }
+        bool eok = true;
+        for (int ci = 0; ci < nchk; ++ci) {
+          const int b = ci & 1;
+          float v[32];
+          tmem_ld32(lane_addr + static_cast<uint32_t>(32 * ci), v);
+          const bool gotb = wait_bounded(eb_bar + 8u * b, (eph >> b) & 1u, ctl, p.err, 6);
+          if (!__all_sync(0xffffffffu, gotb)) {
+            eok = false;
+            break;
+          }
+          eph ^= 1u << b;
+          epend &= ~(1u << b);
+          const float4 *brow = reinterpret_cast<const float4 *>(ebuf + b * kEpiBoxBytes + lane * 128);
+          const int n0c = nc * p.NC + 32 * ci;
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const float4 bq = brow[q ^ (lane & 7)];
+            const float bj[4] = {bq.x, bq.y, bq.z, bq.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int j = 4 * q + e;
+              if (valid && 32 * ci + j < p.NC && n0c + j < p.r) dot = fmaf(bj[e], v[j], dot);
+            }
+          }
+          __syncwarp();
+          if (lane == 0 && ci + 2 < nchk) {
+            mbar_expect_tx(eb_bar + 8u * b, kEpiBoxBytes);
+            tma_load_2d(smem_u32(ebuf + b * kEpiBoxBytes), &mBe, n0c + 64, ybase, eb_bar + 8u * b);
+            epend |= 1u << b;
+          }
+        }
+        if (!eok) {
+          // drain this warp's epilogue copies still in flight, then leave
+          if (lane == 0) {
+            for (int b = 0; b < 2; ++b)
+              if ((epend >> b) & 1u) wait_drain(eb_bar + 8u * b, (eph >> b) & 1u);
+          }
+          ok = false;
+          break;
         }
         if (valid) {
           float2 *dst = reinterpret_cast<float2 *>(p.part) + (static_cast<size_t>(t) * p.maxseg + seg) * kBM + row;
@@ -543,22 +638,32 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ 
 // elementwise helpers
 // ---------------------------------------------------------------------------
 
-// x -> (hi, lo) TF32 split, count elements (multiple of 4, 16-byte aligned)
-__global__ void __launch_bounds__(256) split_kernel(const float *__restrict__ x, long long n4,
-                                                    float *__restrict__ hi, float *__restrict__ lo) {
-  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += (long long)gridDim.x * blockDim.x) {
-    const float4 v = __ldg(reinterpret_cast<const float4 *>(x) + i);
-    float4 h, l;
+// N-side split of a [rows, cols] fp32 matrix (cols % 4 == 0):
+//   hi [rows, cols] fp32: x rounded to TF32
+//   c  [rows, 2*cols8] bf16 (cols8 = cols rounded up to 8): per group q of 8
+//      columns, 8 bf16(hi) then 8 bf16(x - hi); zero past cols
+// One thread per group of 4 columns.
+__global__ void __launch_bounds__(256) split_n_kernel(const float *__restrict__ x, long long rows, int cols,
+                                                      int cols8, float *__restrict__ hi,
+                                                      __nv_bfloat16 *__restrict__ c) {
+  const int g4 = cols8 / 4;
+  const long long n = rows * g4;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
+    const long long row = i / g4;
+    const int k = static_cast<int>(i - row * g4) * 4;   // first column of the group of 4
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (k < cols) v = __ldg(reinterpret_cast<const float4 *>(x + row * cols + k));
+    float4 h;
     h.x = __uint_as_float(tf32_rna(v.x));
     h.y = __uint_as_float(tf32_rna(v.y));
     h.z = __uint_as_float(tf32_rna(v.z));
     h.w = __uint_as_float(tf32_rna(v.w));
-    l.x = __uint_as_float(tf32_rna(v.x - h.x));
-    l.y = __uint_as_float(tf32_rna(v.y - h.y));
-    l.z = __uint_as_float(tf32_rna(v.z - h.z));
-    l.w = __uint_as_float(tf32_rna(v.w - h.w));
-    reinterpret_cast<float4 *>(hi)[i] = h;
-    reinterpret_cast<float4 *>(lo)[i] = l;
+    if (k < cols) *reinterpret_cast<float4 *>(hi + row * cols + k) = h;
+    const long long cbase = row * 2LL * cols8 + 16LL * (k / 8) + (k % 8);
+    uint2 hb = make_uint2(pack_bf16x2(h.x, h.y), pack_bf16x2(h.z, h.w));
+    uint2 lb = make_uint2(pack_bf16x2(v.x - h.x, v.y - h.y), pack_bf16x2(v.z - h.z, v.w - h.w));
+    *reinterpret_cast<uint2 *>(c + cbase) = hb;
+    *reinterpret_cast<uint2 *>(c + cbase + 8) = lb;
   }
 }
 
@@ -578,10 +683,11 @@ struct StreamK {
   int ctas, kbtot, maxseg;
 };
 
-// Gs[k][l] = (s/2) * G[k][l] for k, l < r (zero-padded to npad), split hi/lo
+// Gs[k][l] = (s/2) * G[k][l] for k, l < r (zero-padded to npad), split like
+// split_n_kernel: gh [npad, npad] TF32, gc [npad, 2*npad] bf16 (8 hi, 8 lo per group)
 __global__ void __launch_bounds__(256) gram_reduce_kernel(const float *__restrict__ part, StreamK sk, int nchunks,
                                                           int NC, int r, int npad, float half_s,
-                                                          float *__restrict__ gh, float *__restrict__ gl) {
+                                                          float *__restrict__ gh, __nv_bfloat16 *__restrict__ gc) {
   const long long n = static_cast<long long>(npad) * npad;
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
     const int k = static_cast<int>(i / npad);
@@ -600,7 +706,9 @@ __global__ void __launch_bounds__(256) gram_reduce_kernel(const float *__restric
     }
     const float h = __uint_as_float(tf32_rna(v));
     gh[i] = h;
-    gl[i] = __uint_as_float(tf32_rna(v - h));
+    const long long cb = static_cast<long long>(k) * 2 * npad + 16 * (l / 8) + (l % 8);
+    gc[cb] = __float2bfloat16_rn(h);
+    gc[cb + 8] = __float2bfloat16_rn(v - h);
   }
 }
 
@@ -670,7 +778,8 @@ bool plan_gemm(int mode, int M, int kb1, int kb2, int r, int sms, GemmPlan *gp) 
   p.tmem_cols = cols;
   p.stage_bytes = static_cast<unsigned>(2 * kBM * kRowBytes + 2 * p.NT * kRowBytes);
   p.tx_bytes = static_cast<unsigned>(kBM * kRowBytes + 2 * p.NT * kRowBytes);
-  p.stages = static_cast<int>((kSmemBudget - 2048) / p.stage_bytes);
+  const int epi = mode == kNorm ? kEpiBytes : 0;
+  p.stages = static_cast<int>((kSmemMax - 1024 - epi - 512) / p.stage_bytes);
   if (p.stages > kMaxStages) p.stages = kMaxStages;
   if (p.stages < 2) return false;
   const int mtiles = static_cast<int>(dora::ceil_div(M, kBM));
@@ -685,14 +794,14 @@ bool plan_gemm(int mode, int M, int kb1, int kb2, int r, int sms, GemmPlan *gp) 
   p.r = r;
   const size_t per_row = mode == kGram ? static_cast<size_t>(p.NC) : 2;
   gp->part_bytes = static_cast<size_t>(p.tiles) * p.maxseg * kBM * per_row * sizeof(float);
-  gp->smem_bytes = static_cast<size_t>(p.stages) * p.stage_bytes + 1024 /*align*/ + 8 * (3 * p.stages + 3) + 64;
+  gp->smem_bytes = static_cast<size_t>(p.stages) * p.stage_bytes + epi + 1024 /*align*/ + 8 * (3 * p.stages + 3 + 8) + 64;
   // tensor memory: a CTA holding 512 columns must be alone on its SM
   if (p.tmem_cols > 256 && gp->smem_bytes < 116 * 1024) gp->smem_bytes = 116 * 1024;
   return true;
 }
 
 struct Layout {
-  size_t a_hi, a_lo, g_hi, g_lo, part_g, part_n, b_pad, total;
+  size_t a_hi, a_c, g_hi, g_c, part_g, part_n, b_pad, total;
 };
 
 size_t al256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -711,9 +820,9 @@ bool plan_layout(int64_t out, int64_t in, int64_t r, int sms, GemmPlan *gg, Gemm
     return o;
   };
   L->a_hi = take(static_cast<size_t>(r) * in * 4);
-  L->a_lo = take(static_cast<size_t>(r) * in * 4);
+  L->a_c = take(static_cast<size_t>(r) * dora::round_up(in, 8) * 4);   // bf16 [r, 2*in8]
   L->g_hi = take(static_cast<size_t>(npad) * npad * 4);
-  L->g_lo = take(static_cast<size_t>(npad) * npad * 4);
+  L->g_c = take(static_cast<size_t>(npad) * npad * 4);                 // bf16 [npad, 2*npad]
   L->part_g = take(gg->part_bytes);
   L->part_n = take(gn->part_bytes);
   L->b_pad = (r % 4) ? take(static_cast<size_t>(out) * dora::round_up(r, 4) * 4) : 0;
@@ -745,17 +854,21 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// 2-D fp32 matrix [rows, cols] with row stride ld (elements), box [box_rows, 16]
-bool make_map(CUtensorMap *map, const float *base, int64_t rows, int64_t cols, int64_t ld, int box_rows) {
+// 2-D matrix [rows, cols] with row stride ld (elements); box = box_bytes of a
+// row (64: 64-byte swizzle, 128: 128-byte swizzle) x box_rows rows, zero fill
+bool make_map(CUtensorMap *map, const void *base, bool bf16, int64_t rows, int64_t cols, int64_t ld, int box_rows,
+              int box_bytes = kRowBytes) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
+  const int esz = bf16 ? 2 : 4;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 4};
-  cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), static_cast<cuuint32_t>(box_rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * esz};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(box_bytes / esz), static_cast<cuuint32_t>(box_rows)};
   cuuint32_t estr[2] = {1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
+            const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            box_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 int grid_for(long long n, int sms) {
@@ -813,9 +926,9 @@ extern "C" dora_status dora_norm_factored(const float *W0, const float *A, const
   if (!plan_layout(out, in, r, sms, &gg, &gn, &L)) return DORA_ERR_SHAPE;
   uint8_t *ws = static_cast<uint8_t *>(workspace);
   float *a_hi = reinterpret_cast<float *>(ws + L.a_hi);
-  float *a_lo = reinterpret_cast<float *>(ws + L.a_lo);
+  __nv_bfloat16 *a_c = reinterpret_cast<__nv_bfloat16 *>(ws + L.a_c);
   float *g_hi = reinterpret_cast<float *>(ws + L.g_hi);
-  float *g_lo = reinterpret_cast<float *>(ws + L.g_lo);
+  __nv_bfloat16 *g_c = reinterpret_cast<__nv_bfloat16 *>(ws + L.g_c);
   float *part_g = reinterpret_cast<float *>(ws + L.part_g);
   float *part_n = reinterpret_cast<float *>(ws + L.part_n);
   const float *Bk = B;
@@ -833,7 +946,7 @@ extern "C" dora_status dora_norm_factored(const float *W0, const float *A, const
     if (!err_ptr[device]) {
       void *ptr = nullptr;
       if (cudaGetSymbolAddress(&ptr, g_dora_err) != cudaSuccess) return DORA_ERR_CUDA;
-      if (cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget + 2048) !=
+      if (cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax) !=
           cudaSuccess)
         return DORA_ERR_CUDA;
       err_ptr[device] = static_cast<int *>(ptr);
@@ -845,8 +958,8 @@ extern "C" dora_status dora_norm_factored(const float *W0, const float *A, const
   uint64_t launches = 0;
 
   // 1. N-side split of A; B padded to a TMA-legal row stride when r % 4 != 0
-  const long long a4 = r * in / 4;
-  split_kernel<<<grid_for(a4, sms), 256, 0, cs>>>(A, a4, a_hi, a_lo);
+  const int in8 = static_cast<int>(dora::round_up(in, 8));
+  split_n_kernel<<<grid_for(r * in8 / 4, sms), 256, 0, cs>>>(A, r, static_cast<int>(in), in8, a_hi, a_c);
   ++launches;
   if (r % 4) {
     const int rp = static_cast<int>(dora::round_up(r, 4));
@@ -858,12 +971,13 @@ extern "C" dora_status dora_norm_factored(const float *W0, const float *A, const
   }
 
   // tensor maps
-  CUtensorMap mA, mAh_n, mAl_n, mW0, mB, mGh, mGl;
+  CUtensorMap mA, mAh_n, mAc_n, mW0, mB, mGh, mGc, mBe;
   const int nbox = gn.p.nbox;
-  bool ok = make_map(&mA, A, r, in, in, kBM) && make_map(&mAh_n, a_hi, r, in, in, nbox) &&
-            make_map(&mAl_n, a_lo, r, in, in, nbox) && make_map(&mW0, W0, out, in, in, kBM) &&
-            make_map(&mB, Bk, out, ldb, ldb, kBM) && make_map(&mGh, g_hi, npad, npad, npad, nbox) &&
-            make_map(&mGl, g_lo, npad, npad, npad, nbox);
+  bool ok = make_map(&mA, A, false, r, in, in, kBM) && make_map(&mAh_n, a_hi, false, r, in, in, nbox) &&
+            make_map(&mAc_n, a_c, true, r, 2 * in8, 2 * in8, nbox) && make_map(&mW0, W0, false, out, in, in, kBM) &&
+            make_map(&mB, Bk, false, out, ldb, ldb, kBM) && make_map(&mGh, g_hi, false, npad, npad, npad, nbox) &&
+            make_map(&mGc, g_c, true, npad, 2 * npad, 2 * npad, nbox) &&
+            make_map(&mBe, Bk, false, out, ldb, ldb, 32, 128);
   if (!ok) {
     dora::count_launches(launches);
     return DORA_ERR_CUDA;
@@ -872,20 +986,19 @@ extern "C" dora_status dora_norm_factored(const float *W0, const float *A, const
   // 2. Gram partial tiles
   gg.p.part = part_g;
   gg.p.err = errp;
-  tc_gemm_kernel<<<gg.p.ctas, kThreads, gg.smem_bytes, cs>>>(mA, mA, mAh_n, mAl_n, mAh_n, mAl_n, gg.p);
+  tc_gemm_kernel<<<gg.p.ctas, kThreads, gg.smem_bytes, cs>>>(mA, mA, mAh_n, mAc_n, mAh_n, mAc_n, mA, gg.p);
   ++launches;
 
-  // 3. Gs = (s/2) G, split hi/lo
+  // 3. Gs = (s/2) G, split like A
   StreamK skg{gg.p.units, gg.p.ctas, gg.p.kbtot, gg.p.maxseg};
   gram_reduce_kernel<<<grid_for(static_cast<long long>(npad) * npad, sms), 256, 0, cs>>>(
-      part_g, skg, gg.p.nchunks, gg.p.NC, static_cast<int>(r), npad, 0.5f * s, g_hi, g_lo);
+      part_g, skg, gg.p.nchunks, gg.p.NC, static_cast<int>(r), npad, 0.5f * s, g_hi, g_c);
   ++launches;
 
   // 4. [W0 | B] x [A | Gs]^T with per-segment row reductions
   gn.p.part = part_n;
   gn.p.err = errp;
-  gn.p.B = B;
-  tc_gemm_kernel<<<gn.p.ctas, kThreads, gn.smem_bytes, cs>>>(mW0, mB, mAh_n, mAl_n, mGh, mGl, gn.p);
+  tc_gemm_kernel<<<gn.p.ctas, kThreads, gn.smem_bytes, cs>>>(mW0, mB, mAh_n, mAc_n, mGh, mGc, mBe, gn.p);
   ++launches;
 
   // 5. n and g

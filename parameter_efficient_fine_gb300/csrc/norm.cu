@@ -76,7 +76,7 @@ constexpr int kMinUnitsGram = 16;
 constexpr int kSmemMax = 232448;           // 227 KB: the opt-in maximum per CTA
 constexpr int kEpiBoxBytes = 32 * 32 * 4;   // epilogue B box: 32 rows x 32 fp32 (128-byte swizzle)
 constexpr int kEpiBytes = 4 * 2 * kEpiBoxBytes;  // 4 epilogue warps x 2 buffers
-constexpr int kMaxStages = 6;
+constexpr int kMaxStages = 12;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
 
 enum Mode : int { kGram = 0, kNorm = 1 };

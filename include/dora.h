@@ -83,9 +83,10 @@ size_t dora_norm_factored_workspace(int64_t out, int64_t in, int64_t r);
  *     n_i^2 = ||W0_i||^2 + 2 s <U_i, B_i> + s^2 B_i G B_i^T,
  *     U = W0 A^T [out,r],  G = A A^T [r,r],
  * so the out x in adapted weight is never formed.  The contractions run on the
- * tensor cores in a 3-pass TF32 split (hi*hi + hi*lo + lo*hi) with fp32
- * accumulation; n^2 is clamped at 0 before the square root; g is an IEEE
- * division with no epsilon (n = 0 gives inf/NaN).
+ * tensor cores with every fp32 operand split as x = hi + lo (hi = x rounded to
+ * TF32): hi*hi in one TF32 MMA, lo*hi + hi*lo in one bf16 MMA, fp32
+ * accumulation (relative error ~2^-19 per product); n^2 is clamped at 0 before
+ * the square root; g is an IEEE division with no epsilon (n = 0 gives inf/NaN).
  *
  *   W0    float32 [out, in]    16-byte aligned, in % 4 == 0
  *   A     float32 [r, in]      16-byte aligned
@@ -165,6 +166,44 @@ dora_status dora_compose_bwd(dora_dtype act, const void *grad_out, const void *b
                              void *d_base, void *d_lora, float *d_mag,
                              void *workspace, size_t workspace_bytes,
                              dora_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* (b') compose backward without a workspace                                 */
+/* ------------------------------------------------------------------------ */
+
+/* Size, in floats, of the library's fixed device scratch array (4 MiB). */
+#define DORA_NOALLOC_SCRATCH_FLOATS (1 << 20)
+
+/*
+ * Same results as dora_compose_bwd, but allocation-free for the caller: no
+ * workspace argument.  The paper has no counterpart to this entry point; it
+ * exists for callers that cannot allocate device memory where they run the
+ * backward -- code embedded in an application that owns a fixed device memory
+ * pool and exposes no allocator, or services that forbid cudaMalloc after
+ * start-up because it synchronises the device and fragments shared memory.
+ *
+ * The d_mag partial sums go to one file-scope device array of
+ * DORA_NOALLOC_SCRATCH_FLOATS floats, held on every GPU that loads the library
+ * until the process exits.  The first call on a device looks up that array's
+ * device address (cudaGetSymbolAddress, with the device current); make that
+ * first call before any stream capture.  Every partial sum the call reads is
+ * written earlier in the same call, so nothing needs clearing between calls,
+ * but all calls share the one array: calls that overlap on the GPU (different
+ * streams, or concurrent host threads on one device) race and give wrong
+ * d_mag.  The call itself allocates nothing (no cudaMalloc/cudaFree, no
+ * allocating library routine).
+ *
+ * Arguments, layouts and errors as dora_compose_bwd, plus: out must not exceed
+ * DORA_NOALLOC_SCRATCH_FLOATS (DORA_ERR_SHAPE otherwise).  When the usual
+ * token-lane grid would need more scratch than the array holds, fewer grid
+ * rows are used; d_mag then sums in a different (still fixed) order and may
+ * differ from dora_compose_bwd's by fp32 rounding.
+ */
+dora_status dora_compose_bwd_noalloc(dora_dtype act, const void *grad_out, const void *base,
+                                     const void *lora, const float *g, const float *norm,
+                                     float s, int64_t T, int64_t out,
+                                     void *d_base, void *d_lora, float *d_mag,
+                                     dora_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
 /* diagnostics                                                               */

@@ -21,6 +21,7 @@ __all__ = [
     "dora_compose_fwd",
     "dora_compose_bwd_workspace",
     "dora_compose_bwd",
+    "dora_compose_bwd_noalloc",
     "dora_device_error",
     "dora_kernel_launches",
     "DORA_F32",
@@ -47,6 +48,7 @@ _SIGNATURES = {
     "dora_compose_fwd": (_int, [_int, _vp, _vp, _vp, _f32, _i64, _i64, _vp, _vp]),
     "dora_compose_bwd_workspace": (_sz, [_i64, _i64]),
     "dora_compose_bwd": (_int, [_int, _vp, _vp, _vp, _vp, _vp, _f32, _i64, _i64, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "dora_compose_bwd_noalloc": (_int, [_int, _vp, _vp, _vp, _vp, _vp, _f32, _i64, _i64, _vp, _vp, _vp, _vp]),
     "dora_device_error": (_int, [ctypes.POINTER(_int)]),
     "dora_kernel_launches": (ctypes.c_uint64, []),
 }
@@ -145,6 +147,19 @@ def dora_compose_bwd(grad_out, base, lora, g, norm, s: float, d_base, d_lora, d_
         _ptr(d_base), _ptr(d_lora), _ptr(d_mag), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _stream(stream))
     _check("dora_compose_bwd", st)
+
+
+def dora_compose_bwd_noalloc(grad_out, base, lora, g, norm, s: float, d_base, d_lora, d_mag,
+                             stream=None) -> None:
+    """dora_compose_bwd without a workspace, for callers that cannot allocate
+    device memory where they run the backward: the partial sums use the
+    library's fixed device scratch array (see include/dora.h; calls that
+    overlap on the GPU race on that array)."""
+    T, out = grad_out.shape
+    st = load_library().dora_compose_bwd_noalloc(
+        _act(grad_out), _ptr(grad_out), _ptr(base), _ptr(lora), _ptr(g), _ptr(norm), float(s), T, out,
+        _ptr(d_base), _ptr(d_lora), _ptr(d_mag), _stream(stream))
+    _check("dora_compose_bwd_noalloc", st)
 
 
 def dora_device_error() -> int:

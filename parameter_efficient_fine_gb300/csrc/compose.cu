@@ -430,3 +430,96 @@ extern "C" dora_status dora_compose_bwd(dora_dtype act, const void *grad_out, co
   return launch_bwd<float, 1>(grad_out, base, lora, g, norm, s, T, out, d_base, d_lora, d_mag, part,
                               workspace_bytes, cs, device, info.sms);
 }
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant of the backward.
+//
+// Some callers cannot allocate device memory at the point where they run the
+// backward: code embedded in a host application that owns a fixed device
+// memory pool and hands out no allocator, or services that forbid cudaMalloc
+// after start-up because it synchronises the device and fragments memory that
+// is shared with other work.  For them the d_mag partial sums live in one
+// file-scope device array of fixed size instead of a caller workspace.  Every
+// GPU that loads the library holds this array until the process exits.
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr int64_t kNoAllocScratchFloats = DORA_NOALLOC_SCRATCH_FLOATS;
+static __device__ __align__(256) float g_noalloc_scratch[kNoAllocScratchFloats];
+
+// Device address of g_noalloc_scratch, looked up once per device with that
+// device current (in host code the symbol name is only a host-side stand-in).
+float *noalloc_scratch_address(int device) {
+  static std::mutex mu;
+  static float *addr[64] = {};
+  if (device < 0 || device >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[device]) {
+    void *ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess) return nullptr;
+    addr[device] = static_cast<float *>(ptr);
+  }
+  return addr[device];
+}
+
+template <typename Act, int VEC>
+dora_status launch_bwd_noalloc(const void *dy, const void *base, const void *lora, const float *g,
+                               const float *norm, float s, int64_t T, int64_t out, void *d_base, void *d_lora,
+                               float *d_mag, float *part, cudaStream_t stream, int device, int sms) {
+  auto kern = compose_bwd_kernel<Act, VEC>;
+  const int bps = blocks_per_sm(kern, device);
+  int64_t rows = 0;
+  if (T > 0) {
+    Grid gr = plan_grid(T, out / VEC, (int64_t)sms * bps);
+    // fewer token-lane rows when the partial sums would not fit the scratch
+    const int64_t cap = kNoAllocScratchFloats / out;
+    if (gr.gy > cap) gr.gy = cap;
+    rows = gr.gy;
+    kern<<<dim3((unsigned)gr.gx, (unsigned)gr.gy), dim3(kBX, kBY), 0, stream>>>(
+        static_cast<const Act *>(dy), static_cast<const Act *>(base), static_cast<const Act *>(lora), g, s, T,
+        out, static_cast<Act *>(d_base), static_cast<Act *>(d_lora), part);
+    dora::count_launches(1);
+    if (cudaGetLastError() != cudaSuccess) return DORA_ERR_CUDA;
+  }
+  dmag_reduce_kernel<<<(unsigned)dora::ceil_div(out, 256), 256, 0, stream>>>(part, rows, out, norm, d_mag);
+  dora::count_launches(1);
+  return dora::launch_status();
+}
+
+}  // namespace
+
+extern "C" dora_status dora_compose_bwd_noalloc(dora_dtype act, const void *grad_out, const void *base,
+                                                const void *lora, const float *g, const float *norm, float s,
+                                                int64_t T, int64_t out, void *d_base, void *d_lora, float *d_mag,
+                                                dora_stream_t stream) {
+  if (!valid_dtype(act)) return DORA_ERR_DTYPE;
+  if (T < 0 || out < 0) return DORA_ERR_SHAPE;
+  if (out > kNoAllocScratchFloats) return DORA_ERR_SHAPE;   // one partial row must fit the scratch
+  if (out == 0) return DORA_OK;
+  if (!g || !norm || !d_mag) return DORA_ERR_NULL;
+  if (T > 0 && (!grad_out || !base || !lora || !d_base || !d_lora)) return DORA_ERR_NULL;
+  const size_t esz = act == DORA_F32 ? 4 : 2;
+  if (T > 0 && (!dora::aligned(grad_out, esz) || !dora::aligned(base, esz) || !dora::aligned(lora, esz) ||
+                !dora::aligned(d_base, esz) || !dora::aligned(d_lora, esz)))
+    return DORA_ERR_ALIGN;
+  if (!dora::aligned(g, 4) || !dora::aligned(norm, 4) || !dora::aligned(d_mag, 4)) return DORA_ERR_ALIGN;
+  dora::DeviceInfo info;
+  int device = 0;
+  dora_status st = dora::current_device(&info, &device);
+  if (st != DORA_OK) return st;
+  float *part = noalloc_scratch_address(device);
+  if (!part) return DORA_ERR_CUDA;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  if (act == DORA_BF16) {
+    if (vector_ok<__nv_bfloat16>(out, {grad_out, base, lora, d_base, d_lora}))
+      return launch_bwd_noalloc<__nv_bfloat16, 8>(grad_out, base, lora, g, norm, s, T, out, d_base, d_lora, d_mag,
+                                                  part, cs, device, info.sms);
+    return launch_bwd_noalloc<__nv_bfloat16, 1>(grad_out, base, lora, g, norm, s, T, out, d_base, d_lora, d_mag,
+                                                part, cs, device, info.sms);
+  }
+  if (vector_ok<float>(out, {grad_out, base, lora, d_base, d_lora}))
+    return launch_bwd_noalloc<float, 4>(grad_out, base, lora, g, norm, s, T, out, d_base, d_lora, d_mag, part, cs,
+                                        device, info.sms);
+  return launch_bwd_noalloc<float, 1>(grad_out, base, lora, g, norm, s, T, out, d_base, d_lora, d_mag, part, cs,
+                                      device, info.sms);
+}

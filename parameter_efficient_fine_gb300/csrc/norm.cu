@@ -71,6 +71,7 @@ constexpr int kThreads = 192;
 constexpr int kMaxChunkN = 384;     // largest N handled by one CTA pass
 constexpr int kMaxR = 1024;
 constexpr int kMaxCtas = 256;       // workspace bound: any device up to this size
+constexpr int kMaxCluster = 2;      // largest cluster of the norm pass (4 measured slower)
 constexpr int kMinUnitsNorm = 4;
 constexpr int kMinUnitsGram = 16;
 constexpr int kSmemMax = 232448;           // 227 KB: the opt-in maximum per CTA
@@ -91,15 +92,18 @@ struct TcParams {
   int kbtot;        // K blocks in total (segment 2 = B / Gs columns)
   int nchunks;      // N chunks per M tile
   int NC;           // N per chunk (multiple of 16, <= kMaxChunkN)
+  int csize;        // CTAs per cluster: they take consecutive M tiles over the same K range
+  int sl;           // N-side rows each CTA of a cluster loads (and multicasts to the cluster)
   int nbox;         // rows per N-side TMA box
-  int nloads;       // N-side boxes per stage (per hi / lo)
-  int NT;           // N-side rows in shared memory per stage (nloads * nbox)
+  int nb;           // N-side boxes per CTA per stage (per hi / correction): sl = nb * nbox
+  int NT;           // N-side rows in shared memory per stage (csize * sl >= NC)
   int nmma0, nmma1; // N of the first / second MMA instruction of a chunk
   int tmem_cols;
   int stages;
-  int tiles;        // M tiles * nchunks
+  int tiles;        // M-tile groups (csize M tiles each) * nchunks
   long long units;  // tiles * kbtot
-  int ctas;
+  int ctas;         // clusters * csize
+  int ncl;          // clusters
   int maxseg;
   unsigned stage_bytes;
   unsigned tx_bytes;
@@ -152,6 +156,24 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
       : "memory");
 }
+// the same box into the same shared-memory offset of every CTA in `mask`,
+// completing bytes on each destination CTA's barrier at offset `bar`
+__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar,
+                                               uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster "
+      "[%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "h"(mask)
+      : "memory");
+}
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
 __device__ __forceinline__ void prefetch_map(const CUtensorMap *map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -189,6 +211,13 @@ __device__ __forceinline__ void mma_bf16(uint32_t d, uint64_t adesc, uint64_t bd
 }
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
+}
+// arrive (once MMAs complete) on the barrier at offset `bar` of every CTA in `mask`
+__device__ __forceinline__ void mma_commit_mc(uint32_t bar, uint16_t mask) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+                   bar),
+               "h"(mask)
                : "memory");
 }
 // 32 consecutive fp32 columns of this thread's tensor-memory lane
@@ -317,7 +346,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ 
     for (int s = 0; s < S; ++s) {
       mbar_init(full0 + 8u * s, 1);
       mbar_init(conv0 + 8u * s, 128);
-      mbar_init(empty0 + 8u * s, 1);
+      mbar_init(empty0 + 8u * s, static_cast<uint32_t>(p.csize));   // one MMA release per cluster CTA
     }
     mbar_init(accf, 1);
     mbar_init(acce, 128);
@@ -344,11 +373,15 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ 
   }
   tc_fence_before();
   __syncthreads();
+  if (p.csize > 1) cluster_sync();   // peers' barriers are initialised before any multicast
   tc_fence_after();
   const uint32_t tmem = ctl->tmem_base;
 
-  const long long u_begin = unit_begin(blockIdx.x, p.units, p.ctas);
-  const long long u_end = unit_begin(blockIdx.x + 1, p.units, p.ctas);
+  const int crank = p.csize > 1 ? static_cast<int>(cluster_rank()) : 0;
+  const int cl = static_cast<int>(blockIdx.x) / p.csize;
+  const uint16_t cmask = static_cast<uint16_t>((1u << p.csize) - 1u);
+  const long long u_begin = unit_begin(cl, p.units, p.ncl);
+  const long long u_end = unit_begin(cl + 1, p.units, p.ncl);
 
   if (warp == 0) {
     if (lane == 0) {
@@ -361,8 +394,9 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ 
         const int t = static_cast<int>(u / p.kbtot);
         const int kb0 = static_cast<int>(u - static_cast<long long>(t) * p.kbtot);
         const int kbe = static_cast<int>(min(static_cast<long long>(p.kbtot), kb0 + (u_end - u)));
-        const int mt = t / p.nchunks;
-        const int nc = t - mt * p.nchunks;
+        const int grp = t / p.nchunks;
+        const int nc = t - grp * p.nchunks;
+        const int mt = grp * p.csize + crank;
         for (int kb = kb0; kb < kbe; ++kb) {
           if (!wait_bounded(empty0 + 8u * stage, phase ^ 1u, ctl, p.err, 1)) {
             ok = false;
@@ -376,11 +410,19 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ 
           const bool seg1 = kb < p.kb1;
           const int kx = (seg1 ? kb : kb - p.kb1) * kBK;   // fp32 column of the hi operands
           tma_load_2d(xs, seg1 ? &mX1 : &mX2, kx, mt * kBM, fb);
-          for (int i = 0; i < p.nloads; ++i) {
-            const int ny = nc * p.NC + i * p.nbox;
-            const uint32_t off = static_cast<uint32_t>(i * p.nbox * kRowBytes);
-            tma_load_2d(yh + off, seg1 ? &mY1h : &mY2h, kx, ny, fb);
-            tma_load_2d(yc + off, seg1 ? &mY1c : &mY2c, 2 * kx, ny, fb);   // bf16 column
+          // this CTA's slice of the N-side tile; with a cluster it is multicast
+          // to every CTA of the cluster, which all load the other slices
+          for (int i = 0; i < p.nb; ++i) {
+            const int ro = crank * p.sl + i * p.nbox;
+            const int ny = nc * p.NC + ro;
+            const uint32_t off = static_cast<uint32_t>(ro * kRowBytes);
+            if (p.csize > 1) {
+              tma_load_2d_mc(yh + off, seg1 ? &mY1h : &mY2h, kx, ny, fb, cmask);
+              tma_load_2d_mc(yc + off, seg1 ? &mY1c : &mY2c, 2 * kx, ny, fb, cmask);   // bf16 column
+            } else {
+              tma_load_2d(yh + off, seg1 ? &mY1h : &mY2h, kx, ny, fb);
+              tma_load_2d(yc + off, seg1 ? &mY1c : &mY2c, 2 * kx, ny, fb);
+            }
           }
           ++issued;
           if (++stage == S) {
@@ -452,7 +494,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ 
               mma_tf32(tmem + 256u, ah, bh, id1, 1u);
             }
           }
-          mma_commit(empty0 + 8u * stage);
+          if (p.csize > 1) mma_commit_mc(empty0 + 8u * stage, cmask);
+          else mma_commit(empty0 + 8u * stage);
           if (++stage == S) {
             stage = 0;
             phase ^= 1u;
@@ -486,8 +529,10 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ 
       const int t = static_cast<int>(u / p.kbtot);
       const int kb0 = static_cast<int>(u - static_cast<long long>(t) * p.kbtot);
       const int kbe = static_cast<int>(min(static_cast<long long>(p.kbtot), kb0 + (u_end - u)));
-      const int mt = t / p.nchunks;
-      const int nc = t - mt * p.nchunks;
+      const int grp = t / p.nchunks;
+      const int nc = t - grp * p.nchunks;
+      const int mt = grp * p.csize + crank;
+      const size_t tm = static_cast<size_t>(mt) * p.nchunks + nc;   // (M tile, N chunk) of this CTA's partials
       float n0 = 0.0f;  // sum of W0_i^2 over this segment's K range
       for (int kb = kb0; kb < kbe; ++kb) {
         // every lane waits; the decision to go on is taken warp-wide so that
@@ -547,7 +592,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ 
       tc_fence_after();
       const int grow = mt * kBM + row;
       const bool valid = grow < p.M;
-      const int seg = static_cast<int>(blockIdx.x) - cta_of(static_cast<long long>(t) * p.kbtot, p.units, p.ctas);
+      const int seg = cl - cta_of(static_cast<long long>(t) * p.kbtot, p.units, p.ncl);
       if (p.mode == kNorm) {
         // <B_i, D_i>: the warp's 32 rows of B arrive as 32 x 32 boxes by TMA,
         // two in flight; lane i reads row i (128-byte swizzle: chunk q at q ^ (i & 7))
@@ -602,11 +647,11 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ 
           break;
         }
         if (valid) {
-          float2 *dst = reinterpret_cast<float2 *>(p.part) + (static_cast<size_t>(t) * p.maxseg + seg) * kBM + row;
+          float2 *dst = reinterpret_cast<float2 *>(p.part) + (tm * p.maxseg + seg) * kBM + row;
           *dst = make_float2(n0, dot);
         }
       } else {
-        float *dst = p.part + ((static_cast<size_t>(t) * p.maxseg + seg) * kBM + row) * p.NC;
+        float *dst = p.part + ((tm * p.maxseg + seg) * kBM + row) * p.NC;
         for (int c = 0; c < p.NC; c += 32) {
           float v[32];
           tmem_ld32(lane_addr + static_cast<uint32_t>(c), v);
@@ -627,6 +672,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ 
 
   tc_fence_before();
   __syncthreads();
+  // no CTA leaves while a peer may still multicast into it or arrive on its barriers
+  if (p.csize > 1) cluster_sync();
   tc_fence_after();
   if (warp == 1) {
     __syncwarp();
@@ -678,9 +725,13 @@ __global__ void __launch_bounds__(256) pad_cols_kernel(const float *__restrict__
   }
 }
 
+// how partial results were laid out by tc_gemm_kernel: tile tg = (M-tile group,
+// N chunk) is covered by clusters cta_of(tg*kbtot) .. cta_of((tg+1)*kbtot - 1);
+// the partial of M tile mt, chunk nc, from the j-th of those clusters, is
+// entry (mt*nchunks + nc)*maxseg + j
 struct StreamK {
   long long units;
-  int ctas, kbtot, maxseg;
+  int ncl, kbtot, maxseg, csize;
 };
 
 // Gs[k][l] = (s/2) * G[k][l] for k, l < r (zero-padded to npad), split like
@@ -696,12 +747,13 @@ __global__ void __launch_bounds__(256) gram_reduce_kernel(const float *__restric
     if (k < r && l < r) {
       const int mt = k / kBM, row = k - mt * kBM;
       const int nc = l / NC, col = l - nc * NC;
-      const int t = mt * nchunks + nc;
-      const long long ub = static_cast<long long>(t) * sk.kbtot;
-      const int c0 = cta_of(ub, sk.units, sk.ctas);
-      const int c1 = cta_of(ub + sk.kbtot - 1, sk.units, sk.ctas);
+      const int tg = (mt / sk.csize) * nchunks + nc;
+      const size_t tm = static_cast<size_t>(mt) * nchunks + nc;
+      const long long ub = static_cast<long long>(tg) * sk.kbtot;
+      const int c0 = cta_of(ub, sk.units, sk.ncl);
+      const int c1 = cta_of(ub + sk.kbtot - 1, sk.units, sk.ncl);
       float sum = 0.0f;
-      for (int j = 0; j <= c1 - c0; ++j) sum += part[((static_cast<size_t>(t) * sk.maxseg + j) * kBM + row) * NC + col];
+      for (int j = 0; j <= c1 - c0; ++j) sum += part[((tm * sk.maxseg + j) * kBM + row) * NC + col];
       v = half_s * sum;
     }
     const float h = __uint_as_float(tf32_rna(v));
@@ -721,12 +773,13 @@ __global__ void __launch_bounds__(256) norm_finalize_kernel(const float2 *__rest
   const int mt = i / kBM, row = i - mt * kBM;
   float n0 = 0.0f, dot = 0.0f;
   for (int nc = 0; nc < nchunks; ++nc) {
-    const int t = mt * nchunks + nc;
-    const long long ub = static_cast<long long>(t) * sk.kbtot;
-    const int c0 = cta_of(ub, sk.units, sk.ctas);
-    const int c1 = cta_of(ub + sk.kbtot - 1, sk.units, sk.ctas);
+    const int tg = (mt / sk.csize) * nchunks + nc;
+    const size_t tm = static_cast<size_t>(mt) * nchunks + nc;
+    const long long ub = static_cast<long long>(tg) * sk.kbtot;
+    const int c0 = cta_of(ub, sk.units, sk.ncl);
+    const int c1 = cta_of(ub + sk.kbtot - 1, sk.units, sk.ncl);
     for (int j = 0; j <= c1 - c0; ++j) {
-      const float2 v = part[(static_cast<size_t>(t) * sk.maxseg + j) * kBM + row];
+      const float2 v = part[(tm * sk.maxseg + j) * kBM + row];
       if (nc == 0) n0 += v.x;
       dot += v.y;
     }
@@ -759,18 +812,24 @@ void plan_n(int r, int *npad, int *nchunks, int *NC) {
   *NC = static_cast<int>(dora::round_up(dora::ceil_div(*npad, *nchunks), 16));
 }
 
-bool plan_gemm(int mode, int M, int kb1, int kb2, int r, int sms, GemmPlan *gp) {
+// csize CTAs per cluster, at most max_clusters clusters
+bool plan_gemm(int mode, int M, int kb1, int kb2, int r, int csize, int max_clusters, GemmPlan *gp) {
   TcParams &p = gp->p;
   std::memset(&p, 0, sizeof(p));
   p.mode = mode;
   p.M = M;
   p.kb1 = kb1;
   p.kbtot = kb1 + kb2;
+  p.csize = csize;
   int npad;
   plan_n(r, &npad, &p.nchunks, &p.NC);
-  p.nbox = p.NC <= 128 ? p.NC : 128;
-  p.nloads = static_cast<int>(dora::ceil_div(p.NC, p.nbox));
-  p.NT = p.nloads * p.nbox;
+  // N-side slices: each CTA of a cluster loads sl rows (a multiple of 8, so
+  // every slice starts on a swizzle-pattern boundary) in nb boxes of nbox rows
+  const int sl = static_cast<int>(dora::round_up(dora::ceil_div(p.NC, csize), 8));
+  p.nb = static_cast<int>(dora::ceil_div(sl, 128));
+  p.nbox = static_cast<int>(dora::round_up(dora::ceil_div(sl, p.nb), 8));
+  p.sl = p.nb * p.nbox;
+  p.NT = csize * p.sl;
   p.nmma0 = p.NC <= 256 ? p.NC : 256;
   p.nmma1 = p.NC - p.nmma0;
   int cols = 32;
@@ -783,17 +842,19 @@ bool plan_gemm(int mode, int M, int kb1, int kb2, int r, int sms, GemmPlan *gp) 
   if (p.stages > kMaxStages) p.stages = kMaxStages;
   if (p.stages < 2) return false;
   const int mtiles = static_cast<int>(dora::ceil_div(M, kBM));
-  p.tiles = mtiles * p.nchunks;
+  const int ngroups = static_cast<int>(dora::ceil_div(mtiles, csize));
+  p.tiles = ngroups * p.nchunks;
   p.units = static_cast<long long>(p.tiles) * p.kbtot;
   const int min_units = mode == kGram ? kMinUnitsGram : kMinUnitsNorm;
-  long long ctas = dora::ceil_div(p.units, min_units);
-  if (ctas > sms) ctas = sms;
-  if (ctas < 1) ctas = 1;
-  p.ctas = static_cast<int>(ctas);
-  p.maxseg = seg_bound(p.units, p.ctas, p.kbtot);
+  long long ncl = dora::ceil_div(p.units, min_units);
+  if (ncl > max_clusters) ncl = max_clusters;
+  if (ncl < 1) ncl = 1;
+  p.ncl = static_cast<int>(ncl);
+  p.ctas = p.ncl * csize;
+  p.maxseg = seg_bound(p.units, p.ncl, p.kbtot);
   p.r = r;
   const size_t per_row = mode == kGram ? static_cast<size_t>(p.NC) : 2;
-  gp->part_bytes = static_cast<size_t>(p.tiles) * p.maxseg * kBM * per_row * sizeof(float);
+  gp->part_bytes = static_cast<size_t>(ngroups) * csize * p.nchunks * p.maxseg * kBM * per_row * sizeof(float);
   gp->smem_bytes = static_cast<size_t>(p.stages) * p.stage_bytes + epi + 1024 /*align*/ + 8 * (3 * p.stages + 3 + 8) + 64;
   // tensor memory: a CTA holding 512 columns must be alone on its SM
   if (p.tmem_cols > 256 && gp->smem_bytes < 116 * 1024) gp->smem_bytes = 116 * 1024;
@@ -806,11 +867,13 @@ struct Layout {
 
 size_t al256(size_t x) { return (x + 255) & ~size_t(255); }
 
-bool plan_layout(int64_t out, int64_t in, int64_t r, int sms, GemmPlan *gg, GemmPlan *gn, Layout *L) {
+// sms: CTAs available to the Gram pass; csize / max_clusters: cluster shape of the norm pass
+bool plan_layout(int64_t out, int64_t in, int64_t r, int sms, int csize, int max_clusters, GemmPlan *gg,
+                 GemmPlan *gn, Layout *L) {
   const int kb1 = static_cast<int>(dora::ceil_div(in, kBK));
   const int kb2 = static_cast<int>(dora::ceil_div(r, kBK));
-  if (!plan_gemm(kGram, static_cast<int>(r), kb1, 0, static_cast<int>(r), sms, gg)) return false;
-  if (!plan_gemm(kNorm, static_cast<int>(out), kb1, kb2, static_cast<int>(r), sms, gn)) return false;
+  if (!plan_gemm(kGram, static_cast<int>(r), kb1, 0, static_cast<int>(r), 1, sms, gg)) return false;
+  if (!plan_gemm(kNorm, static_cast<int>(out), kb1, kb2, static_cast<int>(r), csize, max_clusters, gn)) return false;
   int npad, nchunks, NC;
   plan_n(static_cast<int>(r), &npad, &nchunks, &NC);
   size_t off = 0;
@@ -879,14 +942,97 @@ int grid_for(long long n, int sms) {
   return static_cast<int>(b);
 }
 
+cudaError_t launch_gemm(const GemmPlan &gp, cudaStream_t cs, const CUtensorMap &x1, const CUtensorMap &x2,
+                        const CUtensorMap &y1h, const CUtensorMap &y1c, const CUtensorMap &y2h,
+                        const CUtensorMap &y2c, const CUtensorMap &be) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(gp.p.ctas));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = gp.smem_bytes;
+  cfg.stream = cs;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(gp.p.csize);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, tc_gemm_kernel, x1, x2, y1h, y1c, y2h, y2c, be, gp.p);
+}
+
+// Cluster shape of the norm pass.  Sharing the N-side tile pays only when it
+// is large (a full 384-wide chunk: 48 KB per K block); then take the largest
+// cluster (up to kMaxCluster) whose co-resident clusters still cover all but a
+// few SMs.  Otherwise single CTAs.  Occupancy answers are cached per device and
+// shared-memory size.
+void choose_cluster(int device, int sms, int64_t out, int64_t in, int64_t r, int *csize, int *max_clusters) {
+  static std::mutex mu;
+  struct Entry {
+    int device, c;
+    size_t smem;
+    int active;
+  };
+  static Entry cache[64];
+  static int ncache = 0;
+  *csize = 1;
+  *max_clusters = sms;
+  int npad, nchunks, NC;
+  plan_n(static_cast<int>(r), &npad, &nchunks, &NC);
+  if (NC < kMaxChunkN) return;
+  const int kb1 = static_cast<int>(dora::ceil_div(in, kBK));
+  const int kb2 = static_cast<int>(dora::ceil_div(r, kBK));
+  for (int c = kMaxCluster; c >= 2; c /= 2) {
+    GemmPlan gp;
+    if (!plan_gemm(kNorm, static_cast<int>(out), kb1, kb2, static_cast<int>(r), c, sms / c, &gp)) continue;
+    int active = -1;
+    {
+      std::lock_guard<std::mutex> lock(mu);
+      for (int i = 0; i < ncache; ++i)
+        if (cache[i].device == device && cache[i].c == c && cache[i].smem == gp.smem_bytes) active = cache[i].active;
+    }
+    if (active < 0) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(static_cast<unsigned>((sms / c) * c));
+      cfg.blockDim = dim3(kThreads);
+      cfg.dynamicSmemBytes = gp.smem_bytes;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = static_cast<unsigned>(c);
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, tc_gemm_kernel, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        n = 0;
+      }
+      active = n;
+      std::lock_guard<std::mutex> lock(mu);
+      if (ncache < 64) cache[ncache++] = Entry{device, c, gp.smem_bytes, n};
+    }
+    if (active * c >= sms - 8 && active >= 1) {
+      *csize = c;
+      *max_clusters = active;
+      return;
+    }
+  }
+}
+
 }  // namespace
 
 extern "C" size_t dora_norm_factored_workspace(int64_t out, int64_t in, int64_t r) {
   if (!shape_ok(out, in, r)) return 0;
-  GemmPlan gg, gn;
-  Layout L;
-  if (!plan_layout(out > 0 ? out : 1, in, r, kMaxCtas, &gg, &gn, &L)) return 0;
-  return L.total;
+  // the largest layout over every cluster shape the norm pass may pick on any
+  // device with up to kMaxCtas SMs
+  size_t total = 0;
+  for (int c = 1; c <= kMaxCluster; c *= 2) {
+    GemmPlan gg, gn;
+    Layout L;
+    if (!plan_layout(out > 0 ? out : 1, in, r, kMaxCtas, c, kMaxCtas / c, &gg, &gn, &L)) return 0;
+    if (L.total > total) total = L.total;
+  }
+  return total;
 }
 
 extern "C" dora_status dora_device_error(int *code) {
@@ -921,21 +1067,6 @@ extern "C" dora_status dora_norm_factored(const float *W0, const float *A, const
   if (st != DORA_OK) return st;
   const int sms = info.sms < kMaxCtas ? info.sms : kMaxCtas;
 
-  GemmPlan gg, gn;
-  Layout L;
-  if (!plan_layout(out, in, r, sms, &gg, &gn, &L)) return DORA_ERR_SHAPE;
-  uint8_t *ws = static_cast<uint8_t *>(workspace);
-  float *a_hi = reinterpret_cast<float *>(ws + L.a_hi);
-  __nv_bfloat16 *a_c = reinterpret_cast<__nv_bfloat16 *>(ws + L.a_c);
-  float *g_hi = reinterpret_cast<float *>(ws + L.g_hi);
-  __nv_bfloat16 *g_c = reinterpret_cast<__nv_bfloat16 *>(ws + L.g_c);
-  float *part_g = reinterpret_cast<float *>(ws + L.part_g);
-  float *part_n = reinterpret_cast<float *>(ws + L.part_n);
-  const float *Bk = B;
-  int64_t ldb = r;
-  int npad, nchunks, NC;
-  plan_n(static_cast<int>(r), &npad, &nchunks, &NC);
-
   // device error word, passed to the kernels by address
   static std::mutex err_mu;
   static int *err_ptr[64] = {};
@@ -954,6 +1085,23 @@ extern "C" dora_status dora_norm_factored(const float *W0, const float *A, const
     errp = err_ptr[device];
   }
 
+  int csize = 1, max_clusters = sms;
+  choose_cluster(device, sms, out, in, r, &csize, &max_clusters);
+  GemmPlan gg, gn;
+  Layout L;
+  if (!plan_layout(out, in, r, sms, csize, max_clusters, &gg, &gn, &L)) return DORA_ERR_SHAPE;
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  float *a_hi = reinterpret_cast<float *>(ws + L.a_hi);
+  __nv_bfloat16 *a_c = reinterpret_cast<__nv_bfloat16 *>(ws + L.a_c);
+  float *g_hi = reinterpret_cast<float *>(ws + L.g_hi);
+  __nv_bfloat16 *g_c = reinterpret_cast<__nv_bfloat16 *>(ws + L.g_c);
+  float *part_g = reinterpret_cast<float *>(ws + L.part_g);
+  float *part_n = reinterpret_cast<float *>(ws + L.part_n);
+  const float *Bk = B;
+  int64_t ldb = r;
+  int npad, nchunks, NC;
+  plan_n(static_cast<int>(r), &npad, &nchunks, &NC);
+
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   uint64_t launches = 0;
 
@@ -971,9 +1119,12 @@ extern "C" dora_status dora_norm_factored(const float *W0, const float *A, const
   }
 
   // tensor maps
-  CUtensorMap mA, mAh_n, mAc_n, mW0, mB, mGh, mGc, mBe;
+  // the N-side boxes of the two passes may differ in height: one map set each
+  CUtensorMap mA, mAh_g, mAc_g, mAh_n, mAc_n, mW0, mB, mGh, mGc, mBe;
   const int nbox = gn.p.nbox;
   bool ok = make_map(&mA, A, false, r, in, in, kBM) && make_map(&mAh_n, a_hi, false, r, in, in, nbox) &&
+            make_map(&mAh_g, a_hi, false, r, in, in, gg.p.nbox) &&
+            make_map(&mAc_g, a_c, true, r, 2 * in8, 2 * in8, gg.p.nbox) &&
             make_map(&mAc_n, a_c, true, r, 2 * in8, 2 * in8, nbox) && make_map(&mW0, W0, false, out, in, in, kBM) &&
             make_map(&mB, Bk, false, out, ldb, ldb, kBM) && make_map(&mGh, g_hi, false, npad, npad, npad, nbox) &&
             make_map(&mGc, g_c, true, npad, 2 * npad, 2 * npad, nbox) &&
@@ -986,11 +1137,14 @@ extern "C" dora_status dora_norm_factored(const float *W0, const float *A, const
   // 2. Gram partial tiles
   gg.p.part = part_g;
   gg.p.err = errp;
-  tc_gemm_kernel<<<gg.p.ctas, kThreads, gg.smem_bytes, cs>>>(mA, mA, mAh_n, mAc_n, mAh_n, mAc_n, mA, gg.p);
+  if (launch_gemm(gg, cs, mA, mA, mAh_g, mAc_g, mAh_g, mAc_g, mA) != cudaSuccess) {
+    dora::count_launches(launches);
+    return DORA_ERR_CUDA;
+  }
   ++launches;
 
   // 3. Gs = (s/2) G, split like A
-  StreamK skg{gg.p.units, gg.p.ctas, gg.p.kbtot, gg.p.maxseg};
+  StreamK skg{gg.p.units, gg.p.ncl, gg.p.kbtot, gg.p.maxseg, gg.p.csize};
   gram_reduce_kernel<<<grid_for(static_cast<long long>(npad) * npad, sms), 256, 0, cs>>>(
       part_g, skg, gg.p.nchunks, gg.p.NC, static_cast<int>(r), npad, 0.5f * s, g_hi, g_c);
   ++launches;
@@ -998,11 +1152,14 @@ extern "C" dora_status dora_norm_factored(const float *W0, const float *A, const
   // 4. [W0 | B] x [A | Gs]^T with per-segment row reductions
   gn.p.part = part_n;
   gn.p.err = errp;
-  tc_gemm_kernel<<<gn.p.ctas, kThreads, gn.smem_bytes, cs>>>(mW0, mB, mAh_n, mAc_n, mGh, mGc, mBe, gn.p);
+  if (launch_gemm(gn, cs, mW0, mB, mAh_n, mAc_n, mGh, mGc, mBe) != cudaSuccess) {
+    dora::count_launches(launches);
+    return DORA_ERR_CUDA;
+  }
   ++launches;
 
   // 5. n and g
-  StreamK skn{gn.p.units, gn.p.ctas, gn.p.kbtot, gn.p.maxseg};
+  StreamK skn{gn.p.units, gn.p.ncl, gn.p.kbtot, gn.p.maxseg, gn.p.csize};
   norm_finalize_kernel<<<static_cast<unsigned>(dora::ceil_div(out, 256)), 256, 0, cs>>>(
       reinterpret_cast<const float2 *>(part_n), skn, gn.p.nchunks, static_cast<int>(out), m, 2.0f * s, norm, g);
   ++launches;

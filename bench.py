@@ -39,6 +39,10 @@ METRIC = "fused DoRA compose fwd+bwd HBM GB/s (% of GB300 peak); factored-norm Â
 WORKLOAD = "high_rank"
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
+# DRAM read + write bytes of one compose_bwd_kernel launch on this workload,
+# from the ncu capture summarised in profiles/compose_fwd_bwd_high_rank.md;
+# set to None whenever that kernel changes until it is captured again
+COMPOSE_BWD_TRAFFIC_BYTES = 755031552 + 460042496
 
 
 def algorithmic(sh) -> dict:
@@ -50,17 +54,19 @@ def algorithmic(sh) -> dict:
         "fwd_bytes": 3 * T * out * e + 4 * out,                # base, lora -> y ; g
         "bwd_bytes": 5 * T * out * e + 3 * 4 * out,            # dy, base, lora -> d_base, d_lora ; g, n, d_mag
         "norm_bytes": 4 * (out * inp + r * inp + out * r + 3 * out),
-        "norm_flops": 2 * out * inp * r + 2 * r * r * inp + 2 * out * r * r,
+        "norm_flops": 2 * out * (inp + r) * r + 2 * r * r * inp,     # norm pass + Gram pass
     }
 
 
 def peaks() -> dict:
-    p = {"hbm_gbs": FALLBACK_HBM_GBS, "bf16_tflops": FALLBACK_BF16_TFLOPS, "source": "fallback"}
+    p = {"hbm_gbs": FALLBACK_HBM_GBS, "bf16_tflops": FALLBACK_BF16_TFLOPS, "tf32_tflops": 1700.0 / 2,
+         "source": "fallback"}
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
             m = json.load(f)
         p = {"hbm_gbs": float(m["hbm_gbs"]), "bf16_tflops": float(m["bf16_tflops"]),
              "bf16_tflops_sustained": float(m.get("bf16_tflops_sustained", m["bf16_tflops"])), "source": "measured"}
+        p["tf32_tflops"] = p["bf16_tflops_sustained"] / 2
     except Exception:
         pass
     return p
@@ -83,7 +89,7 @@ class ClockSampler:
             os.close(fd)
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
             time.sleep(0.3)
         except Exception:
             self.proc = None
@@ -168,7 +174,10 @@ def run_reference(args, rank, world):
         return
     sh = wl.shape(WORKLOAD)
     d = wl.make_module(sh, wl.seed_for(WORKLOAD))
-    tokens, rows = 768, 256
+    # per-step sample sized so that warm-up + steps stay within about two minutes
+    n = max(1, args.steps + args.warmup)
+    tokens = int(min(768, max(32, 768 * 40 // n)))
+    rows = int(min(256, max(16, 256 * 40 // n)))
     for _ in range(args.warmup):
         oracle_sample(sh, d, tokens, rows)
     times, vals, norm_us = [], [], []
@@ -310,6 +319,7 @@ def run_ours(args, rank, world, local_rank):
             for k, v in host_out.items():
                 v.copy_(dev_out[k], non_blocking=True)
 
+        e2e_steps = min(args.steps, args.e2e_steps)
         for _ in range(max(1, args.warmup)):
             e2e_step()
         torch.cuda.synchronize()
@@ -317,18 +327,18 @@ def run_ours(args, rank, world, local_rank):
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
         a.record(stream)
-        for _ in range(args.steps):
+        for _ in range(e2e_steps):
             e2e_step()
         b.record(stream)
         torch.cuda.synchronize()
         barrier()
-        e2e_ms = a.elapsed_time(b) / args.steps
+        e2e_ms = a.elapsed_time(b) / e2e_steps
         if dist is not None:
             t = torch.tensor([e2e_ms], device=dev)
             dist.all_reduce(t, op=dist.ReduceOp.MAX)
             e2e_ms = t.item()
         e2e = {"value": world * compose_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "steps": e2e_steps}
 
     if rank != 0:
         if dist is not None:
@@ -351,11 +361,19 @@ def run_ours(args, rank, world, local_rank):
         "norm_us_per_module": norm_us,
         "breakdown": {"norm_us": norm_us, "fwd_us": fwd_ms * 1e3, "bwd_us": bwd_ms * 1e3,
                       "fwd_gbs": fwd_gbs, "bwd_gbs": bwd_gbs,
-                      "norm_tflops_algorithmic": alg["norm_flops"] / (norm_ms * 1e-3) / 1e12,
-                      "norm_tflops_issued_3xtf32": 3 * alg["norm_flops"] / (norm_ms * 1e-3) / 1e12},
+                      "norm_tflops_algorithmic": alg["norm_flops"] / (norm_ms * 1e-3) / 1e12},
         "roofline": {"bound": "hbm", "kernel": "compose_bwd", "achieved": bwd_gbs, "peak": pk["hbm_gbs"],
-                     "unit": "GB/s", "frac": bwd_gbs / pk["hbm_gbs"], "traffic": None,
-                     "peak_source": pk["source"]},
+                     "unit": "GB/s", "frac": bwd_gbs / pk["hbm_gbs"],
+                     "traffic": COMPOSE_BWD_TRAFFIC_BYTES,
+                     "algorithmic_bytes": alg["bwd_bytes"], "peak_source": pk["source"] + " (copy bandwidth)"},
+        "roofline_norm": {"bound": "tensor", "kernel": "factored norm (all five launches)",
+                          "achieved": 2 * alg["norm_flops"] / (norm_ms * 1e-3) / 1e12,
+                          "peak": pk["tf32_tflops"], "unit": "TFLOP/s",
+                          "frac": 2 * alg["norm_flops"] / (norm_ms * 1e-3) / 1e12 / pk["tf32_tflops"],
+                          "note": "achieved = TF32-equivalent issued work (one TF32 product + one bf16 product "
+                                  "of twice the K = 2x the algorithmic flops) / norm time; peak = measured "
+                                  "sustained bf16 x 1/2 (TF32:bf16 nominal dense ratio)",
+                          "algorithmic_tflops": alg["norm_flops"] / (norm_ms * 1e-3) / 1e12},
         "gpu_launches": launches,
         "clocks": clk,
     }
@@ -371,8 +389,9 @@ def run_ours(args, rank, world, local_rank):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -91,6 +91,7 @@ struct TcParams {
   int kb1;          // K blocks in segment 1 (W0 or A columns)
   int kbtot;        // K blocks in total (segment 2 = B / Gs columns)
   int nchunks;      // N chunks per M tile
+  int sym;          // Gram pass: only tiles with N chunk >= M tile (G is symmetric; both 128 wide)
   int NC;           // N per chunk (multiple of 16, <= kMaxChunkN)
   int csize;        // CTAs per cluster: they take consecutive M tiles over the same K range
   int sl;           // N-side rows each CTA of a cluster loads (and multicasts to the cluster)
@@ -289,6 +290,30 @@ __host__ __device__ __forceinline__ int cta_of(long long u, long long units, int
   return static_cast<int>(c);
 }
 
+// (M tile, N chunk) of work tile t.  Gram pass: the upper-triangular tiles
+// (nc >= mt) of a q x q grid, row by row.  Norm pass: M-tile group t / nchunks
+// (csize consecutive M tiles, one per cluster rank), N chunk t % nchunks.
+__host__ __device__ __forceinline__ void tile_coords(int t, int nchunks, int sym, int csize, int crank, int *mt,
+                                                     int *nc) {
+  if (sym) {
+    int i = 0;
+    while (t >= nchunks - i) {
+      t -= nchunks - i;
+      ++i;
+    }
+    *mt = i;
+    *nc = i + t;
+  } else {
+    const int grp = t / nchunks;
+    *nc = t - grp * nchunks;
+    *mt = grp * csize + crank;
+  }
+}
+// inverse for the upper-triangular Gram tiles (mt <= nc)
+__host__ __device__ __forceinline__ int sym_tile_index(int mt, int nc, int q) {
+  return mt * q - (mt * (mt - 1)) / 2 + (nc - mt);
+}
+
 struct SharedCtl {
   volatile int abort;
   uint32_t tmem_base;
@@ -394,9 +419,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ 
         const int t = static_cast<int>(u / p.kbtot);
         const int kb0 = static_cast<int>(u - static_cast<long long>(t) * p.kbtot);
         const int kbe = static_cast<int>(min(static_cast<long long>(p.kbtot), kb0 + (u_end - u)));
-        const int grp = t / p.nchunks;
-        const int nc = t - grp * p.nchunks;
-        const int mt = grp * p.csize + crank;
+        int mt, nc;
+        tile_coords(t, p.nchunks, p.sym, p.csize, crank, &mt, &nc);
         for (int kb = kb0; kb < kbe; ++kb) {
           if (!wait_bounded(empty0 + 8u * stage, phase ^ 1u, ctl, p.err, 1)) {
             ok = false;
@@ -529,9 +553,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ 
       const int t = static_cast<int>(u / p.kbtot);
       const int kb0 = static_cast<int>(u - static_cast<long long>(t) * p.kbtot);
       const int kbe = static_cast<int>(min(static_cast<long long>(p.kbtot), kb0 + (u_end - u)));
-      const int grp = t / p.nchunks;
-      const int nc = t - grp * p.nchunks;
-      const int mt = grp * p.csize + crank;
+      int mt, nc;
+      tile_coords(t, p.nchunks, p.sym, p.csize, crank, &mt, &nc);
       const size_t tm = static_cast<size_t>(mt) * p.nchunks + nc;   // (M tile, N chunk) of this CTA's partials
       float n0 = 0.0f;  // sum of W0_i^2 over this segment's K range
       for (int kb = kb0; kb < kbe; ++kb) {
@@ -745,9 +768,13 @@ __global__ void __launch_bounds__(256) gram_reduce_kernel(const float *__restric
     const int l = static_cast<int>(i - static_cast<long long>(k) * npad);
     float v = 0.0f;
     if (k < r && l < r) {
-      const int mt = k / kBM, row = k - mt * kBM;
-      const int nc = l / NC, col = l - nc * NC;
-      const int tg = (mt / sk.csize) * nchunks + nc;
+      // G is symmetric and only the tiles with N chunk >= M tile were formed:
+      // read G[l][k] from its transposed position when (k, l) falls below
+      const int kk = (l / NC < k / kBM) ? l : k;
+      const int ll = (l / NC < k / kBM) ? k : l;
+      const int mt = kk / kBM, row = kk - mt * kBM;
+      const int nc = ll / NC, col = ll - nc * NC;
+      const int tg = sym_tile_index(mt, nc, nchunks);
       const size_t tm = static_cast<size_t>(mt) * nchunks + nc;
       const long long ub = static_cast<long long>(tg) * sk.kbtot;
       const int c0 = cta_of(ub, sk.units, sk.ncl);
@@ -823,6 +850,12 @@ bool plan_gemm(int mode, int M, int kb1, int kb2, int r, int csize, int max_clus
   p.csize = csize;
   int npad;
   plan_n(r, &npad, &p.nchunks, &p.NC);
+  if (mode == kGram) {
+    // G = A A^T: square 128 x 128 tiles, upper triangle only (M tiles = N chunks)
+    p.NC = npad < kBM ? npad : kBM;
+    p.nchunks = static_cast<int>(dora::ceil_div(npad, p.NC));
+    p.sym = 1;
+  }
   // N-side slices: each CTA of a cluster loads sl rows (a multiple of 8, so
   // every slice starts on a swizzle-pattern boundary) in nb boxes of nbox rows
   const int sl = static_cast<int>(dora::round_up(dora::ceil_div(p.NC, csize), 8));
@@ -843,7 +876,7 @@ bool plan_gemm(int mode, int M, int kb1, int kb2, int r, int csize, int max_clus
   if (p.stages < 2) return false;
   const int mtiles = static_cast<int>(dora::ceil_div(M, kBM));
   const int ngroups = static_cast<int>(dora::ceil_div(mtiles, csize));
-  p.tiles = ngroups * p.nchunks;
+  p.tiles = p.sym ? p.nchunks * (p.nchunks + 1) / 2 : ngroups * p.nchunks;
   p.units = static_cast<long long>(p.tiles) * p.kbtot;
   const int min_units = mode == kGram ? kMinUnitsGram : kMinUnitsNorm;
   long long ncl = dora::ceil_div(p.units, min_units);

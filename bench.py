@@ -386,6 +386,124 @@ def run_ours(args, rank, world, local_rank):
         dist.destroy_process_group()
 
 
+# ---------------------------------------------------------------------------
+# reports for the other workloads (one JSON line each; not the bench line)
+# ---------------------------------------------------------------------------
+def _time_ms(fn, reps, stream):
+    import torch
+    for _ in range(3):
+        fn()
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(reps):
+        fn()
+    b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / reps
+
+
+def _device_module(sh, seed, dev):
+    """Seeded inputs drawn on the device (torch Philox), same distributions as
+    parameter_efficient_fine_gb300.workloads: fast enough for 64-module stacks."""
+    import torch
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(seed)
+    W0 = torch.randn(sh.out, sh.inp, device=dev, generator=gen) / math.sqrt(sh.inp)
+    A = torch.randn(sh.r, sh.inp, device=dev, generator=gen) / math.sqrt(sh.inp)
+    B = torch.randn(sh.out, sh.r, device=dev, generator=gen) * sh.sigma_B
+    m = W0.double().norm(dim=1).float() * (1 + sh.sigma_m * torch.randn(sh.out, device=dev, generator=gen))
+    return W0, A, B, m
+
+
+def run_report(args):
+    import torch
+    import parameter_efficient_fine_gb300 as dora
+    from parameter_efficient_fine_gb300 import build as dbuild
+
+    dbuild.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    if args.report == "rank_sweep":
+        # out = in = 8192, T = 8192 bf16: norm time, compose GB/s and the norm's
+        # whole transient (its workspace) against one dense fp32 out x in matrix
+        for k, r in enumerate(wl.RANK_SWEEP):
+            sh = wl.shape("rank_sweep", r=r)
+            W0, A, B, m = _device_module(sh, wl.seed_for("rank_sweep", k), dev)
+            gen = torch.Generator(device=dev)
+            gen.manual_seed(wl.seed_for("rank_sweep", k) + 7)
+            act = [torch.randn(sh.T, sh.out, device=dev, generator=gen).bfloat16() for _ in range(3)]
+            act[1] = (act[1].float() * math.sqrt(sh.r) * sh.sigma_B).bfloat16()
+            base, lora, dy = act
+            norm = torch.empty(sh.out, device=dev)
+            g = torch.empty(sh.out, device=dev)
+            nbytes = dora.dora_norm_factored_workspace(sh.out, sh.inp, sh.r)
+            ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+            y, db, dl = torch.empty_like(base), torch.empty_like(base), torch.empty_like(base)
+            dm = torch.empty(sh.out, device=dev)
+            wsb = torch.empty(dora.dora_compose_bwd_workspace(sh.T, sh.out), dtype=torch.uint8, device=dev)
+            t_norm = _time_ms(lambda: dora.dora_norm_factored(W0, A, B, m, sh.s, norm, g, ws, stream), 20, stream)
+            t_fwd = _time_ms(lambda: dora.dora_compose_fwd(base, lora, g, sh.s, y, stream), 20, stream)
+            t_bwd = _time_ms(lambda: dora.dora_compose_bwd(dy, base, lora, g, norm, sh.s, db, dl, dm, wsb, stream),
+                             20, stream)
+            alg = algorithmic(sh)
+            dense = sh.out * sh.inp * 4
+            print(json.dumps({"report": "rank_sweep", "r": r, "out": sh.out, "in": sh.inp, "T": sh.T,
+                              "norm_us": t_norm * 1e3,
+                              "norm_tflops_algorithmic": alg["norm_flops"] / (t_norm * 1e-3) / 1e12,
+                              "fwd_gbs": alg["fwd_bytes"] / (t_fwd * 1e-3) / 1e9,
+                              "bwd_gbs": alg["bwd_bytes"] / (t_bwd * 1e-3) / 1e9,
+                              "norm_transient_bytes": nbytes, "dense_fp32_matrix_bytes": dense,
+                              "dense_over_transient": dense / nbytes,
+                              "rank_dependent_theory": sh.out * sh.inp / (sh.out * sh.r + sh.r * sh.r)}),
+                  flush=True)
+            del W0, A, B, m, act, base, lora, dy, ws, y, db, dl
+            torch.cuda.empty_cache()
+    elif args.report == "mlp_stack":
+        # 32 gate/up (4096 -> 14336) + 32 down (14336 -> 4096) modules, r = 512,
+        # T = 16384, training step per module (norm + fwd + bwd), independent seeds
+        shapes = [wl.shape("mlp_gate_up"), wl.shape("mlp_down")]
+        mods = []
+        for k in range(wl.MLP_REPEATS):
+            for j, sh in enumerate(shapes):
+                mods.append((sh, _device_module(sh, wl.seed_for(sh.name, 2 * k + j), dev)))
+        bufs = {}
+        for sh in shapes:
+            gen = torch.Generator(device=dev)
+            gen.manual_seed(wl.seed_for(sh.name) + 99)
+            act = [torch.randn(sh.T, sh.out, device=dev, generator=gen).bfloat16() for _ in range(3)]
+            act[1] = (act[1].float() * math.sqrt(sh.r) * sh.sigma_B).bfloat16()
+            bufs[sh.name] = {
+                "act": act, "y": torch.empty_like(act[0]), "db": torch.empty_like(act[0]),
+                "dl": torch.empty_like(act[0]), "norm": torch.empty(sh.out, device=dev),
+                "g": torch.empty(sh.out, device=dev), "dm": torch.empty(sh.out, device=dev),
+                "ws": torch.empty(dora.dora_norm_factored_workspace(sh.out, sh.inp, sh.r), dtype=torch.uint8,
+                                  device=dev),
+                "wsb": torch.empty(dora.dora_compose_bwd_workspace(sh.T, sh.out), dtype=torch.uint8, device=dev)}
+
+        def stack():
+            for sh, (W0, A, B, m) in mods:
+                b = bufs[sh.name]
+                base, lora, dy = b["act"]
+                dora.dora_norm_factored(W0, A, B, m, sh.s, b["norm"], b["g"], b["ws"], stream)
+                dora.dora_compose_fwd(base, lora, b["g"], sh.s, b["y"], stream)
+                dora.dora_compose_bwd(dy, base, lora, b["g"], b["norm"], sh.s, b["db"], b["dl"], b["dm"], b["wsb"],
+                                      stream)
+
+        t = _time_ms(stack, 3, stream)
+        total = sum(sum(v for k, v in algorithmic(sh).items() if k.endswith("_bytes")) for sh, _ in mods)
+        compose = sum(algorithmic(sh)["fwd_bytes"] + algorithmic(sh)["bwd_bytes"] for sh, _ in mods)
+        print(json.dumps({"report": "mlp_stack", "modules": len(mods), "ms_per_stack": t,
+                          "modules_per_s": len(mods) / (t * 1e-3),
+                          "us_per_module": t * 1e3 / len(mods),
+                          "aggregate_algorithmic_gbs": total / (t * 1e-3) / 1e9,
+                          "compose_share_of_bytes": compose / total,
+                          "inputs": "device-drawn (torch Philox), seed per module; activations shared per shape"}),
+              flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -395,13 +513,17 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--report", choices=["rank_sweep", "mlp_stack"], default=None,
+                    help="extra per-workload report lines instead of the bench line")
     args = ap.parse_args()
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     if args.warmup < 3:
         args.warmup = 3
-    if args.impl == "reference":
+    if args.report is not None:
+        run_report(args)
+    elif args.impl == "reference":
         run_reference(args, rank, world)
     else:
         run_ours(args, rank, world, local_rank)

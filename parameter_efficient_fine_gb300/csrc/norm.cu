@@ -370,11 +370,11 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(full0 + 8u * s, 1);
-      mbar_init(conv0 + 8u * s, 128);
+      mbar_init(conv0 + 8u * s, 4);   // one arrival per converter warp
       mbar_init(empty0 + 8u * s, static_cast<uint32_t>(p.csize));   // one MMA release per cluster CTA
     }
     mbar_init(accf, 1);
-    mbar_init(acce, 128);
+    mbar_init(acce, 4);
     mbar_init(fin, 1);
     for (int e = 0; e < 8; ++e) mbar_init(epib0 + 8u * e, 1);
     ctl->abort = 0;
@@ -598,8 +598,11 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ 
                                              pack_bf16x2(hq[4], hq[5]), pack_bf16x2(hq[6], hq[7]));
         }
         if (kb < p.kb1) n0 += blk;
+        // every thread makes its shared-memory writes visible to the tensor
+        // core; then one arrival per warp
         fence_proxy_async();
-        mbar_arrive(conv0 + 8u * stage);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(conv0 + 8u * stage);
         if (++stage == S) {
           stage = 0;
           phase ^= 1u;
@@ -687,7 +690,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ 
         }
       }
       tc_fence_before();
-      mbar_arrive(acce);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acce);
       aphase ^= 1u;
       u += kbe - kb0;
     }

@@ -24,6 +24,7 @@ __all__ = [
     "dora_compose_bwd_noalloc",
     "dora_device_error",
     "dora_kernel_launches",
+    "dora_test_stall_loads",
     "DORA_F32",
     "DORA_BF16",
 ]
@@ -51,6 +52,7 @@ _SIGNATURES = {
     "dora_compose_bwd_noalloc": (_int, [_int, _vp, _vp, _vp, _vp, _vp, _f32, _i64, _i64, _vp, _vp, _vp, _vp]),
     "dora_device_error": (_int, [ctypes.POINTER(_int)]),
     "dora_kernel_launches": (ctypes.c_uint64, []),
+    "dora_test_stall_loads": (_int, [_int, ctypes.c_uint64]),
 }
 
 
@@ -173,3 +175,8 @@ def dora_device_error() -> int:
 
 def dora_kernel_launches() -> int:
     return int(load_library().dora_kernel_launches())
+
+
+def dora_test_stall_loads(on: bool, wait_limit_ns: int = 0) -> None:
+    """Testing hook: make later norm calls' bounded waits expire (see include/dora.h)."""
+    _check("dora_test_stall_loads", load_library().dora_test_stall_loads(1 if on else 0, int(wait_limit_ns)))

@@ -84,6 +84,10 @@ enum Mode : int { kGram = 0, kNorm = 1 };
 
 // device error word: 0 = fine; otherwise the code of the wait that gave up
 __device__ int g_dora_err = 0;
+// test hook (dora_test_stall_loads): the GEMM producers withhold all loads, so
+// the other roles' bounded waits expire; and the limit of those waits
+__device__ int g_dora_stall = 0;
+__device__ unsigned long long g_wait_limit_ns = kWaitLimitNs;
 
 struct TcParams {
   int mode;
@@ -325,7 +329,7 @@ __device__ bool wait_bounded(uint32_t bar, uint32_t parity, SharedCtl *ctl, int 
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
     if (ctl->abort) return false;
-    if ((i & 63u) == 0 && globaltimer() - t0 > kWaitLimitNs) {
+    if ((i & 63u) == 0 && globaltimer() - t0 > *reinterpret_cast<volatile unsigned long long *>(&g_wait_limit_ns)) {
       ctl->abort = 1;
       atomicCAS(err, 0, code);
       return false;
@@ -414,7 +418,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ 
       int stage = 0;
       uint32_t phase = 0;
       int issued = 0;  // loads issued in total (to drain on abort)
-      bool ok = true;
+      bool ok = *reinterpret_cast<volatile int *>(&g_dora_stall) == 0;
       for (long long u = u_begin; u < u_end && ok;) {
         const int t = static_cast<int>(u / p.kbtot);
         const int kb0 = static_cast<int>(u - static_cast<long long>(t) * p.kbtot);
@@ -1070,6 +1074,15 @@ extern "C" size_t dora_norm_factored_workspace(int64_t out, int64_t in, int64_t 
     if (L.total > total) total = L.total;
   }
   return total;
+}
+
+extern "C" dora_status dora_test_stall_loads(int on, uint64_t wait_limit_ns) {
+  const int v = on ? 1 : 0;
+  const unsigned long long lim = wait_limit_ns ? wait_limit_ns : kWaitLimitNs;
+  if (cudaMemcpyToSymbol(g_dora_stall, &v, sizeof(v)) != cudaSuccess ||
+      cudaMemcpyToSymbol(g_wait_limit_ns, &lim, sizeof(lim)) != cudaSuccess)
+    return DORA_ERR_CUDA;
+  return DORA_OK;
 }
 
 extern "C" dora_status dora_device_error(int *code) {

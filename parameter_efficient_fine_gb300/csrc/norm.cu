@@ -767,35 +767,52 @@ struct StreamK {
 
 // Gs[k][l] = (s/2) * G[k][l] for k, l < r (zero-padded to npad), split like
 // split_n_kernel: gh [npad, npad] TF32, gc [npad, 2*npad] bf16 (8 hi, 8 lo per group)
+__device__ __forceinline__ void store_gs(int a, int b, float v, int npad, float *gh, __nv_bfloat16 *gc) {
+  if (a >= npad || b >= npad) return;
+  const float h = __uint_as_float(tf32_rna(v));
+  gh[static_cast<long long>(a) * npad + b] = h;
+  const long long cb = static_cast<long long>(a) * 2 * npad + 16 * (b / 8) + (b % 8);
+  gc[cb] = __float2bfloat16_rn(h);
+  gc[cb + 8] = __float2bfloat16_rn(v - h);
+}
+
+// One 32 x 32 block of an upper-triangular Gram tile (blockIdx.x = tile, whose
+// M tile is mt and N chunk nc >= mt; blockIdx.y = block in the tile): sum the
+// tile's partials over its segments in order (reads coalesced along a row),
+// write the block at (k, l) and, for a tile off the diagonal, the mirrored
+// block at (l, k) through shared memory, so both writes are coalesced too.
 __global__ void __launch_bounds__(256) gram_reduce_kernel(const float *__restrict__ part, StreamK sk, int nchunks,
                                                           int NC, int r, int npad, float half_s,
                                                           float *__restrict__ gh, __nv_bfloat16 *__restrict__ gc) {
-  const long long n = static_cast<long long>(npad) * npad;
-  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
-    const int k = static_cast<int>(i / npad);
-    const int l = static_cast<int>(i - static_cast<long long>(k) * npad);
+  __shared__ float blk[32][33];
+  const int t = blockIdx.x;
+  int mt, nc;
+  tile_coords(t, nchunks, 1, 1, 0, &mt, &nc);
+  const int nsub = (NC + 31) / 32;
+  const int sr = static_cast<int>(blockIdx.y) / nsub, sc = static_cast<int>(blockIdx.y) - sr * nsub;
+  const size_t tm = static_cast<size_t>(mt) * nchunks + nc;
+  const long long ub = static_cast<long long>(t) * sk.kbtot;
+  const int c0 = cta_of(ub, sk.units, sk.ncl);
+  const int c1 = cta_of(ub + sk.kbtot - 1, sk.units, sk.ncl);
+  const int tx = threadIdx.x, ty = threadIdx.y;
+  for (int i = ty; i < 32; i += 8) {
+    const int row = sr * 32 + i, col = sc * 32 + tx;
+    const int k = mt * kBM + row, l = nc * NC + col;
     float v = 0.0f;
-    if (k < r && l < r) {
-      // G is symmetric and only the tiles with N chunk >= M tile were formed:
-      // read G[l][k] from its transposed position when (k, l) falls below
-      const int kk = (l / NC < k / kBM) ? l : k;
-      const int ll = (l / NC < k / kBM) ? k : l;
-      const int mt = kk / kBM, row = kk - mt * kBM;
-      const int nc = ll / NC, col = ll - nc * NC;
-      const int tg = sym_tile_index(mt, nc, nchunks);
-      const size_t tm = static_cast<size_t>(mt) * nchunks + nc;
-      const long long ub = static_cast<long long>(tg) * sk.kbtot;
-      const int c0 = cta_of(ub, sk.units, sk.ncl);
-      const int c1 = cta_of(ub + sk.kbtot - 1, sk.units, sk.ncl);
+    if (row < kBM && col < NC && k < r && l < r) {
       float sum = 0.0f;
       for (int j = 0; j <= c1 - c0; ++j) sum += part[((tm * sk.maxseg + j) * kBM + row) * NC + col];
       v = half_s * sum;
     }
-    const float h = __uint_as_float(tf32_rna(v));
-    gh[i] = h;
-    const long long cb = static_cast<long long>(k) * 2 * npad + 16 * (l / 8) + (l % 8);
-    gc[cb] = __float2bfloat16_rn(h);
-    gc[cb + 8] = __float2bfloat16_rn(v - h);
+    store_gs(k, l, v, npad, gh, gc);
+    blk[i][tx] = v;
+  }
+  if (mt != nc) {
+    __syncthreads();
+    for (int i = ty; i < 32; i += 8) {
+      const int l = nc * NC + sc * 32 + i, k = mt * kBM + sr * 32 + tx;
+      store_gs(l, k, blk[tx][i], npad, gh, gc);
+    }
   }
 }
 
@@ -1195,8 +1212,11 @@ extern "C" dora_status dora_norm_factored(const float *W0, const float *A, const
 
   // 3. Gs = (s/2) G, split like A
   StreamK skg{gg.p.units, gg.p.ncl, gg.p.kbtot, gg.p.maxseg, gg.p.csize};
-  gram_reduce_kernel<<<grid_for(static_cast<long long>(npad) * npad, sms), 256, 0, cs>>>(
-      part_g, skg, gg.p.nchunks, gg.p.NC, static_cast<int>(r), npad, 0.5f * s, g_hi, g_c);
+  {
+    const int nsub = (gg.p.NC + 31) / 32;
+    gram_reduce_kernel<<<dim3(static_cast<unsigned>(gg.p.tiles), static_cast<unsigned>(nsub * nsub)), dim3(32, 8), 0,
+                         cs>>>(part_g, skg, gg.p.nchunks, gg.p.NC, static_cast<int>(r), npad, 0.5f * s, g_hi, g_c);
+  }
   ++launches;
 
   // 4. [W0 | B] x [A | Gs]^T with per-segment row reductions

@@ -65,9 +65,22 @@
 namespace {
 
 constexpr int kBM = 128;            // rows per M tile (= tensor-memory lanes)
-constexpr int kBK = 16;             // fp32 per K block (64 bytes, one swizzle row)
-constexpr int kRowBytes = kBK * 4;  // 64
-constexpr int kThreads = 192;
+// fp32 per K block: 16 (64-byte rows, 64-byte swizzle) or 32 (128-byte rows,
+// 128-byte swizzle).  The wider block is taken where the stage still fits
+// three times into shared memory (N chunks up to kMaxChunkWide): DRAM streams
+// W0 markedly faster through 128-byte box rows than through 64-byte ones.
+constexpr int kBKNarrow = 16;
+constexpr int kBKWide = 32;
+constexpr int kMaxChunkWide = 128;
+// converter warps: kConvSub per tensor-memory lane quadrant; sub-warp j of a
+// quadrant converts the groups of 8 K indices q = j, j + kConvSub, ... of its
+// 32 rows, so one stage is converted by several warps side by side
+constexpr int kConvSub = 1;
+constexpr int kConvWarps = 4 * kConvSub;
+constexpr int kThreads = 64 + 32 * kConvWarps;
+// NORM partial record per row and segment: <B_i, D_i>, then the sum of W0_i^2
+// over the segment's K range from each converter sub-warp
+constexpr int kPartW = 1 + kConvSub;
 constexpr int kMaxChunkN = 384;     // largest N handled by one CTA pass
 constexpr int kMaxR = 1024;
 constexpr int kMaxCtas = 256;       // workspace bound: any device up to this size
@@ -104,6 +117,7 @@ struct TcParams {
   int NT;           // N-side rows in shared memory per stage (csize * sl >= NC)
   int nmma0, nmma1; // N of the first / second MMA instruction of a chunk
   int tmem_cols;
+  int slot0;        // first tensor-memory column of the M-side operand slots (one slot per stage)
   int stages;
   int tiles;        // M-tile groups (csize M tiles each) * nchunks
   long long units;  // tiles * kbtot
@@ -151,9 +165,6 @@ __device__ __forceinline__ unsigned long long globaltimer() {
 __device__ __forceinline__ void fence_barrier_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
-__device__ __forceinline__ void fence_proxy_async() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar) {
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
@@ -198,22 +209,32 @@ __device__ __forceinline__ void tc_fence_before() {
 __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
-__device__ __forceinline__ void mma_tf32(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t acc) {
+// D (+)= A * B on the tensor core, fp32 accumulator in tensor memory at `d`;
+// A (M side) in tensor memory at column address `a`, B (N side) in shared
+// memory by descriptor; accumulate when acc != 0
+__device__ __forceinline__ void mma_tf32_ta(uint32_t d, uint32_t a, uint64_t bdesc, uint32_t idesc, uint32_t acc) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc)
+      "tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
+      "r"(a), "l"(bdesc), "r"(idesc), "r"(acc)
       : "memory");
 }
-__device__ __forceinline__ void mma_bf16(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t acc) {
+__device__ __forceinline__ void mma_bf16_ta(uint32_t d, uint32_t a, uint64_t bdesc, uint32_t idesc, uint32_t acc) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc)
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
+      "r"(a), "l"(bdesc), "r"(idesc), "r"(acc)
       : "memory");
 }
+// 8 consecutive 32-bit columns of this thread's tensor-memory lane
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&v)[8]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+               "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+               : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
                : "memory");
@@ -252,16 +273,28 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
   return *reinterpret_cast<uint32_t *>(&h);
 }
 
-// Shared-memory matrix descriptor: K-major operand, 64-byte swizzle, rows of
-// 64 bytes, 8-row groups 512 bytes apart.
-__device__ __forceinline__ uint64_t sdesc_sw64(uint32_t saddr) {
+// Shared-memory matrix descriptor of a K-major operand whose rows are one
+// swizzle span long: BK = 16 -> 64-byte rows, 64-byte swizzle, 8-row groups
+// 512 bytes apart; BK = 32 -> 128-byte rows, 128-byte swizzle, 1024 bytes.
+template <int BK>
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr) {
+  static_assert(BK == 16 || BK == 32, "K block of 16 or 32 fp32");
+  constexpr uint64_t sbo = 8 * BK * 4;
+  constexpr uint64_t mode = BK == 16 ? 4 : 2;          // 64-byte / 128-byte swizzle
   uint64_t d = 0;
   d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);   // start address >> 4      [0,14)
   d |= static_cast<uint64_t>(1) << 16;                   // leading offset (unused)  [16,30)
-  d |= static_cast<uint64_t>(512 >> 4) << 32;            // stride offset 512 B      [32,46)
+  d |= (sbo >> 4) << 32;                                 // stride offset            [32,46)
   d |= static_cast<uint64_t>(1) << 46;                   // descriptor version       [46,48)
-  d |= static_cast<uint64_t>(4) << 61;                   // swizzle: 64 bytes        [61,64)
+  d |= mode << 61;                                       // swizzle mode             [61,64)
   return d;
+}
+// physical 16-byte chunk of logical chunk c in row `row` of such a tile (the
+// tile starts on a 1024-byte boundary): the swizzle XORs the chunk index with
+// address bits 7.. of the row
+template <int BK>
+__device__ __forceinline__ int swz_chunk(int c, int row) {
+  return BK == 16 ? c ^ ((row >> 1) & 3) : c ^ (row & 7);
 }
 // Instruction descriptor: kind::tf32, fp32 accumulator, both operands K-major,
 // M = 128, N = n.
@@ -313,10 +346,6 @@ __host__ __device__ __forceinline__ void tile_coords(int t, int nchunks, int sym
     *mt = grp * csize + crank;
   }
 }
-// inverse for the upper-triangular Gram tiles (mt <= nc)
-__host__ __device__ __forceinline__ int sym_tile_index(int mt, int nc, int q) {
-  return mt * q - (mt * (mt - 1)) / 2 + (nc - mt);
-}
 
 struct SharedCtl {
   volatile int abort;
@@ -348,11 +377,13 @@ __device__ void wait_drain(uint32_t bar, uint32_t parity) {
 // ---------------------------------------------------------------------------
 // the tensor-core GEMM (GRAM or NORM mode)
 // ---------------------------------------------------------------------------
+template <int BK>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_gemm_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ CUtensorMap mX2,
                const __grid_constant__ CUtensorMap mY1h, const __grid_constant__ CUtensorMap mY1c,
                const __grid_constant__ CUtensorMap mY2h, const __grid_constant__ CUtensorMap mY2c,
                const __grid_constant__ CUtensorMap mBe, const TcParams p) {
+  constexpr int kRowBytes = BK * 4;   // one swizzle span
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int S = p.stages;
@@ -374,7 +405,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(full0 + 8u * s, 1);
-      mbar_init(conv0 + 8u * s, 4);   // one arrival per converter warp
+      mbar_init(conv0 + 8u * s, kConvWarps);   // one arrival per converter warp
       mbar_init(empty0 + 8u * s, static_cast<uint32_t>(p.csize));   // one MMA release per cluster CTA
     }
     mbar_init(accf, 1);
@@ -433,10 +464,10 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ 
           const uint32_t fb = full0 + 8u * stage;
           mbar_expect_tx(fb, p.tx_bytes);
           const uint32_t xs = smem_u32(smem + static_cast<size_t>(stage) * p.stage_bytes);
-          const uint32_t yh = xs + 2u * kBM * kRowBytes;
+          const uint32_t yh = xs + kBM * kRowBytes;
           const uint32_t yc = yh + static_cast<uint32_t>(p.NT) * kRowBytes;
           const bool seg1 = kb < p.kb1;
-          const int kx = (seg1 ? kb : kb - p.kb1) * kBK;   // fp32 column of the hi operands
+          const int kx = (seg1 ? kb : kb - p.kb1) * BK;    // fp32 column of the hi operands
           tma_load_2d(xs, seg1 ? &mX1 : &mX2, kx, mt * kBM, fb);
           // this CTA's slice of the N-side tile; with a cluster it is multicast
           // to every CTA of the cluster, which all load the other slices
@@ -499,27 +530,30 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ 
             break;
           }
           tc_fence_after();
-          const uint32_t xh = smem_u32(smem + static_cast<size_t>(stage) * p.stage_bytes);
-          const uint32_t xc = xh + kBM * kRowBytes;
-          const uint32_t yh = xc + kBM * kRowBytes;
+          // M-side operand slot of this stage in tensor memory: BK columns of
+          // hi (one fp32 per column), then BK/8 groups of 8 columns holding the
+          // group's 16 bf16 correction values (two per column)
+          const uint32_t ah0 = tmem + static_cast<uint32_t>(p.slot0 + stage * 2 * BK);
+          const uint32_t ac0 = ah0 + BK;
+          const uint32_t yh = smem_u32(smem + static_cast<size_t>(stage) * p.stage_bytes) + kBM * kRowBytes;
           const uint32_t yc = yh + static_cast<uint32_t>(p.NT) * kRowBytes;
 #pragma unroll
-          for (int k = 0; k < kBK / 8; ++k) {
+          for (int k = 0; k < BK / 8; ++k) {
             const uint32_t acc0 = (kb != kb0 || k != 0) ? 1u : 0u;
-            // K step k: 8 tf32 (32 bytes) of the hi tiles, 16 bf16 (32 bytes)
-            // of the correction tiles
+            // K step k: 8 tf32 (32 bytes) of the hi operands, 16 bf16 (32 bytes)
+            // of the correction operands
             const uint32_t ko = static_cast<uint32_t>(k) * 32u;
-            const uint64_t ah = sdesc_sw64(xh + ko), ac = sdesc_sw64(xc + ko);
+            const uint32_t ah = ah0 + 8u * k, ac = ac0 + 8u * k;
             {
-              const uint64_t bh = sdesc_sw64(yh + ko), bc = sdesc_sw64(yc + ko);
-              mma_bf16(tmem, ac, bc, ic0, acc0);
-              mma_tf32(tmem, ah, bh, id0, 1u);
+              const uint64_t bh = sdesc<BK>(yh + ko), bc = sdesc<BK>(yc + ko);
+              mma_bf16_ta(tmem, ac, bc, ic0, acc0);
+              mma_tf32_ta(tmem, ah, bh, id0, 1u);
             }
             if (p.nmma1 > 0) {
               const uint32_t no = 256u * kRowBytes;
-              const uint64_t bh = sdesc_sw64(yh + no + ko), bc = sdesc_sw64(yc + no + ko);
-              mma_bf16(tmem + 256u, ac, bc, ic1, acc0);
-              mma_tf32(tmem + 256u, ah, bh, id1, 1u);
+              const uint64_t bh = sdesc<BK>(yh + no + ko), bc = sdesc<BK>(yc + no + ko);
+              mma_bf16_ta(tmem + 256u, ac, bc, ic1, acc0);
+              mma_tf32_ta(tmem + 256u, ah, bh, id1, 1u);
             }
           }
           if (p.csize > 1) mma_commit_mc(empty0 + 8u * stage, cmask);
@@ -541,9 +575,9 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ 
   } else {
     // -------------------------------------------------------- converters + epilogue
     const int quad = warp & 3;            // tensor-memory lane group of this warp
+    const int sub = (warp - 2) >> 2;      // sub-warp of the quadrant; sub-warp 0 also runs the epilogue
     const int row = quad * 32 + lane;     // row within the M tile
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quad * 32) << 16);
-    const int swz = (row >> 1) & 3;       // 64-byte swizzle: chunk c lives at c ^ swz
     // epilogue B buffers of this warp (NORM): two 32 x 32 fp32 boxes
     uint8_t *ebuf = smem + static_cast<size_t>(S) * p.stage_bytes + quad * 2 * kEpiBoxBytes;
     const uint32_t eb_bar = epib0 + 16u * quad;
@@ -569,42 +603,41 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ 
           ok = false;
           break;
         }
-        // this thread's row: 16 fp32 in four 16-byte chunks; logical chunk c
-        // sits at physical chunk c ^ swz in both the fp32 and the bf16 tile
-        float4 *xh = reinterpret_cast<float4 *>(smem + static_cast<size_t>(stage) * p.stage_bytes + row * kRowBytes);
-        uint4 *xc = reinterpret_cast<uint4 *>(reinterpret_cast<uint8_t *>(xh) + kBM * kRowBytes);
-        float v[16], h[16], l[16];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const float4 q = xh[c ^ swz];
-          v[4 * c] = q.x;
-          v[4 * c + 1] = q.y;
-          v[4 * c + 2] = q.z;
-          v[4 * c + 3] = q.w;
-        }
+        // this thread's row: BK fp32 in BK/4 16-byte chunks, stored swizzled
+        // (swz_chunk); one group of 8 K indices at a time, split into the
+        // tensor-memory operand slot of the stage: 8 hi columns and 8 columns
+        // of bf16 pairs (lo then hi) per group
+        const float4 *xr = reinterpret_cast<const float4 *>(smem + static_cast<size_t>(stage) * p.stage_bytes +
+                                                            row * kRowBytes);
+        const uint32_t slot = lane_addr + static_cast<uint32_t>(p.slot0 + stage * 2 * BK);
         float blk = 0.0f;
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          h[e] = __uint_as_float(tf32_rna(v[e]));
-          l[e] = v[e] - h[e];
-          blk = fmaf(v[e], v[e], blk);
-        }
+        for (int q0 = 0; q0 < BK / 8; q0 += kConvSub) {
+          const int q = q0 + sub;
+          if (BK / 8 % kConvSub != 0 && q >= BK / 8) break;
+          const float4 a = xr[swz_chunk<BK>(2 * q, row)], b = xr[swz_chunk<BK>(2 * q + 1, row)];
+          const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+          uint32_t hb[8], cb[8];
+          float l[8];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) xh[c ^ swz] = make_float4(h[4 * c], h[4 * c + 1], h[4 * c + 2], h[4 * c + 3]);
-        // correction tile, per group of 8 K indices: 8 lo then 8 hi (bf16)
+          for (int e = 0; e < 8; ++e) {
+            hb[e] = tf32_rna(v[e]);
+            l[e] = v[e] - __uint_as_float(hb[e]);
+            blk = fmaf(v[e], v[e], blk);
+          }
 #pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          const float *lq = l + 8 * q;
-          const float *hq = h + 8 * q;
-          xc[(2 * q) ^ swz] = make_uint4(pack_bf16x2(lq[0], lq[1]), pack_bf16x2(lq[2], lq[3]),
-                                         pack_bf16x2(lq[4], lq[5]), pack_bf16x2(lq[6], lq[7]));
-          xc[(2 * q + 1) ^ swz] = make_uint4(pack_bf16x2(hq[0], hq[1]), pack_bf16x2(hq[2], hq[3]),
-                                             pack_bf16x2(hq[4], hq[5]), pack_bf16x2(hq[6], hq[7]));
+          for (int e = 0; e < 4; ++e) {
+            cb[e] = pack_bf16x2(l[2 * e], l[2 * e + 1]);
+            cb[4 + e] = pack_bf16x2(__uint_as_float(hb[2 * e]), __uint_as_float(hb[2 * e + 1]));
+          }
+          tmem_st8(slot + 8u * q, hb);
+          tmem_st8(slot + BK + 8u * q, cb);
         }
+        tmem_wait_st();
         if (kb < p.kb1) n0 += blk;
-        // every thread makes its shared-memory writes visible to the tensor
-        // core; then one arrival per warp
-        fence_proxy_async();
+        // the tensor-memory stores are complete (wait::st); order them before
+        // the MMA lane's work, then one arrival per warp
+        tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(conv0 + 8u * stage);
         if (++stage == S) {
@@ -613,6 +646,16 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ 
         }
       }
       if (!ok) break;
+      const int grow = mt * kBM + row;
+      const bool valid = grow < p.M;
+      const int seg = cl - cta_of(static_cast<long long>(t) * p.kbtot, p.units, p.ncl);
+      // this row's NORM record of the segment
+      float *rec = p.part + ((tm * p.maxseg + seg) * kBM + row) * kPartW;
+      if (sub != 0) {
+        if (p.mode == kNorm && valid) rec[1 + sub] = n0;
+        u += kbe - kb0;
+        continue;
+      }
       // ---- epilogue of this segment
       const bool got = wait_bounded(accf, aphase, ctl, p.err, 5);
       if (!__all_sync(0xffffffffu, got)) {
@@ -620,9 +663,6 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ 
         break;
       }
       tc_fence_after();
-      const int grow = mt * kBM + row;
-      const bool valid = grow < p.M;
-      const int seg = cl - cta_of(static_cast<long long>(t) * p.kbtot, p.units, p.ncl);
       if (p.mode == kNorm) {
         // <B_i, D_i>: the warp's 32 rows of B arrive as 32 x 32 boxes by TMA,
         // two in flight; lane i reads row i (128-byte swizzle: chunk q at q ^ (i & 7))
@@ -677,8 +717,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ 
           break;
         }
         if (valid) {
-          float2 *dst = reinterpret_cast<float2 *>(p.part) + (tm * p.maxseg + seg) * kBM + row;
-          *dst = make_float2(n0, dot);
+          rec[0] = dot;
+          rec[1] = n0;
         }
       } else {
         float *dst = p.part + ((tm * p.maxseg + seg) * kBM + row) * p.NC;
@@ -816,8 +856,9 @@ __global__ void __launch_bounds__(256) gram_reduce_kernel(const float *__restric
   }
 }
 
-// n_i = sqrt(max(0, sum n0 + 2 s sum dot)), g_i = m_i / n_i
-__global__ void __launch_bounds__(256) norm_finalize_kernel(const float2 *__restrict__ part, StreamK sk, int nchunks,
+// n_i = sqrt(max(0, sum n0 + 2 s sum dot)), g_i = m_i / n_i; the partials in a
+// fixed order (segments in order; per segment the sub-warps' n0 in order)
+__global__ void __launch_bounds__(256) norm_finalize_kernel(const float *__restrict__ part, StreamK sk, int nchunks,
                                                             int out, const float *__restrict__ m, float two_s,
                                                             float *__restrict__ norm, float *__restrict__ g) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
@@ -831,9 +872,12 @@ __global__ void __launch_bounds__(256) norm_finalize_kernel(const float2 *__rest
     const int c0 = cta_of(ub, sk.units, sk.ncl);
     const int c1 = cta_of(ub + sk.kbtot - 1, sk.units, sk.ncl);
     for (int j = 0; j <= c1 - c0; ++j) {
-      const float2 v = part[(tm * sk.maxseg + j) * kBM + row];
-      if (nc == 0) n0 += v.x;
-      dot += v.y;
+      const float *rec = part + ((tm * sk.maxseg + j) * kBM + row) * kPartW;
+      dot += rec[0];
+      if (nc == 0) {
+#pragma unroll
+        for (int c = 0; c < kConvSub; ++c) n0 += rec[1 + c];
+      }
     }
   }
   const float n2 = fmaf(two_s, dot, n0);
@@ -847,6 +891,7 @@ __global__ void __launch_bounds__(256) norm_finalize_kernel(const float2 *__rest
 // ---------------------------------------------------------------------------
 struct GemmPlan {
   TcParams p;
+  int bk;   // fp32 per K block (the kernel instance)
   size_t smem_bytes;
   size_t part_bytes;
 };
@@ -864,14 +909,12 @@ void plan_n(int r, int *npad, int *nchunks, int *NC) {
   *NC = static_cast<int>(dora::round_up(dora::ceil_div(*npad, *nchunks), 16));
 }
 
-// csize CTAs per cluster, at most max_clusters clusters
-bool plan_gemm(int mode, int M, int kb1, int kb2, int r, int csize, int max_clusters, GemmPlan *gp) {
+// K = in (+ r for the norm pass); csize CTAs per cluster, at most max_clusters clusters
+bool plan_gemm(int mode, int M, int64_t in, int r, int csize, int max_clusters, GemmPlan *gp) {
   TcParams &p = gp->p;
   std::memset(&p, 0, sizeof(p));
   p.mode = mode;
   p.M = M;
-  p.kb1 = kb1;
-  p.kbtot = kb1 + kb2;
   p.csize = csize;
   int npad;
   plan_n(r, &npad, &p.nchunks, &p.NC);
@@ -881,6 +924,10 @@ bool plan_gemm(int mode, int M, int kb1, int kb2, int r, int csize, int max_clus
     p.nchunks = static_cast<int>(dora::ceil_div(npad, p.NC));
     p.sym = 1;
   }
+  gp->bk = p.NC <= kMaxChunkWide ? kBKWide : kBKNarrow;
+  const int row_bytes = gp->bk * 4;
+  p.kb1 = static_cast<int>(dora::ceil_div(in, gp->bk));
+  p.kbtot = p.kb1 + (mode == kNorm ? static_cast<int>(dora::ceil_div(r, gp->bk)) : 0);
   // N-side slices: each CTA of a cluster loads sl rows (a multiple of 8, so
   // every slice starts on a swizzle-pattern boundary) in nb boxes of nbox rows
   const int sl = static_cast<int>(dora::round_up(dora::ceil_div(p.NC, csize), 8));
@@ -890,15 +937,23 @@ bool plan_gemm(int mode, int M, int kb1, int kb2, int r, int csize, int max_clus
   p.NT = csize * p.sl;
   p.nmma0 = p.NC <= 256 ? p.NC : 256;
   p.nmma1 = p.NC - p.nmma0;
-  int cols = 32;
-  while (cols < p.NC) cols *= 2;
-  p.tmem_cols = cols;
-  p.stage_bytes = static_cast<unsigned>(2 * kBM * kRowBytes + 2 * p.NT * kRowBytes);
-  p.tx_bytes = static_cast<unsigned>(kBM * kRowBytes + 2 * p.NT * kRowBytes);
+  // tensor memory: the accumulator (nmma0 columns at 0, nmma1 at 256), then one
+  // M-side operand slot of 2 * bk columns per stage
+  const int acc_cols = static_cast<int>(dora::round_up(p.nmma1 > 0 ? 256 + p.nmma1 : p.nmma0, 32));
+  const int slot_cols = 2 * gp->bk;
+  p.slot0 = acc_cols;
+  // a stage in shared memory: the raw M-side box, then the N-side hi and
+  // correction tiles
+  p.stage_bytes = static_cast<unsigned>(kBM * row_bytes + 2 * p.NT * row_bytes);
+  p.tx_bytes = p.stage_bytes;
   const int epi = mode == kNorm ? kEpiBytes : 0;
   p.stages = static_cast<int>((kSmemMax - 1024 - epi - 512) / p.stage_bytes);
   if (p.stages > kMaxStages) p.stages = kMaxStages;
+  if (p.stages > (512 - acc_cols) / slot_cols) p.stages = (512 - acc_cols) / slot_cols;
   if (p.stages < 2) return false;
+  int cols = 32;
+  while (cols < acc_cols + p.stages * slot_cols) cols *= 2;
+  p.tmem_cols = cols;
   const int mtiles = static_cast<int>(dora::ceil_div(M, kBM));
   const int ngroups = static_cast<int>(dora::ceil_div(mtiles, csize));
   p.tiles = p.sym ? p.nchunks * (p.nchunks + 1) / 2 : ngroups * p.nchunks;
@@ -911,7 +966,7 @@ bool plan_gemm(int mode, int M, int kb1, int kb2, int r, int csize, int max_clus
   p.ctas = p.ncl * csize;
   p.maxseg = seg_bound(p.units, p.ncl, p.kbtot);
   p.r = r;
-  const size_t per_row = mode == kGram ? static_cast<size_t>(p.NC) : 2;
+  const size_t per_row = mode == kGram ? static_cast<size_t>(p.NC) : kPartW;
   gp->part_bytes = static_cast<size_t>(ngroups) * csize * p.nchunks * p.maxseg * kBM * per_row * sizeof(float);
   gp->smem_bytes = static_cast<size_t>(p.stages) * p.stage_bytes + epi + 1024 /*align*/ + 8 * (3 * p.stages + 3 + 8) + 64;
   // tensor memory: a CTA holding 512 columns must be alone on its SM
@@ -928,10 +983,8 @@ size_t al256(size_t x) { return (x + 255) & ~size_t(255); }
 // sms: CTAs available to the Gram pass; csize / max_clusters: cluster shape of the norm pass
 bool plan_layout(int64_t out, int64_t in, int64_t r, int sms, int csize, int max_clusters, GemmPlan *gg,
                  GemmPlan *gn, Layout *L) {
-  const int kb1 = static_cast<int>(dora::ceil_div(in, kBK));
-  const int kb2 = static_cast<int>(dora::ceil_div(r, kBK));
-  if (!plan_gemm(kGram, static_cast<int>(r), kb1, 0, static_cast<int>(r), 1, sms, gg)) return false;
-  if (!plan_gemm(kNorm, static_cast<int>(out), kb1, kb2, static_cast<int>(r), csize, max_clusters, gn)) return false;
+  if (!plan_gemm(kGram, static_cast<int>(r), in, static_cast<int>(r), 1, sms, gg)) return false;
+  if (!plan_gemm(kNorm, static_cast<int>(out), in, static_cast<int>(r), csize, max_clusters, gn)) return false;
   int npad, nchunks, NC;
   plan_n(static_cast<int>(r), &npad, &nchunks, &NC);
   size_t off = 0;
@@ -978,7 +1031,7 @@ EncodeTiledFn encode_fn() {
 // 2-D matrix [rows, cols] with row stride ld (elements); box = box_bytes of a
 // row (64: 64-byte swizzle, 128: 128-byte swizzle) x box_rows rows, zero fill
 bool make_map(CUtensorMap *map, const void *base, bool bf16, int64_t rows, int64_t cols, int64_t ld, int box_rows,
-              int box_bytes = kRowBytes) {
+              int box_bytes) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   const int esz = bf16 ? 2 : 4;
@@ -1015,7 +1068,8 @@ cudaError_t launch_gemm(const GemmPlan &gp, cudaStream_t cs, const CUtensorMap &
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, tc_gemm_kernel, x1, x2, y1h, y1c, y2h, y2c, be, gp.p);
+  if (gp.bk == kBKWide) return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<kBKWide>, x1, x2, y1h, y1c, y2h, y2c, be, gp.p);
+  return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<kBKNarrow>, x1, x2, y1h, y1c, y2h, y2c, be, gp.p);
 }
 
 // Cluster shape of the norm pass.  Sharing the N-side tile pays only when it
@@ -1037,11 +1091,9 @@ void choose_cluster(int device, int sms, int64_t out, int64_t in, int64_t r, int
   int npad, nchunks, NC;
   plan_n(static_cast<int>(r), &npad, &nchunks, &NC);
   if (NC < kMaxChunkN) return;
-  const int kb1 = static_cast<int>(dora::ceil_div(in, kBK));
-  const int kb2 = static_cast<int>(dora::ceil_div(r, kBK));
   for (int c = kMaxCluster; c >= 2; c /= 2) {
     GemmPlan gp;
-    if (!plan_gemm(kNorm, static_cast<int>(out), kb1, kb2, static_cast<int>(r), c, sms / c, &gp)) continue;
+    if (!plan_gemm(kNorm, static_cast<int>(out), in, static_cast<int>(r), c, sms / c, &gp)) continue;
     int active = -1;
     {
       std::lock_guard<std::mutex> lock(mu);
@@ -1061,7 +1113,9 @@ void choose_cluster(int device, int sms, int64_t out, int64_t in, int64_t r, int
       cfg.attrs = attr;
       cfg.numAttrs = 1;
       int n = 0;
-      if (cudaOccupancyMaxActiveClusters(&n, tc_gemm_kernel, &cfg) != cudaSuccess) {
+      const cudaError_t e = gp.bk == kBKWide ? cudaOccupancyMaxActiveClusters(&n, tc_gemm_kernel<kBKWide>, &cfg)
+                                             : cudaOccupancyMaxActiveClusters(&n, tc_gemm_kernel<kBKNarrow>, &cfg);
+      if (e != cudaSuccess) {
         cudaGetLastError();
         n = 0;
       }
@@ -1144,8 +1198,10 @@ extern "C" dora_status dora_norm_factored(const float *W0, const float *A, const
     if (!err_ptr[device]) {
       void *ptr = nullptr;
       if (cudaGetSymbolAddress(&ptr, g_dora_err) != cudaSuccess) return DORA_ERR_CUDA;
-      if (cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax) !=
-          cudaSuccess)
+      if (cudaFuncSetAttribute(tc_gemm_kernel<kBKNarrow>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax) !=
+              cudaSuccess ||
+          cudaFuncSetAttribute(tc_gemm_kernel<kBKWide>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax) !=
+              cudaSuccess)
         return DORA_ERR_CUDA;
       err_ptr[device] = static_cast<int *>(ptr);
     }
@@ -1189,12 +1245,15 @@ extern "C" dora_status dora_norm_factored(const float *W0, const float *A, const
   // the N-side boxes of the two passes may differ in height: one map set each
   CUtensorMap mA, mAh_g, mAc_g, mAh_n, mAc_n, mW0, mB, mGh, mGc, mBe;
   const int nbox = gn.p.nbox;
-  bool ok = make_map(&mA, A, false, r, in, in, kBM) && make_map(&mAh_n, a_hi, false, r, in, in, nbox) &&
-            make_map(&mAh_g, a_hi, false, r, in, in, gg.p.nbox) &&
-            make_map(&mAc_g, a_c, true, r, 2 * in8, 2 * in8, gg.p.nbox) &&
-            make_map(&mAc_n, a_c, true, r, 2 * in8, 2 * in8, nbox) && make_map(&mW0, W0, false, out, in, in, kBM) &&
-            make_map(&mB, Bk, false, out, ldb, ldb, kBM) && make_map(&mGh, g_hi, false, npad, npad, npad, nbox) &&
-            make_map(&mGc, g_c, true, npad, 2 * npad, 2 * npad, nbox) &&
+  // box rows are one K block: gg.bk / gn.bk fp32 (the same bytes of bf16)
+  const int rbg = 4 * gg.bk, rbn = 4 * gn.bk;
+  bool ok = make_map(&mA, A, false, r, in, in, kBM, rbg) && make_map(&mAh_g, a_hi, false, r, in, in, gg.p.nbox, rbg) &&
+            make_map(&mAc_g, a_c, true, r, 2 * in8, 2 * in8, gg.p.nbox, rbg) &&
+            make_map(&mAh_n, a_hi, false, r, in, in, nbox, rbn) &&
+            make_map(&mAc_n, a_c, true, r, 2 * in8, 2 * in8, nbox, rbn) &&
+            make_map(&mW0, W0, false, out, in, in, kBM, rbn) && make_map(&mB, Bk, false, out, ldb, ldb, kBM, rbn) &&
+            make_map(&mGh, g_hi, false, npad, npad, npad, nbox, rbn) &&
+            make_map(&mGc, g_c, true, npad, 2 * npad, 2 * npad, nbox, rbn) &&
             make_map(&mBe, Bk, false, out, ldb, ldb, 32, 128);
   if (!ok) {
     dora::count_launches(launches);
@@ -1231,7 +1290,7 @@ extern "C" dora_status dora_norm_factored(const float *W0, const float *A, const
   // 5. n and g
   StreamK skn{gn.p.units, gn.p.ncl, gn.p.kbtot, gn.p.maxseg, gn.p.csize};
   norm_finalize_kernel<<<static_cast<unsigned>(dora::ceil_div(out, 256)), 256, 0, cs>>>(
-      reinterpret_cast<const float2 *>(part_n), skn, gn.p.nchunks, static_cast<int>(out), m, 2.0f * s, norm, g);
+      part_n, skn, gn.p.nchunks, static_cast<int>(out), m, 2.0f * s, norm, g);
   ++launches;
   dora::count_launches(launches);
   return dora::launch_status();

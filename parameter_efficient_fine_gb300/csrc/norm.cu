@@ -16,8 +16,10 @@
 //   2. tc_gemm (GRAM)    partial tiles of G = A A^T, stream-K over K = in
 //   3. gram_reduce       fixed-order sum of the partial tiles, scaled by s/2, split
 //   4. tc_gemm (NORM)    [W0 | B] x [A | sG/2]^T, stream-K; per segment the epilogue
-//                        reduces each row to (sum W0_i^2 over its K range, <B_i, D_i>)
-//   5. norm_finalize     fixed-order sum of the segments, n = sqrt(max(0, n^2)), g = m/n
+//                        reduces each row to (sum W0_i^2 over its K range, <B_i, D_i>);
+//                        the epilogue warp that writes the last segment of a quarter
+//                        M tile sums its rows' segments in a fixed order and writes
+//                        n = sqrt(max(0, n^2)) and g = m / n
 //
 // Precision: every fp32 operand is split x = hi + lo, hi = x rounded to TF32
 // (nearest, ties away), lo = x - hi exactly, |lo| <= 2^-11 |x|.  Each product
@@ -27,23 +29,26 @@
 //                                  terms side by side along K (K = 16 = 8 + 8)
 // with fp32 accumulation in tensor memory.  The correction terms are ~2^-11 of
 // the product, so their bf16 rounding costs <= 2^-19 of it; lo*lo (2^-22) is
-// dropped.  Against three TF32 passes this issues 2/3 of the tensor work and
-// reads 2/3 of the operand bytes from shared memory per K step.
-// The M-side operand (W0 or B) is split in shared memory by converter warps,
-// which also accumulate ||W0_i||^2 on the way; the N-side operand is split once
-// in global memory (it is re-read by every M tile) into a TF32 matrix and a
-// bf16 matrix holding, per group of 8 K indices, 8 hi values then 8 lo values.
-// The M-side correction tile holds lo then hi per group, so the K-concatenated
-// bf16 MMA yields lo_x*hi_y + hi_x*lo_y.
+// dropped.  Against three TF32 passes this issues 2/3 of the tensor work.
+// The M-side operand (W0 or B) is split by converter warps, which read the raw
+// box from shared memory, accumulate ||W0_i||^2 on the way and write the split
+// operand into tensor memory, where the MMAs take their A operand; the N-side
+// operand is split once in global memory (it is re-read by every M tile) into
+// a TF32 matrix and a bf16 matrix holding, per group of 8 K indices, 8 hi
+// values then 8 lo values.  The M-side correction holds lo then hi per group,
+// so the K-concatenated bf16 MMA yields lo_x*hi_y + hi_x*lo_y.
 //
 // tc_gemm structure (one CTA per SM, persistent, 192 threads):
-//   warp 0      TMA producer: loads the M-side box [128 x 16 fp32] and the
+//   warp 0      TMA producer: loads the raw M-side box [128 x BK fp32] and the
 //               N-side hi/lo boxes of each K block into a ring of stages
 //   warp 1      allocates tensor memory; one lane issues tcgen05.mma
-//   warps 2..5  converters (hi/lo split of the M-side box, row sums of W0^2),
-//               then the epilogue for their 32 tensor-memory lanes each
-// Operand tiles are K-major with the 64-byte swizzle (16 fp32 per row).  The
-// work is the list of (M tile, N chunk, K block) units, split evenly over the
+//   warps 2..5  converters (hi/lo split of the M-side box into the stage's
+//               tensor-memory slot, row sums of W0^2), then the epilogue for
+//               their 32 tensor-memory lanes each
+// Tiles in shared memory are K-major with the swizzle of one K block per row:
+// BK = 16 fp32 (64-byte swizzle) or, for N chunks up to 128, BK = 32 (128-byte
+// swizzle).  Tensor memory holds the accumulator and one operand slot per
+// stage.  The work is the list of (M tile, N chunk, K block) units, split evenly over the
 // CTAs; a CTA's range crosses at most a few tile boundaries, and each piece
 // ("segment") leaves one partial result.  All partial sums are combined in a
 // fixed order, so results are bitwise reproducible.
@@ -72,15 +77,7 @@ constexpr int kBM = 128;            // rows per M tile (= tensor-memory lanes)
 constexpr int kBKNarrow = 16;
 constexpr int kBKWide = 32;
 constexpr int kMaxChunkWide = 128;
-// converter warps: kConvSub per tensor-memory lane quadrant; sub-warp j of a
-// quadrant converts the groups of 8 K indices q = j, j + kConvSub, ... of its
-// 32 rows, so one stage is converted by several warps side by side
-constexpr int kConvSub = 1;
-constexpr int kConvWarps = 4 * kConvSub;
-constexpr int kThreads = 64 + 32 * kConvWarps;
-// NORM partial record per row and segment: <B_i, D_i>, then the sum of W0_i^2
-// over the segment's K range from each converter sub-warp
-constexpr int kPartW = 1 + kConvSub;
+constexpr int kThreads = 192;
 constexpr int kMaxChunkN = 384;     // largest N handled by one CTA pass
 constexpr int kMaxR = 1024;
 constexpr int kMaxCtas = 256;       // workspace bound: any device up to this size
@@ -129,6 +126,11 @@ struct TcParams {
   float *part;      // GRAM: [tiles][maxseg][128][NC]; NORM: [tiles][maxseg][128][2]
   int r;
   int *err;
+  // NORM: the epilogue warp that completes a quarter of an M tile finalises it
+  int *cnt;         // [M tiles][4] records written so far (zeroed before the launch)
+  const float *m;
+  float *norm, *g;
+  float two_s;
 };
 
 // ---------------------------------------------------------------------------
@@ -405,7 +407,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(full0 + 8u * s, 1);
-      mbar_init(conv0 + 8u * s, kConvWarps);   // one arrival per converter warp
+      mbar_init(conv0 + 8u * s, 4);   // one arrival per converter warp
       mbar_init(empty0 + 8u * s, static_cast<uint32_t>(p.csize));   // one MMA release per cluster CTA
     }
     mbar_init(accf, 1);
@@ -575,7 +577,6 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ 
   } else {
     // -------------------------------------------------------- converters + epilogue
     const int quad = warp & 3;            // tensor-memory lane group of this warp
-    const int sub = (warp - 2) >> 2;      // sub-warp of the quadrant; sub-warp 0 also runs the epilogue
     const int row = quad * 32 + lane;     // row within the M tile
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quad * 32) << 16);
     // epilogue B buffers of this warp (NORM): two 32 x 32 fp32 boxes
@@ -612,9 +613,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ 
         const uint32_t slot = lane_addr + static_cast<uint32_t>(p.slot0 + stage * 2 * BK);
         float blk = 0.0f;
 #pragma unroll
-        for (int q0 = 0; q0 < BK / 8; q0 += kConvSub) {
-          const int q = q0 + sub;
-          if (BK / 8 % kConvSub != 0 && q >= BK / 8) break;
+        for (int q = 0; q < BK / 8; ++q) {
           const float4 a = xr[swz_chunk<BK>(2 * q, row)], b = xr[swz_chunk<BK>(2 * q + 1, row)];
           const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
           uint32_t hb[8], cb[8];
@@ -649,13 +648,6 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ 
       const int grow = mt * kBM + row;
       const bool valid = grow < p.M;
       const int seg = cl - cta_of(static_cast<long long>(t) * p.kbtot, p.units, p.ncl);
-      // this row's NORM record of the segment
-      float *rec = p.part + ((tm * p.maxseg + seg) * kBM + row) * kPartW;
-      if (sub != 0) {
-        if (p.mode == kNorm && valid) rec[1 + sub] = n0;
-        u += kbe - kb0;
-        continue;
-      }
       // ---- epilogue of this segment
       const bool got = wait_bounded(accf, aphase, ctl, p.err, 5);
       if (!__all_sync(0xffffffffu, got)) {
@@ -716,9 +708,39 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ 
           ok = false;
           break;
         }
-        if (valid) {
-          rec[0] = dot;
-          rec[1] = n0;
+        float2 *part2 = reinterpret_cast<float2 *>(p.part);
+        if (valid) part2[(tm * p.maxseg + seg) * kBM + row] = make_float2(n0, dot);
+        // count this warp's 32 records of the M tile; the warp that writes the
+        // last ones sums all of them (chunks in order, segments in order) into
+        // n_i = sqrt(max(0, sum n0 + 2 s sum dot)) and g_i = m_i / n_i
+        __threadfence();
+        __syncwarp();
+        int old = 0;
+        if (lane == 0) old = atomicAdd(p.cnt + mt * 4 + quad, 1);
+        old = __shfl_sync(0xffffffffu, old, 0);
+        int expect = 0;
+        for (int c = 0; c < p.nchunks; ++c) {
+          const long long ub = (static_cast<long long>(mt / p.csize) * p.nchunks + c) * p.kbtot;
+          expect += cta_of(ub + p.kbtot - 1, p.units, p.ncl) - cta_of(ub, p.units, p.ncl) + 1;
+        }
+        if (old == expect - 1) {
+          __threadfence();
+          if (valid) {
+            float s0 = 0.0f, sd = 0.0f;
+            for (int c = 0; c < p.nchunks; ++c) {
+              const long long ub = (static_cast<long long>(mt / p.csize) * p.nchunks + c) * p.kbtot;
+              const int nseg = cta_of(ub + p.kbtot - 1, p.units, p.ncl) - cta_of(ub, p.units, p.ncl) + 1;
+              const size_t tmc = static_cast<size_t>(mt) * p.nchunks + c;
+              for (int j = 0; j < nseg; ++j) {
+                const float2 v = __ldcg(part2 + (tmc * p.maxseg + j) * kBM + row);
+                if (c == 0) s0 += v.x;
+                sd += v.y;
+              }
+            }
+            const float nn = sqrtf(fmaxf(fmaf(p.two_s, sd, s0), 0.0f));
+            p.norm[grow] = nn;
+            p.g[grow] = p.m[grow] / nn;
+          }
         }
       } else {
         float *dst = p.part + ((tm * p.maxseg + seg) * kBM + row) * p.NC;
@@ -756,14 +778,18 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ 
 // elementwise helpers
 // ---------------------------------------------------------------------------
 
-// N-side split of a [rows, cols] fp32 matrix (cols % 4 == 0):
+// N-side split of a [rows, cols] fp32 matrix (cols % 4 == 0), and zero fill of
+// the norm pass's ncnt completion counters:
 //   hi [rows, cols] fp32: x rounded to TF32
 //   c  [rows, 2*cols8] bf16 (cols8 = cols rounded up to 8): per group q of 8
 //      columns, 8 bf16(hi) then 8 bf16(x - hi); zero past cols
 // One thread per group of 4 columns.
 __global__ void __launch_bounds__(256) split_n_kernel(const float *__restrict__ x, long long rows, int cols,
                                                       int cols8, float *__restrict__ hi,
-                                                      __nv_bfloat16 *__restrict__ c) {
+                                                      __nv_bfloat16 *__restrict__ c, int *__restrict__ cnt,
+                                                      int ncnt) {
+  // the norm pass's completion counters start at zero
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < ncnt; i += gridDim.x * blockDim.x) cnt[i] = 0;
   const int g4 = cols8 / 4;
   const long long n = rows * g4;
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
@@ -817,14 +843,16 @@ __device__ __forceinline__ void store_gs(int a, int b, float v, int npad, float 
 }
 
 // One 32 x 32 block of an upper-triangular Gram tile (blockIdx.x = tile, whose
-// M tile is mt and N chunk nc >= mt; blockIdx.y = block in the tile): sum the
-// tile's partials over its segments in order (reads coalesced along a row),
-// write the block at (k, l) and, for a tile off the diagonal, the mirrored
-// block at (l, k) through shared memory, so both writes are coalesced too.
+// M tile is mt and N chunk nc >= mt; blockIdx.y = block in the tile).  Warp w
+// sums the segments w, w + 8, ... of the tile's partials (a lane per column,
+// 32 independent row sums, so the loads of a segment are in flight together);
+// the 8 warp sums are then added in warp order.  The block is written at
+// (k, l) and, for a tile off the diagonal, mirrored at (l, k) through shared
+// memory, so both writes are coalesced.
 __global__ void __launch_bounds__(256) gram_reduce_kernel(const float *__restrict__ part, StreamK sk, int nchunks,
                                                           int NC, int r, int npad, float half_s,
                                                           float *__restrict__ gh, __nv_bfloat16 *__restrict__ gc) {
-  __shared__ float blk[32][33];
+  __shared__ float wsum[8][32][33];
   const int t = blockIdx.x;
   int mt, nc;
   tile_coords(t, nchunks, 1, 1, 0, &mt, &nc);
@@ -832,58 +860,51 @@ __global__ void __launch_bounds__(256) gram_reduce_kernel(const float *__restric
   const int sr = static_cast<int>(blockIdx.y) / nsub, sc = static_cast<int>(blockIdx.y) - sr * nsub;
   const size_t tm = static_cast<size_t>(mt) * nchunks + nc;
   const long long ub = static_cast<long long>(t) * sk.kbtot;
-  const int c0 = cta_of(ub, sk.units, sk.ncl);
-  const int c1 = cta_of(ub + sk.kbtot - 1, sk.units, sk.ncl);
+  const int nseg = cta_of(ub + sk.kbtot - 1, sk.units, sk.ncl) - cta_of(ub, sk.units, sk.ncl) + 1;
   const int tx = threadIdx.x, ty = threadIdx.y;
-  for (int i = ty; i < 32; i += 8) {
-    const int row = sr * 32 + i, col = sc * 32 + tx;
-    const int k = mt * kBM + row, l = nc * NC + col;
-    float v = 0.0f;
-    if (row < kBM && col < NC && k < r && l < r) {
-      float sum = 0.0f;
-      for (int j = 0; j <= c1 - c0; ++j) sum += part[((tm * sk.maxseg + j) * kBM + row) * NC + col];
-      v = half_s * sum;
+  // valid rows of this block (G has r rows and columns) and this lane's column
+  const int nrow = min(32, min(kBM, r - mt * kBM) - sr * 32);
+  const int col = sc * 32 + tx;
+  const bool cvalid = col < NC && nc * NC + col < r;
+  float acc[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) acc[i] = 0.0f;
+  if (cvalid) {
+    for (int j = ty; j < nseg; j += 8) {
+      const float *pj = part + ((tm * sk.maxseg + j) * kBM + sr * 32) * NC + col;
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        if (i < nrow) acc[i] += pj[static_cast<size_t>(i) * NC];
     }
-    store_gs(k, l, v, npad, gh, gc);
-    blk[i][tx] = v;
+  }
+#pragma unroll
+  for (int i = 0; i < 32; ++i) wsum[ty][i][tx] = acc[i];
+  __syncthreads();
+  float v[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int i = ty + 8 * q;
+    float sum = 0.0f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) sum += wsum[w][i][tx];
+    v[q] = (i < nrow && cvalid) ? half_s * sum : 0.0f;
+  }
+  __syncthreads();
+  // wsum[0] now holds the block's values for the mirrored write
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int i = ty + 8 * q;
+    store_gs(mt * kBM + sr * 32 + i, nc * NC + col, v[q], npad, gh, gc);
+    wsum[0][i][tx] = v[q];
   }
   if (mt != nc) {
     __syncthreads();
-    for (int i = ty; i < 32; i += 8) {
-      const int l = nc * NC + sc * 32 + i, k = mt * kBM + sr * 32 + tx;
-      store_gs(l, k, blk[tx][i], npad, gh, gc);
-    }
-  }
-}
-
-// n_i = sqrt(max(0, sum n0 + 2 s sum dot)), g_i = m_i / n_i; the partials in a
-// fixed order (segments in order; per segment the sub-warps' n0 in order)
-__global__ void __launch_bounds__(256) norm_finalize_kernel(const float *__restrict__ part, StreamK sk, int nchunks,
-                                                            int out, const float *__restrict__ m, float two_s,
-                                                            float *__restrict__ norm, float *__restrict__ g) {
-  const int i = blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= out) return;
-  const int mt = i / kBM, row = i - mt * kBM;
-  float n0 = 0.0f, dot = 0.0f;
-  for (int nc = 0; nc < nchunks; ++nc) {
-    const int tg = (mt / sk.csize) * nchunks + nc;
-    const size_t tm = static_cast<size_t>(mt) * nchunks + nc;
-    const long long ub = static_cast<long long>(tg) * sk.kbtot;
-    const int c0 = cta_of(ub, sk.units, sk.ncl);
-    const int c1 = cta_of(ub + sk.kbtot - 1, sk.units, sk.ncl);
-    for (int j = 0; j <= c1 - c0; ++j) {
-      const float *rec = part + ((tm * sk.maxseg + j) * kBM + row) * kPartW;
-      dot += rec[0];
-      if (nc == 0) {
 #pragma unroll
-        for (int c = 0; c < kConvSub; ++c) n0 += rec[1 + c];
-      }
+    for (int q = 0; q < 4; ++q) {
+      const int i = ty + 8 * q;
+      store_gs(nc * NC + sc * 32 + i, mt * kBM + sr * 32 + tx, wsum[0][tx][i], npad, gh, gc);
     }
   }
-  const float n2 = fmaf(two_s, dot, n0);
-  const float n = sqrtf(fmaxf(n2, 0.0f));
-  norm[i] = n;
-  g[i] = m[i] / n;
 }
 
 // ---------------------------------------------------------------------------
@@ -966,7 +987,7 @@ bool plan_gemm(int mode, int M, int64_t in, int r, int csize, int max_clusters, 
   p.ctas = p.ncl * csize;
   p.maxseg = seg_bound(p.units, p.ncl, p.kbtot);
   p.r = r;
-  const size_t per_row = mode == kGram ? static_cast<size_t>(p.NC) : kPartW;
+  const size_t per_row = mode == kGram ? static_cast<size_t>(p.NC) : 2;
   gp->part_bytes = static_cast<size_t>(ngroups) * csize * p.nchunks * p.maxseg * kBM * per_row * sizeof(float);
   gp->smem_bytes = static_cast<size_t>(p.stages) * p.stage_bytes + epi + 1024 /*align*/ + 8 * (3 * p.stages + 3 + 8) + 64;
   // tensor memory: a CTA holding 512 columns must be alone on its SM
@@ -975,7 +996,7 @@ bool plan_gemm(int mode, int M, int64_t in, int r, int csize, int max_clusters, 
 }
 
 struct Layout {
-  size_t a_hi, a_c, g_hi, g_c, part_g, part_n, b_pad, total;
+  size_t a_hi, a_c, g_hi, g_c, part_g, part_n, b_pad, cnt, total;
 };
 
 size_t al256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -1000,6 +1021,7 @@ bool plan_layout(int64_t out, int64_t in, int64_t r, int sms, int csize, int max
   L->part_g = take(gg->part_bytes);
   L->part_n = take(gn->part_bytes);
   L->b_pad = (r % 4) ? take(static_cast<size_t>(out) * dora::round_up(r, 4) * 4) : 0;
+  L->cnt = take(static_cast<size_t>(dora::ceil_div(out, kBM)) * 4 * sizeof(int));
   L->total = off;
   return true;
 }
@@ -1230,7 +1252,9 @@ extern "C" dora_status dora_norm_factored(const float *W0, const float *A, const
 
   // 1. N-side split of A; B padded to a TMA-legal row stride when r % 4 != 0
   const int in8 = static_cast<int>(dora::round_up(in, 8));
-  split_n_kernel<<<grid_for(r * in8 / 4, sms), 256, 0, cs>>>(A, r, static_cast<int>(in), in8, a_hi, a_c);
+  int *cnt = reinterpret_cast<int *>(ws + L.cnt);
+  const int ncnt = static_cast<int>(dora::ceil_div(out, kBM)) * 4;
+  split_n_kernel<<<grid_for(r * in8 / 4, sms), 256, 0, cs>>>(A, r, static_cast<int>(in), in8, a_hi, a_c, cnt, ncnt);
   ++launches;
   if (r % 4) {
     const int rp = static_cast<int>(dora::round_up(r, 4));
@@ -1278,19 +1302,19 @@ extern "C" dora_status dora_norm_factored(const float *W0, const float *A, const
   }
   ++launches;
 
-  // 4. [W0 | B] x [A | Gs]^T with per-segment row reductions
+  // 4. [W0 | B] x [A | Gs]^T with per-segment row reductions; the last
+  //    epilogue warp of each quarter M tile writes n and g
   gn.p.part = part_n;
   gn.p.err = errp;
+  gn.p.cnt = cnt;
+  gn.p.m = m;
+  gn.p.norm = norm;
+  gn.p.g = g;
+  gn.p.two_s = 2.0f * s;
   if (launch_gemm(gn, cs, mW0, mB, mAh_n, mAc_n, mGh, mGc, mBe) != cudaSuccess) {
     dora::count_launches(launches);
     return DORA_ERR_CUDA;
   }
-  ++launches;
-
-  // 5. n and g
-  StreamK skn{gn.p.units, gn.p.ncl, gn.p.kbtot, gn.p.maxseg, gn.p.csize};
-  norm_finalize_kernel<<<static_cast<unsigned>(dora::ceil_div(out, 256)), 256, 0, cs>>>(
-      part_n, skn, gn.p.nchunks, static_cast<int>(out), m, 2.0f * s, norm, g);
   ++launches;
   dora::count_launches(launches);
   return dora::launch_status();

@@ -71,6 +71,8 @@ def test_attention_projection_reduced_tokens():
     (130, 64, 768, 16),        # two N chunks of 384 (the largest rank swept)
     (8, 4, 5, 3),              # one K block, mostly out of bounds
     (1, 16, 2, 1),             # a single output row, a single token
+    (300, 1040, 128, 50),      # N = 128, the widest chunk with 32-wide K blocks; K tail of 16
+    (260, 200, 129, 30),       # N = 144: 16-wide K blocks again; K tail of 8
 ])
 def test_shapes_span_tiles_and_ragged_tails(out, inp, r, T):
     sh = wl.shape("high_rank", out=out, inp=inp, r=r, T=T)

@@ -85,8 +85,6 @@ constexpr int kMaxCluster = 2;      // largest cluster of the norm pass (4 measu
 constexpr int kMinUnitsNorm = 4;
 constexpr int kMinUnitsGram = 16;
 constexpr int kSmemMax = 232448;           // 227 KB: the opt-in maximum per CTA
-constexpr int kEpiBoxBytes = 32 * 32 * 4;   // epilogue B box: 32 rows x 32 fp32 (128-byte swizzle)
-constexpr int kEpiBytes = 4 * 2 * kEpiBoxBytes;  // 4 epilogue warps x 2 buffers
 constexpr int kMaxStages = 12;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
 
@@ -131,6 +129,8 @@ struct TcParams {
   const float *m;
   float *norm, *g;
   float two_s;
+  const float *Bk;  // B (or its padded copy) [M, ldb]: the epilogue prefetches its rows into L2
+  int ldb;
 };
 
 // ---------------------------------------------------------------------------
@@ -191,6 +191,11 @@ __device__ __forceinline__ uint32_t cluster_rank() {
 }
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// bring `bytes` (a multiple of 16) at a 16-byte aligned address into L2
+__device__ __forceinline__ void prefetch_l2(const void *ptr, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(ptr)), "r"(bytes)
+               : "memory");
 }
 __device__ __forceinline__ void prefetch_map(const CUtensorMap *map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
@@ -384,22 +389,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 tc_gemm_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ CUtensorMap mX2,
                const __grid_constant__ CUtensorMap mY1h, const __grid_constant__ CUtensorMap mY1c,
                const __grid_constant__ CUtensorMap mY2h, const __grid_constant__ CUtensorMap mY2c,
-               const __grid_constant__ CUtensorMap mBe, const TcParams p) {
+               const TcParams p) {
   constexpr int kRowBytes = BK * 4;   // one swizzle span
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int S = p.stages;
-  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + static_cast<size_t>(S) * p.stage_bytes +
-                                               (p.mode == kNorm ? kEpiBytes : 0));
-  // barrier layout: full[S], conv[S], empty[S], accf, acce, fin, epi[8]
-  SharedCtl *ctl = reinterpret_cast<SharedCtl *>(bars + 3 * S + 3 + 8);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + static_cast<size_t>(S) * p.stage_bytes);
+  // barrier layout: full[S], conv[S], empty[S], accf, acce, fin
+  SharedCtl *ctl = reinterpret_cast<SharedCtl *>(bars + 3 * S + 3);
   const uint32_t full0 = smem_u32(bars);
   const uint32_t conv0 = full0 + 8u * S;
   const uint32_t empty0 = conv0 + 8u * S;
   const uint32_t accf = empty0 + 8u * S;
   const uint32_t acce = accf + 8;
   const uint32_t fin = acce + 8;
-  const uint32_t epib0 = fin + 8;   // epilogue B buffers: barrier of warp quadrant q, buffer b at epib0 + 8*(2q+b)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -413,7 +416,6 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ 
     mbar_init(accf, 1);
     mbar_init(acce, 4);
     mbar_init(fin, 1);
-    for (int e = 0; e < 8; ++e) mbar_init(epib0 + 8u * e, 1);
     ctl->abort = 0;
     fence_barrier_init();
   }
@@ -421,7 +423,6 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ 
     prefetch_map(&mX1);
     prefetch_map(&mY1h);
     prefetch_map(&mY1c);
-    if (p.mode == kNorm) prefetch_map(&mBe);
     if (p.kbtot > p.kb1) {
       prefetch_map(&mX2);
       prefetch_map(&mY2h);
@@ -579,11 +580,6 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ 
     const int quad = warp & 3;            // tensor-memory lane group of this warp
     const int row = quad * 32 + lane;     // row within the M tile
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quad * 32) << 16);
-    // epilogue B buffers of this warp (NORM): two 32 x 32 fp32 boxes
-    uint8_t *ebuf = smem + static_cast<size_t>(S) * p.stage_bytes + quad * 2 * kEpiBoxBytes;
-    const uint32_t eb_bar = epib0 + 16u * quad;
-    uint32_t eph = 0u;    // bit b: phase parity of buffer b's barrier
-    uint32_t epend = 0u;  // bit b: a copy into buffer b is in flight
     int stage = 0;
     uint32_t phase = 0;
     uint32_t aphase = 0;
@@ -596,6 +592,13 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ 
       tile_coords(t, p.nchunks, p.sym, p.csize, crank, &mt, &nc);
       const size_t tm = static_cast<size_t>(mt) * p.nchunks + nc;   // (M tile, N chunk) of this CTA's partials
       float n0 = 0.0f;  // sum of W0_i^2 over this segment's K range
+      if (p.mode == kNorm && lane == 0) {
+        // the epilogue will read this warp's 32 rows of B: start them towards L2 now
+        const int r0 = mt * kBM + quad * 32;
+        const int nr = min(32, p.M - r0);
+        if (nr > 0)
+          prefetch_l2(p.Bk + static_cast<size_t>(r0) * p.ldb, static_cast<uint32_t>(nr) * p.ldb * 4u);
+      }
       for (int kb = kb0; kb < kbe; ++kb) {
         // every lane waits; the decision to go on is taken warp-wide so that
         // the warp stays converged for the tcgen05.ld of the epilogue
@@ -656,57 +659,37 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ 
       }
       tc_fence_after();
       if (p.mode == kNorm) {
-        // <B_i, D_i>: the warp's 32 rows of B arrive as 32 x 32 boxes by TMA,
-        // two in flight; lane i reads row i (128-byte swizzle: chunk q at q ^ (i & 7))
+        // <B_i, D_i>: lane i reads row i of B with 128-bit loads (the rows
+        // were prefetched into L2 at the segment's start), one 32-column
+        // chunk ahead of the tensor-memory chunk it multiplies
         float dot = 0.0f;
         const int nchk = (p.NC + 31) >> 5;
-        const int ybase = mt * kBM + quad * 32;
-        if (lane == 0) {
-          for (int b = 0; b < 2 && b < nchk; ++b) {
-            mbar_expect_tx(eb_bar + 8u * b, kEpiBoxBytes);
-            tma_load_2d(smem_u32(ebuf + b * kEpiBoxBytes), &mBe, nc * p.NC + 32 * b, ybase, eb_bar + 8u * b);
-            epend |= 1u << b;
-          }
-        }
-        bool eok = true;
+        const int cbase = nc * p.NC;
+        const int ncol = min(p.NC, p.r - cbase);   // B columns of this N chunk (zero padding beyond)
+        const float *brow = p.Bk + static_cast<size_t>(valid ? grow : 0) * p.ldb + cbase;
+        float4 cur[8], nxt[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          cur[q] = (valid && 4 * q < ncol) ? __ldg(reinterpret_cast<const float4 *>(brow + 4 * q))
+                                           : make_float4(0.f, 0.f, 0.f, 0.f);
         for (int ci = 0; ci < nchk; ++ci) {
-          const int b = ci & 1;
-          float v[32];
-          tmem_ld32(lane_addr + static_cast<uint32_t>(32 * ci), v);
-          const bool gotb = wait_bounded(eb_bar + 8u * b, (eph >> b) & 1u, ctl, p.err, 6);
-          if (!__all_sync(0xffffffffu, gotb)) {
-            eok = false;
-            break;
-          }
-          eph ^= 1u << b;
-          epend &= ~(1u << b);
-          const float4 *brow = reinterpret_cast<const float4 *>(ebuf + b * kEpiBoxBytes + lane * 128);
-          const int n0c = nc * p.NC + 32 * ci;
 #pragma unroll
           for (int q = 0; q < 8; ++q) {
-            const float4 bq = brow[q ^ (lane & 7)];
-            const float bj[4] = {bq.x, bq.y, bq.z, bq.w};
+            const int c = 32 * (ci + 1) + 4 * q;
+            nxt[q] = (valid && ci + 1 < nchk && c < ncol) ? __ldg(reinterpret_cast<const float4 *>(brow + c))
+                                                        : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+          float v[32];
+          tmem_ld32(lane_addr + static_cast<uint32_t>(32 * ci), v);
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int j = 4 * q + e;
-              if (valid && 32 * ci + j < p.NC && n0c + j < p.r) dot = fmaf(bj[e], v[j], dot);
-            }
+          for (int q = 0; q < 8; ++q) {
+            dot = fmaf(cur[q].x, v[4 * q], dot);
+            dot = fmaf(cur[q].y, v[4 * q + 1], dot);
+            dot = fmaf(cur[q].z, v[4 * q + 2], dot);
+            dot = fmaf(cur[q].w, v[4 * q + 3], dot);
           }
-          __syncwarp();
-          if (lane == 0 && ci + 2 < nchk) {
-            mbar_expect_tx(eb_bar + 8u * b, kEpiBoxBytes);
-            tma_load_2d(smem_u32(ebuf + b * kEpiBoxBytes), &mBe, n0c + 64, ybase, eb_bar + 8u * b);
-            epend |= 1u << b;
-          }
-        }
-        if (!eok) {
-          // drain this warp's epilogue copies still in flight, then leave
-          if (lane == 0) {
-            for (int b = 0; b < 2; ++b)
-              if ((epend >> b) & 1u) wait_drain(eb_bar + 8u * b, (eph >> b) & 1u);
-          }
-          ok = false;
-          break;
+#pragma unroll
+          for (int q = 0; q < 8; ++q) cur[q] = nxt[q];
         }
         float2 *part2 = reinterpret_cast<float2 *>(p.part);
         if (valid) part2[(tm * p.maxseg + seg) * kBM + row] = make_float2(n0, dot);
@@ -967,8 +950,7 @@ bool plan_gemm(int mode, int M, int64_t in, int r, int csize, int max_clusters, 
   // correction tiles
   p.stage_bytes = static_cast<unsigned>(kBM * row_bytes + 2 * p.NT * row_bytes);
   p.tx_bytes = p.stage_bytes;
-  const int epi = mode == kNorm ? kEpiBytes : 0;
-  p.stages = static_cast<int>((kSmemMax - 1024 - epi - 512) / p.stage_bytes);
+  p.stages = static_cast<int>((kSmemMax - 1024 - 512) / p.stage_bytes);
   if (p.stages > kMaxStages) p.stages = kMaxStages;
   if (p.stages > (512 - acc_cols) / slot_cols) p.stages = (512 - acc_cols) / slot_cols;
   if (p.stages < 2) return false;
@@ -989,7 +971,7 @@ bool plan_gemm(int mode, int M, int64_t in, int r, int csize, int max_clusters, 
   p.r = r;
   const size_t per_row = mode == kGram ? static_cast<size_t>(p.NC) : 2;
   gp->part_bytes = static_cast<size_t>(ngroups) * csize * p.nchunks * p.maxseg * kBM * per_row * sizeof(float);
-  gp->smem_bytes = static_cast<size_t>(p.stages) * p.stage_bytes + epi + 1024 /*align*/ + 8 * (3 * p.stages + 3 + 8) + 64;
+  gp->smem_bytes = static_cast<size_t>(p.stages) * p.stage_bytes + 1024 /*align*/ + 8 * (3 * p.stages + 3) + 64;
   // tensor memory: a CTA holding 512 columns must be alone on its SM
   if (p.tmem_cols > 256 && gp->smem_bytes < 116 * 1024) gp->smem_bytes = 116 * 1024;
   return true;
@@ -1077,7 +1059,7 @@ int grid_for(long long n, int sms) {
 
 cudaError_t launch_gemm(const GemmPlan &gp, cudaStream_t cs, const CUtensorMap &x1, const CUtensorMap &x2,
                         const CUtensorMap &y1h, const CUtensorMap &y1c, const CUtensorMap &y2h,
-                        const CUtensorMap &y2c, const CUtensorMap &be) {
+                        const CUtensorMap &y2c) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(gp.p.ctas));
   cfg.blockDim = dim3(kThreads);
@@ -1090,8 +1072,8 @@ cudaError_t launch_gemm(const GemmPlan &gp, cudaStream_t cs, const CUtensorMap &
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (gp.bk == kBKWide) return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<kBKWide>, x1, x2, y1h, y1c, y2h, y2c, be, gp.p);
-  return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<kBKNarrow>, x1, x2, y1h, y1c, y2h, y2c, be, gp.p);
+  if (gp.bk == kBKWide) return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<kBKWide>, x1, x2, y1h, y1c, y2h, y2c, gp.p);
+  return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<kBKNarrow>, x1, x2, y1h, y1c, y2h, y2c, gp.p);
 }
 
 // Cluster shape of the norm pass.  Sharing the N-side tile pays only when it
@@ -1267,7 +1249,7 @@ extern "C" dora_status dora_norm_factored(const float *W0, const float *A, const
 
   // tensor maps
   // the N-side boxes of the two passes may differ in height: one map set each
-  CUtensorMap mA, mAh_g, mAc_g, mAh_n, mAc_n, mW0, mB, mGh, mGc, mBe;
+  CUtensorMap mA, mAh_g, mAc_g, mAh_n, mAc_n, mW0, mB, mGh, mGc;
   const int nbox = gn.p.nbox;
   // box rows are one K block: gg.bk / gn.bk fp32 (the same bytes of bf16)
   const int rbg = 4 * gg.bk, rbn = 4 * gn.bk;
@@ -1277,8 +1259,7 @@ extern "C" dora_status dora_norm_factored(const float *W0, const float *A, const
             make_map(&mAc_n, a_c, true, r, 2 * in8, 2 * in8, nbox, rbn) &&
             make_map(&mW0, W0, false, out, in, in, kBM, rbn) && make_map(&mB, Bk, false, out, ldb, ldb, kBM, rbn) &&
             make_map(&mGh, g_hi, false, npad, npad, npad, nbox, rbn) &&
-            make_map(&mGc, g_c, true, npad, 2 * npad, 2 * npad, nbox, rbn) &&
-            make_map(&mBe, Bk, false, out, ldb, ldb, 32, 128);
+            make_map(&mGc, g_c, true, npad, 2 * npad, 2 * npad, nbox, rbn);
   if (!ok) {
     dora::count_launches(launches);
     return DORA_ERR_CUDA;
@@ -1287,7 +1268,7 @@ extern "C" dora_status dora_norm_factored(const float *W0, const float *A, const
   // 2. Gram partial tiles
   gg.p.part = part_g;
   gg.p.err = errp;
-  if (launch_gemm(gg, cs, mA, mA, mAh_g, mAc_g, mAh_g, mAc_g, mA) != cudaSuccess) {
+  if (launch_gemm(gg, cs, mA, mA, mAh_g, mAc_g, mAh_g, mAc_g) != cudaSuccess) {
     dora::count_launches(launches);
     return DORA_ERR_CUDA;
   }
@@ -1311,7 +1292,9 @@ extern "C" dora_status dora_norm_factored(const float *W0, const float *A, const
   gn.p.norm = norm;
   gn.p.g = g;
   gn.p.two_s = 2.0f * s;
-  if (launch_gemm(gn, cs, mW0, mB, mAh_n, mAc_n, mGh, mGc, mBe) != cudaSuccess) {
+  gn.p.Bk = Bk;
+  gn.p.ldb = static_cast<int>(ldb);
+  if (launch_gemm(gn, cs, mW0, mB, mAh_n, mAc_n, mGh, mGc) != cudaSuccess) {
     dora::count_launches(launches);
     return DORA_ERR_CUDA;
   }

@@ -82,6 +82,7 @@ constexpr int kMaxChunkN = 384;     // largest N handled by one CTA pass
 constexpr int kMaxR = 1024;
 constexpr int kMaxCtas = 256;       // workspace bound: any device up to this size
 constexpr int kMaxCluster = 2;      // largest cluster of the norm pass (4 measured slower)
+constexpr int kMinClusterN = 256;   // narrowest N chunk whose N-side tile the cluster shares
 constexpr int kMinUnitsNorm = 4;
 constexpr int kMinUnitsGram = 16;
 constexpr int kSmemMax = 232448;           // 227 KB: the opt-in maximum per CTA
@@ -1076,11 +1077,11 @@ cudaError_t launch_gemm(const GemmPlan &gp, cudaStream_t cs, const CUtensorMap &
   return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<kBKNarrow>, x1, x2, y1h, y1c, y2h, y2c, gp.p);
 }
 
-// Cluster shape of the norm pass.  Sharing the N-side tile pays only when it
-// is large (a full 384-wide chunk: 48 KB per K block); then take the largest
-// cluster (up to kMaxCluster) whose co-resident clusters still cover all but a
-// few SMs.  Otherwise single CTAs.  Occupancy answers are cached per device and
-// shared-memory size.
+// Cluster shape of the norm pass.  Sharing the N-side tile pays when it is
+// large (chunks of at least kMinClusterN: 32 KB or more per K block); then take
+// the largest cluster (up to kMaxCluster) whose co-resident clusters still
+// cover all but a few SMs.  Otherwise single CTAs.  Occupancy answers are
+// cached per device and shared-memory size.
 void choose_cluster(int device, int sms, int64_t out, int64_t in, int64_t r, int *csize, int *max_clusters) {
   static std::mutex mu;
   struct Entry {
@@ -1094,7 +1095,7 @@ void choose_cluster(int device, int sms, int64_t out, int64_t in, int64_t r, int
   *max_clusters = sms;
   int npad, nchunks, NC;
   plan_n(static_cast<int>(r), &npad, &nchunks, &NC);
-  if (NC < kMaxChunkN) return;
+  if (NC < kMinClusterN) return;
   for (int c = kMaxCluster; c >= 2; c /= 2) {
     GemmPlan gp;
     if (!plan_gemm(kNorm, static_cast<int>(out), in, static_cast<int>(r), c, sms / c, &gp)) continue;

@@ -72,8 +72,10 @@ namespace {
 constexpr int kBM = 128;            // rows per M tile (= tensor-memory lanes)
 // fp32 per K block: 16 (64-byte rows, 64-byte swizzle) or 32 (128-byte rows,
 // 128-byte swizzle).  The wider block is taken where the stage still fits
-// three times into shared memory (N chunks up to kMaxChunkWide): DRAM streams
-// W0 markedly faster through 128-byte box rows than through 64-byte ones.
+// several times into shared memory (N chunks up to kMaxChunkWide): TMA streams
+// a large matrix from HBM faster through 128-byte box rows than through
+// 64-byte ones (measured 4.5 vs 3.8 TB/s on GB300), and each stage carries
+// twice the work per barrier round trip.
 constexpr int kBKNarrow = 16;
 constexpr int kBKWide = 32;
 constexpr int kMaxChunkWide = 128;

@@ -1,0 +1,112 @@
+"""torch.library registration of the DoRA hot path (integration only).
+
+Three custom ops; each allocates its outputs (and the library's workspace)
+with torch and calls the C entry point of the same name on the current CUDA
+stream.  No arithmetic happens here:
+
+  torch.ops.dora.norm_factored(W0, A, B, m, s) -> (norm, g)
+  torch.ops.dora.compose(base, lora, m, g, norm, s) -> y
+  torch.ops.dora.compose_bwd(dy, base, lora, g, norm, s) -> (d_base, d_lora, d_mag)
+
+``compose`` is differentiable in base, lora and m.  It takes m beside g (the
+norm op's output g = m / norm) so that autograd can deliver dL/dm: with the
+row norm treated as a constant in the backward (the method's page,
+"人工智能训练新突破：Anthropic团队破解大模型微调内存瓶颈难题", says nothing about a
+gradient through the norm; this is the reading the library follows),
+dL/dm_j = sum_t dy_tj (base_tj + s lora_tj) / norm_j, which is exactly the
+library's d_mag, and dL/dbase = g dy, dL/dlora = s g dy are its d_base and
+d_lora.  The backward is therefore one call of dora_compose_bwd.
+
+Inputs must be contiguous, row-major and on one CUDA device (the C ABI's
+layout); weights and m are float32, activations float32 or bfloat16.
+"""
+from __future__ import annotations
+
+import torch
+from torch import Tensor
+
+from . import (dora_compose_bwd, dora_compose_bwd_workspace, dora_compose_fwd, dora_norm_factored,
+               dora_norm_factored_workspace)
+
+__all__ = ["norm_factored", "compose", "compose_bwd", "dora_module"]
+
+
+def _contig(name: str, *ts: Tensor) -> None:
+    for t in ts:
+        if not t.is_contiguous():
+            raise ValueError(f"dora::{name}: inputs must be contiguous (row-major)")
+
+
+@torch.library.custom_op("dora::norm_factored", mutates_args=(), device_types="cuda")
+def norm_factored(W0: Tensor, A: Tensor, B: Tensor, m: Tensor, s: float) -> tuple[Tensor, Tensor]:
+    """n_i = ||W0_i + s (B A)_i|| (factored: base + cross + Gram terms) and g = m / n."""
+    _contig("norm_factored", W0, A, B, m)
+    out, inp = W0.shape
+    r = A.shape[0]
+    norm = torch.empty(out, device=W0.device, dtype=torch.float32)
+    g = torch.empty_like(norm)
+    ws = torch.empty(max(dora_norm_factored_workspace(out, inp, r), 1), dtype=torch.uint8, device=W0.device)
+    dora_norm_factored(W0, A, B, m, s, norm, g, ws)
+    return norm, g
+
+
+@norm_factored.register_fake
+def _norm_factored_fake(W0, A, B, m, s):
+    out = W0.shape[0]
+    return W0.new_empty(out, dtype=torch.float32), W0.new_empty(out, dtype=torch.float32)
+
+
+@torch.library.custom_op("dora::compose_bwd", mutates_args=(), device_types="cuda")
+def compose_bwd(dy: Tensor, base: Tensor, lora: Tensor, g: Tensor, norm: Tensor,
+                s: float) -> tuple[Tensor, Tensor, Tensor]:
+    """d_base = g dy, d_lora = s g dy, d_mag = sum_t dy (base + s lora) / norm."""
+    _contig("compose_bwd", dy, base, lora, g, norm)
+    T, out = dy.shape
+    d_base = torch.empty_like(dy)
+    d_lora = torch.empty_like(dy)
+    d_mag = torch.empty(out, device=dy.device, dtype=torch.float32)
+    ws = torch.empty(max(dora_compose_bwd_workspace(T, out), 1), dtype=torch.uint8, device=dy.device)
+    dora_compose_bwd(dy, base, lora, g, norm, s, d_base, d_lora, d_mag, ws)
+    return d_base, d_lora, d_mag
+
+
+@compose_bwd.register_fake
+def _compose_bwd_fake(dy, base, lora, g, norm, s):
+    return torch.empty_like(dy), torch.empty_like(dy), dy.new_empty(dy.shape[1], dtype=torch.float32)
+
+
+@torch.library.custom_op("dora::compose", mutates_args=(), device_types="cuda")
+def compose(base: Tensor, lora: Tensor, m: Tensor, g: Tensor, norm: Tensor, s: float) -> Tensor:
+    """y = base + (g - 1) base + g s lora (fp32 inside, one rounding to the activation dtype)."""
+    _contig("compose", base, lora, g)
+    y = torch.empty_like(base)
+    dora_compose_fwd(base, lora, g, s, y)
+    return y
+
+
+@compose.register_fake
+def _compose_fake(base, lora, m, g, norm, s):
+    return torch.empty_like(base)
+
+
+def _compose_setup(ctx, inputs, output):
+    base, lora, m, g, norm, s = inputs
+    ctx.save_for_backward(base, lora, g, norm)
+    ctx.s = s
+
+
+def _compose_backward(ctx, dy):
+    base, lora, g, norm = ctx.saved_tensors
+    d_base, d_lora, d_mag = compose_bwd(dy.contiguous(), base, lora, g, norm, ctx.s)
+    return d_base, d_lora, d_mag, None, None, None
+
+
+compose.register_autograd(_compose_backward, setup_context=_compose_setup)
+
+
+def dora_module(base: Tensor, lora: Tensor, W0: Tensor, A: Tensor, B: Tensor, m: Tensor, s: float) -> Tensor:
+    """One DoRA module's output from its two matmul results: the factored norm
+    (no gradient through it) and the fused compose, differentiable in base,
+    lora and m."""
+    norm, g = norm_factored(W0.detach(), A.detach(), B.detach(), m.detach(), s)
+    return compose(base, lora, m, g, norm, s)

@@ -1,0 +1,59 @@
+"""The torch.library ops and their autograd give bitwise the results of the
+direct C-ABI calls (they only allocate and call the library)."""
+import numpy as np
+import pytest
+import torch
+
+import parameter_efficient_fine_gb300.ops as ops
+from parameter_efficient_fine_gb300 import workloads as wl
+
+from gpu_util import act_to_dev, assert_no_device_error, f32_dev, run_bwd, run_fwd, run_norm
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("act", ["bf16", "f32"])
+def test_ops_match_direct_calls_and_autograd(act):
+    sh = wl.shape("high_rank", out=264, inp=384, r=40, T=96)
+    d = wl.make_module(sh, 4242)
+    s = d["s"]
+    W0, A, B, m = (f32_dev(d[k]) for k in ("W0", "A", "B", "m"))
+    if act == "bf16":
+        base, lora, dy = (act_to_dev(d[k]) for k in ("base", "lora", "dy"))
+    else:
+        rng = np.random.default_rng(5)
+        base, lora, dy = (f32_dev(rng.standard_normal((sh.T, sh.out)).astype(np.float32)) for _ in range(3))
+
+    norm_d, g_d = run_norm(W0, A, B, m, s)
+    norm_o, g_o = torch.ops.dora.norm_factored(W0, A, B, m, s)
+    assert torch.equal(norm_o, norm_d) and torch.equal(g_o, g_d)
+
+    y_d = run_fwd(base, lora, g_d, s)
+    db_d, dl_d, dm_d = run_bwd(dy, base, lora, g_d, norm_d, s)
+
+    base_a = base.clone().requires_grad_(True)
+    lora_a = lora.clone().requires_grad_(True)
+    m_a = m.clone().requires_grad_(True)
+    y_o = ops.dora_module(base_a, lora_a, W0, A, B, m_a, s)
+    assert torch.equal(y_o, y_d)
+    y_o.backward(dy)
+    assert torch.equal(base_a.grad, db_d)
+    assert torch.equal(lora_a.grad, dl_d)
+    assert torch.equal(m_a.grad, dm_d)
+    assert_no_device_error()
+
+
+def test_opcheck():
+    sh = wl.shape("high_rank", out=128, inp=64, r=8, T=32)
+    d = wl.make_module(sh, 77)
+    s = d["s"]
+    W0, A, B, m = (f32_dev(d[k]) for k in ("W0", "A", "B", "m"))
+    base, lora, dy = (act_to_dev(d[k]) for k in ("base", "lora", "dy"))
+    checks = ("test_schema", "test_autograd_registration", "test_faketensor")
+    torch.library.opcheck(torch.ops.dora.norm_factored.default, (W0, A, B, m, s), test_utils=checks)
+    norm, g = torch.ops.dora.norm_factored(W0, A, B, m, s)
+    base_a = base.clone().requires_grad_(True)
+    m_a = m.clone().requires_grad_(True)
+    torch.library.opcheck(torch.ops.dora.compose.default, (base_a, lora, m_a, g, norm, s), test_utils=checks)
+    torch.library.opcheck(torch.ops.dora.compose_bwd.default, (dy, base, lora, g, norm, s), test_utils=checks)
+    assert_no_device_error()

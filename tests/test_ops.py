@@ -1,0 +1,26 @@
+"""torch.library registration of the hot path: the ops exist and their fake
+(shape) implementations propagate shapes and dtypes without a GPU."""
+import pytest
+
+torch = pytest.importorskip("torch")
+
+
+def test_ops_registered_and_fake_shapes():
+    from torch._subclasses.fake_tensor import FakeTensorMode
+
+    import parameter_efficient_fine_gb300.ops  # noqa: F401  (registers torch.ops.dora.*)
+
+    for name in ("norm_factored", "compose", "compose_bwd"):
+        assert hasattr(torch.ops.dora, name)
+    with FakeTensorMode():
+        W0 = torch.empty(64, 32, device="cuda")
+        A = torch.empty(4, 32, device="cuda")
+        B = torch.empty(64, 4, device="cuda")
+        m = torch.empty(64, device="cuda")
+        n, g = torch.ops.dora.norm_factored(W0, A, B, m, 1.0)
+        assert n.shape == (64,) and g.shape == (64,) and n.dtype == torch.float32
+        base = torch.empty(8, 64, device="cuda", dtype=torch.bfloat16)
+        y = torch.ops.dora.compose(base, base, m, g, n, 1.0)
+        assert y.shape == base.shape and y.dtype == torch.bfloat16
+        db, dl, dm = torch.ops.dora.compose_bwd(base, base, base, g, n, 1.0)
+        assert db.shape == base.shape and dl.dtype == torch.bfloat16 and dm.shape == (64,) and dm.dtype == torch.float32

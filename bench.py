@@ -501,6 +501,32 @@ def run_report(args):
                   flush=True)
             del W0, A, B, m, act, base, lora, dy, ws, y, db, dl
             torch.cuda.empty_cache()
+    elif args.report == "bf16_norm":
+        # the factored norm with bf16 W0, A, B (the same seeded weights rounded
+        # to bf16) at out = in = 8192 over the swept ranks; the row norms of W0
+        # are computed once (W0 is frozen) and timed separately
+        for k, r in enumerate(sorted(wl.RANK_SWEEP + (384,))):
+            sh = wl.shape("rank_sweep", r=r)
+            W0, A, B, m = _device_module(sh, wl.seed_for("rank_sweep", k), dev)
+            W0, A, B = W0.bfloat16(), A.bfloat16(), B.bfloat16()
+            n0 = torch.empty(sh.out, device=dev)
+            norm = torch.empty(sh.out, device=dev)
+            g = torch.empty(sh.out, device=dev)
+            nbytes = dora.dora_norm_factored_bf16_workspace(sh.out, sh.inp, sh.r)
+            ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+            t_row = _time_ms(lambda: dora.dora_row_sumsq_bf16(W0, n0, stream), 20, stream)
+            t_norm = _time_ms(lambda: dora.dora_norm_factored_bf16(W0, A, B, m, n0, sh.s, norm, g, ws, stream), 20,
+                              stream)
+            alg = algorithmic(sh)
+            w_bytes = sh.out * sh.inp * 2
+            print(json.dumps({"report": "bf16_norm", "r": r, "out": sh.out, "in": sh.inp,
+                              "norm_us": t_norm * 1e3,
+                              "norm_tflops_algorithmic": alg["norm_flops"] / (t_norm * 1e-3) / 1e12,
+                              "row_sumsq_us": t_row * 1e3, "row_sumsq_gbs": w_bytes / (t_row * 1e-3) / 1e9,
+                              "w0_stream_gbs_in_norm": w_bytes / (t_norm * 1e-3) / 1e9,
+                              "norm_transient_bytes": nbytes}), flush=True)
+            del W0, A, B, m, ws
+            torch.cuda.empty_cache()
     elif args.report == "mlp_stack":
         # 32 gate/up (4096 -> 14336) + 32 down (14336 -> 4096) modules, r = 512,
         # T = 16384, training step per module (norm + fwd + bwd), independent seeds
@@ -553,7 +579,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--report", choices=["rank_sweep", "mlp_stack"], default=None,
+    ap.add_argument("--report", choices=["rank_sweep", "mlp_stack", "bf16_norm"], default=None,
                     help="extra per-workload report lines instead of the bench line")
     args = ap.parse_args()
     rank = int(os.environ.get("RANK", "0"))

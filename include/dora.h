@@ -108,6 +108,52 @@ dora_status dora_norm_factored(const float *W0, const float *A, const float *B,
                                dora_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
+/* (a') the same norm for bf16 weights                                       */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * n0sq[i] = sum_j W0[i,j]^2 for a bfloat16 W0 [rows, cols], fp32 result in a
+ * fixed summation order.  W0 is frozen during fine-tuning, so its row norms
+ * are computed once and passed to every dora_norm_factored_bf16 call (the
+ * base term of P1 ¶第一个创新是"因式分解规范化"技术).
+ *   W0    bfloat16 [rows, cols]  16-byte aligned, cols % 8 == 0
+ *   n0sq  float32 [rows]         4-byte aligned
+ *   Sizes: rows >= 0 (0 is a no-op), cols >= 1, both < 2^31.
+ */
+dora_status dora_row_sumsq_bf16(const void *W0, int64_t rows, int64_t cols, float *n0sq,
+                                dora_stream_t stream);
+
+/* Bytes of workspace dora_norm_factored_bf16 needs (host arithmetic; 0 for an
+ * invalid shape).  O(out + (out + r) r) bytes: s/2 G in three bf16 pieces,
+ * partial sums, and B padded to a 16-byte row when r % 8 != 0. */
+size_t dora_norm_factored_bf16_workspace(int64_t out, int64_t in, int64_t r);
+
+/*
+ * The factored norm of dora_norm_factored for bfloat16 W0, A and B (the same
+ * definition, P1 ¶第一个创新是"因式分解规范化"技术), with the base term taken from
+ * n0sq:
+ *     n_i^2 = n0sq[i] + 2 s <U_i, B_i> + s^2 B_i G B_i^T,   g_i = m_i / n_i.
+ * Products of bf16 values are exact in fp32, so U = W0 A^T and G = A A^T are
+ * single bf16 tensor-core products with fp32 accumulation; s/2 G enters as three
+ * bf16 pieces whose sum carries it to fp32 precision.  No adapter or weight is
+ * converted or copied (B only when r % 8 != 0).
+ *
+ *   W0    bfloat16 [out, in]   16-byte aligned, in % 8 == 0
+ *   A     bfloat16 [r, in]     16-byte aligned
+ *   B     bfloat16 [out, r]    16-byte aligned (any r >= 1)
+ *   m     float32 [out]        4-byte aligned
+ *   n0sq  float32 [out]        ||W0_i||^2 (dora_row_sumsq_bf16), 4-byte aligned
+ *   s, norm, g, workspace, sizes: as dora_norm_factored (workspace from
+ *   dora_norm_factored_bf16_workspace).
+ */
+dora_status dora_norm_factored_bf16(const void *W0, const void *A, const void *B,
+                                    const float *m, const float *n0sq, float s,
+                                    int64_t out, int64_t in, int64_t r,
+                                    float *norm, float *g,
+                                    void *workspace, size_t workspace_bytes,
+                                    dora_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
 /* (b) fused compose, forward                                                */
 /* ------------------------------------------------------------------------ */
 

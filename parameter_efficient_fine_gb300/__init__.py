@@ -18,6 +18,9 @@ __all__ = [
     "dora_status_str",
     "dora_norm_factored_workspace",
     "dora_norm_factored",
+    "dora_row_sumsq_bf16",
+    "dora_norm_factored_bf16_workspace",
+    "dora_norm_factored_bf16",
     "dora_compose_fwd",
     "dora_compose_bwd_workspace",
     "dora_compose_bwd",
@@ -46,6 +49,9 @@ _SIGNATURES = {
     "dora_status_str": (ctypes.c_char_p, [_int]),
     "dora_norm_factored_workspace": (_sz, [_i64, _i64, _i64]),
     "dora_norm_factored": (_int, [_vp, _vp, _vp, _vp, _f32, _i64, _i64, _i64, _vp, _vp, _vp, _sz, _vp]),
+    "dora_row_sumsq_bf16": (_int, [_vp, _i64, _i64, _vp, _vp]),
+    "dora_norm_factored_bf16_workspace": (_sz, [_i64, _i64, _i64]),
+    "dora_norm_factored_bf16": (_int, [_vp, _vp, _vp, _vp, _vp, _f32, _i64, _i64, _i64, _vp, _vp, _vp, _sz, _vp]),
     "dora_compose_fwd": (_int, [_int, _vp, _vp, _vp, _f32, _i64, _i64, _vp, _vp]),
     "dora_compose_bwd_workspace": (_sz, [_i64, _i64]),
     "dora_compose_bwd": (_int, [_int, _vp, _vp, _vp, _vp, _vp, _f32, _i64, _i64, _vp, _vp, _vp, _vp, _sz, _vp]),
@@ -130,6 +136,27 @@ def dora_norm_factored(W0, A, B, m, s: float, norm, g, workspace, stream=None) -
         _ptr(W0), _ptr(A), _ptr(B), _ptr(m), float(s), out, inp, r, _ptr(norm), _ptr(g),
         _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
     _check("dora_norm_factored", st)
+
+
+def dora_row_sumsq_bf16(W0, n0sq, stream=None) -> None:
+    """n0sq[i] = sum_j W0[i, j]^2 for a bfloat16 W0 (see include/dora.h)."""
+    rows, cols = W0.shape
+    _check("dora_row_sumsq_bf16",
+           load_library().dora_row_sumsq_bf16(_ptr(W0), rows, cols, _ptr(n0sq), _stream(stream)))
+
+
+def dora_norm_factored_bf16_workspace(out: int, inp: int, r: int) -> int:
+    return int(load_library().dora_norm_factored_bf16_workspace(out, inp, r))
+
+
+def dora_norm_factored_bf16(W0, A, B, m, n0sq, s: float, norm, g, workspace, stream=None) -> None:
+    """dora_norm_factored for bfloat16 W0, A, B with the base term from n0sq (see include/dora.h)."""
+    out, inp = W0.shape
+    r = A.shape[0]
+    st = load_library().dora_norm_factored_bf16(
+        _ptr(W0), _ptr(A), _ptr(B), _ptr(m), _ptr(n0sq), float(s), out, inp, r, _ptr(norm), _ptr(g),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
+    _check("dora_norm_factored_bf16", st)
 
 
 def dora_compose_fwd(base, lora, g, s: float, y, stream=None) -> None:

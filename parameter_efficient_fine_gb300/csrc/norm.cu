@@ -896,6 +896,433 @@ __global__ void __launch_bounds__(256) gram_reduce_kernel(const float *__restric
 }
 
 // ---------------------------------------------------------------------------
+// bf16 weights: W0, A, B in bf16 make every product exact in fp32, so the
+// contraction is one kind::f16 MMA per 16 K indices with both operands taken
+// from shared memory as TMA delivers them (no split, no converter warps).  The
+// Gram part of the fold needs s/2 G at fp32 precision: it is split into three
+// bf16 pieces h1 + h2 + h3 (each the bf16 rounding of what is left) laid side by
+// side along K, against B repeated three times.  ||W0_i||^2 is an input (W0 is
+// frozen during fine-tuning, so its row norms are computed once).
+// ---------------------------------------------------------------------------
+struct Tc16Params {
+  int mode;
+  int M;            // valid M-side rows (out, or r for the Gram pass)
+  int kb1;          // K blocks over in (W0 or A columns)
+  int kbr;          // K blocks over r (one piece of the Gram part)
+  int rs;           // column stride of the pieces of s/2 G (r rounded up to 8)
+  int kbtot;        // kb1 + 3 * kbr (NORM) or kb1 (GRAM)
+  int nchunks, sym, NC;
+  int nbox, nb, sl, NT;
+  int nmma0, nmma1;
+  int tmem_cols;
+  int stages;
+  int tiles;
+  long long units;
+  int ctas, ncl, maxseg;
+  unsigned stage_bytes, x_bytes;
+  float *part;
+  int r;
+  int *err;
+  int *cnt;
+  const float *m;
+  const float *n0sq;                 // ||W0_i||^2, fp32 [M]
+  float *norm, *g;
+  float two_s;
+  const __nv_bfloat16 *Bk;           // B [M, ldb] bf16 (the epilogue reads its rows)
+  int ldb;
+};
+
+__device__ __forceinline__ void mma_bf16_ss(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc)
+      : "memory");
+}
+
+// BKE bf16 per K block: 32 (64-byte rows, 64-byte swizzle) or 64 (128-byte rows,
+// 128-byte swizzle); the matching descriptor is sdesc<BKE / 2>.
+template <int BKE>
+__global__ void __launch_bounds__(kThreads, 1)
+tc16_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ CUtensorMap mX2,
+            const __grid_constant__ CUtensorMap mY1, const __grid_constant__ CUtensorMap mY2, const Tc16Params p) {
+  constexpr int kRowBytes = BKE * 2;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int S = p.stages;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + static_cast<size_t>(S) * p.stage_bytes);
+  // barrier layout: full[S], empty[S], accf, acce, fin
+  SharedCtl *ctl = reinterpret_cast<SharedCtl *>(bars + 2 * S + 3);
+  const uint32_t full0 = smem_u32(bars);
+  const uint32_t empty0 = full0 + 8u * S;
+  const uint32_t accf = empty0 + 8u * S;
+  const uint32_t acce = accf + 8;
+  const uint32_t fin = acce + 8;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full0 + 8u * s, 1);
+      mbar_init(empty0 + 8u * s, 1);
+    }
+    mbar_init(accf, 1);
+    mbar_init(acce, 4);
+    mbar_init(fin, 1);
+    ctl->abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_map(&mX1);
+    prefetch_map(&mY1);
+    if (p.kbtot > p.kb1) {
+      prefetch_map(&mX2);
+      prefetch_map(&mY2);
+    }
+  }
+  if (warp == 1) {
+    __syncwarp();
+    tmem_alloc(smem_u32(&ctl->tmem_base), static_cast<uint32_t>(p.tmem_cols));
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl->tmem_base;
+  const int cl = static_cast<int>(blockIdx.x);
+  const long long u_begin = unit_begin(cl, p.units, p.ncl);
+  const long long u_end = unit_begin(cl + 1, p.units, p.ncl);
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ producer
+      int stage = 0;
+      uint32_t phase = 0;
+      int issued = 0;
+      bool ok = *reinterpret_cast<volatile int *>(&g_dora_stall) == 0;
+      for (long long u = u_begin; u < u_end && ok;) {
+        const int t = static_cast<int>(u / p.kbtot);
+        const int kb0 = static_cast<int>(u - static_cast<long long>(t) * p.kbtot);
+        const int kbe = static_cast<int>(min(static_cast<long long>(p.kbtot), kb0 + (u_end - u)));
+        int mt, nc;
+        tile_coords(t, p.nchunks, p.sym, 1, 0, &mt, &nc);
+        for (int kb = kb0; kb < kbe; ++kb) {
+          if (!wait_bounded(empty0 + 8u * stage, phase ^ 1u, ctl, p.err, 1)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = full0 + 8u * stage;
+          mbar_expect_tx(fb, p.stage_bytes);
+          const uint32_t xs = smem_u32(smem + static_cast<size_t>(stage) * p.stage_bytes);
+          const uint32_t ys = xs + p.x_bytes;
+          if (kb < p.kb1) {
+            const int kx = kb * BKE;
+            tma_load_2d(xs, &mX1, kx, mt * kBM, fb);
+            for (int i = 0; i < p.nb; ++i)
+              tma_load_2d(ys + static_cast<uint32_t>(i * p.nbox * kRowBytes), &mY1, kx, nc * p.NC + i * p.nbox, fb);
+          } else {
+            // Gram part: K block kb2 of B (repeated for each piece) against piece kb2 / kbr of s/2 G
+            const int kb2 = kb - p.kb1;
+            const int piece = kb2 / p.kbr, kc = (kb2 - piece * p.kbr) * BKE;
+            tma_load_2d(xs, &mX2, kc, mt * kBM, fb);
+            for (int i = 0; i < p.nb; ++i)
+              tma_load_2d(ys + static_cast<uint32_t>(i * p.nbox * kRowBytes), &mY2, piece * p.rs + kc,
+                          nc * p.NC + i * p.nbox, fb);
+          }
+          ++issued;
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        u += kbe - kb0;
+      }
+      if (!ok) {
+        int st = stage;
+        uint32_t ph = phase;
+        for (int k = 0; k < S && k < issued; ++k) {
+          if (--st < 0) {
+            st = S - 1;
+            ph ^= 1u;
+          }
+          wait_drain(full0 + 8u * st, ph);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ MMA issuer
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t aphase = 0;
+      bool ok = true;
+      const uint32_t ic0 = idesc_bf16(p.nmma0);
+      const uint32_t ic1 = p.nmma1 > 0 ? idesc_bf16(p.nmma1) : 0u;
+      for (long long u = u_begin; u < u_end && ok;) {
+        const int t = static_cast<int>(u / p.kbtot);
+        const int kb0 = static_cast<int>(u - static_cast<long long>(t) * p.kbtot);
+        const int kbe = static_cast<int>(min(static_cast<long long>(p.kbtot), kb0 + (u_end - u)));
+        if (!wait_bounded(acce, aphase ^ 1u, ctl, p.err, 3)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        for (int kb = kb0; kb < kbe; ++kb) {
+          if (!wait_bounded(full0 + 8u * stage, phase, ctl, p.err, 2)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t xs = smem_u32(smem + static_cast<size_t>(stage) * p.stage_bytes);
+          const uint32_t ys = xs + p.x_bytes;
+#pragma unroll
+          for (int k = 0; k < BKE / 16; ++k) {
+            const uint32_t acc0 = (kb != kb0 || k != 0) ? 1u : 0u;
+            const uint32_t ko = static_cast<uint32_t>(k) * 32u;   // 16 bf16
+            const uint64_t a = sdesc<BKE / 2>(xs + ko);
+            mma_bf16_ss(tmem, a, sdesc<BKE / 2>(ys + ko), ic0, acc0);
+            if (p.nmma1 > 0) mma_bf16_ss(tmem + 256u, a, sdesc<BKE / 2>(ys + 256u * kRowBytes + ko), ic1, acc0);
+          }
+          mma_commit(empty0 + 8u * stage);
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        mma_commit(accf);
+        aphase ^= 1u;
+        u += kbe - kb0;
+      }
+      mma_commit(fin);
+      wait_drain(fin, 0);
+    }
+  } else if (warp >= 2 && warp <= 5) {
+    // ---------------------------------------------------------------- epilogue
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+    uint32_t aphase = 0;
+    bool ok = true;
+    for (long long u = u_begin; u < u_end && ok;) {
+      const int t = static_cast<int>(u / p.kbtot);
+      const int kb0 = static_cast<int>(u - static_cast<long long>(t) * p.kbtot);
+      const int kbe = static_cast<int>(min(static_cast<long long>(p.kbtot), kb0 + (u_end - u)));
+      int mt, nc;
+      tile_coords(t, p.nchunks, p.sym, 1, 0, &mt, &nc);
+      const size_t tm = static_cast<size_t>(mt) * p.nchunks + nc;
+      if (p.mode == kNorm && lane == 0) {
+        const int r0 = mt * kBM + quad * 32;
+        const int nr = min(32, p.M - r0);
+        if (nr > 0)
+          prefetch_l2(p.Bk + static_cast<size_t>(r0) * p.ldb, static_cast<uint32_t>(nr) * p.ldb * 2u);
+      }
+      const int grow = mt * kBM + row;
+      const bool valid = grow < p.M;
+      const int seg = cl - cta_of(static_cast<long long>(t) * p.kbtot, p.units, p.ncl);
+      const bool got = wait_bounded(accf, aphase, ctl, p.err, 5);
+      if (!__all_sync(0xffffffffu, got)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      if (p.mode == kNorm) {
+        // <B_i, D_i>: lane i reads row i of B (bf16, 8 per 128-bit load)
+        float dot = 0.0f;
+        const int nchk = (p.NC + 31) >> 5;
+        const int cbase = nc * p.NC;
+        const int ncol = min(p.NC, p.r - cbase);
+        const __nv_bfloat16 *brow = p.Bk + static_cast<size_t>(valid ? grow : 0) * p.ldb + cbase;
+        for (int ci = 0; ci < nchk; ++ci) {
+          uint4 bq[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int c = 32 * ci + 8 * q;
+            bq[q] = (valid && c < ncol) ? __ldg(reinterpret_cast<const uint4 *>(brow + c)) : make_uint4(0, 0, 0, 0);
+          }
+          float v[32];
+          tmem_ld32(lane_addr + static_cast<uint32_t>(32 * ci), v);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const uint32_t w[4] = {bq[q].x, bq[q].y, bq[q].z, bq[q].w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              dot = fmaf(__uint_as_float(w[e] << 16), v[8 * q + 2 * e], dot);
+              dot = fmaf(__uint_as_float(w[e] & 0xffff0000u), v[8 * q + 2 * e + 1], dot);
+            }
+          }
+        }
+        float2 *part2 = reinterpret_cast<float2 *>(p.part);
+        if (valid) part2[(tm * p.maxseg + seg) * kBM + row] = make_float2(0.0f, dot);
+        // the warp that writes the last records of its 32 rows finalises them:
+        // n_i = sqrt(max(0, ||W0_i||^2 + 2 s sum dot)), g_i = m_i / n_i
+        __threadfence();
+        __syncwarp();
+        int old = 0;
+        if (lane == 0) old = atomicAdd(p.cnt + mt * 4 + quad, 1);
+        old = __shfl_sync(0xffffffffu, old, 0);
+        int expect = 0;
+        for (int c = 0; c < p.nchunks; ++c) {
+          const long long ub = (static_cast<long long>(mt) * p.nchunks + c) * p.kbtot;
+          expect += cta_of(ub + p.kbtot - 1, p.units, p.ncl) - cta_of(ub, p.units, p.ncl) + 1;
+        }
+        if (old == expect - 1) {
+          __threadfence();
+          if (valid) {
+            float sd = 0.0f;
+            for (int c = 0; c < p.nchunks; ++c) {
+              const long long ub = (static_cast<long long>(mt) * p.nchunks + c) * p.kbtot;
+              const int nseg = cta_of(ub + p.kbtot - 1, p.units, p.ncl) - cta_of(ub, p.units, p.ncl) + 1;
+              const size_t tmc = static_cast<size_t>(mt) * p.nchunks + c;
+              for (int j = 0; j < nseg; ++j) sd += __ldcg(part2 + (tmc * p.maxseg + j) * kBM + row).y;
+            }
+            const float nn = sqrtf(fmaxf(fmaf(p.two_s, sd, p.n0sq[grow]), 0.0f));
+            p.norm[grow] = nn;
+            p.g[grow] = p.m[grow] / nn;
+          }
+        }
+      } else {
+        float *dst = p.part + ((tm * p.maxseg + seg) * kBM + row) * p.NC;
+        for (int c = 0; c < p.NC; c += 32) {
+          float v[32];
+          tmem_ld32(lane_addr + static_cast<uint32_t>(c), v);
+          if (valid) {
+#pragma unroll
+            for (int j = 0; j < 32; j += 4) {
+              if (c + j < p.NC) *reinterpret_cast<float4 *>(dst + c + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acce);
+      aphase ^= 1u;
+      u += kbe - kb0;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) {
+    __syncwarp();
+    tmem_dealloc(tmem, static_cast<uint32_t>(p.tmem_cols));
+  }
+}
+
+// ||W0_i||^2 of a bf16 [rows, cols] matrix (cols % 8 == 0): one warp per row,
+// lane-strided 128-bit loads, then a fixed shuffle tree
+__global__ void __launch_bounds__(256) row_sumsq_bf16_kernel(const __nv_bfloat16 *__restrict__ W, long long rows,
+                                                             int cols, float *__restrict__ out) {
+  const long long row = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= rows) return;
+  const uint4 *w = reinterpret_cast<const uint4 *>(W + row * cols);
+  float acc = 0.0f;
+  for (int i = lane; i < cols / 8; i += 32) {
+    const uint4 q = __ldcs(w + i);
+    const uint32_t v[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float lo = __uint_as_float(v[e] << 16), hi = __uint_as_float(v[e] & 0xffff0000u);
+      acc = fmaf(lo, lo, acc);
+      acc = fmaf(hi, hi, acc);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  if (lane == 0) out[row] = acc;
+}
+
+// B [rows, r] bf16 -> Bp [rows, rp] with zero columns r..rp-1
+__global__ void __launch_bounds__(256) pad_cols_bf16_kernel(const __nv_bfloat16 *__restrict__ B, long long rows, int r,
+                                                            int rp, __nv_bfloat16 *__restrict__ Bp) {
+  const long long n = rows * rp;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
+    const long long row = i / rp;
+    const int c = static_cast<int>(i - row * rp);
+    Bp[i] = c < r ? B[row * r + c] : __float2bfloat16_rn(0.0f);
+  }
+}
+
+// (s/2) G from the Gram partial tiles (as gram_reduce_kernel), written as three
+// bf16 pieces: g3[a][p * rs + b] for p = 0, 1, 2 with h1 = bf16(v),
+// h2 = bf16(v - h1), h3 = bf16(v - h1 - h2); zero outside r (every column
+// below rs is written).  Also zeroes the norm pass's ncnt completion counters.
+__device__ __forceinline__ void store_g3(int a, int b, float v, int npad, int rs, __nv_bfloat16 *g3) {
+  if (a >= npad || b >= rs) return;
+  const __nv_bfloat16 h1 = __float2bfloat16_rn(v);
+  const float r1 = v - __bfloat162float(h1);
+  const __nv_bfloat16 h2 = __float2bfloat16_rn(r1);
+  const __nv_bfloat16 h3 = __float2bfloat16_rn(r1 - __bfloat162float(h2));
+  __nv_bfloat16 *row = g3 + static_cast<long long>(a) * 3 * rs;
+  row[b] = h1;
+  row[rs + b] = h2;
+  row[2 * rs + b] = h3;
+}
+
+__global__ void __launch_bounds__(256) gram_reduce3_kernel(const float *__restrict__ part, StreamK sk, int nchunks,
+                                                           int NC, int r, int npad, int rs, float half_s,
+                                                           __nv_bfloat16 *__restrict__ g3, int *__restrict__ cnt,
+                                                           int ncnt) {
+  __shared__ float wsum[8][32][33];
+  if (blockIdx.x == 0 && blockIdx.y == 0)
+    for (int i = threadIdx.y * 32 + threadIdx.x; i < ncnt; i += 256) cnt[i] = 0;
+  const int t = blockIdx.x;
+  int mt, nc;
+  tile_coords(t, nchunks, 1, 1, 0, &mt, &nc);
+  const int nsub = (NC + 31) / 32;
+  const int sr = static_cast<int>(blockIdx.y) / nsub, sc = static_cast<int>(blockIdx.y) - sr * nsub;
+  const size_t tm = static_cast<size_t>(mt) * nchunks + nc;
+  const long long ub = static_cast<long long>(t) * sk.kbtot;
+  const int nseg = cta_of(ub + sk.kbtot - 1, sk.units, sk.ncl) - cta_of(ub, sk.units, sk.ncl) + 1;
+  const int tx = threadIdx.x, ty = threadIdx.y;
+  const int nrow = min(32, min(kBM, r - mt * kBM) - sr * 32);
+  const int col = sc * 32 + tx;
+  const bool cvalid = col < NC && nc * NC + col < r;
+  float acc[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) acc[i] = 0.0f;
+  if (cvalid) {
+    for (int j = ty; j < nseg; j += 8) {
+      const float *pj = part + ((tm * sk.maxseg + j) * kBM + sr * 32) * NC + col;
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        if (i < nrow) acc[i] += pj[static_cast<size_t>(i) * NC];
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 32; ++i) wsum[ty][i][tx] = acc[i];
+  __syncthreads();
+  float v[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int i = ty + 8 * q;
+    float sum = 0.0f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) sum += wsum[w][i][tx];
+    v[q] = (i < nrow && cvalid) ? half_s * sum : 0.0f;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int i = ty + 8 * q;
+    store_g3(mt * kBM + sr * 32 + i, nc * NC + col, v[q], npad, rs, g3);
+    wsum[0][i][tx] = v[q];
+  }
+  if (mt != nc) {
+    __syncthreads();
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int i = ty + 8 * q;
+      store_g3(nc * NC + sc * 32 + i, mt * kBM + sr * 32 + tx, wsum[0][tx][i], npad, rs, g3);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
 // host planning
 // ---------------------------------------------------------------------------
 struct GemmPlan {
@@ -1140,6 +1567,132 @@ void choose_cluster(int device, int sms, int64_t out, int64_t in, int64_t r, int
   }
 }
 
+// ---- bf16 weights: planning
+struct Plan16 {
+  Tc16Params p;
+  int bke;   // bf16 per K block (the kernel instance)
+  size_t smem_bytes;
+  size_t part_bytes;
+};
+
+bool plan16(int mode, int M, int64_t in, int r, int max_ctas, Plan16 *gp) {
+  Tc16Params &p = gp->p;
+  std::memset(&p, 0, sizeof(p));
+  p.mode = mode;
+  p.M = M;
+  int npad;
+  plan_n(r, &npad, &p.nchunks, &p.NC);
+  if (mode == kGram) {
+    p.NC = npad < kBM ? npad : kBM;
+    p.nchunks = static_cast<int>(dora::ceil_div(npad, p.NC));
+    p.sym = 1;
+  }
+  const int sl = static_cast<int>(dora::round_up(p.NC, 8));
+  p.nb = static_cast<int>(dora::ceil_div(sl, 128));
+  p.nbox = static_cast<int>(dora::round_up(dora::ceil_div(sl, p.nb), 8));
+  p.sl = p.nb * p.nbox;
+  p.NT = p.sl;
+  p.nmma0 = p.NC <= 256 ? p.NC : 256;
+  p.nmma1 = p.NC - p.nmma0;
+  const int acc_cols = p.nmma1 > 0 ? 256 + p.nmma1 : p.nmma0;
+  int cols = 32;
+  while (cols < acc_cols) cols *= 2;
+  p.tmem_cols = cols;
+  // 64 bf16 per K block (128-byte rows) while a stage fits at least three
+  // times into shared memory, else 32 (64-byte rows)
+  gp->bke = 0;
+  for (int bke = 64; bke >= 32; bke /= 2) {
+    const unsigned xb = static_cast<unsigned>(kBM * bke * 2);
+    const unsigned sb = xb + static_cast<unsigned>(p.NT * bke * 2);
+    const int st = static_cast<int>((kSmemMax - 1024 - 512) / sb);
+    if (st >= 3 || bke == 32) {
+      gp->bke = bke;
+      p.x_bytes = xb;
+      p.stage_bytes = sb;
+      p.stages = st < kMaxStages ? st : kMaxStages;
+      break;
+    }
+  }
+  if (p.stages < 2) return false;
+  p.kb1 = static_cast<int>(dora::ceil_div(in, gp->bke));
+  p.rs = static_cast<int>(dora::round_up(r, 8));
+  p.kbr = static_cast<int>(dora::ceil_div(r, gp->bke));
+  p.kbtot = p.kb1 + (mode == kNorm ? 3 * p.kbr : 0);
+  const int mtiles = static_cast<int>(dora::ceil_div(M, kBM));
+  p.tiles = p.sym ? p.nchunks * (p.nchunks + 1) / 2 : mtiles * p.nchunks;
+  p.units = static_cast<long long>(p.tiles) * p.kbtot;
+  const int min_units = mode == kGram ? kMinUnitsGram : kMinUnitsNorm;
+  long long ncl = dora::ceil_div(p.units, min_units);
+  if (ncl > max_ctas) ncl = max_ctas;
+  if (ncl < 1) ncl = 1;
+  p.ncl = static_cast<int>(ncl);
+  p.ctas = p.ncl;
+  p.maxseg = seg_bound(p.units, p.ncl, p.kbtot);
+  p.r = r;
+  const size_t per_row = mode == kGram ? static_cast<size_t>(p.NC) : 2;
+  gp->part_bytes = static_cast<size_t>(mtiles) * p.nchunks * p.maxseg * kBM * per_row * sizeof(float);
+  gp->smem_bytes = static_cast<size_t>(p.stages) * p.stage_bytes + 1024 /*align*/ + 8 * (2 * p.stages + 3) + 64;
+  if (p.tmem_cols > 256 && gp->smem_bytes < 116 * 1024) gp->smem_bytes = 116 * 1024;
+  return true;
+}
+
+struct Layout16 {
+  size_t g3, part_g, part_n, b_pad, cnt, total;
+};
+
+bool plan_layout16(int64_t out, int64_t in, int64_t r, int sms, Plan16 *gg, Plan16 *gn, Layout16 *L) {
+  if (!plan16(kGram, static_cast<int>(r), in, static_cast<int>(r), sms, gg)) return false;
+  if (!plan16(kNorm, static_cast<int>(out), in, static_cast<int>(r), sms, gn)) return false;
+  int npad, nchunks, NC;
+  plan_n(static_cast<int>(r), &npad, &nchunks, &NC);
+  const int64_t rs = dora::round_up(r, 8);
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off += al256(bytes);
+    return o;
+  };
+  L->g3 = take(static_cast<size_t>(npad) * 3 * rs * 2);
+  L->part_g = take(gg->part_bytes);
+  L->part_n = take(gn->part_bytes);
+  L->b_pad = (r % 8) ? take(static_cast<size_t>(out) * rs * 2) : 0;
+  L->cnt = take(static_cast<size_t>(dora::ceil_div(out, kBM)) * 4 * sizeof(int));
+  L->total = off;
+  return true;
+}
+
+cudaError_t launch16(const Plan16 &gp, cudaStream_t cs, const CUtensorMap &x1, const CUtensorMap &x2,
+                     const CUtensorMap &y1, const CUtensorMap &y2) {
+  const dim3 grid(static_cast<unsigned>(gp.p.ctas)), block(kThreads);
+  if (gp.bke == 64)
+    tc16_kernel<64><<<grid, block, gp.smem_bytes, cs>>>(x1, x2, y1, y2, gp.p);
+  else
+    tc16_kernel<32><<<grid, block, gp.smem_bytes, cs>>>(x1, x2, y1, y2, gp.p);
+  return cudaGetLastError();
+}
+
+// Once per device: the address of the device error word and the shared-memory
+// limit of every tensor-core kernel instance.
+dora_status device_init(int device, int **errp) {
+  static std::mutex mu;
+  static int *err_ptr[64] = {};
+  std::lock_guard<std::mutex> lock(mu);
+  if (device < 0 || device >= 64) return DORA_ERR_CUDA;
+  if (!err_ptr[device]) {
+    void *ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_dora_err) != cudaSuccess) return DORA_ERR_CUDA;
+    const cudaFuncAttribute a = cudaFuncAttributeMaxDynamicSharedMemorySize;
+    if (cudaFuncSetAttribute(tc_gemm_kernel<kBKNarrow>, a, kSmemMax) != cudaSuccess ||
+        cudaFuncSetAttribute(tc_gemm_kernel<kBKWide>, a, kSmemMax) != cudaSuccess ||
+        cudaFuncSetAttribute(tc16_kernel<32>, a, kSmemMax) != cudaSuccess ||
+        cudaFuncSetAttribute(tc16_kernel<64>, a, kSmemMax) != cudaSuccess)
+      return DORA_ERR_CUDA;
+    err_ptr[device] = static_cast<int *>(ptr);
+  }
+  *errp = err_ptr[device];
+  return DORA_OK;
+}
+
 }  // namespace
 
 extern "C" size_t dora_norm_factored_workspace(int64_t out, int64_t in, int64_t r) {
@@ -1197,25 +1750,9 @@ extern "C" dora_status dora_norm_factored(const float *W0, const float *A, const
   if (st != DORA_OK) return st;
   const int sms = info.sms < kMaxCtas ? info.sms : kMaxCtas;
 
-  // device error word, passed to the kernels by address
-  static std::mutex err_mu;
-  static int *err_ptr[64] = {};
   int *errp = nullptr;
-  {
-    std::lock_guard<std::mutex> lock(err_mu);
-    if (device >= 64) return DORA_ERR_CUDA;
-    if (!err_ptr[device]) {
-      void *ptr = nullptr;
-      if (cudaGetSymbolAddress(&ptr, g_dora_err) != cudaSuccess) return DORA_ERR_CUDA;
-      if (cudaFuncSetAttribute(tc_gemm_kernel<kBKNarrow>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax) !=
-              cudaSuccess ||
-          cudaFuncSetAttribute(tc_gemm_kernel<kBKWide>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax) !=
-              cudaSuccess)
-        return DORA_ERR_CUDA;
-      err_ptr[device] = static_cast<int *>(ptr);
-    }
-    errp = err_ptr[device];
-  }
+  st = device_init(device, &errp);
+  if (st != DORA_OK) return st;
 
   int csize = 1, max_clusters = sms;
   choose_cluster(device, sms, out, in, r, &csize, &max_clusters);
@@ -1300,6 +1837,137 @@ extern "C" dora_status dora_norm_factored(const float *W0, const float *A, const
   gn.p.Bk = Bk;
   gn.p.ldb = static_cast<int>(ldb);
   if (launch_gemm(gn, cs, mW0, mB, mAh_n, mAc_n, mGh, mGc) != cudaSuccess) {
+    dora::count_launches(launches);
+    return DORA_ERR_CUDA;
+  }
+  ++launches;
+  dora::count_launches(launches);
+  return dora::launch_status();
+}
+
+// ---------------------------------------------------------------------------
+// bf16 weights
+// ---------------------------------------------------------------------------
+extern "C" size_t dora_norm_factored_bf16_workspace(int64_t out, int64_t in, int64_t r) {
+  if (!shape_ok(out, in, r)) return 0;
+  Plan16 gg, gn;
+  Layout16 L;
+  if (!plan_layout16(out > 0 ? out : 1, in, r, kMaxCtas, &gg, &gn, &L)) return 0;
+  return L.total;
+}
+
+extern "C" dora_status dora_row_sumsq_bf16(const void *W0, int64_t rows, int64_t cols, float *n0sq,
+                                           dora_stream_t stream) {
+  if (rows < 0 || cols < 1 || rows >= (1ll << 31) || cols >= (1ll << 31)) return DORA_ERR_SHAPE;
+  if (rows == 0) return DORA_OK;
+  if (!W0 || !n0sq) return DORA_ERR_NULL;
+  if (cols % 8 != 0 || !dora::aligned(W0, 16) || !dora::aligned(n0sq, 4)) return DORA_ERR_ALIGN;
+  dora::DeviceInfo info;
+  int device = 0;
+  dora_status st = dora::current_device(&info, &device);
+  if (st != DORA_OK) return st;
+  row_sumsq_bf16_kernel<<<static_cast<unsigned>(dora::ceil_div(rows, 8)), 256, 0,
+                          reinterpret_cast<cudaStream_t>(stream)>>>(
+      static_cast<const __nv_bfloat16 *>(W0), rows, static_cast<int>(cols), n0sq);
+  dora::count_launches(1);
+  return dora::launch_status();
+}
+
+extern "C" dora_status dora_norm_factored_bf16(const void *W0, const void *A, const void *B, const float *m,
+                                               const float *n0sq, float s, int64_t out, int64_t in, int64_t r,
+                                               float *norm, float *g, void *workspace, size_t workspace_bytes,
+                                               dora_stream_t stream) {
+  if (!shape_ok(out, in, r)) return DORA_ERR_SHAPE;
+  if (out == 0) return DORA_OK;
+  if (!W0 || !A || !B || !m || !n0sq || !norm || !g) return DORA_ERR_NULL;
+  if (!workspace) return DORA_ERR_WORKSPACE;
+  if (in % 8 != 0) return DORA_ERR_ALIGN;
+  if (!dora::aligned(W0, 16) || !dora::aligned(A, 16) || !dora::aligned(B, 16) || !dora::aligned(m, 4) ||
+      !dora::aligned(n0sq, 4) || !dora::aligned(norm, 4) || !dora::aligned(g, 4))
+    return DORA_ERR_ALIGN;
+  if (!dora::aligned(workspace, 256) || workspace_bytes < dora_norm_factored_bf16_workspace(out, in, r))
+    return DORA_ERR_WORKSPACE;
+
+  dora::DeviceInfo info;
+  int device = 0;
+  dora_status st = dora::current_device(&info, &device);
+  if (st != DORA_OK) return st;
+  const int sms = info.sms < kMaxCtas ? info.sms : kMaxCtas;
+  int *errp = nullptr;
+  st = device_init(device, &errp);
+  if (st != DORA_OK) return st;
+
+  Plan16 gg, gn;
+  Layout16 L;
+  if (!plan_layout16(out, in, r, sms, &gg, &gn, &L)) return DORA_ERR_SHAPE;
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  __nv_bfloat16 *g3 = reinterpret_cast<__nv_bfloat16 *>(ws + L.g3);
+  float *part_g = reinterpret_cast<float *>(ws + L.part_g);
+  float *part_n = reinterpret_cast<float *>(ws + L.part_n);
+  int *cnt = reinterpret_cast<int *>(ws + L.cnt);
+  const int ncnt = static_cast<int>(dora::ceil_div(out, kBM)) * 4;
+  int npad, nchunks, NC;
+  plan_n(static_cast<int>(r), &npad, &nchunks, &NC);
+  const int64_t rs = dora::round_up(r, 8);
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  uint64_t launches = 0;
+
+  // B padded to a 16-byte row when r % 8 != 0
+  const __nv_bfloat16 *Bk = static_cast<const __nv_bfloat16 *>(B);
+  int64_t ldb = r;
+  if (r % 8) {
+    __nv_bfloat16 *bp = reinterpret_cast<__nv_bfloat16 *>(ws + L.b_pad);
+    pad_cols_bf16_kernel<<<grid_for(out * rs, sms), 256, 0, cs>>>(Bk, out, static_cast<int>(r), static_cast<int>(rs),
+                                                                  bp);
+    ++launches;
+    Bk = bp;
+    ldb = rs;
+  }
+
+  // tensor maps (box rows: one K block of bf16, 64 or 128 bytes)
+  CUtensorMap mAx, mAy_g, mW0, mAy_n, mB, mG3;
+  const int rbg = 2 * gg.bke, rbn = 2 * gn.bke;
+  bool ok = make_map(&mAx, A, true, r, in, in, kBM, rbg) && make_map(&mAy_g, A, true, r, in, in, gg.p.nbox, rbg) &&
+            make_map(&mW0, W0, true, out, in, in, kBM, rbn) && make_map(&mAy_n, A, true, r, in, in, gn.p.nbox, rbn) &&
+            make_map(&mB, Bk, true, out, ldb, ldb, kBM, rbn) &&
+            make_map(&mG3, g3, true, npad, 3 * rs, 3 * rs, gn.p.nbox, rbn);
+  if (!ok) {
+    dora::count_launches(launches);
+    return DORA_ERR_CUDA;
+  }
+
+  // 1. Gram partial tiles
+  gg.p.part = part_g;
+  gg.p.err = errp;
+  if (launch16(gg, cs, mAx, mAx, mAy_g, mAy_g) != cudaSuccess) {
+    dora::count_launches(launches);
+    return DORA_ERR_CUDA;
+  }
+  ++launches;
+
+  // 2. s/2 G as three bf16 pieces; the norm pass's counters zeroed
+  {
+    StreamK skg{gg.p.units, gg.p.ncl, gg.p.kbtot, gg.p.maxseg, 1};
+    const int nsub = (gg.p.NC + 31) / 32;
+    gram_reduce3_kernel<<<dim3(static_cast<unsigned>(gg.p.tiles), static_cast<unsigned>(nsub * nsub)), dim3(32, 8), 0,
+                          cs>>>(part_g, skg, gg.p.nchunks, gg.p.NC, static_cast<int>(r), npad, static_cast<int>(rs),
+                                0.5f * s, g3, cnt, ncnt);
+  }
+  ++launches;
+
+  // 3. [W0 | B B B] x [A | h1 h2 h3]^T; the last epilogue warp of each quarter
+  //    M tile writes n and g
+  gn.p.part = part_n;
+  gn.p.err = errp;
+  gn.p.cnt = cnt;
+  gn.p.m = m;
+  gn.p.n0sq = n0sq;
+  gn.p.norm = norm;
+  gn.p.g = g;
+  gn.p.two_s = 2.0f * s;
+  gn.p.Bk = Bk;
+  gn.p.ldb = static_cast<int>(ldb);
+  if (launch16(gn, cs, mW0, mB, mAy_n, mG3) != cudaSuccess) {
     dora::count_launches(launches);
     return DORA_ERR_CUDA;
   }

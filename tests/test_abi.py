@@ -130,3 +130,39 @@ def test_compose_argument_errors(lib):
 
 def test_launch_counter_starts_at_zero(lib):
     assert dora.dora_kernel_launches() >= 0
+
+
+def test_bf16_norm_workspace_and_argument_errors(lib):
+    d = 8192
+    prev = 0
+    for r in (16, 64, 128, 256, 384, 512, 768):
+        ws = dora.dora_norm_factored_bf16_workspace(d, d, r)
+        assert 0 < ws < d * d * 2          # never the size of a bf16 out x in matrix
+        assert ws > prev
+        prev = ws
+    assert dora.dora_norm_factored_bf16_workspace(d, d, 0) == 0
+    assert dora.dora_norm_factored_bf16_workspace(d, 0, 8) == 0
+    f = lib.dora_norm_factored_bf16
+    ok = dict(W0=FAKE, A=FAKE, B=FAKE, m=FAKE, n0=FAKE, s=1.0, out=256, inp=64, r=8, norm=FAKE, g=FAKE, ws=FAKE,
+              wsb=1 << 30, stream=None)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return f(a["W0"], a["A"], a["B"], a["m"], a["n0"], a["s"], a["out"], a["inp"], a["r"], a["norm"], a["g"],
+                 a["ws"], a["wsb"], a["stream"])
+
+    assert call(out=-1) == 2
+    assert call(r=0) == 2
+    assert call(out=0) == 0
+    assert call(n0=None) == 1
+    assert call(W0=None) == 1
+    assert call(inp=60) == 3                    # bf16 row stride not a multiple of 16 bytes
+    assert call(A=FAKE + 8) == 3
+    assert call(ws=FAKE + 16) == 5
+    assert call(wsb=16) == 5
+    rs = lib.dora_row_sumsq_bf16
+    assert rs(FAKE, -1, 64, FAKE, None) == 2
+    assert rs(FAKE, 0, 64, FAKE, None) == 0
+    assert rs(None, 4, 64, FAKE, None) == 1
+    assert rs(FAKE, 4, 60, FAKE, None) == 3
+    assert rs(FAKE + 8, 4, 64, FAKE, None) == 3

@@ -470,6 +470,8 @@ def run_report(args):
         # out = in = 8192, T = 8192 bf16: norm time, compose GB/s and the norm's
         # whole transient (its workspace) against one dense fp32 out x in matrix
         for k, r in enumerate(wl.RANK_SWEEP):
+            if args.ranks and r not in args.ranks:
+                continue
             sh = wl.shape("rank_sweep", r=r)
             W0, A, B, m = _device_module(sh, wl.seed_for("rank_sweep", k), dev)
             gen = torch.Generator(device=dev)
@@ -506,6 +508,8 @@ def run_report(args):
         # to bf16) at out = in = 8192 over the swept ranks; the row norms of W0
         # are computed once (W0 is frozen) and timed separately
         for k, r in enumerate(sorted(wl.RANK_SWEEP + (384,))):
+            if args.ranks and r not in args.ranks:
+                continue
             sh = wl.shape("rank_sweep", r=r)
             W0, A, B, m = _device_module(sh, wl.seed_for("rank_sweep", k), dev)
             W0, A, B = W0.bfloat16(), A.bfloat16(), B.bfloat16()
@@ -581,6 +585,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--report", choices=["rank_sweep", "mlp_stack", "bf16_norm"], default=None,
                     help="extra per-workload report lines instead of the bench line")
+    ap.add_argument("--ranks", type=lambda v: [int(x) for x in v.split(",")], default=None,
+                    help="reports rank_sweep / bf16_norm: only these ranks (comma separated)")
     args = ap.parse_args()
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))

@@ -1,10 +1,12 @@
 """torch.library registration of the DoRA hot path (integration only).
 
-Three custom ops; each allocates its outputs (and the library's workspace)
+Five custom ops; each allocates its outputs (and the library's workspace)
 with torch and calls the C entry point of the same name on the current CUDA
 stream.  No arithmetic happens here:
 
   torch.ops.dora.norm_factored(W0, A, B, m, s) -> (norm, g)
+  torch.ops.dora.row_sumsq(W0) -> n0sq                       (bf16 W0: ||W0_i||^2, once)
+  torch.ops.dora.norm_factored_bf16(W0, A, B, m, n0sq, s) -> (norm, g)   (bf16 W0, A, B)
   torch.ops.dora.compose(base, lora, m, g, norm, s) -> y
   torch.ops.dora.compose_bwd(dy, base, lora, g, norm, s) -> (d_base, d_lora, d_mag)
 
@@ -18,7 +20,8 @@ library's d_mag, and dL/dbase = g dy, dL/dlora = s g dy are its d_base and
 d_lora.  The backward is therefore one call of dora_compose_bwd.
 
 Inputs must be contiguous, row-major and on one CUDA device (the C ABI's
-layout); weights and m are float32, activations float32 or bfloat16.
+layout); m, n0sq, norm and g are float32, the weights float32 (bfloat16 for
+the _bf16 norm and row_sumsq), activations float32 or bfloat16.
 """
 from __future__ import annotations
 
@@ -26,9 +29,10 @@ import torch
 from torch import Tensor
 
 from . import (dora_compose_bwd, dora_compose_bwd_workspace, dora_compose_fwd, dora_norm_factored,
-               dora_norm_factored_workspace)
+               dora_norm_factored_bf16, dora_norm_factored_bf16_workspace, dora_norm_factored_workspace,
+               dora_row_sumsq_bf16)
 
-__all__ = ["norm_factored", "compose", "compose_bwd", "dora_module"]
+__all__ = ["norm_factored", "row_sumsq", "norm_factored_bf16", "compose", "compose_bwd", "dora_module"]
 
 
 def _contig(name: str, *ts: Tensor) -> None:
@@ -52,6 +56,39 @@ def norm_factored(W0: Tensor, A: Tensor, B: Tensor, m: Tensor, s: float) -> tupl
 
 @norm_factored.register_fake
 def _norm_factored_fake(W0, A, B, m, s):
+    out = W0.shape[0]
+    return W0.new_empty(out, dtype=torch.float32), W0.new_empty(out, dtype=torch.float32)
+
+
+@torch.library.custom_op("dora::row_sumsq", mutates_args=(), device_types="cuda")
+def row_sumsq(W0: Tensor) -> Tensor:
+    """||W0_i||^2 of a bfloat16 W0 in fp32 (fixed summation order)."""
+    _contig("row_sumsq", W0)
+    n0sq = torch.empty(W0.shape[0], device=W0.device, dtype=torch.float32)
+    dora_row_sumsq_bf16(W0, n0sq)
+    return n0sq
+
+
+@row_sumsq.register_fake
+def _row_sumsq_fake(W0):
+    return W0.new_empty(W0.shape[0], dtype=torch.float32)
+
+
+@torch.library.custom_op("dora::norm_factored_bf16", mutates_args=(), device_types="cuda")
+def norm_factored_bf16(W0: Tensor, A: Tensor, B: Tensor, m: Tensor, n0sq: Tensor, s: float) -> tuple[Tensor, Tensor]:
+    """The factored norm for bfloat16 W0, A, B with ||W0_i||^2 given (n0sq)."""
+    _contig("norm_factored_bf16", W0, A, B, m, n0sq)
+    out, inp = W0.shape
+    r = A.shape[0]
+    norm = torch.empty(out, device=W0.device, dtype=torch.float32)
+    g = torch.empty_like(norm)
+    ws = torch.empty(max(dora_norm_factored_bf16_workspace(out, inp, r), 1), dtype=torch.uint8, device=W0.device)
+    dora_norm_factored_bf16(W0, A, B, m, n0sq, s, norm, g, ws)
+    return norm, g
+
+
+@norm_factored_bf16.register_fake
+def _norm_factored_bf16_fake(W0, A, B, m, n0sq, s):
     out = W0.shape[0]
     return W0.new_empty(out, dtype=torch.float32), W0.new_empty(out, dtype=torch.float32)
 

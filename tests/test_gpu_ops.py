@@ -57,3 +57,15 @@ def test_opcheck():
     torch.library.opcheck(torch.ops.dora.compose.default, (base_a, lora, m_a, g, norm, s), test_utils=checks)
     torch.library.opcheck(torch.ops.dora.compose_bwd.default, (dy, base, lora, g, norm, s), test_utils=checks)
     assert_no_device_error()
+
+
+def test_bf16_ops_match_direct_calls():
+    from test_gpu_bf16 import _dev16, _module, run_norm_bf16
+    sh = wl.shape("high_rank", out=264, inp=384, r=40, T=8)
+    w, (w0b, ab, bb), _ = _module(sh, 4243)
+    W0, A, B, m = _dev16(w0b), _dev16(ab), _dev16(bb), f32_dev(w["m"])
+    n0_d, norm_d, g_d = run_norm_bf16(W0, A, B, m, w["s"])
+    n0_o = torch.ops.dora.row_sumsq(W0)
+    norm_o, g_o = torch.ops.dora.norm_factored_bf16(W0, A, B, m, n0_o, w["s"])
+    assert torch.equal(n0_o, n0_d) and torch.equal(norm_o, norm_d) and torch.equal(g_o, g_d)
+    assert_no_device_error()

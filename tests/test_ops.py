@@ -10,7 +10,7 @@ def test_ops_registered_and_fake_shapes():
 
     import parameter_efficient_fine_gb300.ops  # noqa: F401  (registers torch.ops.dora.*)
 
-    for name in ("norm_factored", "compose", "compose_bwd"):
+    for name in ("norm_factored", "row_sumsq", "norm_factored_bf16", "compose", "compose_bwd"):
         assert hasattr(torch.ops.dora, name)
     with FakeTensorMode():
         W0 = torch.empty(64, 32, device="cuda")
@@ -24,3 +24,7 @@ def test_ops_registered_and_fake_shapes():
         assert y.shape == base.shape and y.dtype == torch.bfloat16
         db, dl, dm = torch.ops.dora.compose_bwd(base, base, base, g, n, 1.0)
         assert db.shape == base.shape and dl.dtype == torch.bfloat16 and dm.shape == (64,) and dm.dtype == torch.float32
+        W16, A16, B16 = W0.bfloat16(), A.bfloat16(), B.bfloat16()
+        n0 = torch.ops.dora.row_sumsq(W16)
+        n16, g16 = torch.ops.dora.norm_factored_bf16(W16, A16, B16, m, n0, 1.0)
+        assert n0.shape == (64,) and n0.dtype == torch.float32 and n16.shape == (64,) and g16.dtype == torch.float32

@@ -24,6 +24,8 @@ the whole point of the method is that the GPU path never forms it):
   * Backward with the norm treated as a constant (P1 is silent; reading c2):
         d_base = g*dy,  d_lora = s*g*dy,
         d_mag_j = sum_t dy[t,j]*(base[t,j] + s*lora[t,j]) / n_j .
+  * Variant with the norm NOT detached (gradient through n into A and B): the
+    chain rule through g = m/n and n_i = ||V_i||, V = W0 + s B A (norm_grad).
 
 Readings of silent or garbled points are listed in the repository design notes;
 the ones that change arithmetic are repeated at the function that takes them.
@@ -38,7 +40,9 @@ joint column permutation of W0 and A; the factored fp64 identity on
 brute-force tiny shapes; hand-computed fixtures in tests/golden/; central
 finite differences of L(m, base, lora) = <dy, y>; the homogeneity identity
 sum_j m_j d_mag_j = sum dy*y; exact bf16 encodings against torch and against
-hand-made double-rounding cases.
+hand-made double-rounding cases; for norm_grad, central finite differences
+of L(A, B) = <w, g(A, B)>, torch autograd of the dense definition, Euler's
+identity for the degree-1 homogeneous norm (W0 = 0) and the B = 0 closed form.
 """
 from __future__ import annotations
 
@@ -53,6 +57,7 @@ __all__ = [
     "compose_fwd_stable",
     "compose_fwd_naive_bf16",
     "compose_bwd",
+    "norm_grad",
 ]
 
 
@@ -213,3 +218,37 @@ def compose_bwd(dy, base, lora, g, n, s):
     d_lora = s * g * dy
     d_mag = np.sum(dy * (base + s * lora), axis=0) / n
     return d_base, d_lora, d_mag
+
+
+# ----------------------------------------------------------------------------
+# (c) the variant with the norm not detached: gradient through n into A, B
+# ----------------------------------------------------------------------------
+
+def norm_grad(W0, A, B, s, n, g, d_mag):
+    """Gradients w.r.t. A and B that flow through the row norm, fp64.
+
+    The page is silent on a gradient through the norm (its backward treats n
+    as a constant; reading c2).  This is the other plain reading: n is a
+    function of A and B.  The loss sees n only through g = m/n, and d_mag is
+    dL/dm along that route (as compose_bwd returns it), i.e.
+        dL/dg_i = d_mag_i * n_i,   dg_i/dn_i = -m_i/n_i^2 = -g_i/n_i
+        =>  dL/dn_i = -g_i * d_mag_i .
+    With V = W0 + s B A (dense) and dn_i/dV_i = V_i / n_i,
+        dV  = (dL/dn / n)[:, None] * V
+        dB  = s * dV @ A^T          (V = ... + s B A, so dV/dB carries s A)
+        dA  = s * B^T @ dV .
+    n and g are the forward's values, passed in (the backward of the library
+    takes them as inputs too); V is formed densely from the weights.
+    Rows are independent for dB (a row subset of W0, B, n, g, d_mag gives
+    those rows of dB); columns are independent for dA (a column subset of W0
+    and A, with all rows, gives those columns of dA).
+    Returns (dA [r, in], dB [out, r]).
+    """
+    W0 = _f64(W0)
+    A = _f64(A)
+    B = _f64(B)
+    n = _f64(n)
+    dn = -_f64(g) * _f64(d_mag)
+    V = W0 + s * (B @ A)
+    dV = (dn / n)[:, None] * V
+    return s * (B.T @ dV), s * (dV @ A.T)

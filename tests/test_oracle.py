@@ -263,3 +263,106 @@ def test_naive_bf16_matches_hand_steps():
     lora = np.array([[0x3E80]], np.uint16)   # 0.25
     got = oracle.compose_fwd_naive_bf16(base, lora, np.array([0.75]), 3.0)
     assert oracle.bf16_bits_to_f64(got)[0, 0] == 1.6875
+
+
+# --------------------------------------------------------------------------
+# gradient through the norm (the non-detached variant)
+# --------------------------------------------------------------------------
+
+def _norm_grad_case(seed, out=5, inp=7, r=3, s=0.9):
+    rng = np.random.default_rng(seed)
+    W0 = rng.standard_normal((out, inp)) / np.sqrt(inp)
+    A = rng.standard_normal((r, inp)) / np.sqrt(inp)
+    B = rng.standard_normal((out, r)) * 0.3
+    m = rng.uniform(0.5, 1.5, out)
+    w = rng.standard_normal(out)          # dL/dg
+    return W0, A, B, m, w, s
+
+
+def _g_loss(W0, A, B, m, w, s):
+    # L(A, B) = <w, g(A, B)>, g = m / n through the (separately pinned) norm
+    _, g = oracle.weight_norm(W0, A, B, m, s)
+    return float(np.sum(w * g))
+
+
+def _grad_inputs(W0, A, B, m, w, s):
+    n, g = oracle.weight_norm(W0, A, B, m, s)
+    return n, g, w / n                    # d_mag = dL/dm = (dL/dg) / n
+
+
+def test_norm_grad_central_differences():
+    W0, A, B, m, w, s = _norm_grad_case(21)
+    n, g, d_mag = _grad_inputs(W0, A, B, m, w, s)
+    dA, dB = oracle.norm_grad(W0, A, B, s, n, g, d_mag)
+    assert dA.shape == A.shape and dB.shape == B.shape
+    h = 1e-6
+    for X, dX, which in ((A, dA, "A"), (B, dB, "B")):
+        for idx in np.ndindex(X.shape):
+            E = np.zeros_like(X)
+            E[idx] = h
+            if which == "A":
+                fd = (_g_loss(W0, A + E, B, m, w, s) - _g_loss(W0, A - E, B, m, w, s)) / (2 * h)
+            else:
+                fd = (_g_loss(W0, A, B + E, m, w, s) - _g_loss(W0, A, B - E, m, w, s)) / (2 * h)
+            assert abs(fd - dX[idx]) <= 1e-7 * max(1.0, abs(dX[idx])), (which, idx, fd, dX[idx])
+
+
+def test_norm_grad_matches_torch_autograd_of_dense_definition():
+    torch = pytest.importorskip("torch")
+    W0, A, B, m, w, s = _norm_grad_case(22, out=9, inp=13, r=4, s=1.7)
+    n, g, d_mag = _grad_inputs(W0, A, B, m, w, s)
+    dA, dB = oracle.norm_grad(W0, A, B, s, n, g, d_mag)
+    tA = torch.tensor(A, dtype=torch.float64, requires_grad=True)
+    tB = torch.tensor(B, dtype=torch.float64, requires_grad=True)
+    V = torch.tensor(W0, dtype=torch.float64) + s * (tB @ tA)
+    L = torch.sum(torch.tensor(w * m) / torch.linalg.vector_norm(V, dim=1))
+    gA, gB = torch.autograd.grad(L, (tA, tB))
+    assert np.allclose(dA, gA.numpy(), rtol=1e-12, atol=1e-14)
+    assert np.allclose(dB, gB.numpy(), rtol=1e-12, atol=1e-14)
+
+
+def test_norm_grad_euler_identity_without_base():
+    # W0 = 0: n_i = s ||B_i A|| is homogeneous of degree 1 in A and in B, so
+    # <A, dA> = <B, dB> = sum_i (dL/dn_i) n_i with dL/dn = -g d_mag
+    W0, A, B, m, w, s = _norm_grad_case(23, out=11, inp=17, r=5)
+    W0 = np.zeros_like(W0)
+    n, g, d_mag = _grad_inputs(W0, A, B, m, w, s)
+    dA, dB = oracle.norm_grad(W0, A, B, s, n, g, d_mag)
+    want = float(np.sum(-g * d_mag * n))
+    scale = float(np.sum(np.abs(g * d_mag * n)))
+    assert abs(np.sum(A * dA) - want) <= 1e-12 * scale
+    assert abs(np.sum(B * dB) - want) <= 1e-12 * scale
+    assert abs(want) > 1e-3 * scale
+
+
+def test_norm_grad_b_zero_closed_form():
+    # B = 0: V = W0, dA = s B^T dV = 0; with A = [I_r | 0], W0 A^T is the first
+    # r columns of W0, so dB_i = s (dL/dn_i / n_i) W0[i, :r], n_i = ||W0_i||
+    rng = np.random.default_rng(24)
+    out, inp, r, s = 6, 10, 3, 1.3
+    W0 = rng.standard_normal((out, inp))
+    A = np.zeros((r, inp))
+    A[np.arange(r), np.arange(r)] = 1.0
+    B = np.zeros((out, r))
+    m = rng.uniform(0.5, 1.5, out)
+    d_mag = rng.standard_normal(out)
+    n = np.linalg.norm(W0, axis=1)
+    g = m / n
+    dA, dB = oracle.norm_grad(W0, A, B, s, n, g, d_mag)
+    assert np.array_equal(dA, np.zeros_like(A))
+    want = s * (-g * d_mag / n)[:, None] * W0[:, :r]
+    assert np.allclose(dB, want, rtol=1e-14, atol=0)
+
+
+def test_norm_grad_row_and_column_subsets():
+    # the sampled large-shape checks rely on these: dB rows need only their own
+    # rows, dA columns only their own columns of W0 and A
+    W0, A, B, m, w, s = _norm_grad_case(25, out=12, inp=16, r=4)
+    n, g, d_mag = _grad_inputs(W0, A, B, m, w, s)
+    dA, dB = oracle.norm_grad(W0, A, B, s, n, g, d_mag)
+    rows = np.array([0, 5, 11])
+    cols = np.array([1, 2, 15])
+    _, dB_r = oracle.norm_grad(W0[rows], A, B[rows], s, n[rows], g[rows], d_mag[rows])
+    dA_c, _ = oracle.norm_grad(W0[:, cols], A[:, cols], B, s, n, g, d_mag)
+    assert np.allclose(dB_r, dB[rows], rtol=1e-13, atol=0)
+    assert np.allclose(dA_c, dA[:, cols], rtol=1e-13, atol=0)

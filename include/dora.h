@@ -154,6 +154,48 @@ dora_status dora_norm_factored_bf16(const void *W0, const void *A, const void *B
                                     dora_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
+/* (a'') gradient through the norm (the variant with the norm not detached)  */
+/* ------------------------------------------------------------------------ */
+
+/* Bytes of workspace dora_norm_factored_bwd needs (host arithmetic; 0 for an
+ * invalid shape).  O((out + in) r + r^2) bytes, never out*in. */
+size_t dora_norm_factored_bwd_workspace(int64_t out, int64_t in, int64_t r);
+
+/*
+ * The part of dL/dA and dL/dB that flows through the row norm n, for a loss
+ * that sees n only through g = m / n.  P1 is silent on a gradient through the
+ * norm (its backward holds n constant, which is what dora_compose_bwd does);
+ * this entry point is the plain chain rule for callers that do not detach it.
+ * With d_mag = dL/dm as dora_compose_bwd writes it, dL/dn_i = -g_i d_mag_i and,
+ * for V = W0 + s B A and c_i = (dL/dn_i) / n_i,
+ *
+ *   dB = s c (.) (W0 A^T + s B G),         G = A A^T
+ *   dA = s (c (.) B)^T W0 + s^2 H A,       H = B^T diag(c) B
+ *
+ * evaluated in factored form (the out x in matrix V is never formed) on the
+ * tensor cores with the same split-TF32 precision as dora_norm_factored.
+ * The outputs are ONLY the norm's share: the caller adds the gradients of its
+ * own lora = x A^T B^T product.  dA and dB are overwritten.
+ *
+ *   W0, A, B   float32, as for dora_norm_factored (16-byte aligned, in % 4 == 0)
+ *   norm, g    float32 [out]  the forward's outputs (dora_norm_factored)
+ *   d_mag      float32 [out]  dL/dm (dora_compose_bwd)
+ *   dA         float32 [r, in]   dB  float32 [out, r]   (4-byte aligned)
+ *   workspace  >= dora_norm_factored_bwd_workspace(out, in, r) bytes, 256-byte aligned
+ *   Sizes as dora_norm_factored; out == 0 writes zeros to dA (an empty sum).
+ * Launches at most 11 kernels (A split, B padding when r % 4 != 0, the split of
+ * s c (.) B transposed, two Gram passes and their reductions, the dB and dA
+ * passes and the fixed-order sums of their stream-K parts); results are
+ * bitwise reproducible.
+ */
+dora_status dora_norm_factored_bwd(const float *W0, const float *A, const float *B,
+                                   const float *norm, const float *g, const float *d_mag,
+                                   float s, int64_t out, int64_t in, int64_t r,
+                                   float *dA, float *dB,
+                                   void *workspace, size_t workspace_bytes,
+                                   dora_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
 /* (b) fused compose, forward                                                */
 /* ------------------------------------------------------------------------ */
 

@@ -21,6 +21,8 @@ __all__ = [
     "dora_row_sumsq_bf16",
     "dora_norm_factored_bf16_workspace",
     "dora_norm_factored_bf16",
+    "dora_norm_factored_bwd_workspace",
+    "dora_norm_factored_bwd",
     "dora_compose_fwd",
     "dora_compose_bwd_workspace",
     "dora_compose_bwd",
@@ -52,6 +54,8 @@ _SIGNATURES = {
     "dora_row_sumsq_bf16": (_int, [_vp, _i64, _i64, _vp, _vp]),
     "dora_norm_factored_bf16_workspace": (_sz, [_i64, _i64, _i64]),
     "dora_norm_factored_bf16": (_int, [_vp, _vp, _vp, _vp, _vp, _f32, _i64, _i64, _i64, _vp, _vp, _vp, _sz, _vp]),
+    "dora_norm_factored_bwd_workspace": (_sz, [_i64, _i64, _i64]),
+    "dora_norm_factored_bwd": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _f32, _i64, _i64, _i64, _vp, _vp, _vp, _sz, _vp]),
     "dora_compose_fwd": (_int, [_int, _vp, _vp, _vp, _f32, _i64, _i64, _vp, _vp]),
     "dora_compose_bwd_workspace": (_sz, [_i64, _i64]),
     "dora_compose_bwd": (_int, [_int, _vp, _vp, _vp, _vp, _vp, _f32, _i64, _i64, _vp, _vp, _vp, _vp, _sz, _vp]),
@@ -157,6 +161,20 @@ def dora_norm_factored_bf16(W0, A, B, m, n0sq, s: float, norm, g, workspace, str
         _ptr(W0), _ptr(A), _ptr(B), _ptr(m), _ptr(n0sq), float(s), out, inp, r, _ptr(norm), _ptr(g),
         _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
     _check("dora_norm_factored_bf16", st)
+
+
+def dora_norm_factored_bwd_workspace(out: int, inp: int, r: int) -> int:
+    return int(load_library().dora_norm_factored_bwd_workspace(out, inp, r))
+
+
+def dora_norm_factored_bwd(W0, A, B, norm, g, d_mag, s: float, dA, dB, workspace, stream=None) -> None:
+    """dA, dB: the gradient that flows through the row norm (see include/dora.h)."""
+    out, inp = W0.shape
+    r = A.shape[0]
+    st = load_library().dora_norm_factored_bwd(
+        _ptr(W0), _ptr(A), _ptr(B), _ptr(norm), _ptr(g), _ptr(d_mag), float(s), out, inp, r, _ptr(dA), _ptr(dB),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
+    _check("dora_norm_factored_bwd", st)
 
 
 def dora_compose_fwd(base, lora, g, s: float, y, stream=None) -> None:

@@ -90,8 +90,16 @@ constexpr int kMinUnitsGram = 16;
 constexpr int kSmemMax = 232448;           // 227 KB: the opt-in maximum per CTA
 constexpr int kMaxStages = 12;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
+// ROWS passes: K indices per accumulation window.  The tensor core's fp32
+// accumulation rounds toward zero, so its error grows with the length of an
+// accumulation chain; windows of 1024 K summed in round-to-nearest keep the
+// gradient's error near that of a plain fp32 loop.
+constexpr int kChainK = 1024;
 
-enum Mode : int { kGram = 0, kNorm = 1 };
+// kGram: partial tiles of a symmetric product (upper triangle only);
+// kNorm: per-row <B_i, D_i> records and the fused n / g finalize;
+// kRows: partial rows of a plain product per CTA part, summed by rows_reduce_kernel
+enum Mode : int { kGram = 0, kNorm = 1, kRows = 2 };
 
 // device error word: 0 = fine; otherwise the code of the wait that gave up
 __device__ int g_dora_err = 0;
@@ -134,7 +142,26 @@ struct TcParams {
   float two_s;
   const float *Bk;  // B (or its padded copy) [M, ldb]: the epilogue prefetches its rows into L2
   int ldb;
+  // ROWS: K blocks per accumulation window (the tensor-memory accumulator
+  // restarts at every window boundary of the tile's K range, and each window
+  // is added in fp32 round-to-nearest into the CTA's partial rows)
+  int chain;
 };
+
+// c_i = (dL/dn_i) / n_i for a loss that sees n through g = m / n, with d_mag =
+// dL/dm: dL/dn_i = -g_i d_mag_i
+__device__ __forceinline__ float norm_grad_coef(const float *g, const float *d_mag, const float *norm, long long i) {
+  return -(g[i] * d_mag[i]) / norm[i];
+}
+
+// K-block range [kb0, kbe) of the piece that starts at unit u of a CTA range
+// ending at u_end: it ends at the tile's end, the range's end or (chain > 0)
+// the next accumulation-window boundary
+__device__ __forceinline__ int piece_end(long long u, long long u_end, int kb0, int kbtot, int chain) {
+  int kbe = static_cast<int>(min(static_cast<long long>(kbtot), kb0 + (u_end - u)));
+  if (chain > 0) kbe = min(kbe, (kb0 / chain + 1) * chain);
+  return kbe;
+}
 
 // ---------------------------------------------------------------------------
 // PTX wrappers
@@ -254,6 +281,11 @@ __device__ __forceinline__ void mma_commit_mc(uint32_t bar, uint16_t mask) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
                    bar),
                "h"(mask)
+               : "memory");
+}
+// *p += (a, b, c, d) in global memory, fp32 round-to-nearest, no return value
+__device__ __forceinline__ void red_add_f32x4(float4 *p, float a, float b, float c, float d) {
+  asm volatile("red.relaxed.gpu.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d)
                : "memory");
 }
 // 32 consecutive fp32 columns of this thread's tensor-memory lane (the load and
@@ -387,9 +419,14 @@ __device__ void wait_drain(uint32_t bar, uint32_t parity) {
 }
 
 // ---------------------------------------------------------------------------
-// the tensor-core GEMM (GRAM or NORM mode)
+// the tensor-core GEMM (GRAM, NORM or ROWS mode)
+//
+// XT: the M-side operand is stored K-major-transposed in global memory (its
+// rows are K indices, its columns M indices, as W0 is for W0^T): the producer
+// loads an unswizzled [BK x 128] box and the converters read it column-wise
+// (lane = M row, conflict-free), the rest is unchanged.
 // ---------------------------------------------------------------------------
-template <int BK>
+template <int BK, bool XT>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_gemm_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ CUtensorMap mX2,
                const __grid_constant__ CUtensorMap mY1h, const __grid_constant__ CUtensorMap mY1c,
@@ -461,7 +498,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ 
       for (long long u = u_begin; u < u_end && ok;) {
         const int t = static_cast<int>(u / p.kbtot);
         const int kb0 = static_cast<int>(u - static_cast<long long>(t) * p.kbtot);
-        const int kbe = static_cast<int>(min(static_cast<long long>(p.kbtot), kb0 + (u_end - u)));
+        const int kbe = piece_end(u, u_end, kb0, p.kbtot, p.chain);
         int mt, nc;
         tile_coords(t, p.nchunks, p.sym, p.csize, crank, &mt, &nc);
         for (int kb = kb0; kb < kbe; ++kb) {
@@ -476,7 +513,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ 
           const uint32_t yc = yh + static_cast<uint32_t>(p.NT) * kRowBytes;
           const bool seg1 = kb < p.kb1;
           const int kx = (seg1 ? kb : kb - p.kb1) * BK;    // fp32 column of the hi operands
-          tma_load_2d(xs, seg1 ? &mX1 : &mX2, kx, mt * kBM, fb);
+          if (XT) tma_load_2d(xs, seg1 ? &mX1 : &mX2, mt * kBM, kx, fb);
+          else tma_load_2d(xs, seg1 ? &mX1 : &mX2, kx, mt * kBM, fb);
           // this CTA's slice of the N-side tile; with a cluster it is multicast
           // to every CTA of the cluster, which all load the other slices
           for (int i = 0; i < p.nb; ++i) {
@@ -526,7 +564,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ 
       for (long long u = u_begin; u < u_end && ok;) {
         const int t = static_cast<int>(u / p.kbtot);
         const int kb0 = static_cast<int>(u - static_cast<long long>(t) * p.kbtot);
-        const int kbe = static_cast<int>(min(static_cast<long long>(p.kbtot), kb0 + (u_end - u)));
+        const int kbe = piece_end(u, u_end, kb0, p.kbtot, p.chain);
         if (!wait_bounded(acce, aphase ^ 1u, ctl, p.err, 3)) {
           ok = false;
           break;
@@ -592,7 +630,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ 
     for (long long u = u_begin; u < u_end && ok;) {
       const int t = static_cast<int>(u / p.kbtot);
       const int kb0 = static_cast<int>(u - static_cast<long long>(t) * p.kbtot);
-      const int kbe = static_cast<int>(min(static_cast<long long>(p.kbtot), kb0 + (u_end - u)));
+      const int kbe = piece_end(u, u_end, kb0, p.kbtot, p.chain);
       int mt, nc;
       tile_coords(t, p.nchunks, p.sym, p.csize, crank, &mt, &nc);
       const size_t tm = static_cast<size_t>(mt) * p.nchunks + nc;   // (M tile, N chunk) of this CTA's partials
@@ -616,14 +654,22 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ 
         // (swz_chunk); one group of 8 K indices at a time, split into the
         // tensor-memory operand slot of the stage: 8 hi columns and 8 columns
         // of bf16 pairs (lo then hi) per group
-        const float4 *xr = reinterpret_cast<const float4 *>(smem + static_cast<size_t>(stage) * p.stage_bytes +
-                                                            row * kRowBytes);
+        const uint8_t *xbox = smem + static_cast<size_t>(stage) * p.stage_bytes;
+        const float4 *xr = reinterpret_cast<const float4 *>(xbox + row * kRowBytes);
+        const float *xc = reinterpret_cast<const float *>(xbox) + row;   // XT: column `row` of [BK][128]
         const uint32_t slot = lane_addr + static_cast<uint32_t>(p.slot0 + stage * 2 * BK);
         float blk = 0.0f;
 #pragma unroll
         for (int q = 0; q < BK / 8; ++q) {
-          const float4 a = xr[swz_chunk<BK>(2 * q, row)], b = xr[swz_chunk<BK>(2 * q + 1, row)];
-          const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+          float v[8];
+          if (XT) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) v[e] = xc[(8 * q + e) * kBM];
+          } else {
+            const float4 a = xr[swz_chunk<BK>(2 * q, row)], b = xr[swz_chunk<BK>(2 * q + 1, row)];
+            v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+            v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+          }
           uint32_t hb[8], cb[8];
           float l[8];
 #pragma unroll
@@ -730,7 +776,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ 
             p.g[grow] = p.m[grow] / nn;
           }
         }
-      } else {
+      } else if (p.mode == kGram) {
         float *dst = p.part + ((tm * p.maxseg + seg) * kBM + row) * p.NC;
         for (int c = 0; c < p.NC; c += 32) {
           float v[32];
@@ -739,6 +785,29 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ 
 #pragma unroll
             for (int j = 0; j < 32; j += 4) {
               if (c + j < p.NC) *reinterpret_cast<float4 *>(dst + c + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+            }
+          }
+        }
+      } else {
+        // ROWS.  The CTA part's partial rows, [NC/4 column groups][128 rows]
+        // of float4 (a warp's store covers 32 consecutive rows: 512 bytes).
+        // The part's first window stores; later windows add in fp32 with
+        // fire-and-forget reductions (one thread per address, in program
+        // order, so the sum order is fixed).  rows_reduce_kernel sums the parts.
+        const bool first = u == u_begin || kb0 == 0;
+        const size_t slot_f4 = static_cast<size_t>(32) * p.NC;   // float4s per partial slot
+        float4 *mine = reinterpret_cast<float4 *>(p.part) + (tm * p.maxseg + seg) * slot_f4 + row;
+        for (int c = 0; c < p.NC; c += 32) {
+          float v[32];
+          tmem_ld32(lane_addr + static_cast<uint32_t>(c), v);
+          if (valid) {
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              if (c + 4 * q < p.NC) {
+                float4 *dst = mine + static_cast<size_t>(c / 4 + q) * kBM;
+                if (first) *dst = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+                else red_add_f32x4(dst, v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+              }
             }
           }
         }
@@ -892,6 +961,125 @@ __global__ void __launch_bounds__(256) gram_reduce_kernel(const float *__restric
       const int i = ty + 8 * q;
       store_gs(nc * NC + sc * 32 + i, mt * kBM + sr * 32 + tx, wsum[0][tx][i], npad, gh, gc);
     }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// gradient through the norm (norm not detached)
+//
+// With c_i = (dL/dn_i) / n_i and dL/dn_i = -g_i d_mag_i (d_mag = dL/dm along
+// g = m / n), and V = W0 + s B A:
+//     dB   = s c (.) (W0 A^T + s B G)                 G = A A^T
+//     dA^T = W0^T (s c (.) B) + A^T (s^2 H)           H = B^T diag(c) B
+// Both are the norm pass's GEMM shape: dB is [W0 | B] x [A | sG]^T over
+// K = in + r with rows scaled by s c_i at the end; dA^T is [W0^T | A^T] x
+// [(s c B)^T | s^2 H]^T over K = out + r, its M-side operands read transposed.
+// ---------------------------------------------------------------------------
+
+// Y = (s c (.) B)^T [r, out8] split like split_n_kernel: hi [r, out8] TF32 and
+// c [r, 2*out8] bf16 (per group of 8 columns: 8 hi, then 8 lo); columns
+// out..out8-1 are zero.  32 x 32 tiles transposed through shared memory.
+__global__ void __launch_bounds__(256) bs_split_kernel(const float *__restrict__ B, long long out, int r,
+                                                       long long out8, const float *__restrict__ g,
+                                                       const float *__restrict__ d_mag,
+                                                       const float *__restrict__ norm, float s,
+                                                       float *__restrict__ hi, __nv_bfloat16 *__restrict__ c) {
+  __shared__ float tile[32][33];
+  const long long i0 = static_cast<long long>(blockIdx.x) * 32;
+  const int n0 = static_cast<int>(blockIdx.y) * 32;
+  const int tx = threadIdx.x, ty = threadIdx.y;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const long long i = i0 + ty + 8 * q;
+    const int n = n0 + tx;
+    float v = 0.0f;
+    if (i < out && n < r) v = (s * norm_grad_coef(g, d_mag, norm, i)) * B[i * r + n];
+    tile[ty + 8 * q][tx] = v;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int n = n0 + ty + 8 * q;
+    const long long i = i0 + tx;
+    if (n < r && i < out8) {
+      const float x = tile[tx][ty + 8 * q];
+      const float h = __uint_as_float(tf32_rna(x));
+      hi[static_cast<long long>(n) * out8 + i] = h;
+      const long long cb = static_cast<long long>(n) * 2 * out8 + 16 * (i / 8) + (i % 8);
+      c[cb] = __float2bfloat16_rn(h);
+      c[cb + 8] = __float2bfloat16_rn(x - h);
+    }
+  }
+}
+
+// Sum of the parts of a ROWS pass, in part order.  blockIdx.x = M tile *
+// nchunks + N chunk, blockIdx.y = block of 32 columns of the chunk; warp w
+// takes column group 8 * blockIdx.y + w (4 columns, float4 partials) for the
+// tile's 128 rows, lanes along rows.
+//   trans = 0: out[row][col] = s c_row * sum, through shared memory so that a
+//              warp writes 32 consecutive columns of a row          (dB)
+//   trans = 1: out[col][row] = sum, lanes along rows                (dA)
+__global__ void __launch_bounds__(256) rows_reduce_kernel(const float4 *__restrict__ part, StreamK sk, int nchunks,
+                                                          int NC, int M, int ncols, int trans,
+                                                          const float *__restrict__ g,
+                                                          const float *__restrict__ d_mag,
+                                                          const float *__restrict__ norm, float s,
+                                                          float *__restrict__ out, long long ldo) {
+  __shared__ float tile[kBM][33];
+  const int tm = blockIdx.x;
+  const int mt = tm / nchunks, nc = tm - mt * nchunks;
+  const long long ub = (static_cast<long long>(mt / sk.csize) * nchunks + nc) * sk.kbtot;
+  const int nseg = cta_of(ub + sk.kbtot - 1, sk.units, sk.ncl) - cta_of(ub, sk.units, sk.ncl) + 1;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int cg = static_cast<int>(blockIdx.y) * 8 + warp;   // column group within the chunk
+  const int ncol = min(NC, ncols - nc * NC);                 // valid columns of the chunk
+  const size_t slot = static_cast<size_t>(32) * NC;          // float4s per part
+  const long long row0 = static_cast<long long>(mt) * kBM;
+  const float4 *src = part + static_cast<size_t>(tm) * sk.maxseg * slot + static_cast<size_t>(cg) * kBM + lane;
+  float4 acc[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (4 * cg < ncol) {
+    for (int j = 0; j < nseg; ++j) {
+      float4 o[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        o[k] = row0 + 32 * k + lane < M ? __ldcg(src + j * slot + 32 * k) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        acc[k].x += o[k].x;
+        acc[k].y += o[k].y;
+        acc[k].z += o[k].z;
+        acc[k].w += o[k].w;
+      }
+    }
+  }
+  if (trans) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const long long row = row0 + 32 * k + lane;
+      const float w[4] = {acc[k].x, acc[k].y, acc[k].z, acc[k].w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int col = 4 * cg + e;
+        if (row < M && col < ncol) out[(static_cast<long long>(nc) * NC + col) * ldo + row] = w[e];
+      }
+    }
+    return;
+  }
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    tile[32 * k + lane][4 * warp + 0] = acc[k].x;
+    tile[32 * k + lane][4 * warp + 1] = acc[k].y;
+    tile[32 * k + lane][4 * warp + 2] = acc[k].z;
+    tile[32 * k + lane][4 * warp + 3] = acc[k].w;
+  }
+  __syncthreads();
+  const int col = static_cast<int>(blockIdx.y) * 32 + lane;
+  for (int rr = warp; rr < kBM; rr += 8) {
+    const long long row = row0 + rr;
+    if (row < M && col < ncol)
+      out[row * ldo + static_cast<long long>(nc) * NC + col] = (s * norm_grad_coef(g, d_mag, norm, row)) * tile[rr][lane];
   }
 }
 
@@ -1328,6 +1516,7 @@ __global__ void __launch_bounds__(256) gram_reduce3_kernel(const float *__restri
 struct GemmPlan {
   TcParams p;
   int bk;   // fp32 per K block (the kernel instance)
+  bool xt;  // M-side operand stored transposed (the kernel instance)
   size_t smem_bytes;
   size_t part_bytes;
 };
@@ -1345,10 +1534,12 @@ void plan_n(int r, int *npad, int *nchunks, int *NC) {
   *NC = static_cast<int>(dora::round_up(dora::ceil_div(*npad, *nchunks), 16));
 }
 
-// K = in (+ r for the norm pass); csize CTAs per cluster, at most max_clusters clusters
+// K = in (+ r for the norm and row passes); csize CTAs per cluster, at most
+// max_clusters clusters
 bool plan_gemm(int mode, int M, int64_t in, int r, int csize, int max_clusters, GemmPlan *gp) {
   TcParams &p = gp->p;
   std::memset(&p, 0, sizeof(p));
+  gp->xt = false;
   p.mode = mode;
   p.M = M;
   p.csize = csize;
@@ -1363,7 +1554,7 @@ bool plan_gemm(int mode, int M, int64_t in, int r, int csize, int max_clusters, 
   gp->bk = p.NC <= kMaxChunkWide ? kBKWide : kBKNarrow;
   const int row_bytes = gp->bk * 4;
   p.kb1 = static_cast<int>(dora::ceil_div(in, gp->bk));
-  p.kbtot = p.kb1 + (mode == kNorm ? static_cast<int>(dora::ceil_div(r, gp->bk)) : 0);
+  p.kbtot = p.kb1 + (mode != kGram ? static_cast<int>(dora::ceil_div(r, gp->bk)) : 0);
   // N-side slices: each CTA of a cluster loads sl rows (a multiple of 8, so
   // every slice starts on a swizzle-pattern boundary) in nb boxes of nbox rows
   const int sl = static_cast<int>(dora::round_up(dora::ceil_div(p.NC, csize), 8));
@@ -1401,7 +1592,7 @@ bool plan_gemm(int mode, int M, int64_t in, int r, int csize, int max_clusters, 
   p.ctas = p.ncl * csize;
   p.maxseg = seg_bound(p.units, p.ncl, p.kbtot);
   p.r = r;
-  const size_t per_row = mode == kGram ? static_cast<size_t>(p.NC) : 2;
+  const size_t per_row = mode == kNorm ? 2 : static_cast<size_t>(p.NC);
   gp->part_bytes = static_cast<size_t>(ngroups) * csize * p.nchunks * p.maxseg * kBM * per_row * sizeof(float);
   gp->smem_bytes = static_cast<size_t>(p.stages) * p.stage_bytes + 1024 /*align*/ + 8 * (3 * p.stages + 3) + 64;
   // tensor memory: a CTA holding 512 columns must be alone on its SM
@@ -1436,6 +1627,51 @@ bool plan_layout(int64_t out, int64_t in, int64_t r, int sms, int csize, int max
   L->part_n = take(gn->part_bytes);
   L->b_pad = (r % 4) ? take(static_cast<size_t>(out) * dora::round_up(r, 4) * 4) : 0;
   L->cnt = take(static_cast<size_t>(dora::ceil_div(out, kBM)) * 4 * sizeof(int));
+  L->total = off;
+  return true;
+}
+
+// gradient through the norm: four GEMM passes and their workspace
+struct BwdPlans {
+  GemmPlan gg;   // G = A A^T partial tiles (K = in)
+  GemmPlan gh;   // s H = B^T (s c (.) B) partial tiles (K = out; B read transposed)
+  GemmPlan gb;   // dB rows (M = out, K = in + r)
+  GemmPlan ga;   // dA^T rows (M = in, K = out + r; W0 and A read transposed)
+};
+struct BwdLayout {
+  size_t a_hi, a_c, y_hi, y_c, g_hi, g_c, h_hi, h_c, part_t, part_r, b_pad, total;
+};
+
+bool plan_bwd(int64_t out, int64_t in, int64_t r, int sms, int csize, int max_clusters, BwdPlans *P, BwdLayout *L) {
+  const int ri = static_cast<int>(r);
+  if (!plan_gemm(kGram, ri, in, ri, 1, sms, &P->gg)) return false;
+  if (!plan_gemm(kGram, ri, out, ri, 1, sms, &P->gh)) return false;
+  if (!plan_gemm(kRows, static_cast<int>(out), in, ri, csize, max_clusters, &P->gb)) return false;
+  if (!plan_gemm(kRows, static_cast<int>(in), out, ri, csize, max_clusters, &P->ga)) return false;
+  P->gh.xt = true;
+  P->ga.xt = true;
+  P->gb.p.chain = kChainK / P->gb.bk;
+  P->ga.p.chain = kChainK / P->ga.bk;
+  int npad, nchunks, NC;
+  plan_n(ri, &npad, &nchunks, &NC);
+  const size_t out8 = static_cast<size_t>(dora::round_up(out, 8));
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off += al256(bytes);
+    return o;
+  };
+  L->a_hi = take(static_cast<size_t>(r) * in * 4);
+  L->a_c = take(static_cast<size_t>(r) * dora::round_up(in, 8) * 4);   // bf16 [r, 2*in8]
+  L->y_hi = take(static_cast<size_t>(r) * out8 * 4);
+  L->y_c = take(static_cast<size_t>(r) * out8 * 4);                    // bf16 [r, 2*out8]
+  L->g_hi = take(static_cast<size_t>(npad) * npad * 4);
+  L->g_c = take(static_cast<size_t>(npad) * npad * 4);
+  L->h_hi = take(static_cast<size_t>(npad) * npad * 4);
+  L->h_c = take(static_cast<size_t>(npad) * npad * 4);
+  L->part_t = take(P->gg.part_bytes > P->gh.part_bytes ? P->gg.part_bytes : P->gh.part_bytes);
+  L->part_r = take(P->gb.part_bytes > P->ga.part_bytes ? P->gb.part_bytes : P->ga.part_bytes);
+  L->b_pad = (r % 4) ? take(static_cast<size_t>(out) * dora::round_up(r, 4) * 4) : 0;
   L->total = off;
   return true;
 }
@@ -1481,6 +1717,20 @@ bool make_map(CUtensorMap *map, const void *base, bool bf16, int64_t rows, int64
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// the same for a matrix the GEMM reads transposed (XT): an unswizzled box of
+// kBM columns (512 bytes) x box_rows rows
+bool make_map_t(CUtensorMap *map, const float *base, int64_t rows, int64_t cols, int64_t ld, int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 4};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(kBM), static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int grid_for(long long n, int sms) {
   long long b = dora::ceil_div(n, 256);
   const long long cap = static_cast<long long>(sms) * 8;
@@ -1504,8 +1754,13 @@ cudaError_t launch_gemm(const GemmPlan &gp, cudaStream_t cs, const CUtensorMap &
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (gp.bk == kBKWide) return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<kBKWide>, x1, x2, y1h, y1c, y2h, y2c, gp.p);
-  return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<kBKNarrow>, x1, x2, y1h, y1c, y2h, y2c, gp.p);
+  if (gp.xt) {
+    if (gp.bk == kBKWide)
+      return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<kBKWide, true>, x1, x2, y1h, y1c, y2h, y2c, gp.p);
+    return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<kBKNarrow, true>, x1, x2, y1h, y1c, y2h, y2c, gp.p);
+  }
+  if (gp.bk == kBKWide) return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<kBKWide, false>, x1, x2, y1h, y1c, y2h, y2c, gp.p);
+  return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<kBKNarrow, false>, x1, x2, y1h, y1c, y2h, y2c, gp.p);
 }
 
 // Cluster shape of the norm pass.  Sharing the N-side tile pays when it is
@@ -1549,8 +1804,9 @@ void choose_cluster(int device, int sms, int64_t out, int64_t in, int64_t r, int
       cfg.attrs = attr;
       cfg.numAttrs = 1;
       int n = 0;
-      const cudaError_t e = gp.bk == kBKWide ? cudaOccupancyMaxActiveClusters(&n, tc_gemm_kernel<kBKWide>, &cfg)
-                                             : cudaOccupancyMaxActiveClusters(&n, tc_gemm_kernel<kBKNarrow>, &cfg);
+      const cudaError_t e = gp.bk == kBKWide
+                                ? cudaOccupancyMaxActiveClusters(&n, tc_gemm_kernel<kBKWide, false>, &cfg)
+                                : cudaOccupancyMaxActiveClusters(&n, tc_gemm_kernel<kBKNarrow, false>, &cfg);
       if (e != cudaSuccess) {
         cudaGetLastError();
         n = 0;
@@ -1682,8 +1938,10 @@ dora_status device_init(int device, int **errp) {
     void *ptr = nullptr;
     if (cudaGetSymbolAddress(&ptr, g_dora_err) != cudaSuccess) return DORA_ERR_CUDA;
     const cudaFuncAttribute a = cudaFuncAttributeMaxDynamicSharedMemorySize;
-    if (cudaFuncSetAttribute(tc_gemm_kernel<kBKNarrow>, a, kSmemMax) != cudaSuccess ||
-        cudaFuncSetAttribute(tc_gemm_kernel<kBKWide>, a, kSmemMax) != cudaSuccess ||
+    if (cudaFuncSetAttribute(tc_gemm_kernel<kBKNarrow, false>, a, kSmemMax) != cudaSuccess ||
+        cudaFuncSetAttribute(tc_gemm_kernel<kBKWide, false>, a, kSmemMax) != cudaSuccess ||
+        cudaFuncSetAttribute(tc_gemm_kernel<kBKNarrow, true>, a, kSmemMax) != cudaSuccess ||
+        cudaFuncSetAttribute(tc_gemm_kernel<kBKWide, true>, a, kSmemMax) != cudaSuccess ||
         cudaFuncSetAttribute(tc16_kernel<32>, a, kSmemMax) != cudaSuccess ||
         cudaFuncSetAttribute(tc16_kernel<64>, a, kSmemMax) != cudaSuccess)
       return DORA_ERR_CUDA;
@@ -1841,6 +2099,176 @@ extern "C" dora_status dora_norm_factored(const float *W0, const float *A, const
     return DORA_ERR_CUDA;
   }
   ++launches;
+  dora::count_launches(launches);
+  return dora::launch_status();
+}
+
+// ---------------------------------------------------------------------------
+// gradient through the norm
+// ---------------------------------------------------------------------------
+extern "C" size_t dora_norm_factored_bwd_workspace(int64_t out, int64_t in, int64_t r) {
+  if (!shape_ok(out, in, r)) return 0;
+  size_t total = 0;
+  for (int c = 1; c <= kMaxCluster; c *= 2) {
+    BwdPlans P;
+    BwdLayout L;
+    if (!plan_bwd(out > 0 ? out : 1, in, r, kMaxCtas, c, kMaxCtas / c, &P, &L)) return 0;
+    if (L.total > total) total = L.total;
+  }
+  return total;
+}
+
+extern "C" dora_status dora_norm_factored_bwd(const float *W0, const float *A, const float *B, const float *norm,
+                                              const float *g, const float *d_mag, float s, int64_t out, int64_t in,
+                                              int64_t r, float *dA, float *dB, void *workspace,
+                                              size_t workspace_bytes, dora_stream_t stream) {
+  if (!shape_ok(out, in, r)) return DORA_ERR_SHAPE;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  if (out == 0) {
+    // no rows: dA is an empty sum and dB has no elements
+    if (!dA) return DORA_ERR_NULL;
+    if (!dora::aligned(dA, 4)) return DORA_ERR_ALIGN;
+    if (cudaMemsetAsync(dA, 0, static_cast<size_t>(r) * in * sizeof(float), cs) != cudaSuccess) return DORA_ERR_CUDA;
+    return DORA_OK;
+  }
+  if (!W0 || !A || !B || !norm || !g || !d_mag || !dA || !dB) return DORA_ERR_NULL;
+  if (!workspace) return DORA_ERR_WORKSPACE;
+  if (in % 4 != 0) return DORA_ERR_ALIGN;
+  if (!dora::aligned(W0, 16) || !dora::aligned(A, 16) || !dora::aligned(B, 16) || !dora::aligned(norm, 4) ||
+      !dora::aligned(g, 4) || !dora::aligned(d_mag, 4) || !dora::aligned(dA, 4) || !dora::aligned(dB, 4))
+    return DORA_ERR_ALIGN;
+  if (!dora::aligned(workspace, 256) || workspace_bytes < dora_norm_factored_bwd_workspace(out, in, r))
+    return DORA_ERR_WORKSPACE;
+
+  dora::DeviceInfo info;
+  int device = 0;
+  dora_status st = dora::current_device(&info, &device);
+  if (st != DORA_OK) return st;
+  const int sms = info.sms < kMaxCtas ? info.sms : kMaxCtas;
+  int *errp = nullptr;
+  st = device_init(device, &errp);
+  if (st != DORA_OK) return st;
+
+  int csize = 1, max_clusters = sms;
+  choose_cluster(device, sms, out, in, r, &csize, &max_clusters);
+  BwdPlans P;
+  BwdLayout L;
+  if (!plan_bwd(out, in, r, sms, csize, max_clusters, &P, &L)) return DORA_ERR_SHAPE;
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  float *a_hi = reinterpret_cast<float *>(ws + L.a_hi);
+  __nv_bfloat16 *a_c = reinterpret_cast<__nv_bfloat16 *>(ws + L.a_c);
+  float *y_hi = reinterpret_cast<float *>(ws + L.y_hi);
+  __nv_bfloat16 *y_c = reinterpret_cast<__nv_bfloat16 *>(ws + L.y_c);
+  float *g_hi = reinterpret_cast<float *>(ws + L.g_hi);
+  __nv_bfloat16 *g_c = reinterpret_cast<__nv_bfloat16 *>(ws + L.g_c);
+  float *h_hi = reinterpret_cast<float *>(ws + L.h_hi);
+  __nv_bfloat16 *h_c = reinterpret_cast<__nv_bfloat16 *>(ws + L.h_c);
+  float *part_t = reinterpret_cast<float *>(ws + L.part_t);
+  float *part_r = reinterpret_cast<float *>(ws + L.part_r);
+  int npad, nchunks, NC;
+  plan_n(static_cast<int>(r), &npad, &nchunks, &NC);
+  const int64_t in8 = dora::round_up(in, 8), out8 = dora::round_up(out, 8);
+  uint64_t launches = 0;
+  auto fail = [&]() {
+    dora::count_launches(launches);
+    return DORA_ERR_CUDA;
+  };
+
+  // 1. N-side split of A; B padded to a TMA-legal row stride when r % 4 != 0;
+  //    the N-side split of (s c B)^T
+  split_n_kernel<<<grid_for(r * in8 / 4, sms), 256, 0, cs>>>(A, r, static_cast<int>(in), static_cast<int>(in8), a_hi,
+                                                              a_c, nullptr, 0);
+  ++launches;
+  const float *Bk = B;
+  int64_t ldb = r;
+  if (r % 4) {
+    const int rp = static_cast<int>(dora::round_up(r, 4));
+    float *bp = reinterpret_cast<float *>(ws + L.b_pad);
+    pad_cols_kernel<<<grid_for(out * rp, sms), 256, 0, cs>>>(B, out, static_cast<int>(r), rp, bp);
+    ++launches;
+    Bk = bp;
+    ldb = rp;
+  }
+  bs_split_kernel<<<dim3(static_cast<unsigned>(dora::ceil_div(out8, 32)), static_cast<unsigned>(dora::ceil_div(r, 32))),
+                    dim3(32, 8), 0, cs>>>(B, out, static_cast<int>(r), out8, g, d_mag, norm, s, y_hi, y_c);
+  ++launches;
+
+  // tensor maps (box rows: one K block of each pass)
+  const GemmPlan &gg = P.gg, &gh = P.gh, &gb = P.gb, &ga = P.ga;
+  const int rbg = 4 * gg.bk, rbh = 4 * gh.bk, rbb = 4 * gb.bk, rba = 4 * ga.bk;
+  CUtensorMap mA, mAh_g, mAc_g, mBt, mYh_h, mYc_h, mW0, mB, mAh_b, mAc_b, mGh, mGc, mW0t, mAt, mYh_a, mYc_a, mHh, mHc;
+  bool ok = make_map(&mA, A, false, r, in, in, kBM, rbg) && make_map(&mAh_g, a_hi, false, r, in, in, gg.p.nbox, rbg) &&
+            make_map(&mAc_g, a_c, true, r, 2 * in8, 2 * in8, gg.p.nbox, rbg) &&
+            make_map_t(&mBt, Bk, out, r, ldb, gh.bk) &&
+            make_map(&mYh_h, y_hi, false, r, out8, out8, gh.p.nbox, rbh) &&
+            make_map(&mYc_h, y_c, true, r, 2 * out8, 2 * out8, gh.p.nbox, rbh) &&
+            make_map(&mW0, W0, false, out, in, in, kBM, rbb) && make_map(&mB, Bk, false, out, ldb, ldb, kBM, rbb) &&
+            make_map(&mAh_b, a_hi, false, r, in, in, gb.p.nbox, rbb) &&
+            make_map(&mAc_b, a_c, true, r, 2 * in8, 2 * in8, gb.p.nbox, rbb) &&
+            make_map(&mGh, g_hi, false, npad, npad, npad, gb.p.nbox, rbb) &&
+            make_map(&mGc, g_c, true, npad, 2 * npad, 2 * npad, gb.p.nbox, rbb) &&
+            make_map_t(&mW0t, W0, out, in, in, ga.bk) && make_map_t(&mAt, A, r, in, in, ga.bk) &&
+            make_map(&mYh_a, y_hi, false, r, out8, out8, ga.p.nbox, rba) &&
+            make_map(&mYc_a, y_c, true, r, 2 * out8, 2 * out8, ga.p.nbox, rba) &&
+            make_map(&mHh, h_hi, false, npad, npad, npad, ga.p.nbox, rba) &&
+            make_map(&mHc, h_c, true, npad, 2 * npad, 2 * npad, ga.p.nbox, rba);
+  if (!ok) return fail();
+
+  // 2. s G = s A A^T (partial tiles, fixed-order reduction, split)
+  GemmPlan pg = gg;
+  pg.p.part = part_t;
+  pg.p.err = errp;
+  if (launch_gemm(pg, cs, mA, mA, mAh_g, mAc_g, mAh_g, mAc_g) != cudaSuccess) return fail();
+  ++launches;
+  {
+    const StreamK sk{pg.p.units, pg.p.ncl, pg.p.kbtot, pg.p.maxseg, pg.p.csize};
+    const int nsub = (pg.p.NC + 31) / 32;
+    gram_reduce_kernel<<<dim3(static_cast<unsigned>(pg.p.tiles), static_cast<unsigned>(nsub * nsub)), dim3(32, 8), 0,
+                         cs>>>(part_t, sk, pg.p.nchunks, pg.p.NC, static_cast<int>(r), npad, s, g_hi, g_c);
+    ++launches;
+  }
+  // 3. s^2 H = s (B^T (s c (.) B)), B read transposed
+  GemmPlan ph = gh;
+  ph.p.part = part_t;
+  ph.p.err = errp;
+  if (launch_gemm(ph, cs, mBt, mBt, mYh_h, mYc_h, mYh_h, mYc_h) != cudaSuccess) return fail();
+  ++launches;
+  {
+    const StreamK sk{ph.p.units, ph.p.ncl, ph.p.kbtot, ph.p.maxseg, ph.p.csize};
+    const int nsub = (ph.p.NC + 31) / 32;
+    gram_reduce_kernel<<<dim3(static_cast<unsigned>(ph.p.tiles), static_cast<unsigned>(nsub * nsub)), dim3(32, 8), 0,
+                         cs>>>(part_t, sk, ph.p.nchunks, ph.p.NC, static_cast<int>(r), npad, s, h_hi, h_c);
+    ++launches;
+  }
+  // 4. dB = s c (.) ([W0 | B] x [A | s G]^T): partial rows, then their sum
+  GemmPlan pb = gb;
+  pb.p.part = part_r;
+  pb.p.err = errp;
+  if (launch_gemm(pb, cs, mW0, mB, mAh_b, mAc_b, mGh, mGc) != cudaSuccess) return fail();
+  ++launches;
+  {
+    const StreamK sk{pb.p.units, pb.p.ncl, pb.p.kbtot, pb.p.maxseg, pb.p.csize};
+    const unsigned mtiles = static_cast<unsigned>(dora::ceil_div(out, kBM));
+    rows_reduce_kernel<<<dim3(mtiles * pb.p.nchunks, static_cast<unsigned>((pb.p.NC + 31) / 32)), 256, 0, cs>>>(
+        reinterpret_cast<const float4 *>(part_r), sk, pb.p.nchunks, pb.p.NC, static_cast<int>(out),
+        static_cast<int>(r), 0, g, d_mag, norm, s, dB, r);
+    ++launches;
+  }
+  // 5. dA^T = [W0^T | A^T] x [(s c B)^T | s^2 H]^T, summed and written
+  //    transposed into dA
+  GemmPlan pa = ga;
+  pa.p.part = part_r;
+  pa.p.err = errp;
+  if (launch_gemm(pa, cs, mW0t, mAt, mYh_a, mYc_a, mHh, mHc) != cudaSuccess) return fail();
+  ++launches;
+  {
+    const StreamK sk{pa.p.units, pa.p.ncl, pa.p.kbtot, pa.p.maxseg, pa.p.csize};
+    const unsigned mtiles = static_cast<unsigned>(dora::ceil_div(in, kBM));
+    rows_reduce_kernel<<<dim3(mtiles * pa.p.nchunks, static_cast<unsigned>((pa.p.NC + 31) / 32)), 256, 0, cs>>>(
+        reinterpret_cast<const float4 *>(part_r), sk, pa.p.nchunks, pa.p.NC, static_cast<int>(in),
+        static_cast<int>(r), 1, g, d_mag, norm, s, dA, in);
+    ++launches;
+  }
   dora::count_launches(launches);
   return dora::launch_status();
 }

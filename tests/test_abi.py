@@ -166,3 +166,40 @@ def test_bf16_norm_workspace_and_argument_errors(lib):
     assert rs(None, 4, 64, FAKE, None) == 1
     assert rs(FAKE, 4, 60, FAKE, None) == 3
     assert rs(FAKE + 8, 4, 64, FAKE, None) == 3
+
+
+def test_norm_bwd_workspace_and_argument_errors(lib):
+    d = 8192
+    prev = 0
+    for r in (16, 64, 128, 256, 384, 512, 768):
+        ws = dora.dora_norm_factored_bwd_workspace(d, d, r)
+        assert 0 < ws < d * d * 4          # never the size of an fp32 out x in matrix
+        assert ws > prev
+        prev = ws
+    assert dora.dora_norm_factored_bwd_workspace(d, d, 0) == 0
+    assert dora.dora_norm_factored_bwd_workspace(d, 0, 8) == 0
+    assert dora.dora_norm_factored_bwd_workspace(-1, 8, 8) == 0
+    f = lib.dora_norm_factored_bwd
+    ok = dict(W0=FAKE, A=FAKE, B=FAKE, n=FAKE, g=FAKE, dm=FAKE, s=1.0, out=256, inp=64, r=8, dA=FAKE, dB=FAKE,
+              ws=FAKE, wsb=1 << 30, stream=None)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return f(a["W0"], a["A"], a["B"], a["n"], a["g"], a["dm"], a["s"], a["out"], a["inp"], a["r"], a["dA"],
+                 a["dB"], a["ws"], a["wsb"], a["stream"])
+
+    assert call(out=-1) == 2
+    assert call(inp=0) == 2
+    assert call(r=0) == 2
+    assert call(r=2000) == 2
+    assert call(out=0, dA=None) == 1             # out = 0 still writes dA (zeros)
+    assert call(W0=None) == 1
+    assert call(dm=None) == 1
+    assert call(dB=None) == 1
+    assert call(inp=66) == 3                    # row stride not a multiple of 16 bytes
+    assert call(W0=FAKE + 4) == 3
+    assert call(B=FAKE + 8) == 3
+    assert call(dA=FAKE + 2) == 3
+    assert call(ws=None) == 5
+    assert call(ws=FAKE + 16) == 5
+    assert call(wsb=16) == 5

@@ -531,6 +531,37 @@ def run_report(args):
                               "norm_transient_bytes": nbytes}), flush=True)
             del W0, A, B, m, ws
             torch.cuda.empty_cache()
+    elif args.report == "norm_grad":
+        # gradient through the norm (the variant with the norm not detached):
+        # dora_norm_factored_bwd beside the forward norm at out = in = 8192 over
+        # the swept ranks; algorithmic flops of the products it evaluates
+        # (W0 A^T, B G, A A^T for dB; (c B)^T W0, H A, B^T diag(c) B for dA)
+        for k, r in enumerate(sorted(wl.RANK_SWEEP + (384,))):
+            if args.ranks and r not in args.ranks:
+                continue
+            sh = wl.shape("rank_sweep", r=r)
+            W0, A, B, m = _device_module(sh, wl.seed_for("rank_sweep", k), dev)
+            gen = torch.Generator(device=dev)
+            gen.manual_seed(wl.seed_for("rank_sweep", k) + 11)
+            d_mag = 0.1 * torch.randn(sh.out, device=dev, generator=gen)
+            norm = torch.empty(sh.out, device=dev)
+            g = torch.empty(sh.out, device=dev)
+            ws = torch.empty(dora.dora_norm_factored_workspace(sh.out, sh.inp, sh.r), dtype=torch.uint8, device=dev)
+            nbytes = dora.dora_norm_factored_bwd_workspace(sh.out, sh.inp, sh.r)
+            wsb = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+            dA = torch.empty(sh.r, sh.inp, device=dev)
+            dB = torch.empty(sh.out, sh.r, device=dev)
+            t_norm = _time_ms(lambda: dora.dora_norm_factored(W0, A, B, m, sh.s, norm, g, ws, stream), 20, stream)
+            t_grad = _time_ms(lambda: dora.dora_norm_factored_bwd(W0, A, B, norm, g, d_mag, sh.s, dA, dB, wsb,
+                                                                  stream), 20, stream)
+            flops = 4 * sh.out * sh.inp * sh.r + 4 * sh.r * sh.r * (sh.out + sh.inp)
+            print(json.dumps({"report": "norm_grad", "r": r, "out": sh.out, "in": sh.inp,
+                              "norm_us": t_norm * 1e3, "norm_grad_us": t_grad * 1e3,
+                              "norm_grad_tflops_algorithmic": flops / (t_grad * 1e-3) / 1e12,
+                              "norm_grad_transient_bytes": nbytes,
+                              "dense_fp32_matrix_bytes": sh.out * sh.inp * 4}), flush=True)
+            del W0, A, B, m, ws, wsb, dA, dB
+            torch.cuda.empty_cache()
     elif args.report == "mlp_stack":
         # 32 gate/up (4096 -> 14336) + 32 down (14336 -> 4096) modules, r = 512,
         # T = 16384, training step per module (norm + fwd + bwd), independent seeds
@@ -583,7 +614,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--report", choices=["rank_sweep", "mlp_stack", "bf16_norm"], default=None,
+    ap.add_argument("--report", choices=["rank_sweep", "mlp_stack", "bf16_norm", "norm_grad"], default=None,
                     help="extra per-workload report lines instead of the bench line")
     ap.add_argument("--ranks", type=lambda v: [int(x) for x in v.split(",")], default=None,
                     help="reports rank_sweep / bf16_norm: only these ranks (comma separated)")

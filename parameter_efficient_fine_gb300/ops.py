@@ -1,7 +1,7 @@
 """torch.library registration of the DoRA hot path (integration only).
 
-Five custom ops; each allocates its outputs (and the library's workspace)
-with torch and calls the C entry point of the same name on the current CUDA
+Seven custom ops; each allocates its outputs (and the library's workspace)
+with torch and calls the C entry points of the same names on the current CUDA
 stream.  No arithmetic happens here:
 
   torch.ops.dora.norm_factored(W0, A, B, m, s) -> (norm, g)
@@ -9,6 +9,8 @@ stream.  No arithmetic happens here:
   torch.ops.dora.norm_factored_bf16(W0, A, B, m, n0sq, s) -> (norm, g)   (bf16 W0, A, B)
   torch.ops.dora.compose(base, lora, m, g, norm, s) -> y
   torch.ops.dora.compose_bwd(dy, base, lora, g, norm, s) -> (d_base, d_lora, d_mag)
+  torch.ops.dora.norm_factored_bwd(W0, A, B, norm, g, d_mag, s) -> (dA, dB)   (through the norm)
+  torch.ops.dora.module(base, lora, W0, A, B, m, s) -> (y, norm, g)           (norm not detached)
 
 ``compose`` is differentiable in base, lora and m.  It takes m beside g (the
 norm op's output g = m / norm) so that autograd can deliver dL/dm: with the
@@ -18,6 +20,11 @@ gradient through the norm; this is the reading the library follows),
 dL/dm_j = sum_t dy_tj (base_tj + s lora_tj) / norm_j, which is exactly the
 library's d_mag, and dL/dbase = g dy, dL/dlora = s g dy are its d_base and
 d_lora.  The backward is therefore one call of dora_compose_bwd.
+
+``module`` is the variant with the norm NOT detached: differentiable in base,
+lora, A, B and m.  Its backward is one dora_compose_bwd call followed, when A
+or B needs a gradient, by one dora_norm_factored_bwd call on the d_mag it
+returned (dL/dn = -g d_mag); its norm and g outputs are not differentiable.
 
 Inputs must be contiguous, row-major and on one CUDA device (the C ABI's
 layout); m, n0sq, norm and g are float32, the weights float32 (bfloat16 for
@@ -29,10 +36,11 @@ import torch
 from torch import Tensor
 
 from . import (dora_compose_bwd, dora_compose_bwd_workspace, dora_compose_fwd, dora_norm_factored,
-               dora_norm_factored_bf16, dora_norm_factored_bf16_workspace, dora_norm_factored_workspace,
-               dora_row_sumsq_bf16)
+               dora_norm_factored_bf16, dora_norm_factored_bf16_workspace, dora_norm_factored_bwd,
+               dora_norm_factored_bwd_workspace, dora_norm_factored_workspace, dora_row_sumsq_bf16)
 
-__all__ = ["norm_factored", "row_sumsq", "norm_factored_bf16", "compose", "compose_bwd", "dora_module"]
+__all__ = ["norm_factored", "row_sumsq", "norm_factored_bf16", "compose", "compose_bwd", "norm_factored_bwd",
+           "module", "dora_module"]
 
 
 def _contig(name: str, *ts: Tensor) -> None:
@@ -141,9 +149,76 @@ def _compose_backward(ctx, dy):
 compose.register_autograd(_compose_backward, setup_context=_compose_setup)
 
 
-def dora_module(base: Tensor, lora: Tensor, W0: Tensor, A: Tensor, B: Tensor, m: Tensor, s: float) -> Tensor:
-    """One DoRA module's output from its two matmul results: the factored norm
-    (no gradient through it) and the fused compose, differentiable in base,
-    lora and m."""
+@torch.library.custom_op("dora::norm_factored_bwd", mutates_args=(), device_types="cuda")
+def norm_factored_bwd(W0: Tensor, A: Tensor, B: Tensor, norm: Tensor, g: Tensor, d_mag: Tensor,
+                      s: float) -> tuple[Tensor, Tensor]:
+    """dA, dB through the row norm for dL/dn = -g d_mag (d_mag as compose_bwd returns it)."""
+    _contig("norm_factored_bwd", W0, A, B, norm, g, d_mag)
+    out, inp = W0.shape
+    r = A.shape[0]
+    dA = torch.empty(r, inp, device=W0.device, dtype=torch.float32)
+    dB = torch.empty(out, r, device=W0.device, dtype=torch.float32)
+    ws = torch.empty(max(dora_norm_factored_bwd_workspace(out, inp, r), 1), dtype=torch.uint8, device=W0.device)
+    dora_norm_factored_bwd(W0, A, B, norm, g, d_mag, s, dA, dB, ws)
+    return dA, dB
+
+
+@norm_factored_bwd.register_fake
+def _norm_factored_bwd_fake(W0, A, B, norm, g, d_mag, s):
+    return torch.empty_like(A, dtype=torch.float32), torch.empty_like(B, dtype=torch.float32)
+
+
+@torch.library.custom_op("dora::module", mutates_args=(), device_types="cuda")
+def module(base: Tensor, lora: Tensor, W0: Tensor, A: Tensor, B: Tensor, m: Tensor,
+           s: float) -> tuple[Tensor, Tensor, Tensor]:
+    """y = g (base + s lora) with n and g from the factored norm; returns (y, norm, g)."""
+    _contig("module", base, lora, W0, A, B, m)
+    out, inp = W0.shape
+    r = A.shape[0]
+    norm = torch.empty(out, device=W0.device, dtype=torch.float32)
+    g = torch.empty_like(norm)
+    ws = torch.empty(max(dora_norm_factored_workspace(out, inp, r), 1), dtype=torch.uint8, device=W0.device)
+    dora_norm_factored(W0, A, B, m, s, norm, g, ws)
+    y = torch.empty_like(base)
+    dora_compose_fwd(base, lora, g, s, y)
+    return y, norm, g
+
+
+@module.register_fake
+def _module_fake(base, lora, W0, A, B, m, s):
+    out = W0.shape[0]
+    return torch.empty_like(base), W0.new_empty(out, dtype=torch.float32), W0.new_empty(out, dtype=torch.float32)
+
+
+def _module_setup(ctx, inputs, output):
+    base, lora, W0, A, B, m, s = inputs
+    _, norm, g = output
+    ctx.save_for_backward(base, lora, W0, A, B, norm, g)
+    ctx.s = s
+    ctx.mark_non_differentiable(norm, g)
+
+
+def _module_backward(ctx, dy, d_norm_out, d_g_out):
+    base, lora, W0, A, B, norm, g = ctx.saved_tensors
+    d_base, d_lora, d_mag = compose_bwd(dy.contiguous(), base, lora, g, norm, ctx.s)
+    dA = dB = None
+    if ctx.needs_input_grad[3] or ctx.needs_input_grad[4]:
+        dA, dB = norm_factored_bwd(W0, A, B, norm, g, d_mag, ctx.s)
+    return d_base, d_lora, None, dA, dB, d_mag, None
+
+
+module.register_autograd(_module_backward, setup_context=_module_setup)
+
+
+def dora_module(base: Tensor, lora: Tensor, W0: Tensor, A: Tensor, B: Tensor, m: Tensor, s: float,
+                detach_norm: bool = True) -> Tensor:
+    """One DoRA module's output from its two matmul results.
+
+    detach_norm=True (the page's backward): the factored norm carries no
+    gradient; the fused compose is differentiable in base, lora and m.
+    detach_norm=False: the gradient also flows through the norm into A and B
+    (dora::module)."""
+    if not detach_norm:
+        return module(base, lora, W0.detach(), A, B, m, s)[0]
     norm, g = norm_factored(W0.detach(), A.detach(), B.detach(), m.detach(), s)
     return compose(base, lora, m, g, norm, s)

@@ -10,7 +10,8 @@ def test_ops_registered_and_fake_shapes():
 
     import parameter_efficient_fine_gb300.ops  # noqa: F401  (registers torch.ops.dora.*)
 
-    for name in ("norm_factored", "row_sumsq", "norm_factored_bf16", "compose", "compose_bwd"):
+    for name in ("norm_factored", "row_sumsq", "norm_factored_bf16", "compose", "compose_bwd", "norm_factored_bwd",
+                 "module"):
         assert hasattr(torch.ops.dora, name)
     with FakeTensorMode():
         W0 = torch.empty(64, 32, device="cuda")
@@ -28,3 +29,7 @@ def test_ops_registered_and_fake_shapes():
         n0 = torch.ops.dora.row_sumsq(W16)
         n16, g16 = torch.ops.dora.norm_factored_bf16(W16, A16, B16, m, n0, 1.0)
         assert n0.shape == (64,) and n0.dtype == torch.float32 and n16.shape == (64,) and g16.dtype == torch.float32
+        dA, dB = torch.ops.dora.norm_factored_bwd(W0, A, B, n, g, m, 1.0)
+        assert dA.shape == A.shape and dB.shape == B.shape and dA.dtype == torch.float32
+        y2, n2, g2 = torch.ops.dora.module(base, base, W0, A, B, m, 1.0)
+        assert y2.shape == base.shape and y2.dtype == torch.bfloat16 and n2.shape == (64,) and g2.shape == (64,)

@@ -24,6 +24,9 @@ the whole point of the method is that the GPU path never forms it):
   * Backward with the norm treated as a constant (P1 is silent; reading c2):
         d_base = g*dy,  d_lora = s*g*dy,
         d_mag_j = sum_t dy[t,j]*(base[t,j] + s*lora[t,j]) / n_j .
+  * The compose with its adjacent products folded in (compose_lora_fwd,
+    linear_fwd): the same y, from xa = x A^T and the weights instead of from
+    base and lora.
   * Variant with the norm NOT detached (gradient through n into A and B): the
     chain rule through g = m/n and n_i = ||V_i||, V = W0 + s B A (norm_grad).
 
@@ -58,6 +61,8 @@ __all__ = [
     "compose_fwd_naive_bf16",
     "compose_bwd",
     "norm_grad",
+    "compose_lora_fwd",
+    "linear_fwd",
 ]
 
 
@@ -252,3 +257,22 @@ def norm_grad(W0, A, B, s, n, g, d_mag):
     V = W0 + s * (B @ A)
     dV = (dn / n)[:, None] * V
     return s * (B.T @ dV), s * (dV @ A.T)
+
+
+# ----------------------------------------------------------------------------
+# (d) the compose with its adjacent products: y from x, W0, xa = x A^T, B
+# ----------------------------------------------------------------------------
+
+def compose_lora_fwd(base, xa, B, g, s) -> np.ndarray:
+    """y = g * (base + s * lora) with lora = xa B^T formed here, fp64.
+
+    The layer's products on either side of the compose (P1 ¶从技术架构角度来看:
+    base = x W0^T and lora = (x A^T) B^T); xa [T, r] is x A^T.  The matmul is
+    numpy's in fp64; the compose is compose_fwd.
+    """
+    return compose_fwd(base, _f64(xa) @ _f64(B).T, g, s)
+
+
+def linear_fwd(x, W0, xa, B, g, s) -> np.ndarray:
+    """y = g * (x W0^T + s * xa B^T), the whole DoRA layer output, fp64."""
+    return compose_fwd(_f64(x) @ _f64(W0).T, _f64(xa) @ _f64(B).T, g, s)

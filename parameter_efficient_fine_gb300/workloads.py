@@ -145,6 +145,21 @@ def make_activations(sh: ModuleShape, seed: int, weights: dict | None = None) ->
     return {"base": base, "lora": lora, "dy": dy}
 
 
+def make_layer(sh: ModuleShape, seed: int) -> dict:
+    """Inputs of the compose folded into its adjacent products: x [T, in],
+    W0 [out, in], xa [T, r] and base [T, out] as bf16 bit patterns; B [out, r]
+    and g [out] float32; the scale s.  W0 and B are the module's seeded
+    weights (W0 rounded to bf16); x ~ N(0,1); xa ~ N(0,1), the distribution of
+    x A^T for these x and A, drawn directly; base ~ N(0,1); g = 1 + N(0, sigma_m^2)."""
+    rng = np.random.default_rng([seed, 2])
+    w = make_weights(sh, seed)
+    x = f32_to_bf16_bits(_normal(rng, (sh.T, sh.inp), 1.0))
+    xa = f32_to_bf16_bits(_normal(rng, (sh.T, sh.r), 1.0))
+    base = f32_to_bf16_bits(_normal(rng, (sh.T, sh.out), 1.0))
+    g = (1.0 + sh.sigma_m * rng.standard_normal(size=sh.out)).astype(np.float32)
+    return {"x": x, "W0": f32_to_bf16_bits(w["W0"]), "xa": xa, "B": w["B"], "g": g, "base": base, "s": sh.s}
+
+
 def make_module(sh: ModuleShape, seed: int) -> dict:
     w = make_weights(sh, seed)
     a = make_activations(sh, seed, w)

@@ -366,3 +366,28 @@ def test_norm_grad_row_and_column_subsets():
     dA_c, _ = oracle.norm_grad(W0[:, cols], A[:, cols], B, s, n, g, d_mag)
     assert np.allclose(dB_r, dB[rows], rtol=1e-13, atol=0)
     assert np.allclose(dA_c, dA[:, cols], rtol=1e-13, atol=0)
+
+
+# --------------------------------------------------------------------------
+# the compose with its adjacent products
+# --------------------------------------------------------------------------
+
+def test_layer_forward_one_hot_closed_form():
+    # one-hot token rows pick single entries: base[t, j] = W0[j, k_t] and
+    # lora[t, j] = B[j, q_t], so y[t, j] = g_j (W0[j, k_t] + s B[j, q_t])
+    rng = np.random.default_rng(31)
+    T, inp, out, r, s = 6, 9, 7, 4, 1.7
+    W0 = rng.standard_normal((out, inp))
+    B = rng.standard_normal((out, r))
+    g = rng.uniform(0.5, 1.5, out)
+    k = np.array([0, 3, 8, 3, 5, 1])
+    q = np.array([2, 0, 3, 1, 1, 2])
+    x = np.zeros((T, inp))
+    x[np.arange(T), k] = 1.0
+    xa = np.zeros((T, r))
+    xa[np.arange(T), q] = 1.0
+    want = g[None, :] * (W0[:, k].T + s * B[:, q].T)
+    assert np.allclose(oracle.linear_fwd(x, W0, xa, B, g, s), want, rtol=1e-15, atol=0)
+    base = rng.standard_normal((T, out))
+    want_l = g[None, :] * (base + s * B[:, q].T)
+    assert np.allclose(oracle.compose_lora_fwd(base, xa, B, g, s), want_l, rtol=1e-15, atol=0)

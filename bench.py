@@ -562,6 +562,49 @@ def run_report(args):
                               "dense_fp32_matrix_bytes": sh.out * sh.inp * 4}), flush=True)
             del W0, A, B, m, ws, wsb, dA, dB
             torch.cuda.empty_cache()
+    elif args.report == "fused":
+        # the compose folded into its adjacent products on the high-rank layer
+        # (T = 15360, out = in = 8192, r = 384, bf16), beside the unfused path:
+        # cuBLAS bf16 products (torch.matmul) writing base / lora, then the
+        # library's compose pass
+        sh = wl.shape("high_rank")
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(wl.seed_for("high_rank") + 31)
+        T, inp, out, r = sh.T, sh.inp, sh.out, sh.r
+        x = torch.randn(T, inp, device=dev, generator=gen).bfloat16()
+        W0 = (torch.randn(out, inp, device=dev, generator=gen) / math.sqrt(inp)).bfloat16()
+        xa = torch.randn(T, r, device=dev, generator=gen).bfloat16()
+        B = torch.randn(out, r, device=dev, generator=gen) * sh.sigma_B
+        g = 1 + sh.sigma_m * torch.randn(out, device=dev, generator=gen)
+        base = torch.randn(T, out, device=dev, generator=gen).bfloat16()
+        y = torch.empty(T, out, device=dev, dtype=torch.bfloat16)
+        ws = torch.empty(dora.dora_compose_fused_workspace(out, r), dtype=torch.uint8, device=dev)
+        Bs16 = (sh.s * B).bfloat16()
+        t_lora = _time_ms(lambda: dora.dora_compose_lora_fwd(base, xa, B, g, sh.s, y, ws, stream), 20, stream)
+        t_lin = _time_ms(lambda: dora.dora_linear_fwd(x, W0, xa, B, g, sh.s, y, ws, stream), 10, stream)
+
+        def unfused_lora():
+            lora = torch.matmul(xa, Bs16.t())
+            dora.dora_compose_fwd(base, lora, g, 1.0, y, stream)
+
+        def unfused_linear():
+            b = torch.matmul(x, W0.t())
+            lora = torch.matmul(xa, Bs16.t())
+            dora.dora_compose_fwd(b, lora, g, 1.0, y, stream)
+
+        t_lora_u = _time_ms(unfused_lora, 20, stream)
+        t_lin_u = _time_ms(unfused_linear, 10, stream)
+        t_gemm = _time_ms(lambda: torch.matmul(x, W0.t()), 10, stream)
+        lora_bytes = 2 * T * out * 2 + T * r * 2 + 2 * out * r * 2      # base, y, xa, the two bf16 halves of s B
+        flops = 2 * T * out * (inp + r)
+        print(json.dumps({"report": "fused", "T": T, "in": inp, "out": out, "r": r,
+                          "lora_form_us": t_lora * 1e3, "lora_form_gbs": lora_bytes / (t_lora * 1e-3) / 1e9,
+                          "unfused_lora_matmul_plus_compose_us": t_lora_u * 1e3,
+                          "linear_form_us": t_lin * 1e3,
+                          "linear_form_tflops_algorithmic": flops / (t_lin * 1e-3) / 1e12,
+                          "unfused_two_matmuls_plus_compose_us": t_lin_u * 1e3,
+                          "cublas_base_matmul_us": t_gemm * 1e3,
+                          "cublas_base_matmul_tflops": 2 * T * out * inp / (t_gemm * 1e-3) / 1e12}), flush=True)
     elif args.report == "mlp_stack":
         # 32 gate/up (4096 -> 14336) + 32 down (14336 -> 4096) modules, r = 512,
         # T = 16384, training step per module (norm + fwd + bwd), independent seeds
@@ -614,7 +657,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--report", choices=["rank_sweep", "mlp_stack", "bf16_norm", "norm_grad"], default=None,
+    ap.add_argument("--report", choices=["rank_sweep", "mlp_stack", "bf16_norm", "norm_grad", "fused"], default=None,
                     help="extra per-workload report lines instead of the bench line")
     ap.add_argument("--ranks", type=lambda v: [int(x) for x in v.split(",")], default=None,
                     help="reports rank_sweep / bf16_norm: only these ranks (comma separated)")

@@ -294,6 +294,49 @@ dora_status dora_compose_bwd_noalloc(dora_dtype act, const void *grad_out, const
                                      dora_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
+/* (d) the compose folded into its adjacent products                         */
+/* ------------------------------------------------------------------------ */
+
+/* Bytes of workspace the two entry points below need (host arithmetic; 0 for
+ * an invalid shape): s B split into two bf16 [out, r] matrices. */
+size_t dora_compose_fused_workspace(int64_t out, int64_t r);
+
+/*
+ * y = base + (g-1)*base + g*s*lora with lora = xa B^T computed in the same
+ * kernel: the compose moved into the epilogue of the lora up-projection, so
+ * lora never reaches memory (P1 ¶第二个创新是"融合Triton内核"技术 and
+ * ¶从技术架构角度来看: the stable form, fp32 intermediates).  xa = x A^T is the
+ * caller's down-projection.  s B is split into bf16 hi + lo (residual <= 2^-17
+ * of s B), so each product is exact; fp32 accumulation on the tensor cores;
+ * y is rounded once (nearest even) to bf16.
+ *
+ *   base  bf16 [T, out]   xa  bf16 [T, r]   y  bf16 [T, out]  (16-byte aligned)
+ *   B     float32 [out, r] (4-byte aligned)   g  float32 [out] (16-byte aligned)
+ *   workspace  >= dora_compose_fused_workspace(out, r) bytes, 256-byte aligned
+ *   Sizes: T, out >= 0 (either 0 is a no-op), r >= 1; out % 8 == 0 and
+ *   r % 8 == 0 (16-byte rows for the tensor-memory copies).
+ */
+dora_status dora_compose_lora_fwd(const void *base, const void *xa, const float *B,
+                                  const float *g, float s,
+                                  int64_t T, int64_t out, int64_t r, void *y,
+                                  void *workspace, size_t workspace_bytes,
+                                  dora_stream_t stream);
+
+/*
+ * The whole layer output y = g*(x W0^T + s xa B^T) as ONE tensor-core GEMM
+ * over K = in + r ([x | xa] times [W0 | s B]^T), with the compose in its
+ * epilogue: neither base nor lora is formed.  x [T, in] and W0 [out, in] are
+ * bf16 (16-byte aligned, in % 8 == 0); the rest as dora_compose_lora_fwd.
+ * Since base + s lora stays in fp32 until the single rounding of y, this is the
+ * page's stable evaluation with one rounding fewer.
+ */
+dora_status dora_linear_fwd(const void *x, const void *W0, const void *xa, const float *B,
+                            const float *g, float s,
+                            int64_t T, int64_t in, int64_t out, int64_t r, void *y,
+                            void *workspace, size_t workspace_bytes,
+                            dora_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
 /* diagnostics                                                               */
 /* ------------------------------------------------------------------------ */
 

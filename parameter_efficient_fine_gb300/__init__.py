@@ -24,6 +24,9 @@ __all__ = [
     "dora_norm_factored_bwd_workspace",
     "dora_norm_factored_bwd",
     "dora_compose_fwd",
+    "dora_compose_fused_workspace",
+    "dora_compose_lora_fwd",
+    "dora_linear_fwd",
     "dora_compose_bwd_workspace",
     "dora_compose_bwd",
     "dora_compose_bwd_noalloc",
@@ -57,6 +60,9 @@ _SIGNATURES = {
     "dora_norm_factored_bwd_workspace": (_sz, [_i64, _i64, _i64]),
     "dora_norm_factored_bwd": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _f32, _i64, _i64, _i64, _vp, _vp, _vp, _sz, _vp]),
     "dora_compose_fwd": (_int, [_int, _vp, _vp, _vp, _f32, _i64, _i64, _vp, _vp]),
+    "dora_compose_fused_workspace": (_sz, [_i64, _i64]),
+    "dora_compose_lora_fwd": (_int, [_vp, _vp, _vp, _vp, _f32, _i64, _i64, _i64, _vp, _vp, _sz, _vp]),
+    "dora_linear_fwd": (_int, [_vp, _vp, _vp, _vp, _vp, _f32, _i64, _i64, _i64, _i64, _vp, _vp, _sz, _vp]),
     "dora_compose_bwd_workspace": (_sz, [_i64, _i64]),
     "dora_compose_bwd": (_int, [_int, _vp, _vp, _vp, _vp, _vp, _f32, _i64, _i64, _vp, _vp, _vp, _vp, _sz, _vp]),
     "dora_compose_bwd_noalloc": (_int, [_int, _vp, _vp, _vp, _vp, _vp, _f32, _i64, _i64, _vp, _vp, _vp, _vp]),
@@ -183,6 +189,31 @@ def dora_compose_fwd(base, lora, g, s: float, y, stream=None) -> None:
     st = load_library().dora_compose_fwd(_act(base), _ptr(base), _ptr(lora), _ptr(g), float(s), T, out,
                                          _ptr(y), _stream(stream))
     _check("dora_compose_fwd", st)
+
+
+def dora_compose_fused_workspace(out: int, r: int) -> int:
+    return int(load_library().dora_compose_fused_workspace(out, r))
+
+
+def dora_compose_lora_fwd(base, xa, B, g, s: float, y, workspace, stream=None) -> None:
+    """y = base + (g-1) base + g s (xa B^T), lora formed in the kernel (see include/dora.h)."""
+    T, out = base.shape
+    r = xa.shape[1]
+    st = load_library().dora_compose_lora_fwd(
+        _ptr(base), _ptr(xa), _ptr(B), _ptr(g), float(s), T, out, r, _ptr(y),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
+    _check("dora_compose_lora_fwd", st)
+
+
+def dora_linear_fwd(x, W0, xa, B, g, s: float, y, workspace, stream=None) -> None:
+    """y = g (x W0^T + s xa B^T) as one GEMM with the compose in its epilogue (see include/dora.h)."""
+    T, inp = x.shape
+    out = W0.shape[0]
+    r = xa.shape[1]
+    st = load_library().dora_linear_fwd(
+        _ptr(x), _ptr(W0), _ptr(xa), _ptr(B), _ptr(g), float(s), T, inp, out, r, _ptr(y),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
+    _check("dora_linear_fwd", st)
 
 
 def dora_compose_bwd(grad_out, base, lora, g, norm, s: float, d_base, d_lora, d_mag, workspace,

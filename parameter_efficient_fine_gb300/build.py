@@ -18,8 +18,8 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIBDIR = os.path.join(PKG, "lib")
 LIB = os.path.join(LIBDIR, "libdora.so")
-SOURCES = ("abi.cu", "compose.cu", "norm.cu")
-HEADERS = ("common.cuh",)
+SOURCES = ("abi.cu", "compose.cu", "norm.cu", "fused.cu")
+HEADERS = ("common.cuh", "tc_ptx.cuh")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",

@@ -27,6 +27,11 @@ dora_status current_device(DeviceInfo *info, int *device);
 
 inline bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
+// The device error word that the library's kernels write when a bounded wait
+// gives up (read and cleared by dora_device_error); sets up the tensor-core
+// kernels' shared-memory limits on first use of a device.
+dora_status error_word(int device, int **errp);
+
 inline dora_status launch_status() {
   return cudaGetLastError() == cudaSuccess ? DORA_OK : DORA_ERR_CUDA;
 }

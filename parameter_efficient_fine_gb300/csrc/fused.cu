@@ -1,0 +1,569 @@
+// The DoRA compose folded into the epilogue of the GEMM that produces its
+// input, on GB300 (sm_103a) tensor cores.
+//
+// Method source: web page "人工智能训练新突破：Anthropic团队破解大模型微调内存瓶颈难题"
+// (techwalker.com).  Its fused kernel merges the four elementwise passes of the
+// compose into one, in the stable form
+//     y = base + (g - 1) base + g s lora,
+// with base = x W0^T and lora = (x A^T) B^T the products on either side.  Here
+// the compose moves into the epilogue of those products, so y is written
+// directly from the tensor-memory accumulator:
+//
+//   dora_compose_lora_fwd  (the lora up-projection):
+//       acc = xa (s B)^T                       K = r, xa = x A^T (bf16)
+//       y   = base + (g - 1) base + g acc      base read once, lora never stored
+//   dora_linear_fwd        (both products, one K-concatenated GEMM):
+//       acc = [x | xa] [W0 | s B]^T            K = in + r
+//       y   = g acc                            neither base nor lora is stored
+//
+// Operands are bf16, so every product is exact in fp32; the fp32 B is scaled
+// by s and split into bf16 hi + lo (|lo| <= 2^-9 |hi|, residual <= 2^-17 of
+// s B), and xa multiplies both (the xa segment of K appears twice, against hi
+// and against lo).  Accumulation is fp32 in tensor memory; y is rounded once
+// to bf16.
+//
+// Kernel structure (persistent, one CTA per SM, 192 threads):
+//   warp 0      TMA producer: per K block a [128 x 64] bf16 box of the token
+//               side and a [256 x 64] box of the weight side (128-byte swizzle)
+//   warp 1      allocates 512 tensor-memory columns (two 256-column
+//               accumulators, so a tile's epilogue overlaps the next tile's
+//               MMAs); one lane issues tcgen05.mma (M = 128, N = 256, K = 16)
+//   warps 2..5  epilogue: thread = row of the tile (its tensor-memory lane).
+//               Each warp owns 4 KB staging slots in shared memory for its 32
+//               rows (one [32 x 64] bf16 box, 128-byte swizzle) and runs its
+//               own pipeline: per 64-column quarter the accumulator columns,
+//               g (uniform 128-bit loads) and, for the lora form, the base
+//               quarter that the warp's lane 0 loaded into the slot by TMA
+//               one tile ahead; y is written into the slot in place and
+//               stored by TMA.  The epilogue warps never wait for one another
+// Every wait on a shared-memory barrier is bounded; a wait that gives up
+// records a code in the library's device error word and all roles drain and
+// leave.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "tc_ptx.cuh"
+
+namespace {
+
+constexpr int kFM = 128;        // tile rows (tokens) = tensor-memory lanes
+constexpr int kFN = 256;        // tile columns (outputs) = N of one MMA
+constexpr int kFK = 64;         // bf16 per K block: one 128-byte swizzled row
+constexpr int kFQ = 64;         // columns per epilogue quarter (one 128-byte box row)
+constexpr int kFThreads = 192;
+constexpr int kGroupM = 16;     // M tiles per tile-order group (L2 reuse of the weight tiles)
+constexpr int kFMaxCtas = 256;
+constexpr int kFSmemMax = 232448;
+constexpr unsigned kABytes = kFM * kFK * 2;     // 16 KB
+constexpr unsigned kBBytes = kFN * kFK * 2;     // 32 KB
+constexpr unsigned kSlotBytes = 32 * kFQ * 2;  // 4 KB: one warp's 32 rows of a quarter
+constexpr unsigned long long kFWaitNs = 2000000000ull;
+
+struct FusedParams {
+  int T, out;
+  int nseg;             // K segments: (x, W0), (xa, sB_hi), (xa, sB_lo); the lora form has the last two
+  int kb[3];            // K blocks per segment
+  int kbtot;            // 64-wide K blocks per tile over all segments
+  int mtiles, ntiles, tiles;
+  int stages;
+  int nslots;           // staging slots per epilogue warp: 4 with base (one per quarter), 2 without
+  int has_base;
+  const float *g;
+  int *err;
+};
+
+__device__ __forceinline__ void tile_mn(int t, int mtiles, int ntiles, int *mt, int *nt) {
+  const int per = kGroupM * ntiles;
+  const int grp = t / per;
+  const int m0 = grp * kGroupM;
+  const int gm = min(kGroupM, mtiles - m0);
+  const int r = t - grp * per;
+  *mt = m0 + r % gm;
+  *nt = r / gm;
+}
+
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, uint32_t src, int x, int y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y), "r"(src)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// this thread's bulk stores have finished reading shared memory, all but the
+// most recent one (wait_read1) or all of them (wait_read0)
+__device__ __forceinline__ void bulk_wait_read1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__global__ void __launch_bounds__(kFThreads, 1)
+fused_compose_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUtensorMap mA1,
+                     const __grid_constant__ CUtensorMap mB0, const __grid_constant__ CUtensorMap mB1,
+                     const __grid_constant__ CUtensorMap mB2, const __grid_constant__ CUtensorMap mC,
+                     const __grid_constant__ CUtensorMap mY, const FusedParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int S = p.stages;
+  const unsigned stage_bytes = kABytes + kBBytes;
+  // staging: [slot][epilogue warp][32 rows x 128 bytes]
+  uint8_t *cbuf = smem + static_cast<size_t>(S) * stage_bytes;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(cbuf + static_cast<size_t>(p.nslots) * 4 * kSlotBytes);
+  // barriers: full[S], empty[S], accf[2], acce[2], fin, cfull[4 slots][4 warps]
+  SharedCtl *ctl = reinterpret_cast<SharedCtl *>(bars + 2 * S + 21);
+  const uint32_t full0 = smem_u32(bars);
+  const uint32_t empty0 = full0 + 8u * S;
+  const uint32_t accf0 = empty0 + 8u * S;
+  const uint32_t acce0 = accf0 + 16;
+  const uint32_t fin = acce0 + 16;
+  const uint32_t cfull0 = fin + 8;
+  const uint32_t cbase = smem_u32(cbuf);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full0 + 8u * s, 1);
+      mbar_init(empty0 + 8u * s, 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(accf0 + 8u * b, 1);
+      mbar_init(acce0 + 8u * b, 4);   // one arrival per epilogue warp
+    }
+    mbar_init(fin, 1);
+    for (int k = 0; k < 16; ++k) mbar_init(cfull0 + 8u * k, 1);
+    ctl->abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_map(&mA1);
+    prefetch_map(&mB1);
+    prefetch_map(&mB2);
+    prefetch_map(&mY);
+    if (p.nseg == 3) {
+      prefetch_map(&mA0);
+      prefetch_map(&mB0);
+    }
+    if (p.has_base) prefetch_map(&mC);
+  }
+  if (warp == 1) {
+    __syncwarp();
+    tmem_alloc(smem_u32(&ctl->tmem_base), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl->tmem_base;
+  const int cta = static_cast<int>(blockIdx.x);
+  const int ncta = static_cast<int>(gridDim.x);
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------------------------------------------------------- producer
+      int stage = 0;
+      uint32_t phase = 0;
+      int issued = 0;
+      bool ok = true;
+      for (int t = cta; t < p.tiles && ok; t += ncta) {
+        int mt, nt;
+        tile_mn(t, p.mtiles, p.ntiles, &mt, &nt);
+        // the tile's K blocks, segment after segment (the lora form has none in segment 0)
+        for (int kb = 0; kb < p.kbtot && ok; ++kb) {
+          if (!wait_bounded_ns(empty0 + 8u * stage, phase ^ 1u, ctl, p.err, 12, kFWaitNs)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = full0 + 8u * stage;
+          mbar_expect_tx(fb, stage_bytes);
+          const uint32_t xs = smem_u32(smem + static_cast<size_t>(stage) * stage_bytes);
+          int ks = kb;
+          int sg = 0;
+          if (ks >= p.kb[0]) {
+            ks -= p.kb[0];
+            sg = 1;
+            if (ks >= p.kb[1]) {
+              ks -= p.kb[1];
+              sg = 2;
+            }
+          }
+          const CUtensorMap *ma = sg == 0 ? &mA0 : &mA1;
+          const CUtensorMap *mb = sg == 0 ? &mB0 : (sg == 1 ? &mB1 : &mB2);
+          tma_load_2d(xs, ma, ks * kFK, mt * kFM, fb);
+          tma_load_2d(xs + kABytes, mb, ks * kFK, nt * kFN, fb);
+          ++issued;
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        // copies in flight: the last min(issued, S) stages and the base loads
+        int st = stage;
+        uint32_t ph = phase;
+        for (int k = 0; k < S && k < issued; ++k) {
+          if (--st < 0) {
+            st = S - 1;
+            ph ^= 1u;
+          }
+          wait_drain_ns(full0 + 8u * st, ph, kFWaitNs);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------------------------------------------------------- MMA issuer
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      const uint32_t idesc = idesc_bf16(kFN);
+      int li = 0;
+      for (int t = cta; t < p.tiles && ok; t += ncta, ++li) {
+        const int buf = li & 1;
+        const uint32_t use = static_cast<uint32_t>(li >> 1);
+        if (!wait_bounded_ns(acce0 + 8u * buf, (use & 1u) ^ 1u, ctl, p.err, 13, kFWaitNs)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d = tmem + static_cast<uint32_t>(buf * kFN);
+        for (int kb = 0; kb < p.kbtot; ++kb) {
+          if (!wait_bounded_ns(full0 + 8u * stage, phase, ctl, p.err, 14, kFWaitNs)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t xs = smem_u32(smem + static_cast<size_t>(stage) * stage_bytes);
+#pragma unroll
+          for (int k = 0; k < kFK / 16; ++k) {
+            const uint32_t ko = static_cast<uint32_t>(k) * 32u;   // 16 bf16 = 32 bytes along the swizzled row
+            mma_bf16_ss(d, sdesc<32>(xs + ko), sdesc<32>(xs + kABytes + ko), idesc, (kb | k) != 0 ? 1u : 0u);
+          }
+          mma_commit(empty0 + 8u * stage);
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        mma_commit(accf0 + 8u * buf);
+      }
+      mma_commit(fin);
+      wait_drain_ns(fin, 0, kFWaitNs);
+    }
+  } else {
+    // ---------------------------------------------------------------- epilogue
+    const int quad = warp & 3;               // rows quad * 32 + lane of the tile = tensor-memory lanes
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+    // this warp's slot s: cbuf + (s * 4 + quad) * 4 KB (1024-byte aligned, so
+    // the 128-byte swizzle of a [32 x 64] box has the same phase as in a full tile)
+    auto slot_off = [&](int s) { return static_cast<uint32_t>((s * 4 + quad) * kSlotBytes); };
+    auto cfull = [&](int s) { return cfull0 + 8u * static_cast<uint32_t>(s * 4 + quad); };
+    // base quarter q of tile t into slot q (lora form; lane 0): the base of a
+    // tile is requested while the previous tile is being written out, one
+    // tile ahead.  Per slot: whether a load was issued, and the parity of the
+    // number issued (for the drain after an abort)
+    uint32_t any_load = 0, load_par = 0;
+    auto load_base = [&](int t, int q) {
+      int mt, nt;
+      tile_mn(t, p.mtiles, p.ntiles, &mt, &nt);
+      mbar_expect_tx(cfull(q), kSlotBytes);
+      tma_load_2d(cbase + slot_off(q), &mC, nt * kFN + q * kFQ, mt * kFM + quad * 32, cfull(q));
+      any_load |= 1u << q;
+      load_par ^= 1u << q;
+    };
+    if (p.has_base && lane == 0 && cta < p.tiles)
+      for (int q = 0; q < 4; ++q) load_base(cta, q);
+    int li = 0;
+    bool ok = true;
+    for (int t = cta; t < p.tiles && ok; t += ncta, ++li) {
+      int mt, nt;
+      tile_mn(t, p.mtiles, p.ntiles, &mt, &nt);
+      const int tnext = t + ncta;
+      const int buf = li & 1;
+      const uint32_t use = static_cast<uint32_t>(li >> 1);
+      const bool got = wait_bounded_ns(accf0 + 8u * buf, use & 1u, ctl, p.err, 15, kFWaitNs);
+      if (!__all_sync(0xffffffffu, got)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const bool rows_in = mt * kFM + quad * 32 < p.T;   // any of this warp's rows inside y
+      for (int q = 0; q < 4; ++q) {
+        const int sl = q % p.nslots;
+        const int gcol0 = nt * kFN + q * kFQ;
+        if (p.has_base) {
+          // slot q holds this tile's base quarter: the slot's load number li
+          const bool gb = wait_bounded_ns(cfull(q), static_cast<uint32_t>(li) & 1u, ctl, p.err, 16, kFWaitNs);
+          if (!__all_sync(0xffffffffu, gb)) {
+            ok = false;
+            break;
+          }
+        } else {
+          // slot sl: this warp's store from two quarters ago must have read it
+          // (the most recent store may still be reading the other slot)
+          if (lane == 0) bulk_wait_read1();
+          __syncwarp();
+        }
+        // g of the quarter's 64 columns: 16 uniform 128-bit loads issued
+        // together (one latency), zero past `out`
+        float4 gq[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k)
+          gq[k] = gcol0 + 4 * k < p.out ? __ldg(reinterpret_cast<const float4 *>(p.g + gcol0) + k)
+                                        : make_float4(0.f, 0.f, 0.f, 0.f);
+        float v[2][32];
+        const uint32_t col0 = static_cast<uint32_t>(buf * kFN + q * kFQ);
+        tmem_ld32(lane_addr + col0, v[0]);
+        tmem_ld32(lane_addr + col0 + 32, v[1]);
+        if (q == 3) {
+          // the accumulator is read out: the MMA lane may start the tile after next
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(acce0 + 8u * buf);
+        }
+        uint8_t *crow = cbuf + slot_off(sl) + lane * 128;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          // 16-byte chunk j of the row (8 columns), at its swizzled position
+          uint4 *pc = reinterpret_cast<uint4 *>(crow + ((j ^ (lane & 7)) << 4));
+          const float *a = &v[j >> 2][(j & 3) * 8];
+          const float gv[8] = {gq[2 * j].x, gq[2 * j].y, gq[2 * j].z, gq[2 * j].w,
+                               gq[2 * j + 1].x, gq[2 * j + 1].y, gq[2 * j + 1].z, gq[2 * j + 1].w};
+          float yv[8];
+          if (p.has_base) {
+            const uint4 braw = *pc;
+            const __nv_bfloat162 *bb = reinterpret_cast<const __nv_bfloat162 *>(&braw);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float2 b2 = __bfloat1622float2(bb[e]);
+              yv[2 * e] = b2.x + fmaf(gv[2 * e] - 1.0f, b2.x, gv[2 * e] * a[2 * e]);
+              yv[2 * e + 1] = b2.y + fmaf(gv[2 * e + 1] - 1.0f, b2.y, gv[2 * e + 1] * a[2 * e + 1]);
+            }
+          } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) yv[e] = gv[e] * a[e];
+          }
+          uint4 o;
+          o.x = pack_bf16x2(yv[0], yv[1]);
+          o.y = pack_bf16x2(yv[2], yv[3]);
+          o.z = pack_bf16x2(yv[4], yv[5]);
+          o.w = pack_bf16x2(yv[6], yv[7]);
+          *pc = o;
+        }
+        // make the writes visible to the TMA store, then lane 0 stores the
+        // warp's 32 rows of the quarter
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          const bool stored = rows_in && gcol0 < p.out;
+          if (stored) {
+            tma_store_2d(&mY, cbase + slot_off(sl), gcol0, mt * kFM + quad * 32);
+            bulk_commit();
+          }
+          if (p.has_base && q > 0 && tnext < p.tiles) {
+            // the previous quarter's store has read slot q - 1: it takes the
+            // next tile's base quarter
+            if (stored) bulk_wait_read1();
+            else bulk_wait_read0();
+            load_base(tnext, q - 1);
+          }
+        }
+      }
+      if (!ok) break;
+      if (p.has_base && lane == 0 && tnext < p.tiles) {
+        bulk_wait_read0();
+        load_base(tnext, 3);
+      }
+    }
+    if (lane == 0) {
+      bulk_wait0();
+      if (!ok) {
+        // base copies that may still be in flight into this warp's slots: the
+        // k-th load of a slot completes phase k - 1, of parity (count - 1) & 1
+        for (int q = 0; q < 4; ++q)
+          if ((any_load >> q) & 1u) wait_drain_ns(cfull(q), ((load_par >> q) & 1u) ^ 1u, kFWaitNs);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) {
+    __syncwarp();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// s B (fp32 [out, r]) -> bf16 hi = RN(s B), lo = RN(s B - hi), both [out, r]
+__global__ void __launch_bounds__(256) split_sb_kernel(const float *__restrict__ B, long long n, float s,
+                                                       __nv_bfloat16 *__restrict__ hi,
+                                                       __nv_bfloat16 *__restrict__ lo) {
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
+    const float v = s * B[i];
+    const __nv_bfloat16 h = __float2bfloat16_rn(v);
+    hi[i] = h;
+    lo[i] = __float2bfloat16_rn(v - __bfloat162float(h));
+  }
+}
+
+struct FusedPlan {
+  FusedParams p;
+  size_t smem_bytes;
+  int ctas;
+};
+
+bool plan_fused(int64_t T, int64_t in, int64_t out, int64_t r, bool has_base, int sms, FusedPlan *fp) {
+  FusedParams &p = fp->p;
+  p = FusedParams{};
+  p.T = static_cast<int>(T);
+  p.out = static_cast<int>(out);
+  p.nseg = has_base ? 2 : 3;
+  p.kb[0] = has_base ? 0 : static_cast<int>(dora::ceil_div(in, kFK));
+  p.kb[1] = p.kb[2] = static_cast<int>(dora::ceil_div(r, kFK));
+  p.kbtot = p.kb[0] + p.kb[1] + p.kb[2];
+  p.mtiles = static_cast<int>(dora::ceil_div(T, kFM));
+  p.ntiles = static_cast<int>(dora::ceil_div(out, kFN));
+  const long long tiles = static_cast<long long>(p.mtiles) * p.ntiles;
+  if (tiles >= (1ll << 31)) return false;
+  p.tiles = static_cast<int>(tiles);
+  p.has_base = has_base ? 1 : 0;
+  p.nslots = has_base ? 4 : 2;
+  const size_t fixed = 1024 + static_cast<size_t>(p.nslots) * 4 * kSlotBytes + 512;
+  const size_t stage_bytes = kABytes + kBBytes;
+  p.stages = static_cast<int>((kFSmemMax - fixed) / stage_bytes);
+  if (p.stages > 8) p.stages = 8;
+  if (p.stages < 2) return false;
+  fp->smem_bytes = fixed + static_cast<size_t>(p.stages) * stage_bytes;
+  fp->ctas = p.tiles < sms ? p.tiles : sms;
+  return true;
+}
+
+// bf16 [rows, cols] (row stride ld elements) with a [box_rows x 64] box, 128-byte swizzle
+bool map_bf16(CUtensorMap *map, const void *base, int64_t rows, int64_t cols, int64_t ld, int box_rows) {
+  return make_map(map, base, true, rows, cols, ld, box_rows, 128);
+}
+
+dora_status fused_init(int device, int **errp) {
+  static std::mutex mu;
+  static bool done[64] = {};
+  std::lock_guard<std::mutex> lock(mu);
+  if (device < 0 || device >= 64) return DORA_ERR_CUDA;
+  dora_status st = dora::error_word(device, errp);
+  if (st != DORA_OK) return st;
+  if (!done[device]) {
+    if (cudaFuncSetAttribute(fused_compose_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kFSmemMax) !=
+        cudaSuccess)
+      return DORA_ERR_CUDA;
+    done[device] = true;
+  }
+  return DORA_OK;
+}
+
+// shared by both entry points: x / W0 only for the linear form, base only for
+// the lora form
+dora_status fused_run(const void *x, const void *W0, const void *base, const void *xa, const float *B,
+                      const float *g, float s, int64_t T, int64_t in, int64_t out, int64_t r, void *y,
+                      void *workspace, size_t workspace_bytes, dora_stream_t stream) {
+  const bool lora_form = base != nullptr;
+  dora::DeviceInfo info;
+  int device = 0;
+  dora_status st = dora::current_device(&info, &device);
+  if (st != DORA_OK) return st;
+  int *errp = nullptr;
+  st = fused_init(device, &errp);
+  if (st != DORA_OK) return st;
+  const int sms = info.sms < kFMaxCtas ? info.sms : kFMaxCtas;
+  FusedPlan fp;
+  if (!plan_fused(T, in, out, r, lora_form, sms, &fp)) return DORA_ERR_SHAPE;
+  fp.p.g = g;
+  fp.p.err = errp;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  __nv_bfloat16 *hi = static_cast<__nv_bfloat16 *>(workspace);
+  __nv_bfloat16 *lo = reinterpret_cast<__nv_bfloat16 *>(static_cast<uint8_t *>(workspace) +
+                                                        static_cast<size_t>(dora::round_up(out * r * 2, 256)));
+  uint64_t launches = 0;
+  const long long n = out * r;
+  long long blocks = dora::ceil_div(n, 256);
+  if (blocks > static_cast<long long>(sms) * 8) blocks = static_cast<long long>(sms) * 8;
+  split_sb_kernel<<<static_cast<unsigned>(blocks), 256, 0, cs>>>(B, n, s, hi, lo);
+  ++launches;
+
+  CUtensorMap mA0, mA1, mB0, mB1, mB2, mC, mY;
+  bool ok = map_bf16(&mA1, xa, T, r, r, kFM) && map_bf16(&mB1, hi, out, r, r, kFN) &&
+            map_bf16(&mB2, lo, out, r, r, kFN) && map_bf16(&mY, y, T, out, out, 32);
+  if (lora_form) {
+    ok = ok && map_bf16(&mC, base, T, out, out, 32);
+    mA0 = mA1;
+    mB0 = mB1;
+  } else {
+    ok = ok && map_bf16(&mA0, x, T, in, in, kFM) && map_bf16(&mB0, W0, out, in, in, kFN);
+    mC = mY;
+  }
+  if (!ok) {
+    dora::count_launches(launches);
+    return DORA_ERR_CUDA;
+  }
+  fused_compose_kernel<<<static_cast<unsigned>(fp.ctas), kFThreads, fp.smem_bytes, cs>>>(mA0, mA1, mB0, mB1, mB2, mC,
+                                                                                         mY, fp.p);
+  ++launches;
+  dora::count_launches(launches);
+  return dora::launch_status();
+}
+
+}  // namespace
+
+extern "C" size_t dora_compose_fused_workspace(int64_t out, int64_t r) {
+  if (out < 0 || r < 1 || out >= (1ll << 31) || r >= (1ll << 20)) return 0;
+  const size_t piece = static_cast<size_t>(dora::round_up(out * r * 2, 256));
+  return piece > 0 ? 2 * piece : 256;
+}
+
+namespace {
+dora_status fused_check(const void *xa, const float *B, const float *g, int64_t T, int64_t out, int64_t r, void *y,
+                        void *workspace, size_t workspace_bytes) {
+  if (!xa || !B || !g || !y) return DORA_ERR_NULL;
+  if (!workspace) return DORA_ERR_WORKSPACE;
+  // TMA: 16-byte aligned bases and row strides (bf16 rows of out and r elements)
+  if (out % 8 != 0 || r % 8 != 0) return DORA_ERR_ALIGN;
+  if (!dora::aligned(xa, 16) || !dora::aligned(y, 16) || !dora::aligned(B, 4) || !dora::aligned(g, 16))
+    return DORA_ERR_ALIGN;
+  if (!dora::aligned(workspace, 256) || workspace_bytes < dora_compose_fused_workspace(out, r))
+    return DORA_ERR_WORKSPACE;
+  (void)T;
+  return DORA_OK;
+}
+}  // namespace
+
+extern "C" dora_status dora_compose_lora_fwd(const void *base, const void *xa, const float *B, const float *g, float s,
+                                             int64_t T, int64_t out, int64_t r, void *y, void *workspace,
+                                             size_t workspace_bytes, dora_stream_t stream) {
+  if (T < 0 || out < 0 || r < 1 || T >= (1ll << 31) || out >= (1ll << 31) || r >= (1ll << 20)) return DORA_ERR_SHAPE;
+  if (T == 0 || out == 0) return DORA_OK;
+  if (!base) return DORA_ERR_NULL;
+  dora_status st = fused_check(xa, B, g, T, out, r, y, workspace, workspace_bytes);
+  if (st != DORA_OK) return st;
+  if (!dora::aligned(base, 16)) return DORA_ERR_ALIGN;
+  return fused_run(nullptr, nullptr, base, xa, B, g, s, T, 0, out, r, y, workspace, workspace_bytes, stream);
+}
+
+extern "C" dora_status dora_linear_fwd(const void *x, const void *W0, const void *xa, const float *B, const float *g,
+                                       float s, int64_t T, int64_t in, int64_t out, int64_t r, void *y,
+                                       void *workspace, size_t workspace_bytes, dora_stream_t stream) {
+  if (T < 0 || out < 0 || in < 1 || r < 1 || T >= (1ll << 31) || out >= (1ll << 31) || in >= (1ll << 31) ||
+      r >= (1ll << 20))
+    return DORA_ERR_SHAPE;
+  if (T == 0 || out == 0) return DORA_OK;
+  if (!x || !W0) return DORA_ERR_NULL;
+  dora_status st = fused_check(xa, B, g, T, out, r, y, workspace, workspace_bytes);
+  if (st != DORA_OK) return st;
+  if (in % 8 != 0 || !dora::aligned(x, 16) || !dora::aligned(W0, 16)) return DORA_ERR_ALIGN;
+  return fused_run(x, W0, nullptr, xa, B, g, s, T, in, out, r, y, workspace, workspace_bytes, stream);
+}

@@ -66,6 +66,7 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "tc_ptx.cuh"
 
 namespace {
 
@@ -163,202 +164,6 @@ __device__ __forceinline__ int piece_end(long long u, long long u_end, int kb0, 
   return kbe;
 }
 
-// ---------------------------------------------------------------------------
-// PTX wrappers
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t smem_u32(const void *p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-__device__ __forceinline__ unsigned long long globaltimer() {
-  unsigned long long t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-__device__ __forceinline__ void fence_barrier_init() {
-  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
-          dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
-      : "memory");
-}
-// the same box into the same shared-memory offset of every CTA in `mask`,
-// completing bytes on each destination CTA's barrier at offset `bar`
-__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar,
-                                               uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster "
-      "[%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "h"(mask)
-      : "memory");
-}
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-// bring `bytes` (a multiple of 16) at a 16-byte aligned address into L2
-__device__ __forceinline__ void prefetch_l2(const void *ptr, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(ptr)), "r"(bytes)
-               : "memory");
-}
-__device__ __forceinline__ void prefetch_map(const CUtensorMap *map) {
-  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
-}
-__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
-               : "memory");
-}
-__device__ __forceinline__ void tmem_relinquish() {
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
-}
-__device__ __forceinline__ void tc_fence_before() {
-  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-// D (+)= A * B on the tensor core, fp32 accumulator in tensor memory at `d`;
-// A (M side) in tensor memory at column address `a`, B (N side) in shared
-// memory by descriptor; accumulate when acc != 0
-__device__ __forceinline__ void mma_tf32_ta(uint32_t d, uint32_t a, uint64_t bdesc, uint32_t idesc, uint32_t acc) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
-      "r"(a), "l"(bdesc), "r"(idesc), "r"(acc)
-      : "memory");
-}
-__device__ __forceinline__ void mma_bf16_ta(uint32_t d, uint32_t a, uint64_t bdesc, uint32_t idesc, uint32_t acc) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
-      "r"(a), "l"(bdesc), "r"(idesc), "r"(acc)
-      : "memory");
-}
-// 8 consecutive 32-bit columns of this thread's tensor-memory lane
-__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&v)[8]) {
-  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
-               "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
-               : "memory");
-}
-__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-               : "memory");
-}
-// arrive (once MMAs complete) on the barrier at offset `bar` of every CTA in `mask`
-__device__ __forceinline__ void mma_commit_mc(uint32_t bar, uint16_t mask) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-                   bar),
-               "h"(mask)
-               : "memory");
-}
-// *p += (a, b, c, d) in global memory, fp32 round-to-nearest, no return value
-__device__ __forceinline__ void red_add_f32x4(float4 *p, float a, float b, float c, float d) {
-  asm volatile("red.relaxed.gpu.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d)
-               : "memory");
-}
-// 32 consecutive fp32 columns of this thread's tensor-memory lane (the load and
-// its wait in one statement, so the registers are defined only after the wait)
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
-  uint32_t r[32];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n\t"
-      "tcgen05.wait::ld.sync.aligned;"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr)
-      : "memory");
-#pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-}
-__device__ __forceinline__ uint32_t tf32_rna(float x) {
-  uint32_t r;
-  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-  return r;
-}
-// two floats -> two bf16 (nearest even), a in the low half
-__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
-  __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
-  return *reinterpret_cast<uint32_t *>(&h);
-}
-
-// Shared-memory matrix descriptor of a K-major operand whose rows are one
-// swizzle span long: BK = 16 -> 64-byte rows, 64-byte swizzle, 8-row groups
-// 512 bytes apart; BK = 32 -> 128-byte rows, 128-byte swizzle, 1024 bytes.
-template <int BK>
-__device__ __forceinline__ uint64_t sdesc(uint32_t saddr) {
-  static_assert(BK == 16 || BK == 32, "K block of 16 or 32 fp32");
-  constexpr uint64_t sbo = 8 * BK * 4;
-  constexpr uint64_t mode = BK == 16 ? 4 : 2;          // 64-byte / 128-byte swizzle
-  uint64_t d = 0;
-  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);   // start address >> 4      [0,14)
-  d |= static_cast<uint64_t>(1) << 16;                   // leading offset (unused)  [16,30)
-  d |= (sbo >> 4) << 32;                                 // stride offset            [32,46)
-  d |= static_cast<uint64_t>(1) << 46;                   // descriptor version       [46,48)
-  d |= mode << 61;                                       // swizzle mode             [61,64)
-  return d;
-}
-// physical 16-byte chunk of logical chunk c in row `row` of such a tile (the
-// tile starts on a 1024-byte boundary): the swizzle XORs the chunk index with
-// address bits 7.. of the row
-template <int BK>
-__device__ __forceinline__ int swz_chunk(int c, int row) {
-  return BK == 16 ? c ^ ((row >> 1) & 3) : c ^ (row & 7);
-}
-// Instruction descriptor: kind::tf32, fp32 accumulator, both operands K-major,
-// M = 128, N = n.
-__host__ __device__ __forceinline__ uint32_t idesc_tf32(int n) {
-  return (1u << 4)                                  // D format: f32
-         | (2u << 7)                                // A format: tf32
-         | (2u << 10)                               // B format: tf32
-         | (static_cast<uint32_t>(n >> 3) << 17)    // N >> 3
-         | (static_cast<uint32_t>(kBM >> 4) << 24); // M >> 4
-}
-// Instruction descriptor: kind::f16 with bf16 operands, fp32 accumulator,
-// both K-major, M = 128, N = n.
-__host__ __device__ __forceinline__ uint32_t idesc_bf16(int n) {
-  return (1u << 4)                                  // D format: f32
-         | (1u << 7)                                // A format: bf16
-         | (1u << 10)                               // B format: bf16
-         | (static_cast<uint32_t>(n >> 3) << 17)    // N >> 3
-         | (static_cast<uint32_t>(kBM >> 4) << 24); // M >> 4
-}
-
 // CTA that owns work unit u when `units` are split evenly over `ctas`.
 __host__ __device__ __forceinline__ long long unit_begin(long long c, long long units, long long ctas) {
   return c * units / ctas;
@@ -391,32 +196,16 @@ __host__ __device__ __forceinline__ void tile_coords(int t, int nchunks, int sym
   }
 }
 
-struct SharedCtl {
-  volatile int abort;
-  uint32_t tmem_base;
-};
-
+// bounded wait whose limit (g_wait_limit_ns, a test hook) is read only on the
+// slow path, so the common case -- the phase already complete -- touches no
+// global memory
 __device__ bool wait_bounded(uint32_t bar, uint32_t parity, SharedCtl *ctl, int *err, int code) {
   if (mbar_try_wait(bar, parity)) return true;
-  const unsigned long long t0 = globaltimer();
-  for (uint32_t i = 1;; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if (ctl->abort) return false;
-    if ((i & 63u) == 0 && globaltimer() - t0 > *reinterpret_cast<volatile unsigned long long *>(&g_wait_limit_ns)) {
-      ctl->abort = 1;
-      atomicCAS(err, 0, code);
-      return false;
-    }
-  }
+  return wait_bounded_ns(bar, parity, ctl, err, code, *reinterpret_cast<volatile unsigned long long *>(&g_wait_limit_ns));
 }
 
 // wait used while leaving after an abort: ignores the abort flag
-__device__ void wait_drain(uint32_t bar, uint32_t parity) {
-  const unsigned long long t0 = globaltimer();
-  while (!mbar_try_wait(bar, parity)) {
-    if (globaltimer() - t0 > kWaitLimitNs) return;
-  }
-}
+__device__ void wait_drain(uint32_t bar, uint32_t parity) { wait_drain_ns(bar, parity, kWaitLimitNs); }
 
 // ---------------------------------------------------------------------------
 // the tensor-core GEMM (GRAM, NORM or ROWS mode)
@@ -1120,15 +909,6 @@ struct Tc16Params {
   int ldb;
 };
 
-__device__ __forceinline__ void mma_bf16_ss(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t acc) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc)
-      : "memory");
-}
-
 // BKE bf16 per K block: 32 (64-byte rows, 64-byte swizzle) or 64 (128-byte rows,
 // 128-byte swizzle); the matching descriptor is sdesc<BKE / 2>.
 template <int BKE>
@@ -1681,56 +1461,6 @@ bool shape_ok(int64_t out, int64_t in, int64_t r) {
          in * r < (1ll << 40);
 }
 
-// ---- tensor maps (driver entry point fetched through the runtime)
-using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
-                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
-                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static std::once_flag once;
-  static EncodeTiledFn fn = nullptr;
-  std::call_once(once, [] {
-    void *ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(ptr);
-  });
-  return fn;
-}
-
-// 2-D matrix [rows, cols] with row stride ld (elements); box = box_bytes of a
-// row (64: 64-byte swizzle, 128: 128-byte swizzle) x box_rows rows, zero fill
-bool make_map(CUtensorMap *map, const void *base, bool bf16, int64_t rows, int64_t cols, int64_t ld, int box_rows,
-              int box_bytes) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return false;
-  const int esz = bf16 ? 2 : 4;
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * esz};
-  cuuint32_t box[2] = {static_cast<cuuint32_t>(box_bytes / esz), static_cast<cuuint32_t>(box_rows)};
-  cuuint32_t estr[2] = {1, 1};
-  return fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
-            const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-            box_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-// the same for a matrix the GEMM reads transposed (XT): an unswizzled box of
-// kBM columns (512 bytes) x box_rows rows
-bool make_map_t(CUtensorMap *map, const float *base, int64_t rows, int64_t cols, int64_t ld, int box_rows) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 4};
-  cuuint32_t box[2] = {static_cast<cuuint32_t>(kBM), static_cast<cuuint32_t>(box_rows)};
-  cuuint32_t estr[2] = {1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 int grid_for(long long n, int sms) {
   long long b = dora::ceil_div(n, 256);
   const long long cap = static_cast<long long>(sms) * 8;
@@ -1952,6 +1682,10 @@ dora_status device_init(int device, int **errp) {
 }
 
 }  // namespace
+
+namespace dora {
+dora_status error_word(int device, int **errp) { return device_init(device, errp); }
+}  // namespace dora
 
 extern "C" size_t dora_norm_factored_workspace(int64_t out, int64_t in, int64_t r) {
   if (!shape_ok(out, in, r)) return 0;

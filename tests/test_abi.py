@@ -203,3 +203,46 @@ def test_norm_bwd_workspace_and_argument_errors(lib):
     assert call(ws=None) == 5
     assert call(ws=FAKE + 16) == 5
     assert call(wsb=16) == 5
+
+
+def test_fused_forward_workspace_and_argument_errors(lib):
+    assert dora.dora_compose_fused_workspace(8192, 384) >= 2 * 8192 * 384 * 2
+    assert dora.dora_compose_fused_workspace(8192, 0) == 0
+    assert dora.dora_compose_fused_workspace(-1, 8) == 0
+    lf = lib.dora_compose_lora_fwd
+    ok = dict(base=FAKE, xa=FAKE, B=FAKE, g=FAKE, s=1.0, T=64, out=256, r=16, y=FAKE, ws=FAKE, wsb=1 << 30,
+              stream=None)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return lf(a["base"], a["xa"], a["B"], a["g"], a["s"], a["T"], a["out"], a["r"], a["y"], a["ws"], a["wsb"],
+                  a["stream"])
+
+    assert call(T=-1) == 2
+    assert call(r=0) == 2
+    assert call(T=0) == 0 and call(out=0) == 0           # empty: no-op
+    assert call(base=None) == 1
+    assert call(xa=None) == 1
+    assert call(ws=None) == 5
+    assert call(out=260) == 3                            # bf16 rows of 16 bytes
+    assert call(r=12) == 3
+    assert call(y=FAKE + 8) == 3
+    assert call(base=FAKE + 2) == 3
+    assert call(g=FAKE + 4) == 3                         # g is read 16 bytes at a time
+    assert call(ws=FAKE + 16) == 5
+    assert call(wsb=16) == 5
+    lin = lib.dora_linear_fwd
+    okl = dict(x=FAKE, W0=FAKE, xa=FAKE, B=FAKE, g=FAKE, s=1.0, T=64, inp=128, out=256, r=16, y=FAKE, ws=FAKE,
+               wsb=1 << 30, stream=None)
+
+    def call_l(**kw):
+        a = dict(okl, **kw)
+        return lin(a["x"], a["W0"], a["xa"], a["B"], a["g"], a["s"], a["T"], a["inp"], a["out"], a["r"], a["y"],
+                   a["ws"], a["wsb"], a["stream"])
+
+    assert call_l(inp=0) == 2
+    assert call_l(T=0) == 0
+    assert call_l(W0=None) == 1
+    assert call_l(inp=12) == 3
+    assert call_l(x=FAKE + 4) == 3
+    assert call_l(wsb=16) == 5

@@ -352,11 +352,12 @@ uint64_t dora_kernel_launches(void);
 
 /*
  * Testing hook for the failure path; no counterpart in the paper.  With on != 0
- * the tensor-core kernels of later dora_norm_factored calls on the current
- * device withhold all their loads, so their bounded waits expire after
+ * the tensor-core kernels of later dora_norm_factored, dora_norm_factored_bwd,
+ * dora_compose_lora_fwd and dora_linear_fwd calls on the current device
+ * withhold all their operand loads, so their bounded waits expire after
  * wait_limit_ns (0 = the default of 2 s): the kernels then record a code in the
  * device error word (see dora_device_error), free their tensor memory and
- * exit, leaving the context usable; the norm and g they produce are garbage.
+ * exit, leaving the context usable; their outputs are garbage.
  * on = 0 restores normal operation.  Synchronises the device.
  */
 dora_status dora_test_stall_loads(int on, uint64_t wait_limit_ns);

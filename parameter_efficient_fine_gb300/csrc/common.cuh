@@ -32,6 +32,11 @@ inline bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintp
 // kernels' shared-memory limits on first use of a device.
 dora_status error_word(int device, int **errp);
 
+// Device addresses of the failure-test hook (see dora_test_stall_loads): a
+// flag that makes the tensor-core producers withhold their loads, and the
+// limit of the bounded waits.
+dora_status test_hooks(int **stall, unsigned long long **limit_ns);
+
 inline dora_status launch_status() {
   return cudaGetLastError() == cudaSuccess ? DORA_OK : DORA_ERR_CUDA;
 }

@@ -74,6 +74,8 @@ struct FusedParams {
   int has_base;
   const float *g;
   int *err;
+  const int *stall;                      // test hook: the producer withholds its loads
+  const unsigned long long *limit_ns;    // limit of the bounded waits
 };
 
 __device__ __forceinline__ void tile_mn(int t, int mtiles, int ntiles, int *mt, int *nt) {
@@ -100,6 +102,12 @@ __device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.
 __device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// bounded wait; the limit is read only when the phase is not yet complete
+__device__ __forceinline__ bool fwait(uint32_t bar, uint32_t parity, SharedCtl *ctl, const FusedParams &p, int code) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return wait_bounded_ns(bar, parity, ctl, p.err, code, *reinterpret_cast<const volatile unsigned long long *>(p.limit_ns));
 }
 
 __global__ void __launch_bounds__(kFThreads, 1)
@@ -169,13 +177,13 @@ fused_compose_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_const
       int stage = 0;
       uint32_t phase = 0;
       int issued = 0;
-      bool ok = true;
+      bool ok = *reinterpret_cast<const volatile int *>(p.stall) == 0;
       for (int t = cta; t < p.tiles && ok; t += ncta) {
         int mt, nt;
         tile_mn(t, p.mtiles, p.ntiles, &mt, &nt);
         // the tile's K blocks, segment after segment (the lora form has none in segment 0)
         for (int kb = 0; kb < p.kbtot && ok; ++kb) {
-          if (!wait_bounded_ns(empty0 + 8u * stage, phase ^ 1u, ctl, p.err, 12, kFWaitNs)) {
+          if (!fwait(empty0 + 8u * stage, phase ^ 1u, ctl, p, 12)) {
             ok = false;
             break;
           }
@@ -227,14 +235,14 @@ fused_compose_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_const
       for (int t = cta; t < p.tiles && ok; t += ncta, ++li) {
         const int buf = li & 1;
         const uint32_t use = static_cast<uint32_t>(li >> 1);
-        if (!wait_bounded_ns(acce0 + 8u * buf, (use & 1u) ^ 1u, ctl, p.err, 13, kFWaitNs)) {
+        if (!fwait(acce0 + 8u * buf, (use & 1u) ^ 1u, ctl, p, 13)) {
           ok = false;
           break;
         }
         tc_fence_after();
         const uint32_t d = tmem + static_cast<uint32_t>(buf * kFN);
         for (int kb = 0; kb < p.kbtot; ++kb) {
-          if (!wait_bounded_ns(full0 + 8u * stage, phase, ctl, p.err, 14, kFWaitNs)) {
+          if (!fwait(full0 + 8u * stage, phase, ctl, p, 14)) {
             ok = false;
             break;
           }
@@ -288,7 +296,7 @@ fused_compose_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_const
       const int tnext = t + ncta;
       const int buf = li & 1;
       const uint32_t use = static_cast<uint32_t>(li >> 1);
-      const bool got = wait_bounded_ns(accf0 + 8u * buf, use & 1u, ctl, p.err, 15, kFWaitNs);
+      const bool got = fwait(accf0 + 8u * buf, use & 1u, ctl, p, 15);
       if (!__all_sync(0xffffffffu, got)) {
         ok = false;
         break;
@@ -300,7 +308,7 @@ fused_compose_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_const
         const int gcol0 = nt * kFN + q * kFQ;
         if (p.has_base) {
           // slot q holds this tile's base quarter: the slot's load number li
-          const bool gb = wait_bounded_ns(cfull(q), static_cast<uint32_t>(li) & 1u, ctl, p.err, 16, kFWaitNs);
+          const bool gb = fwait(cfull(q), static_cast<uint32_t>(li) & 1u, ctl, p, 16);
           if (!__all_sync(0xffffffffu, gb)) {
             ok = false;
             break;
@@ -451,12 +459,17 @@ bool map_bf16(CUtensorMap *map, const void *base, int64_t rows, int64_t cols, in
   return make_map(map, base, true, rows, cols, ld, box_rows, 128);
 }
 
+int *g_stall_ptr[64] = {};
+unsigned long long *g_limit_ptr[64] = {};
+
 dora_status fused_init(int device, int **errp) {
   static std::mutex mu;
   static bool done[64] = {};
   std::lock_guard<std::mutex> lock(mu);
   if (device < 0 || device >= 64) return DORA_ERR_CUDA;
   dora_status st = dora::error_word(device, errp);
+  if (st != DORA_OK) return st;
+  st = dora::test_hooks(&g_stall_ptr[device], &g_limit_ptr[device]);
   if (st != DORA_OK) return st;
   if (!done[device]) {
     if (cudaFuncSetAttribute(fused_compose_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kFSmemMax) !=
@@ -485,6 +498,8 @@ dora_status fused_run(const void *x, const void *W0, const void *base, const voi
   if (!plan_fused(T, in, out, r, lora_form, sms, &fp)) return DORA_ERR_SHAPE;
   fp.p.g = g;
   fp.p.err = errp;
+  fp.p.stall = g_stall_ptr[device];
+  fp.p.limit_ns = g_limit_ptr[device];
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   __nv_bfloat16 *hi = static_cast<__nv_bfloat16 *>(workspace);
   __nv_bfloat16 *lo = reinterpret_cast<__nv_bfloat16 *>(static_cast<uint8_t *>(workspace) +

@@ -1685,6 +1685,15 @@ dora_status device_init(int device, int **errp) {
 
 namespace dora {
 dora_status error_word(int device, int **errp) { return device_init(device, errp); }
+dora_status test_hooks(int **stall, unsigned long long **limit_ns) {
+  void *a = nullptr, *b = nullptr;
+  if (cudaGetSymbolAddress(&a, g_dora_stall) != cudaSuccess ||
+      cudaGetSymbolAddress(&b, g_wait_limit_ns) != cudaSuccess)
+    return DORA_ERR_CUDA;
+  *stall = static_cast<int *>(a);
+  *limit_ns = static_cast<unsigned long long *>(b);
+  return DORA_OK;
+}
 }  // namespace dora
 
 extern "C" size_t dora_norm_factored_workspace(int64_t out, int64_t in, int64_t r) {

@@ -34,3 +34,47 @@ def test_expired_wait_is_reported_and_context_survives(out, inp, r):
     check_rel("norm", to_f64(norm), n_ref)
     check_rel("g", to_f64(g), g_ref)
     assert_no_device_error()
+
+
+def _stalled(call):
+    assert_no_device_error()
+    dora.dora_test_stall_loads(True, 50_000_000)      # 50 ms
+    try:
+        call()
+        code = dora.dora_device_error()                # synchronises
+    finally:
+        dora.dora_test_stall_loads(False)
+    return code
+
+
+def test_norm_gradient_expired_wait_is_reported():
+    from test_gpu_norm_grad import run_norm_bwd
+    sh = wl.shape("high_rank", out=300, inp=256, r=40, T=8)
+    w = wl.make_weights(sh, 6)
+    W0, A, B, m = (f32_dev(w[k]) for k in ("W0", "A", "B", "m"))
+    norm, g = run_norm(W0, A, B, m, w["s"])
+    dm = f32_dev(np.random.default_rng(6).standard_normal(sh.out).astype(np.float32))
+    assert _stalled(lambda: run_norm_bwd(W0, A, B, norm, g, dm, w["s"])) != 0
+    dA, dB = run_norm_bwd(W0, A, B, norm, g, dm, w["s"])
+    dA_ref, dB_ref = oracle.norm_grad(w["W0"], w["A"], w["B"], w["s"], to_f64(norm), to_f64(g), to_f64(dm))
+    assert np.linalg.norm(to_f64(dA) - dA_ref) <= 1e-5 * np.linalg.norm(dA_ref)
+    assert np.linalg.norm(to_f64(dB) - dB_ref) <= 1e-5 * np.linalg.norm(dB_ref)
+    assert_no_device_error()
+
+
+@pytest.mark.parametrize("form", ["lora", "linear"])
+def test_fused_forward_expired_wait_is_reported(form):
+    # the lora form's epilogue warps have base copies in flight when the
+    # MMA-side waits expire: they must drain them before leaving
+    from gpu_util import check_bf16_rule
+    from test_gpu_fused import _f64, _layer, run_linear, run_lora
+    d = _layer(300, 264, 520, 40, 9800)
+    run = run_lora if form == "lora" else run_linear
+    assert _stalled(lambda: run(d)) != 0
+    y = to_f64(run(d))
+    if form == "lora":
+        ref = oracle.compose_lora_fwd(_f64(d["base"]), _f64(d["xa"]), d["B"], d["g"], d["s"])
+    else:
+        ref = oracle.linear_fwd(_f64(d["x"]), _f64(d["W0"]), _f64(d["xa"]), d["B"], d["g"], d["s"])
+    check_bf16_rule("y", y, ref)
+    assert_no_device_error()

@@ -81,3 +81,48 @@ def test_compose_writes_stay_in_bounds(act, T, out):
     dm_b.check("d_mag")
     ws_b.check("workspace")
     assert_no_device_error()
+
+
+@pytest.mark.parametrize("out,inp,r", [(257, 100, 17), (1000, 1040, 384), (130, 64, 768), (1030, 136, 64)])
+def test_norm_gradient_writes_stay_in_bounds(out, inp, r):
+    sh = wl.shape("high_rank", out=out, inp=inp, r=r, T=8)
+    w = wl.make_weights(sh, 32)
+    W0, A, B, m = (f32_dev(w[k]) for k in ("W0", "A", "B", "m"))
+    norm = torch.empty(out, device=DEV)
+    g = torch.empty(out, device=DEV)
+    ws = torch.empty(dora.dora_norm_factored_workspace(out, inp, r), dtype=torch.uint8, device=DEV)
+    dora.dora_norm_factored(W0, A, B, m, w["s"], norm, g, ws)
+    dm = f32_dev(np.random.default_rng(out).standard_normal(out))
+    dA_b, dB_b = Guarded(r * inp * 4), Guarded(out * r * 4)
+    nbytes = dora.dora_norm_factored_bwd_workspace(out, inp, r)
+    ws_b = Guarded(nbytes)
+    dA, dB = dA_b.view(torch.float32, (r, inp)), dB_b.view(torch.float32, (out, r))
+    dora.dora_norm_factored_bwd(W0, A, B, norm, g, dm, w["s"], dA, dB, ws_b.view(torch.uint8, (nbytes,)))
+    torch.cuda.synchronize()
+    dA_b.check("dA")
+    dB_b.check("dB")
+    ws_b.check("workspace")
+    assert bool(torch.isfinite(dA).all()) and bool(torch.isfinite(dB).all())
+    assert_no_device_error()
+
+
+@pytest.mark.parametrize("T,inp,out,r", [(300, 264, 520, 40), (77, 8, 8, 16), (129, 1032, 776, 128)])
+def test_fused_forward_writes_stay_in_bounds(T, inp, out, r):
+    sh = wl.shape("high_rank", T=T, inp=inp, out=out, r=r)
+    d = wl.make_layer(sh, 33)
+    x, W0, xa, base = (act_to_dev(d[k]) for k in ("x", "W0", "xa", "base"))
+    B, g = f32_dev(d["B"]), f32_dev(d["g"])
+    nbytes = dora.dora_compose_fused_workspace(out, r)
+    for form in ("lora", "linear"):
+        y_b, ws_b = Guarded(T * out * 2), Guarded(nbytes)
+        y = y_b.view(torch.bfloat16, (T, out))
+        ws = ws_b.view(torch.uint8, (nbytes,))
+        if form == "lora":
+            dora.dora_compose_lora_fwd(base, xa, B, g, d["s"], y, ws)
+        else:
+            dora.dora_linear_fwd(x, W0, xa, B, g, d["s"], y, ws)
+        torch.cuda.synchronize()
+        y_b.check(f"y ({form})")
+        ws_b.check(f"workspace ({form})")
+        assert bool(torch.isfinite(y.float()).all())
+    assert_no_device_error()

@@ -212,7 +212,7 @@ fused_compose_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_const
         }
       }
       if (!ok) {
-        // copies in flight: the last min(issued, S) stages and the base loads
+        // copies in flight: the last min(issued, S) stages
         int st = stage;
         uint32_t ph = phase;
         for (int k = 0; k < S && k < issued; ++k) {
@@ -288,6 +288,10 @@ fused_compose_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_const
     };
     if (p.has_base && lane == 0 && cta < p.tiles)
       for (int q = 0; q < 4; ++q) load_base(cta, q);
+    // the staging slot of this warp's most recent TMA store (-1: none yet).
+    // Before a slot is written again, every store that reads it must be done:
+    // all but the most recent store when that one used another slot, else all.
+    int last_slot = -1;
     int li = 0;
     bool ok = true;
     for (int t = cta; t < p.tiles && ok; t += ncta, ++li) {
@@ -306,82 +310,89 @@ fused_compose_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_const
       for (int q = 0; q < 4; ++q) {
         const int sl = q % p.nslots;
         const int gcol0 = nt * kFN + q * kFQ;
+        // a quarter entirely outside y (ragged last tiles) is neither computed
+        // nor stored; warp-uniform
+        const bool live = rows_in && gcol0 < p.out;
         if (p.has_base) {
           // slot q holds this tile's base quarter: the slot's load number li
+          // (consumed even when the quarter is not live, to keep the phases)
           const bool gb = fwait(cfull(q), static_cast<uint32_t>(li) & 1u, ctl, p, 16);
           if (!__all_sync(0xffffffffu, gb)) {
             ok = false;
             break;
           }
-        } else {
-          // slot sl: this warp's store from two quarters ago must have read it
-          // (the most recent store may still be reading the other slot)
-          if (lane == 0) bulk_wait_read1();
-          __syncwarp();
         }
-        // g of the quarter's 64 columns: 16 uniform 128-bit loads issued
-        // together (one latency), zero past `out`
-        float4 gq[16];
+        if (live) {
+          if (!p.has_base) {
+            // the slot takes this quarter's y: earlier stores must have read it
+            if (lane == 0) {
+              if (last_slot == sl) bulk_wait_read0();
+              else bulk_wait_read1();
+            }
+            __syncwarp();
+          }
+          // g of the quarter's 64 columns: 16 uniform 128-bit loads issued
+          // together (one latency), zero past `out`
+          float4 gq[16];
 #pragma unroll
-        for (int k = 0; k < 16; ++k)
-          gq[k] = gcol0 + 4 * k < p.out ? __ldg(reinterpret_cast<const float4 *>(p.g + gcol0) + k)
-                                        : make_float4(0.f, 0.f, 0.f, 0.f);
-        float v[2][32];
-        const uint32_t col0 = static_cast<uint32_t>(buf * kFN + q * kFQ);
-        tmem_ld32(lane_addr + col0, v[0]);
-        tmem_ld32(lane_addr + col0 + 32, v[1]);
+          for (int k = 0; k < 16; ++k)
+            gq[k] = gcol0 + 4 * k < p.out ? __ldg(reinterpret_cast<const float4 *>(p.g + gcol0) + k)
+                                          : make_float4(0.f, 0.f, 0.f, 0.f);
+          float v[2][32];
+          const uint32_t col0 = static_cast<uint32_t>(buf * kFN + q * kFQ);
+          tmem_ld32(lane_addr + col0, v[0]);
+          tmem_ld32(lane_addr + col0 + 32, v[1]);
+          uint8_t *crow = cbuf + slot_off(sl) + lane * 128;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            // 16-byte chunk j of the row (8 columns), at its swizzled position
+            uint4 *pc = reinterpret_cast<uint4 *>(crow + ((j ^ (lane & 7)) << 4));
+            const float *a = &v[j >> 2][(j & 3) * 8];
+            const float gv[8] = {gq[2 * j].x, gq[2 * j].y, gq[2 * j].z, gq[2 * j].w,
+                                 gq[2 * j + 1].x, gq[2 * j + 1].y, gq[2 * j + 1].z, gq[2 * j + 1].w};
+            float yv[8];
+            if (p.has_base) {
+              const uint4 braw = *pc;
+              const __nv_bfloat162 *bb = reinterpret_cast<const __nv_bfloat162 *>(&braw);
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const float2 b2 = __bfloat1622float2(bb[e]);
+                yv[2 * e] = b2.x + fmaf(gv[2 * e] - 1.0f, b2.x, gv[2 * e] * a[2 * e]);
+                yv[2 * e + 1] = b2.y + fmaf(gv[2 * e + 1] - 1.0f, b2.y, gv[2 * e + 1] * a[2 * e + 1]);
+              }
+            } else {
+#pragma unroll
+              for (int e = 0; e < 8; ++e) yv[e] = gv[e] * a[e];
+            }
+            uint4 o;
+            o.x = pack_bf16x2(yv[0], yv[1]);
+            o.y = pack_bf16x2(yv[2], yv[3]);
+            o.z = pack_bf16x2(yv[4], yv[5]);
+            o.w = pack_bf16x2(yv[6], yv[7]);
+            *pc = o;
+          }
+          // make the writes visible to the TMA store, then lane 0 stores the
+          // warp's 32 rows of the quarter
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&mY, cbase + slot_off(sl), gcol0, mt * kFM + quad * 32);
+            bulk_commit();
+            last_slot = sl;
+          }
+        }
         if (q == 3) {
           // the accumulator is read out: the MMA lane may start the tile after next
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(acce0 + 8u * buf);
         }
-        uint8_t *crow = cbuf + slot_off(sl) + lane * 128;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          // 16-byte chunk j of the row (8 columns), at its swizzled position
-          uint4 *pc = reinterpret_cast<uint4 *>(crow + ((j ^ (lane & 7)) << 4));
-          const float *a = &v[j >> 2][(j & 3) * 8];
-          const float gv[8] = {gq[2 * j].x, gq[2 * j].y, gq[2 * j].z, gq[2 * j].w,
-                               gq[2 * j + 1].x, gq[2 * j + 1].y, gq[2 * j + 1].z, gq[2 * j + 1].w};
-          float yv[8];
-          if (p.has_base) {
-            const uint4 braw = *pc;
-            const __nv_bfloat162 *bb = reinterpret_cast<const __nv_bfloat162 *>(&braw);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float2 b2 = __bfloat1622float2(bb[e]);
-              yv[2 * e] = b2.x + fmaf(gv[2 * e] - 1.0f, b2.x, gv[2 * e] * a[2 * e]);
-              yv[2 * e + 1] = b2.y + fmaf(gv[2 * e + 1] - 1.0f, b2.y, gv[2 * e + 1] * a[2 * e + 1]);
-            }
-          } else {
-#pragma unroll
-            for (int e = 0; e < 8; ++e) yv[e] = gv[e] * a[e];
-          }
-          uint4 o;
-          o.x = pack_bf16x2(yv[0], yv[1]);
-          o.y = pack_bf16x2(yv[2], yv[3]);
-          o.z = pack_bf16x2(yv[4], yv[5]);
-          o.w = pack_bf16x2(yv[6], yv[7]);
-          *pc = o;
-        }
-        // make the writes visible to the TMA store, then lane 0 stores the
-        // warp's 32 rows of the quarter
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          const bool stored = rows_in && gcol0 < p.out;
-          if (stored) {
-            tma_store_2d(&mY, cbase + slot_off(sl), gcol0, mt * kFM + quad * 32);
-            bulk_commit();
-          }
-          if (p.has_base && q > 0 && tnext < p.tiles) {
-            // the previous quarter's store has read slot q - 1: it takes the
-            // next tile's base quarter
-            if (stored) bulk_wait_read1();
-            else bulk_wait_read0();
-            load_base(tnext, q - 1);
-          }
+        if (p.has_base && lane == 0 && q > 0 && tnext < p.tiles) {
+          // slot q - 1 takes the next tile's base quarter once every store
+          // that reads it is done: all but this quarter's store, if there was one
+          if (live) bulk_wait_read1();
+          else bulk_wait_read0();
+          load_base(tnext, q - 1);
         }
       }
       if (!ok) break;

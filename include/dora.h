@@ -274,7 +274,10 @@ dora_status dora_compose_bwd(dora_dtype act, const void *grad_out, const void *b
  * DORA_NOALLOC_SCRATCH_FLOATS floats, held on every GPU that loads the library
  * until the process exits.  The first call on a device looks up that array's
  * device address (cudaGetSymbolAddress, with the device current); make that
- * first call before any stream capture.  Every partial sum the call reads is
+ * first call before any stream capture.  A device reset (cudaDeviceReset)
+ * gives the device a new context and invalidates the address: the next call
+ * looks it up again, so after a reset, too, make one call before any capture.
+ * Every partial sum the call reads is
  * written earlier in the same call, so nothing needs clearing between calls,
  * but all calls share the one array: calls that overlap on the GPU (different
  * streams, or concurrent host threads on one device) race and give wrong
@@ -282,10 +285,11 @@ dora_status dora_compose_bwd(dora_dtype act, const void *grad_out, const void *b
  * allocating library routine).
  *
  * Arguments, layouts and errors as dora_compose_bwd, plus: out must not exceed
- * DORA_NOALLOC_SCRATCH_FLOATS (DORA_ERR_SHAPE otherwise).  When the usual
- * token-lane grid would need more scratch than the array holds, fewer grid
- * rows are used; d_mag then sums in a different (still fixed) order and may
- * differ from dora_compose_bwd's by fp32 rounding.
+ * DORA_NOALLOC_SCRATCH_FLOATS (DORA_ERR_SHAPE otherwise).  The call launches
+ * exactly the grid dora_compose_bwd launches, so d_mag is bitwise the same.
+ * That grid's partial rows times out stay below 4096 x the SM count floats,
+ * which fits the array on any device with up to 256 SMs (GB300 has 152); a
+ * device where it would not fit gets DORA_ERR_SHAPE before any launch.
  */
 dora_status dora_compose_bwd_noalloc(dora_dtype act, const void *grad_out, const void *base,
                                      const void *lora, const float *g, const float *norm,

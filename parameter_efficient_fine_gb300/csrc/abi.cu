@@ -1,4 +1,5 @@
 // Status strings, device checks and launch accounting for libdora.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -14,7 +15,33 @@ constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 DeviceInfo g_info[kMaxDevices];
 bool g_known[kMaxDevices] = {};
+using CtxGetCurrentFn = CUresult (*)(CUcontext *);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long *);
 }  // namespace
+
+uint64_t context_id() {
+  static std::once_flag once;
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  std::call_once(once, [] {
+    void *a = nullptr, *b = nullptr;
+    cudaDriverEntryPointQueryResult qa, qb;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &a, 12000, cudaEnableDefault, &qa) == cudaSuccess &&
+        qa == cudaDriverEntryPointSuccess &&
+        cudaGetDriverEntryPointByVersion("cuCtxGetId", &b, 12000, cudaEnableDefault, &qb) == cudaSuccess &&
+        qb == cudaDriverEntryPointSuccess) {
+      get_current = reinterpret_cast<CtxGetCurrentFn>(a);
+      get_id = reinterpret_cast<CtxGetIdFn>(b);
+    }
+  });
+  if (!get_current || !get_id) return 0;
+  // no context yet (the runtime creates it on first real use): 0, so the
+  // caller's set-up runs and records the id that exists after it
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
 
 dora_status current_device(DeviceInfo *info, int *device) {
   int dev = 0;

@@ -25,6 +25,14 @@ struct DeviceInfo {
 // device is not sm_103; DORA_ERR_CUDA when the runtime cannot answer.
 dora_status current_device(DeviceInfo *info, int *device);
 
+// Process-unique id of the calling thread's current CUDA context (the driver's
+// context id, never reused within a process); 0 when it cannot be read or no
+// context is current yet (0 never matches a recorded id).
+// Per-device set-up that belongs to a context (symbol addresses, kernel
+// attributes) is keyed on it, so a device reset -- which destroys the context
+// and reloads the library's module -- makes that set-up run again.
+uint64_t context_id();
+
 inline bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 // The device error word that the library's kernels write when a bounded wait

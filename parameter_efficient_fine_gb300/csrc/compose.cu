@@ -447,17 +447,23 @@ namespace {
 constexpr int64_t kNoAllocScratchFloats = DORA_NOALLOC_SCRATCH_FLOATS;
 static __device__ __align__(256) float g_noalloc_scratch[kNoAllocScratchFloats];
 
-// Device address of g_noalloc_scratch, looked up once per device with that
-// device current (in host code the symbol name is only a host-side stand-in).
+// Device address of g_noalloc_scratch, looked up once per device (and again
+// after a device reset, which gives the device a new context and reloads the
+// module) with that device current.  In host code the symbol name is only a
+// host-side stand-in, never a device address.
 float *noalloc_scratch_address(int device) {
   static std::mutex mu;
   static float *addr[64] = {};
+  static uint64_t ctx_of[64] = {};
   if (device < 0 || device >= 64) return nullptr;
   std::lock_guard<std::mutex> lock(mu);
-  if (!addr[device]) {
+  const uint64_t ctx = dora::context_id();
+  if (!addr[device] || ctx == 0 || ctx != ctx_of[device]) {
+    addr[device] = nullptr;
     void *ptr = nullptr;
     if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess) return nullptr;
     addr[device] = static_cast<float *>(ptr);
+    ctx_of[device] = dora::context_id();
   }
   return addr[device];
 }
@@ -470,10 +476,13 @@ dora_status launch_bwd_noalloc(const void *dy, const void *base, const void *lor
   const int bps = blocks_per_sm(kern, device);
   int64_t rows = 0;
   if (T > 0) {
-    Grid gr = plan_grid(T, out / VEC, (int64_t)sms * bps);
-    // fewer token-lane rows when the partial sums would not fit the scratch
-    const int64_t cap = kNoAllocScratchFloats / out;
-    if (gr.gy > cap) gr.gy = cap;
+    const Grid gr = plan_grid(T, out / VEC, (int64_t)sms * bps);
+    // The grid plan keeps rows * out below 2 x (SMs x resident blocks) x 32 x
+    // VEC <= SMs x 4096 floats (at most 8 resident blocks of 256 threads,
+    // VEC <= 8): under 2^20 on any device with up to 256 SMs (GB300 has 152),
+    // so the partial rows always fit the scratch.  Checked anyway, and refused
+    // rather than launched with a different summation order.
+    if (gr.gy * out > kNoAllocScratchFloats) return DORA_ERR_SHAPE;
     rows = gr.gy;
     kern<<<dim3((unsigned)gr.gx, (unsigned)gr.gy), dim3(kBX, kBY), 0, stream>>>(
         static_cast<const Act *>(dy), static_cast<const Act *>(base), static_cast<const Act *>(lora), g, s, T,

@@ -475,18 +475,19 @@ unsigned long long *g_limit_ptr[64] = {};
 
 dora_status fused_init(int device, int **errp) {
   static std::mutex mu;
-  static bool done[64] = {};
+  static uint64_t done_ctx[64] = {};   // context the attribute was set in
   std::lock_guard<std::mutex> lock(mu);
   if (device < 0 || device >= 64) return DORA_ERR_CUDA;
   dora_status st = dora::error_word(device, errp);
   if (st != DORA_OK) return st;
   st = dora::test_hooks(&g_stall_ptr[device], &g_limit_ptr[device]);
   if (st != DORA_OK) return st;
-  if (!done[device]) {
+  const uint64_t ctx = dora::context_id();
+  if (ctx == 0 || ctx != done_ctx[device]) {
     if (cudaFuncSetAttribute(fused_compose_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kFSmemMax) !=
         cudaSuccess)
       return DORA_ERR_CUDA;
-    done[device] = true;
+    done_ctx[device] = dora::context_id();
   }
   return DORA_OK;
 }

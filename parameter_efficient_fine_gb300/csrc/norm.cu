@@ -84,8 +84,6 @@ constexpr int kThreads = 192;
 constexpr int kMaxChunkN = 384;     // largest N handled by one CTA pass
 constexpr int kMaxR = 1024;
 constexpr int kMaxCtas = 256;       // workspace bound: any device up to this size
-constexpr int kMaxCluster = 2;      // largest cluster of the norm pass (4 measured slower)
-constexpr int kMinClusterN = 256;   // narrowest N chunk whose N-side tile the cluster shares
 constexpr int kMinUnitsNorm = 4;
 constexpr int kMinUnitsGram = 16;
 constexpr int kSmemMax = 232448;           // 227 KB: the opt-in maximum per CTA
@@ -117,19 +115,17 @@ struct TcParams {
   int nchunks;      // N chunks per M tile
   int sym;          // Gram pass: only tiles with N chunk >= M tile (G is symmetric; both 128 wide)
   int NC;           // N per chunk (multiple of 16, <= kMaxChunkN)
-  int csize;        // CTAs per cluster: they take consecutive M tiles over the same K range
-  int sl;           // N-side rows each CTA of a cluster loads (and multicasts to the cluster)
   int nbox;         // rows per N-side TMA box
-  int nb;           // N-side boxes per CTA per stage (per hi / correction): sl = nb * nbox
-  int NT;           // N-side rows in shared memory per stage (csize * sl >= NC)
+  int nb;           // N-side boxes per stage (per hi / correction)
+  int NT;           // N-side rows in shared memory per stage (nb * nbox >= NC)
   int nmma0, nmma1; // N of the first / second MMA instruction of a chunk
   int tmem_cols;
   int slot0;        // first tensor-memory column of the M-side operand slots (one slot per stage)
   int stages;
-  int tiles;        // M-tile groups (csize M tiles each) * nchunks
+  int tiles;        // M tiles * nchunks (Gram pass: the upper-triangular tiles)
   long long units;  // tiles * kbtot
-  int ctas;         // clusters * csize
-  int ncl;          // clusters
+  int ctas;         // CTAs of the launch (one per SM at most)
+  int ncl;          // = ctas: the parts the unit list is cut into
   int maxseg;
   unsigned stage_bytes;
   unsigned tx_bytes;
@@ -177,10 +173,9 @@ __host__ __device__ __forceinline__ int cta_of(long long u, long long units, int
 }
 
 // (M tile, N chunk) of work tile t.  Gram pass: the upper-triangular tiles
-// (nc >= mt) of a q x q grid, row by row.  Norm pass: M-tile group t / nchunks
-// (csize consecutive M tiles, one per cluster rank), N chunk t % nchunks.
-__host__ __device__ __forceinline__ void tile_coords(int t, int nchunks, int sym, int csize, int crank, int *mt,
-                                                     int *nc) {
+// (nc >= mt) of a q x q grid, row by row.  Norm pass: M tile t / nchunks,
+// N chunk t % nchunks.
+__host__ __device__ __forceinline__ void tile_coords(int t, int nchunks, int sym, int *mt, int *nc) {
   if (sym) {
     int i = 0;
     while (t >= nchunks - i) {
@@ -190,9 +185,8 @@ __host__ __device__ __forceinline__ void tile_coords(int t, int nchunks, int sym
     *mt = i;
     *nc = i + t;
   } else {
-    const int grp = t / nchunks;
-    *nc = t - grp * nchunks;
-    *mt = grp * csize + crank;
+    *mt = t / nchunks;
+    *nc = t - *mt * nchunks;
   }
 }
 
@@ -242,7 +236,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ 
     for (int s = 0; s < S; ++s) {
       mbar_init(full0 + 8u * s, 1);
       mbar_init(conv0 + 8u * s, 4);   // one arrival per converter warp
-      mbar_init(empty0 + 8u * s, static_cast<uint32_t>(p.csize));   // one MMA release per cluster CTA
+      mbar_init(empty0 + 8u * s, 1);
     }
     mbar_init(accf, 1);
     mbar_init(acce, 4);
@@ -267,13 +261,10 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ 
   }
   tc_fence_before();
   __syncthreads();
-  if (p.csize > 1) cluster_sync();   // peers' barriers are initialised before any multicast
   tc_fence_after();
   const uint32_t tmem = ctl->tmem_base;
 
-  const int crank = p.csize > 1 ? static_cast<int>(cluster_rank()) : 0;
-  const int cl = static_cast<int>(blockIdx.x) / p.csize;
-  const uint16_t cmask = static_cast<uint16_t>((1u << p.csize) - 1u);
+  const int cl = static_cast<int>(blockIdx.x);
   const long long u_begin = unit_begin(cl, p.units, p.ncl);
   const long long u_end = unit_begin(cl + 1, p.units, p.ncl);
 
@@ -289,7 +280,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ 
         const int kb0 = static_cast<int>(u - static_cast<long long>(t) * p.kbtot);
         const int kbe = piece_end(u, u_end, kb0, p.kbtot, p.chain);
         int mt, nc;
-        tile_coords(t, p.nchunks, p.sym, p.csize, crank, &mt, &nc);
+        tile_coords(t, p.nchunks, p.sym, &mt, &nc);
         for (int kb = kb0; kb < kbe; ++kb) {
           if (!wait_bounded(empty0 + 8u * stage, phase ^ 1u, ctl, p.err, 1)) {
             ok = false;
@@ -304,19 +295,13 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ 
           const int kx = (seg1 ? kb : kb - p.kb1) * BK;    // fp32 column of the hi operands
           if (XT) tma_load_2d(xs, seg1 ? &mX1 : &mX2, mt * kBM, kx, fb);
           else tma_load_2d(xs, seg1 ? &mX1 : &mX2, kx, mt * kBM, fb);
-          // this CTA's slice of the N-side tile; with a cluster it is multicast
-          // to every CTA of the cluster, which all load the other slices
+          // the N-side tile of the chunk, hi and correction operands
           for (int i = 0; i < p.nb; ++i) {
-            const int ro = crank * p.sl + i * p.nbox;
+            const int ro = i * p.nbox;
             const int ny = nc * p.NC + ro;
             const uint32_t off = static_cast<uint32_t>(ro * kRowBytes);
-            if (p.csize > 1) {
-              tma_load_2d_mc(yh + off, seg1 ? &mY1h : &mY2h, kx, ny, fb, cmask);
-              tma_load_2d_mc(yc + off, seg1 ? &mY1c : &mY2c, 2 * kx, ny, fb, cmask);   // bf16 column
-            } else {
-              tma_load_2d(yh + off, seg1 ? &mY1h : &mY2h, kx, ny, fb);
-              tma_load_2d(yc + off, seg1 ? &mY1c : &mY2c, 2 * kx, ny, fb);
-            }
+            tma_load_2d(yh + off, seg1 ? &mY1h : &mY2h, kx, ny, fb);
+            tma_load_2d(yc + off, seg1 ? &mY1c : &mY2c, 2 * kx, ny, fb);   // bf16 column
           }
           ++issued;
           if (++stage == S) {
@@ -391,8 +376,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ 
               mma_tf32_ta(tmem + 256u, ah, bh, id1, 1u);
             }
           }
-          if (p.csize > 1) mma_commit_mc(empty0 + 8u * stage, cmask);
-          else mma_commit(empty0 + 8u * stage);
+          mma_commit(empty0 + 8u * stage);
           if (++stage == S) {
             stage = 0;
             phase ^= 1u;
@@ -421,7 +405,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ 
       const int kb0 = static_cast<int>(u - static_cast<long long>(t) * p.kbtot);
       const int kbe = piece_end(u, u_end, kb0, p.kbtot, p.chain);
       int mt, nc;
-      tile_coords(t, p.nchunks, p.sym, p.csize, crank, &mt, &nc);
+      tile_coords(t, p.nchunks, p.sym, &mt, &nc);
       const size_t tm = static_cast<size_t>(mt) * p.nchunks + nc;   // (M tile, N chunk) of this CTA's partials
       float n0 = 0.0f;  // sum of W0_i^2 over this segment's K range
       if (p.mode == kNorm && lane == 0) {
@@ -543,7 +527,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ 
         old = __shfl_sync(0xffffffffu, old, 0);
         int expect = 0;
         for (int c = 0; c < p.nchunks; ++c) {
-          const long long ub = (static_cast<long long>(mt / p.csize) * p.nchunks + c) * p.kbtot;
+          const long long ub = (static_cast<long long>(mt) * p.nchunks + c) * p.kbtot;
           expect += cta_of(ub + p.kbtot - 1, p.units, p.ncl) - cta_of(ub, p.units, p.ncl) + 1;
         }
         if (old == expect - 1) {
@@ -551,7 +535,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ 
           if (valid) {
             float s0 = 0.0f, sd = 0.0f;
             for (int c = 0; c < p.nchunks; ++c) {
-              const long long ub = (static_cast<long long>(mt / p.csize) * p.nchunks + c) * p.kbtot;
+              const long long ub = (static_cast<long long>(mt) * p.nchunks + c) * p.kbtot;
               const int nseg = cta_of(ub + p.kbtot - 1, p.units, p.ncl) - cta_of(ub, p.units, p.ncl) + 1;
               const size_t tmc = static_cast<size_t>(mt) * p.nchunks + c;
               for (int j = 0; j < nseg; ++j) {
@@ -611,8 +595,6 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ 
 
   tc_fence_before();
   __syncthreads();
-  // no CTA leaves while a peer may still multicast into it or arrive on its barriers
-  if (p.csize > 1) cluster_sync();
   tc_fence_after();
   if (warp == 1) {
     __syncwarp();
@@ -668,13 +650,13 @@ __global__ void __launch_bounds__(256) pad_cols_kernel(const float *__restrict__
   }
 }
 
-// how partial results were laid out by tc_gemm_kernel: tile tg = (M-tile group,
-// N chunk) is covered by clusters cta_of(tg*kbtot) .. cta_of((tg+1)*kbtot - 1);
-// the partial of M tile mt, chunk nc, from the j-th of those clusters, is
-// entry (mt*nchunks + nc)*maxseg + j
+// how partial results were laid out by tc_gemm_kernel: tile t = (M tile, N
+// chunk) is covered by CTAs cta_of(t*kbtot) .. cta_of((t+1)*kbtot - 1); the
+// partial of M tile mt, chunk nc, from the j-th of those CTAs, is entry
+// (mt*nchunks + nc)*maxseg + j
 struct StreamK {
   long long units;
-  int ncl, kbtot, maxseg, csize;
+  int ncl, kbtot, maxseg;
 };
 
 // Gs[k][l] = (s/2) * G[k][l] for k, l < r (zero-padded to npad), split like
@@ -701,7 +683,7 @@ __global__ void __launch_bounds__(256) gram_reduce_kernel(const float *__restric
   __shared__ float wsum[8][32][33];
   const int t = blockIdx.x;
   int mt, nc;
-  tile_coords(t, nchunks, 1, 1, 0, &mt, &nc);
+  tile_coords(t, nchunks, 1, &mt, &nc);
   const int nsub = (NC + 31) / 32;
   const int sr = static_cast<int>(blockIdx.y) / nsub, sc = static_cast<int>(blockIdx.y) - sr * nsub;
   const size_t tm = static_cast<size_t>(mt) * nchunks + nc;
@@ -817,7 +799,7 @@ __global__ void __launch_bounds__(256) rows_reduce_kernel(const float4 *__restri
   __shared__ float tile[kBM][33];
   const int tm = blockIdx.x;
   const int mt = tm / nchunks, nc = tm - mt * nchunks;
-  const long long ub = (static_cast<long long>(mt / sk.csize) * nchunks + nc) * sk.kbtot;
+  const long long ub = (static_cast<long long>(mt) * nchunks + nc) * sk.kbtot;
   const int nseg = cta_of(ub + sk.kbtot - 1, sk.units, sk.ncl) - cta_of(ub, sk.units, sk.ncl) + 1;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int cg = static_cast<int>(blockIdx.y) * 8 + warp;   // column group within the chunk
@@ -889,7 +871,7 @@ struct Tc16Params {
   int rs;           // column stride of the pieces of s/2 G (r rounded up to 8)
   int kbtot;        // kb1 + 3 * kbr (NORM) or kb1 (GRAM)
   int nchunks, sym, NC;
-  int nbox, nb, sl, NT;
+  int nbox, nb, NT;
   int nmma0, nmma1;
   int tmem_cols;
   int stages;
@@ -974,7 +956,7 @@ tc16_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ CUt
         const int kb0 = static_cast<int>(u - static_cast<long long>(t) * p.kbtot);
         const int kbe = static_cast<int>(min(static_cast<long long>(p.kbtot), kb0 + (u_end - u)));
         int mt, nc;
-        tile_coords(t, p.nchunks, p.sym, 1, 0, &mt, &nc);
+        tile_coords(t, p.nchunks, p.sym, &mt, &nc);
         for (int kb = kb0; kb < kbe; ++kb) {
           if (!wait_bounded(empty0 + 8u * stage, phase ^ 1u, ctl, p.err, 1)) {
             ok = false;
@@ -1078,7 +1060,7 @@ tc16_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ CUt
       const int kb0 = static_cast<int>(u - static_cast<long long>(t) * p.kbtot);
       const int kbe = static_cast<int>(min(static_cast<long long>(p.kbtot), kb0 + (u_end - u)));
       int mt, nc;
-      tile_coords(t, p.nchunks, p.sym, 1, 0, &mt, &nc);
+      tile_coords(t, p.nchunks, p.sym, &mt, &nc);
       const size_t tm = static_cast<size_t>(mt) * p.nchunks + nc;
       if (p.mode == kNorm && lane == 0) {
         const int r0 = mt * kBM + quad * 32;
@@ -1240,7 +1222,7 @@ __global__ void __launch_bounds__(256) gram_reduce3_kernel(const float *__restri
     for (int i = threadIdx.y * 32 + threadIdx.x; i < ncnt; i += 256) cnt[i] = 0;
   const int t = blockIdx.x;
   int mt, nc;
-  tile_coords(t, nchunks, 1, 1, 0, &mt, &nc);
+  tile_coords(t, nchunks, 1, &mt, &nc);
   const int nsub = (NC + 31) / 32;
   const int sr = static_cast<int>(blockIdx.y) / nsub, sc = static_cast<int>(blockIdx.y) - sr * nsub;
   const size_t tm = static_cast<size_t>(mt) * nchunks + nc;
@@ -1314,15 +1296,13 @@ void plan_n(int r, int *npad, int *nchunks, int *NC) {
   *NC = static_cast<int>(dora::round_up(dora::ceil_div(*npad, *nchunks), 16));
 }
 
-// K = in (+ r for the norm and row passes); csize CTAs per cluster, at most
-// max_clusters clusters
-bool plan_gemm(int mode, int M, int64_t in, int r, int csize, int max_clusters, GemmPlan *gp) {
+// K = in (+ r for the norm and row passes); at most max_ctas CTAs
+bool plan_gemm(int mode, int M, int64_t in, int r, int max_ctas, GemmPlan *gp) {
   TcParams &p = gp->p;
   std::memset(&p, 0, sizeof(p));
   gp->xt = false;
   p.mode = mode;
   p.M = M;
-  p.csize = csize;
   int npad;
   plan_n(r, &npad, &p.nchunks, &p.NC);
   if (mode == kGram) {
@@ -1335,13 +1315,11 @@ bool plan_gemm(int mode, int M, int64_t in, int r, int csize, int max_clusters, 
   const int row_bytes = gp->bk * 4;
   p.kb1 = static_cast<int>(dora::ceil_div(in, gp->bk));
   p.kbtot = p.kb1 + (mode != kGram ? static_cast<int>(dora::ceil_div(r, gp->bk)) : 0);
-  // N-side slices: each CTA of a cluster loads sl rows (a multiple of 8, so
-  // every slice starts on a swizzle-pattern boundary) in nb boxes of nbox rows
-  const int sl = static_cast<int>(dora::round_up(dora::ceil_div(p.NC, csize), 8));
-  p.nb = static_cast<int>(dora::ceil_div(sl, 128));
-  p.nbox = static_cast<int>(dora::round_up(dora::ceil_div(sl, p.nb), 8));
-  p.sl = p.nb * p.nbox;
-  p.NT = csize * p.sl;
+  // the N-side tile in nb boxes of nbox rows (a multiple of 8, so every box
+  // starts on a swizzle-pattern boundary)
+  p.nb = static_cast<int>(dora::ceil_div(p.NC, 128));
+  p.nbox = static_cast<int>(dora::round_up(dora::ceil_div(p.NC, p.nb), 8));
+  p.NT = p.nb * p.nbox;
   p.nmma0 = p.NC <= 256 ? p.NC : 256;
   p.nmma1 = p.NC - p.nmma0;
   // tensor memory: the accumulator (nmma0 columns at 0, nmma1 at 256), then one
@@ -1361,19 +1339,18 @@ bool plan_gemm(int mode, int M, int64_t in, int r, int csize, int max_clusters, 
   while (cols < acc_cols + p.stages * slot_cols) cols *= 2;
   p.tmem_cols = cols;
   const int mtiles = static_cast<int>(dora::ceil_div(M, kBM));
-  const int ngroups = static_cast<int>(dora::ceil_div(mtiles, csize));
-  p.tiles = p.sym ? p.nchunks * (p.nchunks + 1) / 2 : ngroups * p.nchunks;
+  p.tiles = p.sym ? p.nchunks * (p.nchunks + 1) / 2 : mtiles * p.nchunks;
   p.units = static_cast<long long>(p.tiles) * p.kbtot;
   const int min_units = mode == kGram ? kMinUnitsGram : kMinUnitsNorm;
   long long ncl = dora::ceil_div(p.units, min_units);
-  if (ncl > max_clusters) ncl = max_clusters;
+  if (ncl > max_ctas) ncl = max_ctas;
   if (ncl < 1) ncl = 1;
   p.ncl = static_cast<int>(ncl);
-  p.ctas = p.ncl * csize;
+  p.ctas = p.ncl;
   p.maxseg = seg_bound(p.units, p.ncl, p.kbtot);
   p.r = r;
   const size_t per_row = mode == kNorm ? 2 : static_cast<size_t>(p.NC);
-  gp->part_bytes = static_cast<size_t>(ngroups) * csize * p.nchunks * p.maxseg * kBM * per_row * sizeof(float);
+  gp->part_bytes = static_cast<size_t>(mtiles) * p.nchunks * p.maxseg * kBM * per_row * sizeof(float);
   gp->smem_bytes = static_cast<size_t>(p.stages) * p.stage_bytes + 1024 /*align*/ + 8 * (3 * p.stages + 3) + 64;
   // tensor memory: a CTA holding 512 columns must be alone on its SM
   if (p.tmem_cols > 256 && gp->smem_bytes < 116 * 1024) gp->smem_bytes = 116 * 1024;
@@ -1386,11 +1363,11 @@ struct Layout {
 
 size_t al256(size_t x) { return (x + 255) & ~size_t(255); }
 
-// sms: CTAs available to the Gram pass; csize / max_clusters: cluster shape of the norm pass
-bool plan_layout(int64_t out, int64_t in, int64_t r, int sms, int csize, int max_clusters, GemmPlan *gg,
+// sms: CTAs available to each pass
+bool plan_layout(int64_t out, int64_t in, int64_t r, int sms, GemmPlan *gg,
                  GemmPlan *gn, Layout *L) {
-  if (!plan_gemm(kGram, static_cast<int>(r), in, static_cast<int>(r), 1, sms, gg)) return false;
-  if (!plan_gemm(kNorm, static_cast<int>(out), in, static_cast<int>(r), csize, max_clusters, gn)) return false;
+  if (!plan_gemm(kGram, static_cast<int>(r), in, static_cast<int>(r), sms, gg)) return false;
+  if (!plan_gemm(kNorm, static_cast<int>(out), in, static_cast<int>(r), sms, gn)) return false;
   int npad, nchunks, NC;
   plan_n(static_cast<int>(r), &npad, &nchunks, &NC);
   size_t off = 0;
@@ -1422,12 +1399,12 @@ struct BwdLayout {
   size_t a_hi, a_c, y_hi, y_c, g_hi, g_c, h_hi, h_c, part_t, part_r, b_pad, total;
 };
 
-bool plan_bwd(int64_t out, int64_t in, int64_t r, int sms, int csize, int max_clusters, BwdPlans *P, BwdLayout *L) {
+bool plan_bwd(int64_t out, int64_t in, int64_t r, int sms, BwdPlans *P, BwdLayout *L) {
   const int ri = static_cast<int>(r);
-  if (!plan_gemm(kGram, ri, in, ri, 1, sms, &P->gg)) return false;
-  if (!plan_gemm(kGram, ri, out, ri, 1, sms, &P->gh)) return false;
-  if (!plan_gemm(kRows, static_cast<int>(out), in, ri, csize, max_clusters, &P->gb)) return false;
-  if (!plan_gemm(kRows, static_cast<int>(in), out, ri, csize, max_clusters, &P->ga)) return false;
+  if (!plan_gemm(kGram, ri, in, ri, sms, &P->gg)) return false;
+  if (!plan_gemm(kGram, ri, out, ri, sms, &P->gh)) return false;
+  if (!plan_gemm(kRows, static_cast<int>(out), in, ri, sms, &P->gb)) return false;
+  if (!plan_gemm(kRows, static_cast<int>(in), out, ri, sms, &P->ga)) return false;
   P->gh.xt = true;
   P->ga.xt = true;
   P->gb.p.chain = kChainK / P->gb.bk;
@@ -1472,85 +1449,18 @@ int grid_for(long long n, int sms) {
 cudaError_t launch_gemm(const GemmPlan &gp, cudaStream_t cs, const CUtensorMap &x1, const CUtensorMap &x2,
                         const CUtensorMap &y1h, const CUtensorMap &y1c, const CUtensorMap &y2h,
                         const CUtensorMap &y2c) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(gp.p.ctas));
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = gp.smem_bytes;
-  cfg.stream = cs;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = static_cast<unsigned>(gp.p.csize);
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  const dim3 grid(static_cast<unsigned>(gp.p.ctas)), block(kThreads);
   if (gp.xt) {
     if (gp.bk == kBKWide)
-      return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<kBKWide, true>, x1, x2, y1h, y1c, y2h, y2c, gp.p);
-    return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<kBKNarrow, true>, x1, x2, y1h, y1c, y2h, y2c, gp.p);
+      tc_gemm_kernel<kBKWide, true><<<grid, block, gp.smem_bytes, cs>>>(x1, x2, y1h, y1c, y2h, y2c, gp.p);
+    else
+      tc_gemm_kernel<kBKNarrow, true><<<grid, block, gp.smem_bytes, cs>>>(x1, x2, y1h, y1c, y2h, y2c, gp.p);
+  } else if (gp.bk == kBKWide) {
+    tc_gemm_kernel<kBKWide, false><<<grid, block, gp.smem_bytes, cs>>>(x1, x2, y1h, y1c, y2h, y2c, gp.p);
+  } else {
+    tc_gemm_kernel<kBKNarrow, false><<<grid, block, gp.smem_bytes, cs>>>(x1, x2, y1h, y1c, y2h, y2c, gp.p);
   }
-  if (gp.bk == kBKWide) return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<kBKWide, false>, x1, x2, y1h, y1c, y2h, y2c, gp.p);
-  return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<kBKNarrow, false>, x1, x2, y1h, y1c, y2h, y2c, gp.p);
-}
-
-// Cluster shape of the norm pass.  Sharing the N-side tile pays when it is
-// large (chunks of at least kMinClusterN: 32 KB or more per K block); then take
-// the largest cluster (up to kMaxCluster) whose co-resident clusters still
-// cover all but a few SMs.  Otherwise single CTAs.  Occupancy answers are
-// cached per device and shared-memory size.
-void choose_cluster(int device, int sms, int64_t out, int64_t in, int64_t r, int *csize, int *max_clusters) {
-  static std::mutex mu;
-  struct Entry {
-    int device, c;
-    size_t smem;
-    int active;
-  };
-  static Entry cache[64];
-  static int ncache = 0;
-  *csize = 1;
-  *max_clusters = sms;
-  int npad, nchunks, NC;
-  plan_n(static_cast<int>(r), &npad, &nchunks, &NC);
-  if (NC < kMinClusterN) return;
-  for (int c = kMaxCluster; c >= 2; c /= 2) {
-    GemmPlan gp;
-    if (!plan_gemm(kNorm, static_cast<int>(out), in, static_cast<int>(r), c, sms / c, &gp)) continue;
-    int active = -1;
-    {
-      std::lock_guard<std::mutex> lock(mu);
-      for (int i = 0; i < ncache; ++i)
-        if (cache[i].device == device && cache[i].c == c && cache[i].smem == gp.smem_bytes) active = cache[i].active;
-    }
-    if (active < 0) {
-      cudaLaunchConfig_t cfg = {};
-      cfg.gridDim = dim3(static_cast<unsigned>((sms / c) * c));
-      cfg.blockDim = dim3(kThreads);
-      cfg.dynamicSmemBytes = gp.smem_bytes;
-      cudaLaunchAttribute attr[1];
-      attr[0].id = cudaLaunchAttributeClusterDimension;
-      attr[0].val.clusterDim.x = static_cast<unsigned>(c);
-      attr[0].val.clusterDim.y = 1;
-      attr[0].val.clusterDim.z = 1;
-      cfg.attrs = attr;
-      cfg.numAttrs = 1;
-      int n = 0;
-      const cudaError_t e = gp.bk == kBKWide
-                                ? cudaOccupancyMaxActiveClusters(&n, tc_gemm_kernel<kBKWide, false>, &cfg)
-                                : cudaOccupancyMaxActiveClusters(&n, tc_gemm_kernel<kBKNarrow, false>, &cfg);
-      if (e != cudaSuccess) {
-        cudaGetLastError();
-        n = 0;
-      }
-      active = n;
-      std::lock_guard<std::mutex> lock(mu);
-      if (ncache < 64) cache[ncache++] = Entry{device, c, gp.smem_bytes, n};
-    }
-    if (active * c >= sms - 8 && active >= 1) {
-      *csize = c;
-      *max_clusters = active;
-      return;
-    }
-  }
+  return cudaGetLastError();
 }
 
 // ---- bf16 weights: planning
@@ -1573,11 +1483,9 @@ bool plan16(int mode, int M, int64_t in, int r, int max_ctas, Plan16 *gp) {
     p.nchunks = static_cast<int>(dora::ceil_div(npad, p.NC));
     p.sym = 1;
   }
-  const int sl = static_cast<int>(dora::round_up(p.NC, 8));
-  p.nb = static_cast<int>(dora::ceil_div(sl, 128));
-  p.nbox = static_cast<int>(dora::round_up(dora::ceil_div(sl, p.nb), 8));
-  p.sl = p.nb * p.nbox;
-  p.NT = p.sl;
+  p.nb = static_cast<int>(dora::ceil_div(p.NC, 128));
+  p.nbox = static_cast<int>(dora::round_up(dora::ceil_div(p.NC, p.nb), 8));
+  p.NT = p.nb * p.nbox;
   p.nmma0 = p.NC <= 256 ? p.NC : 256;
   p.nmma1 = p.NC - p.nmma0;
   const int acc_cols = p.nmma1 > 0 ? 256 + p.nmma1 : p.nmma0;
@@ -1657,14 +1565,17 @@ cudaError_t launch16(const Plan16 &gp, cudaStream_t cs, const CUtensorMap &x1, c
   return cudaGetLastError();
 }
 
-// Once per device: the address of the device error word and the shared-memory
-// limit of every tensor-core kernel instance.
+// Once per device and context: the address of the device error word and the
+// shared-memory limit of every tensor-core kernel instance.
 dora_status device_init(int device, int **errp) {
   static std::mutex mu;
   static int *err_ptr[64] = {};
+  static uint64_t ctx_of[64] = {};
   std::lock_guard<std::mutex> lock(mu);
   if (device < 0 || device >= 64) return DORA_ERR_CUDA;
-  if (!err_ptr[device]) {
+  const uint64_t ctx = dora::context_id();
+  if (!err_ptr[device] || ctx == 0 || ctx != ctx_of[device]) {
+    err_ptr[device] = nullptr;
     void *ptr = nullptr;
     if (cudaGetSymbolAddress(&ptr, g_dora_err) != cudaSuccess) return DORA_ERR_CUDA;
     const cudaFuncAttribute a = cudaFuncAttributeMaxDynamicSharedMemorySize;
@@ -1676,6 +1587,7 @@ dora_status device_init(int device, int **errp) {
         cudaFuncSetAttribute(tc16_kernel<64>, a, kSmemMax) != cudaSuccess)
       return DORA_ERR_CUDA;
     err_ptr[device] = static_cast<int *>(ptr);
+    ctx_of[device] = dora::context_id();
   }
   *errp = err_ptr[device];
   return DORA_OK;
@@ -1698,16 +1610,12 @@ dora_status test_hooks(int **stall, unsigned long long **limit_ns) {
 
 extern "C" size_t dora_norm_factored_workspace(int64_t out, int64_t in, int64_t r) {
   if (!shape_ok(out, in, r)) return 0;
-  // the largest layout over every cluster shape the norm pass may pick on any
-  // device with up to kMaxCtas SMs
-  size_t total = 0;
-  for (int c = 1; c <= kMaxCluster; c *= 2) {
-    GemmPlan gg, gn;
-    Layout L;
-    if (!plan_layout(out > 0 ? out : 1, in, r, kMaxCtas, c, kMaxCtas / c, &gg, &gn, &L)) return 0;
-    if (L.total > total) total = L.total;
-  }
-  return total;
+  // the layout for kMaxCtas CTAs: the partial-result space only grows with
+  // the CTA count, so this bounds every device with up to kMaxCtas SMs
+  GemmPlan gg, gn;
+  Layout L;
+  if (!plan_layout(out > 0 ? out : 1, in, r, kMaxCtas, &gg, &gn, &L)) return 0;
+  return L.total;
 }
 
 extern "C" dora_status dora_test_stall_loads(int on, uint64_t wait_limit_ns) {
@@ -1755,11 +1663,9 @@ extern "C" dora_status dora_norm_factored(const float *W0, const float *A, const
   st = device_init(device, &errp);
   if (st != DORA_OK) return st;
 
-  int csize = 1, max_clusters = sms;
-  choose_cluster(device, sms, out, in, r, &csize, &max_clusters);
   GemmPlan gg, gn;
   Layout L;
-  if (!plan_layout(out, in, r, sms, csize, max_clusters, &gg, &gn, &L)) return DORA_ERR_SHAPE;
+  if (!plan_layout(out, in, r, sms, &gg, &gn, &L)) return DORA_ERR_SHAPE;
   uint8_t *ws = static_cast<uint8_t *>(workspace);
   float *a_hi = reinterpret_cast<float *>(ws + L.a_hi);
   __nv_bfloat16 *a_c = reinterpret_cast<__nv_bfloat16 *>(ws + L.a_c);
@@ -1818,7 +1724,7 @@ extern "C" dora_status dora_norm_factored(const float *W0, const float *A, const
   ++launches;
 
   // 3. Gs = (s/2) G, split like A
-  StreamK skg{gg.p.units, gg.p.ncl, gg.p.kbtot, gg.p.maxseg, gg.p.csize};
+  StreamK skg{gg.p.units, gg.p.ncl, gg.p.kbtot, gg.p.maxseg};
   {
     const int nsub = (gg.p.NC + 31) / 32;
     gram_reduce_kernel<<<dim3(static_cast<unsigned>(gg.p.tiles), static_cast<unsigned>(nsub * nsub)), dim3(32, 8), 0,
@@ -1851,14 +1757,10 @@ extern "C" dora_status dora_norm_factored(const float *W0, const float *A, const
 // ---------------------------------------------------------------------------
 extern "C" size_t dora_norm_factored_bwd_workspace(int64_t out, int64_t in, int64_t r) {
   if (!shape_ok(out, in, r)) return 0;
-  size_t total = 0;
-  for (int c = 1; c <= kMaxCluster; c *= 2) {
-    BwdPlans P;
-    BwdLayout L;
-    if (!plan_bwd(out > 0 ? out : 1, in, r, kMaxCtas, c, kMaxCtas / c, &P, &L)) return 0;
-    if (L.total > total) total = L.total;
-  }
-  return total;
+  BwdPlans P;
+  BwdLayout L;
+  if (!plan_bwd(out > 0 ? out : 1, in, r, kMaxCtas, &P, &L)) return 0;
+  return L.total;
 }
 
 extern "C" dora_status dora_norm_factored_bwd(const float *W0, const float *A, const float *B, const float *norm,
@@ -1892,11 +1794,9 @@ extern "C" dora_status dora_norm_factored_bwd(const float *W0, const float *A, c
   st = device_init(device, &errp);
   if (st != DORA_OK) return st;
 
-  int csize = 1, max_clusters = sms;
-  choose_cluster(device, sms, out, in, r, &csize, &max_clusters);
   BwdPlans P;
   BwdLayout L;
-  if (!plan_bwd(out, in, r, sms, csize, max_clusters, &P, &L)) return DORA_ERR_SHAPE;
+  if (!plan_bwd(out, in, r, sms, &P, &L)) return DORA_ERR_SHAPE;
   uint8_t *ws = static_cast<uint8_t *>(workspace);
   float *a_hi = reinterpret_cast<float *>(ws + L.a_hi);
   __nv_bfloat16 *a_c = reinterpret_cast<__nv_bfloat16 *>(ws + L.a_c);
@@ -1964,7 +1864,7 @@ extern "C" dora_status dora_norm_factored_bwd(const float *W0, const float *A, c
   if (launch_gemm(pg, cs, mA, mA, mAh_g, mAc_g, mAh_g, mAc_g) != cudaSuccess) return fail();
   ++launches;
   {
-    const StreamK sk{pg.p.units, pg.p.ncl, pg.p.kbtot, pg.p.maxseg, pg.p.csize};
+    const StreamK sk{pg.p.units, pg.p.ncl, pg.p.kbtot, pg.p.maxseg};
     const int nsub = (pg.p.NC + 31) / 32;
     gram_reduce_kernel<<<dim3(static_cast<unsigned>(pg.p.tiles), static_cast<unsigned>(nsub * nsub)), dim3(32, 8), 0,
                          cs>>>(part_t, sk, pg.p.nchunks, pg.p.NC, static_cast<int>(r), npad, s, g_hi, g_c);
@@ -1977,7 +1877,7 @@ extern "C" dora_status dora_norm_factored_bwd(const float *W0, const float *A, c
   if (launch_gemm(ph, cs, mBt, mBt, mYh_h, mYc_h, mYh_h, mYc_h) != cudaSuccess) return fail();
   ++launches;
   {
-    const StreamK sk{ph.p.units, ph.p.ncl, ph.p.kbtot, ph.p.maxseg, ph.p.csize};
+    const StreamK sk{ph.p.units, ph.p.ncl, ph.p.kbtot, ph.p.maxseg};
     const int nsub = (ph.p.NC + 31) / 32;
     gram_reduce_kernel<<<dim3(static_cast<unsigned>(ph.p.tiles), static_cast<unsigned>(nsub * nsub)), dim3(32, 8), 0,
                          cs>>>(part_t, sk, ph.p.nchunks, ph.p.NC, static_cast<int>(r), npad, s, h_hi, h_c);
@@ -1990,7 +1890,7 @@ extern "C" dora_status dora_norm_factored_bwd(const float *W0, const float *A, c
   if (launch_gemm(pb, cs, mW0, mB, mAh_b, mAc_b, mGh, mGc) != cudaSuccess) return fail();
   ++launches;
   {
-    const StreamK sk{pb.p.units, pb.p.ncl, pb.p.kbtot, pb.p.maxseg, pb.p.csize};
+    const StreamK sk{pb.p.units, pb.p.ncl, pb.p.kbtot, pb.p.maxseg};
     const unsigned mtiles = static_cast<unsigned>(dora::ceil_div(out, kBM));
     rows_reduce_kernel<<<dim3(mtiles * pb.p.nchunks, static_cast<unsigned>((pb.p.NC + 31) / 32)), 256, 0, cs>>>(
         reinterpret_cast<const float4 *>(part_r), sk, pb.p.nchunks, pb.p.NC, static_cast<int>(out),
@@ -2005,7 +1905,7 @@ extern "C" dora_status dora_norm_factored_bwd(const float *W0, const float *A, c
   if (launch_gemm(pa, cs, mW0t, mAt, mYh_a, mYc_a, mHh, mHc) != cudaSuccess) return fail();
   ++launches;
   {
-    const StreamK sk{pa.p.units, pa.p.ncl, pa.p.kbtot, pa.p.maxseg, pa.p.csize};
+    const StreamK sk{pa.p.units, pa.p.ncl, pa.p.kbtot, pa.p.maxseg};
     const unsigned mtiles = static_cast<unsigned>(dora::ceil_div(in, kBM));
     rows_reduce_kernel<<<dim3(mtiles * pa.p.nchunks, static_cast<unsigned>((pa.p.NC + 31) / 32)), 256, 0, cs>>>(
         reinterpret_cast<const float4 *>(part_r), sk, pa.p.nchunks, pa.p.NC, static_cast<int>(in),
@@ -2118,7 +2018,7 @@ extern "C" dora_status dora_norm_factored_bf16(const void *W0, const void *A, co
 
   // 2. s/2 G as three bf16 pieces; the norm pass's counters zeroed
   {
-    StreamK skg{gg.p.units, gg.p.ncl, gg.p.kbtot, gg.p.maxseg, 1};
+    StreamK skg{gg.p.units, gg.p.ncl, gg.p.kbtot, gg.p.maxseg};
     const int nsub = (gg.p.NC + 31) / 32;
     gram_reduce3_kernel<<<dim3(static_cast<unsigned>(gg.p.tiles), static_cast<unsigned>(nsub * nsub)), dim3(32, 8), 0,
                           cs>>>(part_g, skg, gg.p.nchunks, gg.p.NC, static_cast<int>(r), npad, static_cast<int>(rs),

@@ -119,6 +119,17 @@ def make_weights(sh: ModuleShape, seed: int) -> dict:
     return {"W0": W0, "A": A, "B": B, "m": m, "s": sh.s}
 
 
+def stress_magnitude(row_norm: np.ndarray, seed: int) -> np.ndarray:
+    """The g ~ 1 stress set's magnitude: m_i = row_norm_i * (1 + U(-2^-9, 2^-9))
+    as float32.  With row_norm = ||W0_i|| this is the literal definition of the
+    high-rank workload's stress subset; with row_norm = the adapted norm n_i
+    (from the oracle), g - 1 = m/n - 1 lies in bf16's collapse region, where a
+    naive bf16 compose rounds g to 1 and loses the base correction."""
+    rng = np.random.default_rng([seed, 3])
+    u = rng.uniform(-2.0 ** -9, 2.0 ** -9, size=np.shape(row_norm))
+    return (np.asarray(row_norm, np.float64) * (1.0 + u)).astype(np.float32)
+
+
 def make_activations(sh: ModuleShape, seed: int, weights: dict | None = None) -> dict:
     """base, lora, grad_out [T,out]: float32 arrays for act='f32', uint16
     bf16 bit patterns for act='bf16'."""

@@ -1,9 +1,10 @@
 """GPU parity of dora_norm_factored_bwd (gradient through the row norm into A
 and B) against the fp64 oracle's norm_grad, through the C ABI.
 
-Inputs: the seeded weights of the parity shapes, n and g from the library's
-own forward (the backward's inputs; the oracle receives the same fp32
-values), d_mag drawn from a seeded normal.
+Inputs: the seeded weights of the parity shapes; n and g from the oracle's
+dense norm, rounded to fp32 (the backward's inputs -- both sides receive the
+same fp32 values, so no input of the oracle comes from the library); d_mag
+drawn from a seeded normal.
 
 Tolerance, derived from the arithmetic.  Every output element is a sum of
 products evaluated with the split-TF32 scheme (per product error <= 2^-18 of
@@ -69,14 +70,22 @@ def _case(out, inp, r, seed):
     return d, d_mag
 
 
+def oracle_norm_f32(d, rows=None):
+    """The oracle's n and g rounded to fp32 (inputs of the backward on both sides)."""
+    W0, B, m = (d[k] if rows is None else d[k][rows] for k in ("W0", "B", "m"))
+    n, g = oracle.weight_norm(W0, d["A"], B, m, d["s"])
+    return n.astype(np.float32), g.astype(np.float32)
+
+
 def _run_and_check(d, d_mag):
     s = d["s"]
-    W0, A, B, m = (f32_dev(d[k]) for k in ("W0", "A", "B", "m"))
-    norm, g = run_norm(W0, A, B, m, s)
+    W0, A, B = (f32_dev(d[k]) for k in ("W0", "A", "B"))
+    n32, g32 = oracle_norm_f32(d)
+    norm, g = f32_dev(n32), f32_dev(g32)
     dm = f32_dev(d_mag)
     dA, dB = run_norm_bwd(W0, A, B, norm, g, dm, s)
     assert_no_device_error()
-    n32, g32 = to_f64(norm), to_f64(g)
+    n32, g32 = n32.astype(np.float64), g32.astype(np.float64)
     dA_ref, dB_ref = oracle.norm_grad(d["W0"], d["A"], d["B"], s, n32, g32, d_mag)
     dA_abs, dB_abs = abs_refs(d["W0"].astype(np.float64), d["A"].astype(np.float64), d["B"].astype(np.float64), s,
                               n32, g32, d_mag.astype(np.float64))
@@ -155,11 +164,11 @@ def test_full_size_sampled(r):
     out, inp = d["W0"].shape
     rng = np.random.default_rng(9300 + r)
     d_mag = (0.1 * rng.standard_normal(out)).astype(np.float32)
-    W0, A, B, m = (f32_dev(d[k]) for k in ("W0", "A", "B", "m"))
-    norm, g = run_norm(W0, A, B, m, s)
-    dA, dB = run_norm_bwd(W0, A, B, norm, g, f32_dev(d_mag), s)
+    W0, A, B = (f32_dev(d[k]) for k in ("W0", "A", "B"))
+    n32, g32 = oracle_norm_f32(d)
+    dA, dB = run_norm_bwd(W0, A, B, f32_dev(n32), f32_dev(g32), f32_dev(d_mag), s)
     assert_no_device_error()
-    n32, g32 = to_f64(norm), to_f64(g)
+    n32, g32 = n32.astype(np.float64), g32.astype(np.float64)
     rows = np.sort(rng.choice(out, 96, replace=False))
     cols = np.sort(rng.choice(inp, 96, replace=False))
     rows[0], cols[-1] = 0, inp - 1

@@ -6,14 +6,16 @@ allocator, or services that forbid cudaMalloc after start-up because it
 synchronises the device.  For them the library keeps the d_mag partial sums in
 one fixed device array instead of a caller workspace.  This test calls that
 entry point through the C ABI twice in a row (the second call finds the first
-call's leftovers in the shared array) and checks each result against the
-workspace entry point dora_compose_bwd under the usual GPU tolerances.  It is
-collected last so that a failure here cannot hide the other tests' results.
+call's leftovers in the shared array) and checks each result against the fp64
+oracle under the usual GPU tolerances, and against the workspace entry point
+dora_compose_bwd, which launches the same grid and so must agree bitwise.  It
+is collected last so that a failure here cannot hide the other tests' results.
 """
 import numpy as np
 import pytest
 import torch
 
+import oracle
 import parameter_efficient_fine_gb300 as dora
 from parameter_efficient_fine_gb300 import workloads as wl
 
@@ -32,7 +34,7 @@ def _inputs(out, T, seed):
     return a, g, n, sh.s
 
 
-def test_noalloc_backward_matches_workspace_entry_point_twice():
+def test_noalloc_backward_matches_oracle_and_workspace_entry_point_twice():
     for out, T, seed in ((4096, 1536, 1), (1000, 333, 2)):
         a, g, n, s = _inputs(out, T, seed)
         dy, base, lora = (act_to_dev(a[k]) for k in ("dy", "base", "lora"))
@@ -43,11 +45,17 @@ def test_noalloc_backward_matches_workspace_entry_point_twice():
         dm = torch.full((out,), float("nan"), device=DEV)
         dora.dora_compose_bwd_noalloc(dy, base, lora, gd, nd, s, db, dl, dm)
         torch.cuda.synchronize()
-        check_bf16_rule("d_base", to_f64(db), to_f64(db_ref))
-        check_bf16_rule("d_lora", to_f64(dl), to_f64(dl_ref))
+        # the fp64 oracle on the same inputs
         d64, b64, l64 = (act_to_f64(a[k]) for k in ("dy", "base", "lora"))
-        check_bound("d_mag", to_f64(dm), to_f64(dm_ref), dmag_bound(d64, b64, l64, n.astype(np.float64), s))
-        check_bf16_rule("d_mag", to_f64(dm), to_f64(dm_ref))
+        g64, n64 = g.astype(np.float64), n.astype(np.float64)
+        db_o, dl_o, dm_o = oracle.compose_bwd(d64, b64, l64, g64, n64, s)
+        check_bf16_rule("d_base", to_f64(db), db_o)
+        check_bf16_rule("d_lora", to_f64(dl), dl_o)
+        check_bf16_rule("d_mag", to_f64(dm), dm_o)
+        check_bound("d_mag", to_f64(dm), dm_o, dmag_bound(d64, b64, l64, n64, s))
+        # the workspace entry point: same grid, same summation order
+        assert torch.equal(db, db_ref) and torch.equal(dl, dl_ref)
+        assert torch.equal(dm.view(torch.int32), dm_ref.view(torch.int32))
     assert_no_device_error()
 
 

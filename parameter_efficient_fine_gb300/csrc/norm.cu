@@ -209,13 +209,18 @@ __device__ void wait_drain(uint32_t bar, uint32_t parity) { wait_drain_ns(bar, p
 // loads an unswizzled [BK x 128] box and the converters read it column-wise
 // (lane = M row, conflict-free), the rest is unchanged.
 // ---------------------------------------------------------------------------
-template <int BK, bool XT>
+template <int BK, bool XT, bool B3>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_gemm_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ CUtensorMap mX2,
                const __grid_constant__ CUtensorMap mY1h, const __grid_constant__ CUtensorMap mY1c,
                const __grid_constant__ CUtensorMap mY2h, const __grid_constant__ CUtensorMap mY2c,
                const TcParams p) {
-  constexpr int kRowBytes = BK * 4;   // one swizzle span
+  static_assert(!B3 || BK == 32, "the bf16 three-product scheme uses 32-wide K blocks");
+  constexpr int kRowBytes = BK * 4;   // one swizzle span of the raw fp32 M-side box
+  // one N-side row per operand: BK fp32 (TF32 hi) / BK bf16 pairs (correction)
+  // in the TF32 scheme, BK bf16 (h or l) in the bf16 scheme
+  constexpr int kNRowBytes = B3 ? BK * 2 : BK * 4;
+  constexpr int kSlotCols = B3 ? BK : 2 * BK;   // tensor-memory columns of one M-side operand slot
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int S = p.stages;
@@ -290,18 +295,19 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ 
           mbar_expect_tx(fb, p.tx_bytes);
           const uint32_t xs = smem_u32(smem + static_cast<size_t>(stage) * p.stage_bytes);
           const uint32_t yh = xs + kBM * kRowBytes;
-          const uint32_t yc = yh + static_cast<uint32_t>(p.NT) * kRowBytes;
+          const uint32_t yc = yh + static_cast<uint32_t>(p.NT) * kNRowBytes;
           const bool seg1 = kb < p.kb1;
-          const int kx = (seg1 ? kb : kb - p.kb1) * BK;    // fp32 column of the hi operands
+          const int kx = (seg1 ? kb : kb - p.kb1) * BK;    // first K index of the block
           if (XT) tma_load_2d(xs, seg1 ? &mX1 : &mX2, mt * kBM, kx, fb);
           else tma_load_2d(xs, seg1 ? &mX1 : &mX2, kx, mt * kBM, fb);
-          // the N-side tile of the chunk, hi and correction operands
+          // the N-side tile of the chunk: TF32 hi and bf16 correction operands
+          // (TF32 scheme), or the bf16 h and l operands (bf16 scheme)
           for (int i = 0; i < p.nb; ++i) {
             const int ro = i * p.nbox;
             const int ny = nc * p.NC + ro;
-            const uint32_t off = static_cast<uint32_t>(ro * kRowBytes);
+            const uint32_t off = static_cast<uint32_t>(ro * kNRowBytes);
             tma_load_2d(yh + off, seg1 ? &mY1h : &mY2h, kx, ny, fb);
-            tma_load_2d(yc + off, seg1 ? &mY1c : &mY2c, 2 * kx, ny, fb);   // bf16 column
+            tma_load_2d(yc + off, seg1 ? &mY1c : &mY2c, B3 ? kx : 2 * kx, ny, fb);   // bf16 column
           }
           ++issued;
           if (++stage == S) {
@@ -350,13 +356,39 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ 
             break;
           }
           tc_fence_after();
+          const uint32_t yh = smem_u32(smem + static_cast<size_t>(stage) * p.stage_bytes) + kBM * kRowBytes;
+          const uint32_t yc = yh + static_cast<uint32_t>(p.NT) * kNRowBytes;
+          if constexpr (B3) {
+            // M-side operand slot: BK/2 columns of h (two bf16 per column,
+            // K-consecutive), then BK/2 columns of l.  Per K = 16 step three
+            // products h_x h_y + l_x h_y + h_x l_y into the same accumulator.
+            const uint32_t sh = tmem + static_cast<uint32_t>(p.slot0 + stage * kSlotCols);
+            const uint32_t sl = sh + BK / 2;
+#pragma unroll
+            for (int k = 0; k < BK / 16; ++k) {
+              const uint32_t acc0 = (kb != kb0 || k != 0) ? 1u : 0u;
+              const uint32_t ko = static_cast<uint32_t>(k) * 32u;   // 16 bf16 along the 64-byte row
+              const uint32_t ah = sh + 8u * k, al = sl + 8u * k;
+              {
+                const uint64_t bh = sdesc<BK / 2>(yh + ko), bl = sdesc<BK / 2>(yc + ko);
+                mma_bf16_ta(tmem, ah, bh, ic0, acc0);
+                mma_bf16_ta(tmem, al, bh, ic0, 1u);
+                mma_bf16_ta(tmem, ah, bl, ic0, 1u);
+              }
+              if (p.nmma1 > 0) {
+                const uint32_t no = 256u * kNRowBytes;
+                const uint64_t bh = sdesc<BK / 2>(yh + no + ko), bl = sdesc<BK / 2>(yc + no + ko);
+                mma_bf16_ta(tmem + 256u, ah, bh, ic1, acc0);
+                mma_bf16_ta(tmem + 256u, al, bh, ic1, 1u);
+                mma_bf16_ta(tmem + 256u, ah, bl, ic1, 1u);
+              }
+            }
+          } else {
           // M-side operand slot of this stage in tensor memory: BK columns of
           // hi (one fp32 per column), then BK/8 groups of 8 columns holding the
           // group's 16 bf16 correction values (two per column)
-          const uint32_t ah0 = tmem + static_cast<uint32_t>(p.slot0 + stage * 2 * BK);
+          const uint32_t ah0 = tmem + static_cast<uint32_t>(p.slot0 + stage * kSlotCols);
           const uint32_t ac0 = ah0 + BK;
-          const uint32_t yh = smem_u32(smem + static_cast<size_t>(stage) * p.stage_bytes) + kBM * kRowBytes;
-          const uint32_t yc = yh + static_cast<uint32_t>(p.NT) * kRowBytes;
 #pragma unroll
           for (int k = 0; k < BK / 8; ++k) {
             const uint32_t acc0 = (kb != kb0 || k != 0) ? 1u : 0u;
@@ -375,6 +407,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ 
               mma_bf16_ta(tmem + 256u, ac, bc, ic1, acc0);
               mma_tf32_ta(tmem + 256u, ah, bh, id1, 1u);
             }
+          }
           }
           mma_commit(empty0 + 8u * stage);
           if (++stage == S) {
@@ -430,11 +463,9 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ 
         const uint8_t *xbox = smem + static_cast<size_t>(stage) * p.stage_bytes;
         const float4 *xr = reinterpret_cast<const float4 *>(xbox + row * kRowBytes);
         const float *xc = reinterpret_cast<const float *>(xbox) + row;   // XT: column `row` of [BK][128]
-        const uint32_t slot = lane_addr + static_cast<uint32_t>(p.slot0 + stage * 2 * BK);
+        const uint32_t slot = lane_addr + static_cast<uint32_t>(p.slot0 + stage * kSlotCols);
         float blk = 0.0f;
-#pragma unroll
-        for (int q = 0; q < BK / 8; ++q) {
-          float v[8];
+        auto load8 = [&](int q, float (&v)[8]) {
           if (XT) {
 #pragma unroll
             for (int e = 0; e < 8; ++e) v[e] = xc[(8 * q + e) * kBM];
@@ -443,6 +474,36 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ 
             v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
             v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
           }
+        };
+        if constexpr (B3) {
+          // x = h + l: h = bf16(x), l = bf16(x - h); per K = 16 step 8 columns
+          // of h pairs and 8 of l pairs (column c holds K indices 2c, 2c + 1)
+#pragma unroll
+          for (int q16 = 0; q16 < BK / 16; ++q16) {
+            uint32_t hb[8], lb[8];
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+              float v[8];
+              load8(2 * q16 + half, v);
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const float x0 = v[2 * e], x1 = v[2 * e + 1];
+                blk = fmaf(x0, x0, blk);
+                blk = fmaf(x1, x1, blk);
+                const uint32_t h = pack_bf16x2(x0, x1);
+                hb[4 * half + e] = h;
+                lb[4 * half + e] =
+                    pack_bf16x2(x0 - __uint_as_float(h << 16), x1 - __uint_as_float(h & 0xffff0000u));
+              }
+            }
+            tmem_st8(slot + 8u * q16, hb);
+            tmem_st8(slot + BK / 2 + 8u * q16, lb);
+          }
+        } else {
+#pragma unroll
+        for (int q = 0; q < BK / 8; ++q) {
+          float v[8];
+          load8(q, v);
           uint32_t hb[8], cb[8];
           float l[8];
 #pragma unroll
@@ -458,6 +519,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ 
           }
           tmem_st8(slot + 8u * q, hb);
           tmem_st8(slot + BK + 8u * q, cb);
+        }
         }
         tmem_wait_st();
         if (kb < p.kb1) n0 += blk;
@@ -639,6 +701,31 @@ __global__ void __launch_bounds__(256) split_n_kernel(const float *__restrict__ 
   }
 }
 
+// N-side split of a [rows, cols] fp32 matrix for the bf16 three-product
+// scheme, and zero fill of the norm pass's ncnt completion counters:
+//   h [rows, cols8] bf16: x rounded to bf16 (nearest even)
+//   l [rows, cols8] bf16: x - h rounded to bf16;  zero past cols
+// (cols8 = cols rounded up to 8, a 16-byte row).  One thread per group of 4.
+__global__ void __launch_bounds__(256) split_hl_kernel(const float *__restrict__ x, long long rows, int cols,
+                                                       int cols8, __nv_bfloat16 *__restrict__ h,
+                                                       __nv_bfloat16 *__restrict__ l, int *__restrict__ cnt,
+                                                       int ncnt) {
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < ncnt; i += gridDim.x * blockDim.x) cnt[i] = 0;
+  const int g4 = cols8 / 4;
+  const long long n = rows * g4;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
+    const long long row = i / g4;
+    const int k = static_cast<int>(i - row * g4) * 4;
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (k < cols) v = __ldg(reinterpret_cast<const float4 *>(x + row * cols + k));
+    const uint32_t h01 = pack_bf16x2(v.x, v.y), h23 = pack_bf16x2(v.z, v.w);
+    const uint32_t l01 = pack_bf16x2(v.x - __uint_as_float(h01 << 16), v.y - __uint_as_float(h01 & 0xffff0000u));
+    const uint32_t l23 = pack_bf16x2(v.z - __uint_as_float(h23 << 16), v.w - __uint_as_float(h23 & 0xffff0000u));
+    *reinterpret_cast<uint2 *>(h + row * cols8 + k) = make_uint2(h01, h23);
+    *reinterpret_cast<uint2 *>(l + row * cols8 + k) = make_uint2(l01, l23);
+  }
+}
+
 // B [out, r] -> Bp [out, rp] with zero columns r..rp-1 (rp = r rounded up to 4)
 __global__ void __launch_bounds__(256) pad_cols_kernel(const float *__restrict__ B, long long rows, int r, int rp,
                                                        float *__restrict__ Bp) {
@@ -660,14 +747,24 @@ struct StreamK {
 };
 
 // Gs[k][l] = (s/2) * G[k][l] for k, l < r (zero-padded to npad), split like
-// split_n_kernel: gh [npad, npad] TF32, gc [npad, 2*npad] bf16 (8 hi, 8 lo per group)
-__device__ __forceinline__ void store_gs(int a, int b, float v, int npad, float *gh, __nv_bfloat16 *gc) {
+// the N side of the GEMM.  TF32 scheme (split_n_kernel): gh [npad, npad] TF32,
+// gc [npad, 2*npad] bf16 (8 hi, 8 lo per group).  bf16 scheme (split_hl_kernel):
+// gh and gc both bf16 [npad, npad], h = bf16(v) and l = bf16(v - h).
+template <bool B3>
+__device__ __forceinline__ void store_gs(int a, int b, float v, int npad, void *gh, __nv_bfloat16 *gc) {
   if (a >= npad || b >= npad) return;
-  const float h = __uint_as_float(tf32_rna(v));
-  gh[static_cast<long long>(a) * npad + b] = h;
-  const long long cb = static_cast<long long>(a) * 2 * npad + 16 * (b / 8) + (b % 8);
-  gc[cb] = __float2bfloat16_rn(h);
-  gc[cb + 8] = __float2bfloat16_rn(v - h);
+  const long long i = static_cast<long long>(a) * npad + b;
+  if constexpr (B3) {
+    const __nv_bfloat16 h = __float2bfloat16_rn(v);
+    static_cast<__nv_bfloat16 *>(gh)[i] = h;
+    gc[i] = __float2bfloat16_rn(v - __bfloat162float(h));
+  } else {
+    const float h = __uint_as_float(tf32_rna(v));
+    static_cast<float *>(gh)[i] = h;
+    const long long cb = static_cast<long long>(a) * 2 * npad + 16 * (b / 8) + (b % 8);
+    gc[cb] = __float2bfloat16_rn(h);
+    gc[cb + 8] = __float2bfloat16_rn(v - h);
+  }
 }
 
 // One 32 x 32 block of an upper-triangular Gram tile (blockIdx.x = tile, whose
@@ -677,9 +774,10 @@ __device__ __forceinline__ void store_gs(int a, int b, float v, int npad, float 
 // the 8 warp sums are then added in warp order.  The block is written at
 // (k, l) and, for a tile off the diagonal, mirrored at (l, k) through shared
 // memory, so both writes are coalesced.
+template <bool B3>
 __global__ void __launch_bounds__(256) gram_reduce_kernel(const float *__restrict__ part, StreamK sk, int nchunks,
                                                           int NC, int r, int npad, float half_s,
-                                                          float *__restrict__ gh, __nv_bfloat16 *__restrict__ gc) {
+                                                          void *__restrict__ gh, __nv_bfloat16 *__restrict__ gc) {
   __shared__ float wsum[8][32][33];
   const int t = blockIdx.x;
   int mt, nc;
@@ -722,7 +820,7 @@ __global__ void __launch_bounds__(256) gram_reduce_kernel(const float *__restric
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     const int i = ty + 8 * q;
-    store_gs(mt * kBM + sr * 32 + i, nc * NC + col, v[q], npad, gh, gc);
+    store_gs<B3>(mt * kBM + sr * 32 + i, nc * NC + col, v[q], npad, gh, gc);
     wsum[0][i][tx] = v[q];
   }
   if (mt != nc) {
@@ -730,7 +828,7 @@ __global__ void __launch_bounds__(256) gram_reduce_kernel(const float *__restric
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       const int i = ty + 8 * q;
-      store_gs(nc * NC + sc * 32 + i, mt * kBM + sr * 32 + tx, wsum[0][tx][i], npad, gh, gc);
+      store_gs<B3>(nc * NC + sc * 32 + i, mt * kBM + sr * 32 + tx, wsum[0][tx][i], npad, gh, gc);
     }
   }
 }
@@ -1277,8 +1375,9 @@ __global__ void __launch_bounds__(256) gram_reduce3_kernel(const float *__restri
 // ---------------------------------------------------------------------------
 struct GemmPlan {
   TcParams p;
-  int bk;   // fp32 per K block (the kernel instance)
+  int bk;   // K indices per K block (the kernel instance)
   bool xt;  // M-side operand stored transposed (the kernel instance)
+  bool b3;  // bf16 three-product scheme (else TF32 hi + one bf16 correction)
   size_t smem_bytes;
   size_t part_bytes;
 };
@@ -1297,10 +1396,11 @@ void plan_n(int r, int *npad, int *nchunks, int *NC) {
 }
 
 // K = in (+ r for the norm and row passes); at most max_ctas CTAs
-bool plan_gemm(int mode, int M, int64_t in, int r, int max_ctas, GemmPlan *gp) {
+bool plan_gemm(int mode, int M, int64_t in, int r, int max_ctas, GemmPlan *gp, bool b3 = false) {
   TcParams &p = gp->p;
   std::memset(&p, 0, sizeof(p));
   gp->xt = false;
+  gp->b3 = b3;
   p.mode = mode;
   p.M = M;
   int npad;
@@ -1311,8 +1411,9 @@ bool plan_gemm(int mode, int M, int64_t in, int r, int max_ctas, GemmPlan *gp) {
     p.nchunks = static_cast<int>(dora::ceil_div(npad, p.NC));
     p.sym = 1;
   }
-  gp->bk = p.NC <= kMaxChunkWide ? kBKWide : kBKNarrow;
-  const int row_bytes = gp->bk * 4;
+  gp->bk = (b3 || p.NC <= kMaxChunkWide) ? kBKWide : kBKNarrow;
+  const int row_bytes = gp->bk * 4;                   // raw fp32 M-side box
+  const int nrow_bytes = b3 ? gp->bk * 2 : gp->bk * 4;  // each N-side operand
   p.kb1 = static_cast<int>(dora::ceil_div(in, gp->bk));
   p.kbtot = p.kb1 + (mode != kGram ? static_cast<int>(dora::ceil_div(r, gp->bk)) : 0);
   // the N-side tile in nb boxes of nbox rows (a multiple of 8, so every box
@@ -1323,13 +1424,13 @@ bool plan_gemm(int mode, int M, int64_t in, int r, int max_ctas, GemmPlan *gp) {
   p.nmma0 = p.NC <= 256 ? p.NC : 256;
   p.nmma1 = p.NC - p.nmma0;
   // tensor memory: the accumulator (nmma0 columns at 0, nmma1 at 256), then one
-  // M-side operand slot of 2 * bk columns per stage
+  // M-side operand slot per stage (2 * bk columns: TF32 hi and bf16 pairs; or
+  // bk columns: bf16 h and l pairs)
   const int acc_cols = static_cast<int>(dora::round_up(p.nmma1 > 0 ? 256 + p.nmma1 : p.nmma0, 32));
-  const int slot_cols = 2 * gp->bk;
+  const int slot_cols = b3 ? gp->bk : 2 * gp->bk;
   p.slot0 = acc_cols;
-  // a stage in shared memory: the raw M-side box, then the N-side hi and
-  // correction tiles
-  p.stage_bytes = static_cast<unsigned>(kBM * row_bytes + 2 * p.NT * row_bytes);
+  // a stage in shared memory: the raw M-side box, then the two N-side tiles
+  p.stage_bytes = static_cast<unsigned>(kBM * row_bytes + 2 * p.NT * nrow_bytes);
   p.tx_bytes = p.stage_bytes;
   p.stages = static_cast<int>((kSmemMax - 1024 - 512) / p.stage_bytes);
   if (p.stages > kMaxStages) p.stages = kMaxStages;
@@ -1357,8 +1458,12 @@ bool plan_gemm(int mode, int M, int64_t in, int r, int max_ctas, GemmPlan *gp) {
   return true;
 }
 
+// forward-norm workspace (bf16 three-product scheme): the N-side split of A
+// (a_h, a_l: bf16 [r, in8]) and of s/2 G (g_h, g_l: bf16 [npad, npad]), the
+// Gram and norm partials, B padded to a 16-byte row when r % 4 != 0, and the
+// completion counters of the fused n / g finalize
 struct Layout {
-  size_t a_hi, a_c, g_hi, g_c, part_g, part_n, b_pad, cnt, total;
+  size_t a_h, a_l, g_h, g_l, part_g, part_n, b_pad, cnt, total;
 };
 
 size_t al256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -1366,8 +1471,8 @@ size_t al256(size_t x) { return (x + 255) & ~size_t(255); }
 // sms: CTAs available to each pass
 bool plan_layout(int64_t out, int64_t in, int64_t r, int sms, GemmPlan *gg,
                  GemmPlan *gn, Layout *L) {
-  if (!plan_gemm(kGram, static_cast<int>(r), in, static_cast<int>(r), sms, gg)) return false;
-  if (!plan_gemm(kNorm, static_cast<int>(out), in, static_cast<int>(r), sms, gn)) return false;
+  if (!plan_gemm(kGram, static_cast<int>(r), in, static_cast<int>(r), sms, gg, true)) return false;
+  if (!plan_gemm(kNorm, static_cast<int>(out), in, static_cast<int>(r), sms, gn, true)) return false;
   int npad, nchunks, NC;
   plan_n(static_cast<int>(r), &npad, &nchunks, &NC);
   size_t off = 0;
@@ -1376,10 +1481,11 @@ bool plan_layout(int64_t out, int64_t in, int64_t r, int sms, GemmPlan *gg,
     off += al256(bytes);
     return o;
   };
-  L->a_hi = take(static_cast<size_t>(r) * in * 4);
-  L->a_c = take(static_cast<size_t>(r) * dora::round_up(in, 8) * 4);   // bf16 [r, 2*in8]
-  L->g_hi = take(static_cast<size_t>(npad) * npad * 4);
-  L->g_c = take(static_cast<size_t>(npad) * npad * 4);                 // bf16 [npad, 2*npad]
+  const size_t in8 = static_cast<size_t>(dora::round_up(in, 8));
+  L->a_h = take(static_cast<size_t>(r) * in8 * 2);
+  L->a_l = take(static_cast<size_t>(r) * in8 * 2);
+  L->g_h = take(static_cast<size_t>(npad) * npad * 2);
+  L->g_l = take(static_cast<size_t>(npad) * npad * 2);
   L->part_g = take(gg->part_bytes);
   L->part_n = take(gn->part_bytes);
   L->b_pad = (r % 4) ? take(static_cast<size_t>(out) * dora::round_up(r, 4) * 4) : 0;
@@ -1450,15 +1556,20 @@ cudaError_t launch_gemm(const GemmPlan &gp, cudaStream_t cs, const CUtensorMap &
                         const CUtensorMap &y1h, const CUtensorMap &y1c, const CUtensorMap &y2h,
                         const CUtensorMap &y2c) {
   const dim3 grid(static_cast<unsigned>(gp.p.ctas)), block(kThreads);
-  if (gp.xt) {
-    if (gp.bk == kBKWide)
-      tc_gemm_kernel<kBKWide, true><<<grid, block, gp.smem_bytes, cs>>>(x1, x2, y1h, y1c, y2h, y2c, gp.p);
+  if (gp.b3) {
+    if (gp.xt)
+      tc_gemm_kernel<kBKWide, true, true><<<grid, block, gp.smem_bytes, cs>>>(x1, x2, y1h, y1c, y2h, y2c, gp.p);
     else
-      tc_gemm_kernel<kBKNarrow, true><<<grid, block, gp.smem_bytes, cs>>>(x1, x2, y1h, y1c, y2h, y2c, gp.p);
+      tc_gemm_kernel<kBKWide, false, true><<<grid, block, gp.smem_bytes, cs>>>(x1, x2, y1h, y1c, y2h, y2c, gp.p);
+  } else if (gp.xt) {
+    if (gp.bk == kBKWide)
+      tc_gemm_kernel<kBKWide, true, false><<<grid, block, gp.smem_bytes, cs>>>(x1, x2, y1h, y1c, y2h, y2c, gp.p);
+    else
+      tc_gemm_kernel<kBKNarrow, true, false><<<grid, block, gp.smem_bytes, cs>>>(x1, x2, y1h, y1c, y2h, y2c, gp.p);
   } else if (gp.bk == kBKWide) {
-    tc_gemm_kernel<kBKWide, false><<<grid, block, gp.smem_bytes, cs>>>(x1, x2, y1h, y1c, y2h, y2c, gp.p);
+    tc_gemm_kernel<kBKWide, false, false><<<grid, block, gp.smem_bytes, cs>>>(x1, x2, y1h, y1c, y2h, y2c, gp.p);
   } else {
-    tc_gemm_kernel<kBKNarrow, false><<<grid, block, gp.smem_bytes, cs>>>(x1, x2, y1h, y1c, y2h, y2c, gp.p);
+    tc_gemm_kernel<kBKNarrow, false, false><<<grid, block, gp.smem_bytes, cs>>>(x1, x2, y1h, y1c, y2h, y2c, gp.p);
   }
   return cudaGetLastError();
 }
@@ -1579,10 +1690,12 @@ dora_status device_init(int device, int **errp) {
     void *ptr = nullptr;
     if (cudaGetSymbolAddress(&ptr, g_dora_err) != cudaSuccess) return DORA_ERR_CUDA;
     const cudaFuncAttribute a = cudaFuncAttributeMaxDynamicSharedMemorySize;
-    if (cudaFuncSetAttribute(tc_gemm_kernel<kBKNarrow, false>, a, kSmemMax) != cudaSuccess ||
-        cudaFuncSetAttribute(tc_gemm_kernel<kBKWide, false>, a, kSmemMax) != cudaSuccess ||
-        cudaFuncSetAttribute(tc_gemm_kernel<kBKNarrow, true>, a, kSmemMax) != cudaSuccess ||
-        cudaFuncSetAttribute(tc_gemm_kernel<kBKWide, true>, a, kSmemMax) != cudaSuccess ||
+    if (cudaFuncSetAttribute(tc_gemm_kernel<kBKNarrow, false, false>, a, kSmemMax) != cudaSuccess ||
+        cudaFuncSetAttribute(tc_gemm_kernel<kBKWide, false, false>, a, kSmemMax) != cudaSuccess ||
+        cudaFuncSetAttribute(tc_gemm_kernel<kBKNarrow, true, false>, a, kSmemMax) != cudaSuccess ||
+        cudaFuncSetAttribute(tc_gemm_kernel<kBKWide, true, false>, a, kSmemMax) != cudaSuccess ||
+        cudaFuncSetAttribute(tc_gemm_kernel<kBKWide, false, true>, a, kSmemMax) != cudaSuccess ||
+        cudaFuncSetAttribute(tc_gemm_kernel<kBKWide, true, true>, a, kSmemMax) != cudaSuccess ||
         cudaFuncSetAttribute(tc16_kernel<32>, a, kSmemMax) != cudaSuccess ||
         cudaFuncSetAttribute(tc16_kernel<64>, a, kSmemMax) != cudaSuccess)
       return DORA_ERR_CUDA;
@@ -1667,10 +1780,10 @@ extern "C" dora_status dora_norm_factored(const float *W0, const float *A, const
   Layout L;
   if (!plan_layout(out, in, r, sms, &gg, &gn, &L)) return DORA_ERR_SHAPE;
   uint8_t *ws = static_cast<uint8_t *>(workspace);
-  float *a_hi = reinterpret_cast<float *>(ws + L.a_hi);
-  __nv_bfloat16 *a_c = reinterpret_cast<__nv_bfloat16 *>(ws + L.a_c);
-  float *g_hi = reinterpret_cast<float *>(ws + L.g_hi);
-  __nv_bfloat16 *g_c = reinterpret_cast<__nv_bfloat16 *>(ws + L.g_c);
+  __nv_bfloat16 *a_h = reinterpret_cast<__nv_bfloat16 *>(ws + L.a_h);
+  __nv_bfloat16 *a_l = reinterpret_cast<__nv_bfloat16 *>(ws + L.a_l);
+  __nv_bfloat16 *g_h = reinterpret_cast<__nv_bfloat16 *>(ws + L.g_h);
+  __nv_bfloat16 *g_l = reinterpret_cast<__nv_bfloat16 *>(ws + L.g_l);
   float *part_g = reinterpret_cast<float *>(ws + L.part_g);
   float *part_n = reinterpret_cast<float *>(ws + L.part_n);
   const float *Bk = B;
@@ -1681,11 +1794,12 @@ extern "C" dora_status dora_norm_factored(const float *W0, const float *A, const
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   uint64_t launches = 0;
 
-  // 1. N-side split of A; B padded to a TMA-legal row stride when r % 4 != 0
+  // 1. N-side split of A (bf16 h and l); B padded to a TMA-legal row stride
+  //    when r % 4 != 0
   const int in8 = static_cast<int>(dora::round_up(in, 8));
   int *cnt = reinterpret_cast<int *>(ws + L.cnt);
   const int ncnt = static_cast<int>(dora::ceil_div(out, kBM)) * 4;
-  split_n_kernel<<<grid_for(r * in8 / 4, sms), 256, 0, cs>>>(A, r, static_cast<int>(in), in8, a_hi, a_c, cnt, ncnt);
+  split_hl_kernel<<<grid_for(r * in8 / 4, sms), 256, 0, cs>>>(A, r, static_cast<int>(in), in8, a_h, a_l, cnt, ncnt);
   ++launches;
   if (r % 4) {
     const int rp = static_cast<int>(dora::round_up(r, 4));
@@ -1696,19 +1810,16 @@ extern "C" dora_status dora_norm_factored(const float *W0, const float *A, const
     ldb = rp;
   }
 
-  // tensor maps
-  // the N-side boxes of the two passes may differ in height: one map set each
-  CUtensorMap mA, mAh_g, mAc_g, mAh_n, mAc_n, mW0, mB, mGh, mGc;
-  const int nbox = gn.p.nbox;
-  // box rows are one K block: gg.bk / gn.bk fp32 (the same bytes of bf16)
-  const int rbg = 4 * gg.bk, rbn = 4 * gn.bk;
-  bool ok = make_map(&mA, A, false, r, in, in, kBM, rbg) && make_map(&mAh_g, a_hi, false, r, in, in, gg.p.nbox, rbg) &&
-            make_map(&mAc_g, a_c, true, r, 2 * in8, 2 * in8, gg.p.nbox, rbg) &&
-            make_map(&mAh_n, a_hi, false, r, in, in, nbox, rbn) &&
-            make_map(&mAc_n, a_c, true, r, 2 * in8, 2 * in8, nbox, rbn) &&
-            make_map(&mW0, W0, false, out, in, in, kBM, rbn) && make_map(&mB, Bk, false, out, ldb, ldb, kBM, rbn) &&
-            make_map(&mGh, g_hi, false, npad, npad, npad, nbox, rbn) &&
-            make_map(&mGc, g_c, true, npad, 2 * npad, 2 * npad, nbox, rbn);
+  // tensor maps: the raw fp32 M-side boxes are 128 x 32 (128-byte rows), the
+  // bf16 N-side boxes nbox x 32 (64-byte rows); the N-side boxes of the two
+  // passes may differ in height, so one map set each
+  CUtensorMap mA, mAh_g, mAl_g, mAh_n, mAl_n, mW0, mB, mGh, mGl;
+  const int nbg = gg.p.nbox, nbn = gn.p.nbox;
+  bool ok = make_map(&mA, A, false, r, in, in, kBM, 128) &&
+            make_map(&mAh_g, a_h, true, r, in8, in8, nbg, 64) && make_map(&mAl_g, a_l, true, r, in8, in8, nbg, 64) &&
+            make_map(&mAh_n, a_h, true, r, in8, in8, nbn, 64) && make_map(&mAl_n, a_l, true, r, in8, in8, nbn, 64) &&
+            make_map(&mW0, W0, false, out, in, in, kBM, 128) && make_map(&mB, Bk, false, out, ldb, ldb, kBM, 128) &&
+            make_map(&mGh, g_h, true, npad, npad, npad, nbn, 64) && make_map(&mGl, g_l, true, npad, npad, npad, nbn, 64);
   if (!ok) {
     dora::count_launches(launches);
     return DORA_ERR_CUDA;
@@ -1717,7 +1828,7 @@ extern "C" dora_status dora_norm_factored(const float *W0, const float *A, const
   // 2. Gram partial tiles
   gg.p.part = part_g;
   gg.p.err = errp;
-  if (launch_gemm(gg, cs, mA, mA, mAh_g, mAc_g, mAh_g, mAc_g) != cudaSuccess) {
+  if (launch_gemm(gg, cs, mA, mA, mAh_g, mAl_g, mAh_g, mAl_g) != cudaSuccess) {
     dora::count_launches(launches);
     return DORA_ERR_CUDA;
   }
@@ -1727,8 +1838,9 @@ extern "C" dora_status dora_norm_factored(const float *W0, const float *A, const
   StreamK skg{gg.p.units, gg.p.ncl, gg.p.kbtot, gg.p.maxseg};
   {
     const int nsub = (gg.p.NC + 31) / 32;
-    gram_reduce_kernel<<<dim3(static_cast<unsigned>(gg.p.tiles), static_cast<unsigned>(nsub * nsub)), dim3(32, 8), 0,
-                         cs>>>(part_g, skg, gg.p.nchunks, gg.p.NC, static_cast<int>(r), npad, 0.5f * s, g_hi, g_c);
+    gram_reduce_kernel<true><<<dim3(static_cast<unsigned>(gg.p.tiles), static_cast<unsigned>(nsub * nsub)),
+                               dim3(32, 8), 0, cs>>>(part_g, skg, gg.p.nchunks, gg.p.NC, static_cast<int>(r), npad,
+                                                     0.5f * s, g_h, g_l);
   }
   ++launches;
 
@@ -1743,7 +1855,7 @@ extern "C" dora_status dora_norm_factored(const float *W0, const float *A, const
   gn.p.two_s = 2.0f * s;
   gn.p.Bk = Bk;
   gn.p.ldb = static_cast<int>(ldb);
-  if (launch_gemm(gn, cs, mW0, mB, mAh_n, mAc_n, mGh, mGc) != cudaSuccess) {
+  if (launch_gemm(gn, cs, mW0, mB, mAh_n, mAl_n, mGh, mGl) != cudaSuccess) {
     dora::count_launches(launches);
     return DORA_ERR_CUDA;
   }
@@ -1866,7 +1978,7 @@ extern "C" dora_status dora_norm_factored_bwd(const float *W0, const float *A, c
   {
     const StreamK sk{pg.p.units, pg.p.ncl, pg.p.kbtot, pg.p.maxseg};
     const int nsub = (pg.p.NC + 31) / 32;
-    gram_reduce_kernel<<<dim3(static_cast<unsigned>(pg.p.tiles), static_cast<unsigned>(nsub * nsub)), dim3(32, 8), 0,
+    gram_reduce_kernel<false><<<dim3(static_cast<unsigned>(pg.p.tiles), static_cast<unsigned>(nsub * nsub)), dim3(32, 8), 0,
                          cs>>>(part_t, sk, pg.p.nchunks, pg.p.NC, static_cast<int>(r), npad, s, g_hi, g_c);
     ++launches;
   }
@@ -1879,7 +1991,7 @@ extern "C" dora_status dora_norm_factored_bwd(const float *W0, const float *A, c
   {
     const StreamK sk{ph.p.units, ph.p.ncl, ph.p.kbtot, ph.p.maxseg};
     const int nsub = (ph.p.NC + 31) / 32;
-    gram_reduce_kernel<<<dim3(static_cast<unsigned>(ph.p.tiles), static_cast<unsigned>(nsub * nsub)), dim3(32, 8), 0,
+    gram_reduce_kernel<false><<<dim3(static_cast<unsigned>(ph.p.tiles), static_cast<unsigned>(nsub * nsub)), dim3(32, 8), 0,
                          cs>>>(part_t, sk, ph.p.nchunks, ph.p.NC, static_cast<int>(r), npad, s, h_hi, h_c);
     ++launches;
   }

@@ -469,9 +469,8 @@ def run_report(args):
     if args.report == "rank_sweep":
         # out = in = 8192, T = 8192 bf16: norm time, compose GB/s and the norm's
         # whole transient (its workspace) against one dense fp32 out x in matrix
-        for k, r in enumerate(wl.RANK_SWEEP):
-            if args.ranks and r not in args.ranks:
-                continue
+        # the swept ranks, or any ranks given with --ranks (seeded by position)
+        for k, r in enumerate(args.ranks or wl.RANK_SWEEP):
             sh = wl.shape("rank_sweep", r=r)
             W0, A, B, m = _device_module(sh, wl.seed_for("rank_sweep", k), dev)
             gen = torch.Generator(device=dev)
@@ -660,7 +659,8 @@ def main():
     ap.add_argument("--report", choices=["rank_sweep", "mlp_stack", "bf16_norm", "norm_grad", "fused"], default=None,
                     help="extra per-workload report lines instead of the bench line")
     ap.add_argument("--ranks", type=lambda v: [int(x) for x in v.split(",")], default=None,
-                    help="reports rank_sweep / bf16_norm: only these ranks (comma separated)")
+                    help="report rank_sweep: these ranks instead of the sweep; bf16_norm / norm_grad: only "
+                         "these ranks (comma separated)")
     args = ap.parse_args()
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))

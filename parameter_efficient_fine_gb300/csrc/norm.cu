@@ -62,6 +62,8 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
+#include <cmath>
 #include <cstring>
 #include <mutex>
 
@@ -83,7 +85,7 @@ constexpr int kMaxChunkWide = 128;
 constexpr int kThreads = 192;
 constexpr int kMaxChunkN = 384;     // largest N handled by one CTA pass
 constexpr int kMaxR = 1024;
-constexpr int kMaxCtas = 256;       // workspace bound: any device up to this size
+constexpr int kMaxCtas = 160;       // CTAs of a launch at most (GB300 has 152 SMs); bounds the workspace
 constexpr int kMinUnitsNorm = 4;
 constexpr int kMinUnitsGram = 16;
 constexpr int kSmemMax = 232448;           // 227 KB: the opt-in maximum per CTA
@@ -209,18 +211,15 @@ __device__ void wait_drain(uint32_t bar, uint32_t parity) { wait_drain_ns(bar, p
 // loads an unswizzled [BK x 128] box and the converters read it column-wise
 // (lane = M row, conflict-free), the rest is unchanged.
 // ---------------------------------------------------------------------------
-template <int BK, bool XT, bool B3>
+template <int BK, bool XT>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_gemm_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ CUtensorMap mX2,
                const __grid_constant__ CUtensorMap mY1h, const __grid_constant__ CUtensorMap mY1c,
                const __grid_constant__ CUtensorMap mY2h, const __grid_constant__ CUtensorMap mY2c,
                const TcParams p) {
-  static_assert(!B3 || BK == 32, "the bf16 three-product scheme uses 32-wide K blocks");
   constexpr int kRowBytes = BK * 4;   // one swizzle span of the raw fp32 M-side box
-  // one N-side row per operand: BK fp32 (TF32 hi) / BK bf16 pairs (correction)
-  // in the TF32 scheme, BK bf16 (h or l) in the bf16 scheme
-  constexpr int kNRowBytes = B3 ? BK * 2 : BK * 4;
-  constexpr int kSlotCols = B3 ? BK : 2 * BK;   // tensor-memory columns of one M-side operand slot
+  constexpr int kNRowBytes = BK * 4;  // one N-side row: BK TF32 hi / BK bf16 pairs
+  constexpr int kSlotCols = 2 * BK;   // tensor-memory columns of one M-side operand slot
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int S = p.stages;
@@ -301,13 +300,12 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ 
           if (XT) tma_load_2d(xs, seg1 ? &mX1 : &mX2, mt * kBM, kx, fb);
           else tma_load_2d(xs, seg1 ? &mX1 : &mX2, kx, mt * kBM, fb);
           // the N-side tile of the chunk: TF32 hi and bf16 correction operands
-          // (TF32 scheme), or the bf16 h and l operands (bf16 scheme)
           for (int i = 0; i < p.nb; ++i) {
             const int ro = i * p.nbox;
             const int ny = nc * p.NC + ro;
             const uint32_t off = static_cast<uint32_t>(ro * kNRowBytes);
             tma_load_2d(yh + off, seg1 ? &mY1h : &mY2h, kx, ny, fb);
-            tma_load_2d(yc + off, seg1 ? &mY1c : &mY2c, B3 ? kx : 2 * kx, ny, fb);   // bf16 column
+            tma_load_2d(yc + off, seg1 ? &mY1c : &mY2c, 2 * kx, ny, fb);   // bf16 column
           }
           ++issued;
           if (++stage == S) {
@@ -358,32 +356,6 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ 
           tc_fence_after();
           const uint32_t yh = smem_u32(smem + static_cast<size_t>(stage) * p.stage_bytes) + kBM * kRowBytes;
           const uint32_t yc = yh + static_cast<uint32_t>(p.NT) * kNRowBytes;
-          if constexpr (B3) {
-            // M-side operand slot: BK/2 columns of h (two bf16 per column,
-            // K-consecutive), then BK/2 columns of l.  Per K = 16 step three
-            // products h_x h_y + l_x h_y + h_x l_y into the same accumulator.
-            const uint32_t sh = tmem + static_cast<uint32_t>(p.slot0 + stage * kSlotCols);
-            const uint32_t sl = sh + BK / 2;
-#pragma unroll
-            for (int k = 0; k < BK / 16; ++k) {
-              const uint32_t acc0 = (kb != kb0 || k != 0) ? 1u : 0u;
-              const uint32_t ko = static_cast<uint32_t>(k) * 32u;   // 16 bf16 along the 64-byte row
-              const uint32_t ah = sh + 8u * k, al = sl + 8u * k;
-              {
-                const uint64_t bh = sdesc<BK / 2>(yh + ko), bl = sdesc<BK / 2>(yc + ko);
-                mma_bf16_ta(tmem, ah, bh, ic0, acc0);
-                mma_bf16_ta(tmem, al, bh, ic0, 1u);
-                mma_bf16_ta(tmem, ah, bl, ic0, 1u);
-              }
-              if (p.nmma1 > 0) {
-                const uint32_t no = 256u * kNRowBytes;
-                const uint64_t bh = sdesc<BK / 2>(yh + no + ko), bl = sdesc<BK / 2>(yc + no + ko);
-                mma_bf16_ta(tmem + 256u, ah, bh, ic1, acc0);
-                mma_bf16_ta(tmem + 256u, al, bh, ic1, 1u);
-                mma_bf16_ta(tmem + 256u, ah, bl, ic1, 1u);
-              }
-            }
-          } else {
           // M-side operand slot of this stage in tensor memory: BK columns of
           // hi (one fp32 per column), then BK/8 groups of 8 columns holding the
           // group's 16 bf16 correction values (two per column)
@@ -407,7 +379,6 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ 
               mma_bf16_ta(tmem + 256u, ac, bc, ic1, acc0);
               mma_tf32_ta(tmem + 256u, ah, bh, id1, 1u);
             }
-          }
           }
           mma_commit(empty0 + 8u * stage);
           if (++stage == S) {
@@ -475,31 +446,6 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ 
             v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
           }
         };
-        if constexpr (B3) {
-          // x = h + l: h = bf16(x), l = bf16(x - h); per K = 16 step 8 columns
-          // of h pairs and 8 of l pairs (column c holds K indices 2c, 2c + 1)
-#pragma unroll
-          for (int q16 = 0; q16 < BK / 16; ++q16) {
-            uint32_t hb[8], lb[8];
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-              float v[8];
-              load8(2 * q16 + half, v);
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const float x0 = v[2 * e], x1 = v[2 * e + 1];
-                blk = fmaf(x0, x0, blk);
-                blk = fmaf(x1, x1, blk);
-                const uint32_t h = pack_bf16x2(x0, x1);
-                hb[4 * half + e] = h;
-                lb[4 * half + e] =
-                    pack_bf16x2(x0 - __uint_as_float(h << 16), x1 - __uint_as_float(h & 0xffff0000u));
-              }
-            }
-            tmem_st8(slot + 8u * q16, hb);
-            tmem_st8(slot + BK / 2 + 8u * q16, lb);
-          }
-        } else {
 #pragma unroll
         for (int q = 0; q < BK / 8; ++q) {
           float v[8];
@@ -519,7 +465,6 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ 
           }
           tmem_st8(slot + 8u * q, hb);
           tmem_st8(slot + BK + 8u * q, cb);
-        }
         }
         tmem_wait_st();
         if (kb < p.kb1) n0 += blk;
@@ -665,6 +610,641 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ 
 }
 
 // ---------------------------------------------------------------------------
+// the forward norm in one launch, bf16 three-product scheme
+//
+// CTAs are one per SM and all co-resident (cooperative launch).
+//   Gram phase   CTAs 0 .. g-1 only: each upper-triangular tile of G = A A^T
+//                (M side A raw, N side A split) is cut along K into P pieces,
+//                one per CTA, each written as a partial tile;
+//   reduction    the P CTAs of a tile wait for one another's pieces (a
+//                per-tile counter), then each reduces its share of the tile's
+//                32 x 32 blocks of s/2 G: the P pieces of each entry summed in
+//                a fixed order, scaled, split into bf16 h and l, written with
+//                the mirror entry;
+//   norm phase   every CTA: its share of the (M tile, K block) units of
+//                [W0 | B] x [A | s/2 G]^T with the fused per-row epilogue and
+//                n / g finalize.  The split is weighted: the Gram CTAs take
+//                fewer units, so that all CTAs finish together.  A CTA takes
+//                its segments last first, so it reaches an s/2 G tail only
+//                after most of its W0 work; the N-side producer's first tail
+//                load waits for every reduction to be complete (a grid-wide
+//                counter), which by then it always is.
+// The raw M-side boxes have a ring of their own, released by the converter
+// warps as soon as they have split a box into tensor memory; the N-side tiles
+// and the tensor-memory operand slots share a second ring, released by the
+// MMAs.  The rings run on across the two phases, so the producers already
+// fetch the norm phase's W0 while the converter warps reduce G.
+//
+//   warp 0      lane 0: TMA producer of the raw M-side boxes [128 x 32 fp32]
+//   warp 1      allocates tensor memory; lane 0 issues the MMAs
+//   warps 2..5  converters (split into tensor memory, row sums of W0^2), the
+//               epilogues of their 32 tensor-memory lanes, the reduction
+//   warp 6      lane 0: TMA producer of the N-side h and l tiles [NT x 32 bf16]
+// ---------------------------------------------------------------------------
+constexpr int kFwdThreads = 224;
+constexpr int kFwdBK = 32;                       // K indices per K block
+constexpr int kFwdXBytes = kBM * kFwdBK * 4;     // one raw M-side box (128-byte rows)
+constexpr int kFwdNRow = kFwdBK * 2;             // one N-side row of h or l (64 bytes)
+constexpr int kFwdMaxX = 16;
+constexpr int kFwdMaxS = 8;
+constexpr int kGramPieces = 16;                  // CTAs (K pieces) per Gram tile, at most
+
+// one phase's work list and N-side geometry
+struct FwdPhase {
+  int kb1, kbtot;   // K blocks of the first operand pair / in total
+  int nchunks, sym, NC;
+  int nbox, nb;     // N-side rows per TMA box, boxes per tile
+  int nmma0, nmma1; // N of the accumulator's two MMA instructions (nmma1 = 0: one)
+  int tiles;
+  long long units;  // tiles * kbtot
+  int ctas;         // CTAs the units are split over (the first ones of the grid)
+  int P;            // Gram phase: pieces per tile (CTA c < P * tiles takes piece c % P of tile c / P)
+  int g;            // norm phase: the first g CTAs take D units fewer each
+  long long D;
+  int maxseg;
+  float *part;      // Gram: [g][128][NC], the piece of CTA c at c;
+                    // norm: [M tiles][nchunks][maxseg][128] float2
+};
+
+struct FwdParams {
+  FwdPhase ph[2];   // 0: Gram, 1: norm
+  int M;            // out (rows of the norm phase)
+  int r, npad;
+  int NT;           // N-side rows of a stage (the larger phase's)
+  int tmem_cols, slot0;
+  int S;            // N-side stages = tensor-memory operand slots
+  int SX;           // raw M-side box slots
+  unsigned y_bytes; // one N-side stage: the h tile then the l tile
+  int ctas;
+  int *err;
+  int *cnt;         // norm: [M tiles][4] records written so far
+  int *sync;        // [0] converter warps done reducing (4 per Gram CTA), [1 + t] those done with tile t's pieces
+  int nsync;        // 1 + Gram tiles
+  const float *m;
+  float *norm, *g;
+  float two_s, half_s;
+  const float *Bk;
+  int ldb;
+  __nv_bfloat16 *gs_h, *gs_l;   // s/2 G split, [npad, npad] each
+};
+
+// First unit of CTA c when U units are split over C CTAs and the first g of
+// them take D units fewer each (c * (U + g D) / C - min(c, g) D).
+__host__ __device__ __forceinline__ long long wbegin(long long c, long long U, long long C, long long g,
+                                                     long long D) {
+  return c * (U + g * D) / C - (c < g ? c : g) * D;
+}
+// the CTA whose range holds unit u
+__host__ __device__ __forceinline__ int wcta_of(long long u, long long U, int C, long long g, long long D) {
+  const long long W = (U + g * D) / C;   // units of a CTA beyond the first g, about
+  long long c = u < wbegin(g, U, C, g, D) ? (W - D > 0 ? u / (W - D) : 0) : (W > 0 ? (u + g * D) / W : 0);
+  if (c >= C) c = C - 1;
+  if (c < 0) c = 0;
+  while (c + 1 < C && wbegin(c + 1, U, C, g, D) <= u) ++c;
+  while (c > 0 && wbegin(c, U, C, g, D) > u) --c;
+  return static_cast<int>(c);
+}
+
+// The segments of a CTA's unit range [u_begin, hi) are taken last first: the
+// one ending at hi is [max(u_begin, start of its tile), hi).  Returns its
+// start (the next hi) and sets its tile and K-block range.  Taken in this
+// order, a range that starts inside a tile's s/2 G tail reaches that tail
+// last, long after the Gram reduction is complete.
+__device__ __forceinline__ long long seg_range(long long u_begin, long long hi, int kbtot, int *t, int *kb0,
+                                               int *kbe) {
+  *t = static_cast<int>((hi - 1) / kbtot);
+  const long long t0 = static_cast<long long>(*t) * kbtot;
+  const long long lo = u_begin > t0 ? u_begin : t0;
+  *kb0 = static_cast<int>(lo - t0);
+  *kbe = static_cast<int>(hi - t0);
+  return lo;
+}
+
+// This CTA's unit range in a phase: the Gram phase's fixed pieces (a tile's
+// K blocks cut into P equal parts) or the norm phase's weighted split.
+__device__ __forceinline__ void phase_range(const FwdPhase &f, int c, long long *ub, long long *ue) {
+  if (f.P > 0) {
+    *ub = *ue = 0;
+    if (c < f.P * f.tiles) {
+      const int t = c / f.P, q = c - t * f.P;
+      const long long t0 = static_cast<long long>(t) * f.kbtot;
+      *ub = t0 + static_cast<long long>(q) * f.kbtot / f.P;
+      *ue = t0 + static_cast<long long>(q + 1) * f.kbtot / f.P;
+    }
+  } else {
+    *ub = wbegin(c, f.units, f.ctas, f.g, f.D);
+    *ue = wbegin(c + 1, f.units, f.ctas, f.g, f.D);
+  }
+}
+
+// global counter wait (ld.acquire), bounded like the barrier waits
+__device__ __forceinline__ int ld_acquire(const int *p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ bool wait_count(const int *ctr, int target, SharedCtl *ctl, int *err, int code) {
+  if (ld_acquire(ctr) >= target) return true;
+  const unsigned long long t0 = globaltimer();
+  const unsigned long long lim = *reinterpret_cast<volatile unsigned long long *>(&g_wait_limit_ns);
+  for (;;) {
+    __nanosleep(128);
+    if (ld_acquire(ctr) >= target) return true;
+    if (ctl->abort) return false;
+    if (globaltimer() - t0 > lim) {
+      ctl->abort = 1;
+      atomicCAS(err, 0, code);
+      return false;
+    }
+  }
+}
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// s/2 G entry (a, b) split into bf16 h and l
+__device__ __forceinline__ void store_gs3(__nv_bfloat16 *gh, __nv_bfloat16 *gl, int npad, int a, int b, float v) {
+  const __nv_bfloat16 h = __float2bfloat16_rn(v);
+  const long long i = static_cast<long long>(a) * npad + b;
+  gh[i] = h;
+  gl[i] = __float2bfloat16_rn(v - __bfloat162float(h));
+}
+
+__global__ void __launch_bounds__(kFwdThreads, 1)
+fwd_norm_kernel(const __grid_constant__ CUtensorMap mA, const __grid_constant__ CUtensorMap mW0,
+                const __grid_constant__ CUtensorMap mB, const __grid_constant__ CUtensorMap mAh_g,
+                const __grid_constant__ CUtensorMap mAl_g, const __grid_constant__ CUtensorMap mAh_n,
+                const __grid_constant__ CUtensorMap mAl_n, const __grid_constant__ CUtensorMap mGh,
+                const __grid_constant__ CUtensorMap mGl, const FwdParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int S = p.S, SX = p.SX;
+  uint8_t *xring = smem;
+  uint8_t *yring = smem + static_cast<size_t>(SX) * kFwdXBytes;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(yring + static_cast<size_t>(S) * p.y_bytes);
+  // barrier layout: xfull[SX], xempty[SX], yfull[S], sfree[S], tconv[S], accf, acce, fin
+  SharedCtl *ctl = reinterpret_cast<SharedCtl *>(bars + 2 * SX + 3 * S + 3);
+  const uint32_t xfull0 = smem_u32(bars);
+  const uint32_t xempty0 = xfull0 + 8u * SX;
+  const uint32_t yfull0 = xempty0 + 8u * SX;
+  const uint32_t sfree0 = yfull0 + 8u * S;
+  const uint32_t tconv0 = sfree0 + 8u * S;
+  const uint32_t accf = tconv0 + 8u * S;
+  const uint32_t acce = accf + 8;
+  const uint32_t fin = acce + 8;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < SX; ++i) {
+      mbar_init(xfull0 + 8u * i, 1);
+      mbar_init(xempty0 + 8u * i, 4);   // one arrival per converter warp
+    }
+    for (int i = 0; i < S; ++i) {
+      mbar_init(yfull0 + 8u * i, 1);
+      mbar_init(sfree0 + 8u * i, 1);    // the MMAs' commit
+      mbar_init(tconv0 + 8u * i, 4);    // one arrival per converter warp
+    }
+    mbar_init(accf, 1);
+    mbar_init(acce, 4);
+    mbar_init(fin, 1);
+    ctl->abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_map(&mA);
+    prefetch_map(&mW0);
+    prefetch_map(&mB);
+  }
+  if (warp == 6 && lane == 0) {
+    prefetch_map(&mAh_g);
+    prefetch_map(&mAl_g);
+    prefetch_map(&mAh_n);
+    prefetch_map(&mAl_n);
+    prefetch_map(&mGh);
+    prefetch_map(&mGl);
+  }
+  if (warp == 1) {
+    __syncwarp();
+    tmem_alloc(smem_u32(&ctl->tmem_base), static_cast<uint32_t>(p.tmem_cols));
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl->tmem_base;
+  const int cl = static_cast<int>(blockIdx.x);
+
+  if (warp == 0 || warp == 6) {
+    if (lane == 0) {
+      // ------------------------------------------- producers (M side / N side)
+      const bool xside = warp == 0;
+      const int R = xside ? SX : S;
+      const uint32_t full0 = xside ? xfull0 : yfull0;
+      const uint32_t free0 = xside ? xempty0 : sfree0;
+      int slot = 0;
+      uint32_t phase = 0;
+      int issued = 0;
+      bool ok = *reinterpret_cast<volatile int *>(&g_dora_stall) == 0;
+      bool gs_ready = false;
+      for (int ph = 0; ph < 2 && ok; ++ph) {
+        const FwdPhase &f = p.ph[ph];
+        long long u_begin, u_end;
+        phase_range(f, cl, &u_begin, &u_end);
+        // this CTA's segments, last first (see seg_range)
+        for (long long hi = u_end; hi > u_begin && ok;) {
+          int t, kb0, kbe;
+          hi = seg_range(u_begin, hi, f.kbtot, &t, &kb0, &kbe);
+          int mt, nc;
+          tile_coords(t, f.nchunks, f.sym, &mt, &nc);
+          for (int kb = kb0; kb < kbe; ++kb) {
+            const bool seg1 = kb < f.kb1;
+            if (!xside && ph == 1 && !seg1 && !gs_ready) {
+              // the s/2 G tail: written by every CTA's reduction (generic
+              // stores), read here by TMA
+              if (!wait_count(p.sync + 0, 4 * p.ph[0].P * p.ph[0].tiles, ctl, p.err, 10)) {
+                ok = false;
+                break;
+              }
+              fence_proxy_async_global();
+              gs_ready = true;
+            }
+            if (!wait_bounded(free0 + 8u * slot, phase ^ 1u, ctl, p.err, xside ? 1 : 6)) {
+              ok = false;
+              break;
+            }
+            const uint32_t fb = full0 + 8u * slot;
+            const int kx = (seg1 ? kb : kb - f.kb1) * kFwdBK;
+            if (xside) {
+              mbar_expect_tx(fb, kFwdXBytes);
+              const CUtensorMap *mx = ph == 0 ? &mA : (seg1 ? &mW0 : &mB);
+              tma_load_2d(smem_u32(xring + static_cast<size_t>(slot) * kFwdXBytes), mx, kx, mt * kBM, fb);
+            } else {
+              const uint32_t ntile = static_cast<uint32_t>(f.nb * f.nbox) * kFwdNRow;
+              mbar_expect_tx(fb, 2u * ntile);
+              const uint32_t yh = smem_u32(yring + static_cast<size_t>(slot) * p.y_bytes);
+              const uint32_t yl = yh + static_cast<uint32_t>(p.NT) * kFwdNRow;
+              const CUtensorMap *mh = ph == 0 ? &mAh_g : (seg1 ? &mAh_n : &mGh);
+              const CUtensorMap *ml = ph == 0 ? &mAl_g : (seg1 ? &mAl_n : &mGl);
+              for (int i = 0; i < f.nb; ++i) {
+                const int ro = i * f.nbox;
+                const uint32_t off = static_cast<uint32_t>(ro * kFwdNRow);
+                tma_load_2d(yh + off, mh, kx, nc * f.NC + ro, fb);
+                tma_load_2d(yl + off, ml, kx, nc * f.NC + ro, fb);
+              }
+            }
+            ++issued;
+            if (++slot == R) {
+              slot = 0;
+              phase ^= 1u;
+            }
+          }
+        }
+      }
+      if (!ok) {
+        // drain: the last min(issued, R) slots may still have copies in flight
+        int st = slot;
+        uint32_t ph = phase;
+        for (int k = 0; k < R && k < issued; ++k) {
+          if (--st < 0) {
+            st = R - 1;
+            ph ^= 1u;
+          }
+          wait_drain(full0 + 8u * st, ph);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ MMA issuer
+      int ss = 0;
+      uint32_t sph = 0;
+      uint32_t aphase = 0;
+      bool ok = true;
+      for (int ph = 0; ph < 2 && ok; ++ph) {
+        const FwdPhase &f = p.ph[ph];
+        const uint32_t ic0 = idesc_bf16(f.nmma0);
+        const uint32_t ic1 = f.nmma1 > 0 ? idesc_bf16(f.nmma1) : 0u;
+        long long u_begin, u_end;
+        phase_range(f, cl, &u_begin, &u_end);
+        for (long long hi = u_end; hi > u_begin && ok;) {
+          int t, kb0, kbe;
+          hi = seg_range(u_begin, hi, f.kbtot, &t, &kb0, &kbe);
+          if (!wait_bounded(acce, aphase ^ 1u, ctl, p.err, 3)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          for (int kb = kb0; kb < kbe; ++kb) {
+            if (!wait_bounded(tconv0 + 8u * ss, sph, ctl, p.err, 2) ||
+                !wait_bounded(yfull0 + 8u * ss, sph, ctl, p.err, 7)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            // operand slot ss: 16 columns of h pairs, then 16 of l pairs; per
+            // K = 16 step the products h_x h_y + l_x h_y + h_x l_y
+            const uint32_t sh = tmem + static_cast<uint32_t>(p.slot0 + ss * kFwdBK);
+            const uint32_t sl = sh + kFwdBK / 2;
+            const uint32_t yh = smem_u32(yring + static_cast<size_t>(ss) * p.y_bytes);
+            const uint32_t yl = yh + static_cast<uint32_t>(p.NT) * kFwdNRow;
+#pragma unroll
+            for (int k = 0; k < kFwdBK / 16; ++k) {
+              const uint32_t acc0 = (kb != kb0 || k != 0) ? 1u : 0u;
+              const uint32_t ko = static_cast<uint32_t>(k) * 32u;
+              const uint32_t ah = sh + 8u * k, al = sl + 8u * k;
+              {
+                const uint64_t bh = sdesc<kFwdBK / 2>(yh + ko), bl = sdesc<kFwdBK / 2>(yl + ko);
+                mma_bf16_ta(tmem, ah, bh, ic0, acc0);
+                mma_bf16_ta(tmem, al, bh, ic0, 1u);
+                mma_bf16_ta(tmem, ah, bl, ic0, 1u);
+              }
+              if (f.nmma1 > 0) {
+                const uint32_t no = 256u * kFwdNRow;
+                const uint64_t bh = sdesc<kFwdBK / 2>(yh + no + ko), bl = sdesc<kFwdBK / 2>(yl + no + ko);
+                mma_bf16_ta(tmem + 256u, ah, bh, ic1, acc0);
+                mma_bf16_ta(tmem + 256u, al, bh, ic1, 1u);
+                mma_bf16_ta(tmem + 256u, ah, bl, ic1, 1u);
+              }
+            }
+            mma_commit(sfree0 + 8u * ss);
+            if (++ss == S) {
+              ss = 0;
+              sph ^= 1u;
+            }
+          }
+          if (!ok) break;
+          mma_commit(accf);
+          aphase ^= 1u;
+        }
+      }
+      // all issued MMAs must finish before tensor memory is released
+      mma_commit(fin);
+      wait_drain(fin, 0);
+    }
+  } else {
+    // ------------------------------------------- converters, epilogues, reduction
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;
+    const int ct = threadIdx.x - 64;   // 0..127 over the four converter warps
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+    int xs = 0, ss = 0;
+    uint32_t xph = 0, sph = 0;
+    uint32_t aphase = 0;
+    bool ok = true;
+    for (int ph = 0; ph < 2 && ok; ++ph) {
+      const FwdPhase &f = p.ph[ph];
+      const bool norm = ph == 1;
+      long long u_begin, u_end;
+      phase_range(f, cl, &u_begin, &u_end);
+      for (long long hi = u_end; hi > u_begin && ok;) {
+        int t, kb0, kbe;
+        hi = seg_range(u_begin, hi, f.kbtot, &t, &kb0, &kbe);
+        int mt, nc;
+        tile_coords(t, f.nchunks, f.sym, &mt, &nc);
+        const size_t tm = static_cast<size_t>(mt) * f.nchunks + nc;
+        const int kpf = kbe - 8 > kb0 ? kbe - 8 : kb0;   // K block at which B's rows are prefetched
+        float n0 = 0.0f;
+        for (int kb = kb0; kb < kbe; ++kb) {
+          if (norm && kb == kpf && lane == 0) {
+            // the epilogue will read this warp's 32 rows of B: start them
+            // towards L2 a few K blocks before the segment ends
+            const int r0 = mt * kBM + quad * 32;
+            const int nr = min(32, p.M - r0);
+            if (nr > 0)
+              prefetch_l2(p.Bk + static_cast<size_t>(r0) * p.ldb, static_cast<uint32_t>(nr) * p.ldb * 4u);
+          }
+          // the raw box has landed and the operand slot is free (its previous
+          // MMAs are complete); the decision is warp-wide
+          const bool got = wait_bounded(xfull0 + 8u * xs, xph, ctl, p.err, 4) &&
+                           wait_bounded(sfree0 + 8u * ss, sph ^ 1u, ctl, p.err, 8);
+          if (!__all_sync(0xffffffffu, got)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const float4 *xr = reinterpret_cast<const float4 *>(xring + static_cast<size_t>(xs) * kFwdXBytes +
+                                                              row * (kFwdBK * 4));
+          const uint32_t slot = lane_addr + static_cast<uint32_t>(p.slot0 + ss * kFwdBK);
+          float blk = 0.0f;
+#pragma unroll
+          for (int q16 = 0; q16 < kFwdBK / 16; ++q16) {
+            uint32_t hb[8], lb[8];
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+              const int q = 2 * q16 + half;
+              const float4 a = xr[swz_chunk<kFwdBK>(2 * q, row)], b = xr[swz_chunk<kFwdBK>(2 * q + 1, row)];
+              const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const float x0 = v[2 * e], x1 = v[2 * e + 1];
+                blk = fmaf(x0, x0, blk);
+                blk = fmaf(x1, x1, blk);
+                const uint32_t h = pack_bf16x2(x0, x1);
+                hb[4 * half + e] = h;
+                lb[4 * half + e] =
+                    pack_bf16x2(x0 - __uint_as_float(h << 16), x1 - __uint_as_float(h & 0xffff0000u));
+              }
+            }
+            tmem_st8(slot + 8u * q16, hb);
+            tmem_st8(slot + kFwdBK / 2 + 8u * q16, lb);
+          }
+          tmem_wait_st();
+          if (kb < f.kb1) n0 += blk;
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(xempty0 + 8u * xs);   // the raw box is consumed
+            mbar_arrive(tconv0 + 8u * ss);    // the operand slot is written
+          }
+          if (++xs == SX) {
+            xs = 0;
+            xph ^= 1u;
+          }
+          if (++ss == S) {
+            ss = 0;
+            sph ^= 1u;
+          }
+        }
+        if (!ok) break;
+        const int grow = mt * kBM + row;
+        const int seg = norm ? cl - wcta_of(static_cast<long long>(t) * f.kbtot, f.units, f.ctas, f.g, f.D) : 0;
+        // ---- epilogue of this segment
+        const bool got = wait_bounded(accf, aphase, ctl, p.err, 5);
+        if (!__all_sync(0xffffffffu, got)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (norm) {
+          const bool valid = grow < p.M;
+          // <B_i, D_i>: lane i reads row i of B with 128-bit loads, two
+          // 32-column chunks ahead of the tensor-memory chunk it multiplies
+          float dot = 0.0f;
+          const int nchk = (f.NC + 31) >> 5;
+          const int cbase = nc * f.NC;
+          const int ncol = min(f.NC, p.r - cbase);
+          const float *brow = p.Bk + static_cast<size_t>(valid ? grow : 0) * p.ldb + cbase;
+          auto ldb8 = [&](int ci, float4 (&d)[8]) {
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              const int c = 32 * ci + 4 * q;
+              d[q] = (valid && ci < nchk && c < ncol) ? __ldg(reinterpret_cast<const float4 *>(brow + c))
+                                                      : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+          };
+          float4 b0[8], b1[8], b2[8];
+          ldb8(0, b0);
+          ldb8(1, b1);
+          for (int ci = 0; ci < nchk; ++ci) {
+            ldb8(ci + 2, b2);
+            float v[32];
+            tmem_ld32(lane_addr + static_cast<uint32_t>(32 * ci), v);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              dot = fmaf(b0[q].x, v[4 * q], dot);
+              dot = fmaf(b0[q].y, v[4 * q + 1], dot);
+              dot = fmaf(b0[q].z, v[4 * q + 2], dot);
+              dot = fmaf(b0[q].w, v[4 * q + 3], dot);
+            }
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              b0[q] = b1[q];
+              b1[q] = b2[q];
+            }
+          }
+          float2 *part2 = reinterpret_cast<float2 *>(f.part);
+          if (valid) part2[(tm * f.maxseg + seg) * kBM + row] = make_float2(n0, dot);
+          // count this warp's 32 records of the M tile; the warp that writes
+          // the last ones sums all of them (chunks in order, segments in
+          // order) into n_i = sqrt(max(0, sum n0 + 2 s sum dot)), g_i = m_i / n_i
+          __threadfence();
+          __syncwarp();
+          int old = 0;
+          if (lane == 0) old = atomicAdd(p.cnt + mt * 4 + quad, 1);
+          old = __shfl_sync(0xffffffffu, old, 0);
+          int expect = 0;
+          for (int c = 0; c < f.nchunks; ++c) {
+            const long long ub = (static_cast<long long>(mt) * f.nchunks + c) * f.kbtot;
+            expect += wcta_of(ub + f.kbtot - 1, f.units, f.ctas, f.g, f.D) - wcta_of(ub, f.units, f.ctas, f.g, f.D) + 1;
+          }
+          if (old == expect - 1) {
+            __threadfence();
+            if (valid) {
+              float s0 = 0.0f, sd = 0.0f;
+              for (int c = 0; c < f.nchunks; ++c) {
+                const long long ub = (static_cast<long long>(mt) * f.nchunks + c) * f.kbtot;
+                const int nseg =
+                    wcta_of(ub + f.kbtot - 1, f.units, f.ctas, f.g, f.D) - wcta_of(ub, f.units, f.ctas, f.g, f.D) + 1;
+                const size_t tmc = static_cast<size_t>(mt) * f.nchunks + c;
+                for (int j = 0; j < nseg; ++j) {
+                  const float2 v = __ldcg(part2 + (tmc * f.maxseg + j) * kBM + row);
+                  if (c == 0) s0 += v.x;
+                  sd += v.y;
+                }
+              }
+              const float nn = sqrtf(fmaxf(fmaf(p.two_s, sd, s0), 0.0f));
+              p.norm[grow] = nn;
+              p.g[grow] = p.m[grow] / nn;
+            }
+          }
+        } else {
+          // this CTA's Gram piece (rows of G beyond r are zero: the map of A
+          // fills them with zeros)
+          float *dst = f.part + (static_cast<size_t>(cl) * kBM + row) * f.NC;
+          for (int c = 0; c < f.NC; c += 32) {
+            float v[32];
+            tmem_ld32(lane_addr + static_cast<uint32_t>(c), v);
+#pragma unroll
+            for (int j = 0; j < 32; j += 4) {
+              if (c + j < f.NC) *reinterpret_cast<float4 *>(dst + c + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(acce);
+        aphase ^= 1u;
+      }
+      if (ph == 0 && ok && cl < f.P * f.tiles) {
+        // ---- this warp's part of the piece is written; once all P pieces of
+        // the tile are, reduce this CTA's share of its blocks.  Warps signal
+        // and wait on their own (no barrier spans the converter warps), so an
+        // abort in one cannot leave another waiting without a bound.
+        const int tg = cl / f.P, q = cl - tg * f.P;
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) atomicAdd(p.sync + 1 + tg, 1);
+        const bool got = wait_count(p.sync + 1 + tg, 4 * f.P, ctl, p.err, 9);
+        if (!__all_sync(0xffffffffu, got)) {
+          ok = false;
+          break;
+        }
+        __threadfence();
+        // blocks of 32 x 32 entries of tile tg: q, q + P, ...; thread ct takes
+        // column ct % 32 of rows 8 (ct / 32) .. 8 (ct / 32) + 7
+        int gmt, gnc;
+        tile_coords(tg, f.nchunks, 1, &gmt, &gnc);
+        const int nsub = (f.NC + 31) / 32;
+        const int col_l = ct & 31, row_l = (ct >> 5) * 8;
+        const size_t piece = static_cast<size_t>(kBM) * f.NC;
+        for (int sub = q; sub < nsub * nsub; sub += f.P) {
+          const int sr = sub / nsub, sc = sub - sr * nsub;
+          const int cc = sc * 32 + col_l;            // column within the tile
+          const int rr = sr * 32 + row_l;            // first of 8 rows within the tile
+          float acc[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+          if (cc < f.NC) {
+            // the pieces tg * P .. tg * P + P - 1, added in that order; the
+            // loads of eight pieces are issued before any of them is added
+            const float *pj = f.part + (static_cast<size_t>(tg) * f.P * kBM + rr) * f.NC + cc;
+            for (int j0 = 0; j0 < f.P; j0 += 8) {
+              float a[8][8];
+#pragma unroll
+              for (int j = 0; j < 8; ++j)
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                  a[j][i] = (j0 + j < f.P && rr + i < f.NC)
+                                ? __ldcg(pj + (j0 + j) * piece + static_cast<size_t>(i) * f.NC)
+                                : 0.0f;
+#pragma unroll
+              for (int j = 0; j < 8; ++j)
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                  if (j0 + j < f.P) acc[i] += a[j][i];
+            }
+          }
+          const int gc = gnc * f.NC + cc;              // column of G
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int gr = gmt * f.NC + rr + i;        // row of G
+            if (gr >= p.npad || gc >= p.npad || cc >= f.NC || rr + i >= f.NC) continue;
+            const float v = (gr < p.r && gc < p.r) ? p.half_s * acc[i] : 0.0f;
+            store_gs3(p.gs_h, p.gs_l, p.npad, gr, gc, v);
+            if (gmt != gnc) store_gs3(p.gs_h, p.gs_l, p.npad, gc, gr, v);
+          }
+        }
+        // s/2 G is read by the other CTAs' TMA loads (async proxy)
+        __threadfence();
+        fence_proxy_async_global();
+        __syncwarp();
+        if (lane == 0) atomicAdd(p.sync + 0, 1);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) {
+    __syncwarp();
+    tmem_dealloc(tmem, static_cast<uint32_t>(p.tmem_cols));
+  }
+}
+
+// ---------------------------------------------------------------------------
 // elementwise helpers
 // ---------------------------------------------------------------------------
 
@@ -747,24 +1327,14 @@ struct StreamK {
 };
 
 // Gs[k][l] = (s/2) * G[k][l] for k, l < r (zero-padded to npad), split like
-// the N side of the GEMM.  TF32 scheme (split_n_kernel): gh [npad, npad] TF32,
-// gc [npad, 2*npad] bf16 (8 hi, 8 lo per group).  bf16 scheme (split_hl_kernel):
-// gh and gc both bf16 [npad, npad], h = bf16(v) and l = bf16(v - h).
-template <bool B3>
-__device__ __forceinline__ void store_gs(int a, int b, float v, int npad, void *gh, __nv_bfloat16 *gc) {
+// split_n_kernel: gh [npad, npad] TF32, gc [npad, 2*npad] bf16 (8 hi, 8 lo per group)
+__device__ __forceinline__ void store_gs(int a, int b, float v, int npad, float *gh, __nv_bfloat16 *gc) {
   if (a >= npad || b >= npad) return;
-  const long long i = static_cast<long long>(a) * npad + b;
-  if constexpr (B3) {
-    const __nv_bfloat16 h = __float2bfloat16_rn(v);
-    static_cast<__nv_bfloat16 *>(gh)[i] = h;
-    gc[i] = __float2bfloat16_rn(v - __bfloat162float(h));
-  } else {
-    const float h = __uint_as_float(tf32_rna(v));
-    static_cast<float *>(gh)[i] = h;
-    const long long cb = static_cast<long long>(a) * 2 * npad + 16 * (b / 8) + (b % 8);
-    gc[cb] = __float2bfloat16_rn(h);
-    gc[cb + 8] = __float2bfloat16_rn(v - h);
-  }
+  const float h = __uint_as_float(tf32_rna(v));
+  gh[static_cast<long long>(a) * npad + b] = h;
+  const long long cb = static_cast<long long>(a) * 2 * npad + 16 * (b / 8) + (b % 8);
+  gc[cb] = __float2bfloat16_rn(h);
+  gc[cb + 8] = __float2bfloat16_rn(v - h);
 }
 
 // One 32 x 32 block of an upper-triangular Gram tile (blockIdx.x = tile, whose
@@ -774,10 +1344,9 @@ __device__ __forceinline__ void store_gs(int a, int b, float v, int npad, void *
 // the 8 warp sums are then added in warp order.  The block is written at
 // (k, l) and, for a tile off the diagonal, mirrored at (l, k) through shared
 // memory, so both writes are coalesced.
-template <bool B3>
 __global__ void __launch_bounds__(256) gram_reduce_kernel(const float *__restrict__ part, StreamK sk, int nchunks,
                                                           int NC, int r, int npad, float half_s,
-                                                          void *__restrict__ gh, __nv_bfloat16 *__restrict__ gc) {
+                                                          float *__restrict__ gh, __nv_bfloat16 *__restrict__ gc) {
   __shared__ float wsum[8][32][33];
   const int t = blockIdx.x;
   int mt, nc;
@@ -820,7 +1389,7 @@ __global__ void __launch_bounds__(256) gram_reduce_kernel(const float *__restric
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     const int i = ty + 8 * q;
-    store_gs<B3>(mt * kBM + sr * 32 + i, nc * NC + col, v[q], npad, gh, gc);
+    store_gs(mt * kBM + sr * 32 + i, nc * NC + col, v[q], npad, gh, gc);
     wsum[0][i][tx] = v[q];
   }
   if (mt != nc) {
@@ -828,7 +1397,7 @@ __global__ void __launch_bounds__(256) gram_reduce_kernel(const float *__restric
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       const int i = ty + 8 * q;
-      store_gs<B3>(nc * NC + sc * 32 + i, mt * kBM + sr * 32 + tx, wsum[0][tx][i], npad, gh, gc);
+      store_gs(nc * NC + sc * 32 + i, mt * kBM + sr * 32 + tx, wsum[0][tx][i], npad, gh, gc);
     }
   }
 }
@@ -1377,7 +1946,6 @@ struct GemmPlan {
   TcParams p;
   int bk;   // K indices per K block (the kernel instance)
   bool xt;  // M-side operand stored transposed (the kernel instance)
-  bool b3;  // bf16 three-product scheme (else TF32 hi + one bf16 correction)
   size_t smem_bytes;
   size_t part_bytes;
 };
@@ -1396,11 +1964,10 @@ void plan_n(int r, int *npad, int *nchunks, int *NC) {
 }
 
 // K = in (+ r for the norm and row passes); at most max_ctas CTAs
-bool plan_gemm(int mode, int M, int64_t in, int r, int max_ctas, GemmPlan *gp, bool b3 = false) {
+bool plan_gemm(int mode, int M, int64_t in, int r, int max_ctas, GemmPlan *gp) {
   TcParams &p = gp->p;
   std::memset(&p, 0, sizeof(p));
   gp->xt = false;
-  gp->b3 = b3;
   p.mode = mode;
   p.M = M;
   int npad;
@@ -1411,9 +1978,8 @@ bool plan_gemm(int mode, int M, int64_t in, int r, int max_ctas, GemmPlan *gp, b
     p.nchunks = static_cast<int>(dora::ceil_div(npad, p.NC));
     p.sym = 1;
   }
-  gp->bk = (b3 || p.NC <= kMaxChunkWide) ? kBKWide : kBKNarrow;
-  const int row_bytes = gp->bk * 4;                   // raw fp32 M-side box
-  const int nrow_bytes = b3 ? gp->bk * 2 : gp->bk * 4;  // each N-side operand
+  gp->bk = p.NC <= kMaxChunkWide ? kBKWide : kBKNarrow;
+  const int row_bytes = gp->bk * 4;   // the raw fp32 M-side box and each N-side operand
   p.kb1 = static_cast<int>(dora::ceil_div(in, gp->bk));
   p.kbtot = p.kb1 + (mode != kGram ? static_cast<int>(dora::ceil_div(r, gp->bk)) : 0);
   // the N-side tile in nb boxes of nbox rows (a multiple of 8, so every box
@@ -1424,13 +1990,13 @@ bool plan_gemm(int mode, int M, int64_t in, int r, int max_ctas, GemmPlan *gp, b
   p.nmma0 = p.NC <= 256 ? p.NC : 256;
   p.nmma1 = p.NC - p.nmma0;
   // tensor memory: the accumulator (nmma0 columns at 0, nmma1 at 256), then one
-  // M-side operand slot per stage (2 * bk columns: TF32 hi and bf16 pairs; or
-  // bk columns: bf16 h and l pairs)
+  // M-side operand slot of 2 * bk columns (TF32 hi and bf16 pairs) per stage
   const int acc_cols = static_cast<int>(dora::round_up(p.nmma1 > 0 ? 256 + p.nmma1 : p.nmma0, 32));
-  const int slot_cols = b3 ? gp->bk : 2 * gp->bk;
+  const int slot_cols = 2 * gp->bk;
   p.slot0 = acc_cols;
-  // a stage in shared memory: the raw M-side box, then the two N-side tiles
-  p.stage_bytes = static_cast<unsigned>(kBM * row_bytes + 2 * p.NT * nrow_bytes);
+  // a stage in shared memory: the raw M-side box, then the N-side hi and
+  // correction tiles
+  p.stage_bytes = static_cast<unsigned>(kBM * row_bytes + 2 * p.NT * row_bytes);
   p.tx_bytes = p.stage_bytes;
   p.stages = static_cast<int>((kSmemMax - 1024 - 512) / p.stage_bytes);
   if (p.stages > kMaxStages) p.stages = kMaxStages;
@@ -1458,21 +2024,150 @@ bool plan_gemm(int mode, int M, int64_t in, int r, int max_ctas, GemmPlan *gp, b
   return true;
 }
 
+// forward-norm plan: the Gram and norm phases of fwd_norm_kernel
+struct FwdPlan {
+  FwdParams p;
+  size_t smem_bytes;
+  size_t part_g_bytes, part_n_bytes;
+};
+
+// one phase over M rows (Gram: M = r, N = r; norm: M = out, N = r, K tail r)
+void plan_phase(int mode, int M, int64_t in, int r, FwdPhase *f, int *mtiles) {
+  std::memset(f, 0, sizeof(*f));
+  int npad;
+  plan_n(r, &npad, &f->nchunks, &f->NC);
+  if (mode == kGram) {
+    // G = A A^T: square tiles of up to 128 x 128, upper triangle only
+    f->NC = npad < kBM ? npad : kBM;
+    f->nchunks = static_cast<int>(dora::ceil_div(npad, f->NC));
+    f->sym = 1;
+  }
+  f->kb1 = static_cast<int>(dora::ceil_div(in, kFwdBK));
+  f->kbtot = f->kb1 + (mode != kGram ? static_cast<int>(dora::ceil_div(r, kFwdBK)) : 0);
+  f->nb = static_cast<int>(dora::ceil_div(f->NC, 128));
+  f->nbox = static_cast<int>(dora::round_up(dora::ceil_div(f->NC, f->nb), 8));
+  f->nmma0 = f->NC <= 256 ? f->NC : 256;
+  f->nmma1 = f->NC - f->nmma0;
+  *mtiles = static_cast<int>(dora::ceil_div(M, kBM));
+  f->tiles = f->sym ? f->nchunks * (f->nchunks + 1) / 2 : *mtiles * f->nchunks;
+  f->units = static_cast<long long>(f->tiles) * f->kbtot;
+}
+
+bool plan_fwd(int64_t out, int64_t in, int64_t r, int max_ctas, FwdPlan *fp) {
+  FwdParams &p = fp->p;
+  std::memset(&p, 0, sizeof(p));
+  const int ri = static_cast<int>(r);
+  int mt_g, mt_n;
+  plan_phase(kGram, ri, in, ri, &p.ph[0], &mt_g);
+  plan_phase(kNorm, static_cast<int>(out), in, ri, &p.ph[1], &mt_n);
+  FwdPhase &fg = p.ph[0], &fn = p.ph[1];
+  p.M = static_cast<int>(out);
+  p.r = ri;
+  int nch, NCn;
+  plan_n(ri, &p.npad, &nch, &NCn);
+  const int nt_g = fg.nb * fg.nbox, nt_n = fn.nb * fn.nbox;
+  p.NT = nt_g > nt_n ? nt_g : nt_n;
+  const int acc_cols = static_cast<int>(dora::round_up(fn.nmma1 > 0 ? 256 + fn.nmma1 : fn.nmma0, 32));
+  p.slot0 = acc_cols;
+  p.y_bytes = static_cast<unsigned>(p.NT * 2 * kFwdNRow);
+  // shared memory: as many N-side stages as tensor memory and shared memory
+  // allow while leaving at least two more raw-box slots than stages; the rest
+  // goes to raw-box slots
+  const size_t fixed = 1024 + 8 * (2 * kFwdMaxX + 3 * kFwdMaxS + 3) + 64;
+  const size_t budget = kSmemMax - fixed;
+  int S = (512 - acc_cols) / kFwdBK;
+  if (S > kFwdMaxS) S = kFwdMaxS;
+  while (S >= 2 && static_cast<size_t>(S) * p.y_bytes + static_cast<size_t>(S + 2) * kFwdXBytes > budget) --S;
+  if (S < 2) return false;
+  int SX = static_cast<int>((budget - static_cast<size_t>(S) * p.y_bytes) / kFwdXBytes);
+  if (SX > kFwdMaxX) SX = kFwdMaxX;
+  p.S = S;
+  p.SX = SX;
+  int cols = 32;
+  while (cols < acc_cols + S * kFwdBK) cols *= 2;
+  p.tmem_cols = cols;
+  // one CTA per SM, all co-resident: at most max_ctas, at least ... one unit
+  // each of the norm phase
+  // CTAs: at least four norm units each, at least one per Gram tile (there
+  // are never more Gram tiles than norm units), at most one per norm unit
+  long long ctas = dora::ceil_div(fn.units, kMinUnitsNorm);
+  if (ctas < fg.tiles) ctas = fg.tiles;
+  if (ctas > max_ctas) ctas = max_ctas;
+  if (ctas > fn.units) ctas = fn.units;
+  if (ctas < 1) ctas = 1;
+  p.ctas = static_cast<int>(ctas);
+  // Cost model measured on GB300: a Gram unit about 0.6 us (latency-bound),
+  // a norm unit 0.1 us + 3 N tensor cycles at 1.6 GHz and no less than
+  // 0.5 us, a group of reduction loads 1.5 us.
+  const double t_norm = std::max(0.5, 0.1 + 3.0 * fn.NC / 1600.0);
+  // Gram phase: P pieces per tile, one CTA each (the first P * tiles CTAs):
+  // about a third of the grid, and enough pieces that the Gram phase takes
+  // at most ~35% of a CTA's norm work (s/2 G is needed only after most of it)
+  const double t_share = static_cast<double>(fn.units) / p.ctas * t_norm;
+  int P = p.ctas / (3 * fg.tiles);
+  const int need = static_cast<int>(std::ceil(fg.kbtot * 0.6 / (0.35 * t_share)));
+  if (P < need) P = need;
+  if (P > kGramPieces) P = kGramPieces;
+  if (P > fg.kbtot) P = fg.kbtot;
+  if (P * fg.tiles > p.ctas) P = p.ctas / fg.tiles;
+  if (P < 1) return false;   // more Gram tiles than CTAs (not for r <= kMaxR)
+  fg.P = P;
+  fg.ctas = P * fg.tiles;
+  // norm phase: the Gram CTAs take D units fewer, D = their Gram phase and
+  // reduction in norm units
+  fn.ctas = p.ctas;
+  fn.g = fg.ctas;
+  const int nsub = (fg.NC + 31) / 32;
+  const double t_red = 1.5 * ((nsub * nsub + P - 1) / P) * ((P + 7) / 8);
+  long long D = std::llround((static_cast<double>(fg.kbtot) / P * 0.6 + t_red + 2.0) / t_norm);
+  const long long dmax = fn.units / p.ctas / 2;
+  fn.D = D < dmax ? D : dmax;
+  // fewest units of a CTA in the norm phase, for the segment bound
+  const long long per = (fn.units + fn.g * fn.D) / p.ctas - fn.D - 1;
+  fn.maxseg = per >= 1 ? static_cast<int>((fn.kbtot - 1) / per + 2) : fn.kbtot + 1;
+  fg.maxseg = 1;
+  p.nsync = 1 + fg.tiles;
+  fp->part_g_bytes = static_cast<size_t>(fg.ctas) * kBM * fg.NC * sizeof(float);
+  fp->part_n_bytes = static_cast<size_t>(mt_n) * fn.nchunks * fn.maxseg * kBM * 2 * sizeof(float);
+  fp->smem_bytes = static_cast<size_t>(SX) * kFwdXBytes + static_cast<size_t>(S) * p.y_bytes + 1024 +
+                   8 * (2 * SX + 3 * S + 3) + 64;
+  if (p.tmem_cols > 256 && fp->smem_bytes < 116 * 1024) fp->smem_bytes = 116 * 1024;
+  return true;
+}
+
+cudaError_t launch_fwd(const FwdPlan &fp, cudaStream_t cs, const CUtensorMap &mA, const CUtensorMap &mW0,
+                       const CUtensorMap &mB, const CUtensorMap &mAh_g, const CUtensorMap &mAl_g,
+                       const CUtensorMap &mAh_n, const CUtensorMap &mAl_n, const CUtensorMap &mGh,
+                       const CUtensorMap &mGl) {
+  // CTAs wait on one another (grid-wide counters): a cooperative launch makes
+  // them co-resident or fails
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(fp.p.ctas));
+  cfg.blockDim = dim3(kFwdThreads);
+  cfg.dynamicSmemBytes = fp.smem_bytes;
+  cfg.stream = cs;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, fwd_norm_kernel, mA, mW0, mB, mAh_g, mAl_g, mAh_n, mAl_n, mGh, mGl, fp.p);
+}
+
 // forward-norm workspace (bf16 three-product scheme): the N-side split of A
 // (a_h, a_l: bf16 [r, in8]) and of s/2 G (g_h, g_l: bf16 [npad, npad]), the
 // Gram and norm partials, B padded to a 16-byte row when r % 4 != 0, and the
-// completion counters of the fused n / g finalize
+// counters: the fused n / g finalize's [M tiles][4], then the two grid-wide
+// phase counters
 struct Layout {
   size_t a_h, a_l, g_h, g_l, part_g, part_n, b_pad, cnt, total;
 };
 
 size_t al256(size_t x) { return (x + 255) & ~size_t(255); }
 
-// sms: CTAs available to each pass
-bool plan_layout(int64_t out, int64_t in, int64_t r, int sms, GemmPlan *gg,
-                 GemmPlan *gn, Layout *L) {
-  if (!plan_gemm(kGram, static_cast<int>(r), in, static_cast<int>(r), sms, gg, true)) return false;
-  if (!plan_gemm(kNorm, static_cast<int>(out), in, static_cast<int>(r), sms, gn, true)) return false;
+// sms: CTAs available
+bool plan_layout(int64_t out, int64_t in, int64_t r, int sms, FwdPlan *fp, Layout *L) {
+  if (!plan_fwd(out, in, r, sms, fp)) return false;
   int npad, nchunks, NC;
   plan_n(static_cast<int>(r), &npad, &nchunks, &NC);
   size_t off = 0;
@@ -1486,10 +2181,10 @@ bool plan_layout(int64_t out, int64_t in, int64_t r, int sms, GemmPlan *gg,
   L->a_l = take(static_cast<size_t>(r) * in8 * 2);
   L->g_h = take(static_cast<size_t>(npad) * npad * 2);
   L->g_l = take(static_cast<size_t>(npad) * npad * 2);
-  L->part_g = take(gg->part_bytes);
-  L->part_n = take(gn->part_bytes);
+  L->part_g = take(fp->part_g_bytes);
+  L->part_n = take(fp->part_n_bytes);
   L->b_pad = (r % 4) ? take(static_cast<size_t>(out) * dora::round_up(r, 4) * 4) : 0;
-  L->cnt = take(static_cast<size_t>(dora::ceil_div(out, kBM)) * 4 * sizeof(int));
+  L->cnt = take((static_cast<size_t>(dora::ceil_div(out, kBM)) * 4 + fp->p.nsync) * sizeof(int));
   L->total = off;
   return true;
 }
@@ -1556,20 +2251,15 @@ cudaError_t launch_gemm(const GemmPlan &gp, cudaStream_t cs, const CUtensorMap &
                         const CUtensorMap &y1h, const CUtensorMap &y1c, const CUtensorMap &y2h,
                         const CUtensorMap &y2c) {
   const dim3 grid(static_cast<unsigned>(gp.p.ctas)), block(kThreads);
-  if (gp.b3) {
-    if (gp.xt)
-      tc_gemm_kernel<kBKWide, true, true><<<grid, block, gp.smem_bytes, cs>>>(x1, x2, y1h, y1c, y2h, y2c, gp.p);
-    else
-      tc_gemm_kernel<kBKWide, false, true><<<grid, block, gp.smem_bytes, cs>>>(x1, x2, y1h, y1c, y2h, y2c, gp.p);
-  } else if (gp.xt) {
+  if (gp.xt) {
     if (gp.bk == kBKWide)
-      tc_gemm_kernel<kBKWide, true, false><<<grid, block, gp.smem_bytes, cs>>>(x1, x2, y1h, y1c, y2h, y2c, gp.p);
+      tc_gemm_kernel<kBKWide, true><<<grid, block, gp.smem_bytes, cs>>>(x1, x2, y1h, y1c, y2h, y2c, gp.p);
     else
-      tc_gemm_kernel<kBKNarrow, true, false><<<grid, block, gp.smem_bytes, cs>>>(x1, x2, y1h, y1c, y2h, y2c, gp.p);
+      tc_gemm_kernel<kBKNarrow, true><<<grid, block, gp.smem_bytes, cs>>>(x1, x2, y1h, y1c, y2h, y2c, gp.p);
   } else if (gp.bk == kBKWide) {
-    tc_gemm_kernel<kBKWide, false, false><<<grid, block, gp.smem_bytes, cs>>>(x1, x2, y1h, y1c, y2h, y2c, gp.p);
+    tc_gemm_kernel<kBKWide, false><<<grid, block, gp.smem_bytes, cs>>>(x1, x2, y1h, y1c, y2h, y2c, gp.p);
   } else {
-    tc_gemm_kernel<kBKNarrow, false, false><<<grid, block, gp.smem_bytes, cs>>>(x1, x2, y1h, y1c, y2h, y2c, gp.p);
+    tc_gemm_kernel<kBKNarrow, false><<<grid, block, gp.smem_bytes, cs>>>(x1, x2, y1h, y1c, y2h, y2c, gp.p);
   }
   return cudaGetLastError();
 }
@@ -1690,12 +2380,11 @@ dora_status device_init(int device, int **errp) {
     void *ptr = nullptr;
     if (cudaGetSymbolAddress(&ptr, g_dora_err) != cudaSuccess) return DORA_ERR_CUDA;
     const cudaFuncAttribute a = cudaFuncAttributeMaxDynamicSharedMemorySize;
-    if (cudaFuncSetAttribute(tc_gemm_kernel<kBKNarrow, false, false>, a, kSmemMax) != cudaSuccess ||
-        cudaFuncSetAttribute(tc_gemm_kernel<kBKWide, false, false>, a, kSmemMax) != cudaSuccess ||
-        cudaFuncSetAttribute(tc_gemm_kernel<kBKNarrow, true, false>, a, kSmemMax) != cudaSuccess ||
-        cudaFuncSetAttribute(tc_gemm_kernel<kBKWide, true, false>, a, kSmemMax) != cudaSuccess ||
-        cudaFuncSetAttribute(tc_gemm_kernel<kBKWide, false, true>, a, kSmemMax) != cudaSuccess ||
-        cudaFuncSetAttribute(tc_gemm_kernel<kBKWide, true, true>, a, kSmemMax) != cudaSuccess ||
+    if (cudaFuncSetAttribute(tc_gemm_kernel<kBKNarrow, false>, a, kSmemMax) != cudaSuccess ||
+        cudaFuncSetAttribute(tc_gemm_kernel<kBKWide, false>, a, kSmemMax) != cudaSuccess ||
+        cudaFuncSetAttribute(tc_gemm_kernel<kBKNarrow, true>, a, kSmemMax) != cudaSuccess ||
+        cudaFuncSetAttribute(tc_gemm_kernel<kBKWide, true>, a, kSmemMax) != cudaSuccess ||
+        cudaFuncSetAttribute(fwd_norm_kernel, a, kSmemMax) != cudaSuccess ||
         cudaFuncSetAttribute(tc16_kernel<32>, a, kSmemMax) != cudaSuccess ||
         cudaFuncSetAttribute(tc16_kernel<64>, a, kSmemMax) != cudaSuccess)
       return DORA_ERR_CUDA;
@@ -1725,9 +2414,9 @@ extern "C" size_t dora_norm_factored_workspace(int64_t out, int64_t in, int64_t 
   if (!shape_ok(out, in, r)) return 0;
   // the layout for kMaxCtas CTAs: the partial-result space only grows with
   // the CTA count, so this bounds every device with up to kMaxCtas SMs
-  GemmPlan gg, gn;
+  FwdPlan fp;
   Layout L;
-  if (!plan_layout(out > 0 ? out : 1, in, r, kMaxCtas, &gg, &gn, &L)) return 0;
+  if (!plan_layout(out > 0 ? out : 1, in, r, kMaxCtas, &fp, &L)) return 0;
   return L.total;
 }
 
@@ -1776,30 +2465,25 @@ extern "C" dora_status dora_norm_factored(const float *W0, const float *A, const
   st = device_init(device, &errp);
   if (st != DORA_OK) return st;
 
-  GemmPlan gg, gn;
+  FwdPlan fp;
   Layout L;
-  if (!plan_layout(out, in, r, sms, &gg, &gn, &L)) return DORA_ERR_SHAPE;
+  if (!plan_layout(out, in, r, sms, &fp, &L)) return DORA_ERR_SHAPE;
   uint8_t *ws = static_cast<uint8_t *>(workspace);
   __nv_bfloat16 *a_h = reinterpret_cast<__nv_bfloat16 *>(ws + L.a_h);
   __nv_bfloat16 *a_l = reinterpret_cast<__nv_bfloat16 *>(ws + L.a_l);
-  __nv_bfloat16 *g_h = reinterpret_cast<__nv_bfloat16 *>(ws + L.g_h);
-  __nv_bfloat16 *g_l = reinterpret_cast<__nv_bfloat16 *>(ws + L.g_l);
-  float *part_g = reinterpret_cast<float *>(ws + L.part_g);
-  float *part_n = reinterpret_cast<float *>(ws + L.part_n);
   const float *Bk = B;
   int64_t ldb = r;
-  int npad, nchunks, NC;
-  plan_n(static_cast<int>(r), &npad, &nchunks, &NC);
-
+  const int npad = fp.p.npad;
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   uint64_t launches = 0;
 
-  // 1. N-side split of A (bf16 h and l); B padded to a TMA-legal row stride
-  //    when r % 4 != 0
+  // 1. N-side split of A (bf16 h and l) and zero counters; B padded to a
+  //    TMA-legal row stride when r % 4 != 0
   const int in8 = static_cast<int>(dora::round_up(in, 8));
   int *cnt = reinterpret_cast<int *>(ws + L.cnt);
   const int ncnt = static_cast<int>(dora::ceil_div(out, kBM)) * 4;
-  split_hl_kernel<<<grid_for(r * in8 / 4, sms), 256, 0, cs>>>(A, r, static_cast<int>(in), in8, a_h, a_l, cnt, ncnt);
+  split_hl_kernel<<<grid_for(r * in8 / 4, sms), 256, 0, cs>>>(A, r, static_cast<int>(in), in8, a_h, a_l, cnt,
+                                                               ncnt + fp.p.nsync);
   ++launches;
   if (r % 4) {
     const int rp = static_cast<int>(dora::round_up(r, 4));
@@ -1812,50 +2496,39 @@ extern "C" dora_status dora_norm_factored(const float *W0, const float *A, const
 
   // tensor maps: the raw fp32 M-side boxes are 128 x 32 (128-byte rows), the
   // bf16 N-side boxes nbox x 32 (64-byte rows); the N-side boxes of the two
-  // passes may differ in height, so one map set each
+  // phases may differ in height, so one map set each
+  FwdParams &p = fp.p;
+  p.ph[0].part = reinterpret_cast<float *>(ws + L.part_g);
+  p.ph[1].part = reinterpret_cast<float *>(ws + L.part_n);
+  p.err = errp;
+  p.cnt = cnt;
+  p.sync = cnt + ncnt;
+  p.m = m;
+  p.norm = norm;
+  p.g = g;
+  p.two_s = 2.0f * s;
+  p.half_s = 0.5f * s;
+  p.Bk = Bk;
+  p.ldb = static_cast<int>(ldb);
+  p.gs_h = reinterpret_cast<__nv_bfloat16 *>(ws + L.g_h);
+  p.gs_l = reinterpret_cast<__nv_bfloat16 *>(ws + L.g_l);
   CUtensorMap mA, mAh_g, mAl_g, mAh_n, mAl_n, mW0, mB, mGh, mGl;
-  const int nbg = gg.p.nbox, nbn = gn.p.nbox;
+  const int nbg = p.ph[0].nbox, nbn = p.ph[1].nbox;
   bool ok = make_map(&mA, A, false, r, in, in, kBM, 128) &&
             make_map(&mAh_g, a_h, true, r, in8, in8, nbg, 64) && make_map(&mAl_g, a_l, true, r, in8, in8, nbg, 64) &&
             make_map(&mAh_n, a_h, true, r, in8, in8, nbn, 64) && make_map(&mAl_n, a_l, true, r, in8, in8, nbn, 64) &&
             make_map(&mW0, W0, false, out, in, in, kBM, 128) && make_map(&mB, Bk, false, out, ldb, ldb, kBM, 128) &&
-            make_map(&mGh, g_h, true, npad, npad, npad, nbn, 64) && make_map(&mGl, g_l, true, npad, npad, npad, nbn, 64);
+            make_map(&mGh, p.gs_h, true, npad, npad, npad, nbn, 64) &&
+            make_map(&mGl, p.gs_l, true, npad, npad, npad, nbn, 64);
   if (!ok) {
     dora::count_launches(launches);
     return DORA_ERR_CUDA;
   }
 
-  // 2. Gram partial tiles
-  gg.p.part = part_g;
-  gg.p.err = errp;
-  if (launch_gemm(gg, cs, mA, mA, mAh_g, mAl_g, mAh_g, mAl_g) != cudaSuccess) {
-    dora::count_launches(launches);
-    return DORA_ERR_CUDA;
-  }
-  ++launches;
-
-  // 3. Gs = (s/2) G, split like A
-  StreamK skg{gg.p.units, gg.p.ncl, gg.p.kbtot, gg.p.maxseg};
-  {
-    const int nsub = (gg.p.NC + 31) / 32;
-    gram_reduce_kernel<true><<<dim3(static_cast<unsigned>(gg.p.tiles), static_cast<unsigned>(nsub * nsub)),
-                               dim3(32, 8), 0, cs>>>(part_g, skg, gg.p.nchunks, gg.p.NC, static_cast<int>(r), npad,
-                                                     0.5f * s, g_h, g_l);
-  }
-  ++launches;
-
-  // 4. [W0 | B] x [A | Gs]^T with per-segment row reductions; the last
+  // 2. one launch: Gram partials, the reduction into s/2 G (split), and
+  //    [W0 | B] x [A | s/2 G]^T with per-segment row reductions; the last
   //    epilogue warp of each quarter M tile writes n and g
-  gn.p.part = part_n;
-  gn.p.err = errp;
-  gn.p.cnt = cnt;
-  gn.p.m = m;
-  gn.p.norm = norm;
-  gn.p.g = g;
-  gn.p.two_s = 2.0f * s;
-  gn.p.Bk = Bk;
-  gn.p.ldb = static_cast<int>(ldb);
-  if (launch_gemm(gn, cs, mW0, mB, mAh_n, mAl_n, mGh, mGl) != cudaSuccess) {
+  if (launch_fwd(fp, cs, mA, mW0, mB, mAh_g, mAl_g, mAh_n, mAl_n, mGh, mGl) != cudaSuccess) {
     dora::count_launches(launches);
     return DORA_ERR_CUDA;
   }
@@ -1978,7 +2651,7 @@ extern "C" dora_status dora_norm_factored_bwd(const float *W0, const float *A, c
   {
     const StreamK sk{pg.p.units, pg.p.ncl, pg.p.kbtot, pg.p.maxseg};
     const int nsub = (pg.p.NC + 31) / 32;
-    gram_reduce_kernel<false><<<dim3(static_cast<unsigned>(pg.p.tiles), static_cast<unsigned>(nsub * nsub)), dim3(32, 8), 0,
+    gram_reduce_kernel<<<dim3(static_cast<unsigned>(pg.p.tiles), static_cast<unsigned>(nsub * nsub)), dim3(32, 8), 0,
                          cs>>>(part_t, sk, pg.p.nchunks, pg.p.NC, static_cast<int>(r), npad, s, g_hi, g_c);
     ++launches;
   }
@@ -1991,7 +2664,7 @@ extern "C" dora_status dora_norm_factored_bwd(const float *W0, const float *A, c
   {
     const StreamK sk{ph.p.units, ph.p.ncl, ph.p.kbtot, ph.p.maxseg};
     const int nsub = (ph.p.NC + 31) / 32;
-    gram_reduce_kernel<false><<<dim3(static_cast<unsigned>(ph.p.tiles), static_cast<unsigned>(nsub * nsub)), dim3(32, 8), 0,
+    gram_reduce_kernel<<<dim3(static_cast<unsigned>(ph.p.tiles), static_cast<unsigned>(nsub * nsub)), dim3(32, 8), 0,
                          cs>>>(part_t, sk, ph.p.nchunks, ph.p.NC, static_cast<int>(r), npad, s, h_hi, h_c);
     ++launches;
   }

@@ -98,8 +98,10 @@ constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
 constexpr int kChainK = 1024;
 
 // kGram: partial tiles of a symmetric product (upper triangle only);
-// kNorm: per-row <B_i, D_i> records and the fused n / g finalize;
+// kNorm: per-row <B_i, D_i> records and the fused n / g finalize (the forward
+//        norm kernels: fwd_norm_kernel, tc16_kernel);
 // kRows: partial rows of a plain product per CTA part, summed by rows_reduce_kernel
+//        (tc_gemm_kernel, with kGram, for the gradient through the norm)
 enum Mode : int { kGram = 0, kNorm = 1, kRows = 2 };
 
 // device error word: 0 = fine; otherwise the code of the wait that gave up
@@ -131,16 +133,9 @@ struct TcParams {
   int maxseg;
   unsigned stage_bytes;
   unsigned tx_bytes;
-  float *part;      // GRAM: [tiles][maxseg][128][NC]; NORM: [tiles][maxseg][128][2]
+  float *part;      // GRAM: [tiles][maxseg][128][NC]; ROWS: [tiles][maxseg][NC / 4][128] float4
   int r;
   int *err;
-  // NORM: the epilogue warp that completes a quarter of an M tile finalises it
-  int *cnt;         // [M tiles][4] records written so far (zeroed before the launch)
-  const float *m;
-  float *norm, *g;
-  float two_s;
-  const float *Bk;  // B (or its padded copy) [M, ldb]: the epilogue prefetches its rows into L2
-  int ldb;
   // ROWS: K blocks per accumulation window (the tensor-memory accumulator
   // restarts at every window boundary of the tile's K range, and each window
   // is added in fp32 round-to-nearest into the CTA's partial rows)
@@ -411,14 +406,6 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ 
       int mt, nc;
       tile_coords(t, p.nchunks, p.sym, &mt, &nc);
       const size_t tm = static_cast<size_t>(mt) * p.nchunks + nc;   // (M tile, N chunk) of this CTA's partials
-      float n0 = 0.0f;  // sum of W0_i^2 over this segment's K range
-      if (p.mode == kNorm && lane == 0) {
-        // the epilogue will read this warp's 32 rows of B: start them towards L2 now
-        const int r0 = mt * kBM + quad * 32;
-        const int nr = min(32, p.M - r0);
-        if (nr > 0)
-          prefetch_l2(p.Bk + static_cast<size_t>(r0) * p.ldb, static_cast<uint32_t>(nr) * p.ldb * 4u);
-      }
       for (int kb = kb0; kb < kbe; ++kb) {
         // every lane waits; the decision to go on is taken warp-wide so that
         // the warp stays converged for the tcgen05.ld of the epilogue
@@ -435,7 +422,6 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ 
         const float4 *xr = reinterpret_cast<const float4 *>(xbox + row * kRowBytes);
         const float *xc = reinterpret_cast<const float *>(xbox) + row;   // XT: column `row` of [BK][128]
         const uint32_t slot = lane_addr + static_cast<uint32_t>(p.slot0 + stage * kSlotCols);
-        float blk = 0.0f;
         auto load8 = [&](int q, float (&v)[8]) {
           if (XT) {
 #pragma unroll
@@ -456,7 +442,6 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ 
           for (int e = 0; e < 8; ++e) {
             hb[e] = tf32_rna(v[e]);
             l[e] = v[e] - __uint_as_float(hb[e]);
-            blk = fmaf(v[e], v[e], blk);
           }
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
@@ -467,7 +452,6 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ 
           tmem_st8(slot + BK + 8u * q, cb);
         }
         tmem_wait_st();
-        if (kb < p.kb1) n0 += blk;
         // the tensor-memory stores are complete (wait::st); order them before
         // the MMA lane's work, then one arrival per warp
         tc_fence_before();
@@ -489,74 +473,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ 
         break;
       }
       tc_fence_after();
-      if (p.mode == kNorm) {
-        // <B_i, D_i>: lane i reads row i of B with 128-bit loads (the rows
-        // were prefetched into L2 at the segment's start), one 32-column
-        // chunk ahead of the tensor-memory chunk it multiplies
-        float dot = 0.0f;
-        const int nchk = (p.NC + 31) >> 5;
-        const int cbase = nc * p.NC;
-        const int ncol = min(p.NC, p.r - cbase);   // B columns of this N chunk (zero padding beyond)
-        const float *brow = p.Bk + static_cast<size_t>(valid ? grow : 0) * p.ldb + cbase;
-        float4 cur[8], nxt[8];
-#pragma unroll
-        for (int q = 0; q < 8; ++q)
-          cur[q] = (valid && 4 * q < ncol) ? __ldg(reinterpret_cast<const float4 *>(brow + 4 * q))
-                                           : make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int ci = 0; ci < nchk; ++ci) {
-#pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            const int c = 32 * (ci + 1) + 4 * q;
-            nxt[q] = (valid && ci + 1 < nchk && c < ncol) ? __ldg(reinterpret_cast<const float4 *>(brow + c))
-                                                        : make_float4(0.f, 0.f, 0.f, 0.f);
-          }
-          float v[32];
-          tmem_ld32(lane_addr + static_cast<uint32_t>(32 * ci), v);
-#pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            dot = fmaf(cur[q].x, v[4 * q], dot);
-            dot = fmaf(cur[q].y, v[4 * q + 1], dot);
-            dot = fmaf(cur[q].z, v[4 * q + 2], dot);
-            dot = fmaf(cur[q].w, v[4 * q + 3], dot);
-          }
-#pragma unroll
-          for (int q = 0; q < 8; ++q) cur[q] = nxt[q];
-        }
-        float2 *part2 = reinterpret_cast<float2 *>(p.part);
-        if (valid) part2[(tm * p.maxseg + seg) * kBM + row] = make_float2(n0, dot);
-        // count this warp's 32 records of the M tile; the warp that writes the
-        // last ones sums all of them (chunks in order, segments in order) into
-        // n_i = sqrt(max(0, sum n0 + 2 s sum dot)) and g_i = m_i / n_i
-        __threadfence();
-        __syncwarp();
-        int old = 0;
-        if (lane == 0) old = atomicAdd(p.cnt + mt * 4 + quad, 1);
-        old = __shfl_sync(0xffffffffu, old, 0);
-        int expect = 0;
-        for (int c = 0; c < p.nchunks; ++c) {
-          const long long ub = (static_cast<long long>(mt) * p.nchunks + c) * p.kbtot;
-          expect += cta_of(ub + p.kbtot - 1, p.units, p.ncl) - cta_of(ub, p.units, p.ncl) + 1;
-        }
-        if (old == expect - 1) {
-          __threadfence();
-          if (valid) {
-            float s0 = 0.0f, sd = 0.0f;
-            for (int c = 0; c < p.nchunks; ++c) {
-              const long long ub = (static_cast<long long>(mt) * p.nchunks + c) * p.kbtot;
-              const int nseg = cta_of(ub + p.kbtot - 1, p.units, p.ncl) - cta_of(ub, p.units, p.ncl) + 1;
-              const size_t tmc = static_cast<size_t>(mt) * p.nchunks + c;
-              for (int j = 0; j < nseg; ++j) {
-                const float2 v = __ldcg(part2 + (tmc * p.maxseg + j) * kBM + row);
-                if (c == 0) s0 += v.x;
-                sd += v.y;
-              }
-            }
-            const float nn = sqrtf(fmaxf(fmaf(p.two_s, sd, s0), 0.0f));
-            p.norm[grow] = nn;
-            p.g[grow] = p.m[grow] / nn;
-          }
-        }
-      } else if (p.mode == kGram) {
+      if (p.mode == kGram) {
         float *dst = p.part + ((tm * p.maxseg + seg) * kBM + row) * p.NC;
         for (int c = 0; c < p.NC; c += 32) {
           float v[32];
@@ -659,11 +576,10 @@ struct FwdPhase {
   long long units;  // tiles * kbtot
   int ctas;         // CTAs the units are split over (the first ones of the grid)
   int P;            // Gram phase: pieces per tile (CTA c < P * tiles takes piece c % P of tile c / P)
-  int g;            // norm phase: the first g CTAs take D units fewer each
-  long long D;
-  int maxseg;
   float *part;      // Gram: [g][128][NC], the piece of CTA c at c;
-                    // norm: [M tiles][nchunks][maxseg][128] float2
+                    // norm: [tiles + ctas][128] float2, the records of tile t
+                    // from CTA c at t + c (CTAs touch tiles in ascending
+                    // order, so t + c is unique)
 };
 
 struct FwdParams {
@@ -686,23 +602,20 @@ struct FwdParams {
   const float *Bk;
   int ldb;
   __nv_bfloat16 *gs_h, *gs_l;   // s/2 G split, [npad, npad] each
+  int stage_b;      // the last epilogue stages B's rows through the operand rings (they are large enough)
+  long long ub[kMaxCtas + 1];   // norm phase: CTA c takes units [ub[c], ub[c + 1]) (none empty)
 };
 
-// First unit of CTA c when U units are split over C CTAs and the first g of
-// them take D units fewer each (c * (U + g D) / C - min(c, g) D).
-__host__ __device__ __forceinline__ long long wbegin(long long c, long long U, long long C, long long g,
-                                                     long long D) {
-  return c * (U + g * D) / C - (c < g ? c : g) * D;
-}
-// the CTA whose range holds unit u
-__host__ __device__ __forceinline__ int wcta_of(long long u, long long U, int C, long long g, long long D) {
-  const long long W = (U + g * D) / C;   // units of a CTA beyond the first g, about
-  long long c = u < wbegin(g, U, C, g, D) ? (W - D > 0 ? u / (W - D) : 0) : (W > 0 ? (u + g * D) / W : 0);
-  if (c >= C) c = C - 1;
-  if (c < 0) c = 0;
-  while (c + 1 < C && wbegin(c + 1, U, C, g, D) <= u) ++c;
-  while (c > 0 && wbegin(c, U, C, g, D) > u) --c;
-  return static_cast<int>(c);
+// The CTA of the norm phase whose range holds unit u (ranges are non-empty
+// and ascending: the largest c with ub[c] <= u)
+__device__ __forceinline__ int split_cta_of(const long long *ub, int C, long long u) {
+  int lo = 0, hi = C - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (ub[mid] <= u) lo = mid;
+    else hi = mid - 1;
+  }
+  return lo;
 }
 
 // The segments of a CTA's unit range [u_begin, hi) are taken last first: the
@@ -721,8 +634,9 @@ __device__ __forceinline__ long long seg_range(long long u_begin, long long hi, 
 }
 
 // This CTA's unit range in a phase: the Gram phase's fixed pieces (a tile's
-// K blocks cut into P equal parts) or the norm phase's weighted split.
-__device__ __forceinline__ void phase_range(const FwdPhase &f, int c, long long *ub, long long *ue) {
+// K blocks cut into P equal parts) or the norm phase's balanced split.
+__device__ __forceinline__ void phase_range(const FwdParams &p, const FwdPhase &f, int c, long long *ub,
+                                            long long *ue) {
   if (f.P > 0) {
     *ub = *ue = 0;
     if (c < f.P * f.tiles) {
@@ -732,8 +646,8 @@ __device__ __forceinline__ void phase_range(const FwdPhase &f, int c, long long 
       *ue = t0 + static_cast<long long>(q + 1) * f.kbtot / f.P;
     }
   } else {
-    *ub = wbegin(c, f.units, f.ctas, f.g, f.D);
-    *ue = wbegin(c + 1, f.units, f.ctas, f.g, f.D);
+    *ub = p.ub[c];
+    *ue = p.ub[c + 1];
   }
 }
 
@@ -761,6 +675,9 @@ __device__ bool wait_count(const int *ctr, int target, SharedCtl *ctl, int *err,
 __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
 }
+__device__ __forceinline__ void fence_proxy_async_shared() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
 
 // s/2 G entry (a, b) split into bf16 h and l
 __device__ __forceinline__ void store_gs3(__nv_bfloat16 *gh, __nv_bfloat16 *gl, int npad, int a, int b, float v) {
@@ -775,15 +692,16 @@ fwd_norm_kernel(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
                 const __grid_constant__ CUtensorMap mB, const __grid_constant__ CUtensorMap mAh_g,
                 const __grid_constant__ CUtensorMap mAl_g, const __grid_constant__ CUtensorMap mAh_n,
                 const __grid_constant__ CUtensorMap mAl_n, const __grid_constant__ CUtensorMap mGh,
-                const __grid_constant__ CUtensorMap mGl, const FwdParams p) {
+                const __grid_constant__ CUtensorMap mGl, const __grid_constant__ CUtensorMap mBs,
+                const FwdParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int S = p.S, SX = p.SX;
   uint8_t *xring = smem;
   uint8_t *yring = smem + static_cast<size_t>(SX) * kFwdXBytes;
   uint64_t *bars = reinterpret_cast<uint64_t *>(yring + static_cast<size_t>(S) * p.y_bytes);
-  // barrier layout: xfull[SX], xempty[SX], yfull[S], sfree[S], tconv[S], accf, acce, fin
-  SharedCtl *ctl = reinterpret_cast<SharedCtl *>(bars + 2 * SX + 3 * S + 3);
+  // barrier layout: xfull[SX], xempty[SX], yfull[S], sfree[S], tconv[S], accf, acce, fin, stg[4]
+  SharedCtl *ctl = reinterpret_cast<SharedCtl *>(bars + 2 * SX + 3 * S + 7);
   const uint32_t xfull0 = smem_u32(bars);
   const uint32_t xempty0 = xfull0 + 8u * SX;
   const uint32_t yfull0 = xempty0 + 8u * SX;
@@ -792,6 +710,7 @@ fwd_norm_kernel(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
   const uint32_t accf = tconv0 + 8u * S;
   const uint32_t acce = accf + 8;
   const uint32_t fin = acce + 8;
+  const uint32_t stg0 = fin + 8;   // one per converter warp: its rows of B, staged for the last epilogue
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -809,6 +728,7 @@ fwd_norm_kernel(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
     mbar_init(accf, 1);
     mbar_init(acce, 4);
     mbar_init(fin, 1);
+    for (int i = 0; i < 4; ++i) mbar_init(stg0 + 8u * i, 1);
     ctl->abort = 0;
     fence_barrier_init();
   }
@@ -816,6 +736,7 @@ fwd_norm_kernel(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
     prefetch_map(&mA);
     prefetch_map(&mW0);
     prefetch_map(&mB);
+    prefetch_map(&mBs);
   }
   if (warp == 6 && lane == 0) {
     prefetch_map(&mAh_g);
@@ -851,7 +772,7 @@ fwd_norm_kernel(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
       for (int ph = 0; ph < 2 && ok; ++ph) {
         const FwdPhase &f = p.ph[ph];
         long long u_begin, u_end;
-        phase_range(f, cl, &u_begin, &u_end);
+        phase_range(p, f, cl, &u_begin, &u_end);
         // this CTA's segments, last first (see seg_range)
         for (long long hi = u_end; hi > u_begin && ok;) {
           int t, kb0, kbe;
@@ -927,7 +848,7 @@ fwd_norm_kernel(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
         const uint32_t ic0 = idesc_bf16(f.nmma0);
         const uint32_t ic1 = f.nmma1 > 0 ? idesc_bf16(f.nmma1) : 0u;
         long long u_begin, u_end;
-        phase_range(f, cl, &u_begin, &u_end);
+        phase_range(p, f, cl, &u_begin, &u_end);
         for (long long hi = u_end; hi > u_begin && ok;) {
           int t, kb0, kbe;
           hi = seg_range(u_begin, hi, f.kbtot, &t, &kb0, &kbe);
@@ -997,7 +918,7 @@ fwd_norm_kernel(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
       const FwdPhase &f = p.ph[ph];
       const bool norm = ph == 1;
       long long u_begin, u_end;
-      phase_range(f, cl, &u_begin, &u_end);
+      phase_range(p, f, cl, &u_begin, &u_end);
       for (long long hi = u_end; hi > u_begin && ok;) {
         int t, kb0, kbe;
         hi = seg_range(u_begin, hi, f.kbtot, &t, &kb0, &kbe);
@@ -1069,7 +990,9 @@ fwd_norm_kernel(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
         }
         if (!ok) break;
         const int grow = mt * kBM + row;
-        const int seg = norm ? cl - wcta_of(static_cast<long long>(t) * f.kbtot, f.units, f.ctas, f.g, f.D) : 0;
+        // the CTA's last segment: its MMAs and all loads are done, so the
+        // operand rings are free to stage this warp's rows of B
+        const bool staged = norm && p.stage_b && hi == u_begin;
         // ---- epilogue of this segment
         const bool got = wait_bounded(accf, aphase, ctl, p.err, 5);
         if (!__all_sync(0xffffffffu, got)) {
@@ -1086,6 +1009,44 @@ fwd_norm_kernel(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
           const int cbase = nc * f.NC;
           const int ncol = min(f.NC, p.r - cbase);
           const float *brow = p.Bk + static_cast<size_t>(valid ? grow : 0) * p.ldb + cbase;
+          if (staged) {
+            // 32 x 32 boxes of B (128-byte rows, 128-byte swizzle), one per
+            // 32-column chunk, all in flight at once
+            const uint32_t region = smem_u32(smem) + static_cast<uint32_t>(quad * nchk) * 4096u;
+            const uint32_t sb = stg0 + 8u * quad;
+            if (lane == 0) {
+              fence_proxy_async_shared();   // the converters' reads of the X ring come first
+              mbar_expect_tx(sb, static_cast<uint32_t>(nchk) * 4096u);
+              for (int ci = 0; ci < nchk; ++ci)
+                tma_load_2d(region + 4096u * ci, &mBs, cbase + 32 * ci, mt * kBM + quad * 32, sb);
+            }
+            const bool got_b = wait_bounded(sb, 0, ctl, p.err, 11);
+            if (!__all_sync(0xffffffffu, got_b)) {
+              ok = false;
+              break;
+            }
+            const uint8_t *rw = smem + quad * nchk * 4096 + lane * 128;
+            for (int ci = 0; ci < nchk; ++ci) {
+              float v[32];
+              tmem_ld32(lane_addr + static_cast<uint32_t>(32 * ci), v);
+              // columns past the chunk's last valid one: neither B (the box may
+              // reach into the next chunk) nor the accumulator (past N it was
+              // never written) may enter the sum
+#pragma unroll
+              for (int e = 0; e < 32; ++e)
+                if (32 * ci + e >= ncol) v[e] = 0.0f;
+              const float4 *bx = reinterpret_cast<const float4 *>(rw + 4096 * ci);
+#pragma unroll
+              for (int q = 0; q < 8; ++q) {
+                float4 bq = bx[q ^ (lane & 7)];
+                if (32 * ci + 4 * q >= ncol) bq = make_float4(0.f, 0.f, 0.f, 0.f);
+                dot = fmaf(bq.x, v[4 * q], dot);
+                dot = fmaf(bq.y, v[4 * q + 1], dot);
+                dot = fmaf(bq.z, v[4 * q + 2], dot);
+                dot = fmaf(bq.w, v[4 * q + 3], dot);
+              }
+            }
+          } else {
           auto ldb8 = [&](int ci, float4 (&d)[8]) {
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
@@ -1101,6 +1062,11 @@ fwd_norm_kernel(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
             ldb8(ci + 2, b2);
             float v[32];
             tmem_ld32(lane_addr + static_cast<uint32_t>(32 * ci), v);
+            // accumulator columns past the chunk's valid ones (past N they
+            // were never written) stay out of the sum
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+              if (32 * ci + e >= ncol) v[e] = 0.0f;
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
               dot = fmaf(b0[q].x, v[4 * q], dot);
@@ -1114,8 +1080,10 @@ fwd_norm_kernel(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
               b1[q] = b2[q];
             }
           }
+          }
+          // this segment's records: piece t + cl (see FwdPhase::part)
           float2 *part2 = reinterpret_cast<float2 *>(f.part);
-          if (valid) part2[(tm * f.maxseg + seg) * kBM + row] = make_float2(n0, dot);
+          if (valid) part2[(static_cast<size_t>(t) + cl) * kBM + row] = make_float2(n0, dot);
           // count this warp's 32 records of the M tile; the warp that writes
           // the last ones sums all of them (chunks in order, segments in
           // order) into n_i = sqrt(max(0, sum n0 + 2 s sum dot)), g_i = m_i / n_i
@@ -1127,19 +1095,18 @@ fwd_norm_kernel(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
           int expect = 0;
           for (int c = 0; c < f.nchunks; ++c) {
             const long long ub = (static_cast<long long>(mt) * f.nchunks + c) * f.kbtot;
-            expect += wcta_of(ub + f.kbtot - 1, f.units, f.ctas, f.g, f.D) - wcta_of(ub, f.units, f.ctas, f.g, f.D) + 1;
+            expect += split_cta_of(p.ub, f.ctas, ub + f.kbtot - 1) - split_cta_of(p.ub, f.ctas, ub) + 1;
           }
           if (old == expect - 1) {
             __threadfence();
             if (valid) {
               float s0 = 0.0f, sd = 0.0f;
               for (int c = 0; c < f.nchunks; ++c) {
-                const long long ub = (static_cast<long long>(mt) * f.nchunks + c) * f.kbtot;
-                const int nseg =
-                    wcta_of(ub + f.kbtot - 1, f.units, f.ctas, f.g, f.D) - wcta_of(ub, f.units, f.ctas, f.g, f.D) + 1;
-                const size_t tmc = static_cast<size_t>(mt) * f.nchunks + c;
-                for (int j = 0; j < nseg; ++j) {
-                  const float2 v = __ldcg(part2 + (tmc * f.maxseg + j) * kBM + row);
+                const long long tc = static_cast<long long>(mt) * f.nchunks + c;
+                const int c0 = split_cta_of(p.ub, f.ctas, tc * f.kbtot);
+                const int c1 = split_cta_of(p.ub, f.ctas, (tc + 1) * f.kbtot - 1);
+                for (int j = c0; j <= c1; ++j) {
+                  const float2 v = __ldcg(part2 + (static_cast<size_t>(tc) + j) * kBM + row);
                   if (c == 0) s0 += v.x;
                   sd += v.y;
                 }
@@ -1182,48 +1149,76 @@ fwd_norm_kernel(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
           break;
         }
         __threadfence();
-        // blocks of 32 x 32 entries of tile tg: q, q + P, ...; thread ct takes
-        // column ct % 32 of rows 8 (ct / 32) .. 8 (ct / 32) + 7
+        // blocks of 32 x 32 entries of tile tg: q, q + P, ..., two at a time;
+        // thread ct takes 4 consecutive columns (one float4) of two rows of
+        // each.  The loads of eight pieces of both blocks are issued before
+        // any of them is added; each entry sums the pieces in order.
         int gmt, gnc;
         tile_coords(tg, f.nchunks, 1, &gmt, &gnc);
         const int nsub = (f.NC + 31) / 32;
-        const int col_l = ct & 31, row_l = (ct >> 5) * 8;
-        const size_t piece = static_cast<size_t>(kBM) * f.NC;
-        for (int sub = q; sub < nsub * nsub; sub += f.P) {
-          const int sr = sub / nsub, sc = sub - sr * nsub;
-          const int cc = sc * 32 + col_l;            // column within the tile
-          const int rr = sr * 32 + row_l;            // first of 8 rows within the tile
-          float acc[8];
+        const int nmine = (nsub * nsub - q + f.P - 1) / f.P;
+        const int c4 = (ct & 7) * 4, r2 = (ct >> 3) * 2;
+        const float4 *part4 = reinterpret_cast<const float4 *>(f.part);
+        const size_t piece4 = static_cast<size_t>(kBM) * f.NC / 4;
+        for (int k0 = 0; k0 < nmine; k0 += 2) {
+          int cc[2], rr[2];
+          bool vb[2];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
-          if (cc < f.NC) {
-            // the pieces tg * P .. tg * P + P - 1, added in that order; the
-            // loads of eight pieces are issued before any of them is added
-            const float *pj = f.part + (static_cast<size_t>(tg) * f.P * kBM + rr) * f.NC + cc;
-            for (int j0 = 0; j0 < f.P; j0 += 8) {
-              float a[8][8];
-#pragma unroll
-              for (int j = 0; j < 8; ++j)
-#pragma unroll
-                for (int i = 0; i < 8; ++i)
-                  a[j][i] = (j0 + j < f.P && rr + i < f.NC)
-                                ? __ldcg(pj + (j0 + j) * piece + static_cast<size_t>(i) * f.NC)
-                                : 0.0f;
-#pragma unroll
-              for (int j = 0; j < 8; ++j)
-#pragma unroll
-                for (int i = 0; i < 8; ++i)
-                  if (j0 + j < f.P) acc[i] += a[j][i];
-            }
+          for (int kk = 0; kk < 2; ++kk) {
+            const int sub = q + (k0 + kk) * f.P;
+            const int sr = sub / nsub, sc = sub - sr * nsub;
+            vb[kk] = k0 + kk < nmine;
+            cc[kk] = sc * 32 + c4;   // first of 4 columns within the tile
+            rr[kk] = sr * 32 + r2;   // first of 2 rows within the tile
+            vb[kk] = vb[kk] && cc[kk] < f.NC;
           }
-          const int gc = gnc * f.NC + cc;              // column of G
+          float4 acc[2][2];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int gr = gmt * f.NC + rr + i;        // row of G
-            if (gr >= p.npad || gc >= p.npad || cc >= f.NC || rr + i >= f.NC) continue;
-            const float v = (gr < p.r && gc < p.r) ? p.half_s * acc[i] : 0.0f;
-            store_gs3(p.gs_h, p.gs_l, p.npad, gr, gc, v);
-            if (gmt != gnc) store_gs3(p.gs_h, p.gs_l, p.npad, gc, gr, v);
+          for (int kk = 0; kk < 2; ++kk)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) acc[kk][e] = make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int j0 = 0; j0 < f.P; j0 += 8) {
+            float4 a[2][8][2];
+#pragma unroll
+            for (int kk = 0; kk < 2; ++kk)
+#pragma unroll
+              for (int jj = 0; jj < 8; ++jj)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                  const bool ld = vb[kk] && j0 + jj < f.P && rr[kk] + e < f.NC;
+                  const size_t off = (static_cast<size_t>(tg) * f.P + j0 + jj) * piece4 +
+                                     (static_cast<size_t>(rr[kk] + e) * f.NC + cc[kk]) / 4;
+                  a[kk][jj][e] = ld ? __ldcg(part4 + off) : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+#pragma unroll
+            for (int kk = 0; kk < 2; ++kk)
+#pragma unroll
+              for (int jj = 0; jj < 8; ++jj)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                  acc[kk][e].x += a[kk][jj][e].x;
+                  acc[kk][e].y += a[kk][jj][e].y;
+                  acc[kk][e].z += a[kk][jj][e].z;
+                  acc[kk][e].w += a[kk][jj][e].w;
+                }
+          }
+#pragma unroll
+          for (int kk = 0; kk < 2; ++kk) {
+            if (!vb[kk]) continue;
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int gr = gmt * f.NC + rr[kk] + e;   // row of G
+              if (rr[kk] + e >= f.NC || gr >= p.npad) continue;
+              const float w[4] = {acc[kk][e].x, acc[kk][e].y, acc[kk][e].z, acc[kk][e].w};
+#pragma unroll
+              for (int x = 0; x < 4; ++x) {
+                const int gc = gnc * f.NC + cc[kk] + x;   // column of G
+                if (gc >= p.npad) continue;
+                const float v = (gr < p.r && gc < p.r) ? p.half_s * w[x] : 0.0f;
+                store_gs3(p.gs_h, p.gs_l, p.npad, gr, gc, v);
+                if (gmt != gnc) store_gs3(p.gs_h, p.gs_l, p.npad, gc, gr, v);
+              }
+            }
           }
         }
         // s/2 G is read by the other CTAs' TMA loads (async proxy)
@@ -1760,6 +1755,11 @@ tc16_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ CUt
           }
           float v[32];
           tmem_ld32(lane_addr + static_cast<uint32_t>(32 * ci), v);
+          // accumulator columns past the chunk's valid ones (past N they were
+          // never written) stay out of the sum
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            if (32 * ci + e >= ncol) v[e] = 0.0f;
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             const uint32_t w[4] = {bq[q].x, bq[q].y, bq[q].z, bq[q].w};
@@ -2053,7 +2053,49 @@ void plan_phase(int mode, int M, int64_t in, int r, FwdPhase *f, int *mtiles) {
   f->units = static_cast<long long>(f->tiles) * f->kbtot;
 }
 
-bool plan_fwd(int64_t out, int64_t in, int64_t r, int max_ctas, FwdPlan *fp) {
+// Norm-phase CTA boundaries: ub[c] for c = 0 .. C (ub[C] = U), every range
+// non-empty, balancing t_unit per unit, t_seg per segment beyond a range's
+// first, and t_gram more for the first g CTAs (their Gram phase).  The
+// smallest time T at which C ranges cover all units is found by bisection.
+void balance_split(long long U, int kbtot, int C, int g, double t_unit, double t_seg, double t_gram,
+                   long long *ub) {
+  auto fill = [&](double T, bool commit) -> bool {
+    long long u = 0;
+    for (int c = 0; c < C; ++c) {
+      if (commit) ub[c] = u;
+      const long long lim = U - (C - 1 - c);   // leave a unit for every later CTA
+      double budget = T - (c < g ? t_gram : 0.0);
+      const long long start = u;
+      while (u < lim) {
+        if (u != start && u % kbtot == 0) {   // a new segment
+          budget -= t_seg;
+          if (budget < t_unit) break;
+        }
+        long long take = static_cast<long long>(budget / t_unit);
+        const long long rem = kbtot - u % kbtot;
+        if (take > rem) take = rem;
+        if (take > lim - u) take = lim - u;
+        if (take <= 0) break;
+        u += take;
+        budget -= take * t_unit;
+      }
+      if (u == start) ++u;   // never empty
+    }
+    if (commit) ub[C] = U;
+    return u >= U;
+  };
+  double lo = U * t_unit / C, hi = lo + t_gram + 2 * t_seg + t_unit;
+  while (!fill(hi, false)) hi *= 2;
+  for (int it = 0; it < 40; ++it) {
+    const double mid = 0.5 * (lo + hi);
+    if (fill(mid, false)) hi = mid;
+    else lo = mid;
+  }
+  fill(hi, true);
+}
+
+// with_split = false: the geometry and workspace only (no CTA ranges)
+bool plan_fwd(int64_t out, int64_t in, int64_t r, int max_ctas, FwdPlan *fp, bool with_split = true) {
   FwdParams &p = fp->p;
   std::memset(&p, 0, sizeof(p));
   const int ri = static_cast<int>(r);
@@ -2073,7 +2115,7 @@ bool plan_fwd(int64_t out, int64_t in, int64_t r, int max_ctas, FwdPlan *fp) {
   // shared memory: as many N-side stages as tensor memory and shared memory
   // allow while leaving at least two more raw-box slots than stages; the rest
   // goes to raw-box slots
-  const size_t fixed = 1024 + 8 * (2 * kFwdMaxX + 3 * kFwdMaxS + 3) + 64;
+  const size_t fixed = 1024 + 8 * (2 * kFwdMaxX + 3 * kFwdMaxS + 7) + 64;
   const size_t budget = kSmemMax - fixed;
   int S = (512 - acc_cols) / kFwdBK;
   if (S > kFwdMaxS) S = kFwdMaxS;
@@ -2113,24 +2155,24 @@ bool plan_fwd(int64_t out, int64_t in, int64_t r, int max_ctas, FwdPlan *fp) {
   if (P < 1) return false;   // more Gram tiles than CTAs (not for r <= kMaxR)
   fg.P = P;
   fg.ctas = P * fg.tiles;
-  // norm phase: the Gram CTAs take D units fewer, D = their Gram phase and
-  // reduction in norm units
+  // norm phase: CTA ranges that balance the estimated time per CTA.  Cost
+  // model (measured on GB300): a Gram unit 0.75 us; a reduction 1.2 us plus
+  // 1.6 us per 32 x 32 block; each segment of a range beyond its first costs
+  // an epilogue and the pipeline restart behind it, 1 us + 12.5 us x N / 384
   fn.ctas = p.ctas;
-  fn.g = fg.ctas;
   const int nsub = (fg.NC + 31) / 32;
-  const double t_red = 1.5 * ((nsub * nsub + P - 1) / P) * ((P + 7) / 8);
-  long long D = std::llround((static_cast<double>(fg.kbtot) / P * 0.6 + t_red + 2.0) / t_norm);
-  const long long dmax = fn.units / p.ctas / 2;
-  fn.D = D < dmax ? D : dmax;
-  // fewest units of a CTA in the norm phase, for the segment bound
-  const long long per = (fn.units + fn.g * fn.D) / p.ctas - fn.D - 1;
-  fn.maxseg = per >= 1 ? static_cast<int>((fn.kbtot - 1) / per + 2) : fn.kbtot + 1;
-  fg.maxseg = 1;
+  const double t_gram = fg.kbtot / static_cast<double>(P) * 0.75 + 1.2 + 1.6 * ((nsub * nsub + P - 1) / P);
+  const double t_seg = 1.0 + 12.5 * fn.NC / 384.0;
+  if (with_split) balance_split(fn.units, fn.kbtot, p.ctas, fg.ctas, t_norm, t_seg, t_gram, p.ub);
+
   p.nsync = 1 + fg.tiles;
   fp->part_g_bytes = static_cast<size_t>(fg.ctas) * kBM * fg.NC * sizeof(float);
-  fp->part_n_bytes = static_cast<size_t>(mt_n) * fn.nchunks * fn.maxseg * kBM * 2 * sizeof(float);
+  fp->part_n_bytes = static_cast<size_t>(fn.tiles + p.ctas) * kBM * 2 * sizeof(float);
   fp->smem_bytes = static_cast<size_t>(SX) * kFwdXBytes + static_cast<size_t>(S) * p.y_bytes + 1024 +
-                   8 * (2 * SX + 3 * S + 3) + 64;
+                   8 * (2 * SX + 3 * S + 7) + 64;
+  // the last epilogue's B staging: 4 warps x 32 rows x (N chunk) fp32
+  const size_t stage = 4 * static_cast<size_t>((fn.NC + 31) / 32) * 4096;
+  p.stage_b = stage <= static_cast<size_t>(SX) * kFwdXBytes + static_cast<size_t>(S) * p.y_bytes ? 1 : 0;
   if (p.tmem_cols > 256 && fp->smem_bytes < 116 * 1024) fp->smem_bytes = 116 * 1024;
   return true;
 }
@@ -2138,7 +2180,7 @@ bool plan_fwd(int64_t out, int64_t in, int64_t r, int max_ctas, FwdPlan *fp) {
 cudaError_t launch_fwd(const FwdPlan &fp, cudaStream_t cs, const CUtensorMap &mA, const CUtensorMap &mW0,
                        const CUtensorMap &mB, const CUtensorMap &mAh_g, const CUtensorMap &mAl_g,
                        const CUtensorMap &mAh_n, const CUtensorMap &mAl_n, const CUtensorMap &mGh,
-                       const CUtensorMap &mGl) {
+                       const CUtensorMap &mGl, const CUtensorMap &mBs) {
   // CTAs wait on one another (grid-wide counters): a cooperative launch makes
   // them co-resident or fails
   cudaLaunchConfig_t cfg = {};
@@ -2151,7 +2193,7 @@ cudaError_t launch_fwd(const FwdPlan &fp, cudaStream_t cs, const CUtensorMap &mA
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, fwd_norm_kernel, mA, mW0, mB, mAh_g, mAl_g, mAh_n, mAl_n, mGh, mGl, fp.p);
+  return cudaLaunchKernelEx(&cfg, fwd_norm_kernel, mA, mW0, mB, mAh_g, mAl_g, mAh_n, mAl_n, mGh, mGl, mBs, fp.p);
 }
 
 // forward-norm workspace (bf16 three-product scheme): the N-side split of A
@@ -2166,8 +2208,8 @@ struct Layout {
 size_t al256(size_t x) { return (x + 255) & ~size_t(255); }
 
 // sms: CTAs available
-bool plan_layout(int64_t out, int64_t in, int64_t r, int sms, FwdPlan *fp, Layout *L) {
-  if (!plan_fwd(out, in, r, sms, fp)) return false;
+bool plan_layout(int64_t out, int64_t in, int64_t r, int sms, FwdPlan *fp, Layout *L, bool with_split = true) {
+  if (!plan_fwd(out, in, r, sms, fp, with_split)) return false;
   int npad, nchunks, NC;
   plan_n(static_cast<int>(r), &npad, &nchunks, &NC);
   size_t off = 0;
@@ -2416,7 +2458,7 @@ extern "C" size_t dora_norm_factored_workspace(int64_t out, int64_t in, int64_t 
   // the CTA count, so this bounds every device with up to kMaxCtas SMs
   FwdPlan fp;
   Layout L;
-  if (!plan_layout(out > 0 ? out : 1, in, r, kMaxCtas, &fp, &L)) return 0;
+  if (!plan_layout(out > 0 ? out : 1, in, r, kMaxCtas, &fp, &L, false)) return 0;
   return L.total;
 }
 
@@ -2440,6 +2482,90 @@ extern "C" dora_status dora_device_error(int *code) {
   }
   return DORA_OK;
 }
+
+namespace {
+// Host-side caches of the forward norm, so that repeated calls (a training
+// loop calls it with the same shapes and, mostly, the same buffers every
+// step) skip the planning and the tensor-map encoding:
+//   plans  per (device, out, in, r): the phase geometry, the balanced CTA
+//          ranges and the workspace layout;
+//   maps   per (device, W0, A, B, workspace, out, in, r): the ten encoded
+//          tensor maps (they hold these addresses).
+// Both are small rings of entries; a miss recomputes and replaces the oldest.
+constexpr int kCacheEntries = 8;
+struct PlanEntry {
+  bool used;
+  int device, sms;
+  int64_t out, in, r;
+  FwdPlan fp;
+  Layout L;
+};
+struct MapEntry {
+  bool used;
+  int device;
+  const void *W0, *A, *B, *ws;
+  int64_t out, in, r;
+  CUtensorMap maps[10];
+};
+std::mutex g_cache_mu;
+PlanEntry g_plans[kCacheEntries];
+MapEntry g_maps[kCacheEntries];
+int g_plan_next = 0, g_map_next = 0;
+
+bool cached_plan(int device, int sms, int64_t out, int64_t in, int64_t r, FwdPlan *fp, Layout *L) {
+  {
+    std::lock_guard<std::mutex> lock(g_cache_mu);
+    for (const PlanEntry &e : g_plans)
+      if (e.used && e.device == device && e.sms == sms && e.out == out && e.in == in && e.r == r) {
+        *fp = e.fp;
+        *L = e.L;
+        return true;
+      }
+  }
+  if (!plan_layout(out, in, r, sms, fp, L)) return false;
+  std::lock_guard<std::mutex> lock(g_cache_mu);
+  PlanEntry &e = g_plans[g_plan_next];
+  g_plan_next = (g_plan_next + 1) % kCacheEntries;
+  e.used = true;
+  e.device = device;
+  e.sms = sms;
+  e.out = out;
+  e.in = in;
+  e.r = r;
+  e.fp = *fp;
+  e.L = *L;
+  return true;
+}
+
+bool find_maps(int device, const void *W0, const void *A, const void *B, const void *ws, int64_t out, int64_t in,
+               int64_t r, CUtensorMap *maps) {
+  std::lock_guard<std::mutex> lock(g_cache_mu);
+  for (const MapEntry &e : g_maps)
+    if (e.used && e.device == device && e.W0 == W0 && e.A == A && e.B == B && e.ws == ws && e.out == out &&
+        e.in == in && e.r == r) {
+      std::memcpy(maps, e.maps, sizeof(e.maps));
+      return true;
+    }
+  return false;
+}
+
+void keep_maps(int device, const void *W0, const void *A, const void *B, const void *ws, int64_t out, int64_t in,
+               int64_t r, const CUtensorMap *maps) {
+  std::lock_guard<std::mutex> lock(g_cache_mu);
+  MapEntry &e = g_maps[g_map_next];
+  g_map_next = (g_map_next + 1) % kCacheEntries;
+  e.used = true;
+  e.device = device;
+  e.W0 = W0;
+  e.A = A;
+  e.B = B;
+  e.ws = ws;
+  e.out = out;
+  e.in = in;
+  e.r = r;
+  std::memcpy(e.maps, maps, sizeof(e.maps));
+}
+}  // namespace
 
 extern "C" dora_status dora_norm_factored(const float *W0, const float *A, const float *B, const float *m, float s,
                                           int64_t out, int64_t in, int64_t r, float *norm, float *g,
@@ -2467,7 +2593,8 @@ extern "C" dora_status dora_norm_factored(const float *W0, const float *A, const
 
   FwdPlan fp;
   Layout L;
-  if (!plan_layout(out, in, r, sms, &fp, &L)) return DORA_ERR_SHAPE;
+  if (!cached_plan(device, sms, out, in, r, &fp, &L)) return DORA_ERR_SHAPE;
+  if (workspace_bytes < L.total) return DORA_ERR_WORKSPACE;   // never: the size above bounds every device
   uint8_t *ws = static_cast<uint8_t *>(workspace);
   __nv_bfloat16 *a_h = reinterpret_cast<__nv_bfloat16 *>(ws + L.a_h);
   __nv_bfloat16 *a_l = reinterpret_cast<__nv_bfloat16 *>(ws + L.a_l);
@@ -2512,23 +2639,29 @@ extern "C" dora_status dora_norm_factored(const float *W0, const float *A, const
   p.ldb = static_cast<int>(ldb);
   p.gs_h = reinterpret_cast<__nv_bfloat16 *>(ws + L.g_h);
   p.gs_l = reinterpret_cast<__nv_bfloat16 *>(ws + L.g_l);
-  CUtensorMap mA, mAh_g, mAl_g, mAh_n, mAl_n, mW0, mB, mGh, mGl;
-  const int nbg = p.ph[0].nbox, nbn = p.ph[1].nbox;
-  bool ok = make_map(&mA, A, false, r, in, in, kBM, 128) &&
-            make_map(&mAh_g, a_h, true, r, in8, in8, nbg, 64) && make_map(&mAl_g, a_l, true, r, in8, in8, nbg, 64) &&
-            make_map(&mAh_n, a_h, true, r, in8, in8, nbn, 64) && make_map(&mAl_n, a_l, true, r, in8, in8, nbn, 64) &&
-            make_map(&mW0, W0, false, out, in, in, kBM, 128) && make_map(&mB, Bk, false, out, ldb, ldb, kBM, 128) &&
-            make_map(&mGh, p.gs_h, true, npad, npad, npad, nbn, 64) &&
-            make_map(&mGl, p.gs_l, true, npad, npad, npad, nbn, 64);
-  if (!ok) {
-    dora::count_launches(launches);
-    return DORA_ERR_CUDA;
+  // map order: A, Ah_g, Al_g, Ah_n, Al_n, W0, B, Gh, Gl, B staging
+  CUtensorMap mp[10];
+  if (!find_maps(device, W0, A, B, workspace, out, in, r, mp)) {
+    const int nbg = p.ph[0].nbox, nbn = p.ph[1].nbox;
+    const bool ok =
+        make_map(&mp[0], A, false, r, in, in, kBM, 128) && make_map(&mp[1], a_h, true, r, in8, in8, nbg, 64) &&
+        make_map(&mp[2], a_l, true, r, in8, in8, nbg, 64) && make_map(&mp[3], a_h, true, r, in8, in8, nbn, 64) &&
+        make_map(&mp[4], a_l, true, r, in8, in8, nbn, 64) && make_map(&mp[5], W0, false, out, in, in, kBM, 128) &&
+        make_map(&mp[6], Bk, false, out, ldb, ldb, kBM, 128) &&
+        make_map(&mp[7], p.gs_h, true, npad, npad, npad, nbn, 64) &&
+        make_map(&mp[8], p.gs_l, true, npad, npad, npad, nbn, 64) &&
+        make_map(&mp[9], Bk, false, out, ldb, ldb, 32, 128);   // 32 x 32 boxes for the B staging
+    if (!ok) {
+      dora::count_launches(launches);
+      return DORA_ERR_CUDA;
+    }
+    keep_maps(device, W0, A, B, workspace, out, in, r, mp);
   }
 
   // 2. one launch: Gram partials, the reduction into s/2 G (split), and
   //    [W0 | B] x [A | s/2 G]^T with per-segment row reductions; the last
   //    epilogue warp of each quarter M tile writes n and g
-  if (launch_fwd(fp, cs, mA, mW0, mB, mAh_g, mAl_g, mAh_n, mAl_n, mGh, mGl) != cudaSuccess) {
+  if (launch_fwd(fp, cs, mp[0], mp[5], mp[6], mp[1], mp[2], mp[3], mp[4], mp[7], mp[8], mp[9]) != cudaSuccess) {
     dora::count_launches(launches);
     return DORA_ERR_CUDA;
   }

@@ -8,7 +8,8 @@ backward, through the C ABI.  Prints ONE JSON line (rank 0).
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
 --impl reference times the fp64 CPU oracle (the method's plain definition) on
-a bounded sample of the same workload, on the host cores.
+a bounded sample of the same workload, on all the host cores (a process pool
+over independent columns and rows).
 
 Multi-GPU: one process per GPU under torchrun; every rank runs an independent
 replica on its own seeded inputs (the path has no exchange step), timing is
@@ -26,7 +27,9 @@ import sys
 import tempfile
 import time
 
-os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")   # the CPU baseline runs single-threaded
+# one BLAS thread per process: the single-core baseline runs here, the
+# all-core one in a pool of worker processes
+os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")
 
 import numpy as np
 
@@ -39,10 +42,13 @@ METRIC = "fused DoRA compose fwd+bwd HBM GB/s (% of GB300 peak); factored-norm Â
 WORKLOAD = "high_rank"
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
-# DRAM read + write bytes of one compose_bwd_kernel launch on this workload,
-# from the ncu capture summarised in profiles/compose_fwd_bwd_high_rank.md;
-# set to None whenever that kernel changes until it is captured again
-COMPOSE_BWD_TRAFFIC_BYTES = 755031552 + 460042496
+# dram__bytes_read.sum + dram__bytes_write.sum of one compose_bwd_kernel launch
+# on this workload with the inputs rotated as below, from one ncu capture of
+# that kernel (755,076,352 read: exactly dy, base and lora; 459,657,984
+# written of the 503 MB of d_base and d_lora, the rest still dirty in L2 when
+# the kernel ends); None whenever the kernel changes, until captured again
+COMPOSE_BWD_TRAFFIC_BYTES = 755076352 + 459657984
+INPUT_SETS = 3   # input sets rotated over the steps: each is larger than L2
 
 
 def algorithmic(sh) -> dict:
@@ -59,8 +65,8 @@ def algorithmic(sh) -> dict:
 
 
 def peaks() -> dict:
-    p = {"hbm_gbs": FALLBACK_HBM_GBS, "bf16_tflops": FALLBACK_BF16_TFLOPS, "tf32_tflops": 1700.0 / 2,
-         "source": "fallback"}
+    p = {"hbm_gbs": FALLBACK_HBM_GBS, "bf16_tflops": FALLBACK_BF16_TFLOPS, "bf16_tflops_sustained": 1700.0,
+         "tf32_tflops": 1700.0 / 2, "source": "fallback"}
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
             m = json.load(f)
@@ -170,22 +176,117 @@ def oracle_sample(sh, d, tokens: int, rows: int) -> dict:
             "norm_us_per_module": (t1 - t0) * 1e6 * sh.out / rows, "tokens": tokens, "rows": rows}
 
 
+def _shm_put(arrays):
+    """Copies arrays into shared memory blocks; returns the blocks and their
+    (name, shape, dtype) descriptions for the workers."""
+    from multiprocessing import shared_memory
+    blocks, desc = [], {}
+    for k, a in arrays.items():
+        a = np.ascontiguousarray(a)
+        b = shared_memory.SharedMemory(create=True, size=max(a.nbytes, 1))
+        np.ndarray(a.shape, a.dtype, buffer=b.buf)[...] = a
+        blocks.append(b)
+        desc[k] = (b.name, a.shape, a.dtype.str)
+    return blocks, desc
+
+
+def _oracle_part(task):
+    """Worker: the oracle on one slice, from the shared-memory sample.
+    kind 'norm': dense norm of rows [lo, hi); kind 'compose': compose fwd + bwd
+    of columns [lo, hi) (columns are independent in both)."""
+    from multiprocessing import shared_memory
+    import oracle
+    kind, desc, s, lo, hi = task
+    blocks, a = [], {}
+    for k, (name, shape, dt) in desc.items():
+        b = shared_memory.SharedMemory(name=name)
+        blocks.append(b)
+        a[k] = np.ndarray(shape, np.dtype(dt), buffer=b.buf)
+    if kind == "norm":
+        oracle.weight_norm(a["W0"][lo:hi], a["A"], a["B"][lo:hi], a["m"][lo:hi], s)
+    else:
+        base = oracle.bf16_bits_to_f64(a["base"][:, lo:hi])
+        lora = oracle.bf16_bits_to_f64(a["lora"][:, lo:hi])
+        dy = oracle.bf16_bits_to_f64(a["dy"][:, lo:hi])
+        g = np.ones(hi - lo)
+        oracle.compose_fwd(base, lora, g, s)
+        oracle.compose_bwd(dy, base, lora, g, g, s)
+    a.clear()
+    for b in blocks:
+        b.close()
+    return hi - lo
+
+
+class ParallelOracle:
+    """The oracle as it stands on every host core: a pool of worker processes
+    (spawn start method: safe beside a CUDA context), each taking a slice of
+    columns (compose) or rows (norm) of a bounded sample held in shared memory."""
+
+    def __init__(self, sh, d, tokens, rows, cores=None):
+        import concurrent.futures as cf
+        import multiprocessing as mp
+        self.sh, self.tokens, self.rows = sh, tokens, rows
+        self.cores = cores or os.cpu_count() or 1
+        self.blocks, self.desc = _shm_put({
+            "base": d["base"][:tokens], "lora": d["lora"][:tokens], "dy": d["dy"][:tokens],
+            "W0": d["W0"][:rows], "A": d["A"], "B": d["B"][:rows], "m": d["m"][:rows]})
+        self.s = d["s"]
+        self.pool = cf.ProcessPoolExecutor(max_workers=self.cores, mp_context=mp.get_context("spawn"))
+        self.run()   # start the workers and import numpy / the oracle in each
+
+    def _map(self, kind, n):
+        cuts = np.linspace(0, n, self.cores + 1).astype(int)
+        tasks = [(kind, self.desc, self.s, int(cuts[i]), int(cuts[i + 1])) for i in range(self.cores)
+                 if cuts[i + 1] > cuts[i]]
+        t0 = time.perf_counter()
+        list(self.pool.map(_oracle_part, tasks))
+        return time.perf_counter() - t0
+
+    def run(self) -> dict:
+        norm_s = self._map("norm", self.rows)
+        compose_s = self._map("compose", self.sh.out)
+        sub = wl.ModuleShape(self.sh.name, self.sh.out, self.sh.inp, self.sh.r, self.tokens, self.sh.act,
+                             self.sh.sigma_B, self.sh.sigma_m, True, False)
+        a = algorithmic(sub)
+        return {"compose_s": compose_s, "norm_s": norm_s, "compose_bytes": a["fwd_bytes"] + a["bwd_bytes"],
+                "norm_us_per_module": norm_s * 1e6 * self.sh.out / self.rows}
+
+    def close(self):
+        self.pool.shutdown()
+        for b in self.blocks:
+            b.close()
+            b.unlink()
+
+
 def cpu_baseline(sh, d, tokens=4096, rows=1024, budget_s=10.0, max_reps=8) -> dict:
-    """The oracle as it stands, single-threaded, repeated on the same bounded
-    sample until about `budget_s` seconds of CPU work have been timed."""
-    cb = cs = ns = 0.0
-    reps = 0
-    t0 = time.perf_counter()
-    while reps < max_reps and (reps == 0 or time.perf_counter() - t0 < budget_s):
-        r = oracle_sample(sh, d, tokens, rows)
-        cb += r["compose_bytes"]
-        cs += r["compose_s"]
-        ns += r["norm_s"]
-        reps += 1
-    return {"value": cb / cs / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"fp64 numpy oracle, 1 thread, {reps} repetitions: compose fwd+bwd on {tokens} of {sh.T} "
-                      f"tokens x {sh.out} columns; dense norm on {rows} of {sh.out} rows",
-            "norm_us_per_module": ns / reps * 1e6 * sh.out / rows}
+    """The oracle as it stands, repeated on the same bounded sample until about
+    `budget_s` seconds of CPU work have been timed: on all host cores (the
+    reported value) and on one core."""
+    def repeat(fn):
+        cb = cs = ns = 0.0
+        reps = 0
+        t0 = time.perf_counter()
+        while reps < max_reps and (reps == 0 or time.perf_counter() - t0 < budget_s):
+            r = fn()
+            cb += r["compose_bytes"]
+            cs += r["compose_s"]
+            ns += r["norm_s"]
+            reps += 1
+        return cb / cs / 1e9, ns / reps * 1e6 * sh.out / rows, reps
+
+    one_gbs, one_norm, one_reps = repeat(lambda: oracle_sample(sh, d, tokens, rows))
+    po = ParallelOracle(sh, d, tokens, rows)
+    try:
+        all_gbs, all_norm, all_reps = repeat(po.run)
+    finally:
+        po.close()
+    return {"value": all_gbs, "unit": "GB/s", "cores": po.cores, "kind": "oracle",
+            "sample": f"fp64 numpy oracle on {po.cores} worker processes (one thread each), {all_reps} repetitions: "
+                      f"compose fwd+bwd on {tokens} of {sh.T} tokens x {sh.out} columns, split by columns; dense "
+                      f"norm on {rows} of {sh.out} rows, split by rows",
+            "norm_us_per_module": all_norm,
+            "single_core": {"value": one_gbs, "unit": "GB/s", "cores": 1, "norm_us_per_module": one_norm,
+                            "repetitions": one_reps}}
 
 
 def run_reference(args, rank, world):
@@ -193,19 +294,24 @@ def run_reference(args, rank, world):
         return
     sh = wl.shape(WORKLOAD)
     d = wl.make_module(sh, wl.seed_for(WORKLOAD))
-    # per-step sample sized so that warm-up + steps stay within about two minutes
+    # per-step sample sized so that warm-up + steps stay within about two
+    # minutes on all host cores
     n = max(1, args.steps + args.warmup)
-    tokens = int(min(768, max(32, 768 * 40 // n)))
-    rows = int(min(256, max(16, 256 * 40 // n)))
-    for _ in range(args.warmup):
-        oracle_sample(sh, d, tokens, rows)
-    times, vals, norm_us = [], [], []
-    for _ in range(args.steps):
-        t0 = time.perf_counter()
-        r = oracle_sample(sh, d, tokens, rows)
-        times.append(time.perf_counter() - t0)
-        vals.append(r["compose_bytes"] / r["compose_s"] / 1e9)
-        norm_us.append(r["norm_us_per_module"])
+    tokens = int(min(4096, max(64, 4096 * 40 // n)))
+    rows = int(min(1024, max(32, 1024 * 40 // n)))
+    po = ParallelOracle(sh, d, tokens, rows)
+    try:
+        for _ in range(args.warmup):
+            po.run()
+        times, vals, norm_us = [], [], []
+        for _ in range(args.steps):
+            t0 = time.perf_counter()
+            r = po.run()
+            times.append(time.perf_counter() - t0)
+            vals.append(r["compose_bytes"] / r["compose_s"] / 1e9)
+            norm_us.append(r["norm_us_per_module"])
+    finally:
+        po.close()
     value = statistics.mean(vals)
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
@@ -214,8 +320,9 @@ def run_reference(args, rank, world):
         "config": {"workload": f"{WORKLOAD}: out=in={sh.out}, r={sh.r}, T={sh.T} bf16 activations, fp32 weights",
                    "sample_per_step": f"compose fwd+bwd on {tokens} tokens, dense norm on {rows} rows"},
         "norm_us_per_module": statistics.mean(norm_us),
-        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
-                         "sample": f"{tokens} tokens x {sh.out} columns compose fwd+bwd; {rows} norm rows"},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": po.cores, "kind": "oracle",
+                         "sample": f"{tokens} tokens x {sh.out} columns compose fwd+bwd (split by columns); "
+                                   f"{rows} norm rows (split by rows); {po.cores} worker processes"},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -250,6 +357,12 @@ def run_ours(args, rank, world, local_rank):
 
     W0, A, B, m = (f32(d[k]) for k in ("W0", "A", "B", "m"))
     base, lora, dy = (bf16(d[k]) for k in ("base", "lora", "dy"))
+    # INPUT_SETS copies of the inputs in separate buffers (each ~1 GB, far
+    # above L2), rotated over the steps: no launch reads lines that the
+    # previous step left in L2
+    sets_in = [(W0, A, B, m, base, lora, dy)]
+    for _ in range(INPUT_SETS - 1):
+        sets_in.append(tuple(t.clone() for t in sets_in[0]))
     norm = torch.empty(sh.out, device=dev)
     g = torch.empty(sh.out, device=dev)
     y = torch.empty_like(base)
@@ -260,21 +373,30 @@ def run_ours(args, rank, world, local_rank):
     ws_b = torch.empty(dora.dora_compose_bwd_workspace(sh.T, sh.out), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
-    def step(ev=None):
+    def step(k, ev=None):
+        W0_, A_, B_, m_, base_, lora_, dy_ = sets_in[k % INPUT_SETS]
         if ev is not None:
             ev[0].record(stream)
-        dora.dora_norm_factored(W0, A, B, m, s, norm, g, ws_n, stream)
+        dora.dora_norm_factored(W0_, A_, B_, m_, s, norm, g, ws_n, stream)
         if ev is not None:
             ev[1].record(stream)
-        dora.dora_compose_fwd(base, lora, g, s, y, stream)
+        dora.dora_compose_fwd(base_, lora_, g, s, y, stream)
         if ev is not None:
             ev[2].record(stream)
-        dora.dora_compose_bwd(dy, base, lora, g, norm, s, db, dl, dm, ws_b, stream)
+        dora.dora_compose_bwd(dy_, base_, lora_, g, norm, s, db, dl, dm, ws_b, stream)
         if ev is not None:
             ev[3].record(stream)
 
-    for _ in range(args.warmup):
-        step()
+    # the clock sampler starts before the warm-up, so that its start-up (an
+    # nvidia-smi process) is not inside the timed region
+    try:
+        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        gpu_id = str(local_rank)
+    clocks = ClockSampler(gpu_id)
+    clocks.start()
+    for k in range(args.warmup):
+        step(k)
     torch.cuda.synchronize()
     if dora.dora_device_error() != 0:
         raise RuntimeError("a kernel wait gave up during warm-up")
@@ -284,12 +406,6 @@ def run_ours(args, rank, world, local_rank):
             dist.barrier()
 
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
-    try:
-        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
-    except Exception:
-        gpu_id = str(local_rank)
-    clocks = ClockSampler(gpu_id)
-    clocks.start()
     launches0 = dora.dora_kernel_launches()
     barrier()
     torch.cuda.synchronize()
@@ -297,7 +413,7 @@ def run_ours(args, rank, world, local_rank):
     t_end = torch.cuda.Event(enable_timing=True)
     t_start.record(stream)
     for k in range(args.steps):
-        step(evs[k])
+        step(k, evs[k])
     t_end.record(stream)
     torch.cuda.synchronize()
     barrier()
@@ -395,7 +511,8 @@ def run_ours(args, rank, world, local_rank):
         "config": {"workload": f"{WORKLOAD}: DoRA module out=in={sh.out}, r={sh.r} (s=32/sqrt(r)), "
                                f"T={sh.T} tokens (batch 3 x seq 5120), bf16 activations, fp32 weights; "
                                "step = factored norm + compose fwd + compose bwd",
-                   "l2": "inputs larger than L2 (W0 268 MB; each activation 252 MB)",
+                   "l2": f"{INPUT_SETS} input sets in separate buffers (each ~1 GB: W0 268 MB, each activation "
+                         "252 MB) rotated over the steps, so no launch reads what the previous step left in L2",
                    "parallelism": "replicas" if world > 1 else "single"},
         "pct_of_hbm_peak": 100.0 * value / world / pk["hbm_gbs"],
         "norm_us_per_module": norm_us,
@@ -406,19 +523,37 @@ def run_ours(args, rank, world, local_rank):
                      "unit": "GB/s", "frac": bwd_gbs / pk["hbm_gbs"],
                      "traffic": COMPOSE_BWD_TRAFFIC_BYTES,
                      "algorithmic_bytes": alg["bwd_bytes"], "peak_source": pk["source"] + " (copy bandwidth)"},
-        "roofline_norm": {"bound": "tensor", "kernel": "factored norm (all four launches)",
-                          "achieved": 2 * alg["norm_flops"] / (norm_ms * 1e-3) / 1e12,
-                          "peak": pk["tf32_tflops"], "unit": "TFLOP/s",
-                          "frac": 2 * alg["norm_flops"] / (norm_ms * 1e-3) / 1e12 / pk["tf32_tflops"],
-                          "note": "achieved = TF32-equivalent issued work (one TF32 product + one bf16 product "
-                                  "of twice the K = 2x the algorithmic flops) / norm time; peak = measured "
-                                  "sustained bf16 x 1/2 (TF32:bf16 nominal dense ratio)",
-                          "algorithmic_tflops": alg["norm_flops"] / (norm_ms * 1e-3) / 1e12},
+        "roofline_norm": {"bound": "tensor",
+                          "kernel": "factored norm (the split of A, then one launch: Gram pieces, reduction of "
+                                    "s/2 G and the norm GEMM)",
+                          "achieved": 3 * alg["norm_flops"] / (norm_ms * 1e-3) / 1e12,
+                          "peak": pk["bf16_tflops_sustained"], "unit": "TFLOP/s",
+                          "frac": 3 * alg["norm_flops"] / (norm_ms * 1e-3) / 1e12 / pk["bf16_tflops_sustained"],
+                          "note": "achieved = issued bf16 tensor work (each fp32 product is three bf16 products "
+                                  "h_x h_y + l_x h_y + h_x l_y: 3x the algorithmic flops) / norm time; peak = "
+                                  "measured sustained bf16 (of " + pk["source"] + "; the norm runs inside a long "
+                                  "step)",
+                          "algorithmic_tflops": alg["norm_flops"] / (norm_ms * 1e-3) / 1e12,
+                          "peak_algorithmic": pk["bf16_tflops"] / 2,
+                          "frac_algorithmic": alg["norm_flops"] / (norm_ms * 1e-3) / 1e12 / (pk["bf16_tflops"] / 2),
+                          "note_algorithmic": "the method's flops (one pass, fp32 products) against the dense TF32 "
+                                              "rate: measured burst bf16 x 1/2 (nominal TF32:bf16 ratio)"},
         "gpu_launches": launches,
         "clocks": clk,
     }
     if e2e is not None:
         line["e2e"] = e2e
+    if not args.no_workloads:
+        # the other workloads, timed in the same run after the timed region
+        # (inputs drawn on the device; each kernel timed over repeated calls)
+        del sets_in
+        torch.cuda.empty_cache()
+        line["workloads"] = {
+            "attn_proj_inference": attn_proj_row(dora, dev, stream),
+            "rank_sweep": rank_sweep_rows(dora, dev, stream, wl.RANK_SWEEP),
+            "mlp_stack": mlp_stack_row(dora, dev, stream)}
+        line["workloads"]["mlp_stack"]["frac_of_hbm"] = (
+            line["workloads"]["mlp_stack"]["aggregate_algorithmic_gbs"] / pk["hbm_gbs"])
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(sh, d)
     print(json.dumps(line), flush=True)
@@ -457,6 +592,131 @@ def _device_module(sh, seed, dev):
     return W0, A, B, m
 
 
+def rank_sweep_rows(dora, dev, stream, ranks):
+    """out = in = 8192, T = 8192 bf16, per rank: norm time (and its host time
+    per call), compose GB/s and the norm's whole transient (its workspace)
+    against one dense fp32 out x in matrix.  Inputs drawn on the device,
+    seeded by position."""
+    import torch
+    rows = []
+    for k, r in enumerate(ranks):
+        sh = wl.shape("rank_sweep", r=r)
+        W0, A, B, m = _device_module(sh, wl.seed_for("rank_sweep", k), dev)
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(wl.seed_for("rank_sweep", k) + 7)
+        act = [torch.randn(sh.T, sh.out, device=dev, generator=gen).bfloat16() for _ in range(3)]
+        act[1] = (act[1].float() * math.sqrt(sh.r) * sh.sigma_B).bfloat16()
+        base, lora, dy = act
+        norm = torch.empty(sh.out, device=dev)
+        g = torch.empty(sh.out, device=dev)
+        nbytes = dora.dora_norm_factored_workspace(sh.out, sh.inp, sh.r)
+        ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        y, db, dl = torch.empty_like(base), torch.empty_like(base), torch.empty_like(base)
+        dm = torch.empty(sh.out, device=dev)
+        wsb = torch.empty(dora.dora_compose_bwd_workspace(sh.T, sh.out), dtype=torch.uint8, device=dev)
+        t_norm = _time_ms(lambda: dora.dora_norm_factored(W0, A, B, m, sh.s, norm, g, ws, stream), 20, stream)
+        # host time of one call (the device is kept busy, so the call returns
+        # as soon as its launches are queued)
+        torch.cuda.synchronize()
+        h0 = time.perf_counter()
+        for _ in range(20):
+            dora.dora_norm_factored(W0, A, B, m, sh.s, norm, g, ws, stream)
+        host_us = (time.perf_counter() - h0) / 20 * 1e6
+        torch.cuda.synchronize()
+        t_fwd = _time_ms(lambda: dora.dora_compose_fwd(base, lora, g, sh.s, y, stream), 20, stream)
+        t_bwd = _time_ms(lambda: dora.dora_compose_bwd(dy, base, lora, g, norm, sh.s, db, dl, dm, wsb, stream),
+                         20, stream)
+        alg = algorithmic(sh)
+        dense = sh.out * sh.inp * 4
+        rows.append({"r": r, "out": sh.out, "in": sh.inp, "T": sh.T,
+                     "norm_us": t_norm * 1e3, "norm_host_us_per_call": host_us,
+                     "norm_tflops_algorithmic": alg["norm_flops"] / (t_norm * 1e-3) / 1e12,
+                     "fwd_gbs": alg["fwd_bytes"] / (t_fwd * 1e-3) / 1e9,
+                     "bwd_gbs": alg["bwd_bytes"] / (t_bwd * 1e-3) / 1e9,
+                     "norm_transient_bytes": nbytes, "dense_fp32_matrix_bytes": dense,
+                     "dense_over_transient": dense / nbytes,
+                     "rank_dependent_theory": sh.out * sh.inp / (sh.out * sh.r + sh.r * sh.r)})
+        del W0, A, B, m, act, base, lora, dy, ws, y, db, dl
+        torch.cuda.empty_cache()
+    return rows
+
+
+def mlp_stack_row(dora, dev, stream, reps=3):
+    """32 gate/up (4096 -> 14336) + 32 down (14336 -> 4096) modules, r = 512,
+    T = 16384, training step per module (norm + fwd + bwd), independent seeds,
+    back to back: modules/s and aggregate algorithmic GB/s."""
+    import torch
+    shapes = [wl.shape("mlp_gate_up"), wl.shape("mlp_down")]
+    mods = []
+    for k in range(wl.MLP_REPEATS):
+        for j, sh in enumerate(shapes):
+            mods.append((sh, _device_module(sh, wl.seed_for(sh.name, 2 * k + j), dev)))
+    bufs = {}
+    for sh in shapes:
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(wl.seed_for(sh.name) + 99)
+        act = [torch.randn(sh.T, sh.out, device=dev, generator=gen).bfloat16() for _ in range(3)]
+        act[1] = (act[1].float() * math.sqrt(sh.r) * sh.sigma_B).bfloat16()
+        bufs[sh.name] = {
+            "act": act, "y": torch.empty_like(act[0]), "db": torch.empty_like(act[0]),
+            "dl": torch.empty_like(act[0]), "norm": torch.empty(sh.out, device=dev),
+            "g": torch.empty(sh.out, device=dev), "dm": torch.empty(sh.out, device=dev),
+            "ws": torch.empty(dora.dora_norm_factored_workspace(sh.out, sh.inp, sh.r), dtype=torch.uint8,
+                              device=dev),
+            "wsb": torch.empty(dora.dora_compose_bwd_workspace(sh.T, sh.out), dtype=torch.uint8, device=dev)}
+
+    def stack():
+        for sh, (W0, A, B, m) in mods:
+            b = bufs[sh.name]
+            base, lora, dy = b["act"]
+            dora.dora_norm_factored(W0, A, B, m, sh.s, b["norm"], b["g"], b["ws"], stream)
+            dora.dora_compose_fwd(base, lora, b["g"], sh.s, b["y"], stream)
+            dora.dora_compose_bwd(dy, base, lora, b["g"], b["norm"], sh.s, b["db"], b["dl"], b["dm"], b["wsb"],
+                                  stream)
+
+    t = _time_ms(stack, reps, stream)
+    total = sum(sum(v for k, v in algorithmic(sh).items() if k.endswith("_bytes")) for sh, _ in mods)
+    compose = sum(algorithmic(sh)["fwd_bytes"] + algorithmic(sh)["bwd_bytes"] for sh, _ in mods)
+    row = {"modules": len(mods), "ms_per_stack": t, "modules_per_s": len(mods) / (t * 1e-3),
+           "us_per_module": t * 1e3 / len(mods), "aggregate_algorithmic_gbs": total / (t * 1e-3) / 1e9,
+           "compose_share_of_bytes": compose / total,
+           "inputs": "device-drawn (torch Philox), seed per module; activations shared per shape"}
+    del mods, bufs
+    torch.cuda.empty_cache()
+    return row
+
+
+def attn_proj_row(dora, dev, stream, reps=20):
+    """The attention-projection module, inference path: out = in = 4096,
+    r = 64, T = 8192 bf16; factored norm then compose forward."""
+    import torch
+    sh = wl.shape("attn_proj")
+    W0, A, B, m = _device_module(sh, wl.seed_for("attn_proj"), dev)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(wl.seed_for("attn_proj") + 7)
+    base = torch.randn(sh.T, sh.out, device=dev, generator=gen).bfloat16()
+    lora = (torch.randn(sh.T, sh.out, device=dev, generator=gen) * math.sqrt(sh.r) * sh.sigma_B).bfloat16()
+    norm = torch.empty(sh.out, device=dev)
+    g = torch.empty(sh.out, device=dev)
+    y = torch.empty_like(base)
+    ws = torch.empty(dora.dora_norm_factored_workspace(sh.out, sh.inp, sh.r), dtype=torch.uint8, device=dev)
+    t_norm = _time_ms(lambda: dora.dora_norm_factored(W0, A, B, m, sh.s, norm, g, ws, stream), reps, stream)
+    t_fwd = _time_ms(lambda: dora.dora_compose_fwd(base, lora, g, sh.s, y, stream), reps, stream)
+
+    def step():
+        dora.dora_norm_factored(W0, A, B, m, sh.s, norm, g, ws, stream)
+        dora.dora_compose_fwd(base, lora, g, sh.s, y, stream)
+
+    t_step = _time_ms(step, reps, stream)
+    alg = algorithmic(sh)
+    row = {"out": sh.out, "in": sh.inp, "r": sh.r, "T": sh.T, "norm_us": t_norm * 1e3, "fwd_us": t_fwd * 1e3,
+           "fwd_gbs": alg["fwd_bytes"] / (t_fwd * 1e-3) / 1e9, "us_per_step": t_step * 1e3,
+           "norm_transient_bytes": ws.numel()}
+    del W0, A, B, m, base, lora, y, ws
+    torch.cuda.empty_cache()
+    return row
+
+
 def run_report(args):
     import torch
     import parameter_efficient_fine_gb300 as dora
@@ -467,41 +727,8 @@ def run_report(args):
     torch.cuda.set_device(dev)
     stream = torch.cuda.current_stream()
     if args.report == "rank_sweep":
-        # out = in = 8192, T = 8192 bf16: norm time, compose GB/s and the norm's
-        # whole transient (its workspace) against one dense fp32 out x in matrix
-        # the swept ranks, or any ranks given with --ranks (seeded by position)
-        for k, r in enumerate(args.ranks or wl.RANK_SWEEP):
-            sh = wl.shape("rank_sweep", r=r)
-            W0, A, B, m = _device_module(sh, wl.seed_for("rank_sweep", k), dev)
-            gen = torch.Generator(device=dev)
-            gen.manual_seed(wl.seed_for("rank_sweep", k) + 7)
-            act = [torch.randn(sh.T, sh.out, device=dev, generator=gen).bfloat16() for _ in range(3)]
-            act[1] = (act[1].float() * math.sqrt(sh.r) * sh.sigma_B).bfloat16()
-            base, lora, dy = act
-            norm = torch.empty(sh.out, device=dev)
-            g = torch.empty(sh.out, device=dev)
-            nbytes = dora.dora_norm_factored_workspace(sh.out, sh.inp, sh.r)
-            ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
-            y, db, dl = torch.empty_like(base), torch.empty_like(base), torch.empty_like(base)
-            dm = torch.empty(sh.out, device=dev)
-            wsb = torch.empty(dora.dora_compose_bwd_workspace(sh.T, sh.out), dtype=torch.uint8, device=dev)
-            t_norm = _time_ms(lambda: dora.dora_norm_factored(W0, A, B, m, sh.s, norm, g, ws, stream), 20, stream)
-            t_fwd = _time_ms(lambda: dora.dora_compose_fwd(base, lora, g, sh.s, y, stream), 20, stream)
-            t_bwd = _time_ms(lambda: dora.dora_compose_bwd(dy, base, lora, g, norm, sh.s, db, dl, dm, wsb, stream),
-                             20, stream)
-            alg = algorithmic(sh)
-            dense = sh.out * sh.inp * 4
-            print(json.dumps({"report": "rank_sweep", "r": r, "out": sh.out, "in": sh.inp, "T": sh.T,
-                              "norm_us": t_norm * 1e3,
-                              "norm_tflops_algorithmic": alg["norm_flops"] / (t_norm * 1e-3) / 1e12,
-                              "fwd_gbs": alg["fwd_bytes"] / (t_fwd * 1e-3) / 1e9,
-                              "bwd_gbs": alg["bwd_bytes"] / (t_bwd * 1e-3) / 1e9,
-                              "norm_transient_bytes": nbytes, "dense_fp32_matrix_bytes": dense,
-                              "dense_over_transient": dense / nbytes,
-                              "rank_dependent_theory": sh.out * sh.inp / (sh.out * sh.r + sh.r * sh.r)}),
-                  flush=True)
-            del W0, A, B, m, act, base, lora, dy, ws, y, db, dl
-            torch.cuda.empty_cache()
+        for row in rank_sweep_rows(dora, dev, stream, args.ranks or wl.RANK_SWEEP):
+            print(json.dumps(dict(report="rank_sweep", **row)), flush=True)
     elif args.report == "bf16_norm":
         # the factored norm with bf16 W0, A, B (the same seeded weights rounded
         # to bf16) at out = in = 8192 over the swept ranks; the row norms of W0
@@ -605,46 +832,9 @@ def run_report(args):
                           "cublas_base_matmul_us": t_gemm * 1e3,
                           "cublas_base_matmul_tflops": 2 * T * out * inp / (t_gemm * 1e-3) / 1e12}), flush=True)
     elif args.report == "mlp_stack":
-        # 32 gate/up (4096 -> 14336) + 32 down (14336 -> 4096) modules, r = 512,
-        # T = 16384, training step per module (norm + fwd + bwd), independent seeds
-        shapes = [wl.shape("mlp_gate_up"), wl.shape("mlp_down")]
-        mods = []
-        for k in range(wl.MLP_REPEATS):
-            for j, sh in enumerate(shapes):
-                mods.append((sh, _device_module(sh, wl.seed_for(sh.name, 2 * k + j), dev)))
-        bufs = {}
-        for sh in shapes:
-            gen = torch.Generator(device=dev)
-            gen.manual_seed(wl.seed_for(sh.name) + 99)
-            act = [torch.randn(sh.T, sh.out, device=dev, generator=gen).bfloat16() for _ in range(3)]
-            act[1] = (act[1].float() * math.sqrt(sh.r) * sh.sigma_B).bfloat16()
-            bufs[sh.name] = {
-                "act": act, "y": torch.empty_like(act[0]), "db": torch.empty_like(act[0]),
-                "dl": torch.empty_like(act[0]), "norm": torch.empty(sh.out, device=dev),
-                "g": torch.empty(sh.out, device=dev), "dm": torch.empty(sh.out, device=dev),
-                "ws": torch.empty(dora.dora_norm_factored_workspace(sh.out, sh.inp, sh.r), dtype=torch.uint8,
-                                  device=dev),
-                "wsb": torch.empty(dora.dora_compose_bwd_workspace(sh.T, sh.out), dtype=torch.uint8, device=dev)}
-
-        def stack():
-            for sh, (W0, A, B, m) in mods:
-                b = bufs[sh.name]
-                base, lora, dy = b["act"]
-                dora.dora_norm_factored(W0, A, B, m, sh.s, b["norm"], b["g"], b["ws"], stream)
-                dora.dora_compose_fwd(base, lora, b["g"], sh.s, b["y"], stream)
-                dora.dora_compose_bwd(dy, base, lora, b["g"], b["norm"], sh.s, b["db"], b["dl"], b["dm"], b["wsb"],
-                                      stream)
-
-        t = _time_ms(stack, 3, stream)
-        total = sum(sum(v for k, v in algorithmic(sh).items() if k.endswith("_bytes")) for sh, _ in mods)
-        compose = sum(algorithmic(sh)["fwd_bytes"] + algorithmic(sh)["bwd_bytes"] for sh, _ in mods)
-        print(json.dumps({"report": "mlp_stack", "modules": len(mods), "ms_per_stack": t,
-                          "modules_per_s": len(mods) / (t * 1e-3),
-                          "us_per_module": t * 1e3 / len(mods),
-                          "aggregate_algorithmic_gbs": total / (t * 1e-3) / 1e9,
-                          "compose_share_of_bytes": compose / total,
-                          "inputs": "device-drawn (torch Philox), seed per module; activations shared per shape"}),
-              flush=True)
+        print(json.dumps(dict(report="mlp_stack", **mlp_stack_row(dora, dev, stream))), flush=True)
+    elif args.report == "attn_proj":
+        print(json.dumps(dict(report="attn_proj", **attn_proj_row(dora, dev, stream))), flush=True)
 
 
 def main():
@@ -656,7 +846,10 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--report", choices=["rank_sweep", "mlp_stack", "bf16_norm", "norm_grad", "fused"], default=None,
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the attention-projection, rank-sweep and MLP-stack keys of the bench line")
+    ap.add_argument("--report", choices=["rank_sweep", "mlp_stack", "attn_proj", "bf16_norm", "norm_grad", "fused"],
+                    default=None,
                     help="extra per-workload report lines instead of the bench line")
     ap.add_argument("--ranks", type=lambda v: [int(x) for x in v.split(",")], default=None,
                     help="report rank_sweep: these ranks instead of the sweep; bf16_norm / norm_grad: only "

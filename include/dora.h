@@ -83,10 +83,15 @@ size_t dora_norm_factored_workspace(int64_t out, int64_t in, int64_t r);
  *     n_i^2 = ||W0_i||^2 + 2 s <U_i, B_i> + s^2 B_i G B_i^T,
  *     U = W0 A^T [out,r],  G = A A^T [r,r],
  * so the out x in adapted weight is never formed.  The contractions run on the
- * tensor cores with every fp32 operand split as x = hi + lo (hi = x rounded to
- * TF32): hi*hi in one TF32 MMA, lo*hi + hi*lo in one bf16 MMA, fp32
- * accumulation (relative error ~2^-19 per product); n^2 is clamped at 0 before
- * the square root; g is an IEEE division with no epsilon (n = 0 gives inf/NaN).
+ * tensor cores with every fp32 operand split as x = h + l (h = bf16(x),
+ * l = bf16(x - h)): each product as three bf16 products h*h + l*h + h*l with
+ * fp32 accumulation (dropped terms <= 3 * 2^-18 of the product); n^2 is
+ * clamped at 0 before the square root; g is an IEEE division with no epsilon
+ * (n = 0 gives inf/NaN).  Two launches (the split of A, then one cooperative
+ * launch with one CTA per SM whose CTAs wait on one another through counters
+ * in the workspace); a device that cannot hold every CTA at once gets
+ * DORA_ERR_CUDA.  Plans and encoded tensor maps are cached per shape and per
+ * buffer set, so repeated calls cost a few microseconds of host time.
  *
  *   W0    float32 [out, in]    16-byte aligned, in % 4 == 0
  *   A     float32 [r, in]      16-byte aligned

@@ -11,40 +11,45 @@
 //     n_i^2 = ||W0_i||^2 + 2 s <B_i, D_i>
 // so U never reaches global memory; only G (r x r) does.
 //
-// Launch sequence of dora_norm_factored:
-//   1. split_n_kernel    A -> (A_hi, A_c), the split N operand (see Precision)
-//   2. tc_gemm (GRAM)    partial tiles of G = A A^T, stream-K over K = in
-//   3. gram_reduce       fixed-order sum of the partial tiles, scaled by s/2, split
-//   4. tc_gemm (NORM)    [W0 | B] x [A | sG/2]^T, stream-K; per segment the epilogue
-//                        reduces each row to (sum W0_i^2 over its K range, <B_i, D_i>);
-//                        the epilogue warp that writes the last segment of a quarter
-//                        M tile sums its rows' segments in a fixed order and writes
-//                        n = sqrt(max(0, n^2)) and g = m / n
+// Launch sequence of dora_norm_factored (the forward norm):
+//   1. split_hl_kernel   A -> bf16 (A_h, A_l), the split N operand (see
+//                        Precision); zeroes the launch's counters
+//   2. fwd_norm_kernel   one cooperative launch: the Gram pieces of G = A A^T,
+//                        their reduction into s/2 G (split like A), and the
+//                        norm GEMM [W0 | B] x [A | s/2 G]^T whose epilogue
+//                        reduces each row to (sum W0_i^2 over its K range,
+//                        <B_i, D_i>); the epilogue warp that writes the last
+//                        records of a quarter M tile sums them in a fixed
+//                        order and writes n = sqrt(max(0, n^2)) and g = m / n
+// (structure and work split: see the comment above fwd_norm_kernel)
 //
-// Precision: every fp32 operand is split x = hi + lo, hi = x rounded to TF32
-// (nearest, ties away), lo = x - hi exactly, |lo| <= 2^-11 |x|.  Each product
-// is evaluated as
-//     x*y ~ hi_x*hi_y            one kind::tf32 MMA (exact products)
-//         + lo_x*hi_y + hi_x*lo_y  one kind::f16 MMA on bf16 operands, the two
-//                                  terms side by side along K (K = 16 = 8 + 8)
-// with fp32 accumulation in tensor memory.  The correction terms are ~2^-11 of
-// the product, so their bf16 rounding costs <= 2^-19 of it; lo*lo (2^-22) is
-// dropped.  Against three TF32 passes this issues 2/3 of the tensor work.
-// The M-side operand (W0 or B) is split by converter warps, which read the raw
-// box from shared memory, accumulate ||W0_i||^2 on the way and write the split
-// operand into tensor memory, where the MMAs take their A operand; the N-side
-// operand is split once in global memory (it is re-read by every M tile) into
-// a TF32 matrix and a bf16 matrix holding, per group of 8 K indices, 8 hi
-// values then 8 lo values.  The M-side correction holds lo then hi per group,
-// so the K-concatenated bf16 MMA yields lo_x*hi_y + hi_x*lo_y.
+// Precision of the forward norm: every fp32 operand is split x = h + l,
+// h = bf16(x) and l = bf16(x - h) (nearest even; x - h is exact in fp32, so
+// |x - h - l| <= 2^-18 |x|).  Each product is three kind::f16 MMAs on bf16
+// operands,
+//     x*y ~ h_x*h_y + l_x*h_y + h_x*l_y
+// with fp32 accumulation in tensor memory; every bf16 x bf16 product is exact
+// in fp32, and the dropped l_x*l_y and residual terms are <= 3 * 2^-18 of the
+// product.  The M-side operand (W0, B or A) is split by converter warps, which
+// read the raw box from shared memory, accumulate ||W0_i||^2 on the way and
+// write h and l into tensor memory, where the MMAs take their A operand; the
+// N-side operand (A, re-read by every M tile, and s/2 G) is split once in
+// global memory.
+//
+// The gradient through the norm (dora_norm_factored_bwd) uses tc_gemm_kernel
+// with an older scheme: hi = x rounded to TF32, lo = x - hi; hi*hi in one
+// kind::tf32 MMA and lo*hi + hi*lo in one kind::f16 MMA with the two terms
+// side by side along K (the N side split once in global memory into a TF32
+// matrix and a bf16 matrix holding, per group of 8 K indices, 8 hi then 8 lo
+// values; the M-side correction holds lo then hi per group).
 //
 // tc_gemm structure (one CTA per SM, persistent, 192 threads):
 //   warp 0      TMA producer: loads the raw M-side box [128 x BK fp32] and the
 //               N-side hi/lo boxes of each K block into a ring of stages
 //   warp 1      allocates tensor memory; one lane issues tcgen05.mma
 //   warps 2..5  converters (hi/lo split of the M-side box into the stage's
-//               tensor-memory slot, row sums of W0^2), then the epilogue for
-//               their 32 tensor-memory lanes each
+//               tensor-memory slot), then the epilogue for their 32
+//               tensor-memory lanes each
 // Tiles in shared memory are K-major with the swizzle of one K block per row:
 // BK = 16 fp32 (64-byte swizzle) or, for N chunks up to 128, BK = 32 (128-byte
 // swizzle).  Tensor memory holds the accumulator and one operand slot per
@@ -53,11 +58,12 @@
 // ("segment") leaves one partial result.  All partial sums are combined in a
 // fixed order, so results are bitwise reproducible.
 //
-// Every wait on a shared-memory barrier is bounded (kWaitLimitNs).  A wait that
-// gives up sets a CTA abort flag, records a code in a device error word and
-// makes all roles leave their loops; the producer then waits (bounded) for its
-// copies in flight, the MMA lane for its issued MMAs, and tensor memory is
-// freed before the CTA exits.
+// Every wait on a shared-memory barrier (and, in fwd_norm_kernel, on a global
+// counter) is bounded (kWaitLimitNs).  A wait that gives up sets a CTA abort
+// flag, records a code in a device error word and makes all roles leave their
+// loops; the producers then wait (bounded) for their copies in flight, the
+// MMA lane for its issued MMAs, and tensor memory is freed before the CTA
+// exits.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>

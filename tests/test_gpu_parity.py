@@ -73,6 +73,9 @@ def test_attention_projection_reduced_tokens():
     (1, 16, 2, 1),             # a single output row, a single token
     (300, 1040, 128, 50),      # N = 128, the widest chunk with 32-wide K blocks; K tail of 16
     (260, 200, 129, 30),       # N = 144: 16-wide K blocks again; K tail of 8
+    (64, 8, 1024, 5),          # the largest rank: 36 Gram tiles of one K piece each, more Gram tiles than
+                               # norm units per CTA, three N chunks of 352
+    (2048, 64, 1024, 12),      # the largest rank with 152 CTAs, 36 of them Gram CTAs
 ])
 def test_shapes_span_tiles_and_ragged_tails(out, inp, r, T):
     sh = wl.shape("high_rank", out=out, inp=inp, r=r, T=T)
@@ -219,4 +222,31 @@ def test_g_near_one_stress_keeps_base_correction():
     print(f"g~1 stress: correctly rounded match stable={stable_frac:.5f} naive={naive_frac:.5f}")
     assert stable_frac >= 0.999
     assert naive_frac < stable_frac
+    assert_no_device_error()
+
+
+def test_norm_caches_across_shapes_and_buffers():
+    # The library caches plans per shape and encoded tensor maps per buffer
+    # set.  Interleaved calls on two shapes and two buffer sets per shape must
+    # each give what the first call on that shape and buffer set gave
+    # (bitwise) and what the oracle gives.
+    cases = []
+    for k, (out, inp, r) in enumerate([(640, 512, 96), (384, 1024, 40)]):
+        sh = wl.shape("high_rank", out=out, inp=inp, r=r, T=1)
+        for j in range(2):
+            w = wl.make_weights(sh, 8100 + 10 * k + j)
+            dev = _weights_dev(w)
+            n_ref, g_ref = oracle.weight_norm(w["W0"], w["A"], w["B"], w["m"], w["s"])
+            cases.append((dev, w["s"], n_ref, g_ref))
+    first = {}
+    for rep in range(3):
+        for i in (0, 2, 1, 3):
+            (W0, A, B, m), s, n_ref, g_ref = cases[i]
+            norm, g = run_norm(W0, A, B, m, s)
+            if rep == 0:
+                check_rel("norm", to_f64(norm), n_ref)
+                check_rel("g", to_f64(g), g_ref)
+                first[i] = (norm.clone(), g.clone())
+            else:
+                assert torch.equal(norm, first[i][0]) and torch.equal(g, first[i][1])
     assert_no_device_error()

@@ -178,7 +178,8 @@ size_t dora_norm_factored_bwd_workspace(int64_t out, int64_t in, int64_t r);
  *   dA = s (c (.) B)^T W0 + s^2 H A,       H = B^T diag(c) B
  *
  * evaluated in factored form (the out x in matrix V is never formed) on the
- * tensor cores with the same split-TF32 precision as dora_norm_factored.
+ * tensor cores with the same bf16 three-product split (x = h + l, each
+ * product h h + l h + h l, fp32 accumulation) as dora_norm_factored.
  * The outputs are ONLY the norm's share: the caller adds the gradients of its
  * own lora = x A^T B^T product.  dA and dB are overwritten.
  *

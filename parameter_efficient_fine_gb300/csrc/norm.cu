@@ -36,24 +36,21 @@
 // N-side operand (A, re-read by every M tile, and s/2 G) is split once in
 // global memory.
 //
-// The gradient through the norm (dora_norm_factored_bwd) uses tc_gemm_kernel
-// with an older scheme: hi = x rounded to TF32, lo = x - hi; hi*hi in one
-// kind::tf32 MMA and lo*hi + hi*lo in one kind::f16 MMA with the two terms
-// side by side along K (the N side split once in global memory into a TF32
-// matrix and a bf16 matrix holding, per group of 8 K indices, 8 hi then 8 lo
-// values; the M-side correction holds lo then hi per group).
+// The gradient through the norm (dora_norm_factored_bwd) runs the same
+// scheme in tc_gemm_kernel, four passes of separate launches.
 //
 // tc_gemm structure (one CTA per SM, persistent, 192 threads):
-//   warp 0      TMA producer: loads the raw M-side box [128 x BK fp32] and the
-//               N-side hi/lo boxes of each K block into a ring of stages
+//   warp 0      TMA producer: loads the raw M-side box [128 x 32 fp32] and the
+//               N-side h / l boxes [NC x 32 bf16] of each K block into a ring
+//               of stages
 //   warp 1      allocates tensor memory; one lane issues tcgen05.mma
-//   warps 2..5  converters (hi/lo split of the M-side box into the stage's
+//   warps 2..5  converters (h / l split of the M-side box into the stage's
 //               tensor-memory slot), then the epilogue for their 32
 //               tensor-memory lanes each
 // Tiles in shared memory are K-major with the swizzle of one K block per row:
-// BK = 16 fp32 (64-byte swizzle) or, for N chunks up to 128, BK = 32 (128-byte
-// swizzle).  Tensor memory holds the accumulator and one operand slot per
-// stage.  The work is the list of (M tile, N chunk, K block) units, split evenly over the
+// the raw fp32 box 128-byte rows (128-byte swizzle), the bf16 N-side boxes
+// 64-byte rows (64-byte swizzle).  Tensor memory holds the accumulator and one
+// operand slot per stage.  The work is the list of (M tile, N chunk, K block) units, split evenly over the
 // CTAs; a CTA's range crosses at most a few tile boundaries, and each piece
 // ("segment") leaves one partial result.  All partial sums are combined in a
 // fixed order, so results are bitwise reproducible.
@@ -79,15 +76,10 @@
 namespace {
 
 constexpr int kBM = 128;            // rows per M tile (= tensor-memory lanes)
-// fp32 per K block: 16 (64-byte rows, 64-byte swizzle) or 32 (128-byte rows,
-// 128-byte swizzle).  The wider block is taken where the stage still fits
-// several times into shared memory (N chunks up to kMaxChunkWide): TMA streams
-// a large matrix from HBM faster through 128-byte box rows than through
-// 64-byte ones (measured 4.5 vs 3.8 TB/s on GB300), and each stage carries
-// twice the work per barrier round trip.
-constexpr int kBKNarrow = 16;
-constexpr int kBKWide = 32;
-constexpr int kMaxChunkWide = 128;
+// K indices per K block of tc_gemm_kernel: one 128-byte fp32 row of the raw
+// M-side box (TMA streams a large matrix from HBM faster through 128-byte box
+// rows than through 64-byte ones: measured 4.5 vs 3.8 TB/s on GB300)
+constexpr int kBK = 32;
 constexpr int kThreads = 192;
 constexpr int kMaxChunkN = 384;     // largest N handled by one CTA pass
 constexpr int kMaxR = 1024;
@@ -126,7 +118,7 @@ struct TcParams {
   int sym;          // Gram pass: only tiles with N chunk >= M tile (G is symmetric; both 128 wide)
   int NC;           // N per chunk (multiple of 16, <= kMaxChunkN)
   int nbox;         // rows per N-side TMA box
-  int nb;           // N-side boxes per stage (per hi / correction)
+  int nb;           // N-side boxes per stage (per h / l operand)
   int NT;           // N-side rows in shared memory per stage (nb * nbox >= NC)
   int nmma0, nmma1; // N of the first / second MMA instruction of a chunk
   int tmem_cols;
@@ -212,15 +204,16 @@ __device__ void wait_drain(uint32_t bar, uint32_t parity) { wait_drain_ns(bar, p
 // loads an unswizzled [BK x 128] box and the converters read it column-wise
 // (lane = M row, conflict-free), the rest is unchanged.
 // ---------------------------------------------------------------------------
-template <int BK, bool XT>
+template <bool XT>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_gemm_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ CUtensorMap mX2,
-               const __grid_constant__ CUtensorMap mY1h, const __grid_constant__ CUtensorMap mY1c,
-               const __grid_constant__ CUtensorMap mY2h, const __grid_constant__ CUtensorMap mY2c,
+               const __grid_constant__ CUtensorMap mY1h, const __grid_constant__ CUtensorMap mY1l,
+               const __grid_constant__ CUtensorMap mY2h, const __grid_constant__ CUtensorMap mY2l,
                const TcParams p) {
-  constexpr int kRowBytes = BK * 4;   // one swizzle span of the raw fp32 M-side box
-  constexpr int kNRowBytes = BK * 4;  // one N-side row: BK TF32 hi / BK bf16 pairs
-  constexpr int kSlotCols = 2 * BK;   // tensor-memory columns of one M-side operand slot
+  constexpr int BK = kBK;
+  constexpr int kRowBytes = BK * 4;    // one swizzle span of the raw fp32 M-side box
+  constexpr int kNRowBytes = BK * 2;   // one N-side row of BK bf16 (h or l)
+  constexpr int kSlotCols = BK;        // tensor-memory columns of one M-side operand slot (h, then l)
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int S = p.stages;
@@ -252,11 +245,11 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ 
   if (warp == 0 && lane == 0) {
     prefetch_map(&mX1);
     prefetch_map(&mY1h);
-    prefetch_map(&mY1c);
+    prefetch_map(&mY1l);
     if (p.kbtot > p.kb1) {
       prefetch_map(&mX2);
       prefetch_map(&mY2h);
-      prefetch_map(&mY2c);
+      prefetch_map(&mY2l);
     }
   }
   if (warp == 1) {
@@ -295,18 +288,18 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ 
           mbar_expect_tx(fb, p.tx_bytes);
           const uint32_t xs = smem_u32(smem + static_cast<size_t>(stage) * p.stage_bytes);
           const uint32_t yh = xs + kBM * kRowBytes;
-          const uint32_t yc = yh + static_cast<uint32_t>(p.NT) * kNRowBytes;
+          const uint32_t yl = yh + static_cast<uint32_t>(p.NT) * kNRowBytes;
           const bool seg1 = kb < p.kb1;
           const int kx = (seg1 ? kb : kb - p.kb1) * BK;    // first K index of the block
           if (XT) tma_load_2d(xs, seg1 ? &mX1 : &mX2, mt * kBM, kx, fb);
           else tma_load_2d(xs, seg1 ? &mX1 : &mX2, kx, mt * kBM, fb);
-          // the N-side tile of the chunk: TF32 hi and bf16 correction operands
+          // the N-side tile of the chunk: the bf16 h and l operands
           for (int i = 0; i < p.nb; ++i) {
             const int ro = i * p.nbox;
             const int ny = nc * p.NC + ro;
             const uint32_t off = static_cast<uint32_t>(ro * kNRowBytes);
             tma_load_2d(yh + off, seg1 ? &mY1h : &mY2h, kx, ny, fb);
-            tma_load_2d(yc + off, seg1 ? &mY1c : &mY2c, 2 * kx, ny, fb);   // bf16 column
+            tma_load_2d(yl + off, seg1 ? &mY1l : &mY2l, kx, ny, fb);
           }
           ++issued;
           if (++stage == S) {
@@ -336,8 +329,6 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ 
       uint32_t phase = 0;
       uint32_t aphase = 0;
       bool ok = true;
-      const uint32_t id0 = idesc_tf32(p.nmma0);
-      const uint32_t id1 = p.nmma1 > 0 ? idesc_tf32(p.nmma1) : 0u;
       const uint32_t ic0 = idesc_bf16(p.nmma0);
       const uint32_t ic1 = p.nmma1 > 0 ? idesc_bf16(p.nmma1) : 0u;
       for (long long u = u_begin; u < u_end && ok;) {
@@ -356,29 +347,29 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ 
           }
           tc_fence_after();
           const uint32_t yh = smem_u32(smem + static_cast<size_t>(stage) * p.stage_bytes) + kBM * kRowBytes;
-          const uint32_t yc = yh + static_cast<uint32_t>(p.NT) * kNRowBytes;
-          // M-side operand slot of this stage in tensor memory: BK columns of
-          // hi (one fp32 per column), then BK/8 groups of 8 columns holding the
-          // group's 16 bf16 correction values (two per column)
-          const uint32_t ah0 = tmem + static_cast<uint32_t>(p.slot0 + stage * kSlotCols);
-          const uint32_t ac0 = ah0 + BK;
+          const uint32_t yl = yh + static_cast<uint32_t>(p.NT) * kNRowBytes;
+          // M-side operand slot: BK/2 columns of h (two bf16 per column,
+          // K-consecutive), then BK/2 columns of l.  Per K = 16 step three
+          // products h_x h_y + l_x h_y + h_x l_y into the same accumulator.
+          const uint32_t sh = tmem + static_cast<uint32_t>(p.slot0 + stage * kSlotCols);
+          const uint32_t sl = sh + BK / 2;
 #pragma unroll
-          for (int k = 0; k < BK / 8; ++k) {
+          for (int k = 0; k < BK / 16; ++k) {
             const uint32_t acc0 = (kb != kb0 || k != 0) ? 1u : 0u;
-            // K step k: 8 tf32 (32 bytes) of the hi operands, 16 bf16 (32 bytes)
-            // of the correction operands
-            const uint32_t ko = static_cast<uint32_t>(k) * 32u;
-            const uint32_t ah = ah0 + 8u * k, ac = ac0 + 8u * k;
+            const uint32_t ko = static_cast<uint32_t>(k) * 32u;   // 16 bf16 along the 64-byte row
+            const uint32_t ah = sh + 8u * k, al = sl + 8u * k;
             {
-              const uint64_t bh = sdesc<BK>(yh + ko), bc = sdesc<BK>(yc + ko);
-              mma_bf16_ta(tmem, ac, bc, ic0, acc0);
-              mma_tf32_ta(tmem, ah, bh, id0, 1u);
+              const uint64_t bh = sdesc<BK / 2>(yh + ko), bl = sdesc<BK / 2>(yl + ko);
+              mma_bf16_ta(tmem, ah, bh, ic0, acc0);
+              mma_bf16_ta(tmem, al, bh, ic0, 1u);
+              mma_bf16_ta(tmem, ah, bl, ic0, 1u);
             }
             if (p.nmma1 > 0) {
-              const uint32_t no = 256u * kRowBytes;
-              const uint64_t bh = sdesc<BK>(yh + no + ko), bc = sdesc<BK>(yc + no + ko);
-              mma_bf16_ta(tmem + 256u, ac, bc, ic1, acc0);
-              mma_tf32_ta(tmem + 256u, ah, bh, id1, 1u);
+              const uint32_t no = 256u * kNRowBytes;
+              const uint64_t bh = sdesc<BK / 2>(yh + no + ko), bl = sdesc<BK / 2>(yl + no + ko);
+              mma_bf16_ta(tmem + 256u, ah, bh, ic1, acc0);
+              mma_bf16_ta(tmem + 256u, al, bh, ic1, 1u);
+              mma_bf16_ta(tmem + 256u, ah, bl, ic1, 1u);
             }
           }
           mma_commit(empty0 + 8u * stage);
@@ -421,9 +412,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ 
           break;
         }
         // this thread's row: BK fp32 in BK/4 16-byte chunks, stored swizzled
-        // (swz_chunk); one group of 8 K indices at a time, split into the
-        // tensor-memory operand slot of the stage: 8 hi columns and 8 columns
-        // of bf16 pairs (lo then hi) per group
+        // (swz_chunk); one K = 16 step at a time, split into the stage's
+        // tensor-memory operand slot: 8 columns of h pairs and 8 of l pairs
         const uint8_t *xbox = smem + static_cast<size_t>(stage) * p.stage_bytes;
         const float4 *xr = reinterpret_cast<const float4 *>(xbox + row * kRowBytes);
         const float *xc = reinterpret_cast<const float *>(xbox) + row;   // XT: column `row` of [BK][128]
@@ -438,24 +428,26 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ 
             v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
           }
         };
+        // x = h + l: h = bf16(x), l = bf16(x - h); column c of a step holds
+        // the K indices 2c, 2c + 1
 #pragma unroll
-        for (int q = 0; q < BK / 8; ++q) {
-          float v[8];
-          load8(q, v);
-          uint32_t hb[8], cb[8];
-          float l[8];
+        for (int q16 = 0; q16 < BK / 16; ++q16) {
+          uint32_t hb[8], lb[8];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            hb[e] = tf32_rna(v[e]);
-            l[e] = v[e] - __uint_as_float(hb[e]);
+          for (int half = 0; half < 2; ++half) {
+            float v[8];
+            load8(2 * q16 + half, v);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float x0 = v[2 * e], x1 = v[2 * e + 1];
+              const uint32_t h = pack_bf16x2(x0, x1);
+              hb[4 * half + e] = h;
+              lb[4 * half + e] =
+                  pack_bf16x2(x0 - __uint_as_float(h << 16), x1 - __uint_as_float(h & 0xffff0000u));
+            }
           }
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            cb[e] = pack_bf16x2(l[2 * e], l[2 * e + 1]);
-            cb[4 + e] = pack_bf16x2(__uint_as_float(hb[2 * e]), __uint_as_float(hb[2 * e + 1]));
-          }
-          tmem_st8(slot + 8u * q, hb);
-          tmem_st8(slot + BK + 8u * q, cb);
+          tmem_st8(slot + 8u * q16, hb);
+          tmem_st8(slot + BK / 2 + 8u * q16, lb);
         }
         tmem_wait_st();
         // the tensor-memory stores are complete (wait::st); order them before
@@ -1255,33 +1247,6 @@ fwd_norm_kernel(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
 //   c  [rows, 2*cols8] bf16 (cols8 = cols rounded up to 8): per group q of 8
 //      columns, 8 bf16(hi) then 8 bf16(x - hi); zero past cols
 // One thread per group of 4 columns.
-__global__ void __launch_bounds__(256) split_n_kernel(const float *__restrict__ x, long long rows, int cols,
-                                                      int cols8, float *__restrict__ hi,
-                                                      __nv_bfloat16 *__restrict__ c, int *__restrict__ cnt,
-                                                      int ncnt) {
-  // the norm pass's completion counters start at zero
-  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < ncnt; i += gridDim.x * blockDim.x) cnt[i] = 0;
-  const int g4 = cols8 / 4;
-  const long long n = rows * g4;
-  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
-    const long long row = i / g4;
-    const int k = static_cast<int>(i - row * g4) * 4;   // first column of the group of 4
-    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (k < cols) v = __ldg(reinterpret_cast<const float4 *>(x + row * cols + k));
-    float4 h;
-    h.x = __uint_as_float(tf32_rna(v.x));
-    h.y = __uint_as_float(tf32_rna(v.y));
-    h.z = __uint_as_float(tf32_rna(v.z));
-    h.w = __uint_as_float(tf32_rna(v.w));
-    if (k < cols) *reinterpret_cast<float4 *>(hi + row * cols + k) = h;
-    const long long cbase = row * 2LL * cols8 + 16LL * (k / 8) + (k % 8);
-    uint2 hb = make_uint2(pack_bf16x2(h.x, h.y), pack_bf16x2(h.z, h.w));
-    uint2 lb = make_uint2(pack_bf16x2(v.x - h.x, v.y - h.y), pack_bf16x2(v.z - h.z, v.w - h.w));
-    *reinterpret_cast<uint2 *>(c + cbase) = hb;
-    *reinterpret_cast<uint2 *>(c + cbase + 8) = lb;
-  }
-}
-
 // N-side split of a [rows, cols] fp32 matrix for the bf16 three-product
 // scheme, and zero fill of the norm pass's ncnt completion counters:
 //   h [rows, cols8] bf16: x rounded to bf16 (nearest even)
@@ -1327,15 +1292,14 @@ struct StreamK {
   int ncl, kbtot, maxseg;
 };
 
-// Gs[k][l] = (s/2) * G[k][l] for k, l < r (zero-padded to npad), split like
-// split_n_kernel: gh [npad, npad] TF32, gc [npad, 2*npad] bf16 (8 hi, 8 lo per group)
-__device__ __forceinline__ void store_gs(int a, int b, float v, int npad, float *gh, __nv_bfloat16 *gc) {
+// entry (a, b) of a Gram result v, zero-padded to [npad, npad] and split for
+// the N side: h [npad, npad] = bf16(v), l [npad, npad] = bf16(v - h)
+__device__ __forceinline__ void store_gs_hl(int a, int b, float v, int npad, __nv_bfloat16 *gh, __nv_bfloat16 *gl) {
   if (a >= npad || b >= npad) return;
-  const float h = __uint_as_float(tf32_rna(v));
-  gh[static_cast<long long>(a) * npad + b] = h;
-  const long long cb = static_cast<long long>(a) * 2 * npad + 16 * (b / 8) + (b % 8);
-  gc[cb] = __float2bfloat16_rn(h);
-  gc[cb + 8] = __float2bfloat16_rn(v - h);
+  const __nv_bfloat16 h = __float2bfloat16_rn(v);
+  const long long i = static_cast<long long>(a) * npad + b;
+  gh[i] = h;
+  gl[i] = __float2bfloat16_rn(v - __bfloat162float(h));
 }
 
 // One 32 x 32 block of an upper-triangular Gram tile (blockIdx.x = tile, whose
@@ -1345,9 +1309,11 @@ __device__ __forceinline__ void store_gs(int a, int b, float v, int npad, float 
 // the 8 warp sums are then added in warp order.  The block is written at
 // (k, l) and, for a tile off the diagonal, mirrored at (l, k) through shared
 // memory, so both writes are coalesced.
+// The result is written split, as the bf16 h and l [npad, npad] (store_gs_hl).
 __global__ void __launch_bounds__(256) gram_reduce_kernel(const float *__restrict__ part, StreamK sk, int nchunks,
                                                           int NC, int r, int npad, float half_s,
-                                                          float *__restrict__ gh, __nv_bfloat16 *__restrict__ gc) {
+                                                          __nv_bfloat16 *__restrict__ gh, __nv_bfloat16 *__restrict__ gl) {
+  auto store = [&](int a, int b, float v) { store_gs_hl(a, b, v, npad, gh, gl); };
   __shared__ float wsum[8][32][33];
   const int t = blockIdx.x;
   int mt, nc;
@@ -1390,7 +1356,7 @@ __global__ void __launch_bounds__(256) gram_reduce_kernel(const float *__restric
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     const int i = ty + 8 * q;
-    store_gs(mt * kBM + sr * 32 + i, nc * NC + col, v[q], npad, gh, gc);
+    store(mt * kBM + sr * 32 + i, nc * NC + col, v[q]);
     wsum[0][i][tx] = v[q];
   }
   if (mt != nc) {
@@ -1398,7 +1364,7 @@ __global__ void __launch_bounds__(256) gram_reduce_kernel(const float *__restric
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       const int i = ty + 8 * q;
-      store_gs(nc * NC + sc * 32 + i, mt * kBM + sr * 32 + tx, wsum[0][tx][i], npad, gh, gc);
+      store(nc * NC + sc * 32 + i, mt * kBM + sr * 32 + tx, wsum[0][tx][i]);
     }
   }
 }
@@ -1415,14 +1381,14 @@ __global__ void __launch_bounds__(256) gram_reduce_kernel(const float *__restric
 // [(s c B)^T | s^2 H]^T over K = out + r, its M-side operands read transposed.
 // ---------------------------------------------------------------------------
 
-// Y = (s c (.) B)^T [r, out8] split like split_n_kernel: hi [r, out8] TF32 and
-// c [r, 2*out8] bf16 (per group of 8 columns: 8 hi, then 8 lo); columns
-// out..out8-1 are zero.  32 x 32 tiles transposed through shared memory.
+// Y = (s c (.) B)^T [r, out8], columns out..out8-1 zero, split for the N side
+// like split_hl_kernel: h and l [r, out8] bf16.  32 x 32 tiles transposed
+// through shared memory.
 __global__ void __launch_bounds__(256) bs_split_kernel(const float *__restrict__ B, long long out, int r,
                                                        long long out8, const float *__restrict__ g,
                                                        const float *__restrict__ d_mag,
                                                        const float *__restrict__ norm, float s,
-                                                       float *__restrict__ hi, __nv_bfloat16 *__restrict__ c) {
+                                                       __nv_bfloat16 *__restrict__ yh, __nv_bfloat16 *__restrict__ yl) {
   __shared__ float tile[32][33];
   const long long i0 = static_cast<long long>(blockIdx.x) * 32;
   const int n0 = static_cast<int>(blockIdx.y) * 32;
@@ -1442,11 +1408,10 @@ __global__ void __launch_bounds__(256) bs_split_kernel(const float *__restrict__
     const long long i = i0 + tx;
     if (n < r && i < out8) {
       const float x = tile[tx][ty + 8 * q];
-      const float h = __uint_as_float(tf32_rna(x));
-      hi[static_cast<long long>(n) * out8 + i] = h;
-      const long long cb = static_cast<long long>(n) * 2 * out8 + 16 * (i / 8) + (i % 8);
-      c[cb] = __float2bfloat16_rn(h);
-      c[cb + 8] = __float2bfloat16_rn(x - h);
+      const long long o = static_cast<long long>(n) * out8 + i;
+      const __nv_bfloat16 h = __float2bfloat16_rn(x);
+      yh[o] = h;
+      yl[o] = __float2bfloat16_rn(x - __bfloat162float(h));
     }
   }
 }
@@ -1950,7 +1915,6 @@ __global__ void __launch_bounds__(256) gram_reduce3_kernel(const float *__restri
 // ---------------------------------------------------------------------------
 struct GemmPlan {
   TcParams p;
-  int bk;   // K indices per K block (the kernel instance)
   bool xt;  // M-side operand stored transposed (the kernel instance)
   size_t smem_bytes;
   size_t part_bytes;
@@ -1984,10 +1948,10 @@ bool plan_gemm(int mode, int M, int64_t in, int r, int max_ctas, GemmPlan *gp) {
     p.nchunks = static_cast<int>(dora::ceil_div(npad, p.NC));
     p.sym = 1;
   }
-  gp->bk = p.NC <= kMaxChunkWide ? kBKWide : kBKNarrow;
-  const int row_bytes = gp->bk * 4;   // the raw fp32 M-side box and each N-side operand
-  p.kb1 = static_cast<int>(dora::ceil_div(in, gp->bk));
-  p.kbtot = p.kb1 + (mode != kGram ? static_cast<int>(dora::ceil_div(r, gp->bk)) : 0);
+  const int row_bytes = kBK * 4;    // the raw fp32 M-side box
+  const int nrow_bytes = kBK * 2;   // each bf16 N-side operand
+  p.kb1 = static_cast<int>(dora::ceil_div(in, kBK));
+  p.kbtot = p.kb1 + (mode != kGram ? static_cast<int>(dora::ceil_div(r, kBK)) : 0);
   // the N-side tile in nb boxes of nbox rows (a multiple of 8, so every box
   // starts on a swizzle-pattern boundary)
   p.nb = static_cast<int>(dora::ceil_div(p.NC, 128));
@@ -1996,13 +1960,12 @@ bool plan_gemm(int mode, int M, int64_t in, int r, int max_ctas, GemmPlan *gp) {
   p.nmma0 = p.NC <= 256 ? p.NC : 256;
   p.nmma1 = p.NC - p.nmma0;
   // tensor memory: the accumulator (nmma0 columns at 0, nmma1 at 256), then one
-  // M-side operand slot of 2 * bk columns (TF32 hi and bf16 pairs) per stage
+  // M-side operand slot per stage (kBK columns: bf16 h pairs, then l pairs)
   const int acc_cols = static_cast<int>(dora::round_up(p.nmma1 > 0 ? 256 + p.nmma1 : p.nmma0, 32));
-  const int slot_cols = 2 * gp->bk;
+  const int slot_cols = kBK;
   p.slot0 = acc_cols;
-  // a stage in shared memory: the raw M-side box, then the N-side hi and
-  // correction tiles
-  p.stage_bytes = static_cast<unsigned>(kBM * row_bytes + 2 * p.NT * row_bytes);
+  // a stage in shared memory: the raw M-side box, then the two N-side tiles
+  p.stage_bytes = static_cast<unsigned>(kBM * row_bytes + 2 * p.NT * nrow_bytes);
   p.tx_bytes = p.stage_bytes;
   p.stages = static_cast<int>((kSmemMax - 1024 - 512) / p.stage_bytes);
   if (p.stages > kMaxStages) p.stages = kMaxStages;
@@ -2244,8 +2207,9 @@ struct BwdPlans {
   GemmPlan gb;   // dB rows (M = out, K = in + r)
   GemmPlan ga;   // dA^T rows (M = in, K = out + r; W0 and A read transposed)
 };
+// the N-side operands of the four passes, each a bf16 h / l pair
 struct BwdLayout {
-  size_t a_hi, a_c, y_hi, y_c, g_hi, g_c, h_hi, h_c, part_t, part_r, b_pad, total;
+  size_t a_h, a_l, y_h, y_l, g_h, g_l, h_h, h_l, part_t, part_r, b_pad, total;
 };
 
 bool plan_bwd(int64_t out, int64_t in, int64_t r, int sms, BwdPlans *P, BwdLayout *L) {
@@ -2256,8 +2220,8 @@ bool plan_bwd(int64_t out, int64_t in, int64_t r, int sms, BwdPlans *P, BwdLayou
   if (!plan_gemm(kRows, static_cast<int>(in), out, ri, sms, &P->ga)) return false;
   P->gh.xt = true;
   P->ga.xt = true;
-  P->gb.p.chain = kChainK / P->gb.bk;
-  P->ga.p.chain = kChainK / P->ga.bk;
+  P->gb.p.chain = kChainK / kBK;
+  P->ga.p.chain = kChainK / kBK;
   int npad, nchunks, NC;
   plan_n(ri, &npad, &nchunks, &NC);
   const size_t out8 = static_cast<size_t>(dora::round_up(out, 8));
@@ -2267,14 +2231,15 @@ bool plan_bwd(int64_t out, int64_t in, int64_t r, int sms, BwdPlans *P, BwdLayou
     off += al256(bytes);
     return o;
   };
-  L->a_hi = take(static_cast<size_t>(r) * in * 4);
-  L->a_c = take(static_cast<size_t>(r) * dora::round_up(in, 8) * 4);   // bf16 [r, 2*in8]
-  L->y_hi = take(static_cast<size_t>(r) * out8 * 4);
-  L->y_c = take(static_cast<size_t>(r) * out8 * 4);                    // bf16 [r, 2*out8]
-  L->g_hi = take(static_cast<size_t>(npad) * npad * 4);
-  L->g_c = take(static_cast<size_t>(npad) * npad * 4);
-  L->h_hi = take(static_cast<size_t>(npad) * npad * 4);
-  L->h_c = take(static_cast<size_t>(npad) * npad * 4);
+  const size_t in8 = static_cast<size_t>(dora::round_up(in, 8));
+  L->a_h = take(static_cast<size_t>(r) * in8 * 2);     // A: bf16 [r, in8] each
+  L->a_l = take(static_cast<size_t>(r) * in8 * 2);
+  L->y_h = take(static_cast<size_t>(r) * out8 * 2);    // (s c B)^T: bf16 [r, out8] each
+  L->y_l = take(static_cast<size_t>(r) * out8 * 2);
+  L->g_h = take(static_cast<size_t>(npad) * npad * 2); // s G: bf16 [npad, npad] each
+  L->g_l = take(static_cast<size_t>(npad) * npad * 2);
+  L->h_h = take(static_cast<size_t>(npad) * npad * 2); // s^2 H: bf16 [npad, npad] each
+  L->h_l = take(static_cast<size_t>(npad) * npad * 2);
   L->part_t = take(P->gg.part_bytes > P->gh.part_bytes ? P->gg.part_bytes : P->gh.part_bytes);
   L->part_r = take(P->gb.part_bytes > P->ga.part_bytes ? P->gb.part_bytes : P->ga.part_bytes);
   L->b_pad = (r % 4) ? take(static_cast<size_t>(out) * dora::round_up(r, 4) * 4) : 0;
@@ -2296,19 +2261,13 @@ int grid_for(long long n, int sms) {
 }
 
 cudaError_t launch_gemm(const GemmPlan &gp, cudaStream_t cs, const CUtensorMap &x1, const CUtensorMap &x2,
-                        const CUtensorMap &y1h, const CUtensorMap &y1c, const CUtensorMap &y2h,
-                        const CUtensorMap &y2c) {
+                        const CUtensorMap &y1h, const CUtensorMap &y1l, const CUtensorMap &y2h,
+                        const CUtensorMap &y2l) {
   const dim3 grid(static_cast<unsigned>(gp.p.ctas)), block(kThreads);
-  if (gp.xt) {
-    if (gp.bk == kBKWide)
-      tc_gemm_kernel<kBKWide, true><<<grid, block, gp.smem_bytes, cs>>>(x1, x2, y1h, y1c, y2h, y2c, gp.p);
-    else
-      tc_gemm_kernel<kBKNarrow, true><<<grid, block, gp.smem_bytes, cs>>>(x1, x2, y1h, y1c, y2h, y2c, gp.p);
-  } else if (gp.bk == kBKWide) {
-    tc_gemm_kernel<kBKWide, false><<<grid, block, gp.smem_bytes, cs>>>(x1, x2, y1h, y1c, y2h, y2c, gp.p);
-  } else {
-    tc_gemm_kernel<kBKNarrow, false><<<grid, block, gp.smem_bytes, cs>>>(x1, x2, y1h, y1c, y2h, y2c, gp.p);
-  }
+  if (gp.xt)
+    tc_gemm_kernel<true><<<grid, block, gp.smem_bytes, cs>>>(x1, x2, y1h, y1l, y2h, y2l, gp.p);
+  else
+    tc_gemm_kernel<false><<<grid, block, gp.smem_bytes, cs>>>(x1, x2, y1h, y1l, y2h, y2l, gp.p);
   return cudaGetLastError();
 }
 
@@ -2428,10 +2387,8 @@ dora_status device_init(int device, int **errp) {
     void *ptr = nullptr;
     if (cudaGetSymbolAddress(&ptr, g_dora_err) != cudaSuccess) return DORA_ERR_CUDA;
     const cudaFuncAttribute a = cudaFuncAttributeMaxDynamicSharedMemorySize;
-    if (cudaFuncSetAttribute(tc_gemm_kernel<kBKNarrow, false>, a, kSmemMax) != cudaSuccess ||
-        cudaFuncSetAttribute(tc_gemm_kernel<kBKWide, false>, a, kSmemMax) != cudaSuccess ||
-        cudaFuncSetAttribute(tc_gemm_kernel<kBKNarrow, true>, a, kSmemMax) != cudaSuccess ||
-        cudaFuncSetAttribute(tc_gemm_kernel<kBKWide, true>, a, kSmemMax) != cudaSuccess ||
+    if (cudaFuncSetAttribute(tc_gemm_kernel<false>, a, kSmemMax) != cudaSuccess ||
+        cudaFuncSetAttribute(tc_gemm_kernel<true>, a, kSmemMax) != cudaSuccess ||
         cudaFuncSetAttribute(fwd_norm_kernel, a, kSmemMax) != cudaSuccess ||
         cudaFuncSetAttribute(tc16_kernel<32>, a, kSmemMax) != cudaSuccess ||
         cudaFuncSetAttribute(tc16_kernel<64>, a, kSmemMax) != cudaSuccess)
@@ -2722,14 +2679,9 @@ extern "C" dora_status dora_norm_factored_bwd(const float *W0, const float *A, c
   BwdLayout L;
   if (!plan_bwd(out, in, r, sms, &P, &L)) return DORA_ERR_SHAPE;
   uint8_t *ws = static_cast<uint8_t *>(workspace);
-  float *a_hi = reinterpret_cast<float *>(ws + L.a_hi);
-  __nv_bfloat16 *a_c = reinterpret_cast<__nv_bfloat16 *>(ws + L.a_c);
-  float *y_hi = reinterpret_cast<float *>(ws + L.y_hi);
-  __nv_bfloat16 *y_c = reinterpret_cast<__nv_bfloat16 *>(ws + L.y_c);
-  float *g_hi = reinterpret_cast<float *>(ws + L.g_hi);
-  __nv_bfloat16 *g_c = reinterpret_cast<__nv_bfloat16 *>(ws + L.g_c);
-  float *h_hi = reinterpret_cast<float *>(ws + L.h_hi);
-  __nv_bfloat16 *h_c = reinterpret_cast<__nv_bfloat16 *>(ws + L.h_c);
+  auto bf = [&](size_t o) { return reinterpret_cast<__nv_bfloat16 *>(ws + o); };
+  __nv_bfloat16 *a_h = bf(L.a_h), *a_l = bf(L.a_l), *y_h = bf(L.y_h), *y_l = bf(L.y_l);
+  __nv_bfloat16 *g_h = bf(L.g_h), *g_l = bf(L.g_l), *h_h = bf(L.h_h), *h_l = bf(L.h_l);
   float *part_t = reinterpret_cast<float *>(ws + L.part_t);
   float *part_r = reinterpret_cast<float *>(ws + L.part_r);
   int npad, nchunks, NC;
@@ -2743,8 +2695,8 @@ extern "C" dora_status dora_norm_factored_bwd(const float *W0, const float *A, c
 
   // 1. N-side split of A; B padded to a TMA-legal row stride when r % 4 != 0;
   //    the N-side split of (s c B)^T
-  split_n_kernel<<<grid_for(r * in8 / 4, sms), 256, 0, cs>>>(A, r, static_cast<int>(in), static_cast<int>(in8), a_hi,
-                                                              a_c, nullptr, 0);
+  split_hl_kernel<<<grid_for(r * in8 / 4, sms), 256, 0, cs>>>(A, r, static_cast<int>(in), static_cast<int>(in8), a_h,
+                                                               a_l, nullptr, 0);
   ++launches;
   const float *Bk = B;
   int64_t ldb = r;
@@ -2756,62 +2708,67 @@ extern "C" dora_status dora_norm_factored_bwd(const float *W0, const float *A, c
     Bk = bp;
     ldb = rp;
   }
-  bs_split_kernel<<<dim3(static_cast<unsigned>(dora::ceil_div(out8, 32)), static_cast<unsigned>(dora::ceil_div(r, 32))),
-                    dim3(32, 8), 0, cs>>>(B, out, static_cast<int>(r), out8, g, d_mag, norm, s, y_hi, y_c);
+  bs_split_kernel<<<dim3(static_cast<unsigned>(dora::ceil_div(out8, 32)),
+                               static_cast<unsigned>(dora::ceil_div(r, 32))),
+                          dim3(32, 8), 0, cs>>>(B, out, static_cast<int>(r), out8, g, d_mag, norm, s, y_h, y_l);
   ++launches;
 
-  // tensor maps (box rows: one K block of each pass)
+  // tensor maps: the raw fp32 M-side boxes (one K block of 32 by 128 rows) and
+  // the bf16 N-side boxes (64-byte rows of 32 K indices)
   const GemmPlan &gg = P.gg, &gh = P.gh, &gb = P.gb, &ga = P.ga;
-  const int rbg = 4 * gg.bk, rbh = 4 * gh.bk, rbb = 4 * gb.bk, rba = 4 * ga.bk;
-  CUtensorMap mA, mAh_g, mAc_g, mBt, mYh_h, mYc_h, mW0, mB, mAh_b, mAc_b, mGh, mGc, mW0t, mAt, mYh_a, mYc_a, mHh, mHc;
-  bool ok = make_map(&mA, A, false, r, in, in, kBM, rbg) && make_map(&mAh_g, a_hi, false, r, in, in, gg.p.nbox, rbg) &&
-            make_map(&mAc_g, a_c, true, r, 2 * in8, 2 * in8, gg.p.nbox, rbg) &&
-            make_map_t(&mBt, Bk, out, r, ldb, gh.bk) &&
-            make_map(&mYh_h, y_hi, false, r, out8, out8, gh.p.nbox, rbh) &&
-            make_map(&mYc_h, y_c, true, r, 2 * out8, 2 * out8, gh.p.nbox, rbh) &&
-            make_map(&mW0, W0, false, out, in, in, kBM, rbb) && make_map(&mB, Bk, false, out, ldb, ldb, kBM, rbb) &&
-            make_map(&mAh_b, a_hi, false, r, in, in, gb.p.nbox, rbb) &&
-            make_map(&mAc_b, a_c, true, r, 2 * in8, 2 * in8, gb.p.nbox, rbb) &&
-            make_map(&mGh, g_hi, false, npad, npad, npad, gb.p.nbox, rbb) &&
-            make_map(&mGc, g_c, true, npad, 2 * npad, 2 * npad, gb.p.nbox, rbb) &&
-            make_map_t(&mW0t, W0, out, in, in, ga.bk) && make_map_t(&mAt, A, r, in, in, ga.bk) &&
-            make_map(&mYh_a, y_hi, false, r, out8, out8, ga.p.nbox, rba) &&
-            make_map(&mYc_a, y_c, true, r, 2 * out8, 2 * out8, ga.p.nbox, rba) &&
-            make_map(&mHh, h_hi, false, npad, npad, npad, ga.p.nbox, rba) &&
-            make_map(&mHc, h_c, true, npad, 2 * npad, 2 * npad, ga.p.nbox, rba);
+  const int rb = 4 * kBK, nb = 2 * kBK;
+  CUtensorMap mA, mAh_g, mAl_g, mBt, mYh_h, mYl_h, mW0, mB, mAh_b, mAl_b, mGh, mGl, mW0t, mAt, mYh_a, mYl_a, mHh, mHl;
+  bool ok = make_map(&mA, A, false, r, in, in, kBM, rb) &&
+            make_map(&mAh_g, a_h, true, r, in8, in8, gg.p.nbox, nb) &&
+            make_map(&mAl_g, a_l, true, r, in8, in8, gg.p.nbox, nb) &&
+            make_map_t(&mBt, Bk, out, r, ldb, kBK) &&
+            make_map(&mYh_h, y_h, true, r, out8, out8, gh.p.nbox, nb) &&
+            make_map(&mYl_h, y_l, true, r, out8, out8, gh.p.nbox, nb) &&
+            make_map(&mW0, W0, false, out, in, in, kBM, rb) && make_map(&mB, Bk, false, out, ldb, ldb, kBM, rb) &&
+            make_map(&mAh_b, a_h, true, r, in8, in8, gb.p.nbox, nb) &&
+            make_map(&mAl_b, a_l, true, r, in8, in8, gb.p.nbox, nb) &&
+            make_map(&mGh, g_h, true, npad, npad, npad, gb.p.nbox, nb) &&
+            make_map(&mGl, g_l, true, npad, npad, npad, gb.p.nbox, nb) &&
+            make_map_t(&mW0t, W0, out, in, in, kBK) && make_map_t(&mAt, A, r, in, in, kBK) &&
+            make_map(&mYh_a, y_h, true, r, out8, out8, ga.p.nbox, nb) &&
+            make_map(&mYl_a, y_l, true, r, out8, out8, ga.p.nbox, nb) &&
+            make_map(&mHh, h_h, true, npad, npad, npad, ga.p.nbox, nb) &&
+            make_map(&mHl, h_l, true, npad, npad, npad, ga.p.nbox, nb);
   if (!ok) return fail();
 
   // 2. s G = s A A^T (partial tiles, fixed-order reduction, split)
   GemmPlan pg = gg;
   pg.p.part = part_t;
   pg.p.err = errp;
-  if (launch_gemm(pg, cs, mA, mA, mAh_g, mAc_g, mAh_g, mAc_g) != cudaSuccess) return fail();
+  if (launch_gemm(pg, cs, mA, mA, mAh_g, mAl_g, mAh_g, mAl_g) != cudaSuccess) return fail();
   ++launches;
   {
     const StreamK sk{pg.p.units, pg.p.ncl, pg.p.kbtot, pg.p.maxseg};
     const int nsub = (pg.p.NC + 31) / 32;
-    gram_reduce_kernel<<<dim3(static_cast<unsigned>(pg.p.tiles), static_cast<unsigned>(nsub * nsub)), dim3(32, 8), 0,
-                         cs>>>(part_t, sk, pg.p.nchunks, pg.p.NC, static_cast<int>(r), npad, s, g_hi, g_c);
+    gram_reduce_kernel<<<dim3(static_cast<unsigned>(pg.p.tiles), static_cast<unsigned>(nsub * nsub)),
+                               dim3(32, 8), 0, cs>>>(part_t, sk, pg.p.nchunks, pg.p.NC, static_cast<int>(r), npad, s,
+                                                     g_h, g_l);
     ++launches;
   }
   // 3. s^2 H = s (B^T (s c (.) B)), B read transposed
   GemmPlan ph = gh;
   ph.p.part = part_t;
   ph.p.err = errp;
-  if (launch_gemm(ph, cs, mBt, mBt, mYh_h, mYc_h, mYh_h, mYc_h) != cudaSuccess) return fail();
+  if (launch_gemm(ph, cs, mBt, mBt, mYh_h, mYl_h, mYh_h, mYl_h) != cudaSuccess) return fail();
   ++launches;
   {
     const StreamK sk{ph.p.units, ph.p.ncl, ph.p.kbtot, ph.p.maxseg};
     const int nsub = (ph.p.NC + 31) / 32;
-    gram_reduce_kernel<<<dim3(static_cast<unsigned>(ph.p.tiles), static_cast<unsigned>(nsub * nsub)), dim3(32, 8), 0,
-                         cs>>>(part_t, sk, ph.p.nchunks, ph.p.NC, static_cast<int>(r), npad, s, h_hi, h_c);
+    gram_reduce_kernel<<<dim3(static_cast<unsigned>(ph.p.tiles), static_cast<unsigned>(nsub * nsub)),
+                               dim3(32, 8), 0, cs>>>(part_t, sk, ph.p.nchunks, ph.p.NC, static_cast<int>(r), npad, s,
+                                                     h_h, h_l);
     ++launches;
   }
   // 4. dB = s c (.) ([W0 | B] x [A | s G]^T): partial rows, then their sum
   GemmPlan pb = gb;
   pb.p.part = part_r;
   pb.p.err = errp;
-  if (launch_gemm(pb, cs, mW0, mB, mAh_b, mAc_b, mGh, mGc) != cudaSuccess) return fail();
+  if (launch_gemm(pb, cs, mW0, mB, mAh_b, mAl_b, mGh, mGl) != cudaSuccess) return fail();
   ++launches;
   {
     const StreamK sk{pb.p.units, pb.p.ncl, pb.p.kbtot, pb.p.maxseg};
@@ -2826,7 +2783,7 @@ extern "C" dora_status dora_norm_factored_bwd(const float *W0, const float *A, c
   GemmPlan pa = ga;
   pa.p.part = part_r;
   pa.p.err = errp;
-  if (launch_gemm(pa, cs, mW0t, mAt, mYh_a, mYc_a, mHh, mHc) != cudaSuccess) return fail();
+  if (launch_gemm(pa, cs, mW0t, mAt, mYh_a, mYl_a, mHh, mHl) != cudaSuccess) return fail();
   ++launches;
   {
     const StreamK sk{pa.p.units, pa.p.ncl, pa.p.kbtot, pa.p.maxseg};

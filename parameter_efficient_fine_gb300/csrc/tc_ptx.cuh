@@ -82,14 +82,6 @@ __device__ __forceinline__ void tc_fence_after() {
 // D (+)= A * B on the tensor core, fp32 accumulator in tensor memory at `d`;
 // A (M side) in tensor memory at column address `a`, B (N side) in shared
 // memory by descriptor; accumulate when acc != 0
-__device__ __forceinline__ void mma_tf32_ta(uint32_t d, uint32_t a, uint64_t bdesc, uint32_t idesc, uint32_t acc) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
-      "r"(a), "l"(bdesc), "r"(idesc), "r"(acc)
-      : "memory");
-}
 __device__ __forceinline__ void mma_bf16_ta(uint32_t d, uint32_t a, uint64_t bdesc, uint32_t idesc, uint32_t acc) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
@@ -132,11 +124,6 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
 #pragma unroll
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
-__device__ __forceinline__ uint32_t tf32_rna(float x) {
-  uint32_t r;
-  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-  return r;
-}
 // two floats -> two bf16 (nearest even), a in the low half
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
   __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
@@ -165,15 +152,6 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t saddr) {
 template <int BK>
 __device__ __forceinline__ int swz_chunk(int c, int row) {
   return BK == 16 ? c ^ ((row >> 1) & 3) : c ^ (row & 7);
-}
-// Instruction descriptor: kind::tf32, fp32 accumulator, both operands K-major,
-// M = 128, N = n.
-__host__ __device__ __forceinline__ uint32_t idesc_tf32(int n) {
-  return (1u << 4)                                  // D format: f32
-         | (2u << 7)                                // A format: tf32
-         | (2u << 10)                               // B format: tf32
-         | (static_cast<uint32_t>(n >> 3) << 17)    // N >> 3
-         | (static_cast<uint32_t>(kTcM >> 4) << 24); // M >> 4
 }
 // Instruction descriptor: kind::f16 with bf16 operands, fp32 accumulator,
 // both K-major, M = 128, N = n.

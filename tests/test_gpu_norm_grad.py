@@ -7,9 +7,10 @@ same fp32 values, so no input of the oracle comes from the library); d_mag
 drawn from a seeded normal.
 
 Tolerance, derived from the arithmetic.  Every output element is a sum of
-products evaluated with the split-TF32 scheme (per product error <= 2^-18 of
-its magnitude, see dora_norm_factored) and fp32 accumulation; dA also carries
-the error of s^2 H, itself such a sum.  With |.| the same expressions over
+products evaluated with the bf16 three-product split (x = h + l with h =
+bf16(x), l = bf16(x - h); per product the dropped l l term and the residuals
+are <= 3 * 2^-18 of its magnitude, see dora_norm_factored) and fp32
+accumulation; dA also carries the error of s^2 H, itself such a sum.  With |.| the same expressions over
 absolute values (abs_ref), a rigorous elementwise bound is
     |err| <= (2^-16 + 2^-23 (K + 64)) * abs_ref,   K = out + in + 2 r
 (2^-23 per addition allows for an accumulator that truncates).  Because that

@@ -59,7 +59,7 @@ constexpr int kGroupM = 16;     // M tiles per tile-order group (L2 reuse of the
 constexpr int kFMaxCtas = 256;
 constexpr int kFSmemMax = 232448;
 constexpr unsigned kABytes = kFM * kFK * 2;     // 16 KB
-constexpr unsigned kBBytes = kFN * kFK * 2;     // 32 KB
+constexpr unsigned kBBytes = kFN * kFK * 2;     // 32 KB (one CTA); a CTA of a pair holds half
 constexpr unsigned kSlotBytes = 32 * kFQ * 2;  // 4 KB: one warp's 32 rows of a quarter
 constexpr unsigned long long kFWaitNs = 2000000000ull;
 
@@ -110,6 +110,14 @@ __device__ __forceinline__ bool fwait(uint32_t bar, uint32_t parity, SharedCtl *
   return wait_bounded_ns(bar, parity, ctl, p.err, code, *reinterpret_cast<const volatile unsigned long long *>(p.limit_ns));
 }
 
+// PAIR = false: one CTA per tile of 128 x 256, launched as independent CTAs.
+// PAIR = true: clusters of two CTAs; a pair computes a 256 x 256 tile with
+// cta_group::2 MMAs (M = 256), CTA rank c holding tokens [128 c, 128 c + 128)
+// of the tile and weight rows [128 c, 128 c + 128), so each SM stages 32 KB per
+// K block instead of 48.  Both CTAs' copies of a stage complete on the even
+// CTA's stage barrier; the even CTA's lane issues the MMAs and signals both
+// CTAs' stage-free and accumulator barriers.
+template <bool PAIR>
 __global__ void __launch_bounds__(kFThreads, 1)
 fused_compose_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUtensorMap mA1,
                      const __grid_constant__ CUtensorMap mB0, const __grid_constant__ CUtensorMap mB1,
@@ -118,7 +126,16 @@ fused_compose_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_const
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int S = p.stages;
-  const unsigned stage_bytes = kABytes + kBBytes;
+  constexpr unsigned kBRows = PAIR ? kFN / 2 : kFN;   // weight rows staged by this CTA
+  // K atoms (64-wide boxes) per stage: two for a pair (8 MMAs per stage wait;
+  // 64 KB stages), one for a single CTA (48 KB stages)
+  constexpr int kAtoms = PAIR ? 2 : 1;
+  constexpr unsigned kBAtom = kBRows * kFK * 2;
+  constexpr unsigned stage_bytes = kAtoms * (kABytes + kBAtom);
+  constexpr int kTileRows = PAIR ? 2 * kFM : kFM;     // tokens per tile
+  const uint32_t crank = PAIR ? cluster_ctarank() : 0u;
+  const bool leader = crank == 0;
+  const uint32_t peer = crank ^ 1u;
   // staging: [slot][epilogue warp][32 rows x 128 bytes]
   uint8_t *cbuf = smem + static_cast<size_t>(S) * stage_bytes;
   uint64_t *bars = reinterpret_cast<uint64_t *>(cbuf + static_cast<size_t>(p.nslots) * 4 * kSlotBytes);
@@ -136,12 +153,13 @@ fused_compose_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_const
   const int lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
+      // a pair uses the even CTA's full barriers only
       mbar_init(full0 + 8u * s, 1);
       mbar_init(empty0 + 8u * s, 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(accf0 + 8u * b, 1);
-      mbar_init(acce0 + 8u * b, 4);   // one arrival per epilogue warp
+      mbar_init(acce0 + 8u * b, PAIR ? 8 : 4);   // one arrival per epilogue warp (of both CTAs)
     }
     mbar_init(fin, 1);
     for (int k = 0; k < 16; ++k) mbar_init(cfull0 + 8u * k, 1);
@@ -161,15 +179,23 @@ fused_compose_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_const
   }
   if (warp == 1) {
     __syncwarp();
-    tmem_alloc(smem_u32(&ctl->tmem_base), 512);
-    tmem_relinquish();
+    if (PAIR) {
+      tmem_alloc_pair(smem_u32(&ctl->tmem_base), 512);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_u32(&ctl->tmem_base), 512);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
   __syncthreads();
+  // PAIR: both CTAs' barriers are initialised before either signals the other's
+  if (PAIR) cluster_sync();
   tc_fence_after();
   const uint32_t tmem = ctl->tmem_base;
-  const int cta = static_cast<int>(blockIdx.x);
-  const int ncta = static_cast<int>(gridDim.x);
+  // tile sequence of this CTA (of its pair: both CTAs run the same sequence)
+  const int cta = static_cast<int>(PAIR ? blockIdx.x / 2 : blockIdx.x);
+  const int ncta = static_cast<int>(PAIR ? gridDim.x / 2 : gridDim.x);
 
   if (warp == 0) {
     if (lane == 0) {
@@ -188,7 +214,10 @@ fused_compose_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_const
             break;
           }
           const uint32_t fb = full0 + 8u * stage;
-          mbar_expect_tx(fb, stage_bytes);
+          // a pair: the even CTA's barrier counts both CTAs' bytes (the odd
+          // CTA's copies may land before this arrival; the phase cannot
+          // complete without it)
+          if (!PAIR || leader) mbar_expect_tx(fb, PAIR ? 2 * stage_bytes : stage_bytes);
           const uint32_t xs = smem_u32(smem + static_cast<size_t>(stage) * stage_bytes);
           int ks = kb;
           int sg = 0;
@@ -202,8 +231,22 @@ fused_compose_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_const
           }
           const CUtensorMap *ma = sg == 0 ? &mA0 : &mA1;
           const CUtensorMap *mb = sg == 0 ? &mB0 : (sg == 1 ? &mB1 : &mB2);
-          tma_load_2d(xs, ma, ks * kFK, mt * kFM, fb);
-          tma_load_2d(xs + kABytes, mb, ks * kFK, nt * kFN, fb);
+          const int ya = mt * kTileRows + static_cast<int>(crank) * kFM;
+          const int yb = nt * kFN + static_cast<int>(crank * kBRows);
+          // stage layout: the kAtoms token-side boxes, then the weight-side boxes
+#pragma unroll
+          for (int a = 0; a < kAtoms; ++a) {
+            const int kx = (kAtoms * ks + a) * kFK;
+            const uint32_t da = xs + a * kABytes, db = xs + kAtoms * kABytes + a * kBAtom;
+            if (PAIR) {
+              const uint32_t lb = mapa_shared(fb, 0);
+              tma_load_2d_pair(da, ma, kx, ya, lb);
+              tma_load_2d_pair(db, mb, kx, yb, lb);
+            } else {
+              tma_load_2d(da, ma, kx, ya, fb);
+              tma_load_2d(db, mb, kx, yb, fb);
+            }
+          }
           ++issued;
           if (++stage == S) {
             stage = 0;
@@ -211,26 +254,45 @@ fused_compose_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_const
           }
         }
       }
-      if (!ok) {
-        // copies in flight: the last min(issued, S) stages
-        int st = stage;
-        uint32_t ph = phase;
-        for (int k = 0; k < S && k < issued; ++k) {
-          if (--st < 0) {
-            st = S - 1;
-            ph ^= 1u;
+      if (!ok && issued > 0) {
+        if (PAIR) {
+          // the stage barriers (the even CTA's) also count the other CTA's
+          // copies, which may never be issued after an abort; copies in
+          // flight land within microseconds: wait 1 ms
+          const unsigned long long t0 = globaltimer();
+          while (globaltimer() - t0 < 1000000ull) {
           }
-          wait_drain_ns(full0 + 8u * st, ph, kFWaitNs);
+        } else {
+          // copies in flight: the last min(issued, S) stages
+          int st = stage;
+          uint32_t ph = phase;
+          for (int k = 0; k < S && k < issued; ++k) {
+            if (--st < 0) {
+              st = S - 1;
+              ph ^= 1u;
+            }
+            wait_drain_ns(full0 + 8u * st, ph, kFWaitNs);
+          }
         }
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
+    if (lane == 0 && leader) {
       // ---------------------------------------------------------------- MMA issuer
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      const uint32_t idesc = idesc_bf16(kFN);
+      const uint32_t idesc = PAIR ? idesc_bf16_pair(kFN) : idesc_bf16(kFN);
+      // a commit arrives on the barrier of this CTA and, for a pair, on the
+      // same barrier of the peer
+      auto commit = [&](uint32_t bar) {
+        if (PAIR) {
+          mma_commit_pair(bar);
+          mma_commit_pair(mapa_shared(bar, peer));
+        } else {
+          mma_commit(bar);
+        }
+      };
       int li = 0;
       for (int t = cta; t < p.tiles && ok; t += ncta, ++li) {
         const int buf = li & 1;
@@ -249,20 +311,25 @@ fused_compose_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_const
           tc_fence_after();
           const uint32_t xs = smem_u32(smem + static_cast<size_t>(stage) * stage_bytes);
 #pragma unroll
-          for (int k = 0; k < kFK / 16; ++k) {
-            const uint32_t ko = static_cast<uint32_t>(k) * 32u;   // 16 bf16 = 32 bytes along the swizzled row
-            mma_bf16_ss(d, sdesc<32>(xs + ko), sdesc<32>(xs + kABytes + ko), idesc, (kb | k) != 0 ? 1u : 0u);
+          for (int k = 0; k < kAtoms * kFK / 16; ++k) {
+            const uint32_t a = static_cast<uint32_t>(k / (kFK / 16));             // K atom of the stage
+            const uint32_t ko = static_cast<uint32_t>(k % (kFK / 16)) * 32u;      // 16 bf16 = 32 bytes along the swizzled row
+            const uint64_t ad = sdesc<32>(xs + a * kABytes + ko);
+            const uint64_t bd = sdesc<32>(xs + kAtoms * kABytes + a * kBAtom + ko);
+            if (PAIR) mma_bf16_ss_pair(d, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+            else mma_bf16_ss(d, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
           }
-          mma_commit(empty0 + 8u * stage);
+          commit(empty0 + 8u * stage);
           if (++stage == S) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        mma_commit(accf0 + 8u * buf);
+        commit(accf0 + 8u * buf);
       }
-      mma_commit(fin);
+      if (PAIR) mma_commit_pair(fin);
+      else mma_commit(fin);
       wait_drain_ns(fin, 0, kFWaitNs);
     }
   } else {
@@ -282,7 +349,8 @@ fused_compose_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_const
       int mt, nt;
       tile_mn(t, p.mtiles, p.ntiles, &mt, &nt);
       mbar_expect_tx(cfull(q), kSlotBytes);
-      tma_load_2d(cbase + slot_off(q), &mC, nt * kFN + q * kFQ, mt * kFM + quad * 32, cfull(q));
+      tma_load_2d(cbase + slot_off(q), &mC, nt * kFN + q * kFQ,
+                  mt * kTileRows + static_cast<int>(crank) * kFM + quad * 32, cfull(q));
       any_load |= 1u << q;
       load_par ^= 1u << q;
     };
@@ -306,7 +374,8 @@ fused_compose_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_const
         break;
       }
       tc_fence_after();
-      const bool rows_in = mt * kFM + quad * 32 < p.T;   // any of this warp's rows inside y
+      const int row0 = mt * kTileRows + static_cast<int>(crank) * kFM;   // this CTA's first row of the tile
+      const bool rows_in = row0 + quad * 32 < p.T;   // any of this warp's rows inside y
       for (int q = 0; q < 4; ++q) {
         const int sl = q % p.nslots;
         const int gcol0 = nt * kFN + q * kFQ;
@@ -376,7 +445,7 @@ fused_compose_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_const
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            tma_store_2d(&mY, cbase + slot_off(sl), gcol0, mt * kFM + quad * 32);
+            tma_store_2d(&mY, cbase + slot_off(sl), gcol0, row0 + quad * 32);
             bulk_commit();
             last_slot = sl;
           }
@@ -385,7 +454,10 @@ fused_compose_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_const
           // the accumulator is read out: the MMA lane may start the tile after next
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(acce0 + 8u * buf);
+          if (lane == 0) {
+            if (PAIR) mbar_arrive_cluster(mapa_shared(acce0 + 8u * buf, 0));   // the even CTA's barrier
+            else mbar_arrive(acce0 + 8u * buf);
+          }
         }
         if (p.has_base && lane == 0 && q > 0 && tnext < p.tiles) {
           // slot q - 1 takes the next tile's base quarter once every store
@@ -414,10 +486,14 @@ fused_compose_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_const
 
   tc_fence_before();
   __syncthreads();
+  // PAIR: the even CTA's MMAs (which read this CTA's shared memory and write
+  // its tensor memory) are complete, and both CTAs' epilogues are done
+  if (PAIR) cluster_sync();
   tc_fence_after();
   if (warp == 1) {
     __syncwarp();
-    tmem_dealloc(tmem, 512);
+    if (PAIR) tmem_dealloc_pair(tmem, 512);
+    else tmem_dealloc(tmem, 512);
   }
 }
 
@@ -437,18 +513,23 @@ struct FusedPlan {
   FusedParams p;
   size_t smem_bytes;
   int ctas;
+  bool pair;   // CTA pairs (fused_compose_kernel<true>, clusters of two)
 };
 
-bool plan_fused(int64_t T, int64_t in, int64_t out, int64_t r, bool has_base, int sms, FusedPlan *fp) {
+// max_units: CTAs (one per SM) or, for pairs, the pairs that can be resident at once
+bool plan_fused(int64_t T, int64_t in, int64_t out, int64_t r, bool has_base, bool pair, int max_units,
+                FusedPlan *fp) {
   FusedParams &p = fp->p;
   p = FusedParams{};
+  fp->pair = pair;
   p.T = static_cast<int>(T);
   p.out = static_cast<int>(out);
   p.nseg = has_base ? 2 : 3;
-  p.kb[0] = has_base ? 0 : static_cast<int>(dora::ceil_div(in, kFK));
-  p.kb[1] = p.kb[2] = static_cast<int>(dora::ceil_div(r, kFK));
+  const int kstage = pair ? 2 * kFK : kFK;   // K per stage (the kernel's kAtoms boxes)
+  p.kb[0] = has_base ? 0 : static_cast<int>(dora::ceil_div(in, kstage));
+  p.kb[1] = p.kb[2] = static_cast<int>(dora::ceil_div(r, kstage));
   p.kbtot = p.kb[0] + p.kb[1] + p.kb[2];
-  p.mtiles = static_cast<int>(dora::ceil_div(T, kFM));
+  p.mtiles = static_cast<int>(dora::ceil_div(T, pair ? 2 * kFM : kFM));
   p.ntiles = static_cast<int>(dora::ceil_div(out, kFN));
   const long long tiles = static_cast<long long>(p.mtiles) * p.ntiles;
   if (tiles >= (1ll << 31)) return false;
@@ -456,12 +537,13 @@ bool plan_fused(int64_t T, int64_t in, int64_t out, int64_t r, bool has_base, in
   p.has_base = has_base ? 1 : 0;
   p.nslots = has_base ? 4 : 2;
   const size_t fixed = 1024 + static_cast<size_t>(p.nslots) * 4 * kSlotBytes + 512;
-  const size_t stage_bytes = kABytes + kBBytes;
+  const size_t stage_bytes = pair ? 2 * (kABytes + kBBytes / 2) : kABytes + kBBytes;
   p.stages = static_cast<int>((kFSmemMax - fixed) / stage_bytes);
   if (p.stages > 8) p.stages = 8;
   if (p.stages < 2) return false;
   fp->smem_bytes = fixed + static_cast<size_t>(p.stages) * stage_bytes;
-  fp->ctas = p.tiles < sms ? p.tiles : sms;
+  const int units = p.tiles < max_units ? p.tiles : max_units;
+  fp->ctas = pair ? 2 * units : units;
   return true;
 }
 
@@ -472,10 +554,25 @@ bool map_bf16(CUtensorMap *map, const void *base, int64_t rows, int64_t cols, in
 
 int *g_stall_ptr[64] = {};
 unsigned long long *g_limit_ptr[64] = {};
+int g_max_pairs[64] = {};   // clusters of two of fused_compose_kernel<true> resident at once
 
-dora_status fused_init(int device, int **errp) {
+// launch configuration of the pair kernel: clusters of two CTAs along x
+void pair_config(cudaLaunchConfig_t *cfg, cudaLaunchAttribute *attr, unsigned ctas, size_t smem, cudaStream_t cs) {
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg->gridDim = dim3(ctas);
+  cfg->blockDim = dim3(kFThreads);
+  cfg->dynamicSmemBytes = smem;
+  cfg->stream = cs;
+  cfg->attrs = attr;
+  cfg->numAttrs = 1;
+}
+
+dora_status fused_init(int device, int sms, int **errp) {
   static std::mutex mu;
-  static uint64_t done_ctx[64] = {};   // context the attribute was set in
+  static uint64_t done_ctx[64] = {};   // context the attributes were set in
   std::lock_guard<std::mutex> lock(mu);
   if (device < 0 || device >= 64) return DORA_ERR_CUDA;
   dora_status st = dora::error_word(device, errp);
@@ -484,9 +581,20 @@ dora_status fused_init(int device, int **errp) {
   if (st != DORA_OK) return st;
   const uint64_t ctx = dora::context_id();
   if (ctx == 0 || ctx != done_ctx[device]) {
-    if (cudaFuncSetAttribute(fused_compose_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kFSmemMax) !=
-        cudaSuccess)
+    const auto a = cudaFuncAttributeMaxDynamicSharedMemorySize;
+    if (cudaFuncSetAttribute(fused_compose_kernel<false>, a, kFSmemMax) != cudaSuccess ||
+        cudaFuncSetAttribute(fused_compose_kernel<true>, a, kFSmemMax) != cudaSuccess)
       return DORA_ERR_CUDA;
+    // pairs resident at once with the largest shared-memory footprint (one CTA per SM)
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    pair_config(&cfg, attr, static_cast<unsigned>(2 * (sms / 2)), kFSmemMax, nullptr);
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, fused_compose_kernel<true>, &cfg) != cudaSuccess) {
+      cudaGetLastError();
+      n = 0;
+    }
+    g_max_pairs[device] = n;
     done_ctx[device] = dora::context_id();
   }
   return DORA_OK;
@@ -502,12 +610,18 @@ dora_status fused_run(const void *x, const void *W0, const void *base, const voi
   int device = 0;
   dora_status st = dora::current_device(&info, &device);
   if (st != DORA_OK) return st;
-  int *errp = nullptr;
-  st = fused_init(device, &errp);
-  if (st != DORA_OK) return st;
   const int sms = info.sms < kFMaxCtas ? info.sms : kFMaxCtas;
+  int *errp = nullptr;
+  st = fused_init(device, sms, &errp);
+  if (st != DORA_OK) return st;
+  // CTA pairs for the linear form (its long K loop is bound by the MMA
+  // pipeline, which the pair's M = 256 tiles and 8-MMA stages feed better);
+  // single CTAs for the lora form (its 12 K blocks per tile make the epilogue
+  // the limit, and one CTA holds more staging per tile)
+  const int max_pairs = g_max_pairs[device];
+  const bool pair = !lora_form && max_pairs > 0;
   FusedPlan fp;
-  if (!plan_fused(T, in, out, r, lora_form, sms, &fp)) return DORA_ERR_SHAPE;
+  if (!plan_fused(T, in, out, r, lora_form, pair, pair ? max_pairs : sms, &fp)) return DORA_ERR_SHAPE;
   fp.p.g = g;
   fp.p.err = errp;
   fp.p.stall = g_stall_ptr[device];
@@ -523,23 +637,35 @@ dora_status fused_run(const void *x, const void *W0, const void *base, const voi
   split_sb_kernel<<<static_cast<unsigned>(blocks), 256, 0, cs>>>(B, n, s, hi, lo);
   ++launches;
 
+  // weight-side boxes: the whole 256-row tile, or a CTA's half of it in a pair
+  const int brows = pair ? kFN / 2 : kFN;
   CUtensorMap mA0, mA1, mB0, mB1, mB2, mC, mY;
-  bool ok = map_bf16(&mA1, xa, T, r, r, kFM) && map_bf16(&mB1, hi, out, r, r, kFN) &&
-            map_bf16(&mB2, lo, out, r, r, kFN) && map_bf16(&mY, y, T, out, out, 32);
+  bool ok = map_bf16(&mA1, xa, T, r, r, kFM) && map_bf16(&mB1, hi, out, r, r, brows) &&
+            map_bf16(&mB2, lo, out, r, r, brows) && map_bf16(&mY, y, T, out, out, 32);
   if (lora_form) {
     ok = ok && map_bf16(&mC, base, T, out, out, 32);
     mA0 = mA1;
     mB0 = mB1;
   } else {
-    ok = ok && map_bf16(&mA0, x, T, in, in, kFM) && map_bf16(&mB0, W0, out, in, in, kFN);
+    ok = ok && map_bf16(&mA0, x, T, in, in, kFM) && map_bf16(&mB0, W0, out, in, in, brows);
     mC = mY;
   }
   if (!ok) {
     dora::count_launches(launches);
     return DORA_ERR_CUDA;
   }
-  fused_compose_kernel<<<static_cast<unsigned>(fp.ctas), kFThreads, fp.smem_bytes, cs>>>(mA0, mA1, mB0, mB1, mB2, mC,
-                                                                                         mY, fp.p);
+  if (pair) {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    pair_config(&cfg, attr, static_cast<unsigned>(fp.ctas), fp.smem_bytes, cs);
+    if (cudaLaunchKernelEx(&cfg, fused_compose_kernel<true>, mA0, mA1, mB0, mB1, mB2, mC, mY, fp.p) != cudaSuccess) {
+      dora::count_launches(launches);
+      return DORA_ERR_CUDA;
+    }
+  } else {
+    fused_compose_kernel<false><<<static_cast<unsigned>(fp.ctas), kFThreads, fp.smem_bytes, cs>>>(
+        mA0, mA1, mB0, mB1, mB2, mC, mY, fp.p);
+  }
   ++launches;
   dora::count_launches(launches);
   return dora::launch_status();

@@ -54,7 +54,9 @@ constexpr int kFM = 128;        // tile rows (tokens) = tensor-memory lanes
 constexpr int kFN = 256;        // tile columns (outputs) = N of one MMA
 constexpr int kFK = 64;         // bf16 per K block: one 128-byte swizzled row
 constexpr int kFQ = 64;         // columns per epilogue quarter (one 128-byte box row)
-constexpr int kFThreads = 192;
+constexpr int kEpiWarps = 8;    // epilogue warps: two per tensor-memory lane quadrant
+constexpr int kQPW = 4 * 4 / kEpiWarps;   // 64-column quarters of a tile per epilogue warp
+constexpr int kFThreads = 64 + 32 * kEpiWarps;
 constexpr int kGroupM = 16;     // M tiles per tile-order group (L2 reuse of the weight tiles)
 constexpr int kFMaxCtas = 256;
 constexpr int kFSmemMax = 232448;
@@ -70,7 +72,9 @@ struct FusedParams {
   int kbtot;            // 64-wide K blocks per tile over all segments
   int mtiles, ntiles, tiles;
   int stages;
-  int nslots;           // staging slots per epilogue warp: 4 with base (one per quarter), 2 without
+  int na;               // token-side boxes per stage (a pair's linear form: 2)
+  unsigned stage_bytes; // na token-side boxes + the weight-side boxes
+  int nslots;           // staging slots per epilogue warp: one per quarter with base, else one
   int has_base;
   const float *g;
   int *err;
@@ -127,19 +131,20 @@ fused_compose_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_const
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int S = p.stages;
   constexpr unsigned kBRows = PAIR ? kFN / 2 : kFN;   // weight rows staged by this CTA
-  // K atoms (64-wide boxes) per stage: two for a pair (8 MMAs per stage wait;
-  // 64 KB stages), one for a single CTA (48 KB stages)
+  // weight-side boxes (64 K wide) per stage: two for a pair (8 MMAs per stage
+  // wait), one for a single CTA; the token-side boxes: p.na
   constexpr int kAtoms = PAIR ? 2 : 1;
   constexpr unsigned kBAtom = kBRows * kFK * 2;
-  constexpr unsigned stage_bytes = kAtoms * (kABytes + kBAtom);
+  const unsigned stage_bytes = p.stage_bytes;
+  const uint32_t boff = static_cast<uint32_t>(p.na) * kABytes;   // first weight-side box of a stage
   constexpr int kTileRows = PAIR ? 2 * kFM : kFM;     // tokens per tile
   const uint32_t crank = PAIR ? cluster_ctarank() : 0u;
   const bool leader = crank == 0;
   const uint32_t peer = crank ^ 1u;
   // staging: [slot][epilogue warp][32 rows x 128 bytes]
   uint8_t *cbuf = smem + static_cast<size_t>(S) * stage_bytes;
-  uint64_t *bars = reinterpret_cast<uint64_t *>(cbuf + static_cast<size_t>(p.nslots) * 4 * kSlotBytes);
-  // barriers: full[S], empty[S], accf[2], acce[2], fin, cfull[4 slots][4 warps]
+  uint64_t *bars = reinterpret_cast<uint64_t *>(cbuf + static_cast<size_t>(p.nslots) * kEpiWarps * kSlotBytes);
+  // barriers: full[S], empty[S], accf[2], acce[2], fin, cfull[2 slots][8 warps]
   SharedCtl *ctl = reinterpret_cast<SharedCtl *>(bars + 2 * S + 21);
   const uint32_t full0 = smem_u32(bars);
   const uint32_t empty0 = full0 + 8u * S;
@@ -159,10 +164,10 @@ fused_compose_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_const
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(accf0 + 8u * b, 1);
-      mbar_init(acce0 + 8u * b, PAIR ? 8 : 4);   // one arrival per epilogue warp (of both CTAs)
+      mbar_init(acce0 + 8u * b, PAIR ? 2 * kEpiWarps : kEpiWarps);   // one arrival per epilogue warp (of both CTAs)
     }
     mbar_init(fin, 1);
-    for (int k = 0; k < 16; ++k) mbar_init(cfull0 + 8u * k, 1);
+    for (int k = 0; k < kQPW * kEpiWarps; ++k) mbar_init(cfull0 + 8u * k, 1);
     ctl->abort = 0;
     fence_barrier_init();
   }
@@ -214,10 +219,6 @@ fused_compose_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_const
             break;
           }
           const uint32_t fb = full0 + 8u * stage;
-          // a pair: the even CTA's barrier counts both CTAs' bytes (the odd
-          // CTA's copies may land before this arrival; the phase cannot
-          // complete without it)
-          if (!PAIR || leader) mbar_expect_tx(fb, PAIR ? 2 * stage_bytes : stage_bytes);
           const uint32_t xs = smem_u32(smem + static_cast<size_t>(stage) * stage_bytes);
           int ks = kb;
           int sg = 0;
@@ -229,23 +230,35 @@ fused_compose_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_const
               sg = 2;
             }
           }
-          const CUtensorMap *ma = sg == 0 ? &mA0 : &mA1;
-          const CUtensorMap *mb = sg == 0 ? &mB0 : (sg == 1 ? &mB1 : &mB2);
           const int ya = mt * kTileRows + static_cast<int>(crank) * kFM;
           const int yb = nt * kFN + static_cast<int>(crank * kBRows);
-          // stage layout: the kAtoms token-side boxes, then the weight-side boxes
+          if (PAIR) {
+            // stage layout [A0][A1 (linear form)][B0][B1].  Segment 0: two K
+            // atoms of x and W0.  Segment 1: one K atom of xa in A0, against
+            // s B hi in B0 and s B lo in B1 (xa is loaded once for both
+            // halves).  The even CTA's barrier counts both CTAs' bytes; the
+            // odd CTA's copies may land before this arrival (the phase cannot
+            // complete without it)
+            if (leader) mbar_expect_tx(fb, 2 * (sg == 0 ? 2 * kABytes : kABytes) + 4 * kBAtom);
+            const uint32_t lb = mapa_shared(fb, 0);
+            if (sg == 0) {
 #pragma unroll
-          for (int a = 0; a < kAtoms; ++a) {
-            const int kx = (kAtoms * ks + a) * kFK;
-            const uint32_t da = xs + a * kABytes, db = xs + kAtoms * kABytes + a * kBAtom;
-            if (PAIR) {
-              const uint32_t lb = mapa_shared(fb, 0);
-              tma_load_2d_pair(da, ma, kx, ya, lb);
-              tma_load_2d_pair(db, mb, kx, yb, lb);
+              for (int a = 0; a < 2; ++a) {
+                const int kx = (2 * ks + a) * kFK;
+                tma_load_2d_pair(xs + a * kABytes, &mA0, kx, ya, lb);
+                tma_load_2d_pair(xs + boff + a * kBAtom, &mB0, kx, yb, lb);
+              }
             } else {
-              tma_load_2d(da, ma, kx, ya, fb);
-              tma_load_2d(db, mb, kx, yb, fb);
+              tma_load_2d_pair(xs, &mA1, ks * kFK, ya, lb);
+              tma_load_2d_pair(xs + boff, &mB1, ks * kFK, yb, lb);
+              tma_load_2d_pair(xs + boff + kBAtom, &mB2, ks * kFK, yb, lb);
             }
+          } else {
+            mbar_expect_tx(fb, stage_bytes);
+            const CUtensorMap *ma = sg == 0 ? &mA0 : &mA1;
+            const CUtensorMap *mb = sg == 0 ? &mB0 : (sg == 1 ? &mB1 : &mB2);
+            tma_load_2d(xs, ma, ks * kFK, ya, fb);
+            tma_load_2d(xs + boff, mb, ks * kFK, yb, fb);
           }
           ++issued;
           if (++stage == S) {
@@ -310,12 +323,14 @@ fused_compose_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_const
           }
           tc_fence_after();
           const uint32_t xs = smem_u32(smem + static_cast<size_t>(stage) * stage_bytes);
+          // a pair's segment-1 stages use A0 against both weight boxes
+          const uint32_t a1 = (PAIR && kb >= p.kb[0]) ? 0u : 1u;
 #pragma unroll
           for (int k = 0; k < kAtoms * kFK / 16; ++k) {
-            const uint32_t a = static_cast<uint32_t>(k / (kFK / 16));             // K atom of the stage
+            const uint32_t a = static_cast<uint32_t>(k / (kFK / 16));             // weight box (K atom) of the stage
             const uint32_t ko = static_cast<uint32_t>(k % (kFK / 16)) * 32u;      // 16 bf16 = 32 bytes along the swizzled row
-            const uint64_t ad = sdesc<32>(xs + a * kABytes + ko);
-            const uint64_t bd = sdesc<32>(xs + kAtoms * kABytes + a * kBAtom + ko);
+            const uint64_t ad = sdesc<32>(xs + a * a1 * kABytes + ko);
+            const uint64_t bd = sdesc<32>(xs + boff + a * kBAtom + ko);
             if (PAIR) mma_bf16_ss_pair(d, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
             else mma_bf16_ss(d, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
           }
@@ -334,28 +349,33 @@ fused_compose_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_const
     }
   } else {
     // ---------------------------------------------------------------- epilogue
-    const int quad = warp & 3;               // rows quad * 32 + lane of the tile = tensor-memory lanes
+    // warp e of the epilogue: tensor-memory lanes (rows of the tile) quad * 32
+    // .. + 31 (a warp reaches the lane quadrant of its index mod 4), quarters
+    // qb .. qb + kQPW - 1 of the tile's 256 columns
+    const int e = warp - 2;
+    const int quad = warp & 3;
+    const int qb = (e / 4) * kQPW;
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quad * 32) << 16);
-    // this warp's slot s: cbuf + (s * 4 + quad) * 4 KB (1024-byte aligned, so
-    // the 128-byte swizzle of a [32 x 64] box has the same phase as in a full tile)
-    auto slot_off = [&](int s) { return static_cast<uint32_t>((s * 4 + quad) * kSlotBytes); };
-    auto cfull = [&](int s) { return cfull0 + 8u * static_cast<uint32_t>(s * 4 + quad); };
-    // base quarter q of tile t into slot q (lora form; lane 0): the base of a
-    // tile is requested while the previous tile is being written out, one
-    // tile ahead.  Per slot: whether a load was issued, and the parity of the
-    // number issued (for the drain after an abort)
+    // this warp's slot s: cbuf + (s * kEpiWarps + e) * 4 KB (1024-byte aligned,
+    // so the 128-byte swizzle of a [32 x 64] box has the same phase as in a full tile)
+    auto slot_off = [&](int s) { return static_cast<uint32_t>((s * kEpiWarps + e) * kSlotBytes); };
+    auto cfull = [&](int s) { return cfull0 + 8u * static_cast<uint32_t>(s * kEpiWarps + e); };
+    // base of this warp's quarter qb + j of tile t into slot j (lora form;
+    // lane 0): the base of a tile is requested while the previous tile is
+    // being written out, one tile ahead.  Per slot: whether a load was
+    // issued, and the parity of the number issued (for the drain after an abort)
     uint32_t any_load = 0, load_par = 0;
-    auto load_base = [&](int t, int q) {
+    auto load_base = [&](int t, int j) {
       int mt, nt;
       tile_mn(t, p.mtiles, p.ntiles, &mt, &nt);
-      mbar_expect_tx(cfull(q), kSlotBytes);
-      tma_load_2d(cbase + slot_off(q), &mC, nt * kFN + q * kFQ,
-                  mt * kTileRows + static_cast<int>(crank) * kFM + quad * 32, cfull(q));
-      any_load |= 1u << q;
-      load_par ^= 1u << q;
+      mbar_expect_tx(cfull(j), kSlotBytes);
+      tma_load_2d(cbase + slot_off(j), &mC, nt * kFN + (qb + j) * kFQ,
+                  mt * kTileRows + static_cast<int>(crank) * kFM + quad * 32, cfull(j));
+      any_load |= 1u << j;
+      load_par ^= 1u << j;
     };
     if (p.has_base && lane == 0 && cta < p.tiles)
-      for (int q = 0; q < 4; ++q) load_base(cta, q);
+      for (int j = 0; j < kQPW; ++j) load_base(cta, j);
     // the staging slot of this warp's most recent TMA store (-1: none yet).
     // Before a slot is written again, every store that reads it must be done:
     // all but the most recent store when that one used another slot, else all.
@@ -376,16 +396,17 @@ fused_compose_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_const
       tc_fence_after();
       const int row0 = mt * kTileRows + static_cast<int>(crank) * kFM;   // this CTA's first row of the tile
       const bool rows_in = row0 + quad * 32 < p.T;   // any of this warp's rows inside y
-      for (int q = 0; q < 4; ++q) {
-        const int sl = q % p.nslots;
+      for (int j = 0; j < kQPW; ++j) {
+        const int q = qb + j;
+        const int sl = j % p.nslots;
         const int gcol0 = nt * kFN + q * kFQ;
         // a quarter entirely outside y (ragged last tiles) is neither computed
         // nor stored; warp-uniform
         const bool live = rows_in && gcol0 < p.out;
         if (p.has_base) {
-          // slot q holds this tile's base quarter: the slot's load number li
+          // slot j holds this tile's base quarter: the slot's load number li
           // (consumed even when the quarter is not live, to keep the phases)
-          const bool gb = fwait(cfull(q), static_cast<uint32_t>(li) & 1u, ctl, p, 16);
+          const bool gb = fwait(cfull(j), static_cast<uint32_t>(li) & 1u, ctl, p, 16);
           if (!__all_sync(0xffffffffu, gb)) {
             ok = false;
             break;
@@ -450,7 +471,7 @@ fused_compose_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_const
             last_slot = sl;
           }
         }
-        if (q == 3) {
+        if (j == kQPW - 1) {
           // the accumulator is read out: the MMA lane may start the tile after next
           tc_fence_before();
           __syncwarp();
@@ -459,18 +480,18 @@ fused_compose_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_const
             else mbar_arrive(acce0 + 8u * buf);
           }
         }
-        if (p.has_base && lane == 0 && q > 0 && tnext < p.tiles) {
-          // slot q - 1 takes the next tile's base quarter once every store
+        if (p.has_base && lane == 0 && j > 0 && tnext < p.tiles) {
+          // slot j - 1 takes the next tile's base quarter once every store
           // that reads it is done: all but this quarter's store, if there was one
           if (live) bulk_wait_read1();
           else bulk_wait_read0();
-          load_base(tnext, q - 1);
+          load_base(tnext, j - 1);
         }
       }
       if (!ok) break;
       if (p.has_base && lane == 0 && tnext < p.tiles) {
         bulk_wait_read0();
-        load_base(tnext, 3);
+        load_base(tnext, kQPW - 1);
       }
     }
     if (lane == 0) {
@@ -478,8 +499,8 @@ fused_compose_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_const
       if (!ok) {
         // base copies that may still be in flight into this warp's slots: the
         // k-th load of a slot completes phase k - 1, of parity (count - 1) & 1
-        for (int q = 0; q < 4; ++q)
-          if ((any_load >> q) & 1u) wait_drain_ns(cfull(q), ((load_par >> q) & 1u) ^ 1u, kFWaitNs);
+        for (int j = 0; j < kQPW; ++j)
+          if ((any_load >> j) & 1u) wait_drain_ns(cfull(j), ((load_par >> j) & 1u) ^ 1u, kFWaitNs);
       }
     }
   }
@@ -525,9 +546,11 @@ bool plan_fused(int64_t T, int64_t in, int64_t out, int64_t r, bool has_base, bo
   p.T = static_cast<int>(T);
   p.out = static_cast<int>(out);
   p.nseg = has_base ? 2 : 3;
-  const int kstage = pair ? 2 * kFK : kFK;   // K per stage (the kernel's kAtoms boxes)
-  p.kb[0] = has_base ? 0 : static_cast<int>(dora::ceil_div(in, kstage));
-  p.kb[1] = p.kb[2] = static_cast<int>(dora::ceil_div(r, kstage));
+  // K blocks (stages) per segment: single CTA (x, W0), (xa, s B hi), (xa, s B
+  // lo), 64 K each; a pair (x, W0) by 128 K, then (xa; s B hi, s B lo) by 64 K
+  p.kb[0] = has_base ? 0 : static_cast<int>(dora::ceil_div(in, pair ? 2 * kFK : kFK));
+  p.kb[1] = static_cast<int>(dora::ceil_div(r, kFK));
+  p.kb[2] = pair ? 0 : p.kb[1];
   p.kbtot = p.kb[0] + p.kb[1] + p.kb[2];
   p.mtiles = static_cast<int>(dora::ceil_div(T, pair ? 2 * kFM : kFM));
   p.ntiles = static_cast<int>(dora::ceil_div(out, kFN));
@@ -535,9 +558,14 @@ bool plan_fused(int64_t T, int64_t in, int64_t out, int64_t r, bool has_base, bo
   if (tiles >= (1ll << 31)) return false;
   p.tiles = static_cast<int>(tiles);
   p.has_base = has_base ? 1 : 0;
-  p.nslots = has_base ? 4 : 2;
-  const size_t fixed = 1024 + static_cast<size_t>(p.nslots) * 4 * kSlotBytes + 512;
-  const size_t stage_bytes = pair ? 2 * (kABytes + kBBytes / 2) : kABytes + kBBytes;
+  p.nslots = has_base ? kQPW : 1;
+  const size_t fixed = 1024 + static_cast<size_t>(p.nslots) * kEpiWarps * kSlotBytes + 512;
+  // a pair: two token-side boxes per stage for the linear form's (x, W0)
+  // segment, one for the lora form; two half weight boxes.  A single CTA: one
+  // token-side box and one weight box
+  p.na = (pair && !has_base) ? 2 : 1;
+  const size_t stage_bytes = static_cast<size_t>(p.na) * kABytes + kBBytes;
+  p.stage_bytes = static_cast<unsigned>(stage_bytes);
   p.stages = static_cast<int>((kFSmemMax - fixed) / stage_bytes);
   if (p.stages > 8) p.stages = 8;
   if (p.stages < 2) return false;
@@ -619,7 +647,7 @@ dora_status fused_run(const void *x, const void *W0, const void *base, const voi
   // single CTAs for the lora form (its 12 K blocks per tile make the epilogue
   // the limit, and one CTA holds more staging per tile)
   const int max_pairs = g_max_pairs[device];
-  const bool pair = !lora_form && max_pairs > 0;
+  const bool pair = max_pairs > 0;
   FusedPlan fp;
   if (!plan_fused(T, in, out, r, lora_form, pair, pair ? max_pairs : sms, &fp)) return DORA_ERR_SHAPE;
   fp.p.g = g;

@@ -325,6 +325,10 @@ size_t dora_compose_fused_workspace(int64_t out, int64_t r);
  *   workspace  >= dora_compose_fused_workspace(out, r) bytes, 256-byte aligned
  *   Sizes: T, out >= 0 (either 0 is a no-op), r >= 1; out % 8 == 0 and
  *   r % 8 == 0 (16-byte rows for the tensor-memory copies).
+ * Two launches: the split of s B, then the fused kernel, as clusters of two
+ * CTAs (one 256 x 256 tile of y per pair, tcgen05.mma.cta_group::2) where
+ * the device can hold such clusters, else as single CTAs (128 x 256 tiles).
+ * Results are bitwise reproducible for a given shape and device.
  */
 dora_status dora_compose_lora_fwd(const void *base, const void *xa, const float *B,
                                   const float *g, float s,
@@ -338,7 +342,8 @@ dora_status dora_compose_lora_fwd(const void *base, const void *xa, const float 
  * epilogue: neither base nor lora is formed.  x [T, in] and W0 [out, in] are
  * bf16 (16-byte aligned, in % 8 == 0); the rest as dora_compose_lora_fwd.
  * Since base + s lora stays in fp32 until the single rounding of y, this is the
- * page's stable evaluation with one rounding fewer.
+ * page's stable evaluation with one rounding fewer.  Launches as
+ * dora_compose_lora_fwd.
  */
 dora_status dora_linear_fwd(const void *x, const void *W0, const void *xa, const float *B,
                             const float *g, float s,

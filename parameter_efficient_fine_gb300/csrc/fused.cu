@@ -18,24 +18,37 @@
 //
 // Operands are bf16, so every product is exact in fp32; the fp32 B is scaled
 // by s and split into bf16 hi + lo (|lo| <= 2^-9 |hi|, residual <= 2^-17 of
-// s B), and xa multiplies both (the xa segment of K appears twice, against hi
-// and against lo).  Accumulation is fp32 in tensor memory; y is rounded once
+// s B), and xa multiplies both (the xa segment of K is taken twice, against
+// hi and against lo).  Accumulation is fp32 in tensor memory; y is rounded once
 // to bf16.
 //
-// Kernel structure (persistent, one CTA per SM, 192 threads):
-//   warp 0      TMA producer: per K block a [128 x 64] bf16 box of the token
-//               side and a [256 x 64] box of the weight side (128-byte swizzle)
+// Kernel structure (persistent, one CTA per SM, 320 threads).  On GB300 both
+// forms run on CTA pairs (clusters of two CTAs on two SMs): one
+// tcgen05.mma.cta_group::2 computes an M = 256 x N = 256 tile, each CTA
+// holding 128 of the tokens and 128 of the weight rows, so an SM stages half
+// of the weight tile.  Without cluster support the same kernel runs single
+// CTAs on 128 x 256 tiles.
+//   warp 0      TMA producer (each CTA its own boxes): per stage the token
+//               boxes [128 x 64] and the weight boxes [128 x 64] (a pair;
+//               [256 x 64] for a single CTA), 128-byte swizzle.  A pair's
+//               stage is two K atoms of (x, W0) or one K atom of xa against
+//               both halves of s B (xa loaded once); all copies of a stage
+//               complete on the even CTA's barrier
 //   warp 1      allocates 512 tensor-memory columns (two 256-column
 //               accumulators, so a tile's epilogue overlaps the next tile's
-//               MMAs); one lane issues tcgen05.mma (M = 128, N = 256, K = 16)
-//   warps 2..5  epilogue: thread = row of the tile (its tensor-memory lane).
-//               Each warp owns 4 KB staging slots in shared memory for its 32
-//               rows (one [32 x 64] bf16 box, 128-byte swizzle) and runs its
-//               own pipeline: per 64-column quarter the accumulator columns,
-//               g (uniform 128-bit loads) and, for the lora form, the base
-//               quarter that the warp's lane 0 loaded into the slot by TMA
-//               one tile ahead; y is written into the slot in place and
-//               stored by TMA.  The epilogue warps never wait for one another
+//               MMAs); in the even CTA one lane issues the MMAs (8 per
+//               stage) and signals both CTAs' stage-free and accumulator
+//               barriers
+//   warps 2..9  epilogue, two warps per tensor-memory lane quadrant: thread =
+//               row of the tile (its tensor-memory lane), each warp two
+//               64-column quarters of the tile.  Each warp owns 4 KB staging
+//               slots in shared memory for its 32 rows (one [32 x 64] bf16
+//               box, 128-byte swizzle) and runs its own pipeline: per quarter
+//               the accumulator columns, g (uniform 128-bit loads) and, for
+//               the lora form, the base quarter that the warp's lane 0
+//               loaded into the slot by TMA one tile ahead; y is written
+//               into the slot in place and stored by TMA.  The epilogue
+//               warps never wait for one another
 // Every wait on a shared-memory barrier is bounded; a wait that gives up
 // records a code in the library's device error word and all roles drain and
 // leave.
@@ -642,10 +655,9 @@ dora_status fused_run(const void *x, const void *W0, const void *base, const voi
   int *errp = nullptr;
   st = fused_init(device, sms, &errp);
   if (st != DORA_OK) return st;
-  // CTA pairs for the linear form (its long K loop is bound by the MMA
-  // pipeline, which the pair's M = 256 tiles and 8-MMA stages feed better);
-  // single CTAs for the lora form (its 12 K blocks per tile make the epilogue
-  // the limit, and one CTA holds more staging per tile)
+  // CTA pairs wherever clusters of two can be resident: each SM stages half
+  // of the weight tile, the MMA lane waits once per 8 MMAs, and the lora
+  // form loads xa once for both halves of s B
   const int max_pairs = g_max_pairs[device];
   const bool pair = max_pairs > 0;
   FusedPlan fp;

@@ -856,8 +856,9 @@ fwd_norm_kernel(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
           }
           tc_fence_after();
           for (int kb = kb0; kb < kbe; ++kb) {
-            if (!wait_bounded(tconv0 + 8u * ss, sph, ctl, p.err, 2) ||
-                !wait_bounded(yfull0 + 8u * ss, sph, ctl, p.err, 7)) {
+            // the converters arrive once the slot is written AND its
+            // N-side tile has landed: one barrier wait per K block here
+            if (!wait_bounded(tconv0 + 8u * ss, sph, ctl, p.err, 2)) {
               ok = false;
               break;
             }
@@ -973,9 +974,19 @@ fwd_norm_kernel(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
           if (kb < f.kb1) n0 += blk;
           tc_fence_before();
           __syncwarp();
+          bool yok = true;
           if (lane == 0) {
             mbar_arrive(xempty0 + 8u * xs);   // the raw box is consumed
-            mbar_arrive(tconv0 + 8u * ss);    // the operand slot is written
+            // the operand slot is written; its arrival also waits for the
+            // stage's N-side tile, so that the MMA lane, whose every
+            // shared-memory access costs hundreds of cycles while MMAs are
+            // in flight, waits on one barrier per K block
+            yok = wait_bounded(yfull0 + 8u * ss, sph, ctl, p.err, 7);
+            if (yok) mbar_arrive(tconv0 + 8u * ss);
+          }
+          if (!__shfl_sync(0xffffffffu, yok ? 1 : 0, 0)) {
+            ok = false;
+            break;
           }
           if (++xs == SX) {
             xs = 0;

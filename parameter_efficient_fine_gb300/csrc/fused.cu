@@ -447,12 +447,12 @@ fused_compose_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_const
           tmem_ld32(lane_addr + col0 + 32, v[1]);
           uint8_t *crow = cbuf + slot_off(sl) + lane * 128;
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            // 16-byte chunk j of the row (8 columns), at its swizzled position
-            uint4 *pc = reinterpret_cast<uint4 *>(crow + ((j ^ (lane & 7)) << 4));
-            const float *a = &v[j >> 2][(j & 3) * 8];
-            const float gv[8] = {gq[2 * j].x, gq[2 * j].y, gq[2 * j].z, gq[2 * j].w,
-                                 gq[2 * j + 1].x, gq[2 * j + 1].y, gq[2 * j + 1].z, gq[2 * j + 1].w};
+          for (int c = 0; c < 8; ++c) {
+            // 16-byte chunk c of the row (8 columns), at its swizzled position
+            uint4 *pc = reinterpret_cast<uint4 *>(crow + ((c ^ (lane & 7)) << 4));
+            const float *a = &v[c >> 2][(c & 3) * 8];
+            const float gv[8] = {gq[2 * c].x, gq[2 * c].y, gq[2 * c].z, gq[2 * c].w,
+                                 gq[2 * c + 1].x, gq[2 * c + 1].y, gq[2 * c + 1].z, gq[2 * c + 1].w};
             float yv[8];
             if (p.has_base) {
               const uint4 braw = *pc;

@@ -1964,8 +1964,8 @@ bool plan_gemm(int mode, int M, int64_t in, int r, int max_ctas, GemmPlan *gp) {
   p.kb1 = static_cast<int>(dora::ceil_div(in, kBK));
   p.kbtot = p.kb1 + (mode != kGram ? static_cast<int>(dora::ceil_div(r, kBK)) : 0);
   // the N-side tile in nb boxes of nbox rows (a multiple of 8, so every box
-  // starts on a swizzle-pattern boundary)
-  p.nb = static_cast<int>(dora::ceil_div(p.NC, 128));
+  // starts on a swizzle-pattern boundary; at most 256, the box limit)
+  p.nb = static_cast<int>(dora::ceil_div(p.NC, 256));
   p.nbox = static_cast<int>(dora::round_up(dora::ceil_div(p.NC, p.nb), 8));
   p.NT = p.nb * p.nbox;
   p.nmma0 = p.NC <= 256 ? p.NC : 256;
@@ -2024,7 +2024,8 @@ void plan_phase(int mode, int M, int64_t in, int r, FwdPhase *f, int *mtiles) {
   }
   f->kb1 = static_cast<int>(dora::ceil_div(in, kFwdBK));
   f->kbtot = f->kb1 + (mode != kGram ? static_cast<int>(dora::ceil_div(r, kFwdBK)) : 0);
-  f->nb = static_cast<int>(dora::ceil_div(f->NC, 128));
+  // N-side TMA boxes of up to 256 rows (the box limit): fewer copies per stage
+  f->nb = static_cast<int>(dora::ceil_div(f->NC, 256));
   f->nbox = static_cast<int>(dora::round_up(dora::ceil_div(f->NC, f->nb), 8));
   f->nmma0 = f->NC <= 256 ? f->NC : 256;
   f->nmma1 = f->NC - f->nmma0;
@@ -2302,7 +2303,7 @@ bool plan16(int mode, int M, int64_t in, int r, int max_ctas, Plan16 *gp) {
     p.nchunks = static_cast<int>(dora::ceil_div(npad, p.NC));
     p.sym = 1;
   }
-  p.nb = static_cast<int>(dora::ceil_div(p.NC, 128));
+  p.nb = static_cast<int>(dora::ceil_div(p.NC, 256));   // N-side boxes of up to 256 rows
   p.nbox = static_cast<int>(dora::round_up(dora::ceil_div(p.NC, p.nb), 8));
   p.NT = p.nb * p.nbox;
   p.nmma0 = p.NC <= 256 ? p.NC : 256;

@@ -22,7 +22,8 @@
 // hi and against lo).  Accumulation is fp32 in tensor memory; y is rounded once
 // to bf16.
 //
-// Kernel structure (persistent, one CTA per SM, 320 threads).  On GB300 both
+// Kernel structure (persistent, one CTA per SM, 320 threads for the linear
+// form, 576 for the lora form).  On GB300 both
 // forms run on CTA pairs (clusters of two CTAs on two SMs): one
 // tcgen05.mma.cta_group::2 computes an M = 256 x N = 256 tile, each CTA
 // holding 128 of the tokens and 128 of the weight rows, so an SM stages half
@@ -39,9 +40,11 @@
 //               MMAs); in the even CTA one lane issues the MMAs (8 per
 //               stage) and signals both CTAs' stage-free and accumulator
 //               barriers
-//   warps 2..9  epilogue, two warps per tensor-memory lane quadrant: thread =
-//               row of the tile (its tensor-memory lane), each warp two
-//               64-column quarters of the tile.  Each warp owns 4 KB staging
+//   warps 2..   epilogue, thread = row of the tile (its tensor-memory lane):
+//               8 warps (linear form; two per tensor-memory lane quadrant,
+//               two 64-column quarters of the tile each) or 16 (lora form,
+//               whose epilogue is its limit; one quarter each, in two
+//               32-column passes).  Each warp owns 4 KB staging
 //               slots in shared memory for its 32 rows (one [32 x 64] bf16
 //               box, 128-byte swizzle) and runs its own pipeline: per quarter
 //               the accumulator columns, g (uniform 128-bit loads) and, for
@@ -67,9 +70,10 @@ constexpr int kFM = 128;        // tile rows (tokens) = tensor-memory lanes
 constexpr int kFN = 256;        // tile columns (outputs) = N of one MMA
 constexpr int kFK = 64;         // bf16 per K block: one 128-byte swizzled row
 constexpr int kFQ = 64;         // columns per epilogue quarter (one 128-byte box row)
-constexpr int kEpiWarps = 8;    // epilogue warps: two per tensor-memory lane quadrant
-constexpr int kQPW = 4 * 4 / kEpiWarps;   // 64-column quarters of a tile per epilogue warp
-constexpr int kFThreads = 64 + 32 * kEpiWarps;
+// epilogue warps: EPI = 8 (two per tensor-memory lane quadrant, two 64-column
+// quarters of a tile each) or 16 (four per quadrant, one quarter each, taken
+// in two 32-column halves to bound the registers of 576 threads)
+constexpr int fthreads(int epi) { return 64 + 32 * epi; }
 constexpr int kGroupM = 16;     // M tiles per tile-order group (L2 reuse of the weight tiles)
 constexpr int kFMaxCtas = 256;
 constexpr int kFSmemMax = 232448;
@@ -134,8 +138,8 @@ __device__ __forceinline__ bool fwait(uint32_t bar, uint32_t parity, SharedCtl *
 // K block instead of 48.  Both CTAs' copies of a stage complete on the even
 // CTA's stage barrier; the even CTA's lane issues the MMAs and signals both
 // CTAs' stage-free and accumulator barriers.
-template <bool PAIR>
-__global__ void __launch_bounds__(kFThreads, 1)
+template <bool PAIR, int EPI>
+__global__ void __launch_bounds__(fthreads(EPI), 1)
 fused_compose_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUtensorMap mA1,
                      const __grid_constant__ CUtensorMap mB0, const __grid_constant__ CUtensorMap mB1,
                      const __grid_constant__ CUtensorMap mB2, const __grid_constant__ CUtensorMap mC,
@@ -143,6 +147,11 @@ fused_compose_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_const
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int S = p.stages;
+  static_assert(EPI == 8 || EPI == 16, "8 or 16 epilogue warps");
+  constexpr int kEpiWarps = EPI;
+  constexpr int kQPW = 16 / EPI;   // 64-column quarters of a tile per epilogue warp
+  constexpr int kNH = EPI == 16 ? 2 : 1;   // passes per quarter
+  constexpr int kCP = kFQ / kNH;           // columns per pass
   constexpr unsigned kBRows = PAIR ? kFN / 2 : kFN;   // weight rows staged by this CTA
   // weight-side boxes (64 K wide) per stage: two for a pair (8 MMAs per stage
   // wait), one for a single CTA; the token-side boxes: p.na
@@ -434,45 +443,50 @@ fused_compose_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_const
             }
             __syncwarp();
           }
-          // g of the quarter's 64 columns: 16 uniform 128-bit loads issued
-          // together (one latency), zero past `out`
-          float4 gq[16];
-#pragma unroll
-          for (int k = 0; k < 16; ++k)
-            gq[k] = gcol0 + 4 * k < p.out ? __ldg(reinterpret_cast<const float4 *>(p.g + gcol0) + k)
-                                          : make_float4(0.f, 0.f, 0.f, 0.f);
-          float v[2][32];
-          const uint32_t col0 = static_cast<uint32_t>(buf * kFN + q * kFQ);
-          tmem_ld32(lane_addr + col0, v[0]);
-          tmem_ld32(lane_addr + col0 + 32, v[1]);
           uint8_t *crow = cbuf + slot_off(sl) + lane * 128;
 #pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            // 16-byte chunk c of the row (8 columns), at its swizzled position
-            uint4 *pc = reinterpret_cast<uint4 *>(crow + ((c ^ (lane & 7)) << 4));
-            const float *a = &v[c >> 2][(c & 3) * 8];
-            const float gv[8] = {gq[2 * c].x, gq[2 * c].y, gq[2 * c].z, gq[2 * c].w,
-                                 gq[2 * c + 1].x, gq[2 * c + 1].y, gq[2 * c + 1].z, gq[2 * c + 1].w};
-            float yv[8];
-            if (p.has_base) {
-              const uint4 braw = *pc;
-              const __nv_bfloat162 *bb = reinterpret_cast<const __nv_bfloat162 *>(&braw);
+          for (int hh = 0; hh < kNH; ++hh) {
+            // g of the pass's columns: uniform 128-bit loads issued together
+            // (one latency), zero past `out`
+            const int c0 = gcol0 + hh * kCP;
+            float4 gq[kCP / 4];
 #pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const float2 b2 = __bfloat1622float2(bb[e]);
-                yv[2 * e] = b2.x + fmaf(gv[2 * e] - 1.0f, b2.x, gv[2 * e] * a[2 * e]);
-                yv[2 * e + 1] = b2.y + fmaf(gv[2 * e + 1] - 1.0f, b2.y, gv[2 * e + 1] * a[2 * e + 1]);
+            for (int k = 0; k < kCP / 4; ++k)
+              gq[k] = c0 + 4 * k < p.out ? __ldg(reinterpret_cast<const float4 *>(p.g + c0) + k)
+                                         : make_float4(0.f, 0.f, 0.f, 0.f);
+            float v[kCP / 32][32];
+            const uint32_t col0 = static_cast<uint32_t>(buf * kFN + q * kFQ + hh * kCP);
+#pragma unroll
+            for (int w = 0; w < kCP / 32; ++w) tmem_ld32(lane_addr + col0 + 32 * w, v[w]);
+#pragma unroll
+            for (int c = 0; c < kCP / 8; ++c) {
+              // 16-byte chunk cq of the row (8 columns), at its swizzled position
+              const int cq = hh * (kCP / 8) + c;
+              uint4 *pc = reinterpret_cast<uint4 *>(crow + ((cq ^ (lane & 7)) << 4));
+              const float *a = &v[c >> 2][(c & 3) * 8];
+              const float gv[8] = {gq[2 * c].x, gq[2 * c].y, gq[2 * c].z, gq[2 * c].w,
+                                   gq[2 * c + 1].x, gq[2 * c + 1].y, gq[2 * c + 1].z, gq[2 * c + 1].w};
+              float yv[8];
+              if (p.has_base) {
+                const uint4 braw = *pc;
+                const __nv_bfloat162 *bb = reinterpret_cast<const __nv_bfloat162 *>(&braw);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  const float2 b2 = __bfloat1622float2(bb[e]);
+                  yv[2 * e] = b2.x + fmaf(gv[2 * e] - 1.0f, b2.x, gv[2 * e] * a[2 * e]);
+                  yv[2 * e + 1] = b2.y + fmaf(gv[2 * e + 1] - 1.0f, b2.y, gv[2 * e + 1] * a[2 * e + 1]);
+                }
+              } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) yv[e] = gv[e] * a[e];
               }
-            } else {
-#pragma unroll
-              for (int e = 0; e < 8; ++e) yv[e] = gv[e] * a[e];
+              uint4 o;
+              o.x = pack_bf16x2(yv[0], yv[1]);
+              o.y = pack_bf16x2(yv[2], yv[3]);
+              o.z = pack_bf16x2(yv[4], yv[5]);
+              o.w = pack_bf16x2(yv[6], yv[7]);
+              *pc = o;
             }
-            uint4 o;
-            o.x = pack_bf16x2(yv[0], yv[1]);
-            o.y = pack_bf16x2(yv[2], yv[3]);
-            o.z = pack_bf16x2(yv[4], yv[5]);
-            o.w = pack_bf16x2(yv[6], yv[7]);
-            *pc = o;
           }
           // make the writes visible to the TMA store, then lane 0 stores the
           // warp's 32 rows of the quarter
@@ -547,7 +561,8 @@ struct FusedPlan {
   FusedParams p;
   size_t smem_bytes;
   int ctas;
-  bool pair;   // CTA pairs (fused_compose_kernel<true>, clusters of two)
+  bool pair;   // CTA pairs (fused_compose_kernel<true, .>, clusters of two)
+  int epi;     // epilogue warps (the kernel instance)
 };
 
 // max_units: CTAs (one per SM) or, for pairs, the pairs that can be resident at once
@@ -556,6 +571,9 @@ bool plan_fused(int64_t T, int64_t in, int64_t out, int64_t r, bool has_base, bo
   FusedParams &p = fp->p;
   p = FusedParams{};
   fp->pair = pair;
+  // the lora form's epilogue (base read, y written per quarter) is its limit:
+  // 16 warps; the linear form's MMA loop is: 8 (fewer threads and registers)
+  fp->epi = has_base ? 16 : 8;
   p.T = static_cast<int>(T);
   p.out = static_cast<int>(out);
   p.nseg = has_base ? 2 : 3;
@@ -571,8 +589,8 @@ bool plan_fused(int64_t T, int64_t in, int64_t out, int64_t r, bool has_base, bo
   if (tiles >= (1ll << 31)) return false;
   p.tiles = static_cast<int>(tiles);
   p.has_base = has_base ? 1 : 0;
-  p.nslots = has_base ? kQPW : 1;
-  const size_t fixed = 1024 + static_cast<size_t>(p.nslots) * kEpiWarps * kSlotBytes + 512;
+  p.nslots = has_base ? 16 / fp->epi : 1;
+  const size_t fixed = 1024 + static_cast<size_t>(p.nslots) * fp->epi * kSlotBytes + 512;
   // a pair: two token-side boxes per stage for the linear form's (x, W0)
   // segment, one for the lora form; two half weight boxes.  A single CTA: one
   // token-side box and one weight box
@@ -595,16 +613,17 @@ bool map_bf16(CUtensorMap *map, const void *base, int64_t rows, int64_t cols, in
 
 int *g_stall_ptr[64] = {};
 unsigned long long *g_limit_ptr[64] = {};
-int g_max_pairs[64] = {};   // clusters of two of fused_compose_kernel<true> resident at once
+int g_max_pairs[64] = {};   // clusters of two of fused_compose_kernel<true, .> resident at once
 
 // launch configuration of the pair kernel: clusters of two CTAs along x
-void pair_config(cudaLaunchConfig_t *cfg, cudaLaunchAttribute *attr, unsigned ctas, size_t smem, cudaStream_t cs) {
+void pair_config(cudaLaunchConfig_t *cfg, cudaLaunchAttribute *attr, unsigned ctas, unsigned threads, size_t smem,
+                 cudaStream_t cs) {
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg->gridDim = dim3(ctas);
-  cfg->blockDim = dim3(kFThreads);
+  cfg->blockDim = dim3(threads);
   cfg->dynamicSmemBytes = smem;
   cfg->stream = cs;
   cfg->attrs = attr;
@@ -623,15 +642,17 @@ dora_status fused_init(int device, int sms, int **errp) {
   const uint64_t ctx = dora::context_id();
   if (ctx == 0 || ctx != done_ctx[device]) {
     const auto a = cudaFuncAttributeMaxDynamicSharedMemorySize;
-    if (cudaFuncSetAttribute(fused_compose_kernel<false>, a, kFSmemMax) != cudaSuccess ||
-        cudaFuncSetAttribute(fused_compose_kernel<true>, a, kFSmemMax) != cudaSuccess)
+    if (cudaFuncSetAttribute(fused_compose_kernel<false, 8>, a, kFSmemMax) != cudaSuccess ||
+        cudaFuncSetAttribute(fused_compose_kernel<true, 8>, a, kFSmemMax) != cudaSuccess ||
+        cudaFuncSetAttribute(fused_compose_kernel<false, 16>, a, kFSmemMax) != cudaSuccess ||
+        cudaFuncSetAttribute(fused_compose_kernel<true, 16>, a, kFSmemMax) != cudaSuccess)
       return DORA_ERR_CUDA;
     // pairs resident at once with the largest shared-memory footprint (one CTA per SM)
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
-    pair_config(&cfg, attr, static_cast<unsigned>(2 * (sms / 2)), kFSmemMax, nullptr);
+    pair_config(&cfg, attr, static_cast<unsigned>(2 * (sms / 2)), fthreads(16), kFSmemMax, nullptr);
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, fused_compose_kernel<true>, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&n, fused_compose_kernel<true, 16>, &cfg) != cudaSuccess) {
       cudaGetLastError();
       n = 0;
     }
@@ -697,14 +718,22 @@ dora_status fused_run(const void *x, const void *W0, const void *base, const voi
   if (pair) {
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
-    pair_config(&cfg, attr, static_cast<unsigned>(fp.ctas), fp.smem_bytes, cs);
-    if (cudaLaunchKernelEx(&cfg, fused_compose_kernel<true>, mA0, mA1, mB0, mB1, mB2, mC, mY, fp.p) != cudaSuccess) {
+    pair_config(&cfg, attr, static_cast<unsigned>(fp.ctas), fthreads(fp.epi), fp.smem_bytes, cs);
+    const cudaError_t e = fp.epi == 16
+                              ? cudaLaunchKernelEx(&cfg, fused_compose_kernel<true, 16>, mA0, mA1, mB0, mB1, mB2, mC, mY,
+                                                   fp.p)
+                              : cudaLaunchKernelEx(&cfg, fused_compose_kernel<true, 8>, mA0, mA1, mB0, mB1, mB2, mC, mY,
+                                                   fp.p);
+    if (e != cudaSuccess) {
       dora::count_launches(launches);
       return DORA_ERR_CUDA;
     }
   } else {
-    fused_compose_kernel<false><<<static_cast<unsigned>(fp.ctas), kFThreads, fp.smem_bytes, cs>>>(
-        mA0, mA1, mB0, mB1, mB2, mC, mY, fp.p);
+    const unsigned th = static_cast<unsigned>(fthreads(fp.epi)), nb = static_cast<unsigned>(fp.ctas);
+    if (fp.epi == 16)
+      fused_compose_kernel<false, 16><<<nb, th, fp.smem_bytes, cs>>>(mA0, mA1, mB0, mB1, mB2, mC, mY, fp.p);
+    else
+      fused_compose_kernel<false, 8><<<nb, th, fp.smem_bytes, cs>>>(mA0, mA1, mB0, mB1, mB2, mC, mY, fp.p);
   }
   ++launches;
   dora::count_launches(launches);

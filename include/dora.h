@@ -377,6 +377,15 @@ uint64_t dora_kernel_launches(void);
  */
 dora_status dora_test_stall_loads(int on, uint64_t wait_limit_ns);
 
+/*
+ * Testing hook; no counterpart in the paper.  With allow = 0, later
+ * dora_compose_lora_fwd and dora_linear_fwd calls run their fused kernel as
+ * single CTAs (128 x 256 tiles), as on a device that cannot hold clusters of
+ * two; allow != 0 (the default) restores CTA pairs where the device has them.
+ * Process-wide; never fails.
+ */
+dora_status dora_test_fused_pairs(int allow);
+
 #ifdef __cplusplus
 }
 #endif

@@ -33,6 +33,7 @@ __all__ = [
     "dora_device_error",
     "dora_kernel_launches",
     "dora_test_stall_loads",
+    "dora_test_fused_pairs",
     "DORA_F32",
     "DORA_BF16",
 ]
@@ -69,6 +70,7 @@ _SIGNATURES = {
     "dora_device_error": (_int, [ctypes.POINTER(_int)]),
     "dora_kernel_launches": (ctypes.c_uint64, []),
     "dora_test_stall_loads": (_int, [_int, ctypes.c_uint64]),
+    "dora_test_fused_pairs": (_int, [_int]),
 }
 
 
@@ -256,3 +258,8 @@ def dora_kernel_launches() -> int:
 def dora_test_stall_loads(on: bool, wait_limit_ns: int = 0) -> None:
     """Testing hook: make later norm calls' bounded waits expire (see include/dora.h)."""
     _check("dora_test_stall_loads", load_library().dora_test_stall_loads(1 if on else 0, int(wait_limit_ns)))
+
+
+def dora_test_fused_pairs(allow: bool) -> None:
+    """Testing hook: run the fused kernels as single CTAs when False (see include/dora.h)."""
+    _check("dora_test_fused_pairs", load_library().dora_test_fused_pairs(1 if allow else 0))

@@ -59,6 +59,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "common.cuh"
@@ -614,6 +615,7 @@ bool map_bf16(CUtensorMap *map, const void *base, int64_t rows, int64_t cols, in
 int *g_stall_ptr[64] = {};
 unsigned long long *g_limit_ptr[64] = {};
 int g_max_pairs[64] = {};   // clusters of two of fused_compose_kernel<true, .> resident at once
+std::atomic<int> g_pairs_allowed{1};   // test hook (dora_test_fused_pairs)
 
 // launch configuration of the pair kernel: clusters of two CTAs along x
 void pair_config(cudaLaunchConfig_t *cfg, cudaLaunchAttribute *attr, unsigned ctas, unsigned threads, size_t smem,
@@ -680,7 +682,7 @@ dora_status fused_run(const void *x, const void *W0, const void *base, const voi
   // of the weight tile, the MMA lane waits once per 8 MMAs, and the lora
   // form loads xa once for both halves of s B
   const int max_pairs = g_max_pairs[device];
-  const bool pair = max_pairs > 0;
+  const bool pair = max_pairs > 0 && g_pairs_allowed.load() != 0;
   FusedPlan fp;
   if (!plan_fused(T, in, out, r, lora_form, pair, pair ? max_pairs : sms, &fp)) return DORA_ERR_SHAPE;
   fp.p.g = g;
@@ -788,4 +790,9 @@ extern "C" dora_status dora_linear_fwd(const void *x, const void *W0, const void
   if (st != DORA_OK) return st;
   if (in % 8 != 0 || !dora::aligned(x, 16) || !dora::aligned(W0, 16)) return DORA_ERR_ALIGN;
   return fused_run(x, W0, nullptr, xa, B, g, s, T, in, out, r, y, workspace, workspace_bytes, stream);
+}
+
+extern "C" dora_status dora_test_fused_pairs(int allow) {
+  g_pairs_allowed.store(allow ? 1 : 0);
+  return DORA_OK;
 }

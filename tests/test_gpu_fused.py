@@ -21,6 +21,15 @@ pytestmark = pytest.mark.gpu
 CR_MIN = 0.95    # fraction of outputs that are the correctly rounded bf16 of the exact result
 
 
+@pytest.fixture(params=["pairs", "single"])
+def layout(request):
+    """The fused kernel on CTA pairs (the default on GB300) or as single CTAs
+    (the layout of a device without clusters of two, forced by the test hook)."""
+    dora.dora_test_fused_pairs(request.param == "pairs")
+    yield request.param
+    dora.dora_test_fused_pairs(True)
+
+
 def _layer(T, inp, out, r, seed):
     sh = wl.shape("high_rank", T=T, inp=inp, out=out, r=r)
     return wl.make_layer(sh, seed)
@@ -67,7 +76,7 @@ def _f64(bits):
     (513, 4096, 768),    # many output tiles, a single-row last token tile
     (1, 264, 64),        # one token
 ])
-def test_lora_form(T, out, r):
+def test_lora_form(T, out, r, layout):
     d = _layer(T, 16, out, r, 9500 + T + out + r)
     y = run_lora(d)
     assert_no_device_error()
@@ -83,7 +92,7 @@ def test_lora_form(T, out, r):
     (640, 4096, 1024, 64),   # long K
     (200, 520, 4104, 24),    # 17 output tiles, the last one 8 columns wide
 ])
-def test_linear_form(T, inp, out, r):
+def test_linear_form(T, inp, out, r, layout):
     d = _layer(T, inp, out, r, 9600 + T + inp + out + r)
     y = run_linear(d)
     assert_no_device_error()
@@ -91,7 +100,7 @@ def test_linear_form(T, inp, out, r):
     _check("y (linear form)", y, ref)
 
 
-def test_bitwise_reproducible():
+def test_bitwise_reproducible(layout):
     d = _layer(300, 264, 520, 40, 9700)
     assert torch.equal(run_linear(d), run_linear(d))
     assert torch.equal(run_lora(d), run_lora(d))

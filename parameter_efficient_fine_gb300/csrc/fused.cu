@@ -75,7 +75,7 @@ constexpr int kFQ = 64;         // columns per epilogue quarter (one 128-byte bo
 // quarters of a tile each) or 16 (four per quadrant, one quarter each, taken
 // in two 32-column halves to bound the registers of 576 threads)
 constexpr int fthreads(int epi) { return 64 + 32 * epi; }
-constexpr int kGroupM = 16;     // M tiles per tile-order group (L2 reuse of the weight tiles)
+constexpr int kGroupM = 16;     // M tiles per tile-order group of the linear form (L2 reuse of W0's tiles)
 constexpr int kFMaxCtas = 256;
 constexpr int kFSmemMax = 232448;
 constexpr unsigned kABytes = kFM * kFK * 2;     // 16 KB
@@ -93,6 +93,7 @@ struct FusedParams {
   int na;               // token-side boxes per stage (a pair's linear form: 2)
   unsigned stage_bytes; // na token-side boxes + the weight-side boxes
   int nslots;           // staging slots per epilogue warp: one per quarter with base, else one
+  int groupm;           // M tiles per tile-order group (tile_mn)
   int has_base;
   const float *g;
   int *err;
@@ -100,11 +101,13 @@ struct FusedParams {
   const unsigned long long *limit_ns;    // limit of the bounded waits
 };
 
-__device__ __forceinline__ void tile_mn(int t, int mtiles, int ntiles, int *mt, int *nt) {
-  const int per = kGroupM * ntiles;
+// tile t's (M tile, N tile): groups of `group` M tiles, column by column
+// within a group (group = 1: row by row)
+__device__ __forceinline__ void tile_mn(int t, int mtiles, int ntiles, int group, int *mt, int *nt) {
+  const int per = group * ntiles;
   const int grp = t / per;
-  const int m0 = grp * kGroupM;
-  const int gm = min(kGroupM, mtiles - m0);
+  const int m0 = grp * group;
+  const int gm = min(group, mtiles - m0);
   const int r = t - grp * per;
   *mt = m0 + r % gm;
   *nt = r / gm;
@@ -234,7 +237,7 @@ fused_compose_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_const
       bool ok = *reinterpret_cast<const volatile int *>(p.stall) == 0;
       for (int t = cta; t < p.tiles && ok; t += ncta) {
         int mt, nt;
-        tile_mn(t, p.mtiles, p.ntiles, &mt, &nt);
+        tile_mn(t, p.mtiles, p.ntiles, p.groupm, &mt, &nt);
         // the tile's K blocks, segment after segment (the lora form has none in segment 0)
         for (int kb = 0; kb < p.kbtot && ok; ++kb) {
           if (!fwait(empty0 + 8u * stage, phase ^ 1u, ctl, p, 12)) {
@@ -390,7 +393,7 @@ fused_compose_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_const
     uint32_t any_load = 0, load_par = 0;
     auto load_base = [&](int t, int j) {
       int mt, nt;
-      tile_mn(t, p.mtiles, p.ntiles, &mt, &nt);
+      tile_mn(t, p.mtiles, p.ntiles, p.groupm, &mt, &nt);
       mbar_expect_tx(cfull(j), kSlotBytes);
       tma_load_2d(cbase + slot_off(j), &mC, nt * kFN + (qb + j) * kFQ,
                   mt * kTileRows + static_cast<int>(crank) * kFM + quad * 32, cfull(j));
@@ -407,7 +410,7 @@ fused_compose_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_const
     bool ok = true;
     for (int t = cta; t < p.tiles && ok; t += ncta, ++li) {
       int mt, nt;
-      tile_mn(t, p.mtiles, p.ntiles, &mt, &nt);
+      tile_mn(t, p.mtiles, p.ntiles, p.groupm, &mt, &nt);
       const int tnext = t + ncta;
       const int buf = li & 1;
       const uint32_t use = static_cast<uint32_t>(li >> 1);
@@ -591,6 +594,11 @@ bool plan_fused(int64_t T, int64_t in, int64_t out, int64_t r, bool has_base, bo
   p.tiles = static_cast<int>(tiles);
   p.has_base = has_base ? 1 : 0;
   p.nslots = has_base ? 16 / fp->epi : 1;
+  // tile order: the linear form in groups of kGroupM M tiles (W0's tiles,
+  // 134 MB at the high-rank layer, are re-read from L2 across the group); the
+  // lora form, whose operands stay in L2, row by row, so that concurrent
+  // tiles cover whole row segments of base and y
+  p.groupm = has_base ? 1 : kGroupM;
   const size_t fixed = 1024 + static_cast<size_t>(p.nslots) * fp->epi * kSlotBytes + 512;
   // a pair: two token-side boxes per stage for the linear form's (x, W0)
   // segment, one for the lora form; two half weight boxes.  A single CTA: one

@@ -50,10 +50,11 @@
 // Tiles in shared memory are K-major with the swizzle of one K block per row:
 // the raw fp32 box 128-byte rows (128-byte swizzle), the bf16 N-side boxes
 // 64-byte rows (64-byte swizzle).  Tensor memory holds the accumulator and one
-// operand slot per stage.  The work is the list of (M tile, N chunk, K block) units, split evenly over the
-// CTAs; a CTA's range crosses at most a few tile boundaries, and each piece
-// ("segment") leaves one partial result.  All partial sums are combined in a
-// fixed order, so results are bitwise reproducible.
+// operand slot per stage.  The work is the list of (M tile, N chunk, K block)
+// units, split evenly over the CTAs; a CTA's range crosses at most a few tile
+// boundaries, and each piece ("segment") leaves one partial result.  All
+// partial sums are combined in a fixed order, so results are bitwise
+// reproducible.
 //
 // Every wait on a shared-memory barrier (and, in fwd_norm_kernel, on a global
 // counter) is bounded (kWaitLimitNs).  A wait that gives up sets a CTA abort
@@ -197,7 +198,7 @@ __device__ bool wait_bounded(uint32_t bar, uint32_t parity, SharedCtl *ctl, int 
 __device__ void wait_drain(uint32_t bar, uint32_t parity) { wait_drain_ns(bar, parity, kWaitLimitNs); }
 
 // ---------------------------------------------------------------------------
-// the tensor-core GEMM (GRAM, NORM or ROWS mode)
+// the tensor-core GEMM of the gradient passes (GRAM or ROWS mode)
 //
 // XT: the M-side operand is stored K-major-transposed in global memory (its
 // rows are K indices, its columns M indices, as W0 is for W0^T): the producer
@@ -1252,12 +1253,6 @@ fwd_norm_kernel(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
 // elementwise helpers
 // ---------------------------------------------------------------------------
 
-// N-side split of a [rows, cols] fp32 matrix (cols % 4 == 0), and zero fill of
-// the norm pass's ncnt completion counters:
-//   hi [rows, cols] fp32: x rounded to TF32
-//   c  [rows, 2*cols8] bf16 (cols8 = cols rounded up to 8): per group q of 8
-//      columns, 8 bf16(hi) then 8 bf16(x - hi); zero past cols
-// One thread per group of 4 columns.
 // N-side split of a [rows, cols] fp32 matrix for the bf16 three-product
 // scheme, and zero fill of the norm pass's ncnt completion counters:
 //   h [rows, cols8] bf16: x rounded to bf16 (nearest even)

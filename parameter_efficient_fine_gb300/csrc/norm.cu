@@ -558,9 +558,11 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ 
 //   warp 6      lane 0: TMA producer of the N-side h and l tiles [NT x 32 bf16]
 // ---------------------------------------------------------------------------
 constexpr int kFwdThreads = 224;
-constexpr int kFwdBK = 32;                       // K indices per K block
-constexpr int kFwdXBytes = kBM * kFwdBK * 4;     // one raw M-side box (128-byte rows)
-constexpr int kFwdNRow = kFwdBK * 2;             // one N-side row of h or l (64 bytes)
+// K indices per K block of fwd_norm_kernel<FBK>: 32, or 64 where the
+// accumulator leaves tensor memory for at least four 64-column operand slots
+// (N <= 256): half the barrier waits and slot releases per W0 byte
+constexpr int kFwdBox = 32;                      // K indices of one raw M-side box (128-byte rows)
+constexpr int kFwdBoxBytes = kBM * kFwdBox * 4;  // 16 KB
 constexpr int kFwdMaxX = 16;
 constexpr int kFwdMaxS = 8;
 constexpr int kGramPieces = 16;                  // CTAs (K pieces) per Gram tile, at most
@@ -583,6 +585,7 @@ struct FwdPhase {
 
 struct FwdParams {
   FwdPhase ph[2];   // 0: Gram, 1: norm
+  int fbk;          // K indices per K block (the kernel instance)
   int M;            // out (rows of the norm phase)
   int r, npad;
   int NT;           // N-side rows of a stage (the larger phase's)
@@ -686,6 +689,7 @@ __device__ __forceinline__ void store_gs3(__nv_bfloat16 *gh, __nv_bfloat16 *gl, 
   gl[i] = __float2bfloat16_rn(v - __bfloat162float(h));
 }
 
+template <int FBK>
 __global__ void __launch_bounds__(kFwdThreads, 1)
 fwd_norm_kernel(const __grid_constant__ CUtensorMap mA, const __grid_constant__ CUtensorMap mW0,
                 const __grid_constant__ CUtensorMap mB, const __grid_constant__ CUtensorMap mAh_g,
@@ -695,6 +699,11 @@ fwd_norm_kernel(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
                 const FwdParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  static_assert(FBK == 32 || FBK == 64, "K blocks of 32 or 64");
+  constexpr int kFwdBK = FBK;                        // K indices per K block
+  constexpr int kXBoxes = FBK / kFwdBox;             // raw 32-wide boxes per raw-box slot
+  constexpr int kFwdXBytes = kXBoxes * kFwdBoxBytes; // one raw-box slot
+  constexpr int kFwdNRow = FBK * 2;                  // one N-side row of h or l (64 or 128 bytes)
   const int S = p.S, SX = p.SX;
   uint8_t *xring = smem;
   uint8_t *yring = smem + static_cast<size_t>(SX) * kFwdXBytes;
@@ -799,7 +808,10 @@ fwd_norm_kernel(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
             if (xside) {
               mbar_expect_tx(fb, kFwdXBytes);
               const CUtensorMap *mx = ph == 0 ? &mA : (seg1 ? &mW0 : &mB);
-              tma_load_2d(smem_u32(xring + static_cast<size_t>(slot) * kFwdXBytes), mx, kx, mt * kBM, fb);
+#pragma unroll
+              for (int b = 0; b < kXBoxes; ++b)
+                tma_load_2d(smem_u32(xring + static_cast<size_t>(slot) * kFwdXBytes + b * kFwdBoxBytes), mx,
+                            kx + kFwdBox * b, mt * kBM, fb);
             } else {
               const uint32_t ntile = static_cast<uint32_t>(f.nb * f.nbox) * kFwdNRow;
               mbar_expect_tx(fb, 2u * ntile);
@@ -945,8 +957,8 @@ fwd_norm_kernel(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
             break;
           }
           tc_fence_after();
-          const float4 *xr = reinterpret_cast<const float4 *>(xring + static_cast<size_t>(xs) * kFwdXBytes +
-                                                              row * (kFwdBK * 4));
+          // row `row` of raw box b: 32 fp32 in 8 16-byte chunks, swizzled
+          const uint8_t *xrow = xring + static_cast<size_t>(xs) * kFwdXBytes + row * (kFwdBox * 4);
           const uint32_t slot = lane_addr + static_cast<uint32_t>(p.slot0 + ss * kFwdBK);
           float blk = 0.0f;
 #pragma unroll
@@ -955,7 +967,9 @@ fwd_norm_kernel(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
               const int q = 2 * q16 + half;
-              const float4 a = xr[swz_chunk<kFwdBK>(2 * q, row)], b = xr[swz_chunk<kFwdBK>(2 * q + 1, row)];
+              const float4 *xr = reinterpret_cast<const float4 *>(xrow + (q >> 2) * kFwdBoxBytes);
+              const int qq = q & 3;   // group of 8 K within the box
+              const float4 a = xr[swz_chunk<kFwdBox>(2 * qq, row)], b = xr[swz_chunk<kFwdBox>(2 * qq + 1, row)];
               const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
 #pragma unroll
               for (int e = 0; e < 4; ++e) {
@@ -2007,7 +2021,7 @@ struct FwdPlan {
 };
 
 // one phase over M rows (Gram: M = r, N = r; norm: M = out, N = r, K tail r)
-void plan_phase(int mode, int M, int64_t in, int r, FwdPhase *f, int *mtiles) {
+void plan_phase(int mode, int M, int64_t in, int r, int fbk, FwdPhase *f, int *mtiles) {
   std::memset(f, 0, sizeof(*f));
   int npad;
   plan_n(r, &npad, &f->nchunks, &f->NC);
@@ -2017,8 +2031,8 @@ void plan_phase(int mode, int M, int64_t in, int r, FwdPhase *f, int *mtiles) {
     f->nchunks = static_cast<int>(dora::ceil_div(npad, f->NC));
     f->sym = 1;
   }
-  f->kb1 = static_cast<int>(dora::ceil_div(in, kFwdBK));
-  f->kbtot = f->kb1 + (mode != kGram ? static_cast<int>(dora::ceil_div(r, kFwdBK)) : 0);
+  f->kb1 = static_cast<int>(dora::ceil_div(in, fbk));
+  f->kbtot = f->kb1 + (mode != kGram ? static_cast<int>(dora::ceil_div(r, fbk)) : 0);
   // N-side TMA boxes of up to 256 rows (the box limit): fewer copies per stage
   f->nb = static_cast<int>(dora::ceil_div(f->NC, 256));
   f->nbox = static_cast<int>(dora::round_up(dora::ceil_div(f->NC, f->nb), 8));
@@ -2070,14 +2084,23 @@ void balance_split(long long U, int kbtot, int C, int g, double t_unit, double t
   fill(hi, true);
 }
 
-// with_split = false: the geometry and workspace only (no CTA ranges)
-bool plan_fwd(int64_t out, int64_t in, int64_t r, int max_ctas, FwdPlan *fp, bool with_split = true) {
+// with_split = false: the geometry and workspace only (no CTA ranges);
+// fbk: K indices per K block (32 or 64; 0 = 64 where at least three 64-wide
+// stages fit into tensor and shared memory, else 32)
+bool plan_fwd(int64_t out, int64_t in, int64_t r, int max_ctas, FwdPlan *fp, bool with_split = true, int fbk = 0) {
+  if (fbk == 0) {
+    if (plan_fwd(out, in, r, max_ctas, fp, with_split, 64) && fp->p.S >= 3) return true;
+    return plan_fwd(out, in, r, max_ctas, fp, with_split, 32);
+  }
   FwdParams &p = fp->p;
   std::memset(&p, 0, sizeof(p));
   const int ri = static_cast<int>(r);
+  p.fbk = fbk;
+  const int xbytes = (fbk / kFwdBox) * kFwdBoxBytes;   // one raw-box slot
+  const int nrow = fbk * 2;                            // one N-side row of h or l
   int mt_g, mt_n;
-  plan_phase(kGram, ri, in, ri, &p.ph[0], &mt_g);
-  plan_phase(kNorm, static_cast<int>(out), in, ri, &p.ph[1], &mt_n);
+  plan_phase(kGram, ri, in, ri, fbk, &p.ph[0], &mt_g);
+  plan_phase(kNorm, static_cast<int>(out), in, ri, fbk, &p.ph[1], &mt_n);
   FwdPhase &fg = p.ph[0], &fn = p.ph[1];
   p.M = static_cast<int>(out);
   p.r = ri;
@@ -2087,22 +2110,22 @@ bool plan_fwd(int64_t out, int64_t in, int64_t r, int max_ctas, FwdPlan *fp, boo
   p.NT = nt_g > nt_n ? nt_g : nt_n;
   const int acc_cols = static_cast<int>(dora::round_up(fn.nmma1 > 0 ? 256 + fn.nmma1 : fn.nmma0, 32));
   p.slot0 = acc_cols;
-  p.y_bytes = static_cast<unsigned>(p.NT * 2 * kFwdNRow);
+  p.y_bytes = static_cast<unsigned>(p.NT * 2 * nrow);
   // shared memory: as many N-side stages as tensor memory and shared memory
   // allow while leaving at least two more raw-box slots than stages; the rest
   // goes to raw-box slots
   const size_t fixed = 1024 + 8 * (2 * kFwdMaxX + 3 * kFwdMaxS + 7) + 64;
   const size_t budget = kSmemMax - fixed;
-  int S = (512 - acc_cols) / kFwdBK;
+  int S = (512 - acc_cols) / fbk;
   if (S > kFwdMaxS) S = kFwdMaxS;
-  while (S >= 2 && static_cast<size_t>(S) * p.y_bytes + static_cast<size_t>(S + 2) * kFwdXBytes > budget) --S;
+  while (S >= 2 && static_cast<size_t>(S) * p.y_bytes + static_cast<size_t>(S + 2) * xbytes > budget) --S;
   if (S < 2) return false;
-  int SX = static_cast<int>((budget - static_cast<size_t>(S) * p.y_bytes) / kFwdXBytes);
+  int SX = static_cast<int>((budget - static_cast<size_t>(S) * p.y_bytes) / xbytes);
   if (SX > kFwdMaxX) SX = kFwdMaxX;
   p.S = S;
   p.SX = SX;
   int cols = 32;
-  while (cols < acc_cols + S * kFwdBK) cols *= 2;
+  while (cols < acc_cols + S * fbk) cols *= 2;
   p.tmem_cols = cols;
   // one CTA per SM, all co-resident: at most max_ctas, at least ... one unit
   // each of the norm phase
@@ -2117,13 +2140,14 @@ bool plan_fwd(int64_t out, int64_t in, int64_t r, int max_ctas, FwdPlan *fp, boo
   // Cost model measured on GB300: a Gram unit about 0.6 us (latency-bound),
   // a norm unit 0.1 us + 3 N tensor cycles at 1.6 GHz and no less than
   // 0.5 us, a group of reduction loads 1.5 us.
-  const double t_norm = std::max(0.5, 0.1 + 3.0 * fn.NC / 1600.0);
+  const double kscale = fbk / 32.0;   // the unit costs below are for 32-wide K blocks
+  const double t_norm = std::max(0.5, 0.1 + 3.0 * fn.NC / 1600.0) * kscale;
   // Gram phase: P pieces per tile, one CTA each (the first P * tiles CTAs):
   // about a third of the grid, and enough pieces that the Gram phase takes
   // at most ~35% of a CTA's norm work (s/2 G is needed only after most of it)
   const double t_share = static_cast<double>(fn.units) / p.ctas * t_norm;
   int P = p.ctas / (3 * fg.tiles);
-  const int need = static_cast<int>(std::ceil(fg.kbtot * 0.6 / (0.35 * t_share)));
+  const int need = static_cast<int>(std::ceil(fg.kbtot * 0.6 * kscale / (0.35 * t_share)));
   if (P < need) P = need;
   if (P > kGramPieces) P = kGramPieces;
   if (P > fg.kbtot) P = fg.kbtot;
@@ -2137,18 +2161,19 @@ bool plan_fwd(int64_t out, int64_t in, int64_t r, int max_ctas, FwdPlan *fp, boo
   // an epilogue and the pipeline restart behind it, 1 us + 12.5 us x N / 384
   fn.ctas = p.ctas;
   const int nsub = (fg.NC + 31) / 32;
-  const double t_gram = fg.kbtot / static_cast<double>(P) * 0.75 + 1.2 + 1.6 * ((nsub * nsub + P - 1) / P);
+  const double t_gram =
+      fg.kbtot / static_cast<double>(P) * 0.75 * kscale + 1.2 + 1.6 * ((nsub * nsub + P - 1) / P);
   const double t_seg = 1.0 + 12.5 * fn.NC / 384.0;
   if (with_split) balance_split(fn.units, fn.kbtot, p.ctas, fg.ctas, t_norm, t_seg, t_gram, p.ub);
 
   p.nsync = 1 + fg.tiles;
   fp->part_g_bytes = static_cast<size_t>(fg.ctas) * kBM * fg.NC * sizeof(float);
   fp->part_n_bytes = static_cast<size_t>(fn.tiles + p.ctas) * kBM * 2 * sizeof(float);
-  fp->smem_bytes = static_cast<size_t>(SX) * kFwdXBytes + static_cast<size_t>(S) * p.y_bytes + 1024 +
+  fp->smem_bytes = static_cast<size_t>(SX) * xbytes + static_cast<size_t>(S) * p.y_bytes + 1024 +
                    8 * (2 * SX + 3 * S + 7) + 64;
   // the last epilogue's B staging: 4 warps x 32 rows x (N chunk) fp32
   const size_t stage = 4 * static_cast<size_t>((fn.NC + 31) / 32) * 4096;
-  p.stage_b = stage <= static_cast<size_t>(SX) * kFwdXBytes + static_cast<size_t>(S) * p.y_bytes ? 1 : 0;
+  p.stage_b = stage <= static_cast<size_t>(SX) * xbytes + static_cast<size_t>(S) * p.y_bytes ? 1 : 0;
   if (p.tmem_cols > 256 && fp->smem_bytes < 116 * 1024) fp->smem_bytes = 116 * 1024;
   return true;
 }
@@ -2169,7 +2194,9 @@ cudaError_t launch_fwd(const FwdPlan &fp, cudaStream_t cs, const CUtensorMap &mA
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, fwd_norm_kernel, mA, mW0, mB, mAh_g, mAl_g, mAh_n, mAl_n, mGh, mGl, mBs, fp.p);
+  if (fp.p.fbk == 64)
+    return cudaLaunchKernelEx(&cfg, fwd_norm_kernel<64>, mA, mW0, mB, mAh_g, mAl_g, mAh_n, mAl_n, mGh, mGl, mBs, fp.p);
+  return cudaLaunchKernelEx(&cfg, fwd_norm_kernel<32>, mA, mW0, mB, mAh_g, mAl_g, mAh_n, mAl_n, mGh, mGl, mBs, fp.p);
 }
 
 // forward-norm workspace (bf16 three-product scheme): the N-side split of A
@@ -2396,7 +2423,8 @@ dora_status device_init(int device, int **errp) {
     const cudaFuncAttribute a = cudaFuncAttributeMaxDynamicSharedMemorySize;
     if (cudaFuncSetAttribute(tc_gemm_kernel<false>, a, kSmemMax) != cudaSuccess ||
         cudaFuncSetAttribute(tc_gemm_kernel<true>, a, kSmemMax) != cudaSuccess ||
-        cudaFuncSetAttribute(fwd_norm_kernel, a, kSmemMax) != cudaSuccess ||
+        cudaFuncSetAttribute(fwd_norm_kernel<32>, a, kSmemMax) != cudaSuccess ||
+        cudaFuncSetAttribute(fwd_norm_kernel<64>, a, kSmemMax) != cudaSuccess ||
         cudaFuncSetAttribute(tc16_kernel<32>, a, kSmemMax) != cudaSuccess ||
         cudaFuncSetAttribute(tc16_kernel<64>, a, kSmemMax) != cudaSuccess)
       return DORA_ERR_CUDA;
@@ -2613,13 +2641,14 @@ extern "C" dora_status dora_norm_factored(const float *W0, const float *A, const
   CUtensorMap mp[10];
   if (!find_maps(device, W0, A, B, workspace, out, in, r, mp)) {
     const int nbg = p.ph[0].nbox, nbn = p.ph[1].nbox;
+    const int yb = 2 * p.fbk;   // bytes of an N-side box row (one K block of bf16)
     const bool ok =
-        make_map(&mp[0], A, false, r, in, in, kBM, 128) && make_map(&mp[1], a_h, true, r, in8, in8, nbg, 64) &&
-        make_map(&mp[2], a_l, true, r, in8, in8, nbg, 64) && make_map(&mp[3], a_h, true, r, in8, in8, nbn, 64) &&
-        make_map(&mp[4], a_l, true, r, in8, in8, nbn, 64) && make_map(&mp[5], W0, false, out, in, in, kBM, 128) &&
+        make_map(&mp[0], A, false, r, in, in, kBM, 128) && make_map(&mp[1], a_h, true, r, in8, in8, nbg, yb) &&
+        make_map(&mp[2], a_l, true, r, in8, in8, nbg, yb) && make_map(&mp[3], a_h, true, r, in8, in8, nbn, yb) &&
+        make_map(&mp[4], a_l, true, r, in8, in8, nbn, yb) && make_map(&mp[5], W0, false, out, in, in, kBM, 128) &&
         make_map(&mp[6], Bk, false, out, ldb, ldb, kBM, 128) &&
-        make_map(&mp[7], p.gs_h, true, npad, npad, npad, nbn, 64) &&
-        make_map(&mp[8], p.gs_l, true, npad, npad, npad, nbn, 64) &&
+        make_map(&mp[7], p.gs_h, true, npad, npad, npad, nbn, yb) &&
+        make_map(&mp[8], p.gs_l, true, npad, npad, npad, nbn, yb) &&
         make_map(&mp[9], Bk, false, out, ldb, ldb, 32, 128);   // 32 x 32 boxes for the B staging
     if (!ok) {
       dora::count_launches(launches);

@@ -2118,7 +2118,10 @@ bool plan_fwd(int64_t out, int64_t in, int64_t r, int max_ctas, FwdPlan *fp, boo
   const size_t budget = kSmemMax - fixed;
   int S = (512 - acc_cols) / fbk;
   if (S > kFwdMaxS) S = kFwdMaxS;
-  while (S >= 2 && static_cast<size_t>(S) * p.y_bytes + static_cast<size_t>(S + 2) * xbytes > budget) --S;
+  // raw-box slots: at least two more than stages (one more for 64-wide
+  // blocks, whose slots are twice the size)
+  const int xspare = fbk == 64 ? 1 : 2;
+  while (S >= 2 && static_cast<size_t>(S) * p.y_bytes + static_cast<size_t>(S + xspare) * xbytes > budget) --S;
   if (S < 2) return false;
   int SX = static_cast<int>((budget - static_cast<size_t>(S) * p.y_bytes) / xbytes);
   if (SX > kFwdMaxX) SX = kFwdMaxX;

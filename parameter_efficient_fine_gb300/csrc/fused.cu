@@ -50,8 +50,10 @@
 //               the accumulator columns, g (uniform 128-bit loads) and, for
 //               the lora form, the base quarter that the warp's lane 0
 //               loaded into the slot by TMA one tile ahead; y is written
-//               into the slot in place and stored by TMA.  The epilogue
-//               warps never wait for one another
+//               into the slot in place and stored by TMA.  A warp frees the
+//               accumulator right after its last tensor-memory load of the
+//               tile, before computing y.  The epilogue warps never wait
+//               for one another
 // Every wait on a shared-memory barrier is bounded; a wait that gives up
 // records a code in the library's device error word and all roles drain and
 // leave.
@@ -422,6 +424,7 @@ fused_compose_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_const
       tc_fence_after();
       const int row0 = mt * kTileRows + static_cast<int>(crank) * kFM;   // this CTA's first row of the tile
       const bool rows_in = row0 + quad * 32 < p.T;   // any of this warp's rows inside y
+      bool freed = false;   // this warp's arrival on the accumulator-empty barrier is done
       for (int j = 0; j < kQPW; ++j) {
         const int q = qb + j;
         const int sl = j % p.nslots;
@@ -462,6 +465,17 @@ fused_compose_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_const
             const uint32_t col0 = static_cast<uint32_t>(buf * kFN + q * kFQ + hh * kCP);
 #pragma unroll
             for (int w = 0; w < kCP / 32; ++w) tmem_ld32(lane_addr + col0 + 32 * w, v[w]);
+            if (hh == kNH - 1 && j == kQPW - 1) {
+              // the warp's last tensor-memory load of the tile is done: the
+              // MMA lane may start the tile after next while y is computed
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) {
+                if (PAIR) mbar_arrive_cluster(mapa_shared(acce0 + 8u * buf, 0));   // the even CTA's barrier
+                else mbar_arrive(acce0 + 8u * buf);
+              }
+              freed = true;
+            }
 #pragma unroll
             for (int c = 0; c < kCP / 8; ++c) {
               // 16-byte chunk cq of the row (8 columns), at its swizzled position
@@ -502,8 +516,8 @@ fused_compose_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_const
             last_slot = sl;
           }
         }
-        if (j == kQPW - 1) {
-          // the accumulator is read out: the MMA lane may start the tile after next
+        if (j == kQPW - 1 && !freed) {
+          // a quarter that was not live: the accumulator is not read
           tc_fence_before();
           __syncwarp();
           if (lane == 0) {

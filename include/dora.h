@@ -328,6 +328,8 @@ size_t dora_compose_fused_workspace(int64_t out, int64_t r);
  * Two launches: the split of s B, then the fused kernel, as clusters of two
  * CTAs (one 256 x 256 tile of y per pair, tcgen05.mma.cta_group::2) where
  * the device can hold such clusters, else as single CTAs (128 x 256 tiles).
+ * The fused kernel is a programmatic dependent launch on the split (its
+ * set-up overlaps it); stream order is unchanged for the caller.
  * Results are bitwise reproducible for a given shape and device.
  */
 dora_status dora_compose_lora_fwd(const void *base, const void *xa, const float *B,

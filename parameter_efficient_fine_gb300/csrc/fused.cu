@@ -54,6 +54,10 @@
 //               accumulator right after its last tensor-memory load of the
 //               tile, before computing y.  The epilogue warps never wait
 //               for one another
+// A call is two launches: split_sb_kernel (s B into hi and lo), then this
+// kernel as a programmatic dependent launch on it: its prologue and the
+// epilogue's first base loads overlap the split, and only the producer,
+// which loads hi and lo, waits for the split to complete.
 // Every wait on a shared-memory barrier is bounded; a wait that gives up
 // records a code in the library's device error word and all roles drain and
 // leave.
@@ -236,6 +240,9 @@ fused_compose_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_const
       int stage = 0;
       uint32_t phase = 0;
       int issued = 0;
+      // s B hi / lo come from the launch before this one (programmatic
+      // dependent launch); the other roles read only the call's inputs
+      pdl_wait();
       bool ok = *reinterpret_cast<const volatile int *>(p.stall) == 0;
       for (int t = cta; t < p.tiles && ok; t += ncta) {
         int mt, nt;
@@ -567,6 +574,7 @@ fused_compose_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_const
 __global__ void __launch_bounds__(256) split_sb_kernel(const float *__restrict__ B, long long n, float s,
                                                        __nv_bfloat16 *__restrict__ hi,
                                                        __nv_bfloat16 *__restrict__ lo) {
+  pdl_trigger();   // the fused kernel's prologue and first base loads may start meanwhile
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
     const float v = s * B[i];
     const __nv_bfloat16 h = __float2bfloat16_rn(v);
@@ -652,6 +660,12 @@ void pair_config(cudaLaunchConfig_t *cfg, cudaLaunchAttribute *attr, unsigned ct
   cfg->stream = cs;
   cfg->attrs = attr;
   cfg->numAttrs = 1;
+}
+// programmatic dependent launch on the launch before (the split of s B)
+void add_pdl(cudaLaunchConfig_t *cfg, cudaLaunchAttribute *attr) {
+  attr[cfg->numAttrs].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[cfg->numAttrs].val.programmaticStreamSerializationAllowed = 1;
+  ++cfg->numAttrs;
 }
 
 dora_status fused_init(int device, int sms, int **errp) {
@@ -741,8 +755,9 @@ dora_status fused_run(const void *x, const void *W0, const void *base, const voi
   }
   if (pair) {
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     pair_config(&cfg, attr, static_cast<unsigned>(fp.ctas), fthreads(fp.epi), fp.smem_bytes, cs);
+    add_pdl(&cfg, attr);
     const cudaError_t e = fp.epi == 16
                               ? cudaLaunchKernelEx(&cfg, fused_compose_kernel<true, 16>, mA0, mA1, mB0, mB1, mB2, mC, mY,
                                                    fp.p)
@@ -753,11 +768,23 @@ dora_status fused_run(const void *x, const void *W0, const void *base, const voi
       return DORA_ERR_CUDA;
     }
   } else {
-    const unsigned th = static_cast<unsigned>(fthreads(fp.epi)), nb = static_cast<unsigned>(fp.ctas);
-    if (fp.epi == 16)
-      fused_compose_kernel<false, 16><<<nb, th, fp.smem_bytes, cs>>>(mA0, mA1, mB0, mB1, mB2, mC, mY, fp.p);
-    else
-      fused_compose_kernel<false, 8><<<nb, th, fp.smem_bytes, cs>>>(mA0, mA1, mB0, mB1, mB2, mC, mY, fp.p);
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    cfg.gridDim = dim3(static_cast<unsigned>(fp.ctas));
+    cfg.blockDim = dim3(static_cast<unsigned>(fthreads(fp.epi)));
+    cfg.dynamicSmemBytes = fp.smem_bytes;
+    cfg.stream = cs;
+    cfg.attrs = attr;
+    cfg.numAttrs = 0;
+    add_pdl(&cfg, attr);
+    const cudaError_t e =
+        fp.epi == 16
+            ? cudaLaunchKernelEx(&cfg, fused_compose_kernel<false, 16>, mA0, mA1, mB0, mB1, mB2, mC, mY, fp.p)
+            : cudaLaunchKernelEx(&cfg, fused_compose_kernel<false, 8>, mA0, mA1, mB0, mB1, mB2, mC, mY, fp.p);
+    if (e != cudaSuccess) {
+      dora::count_launches(launches);
+      return DORA_ERR_CUDA;
+    }
   }
   ++launches;
   dora::count_launches(launches);

@@ -60,6 +60,13 @@ __device__ __forceinline__ void prefetch_l2(const void *ptr, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(ptr)), "r"(bytes)
                : "memory");
 }
+// programmatic dependent launch.  pdl_wait: this thread waits until the
+// launch before this one in the stream has completed and its writes are
+// visible (at once when this grid was launched without programmatic
+// serialization).  pdl_trigger: the launch after this one may start once
+// every block of this grid has called it or exited
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ void prefetch_map(const CUtensorMap *map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }

@@ -554,6 +554,8 @@ def run_ours(args, rank, world, local_rank):
             "mlp_stack": mlp_stack_row(dora, dev, stream)}
         line["workloads"]["mlp_stack"]["frac_of_hbm"] = (
             line["workloads"]["mlp_stack"]["aggregate_algorithmic_gbs"] / pk["hbm_gbs"])
+        line["workloads"]["mlp_stack"]["frac_of_hbm_graph"] = (
+            line["workloads"]["mlp_stack"]["aggregate_algorithmic_gbs_graph"] / pk["hbm_gbs"])
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(sh, d)
     print(json.dumps(line), flush=True)
@@ -666,13 +668,13 @@ def mlp_stack_row(dora, dev, stream, reps=3):
             "wsb": torch.empty(dora.dora_compose_bwd_workspace(sh.T, sh.out), dtype=torch.uint8, device=dev)}
 
     def stack():
+        st = torch.cuda.current_stream()   # the capture stream while a graph is captured
         for sh, (W0, A, B, m) in mods:
             b = bufs[sh.name]
             base, lora, dy = b["act"]
-            dora.dora_norm_factored(W0, A, B, m, sh.s, b["norm"], b["g"], b["ws"], stream)
-            dora.dora_compose_fwd(base, lora, b["g"], sh.s, b["y"], stream)
-            dora.dora_compose_bwd(dy, base, lora, b["g"], b["norm"], sh.s, b["db"], b["dl"], b["dm"], b["wsb"],
-                                  stream)
+            dora.dora_norm_factored(W0, A, B, m, sh.s, b["norm"], b["g"], b["ws"], st)
+            dora.dora_compose_fwd(base, lora, b["g"], sh.s, b["y"], st)
+            dora.dora_compose_bwd(dy, base, lora, b["g"], b["norm"], sh.s, b["db"], b["dl"], b["dm"], b["wsb"], st)
 
     t = _time_ms(stack, reps, stream)
     total = sum(sum(v for k, v in algorithmic(sh).items() if k.endswith("_bytes")) for sh, _ in mods)
@@ -681,7 +683,22 @@ def mlp_stack_row(dora, dev, stream, reps=3):
            "us_per_module": t * 1e3 / len(mods), "aggregate_algorithmic_gbs": total / (t * 1e-3) / 1e9,
            "compose_share_of_bytes": compose / total,
            "inputs": "device-drawn (torch Philox), seed per module; activations shared per shape"}
-    del mods, bufs
+    # the same stack captured once in a CUDA graph (the calls above have set
+    # up every plan and tensor map) and replayed: the kernels' own launch
+    # overhead without the host's
+    side = torch.cuda.Stream()
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        stack()
+    stream.wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        stack()
+    tg = _time_ms(graph.replay, reps, stream)
+    row.update({"ms_per_stack_graph": tg, "modules_per_s_graph": len(mods) / (tg * 1e-3),
+                "aggregate_algorithmic_gbs_graph": total / (tg * 1e-3) / 1e9})
+    del graph, mods, bufs
     torch.cuda.empty_cache()
     return row
 

@@ -28,6 +28,11 @@
  *     bounded time and record it in a device word read by dora_device_error().
  *   - Results are bitwise reproducible for a given shape on a given device.
  *   - Only sm_103 devices are accepted (DORA_ERR_ARCH otherwise).
+ *   - The calls may be captured in a CUDA graph once the same call (same
+ *     shapes and buffers) has run outside capture: the first call of a
+ *     device sets up kernel attributes, and the first with a shape or a set
+ *     of buffers builds the plan and tensor maps it then reuses.  A replay
+ *     gives the same bits as the calls launched one by one.
  */
 #ifndef DORA_H
 #define DORA_H

@@ -1402,36 +1402,52 @@ __global__ void __launch_bounds__(256) gram_reduce_kernel(const float *__restric
 // ---------------------------------------------------------------------------
 
 // Y = (s c (.) B)^T [r, out8], columns out..out8-1 zero, split for the N side
-// like split_hl_kernel: h and l [r, out8] bf16.  32 x 32 tiles transposed
-// through shared memory.
+// like split_hl_kernel: h and l [r, out8] bf16.  A block transposes 32 rows of
+// B by 128 of its columns (four 32 x 32 tiles through shared memory, all
+// sixteen loads of a thread in flight together); the rows' coefficients
+// s c_i are formed once per block.
+constexpr int kBsCols = 128;   // columns of B (rows of Y) per bs_split_kernel block
 __global__ void __launch_bounds__(256) bs_split_kernel(const float *__restrict__ B, long long out, int r,
                                                        long long out8, const float *__restrict__ g,
                                                        const float *__restrict__ d_mag,
                                                        const float *__restrict__ norm, float s,
                                                        __nv_bfloat16 *__restrict__ yh, __nv_bfloat16 *__restrict__ yl) {
-  __shared__ float tile[32][33];
+  __shared__ float tile[kBsCols / 32][32][33];
+  __shared__ float coef[32];
   const long long i0 = static_cast<long long>(blockIdx.x) * 32;
-  const int n0 = static_cast<int>(blockIdx.y) * 32;
+  const int n0 = static_cast<int>(blockIdx.y) * kBsCols;
   const int tx = threadIdx.x, ty = threadIdx.y;
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const long long i = i0 + ty + 8 * q;
-    const int n = n0 + tx;
-    float v = 0.0f;
-    if (i < out && n < r) v = (s * norm_grad_coef(g, d_mag, norm, i)) * B[i * r + n];
-    tile[ty + 8 * q][tx] = v;
+  if (ty == 0) {
+    const long long i = i0 + tx;
+    coef[tx] = i < out ? s * norm_grad_coef(g, d_mag, norm, i) : 0.0f;
   }
   __syncthreads();
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const int n = n0 + ty + 8 * q;
-    const long long i = i0 + tx;
-    if (n < r && i < out8) {
-      const float x = tile[tx][ty + 8 * q];
-      const long long o = static_cast<long long>(n) * out8 + i;
-      const __nv_bfloat16 h = __float2bfloat16_rn(x);
-      yh[o] = h;
-      yl[o] = __float2bfloat16_rn(x - __bfloat162float(h));
+  for (int c = 0; c < kBsCols / 32; ++c) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int il = ty + 8 * q;
+      const long long i = i0 + il;
+      const int n = n0 + 32 * c + tx;
+      float v = 0.0f;
+      if (i < out && n < r) v = coef[il] * B[i * r + n];
+      tile[c][il][tx] = v;
+    }
+  }
+  __syncthreads();
+#pragma unroll
+  for (int c = 0; c < kBsCols / 32; ++c) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int n = n0 + 32 * c + ty + 8 * q;
+      const long long i = i0 + tx;
+      if (n < r && i < out8) {
+        const float x = tile[c][tx][ty + 8 * q];
+        const long long o = static_cast<long long>(n) * out8 + i;
+        const __nv_bfloat16 h = __float2bfloat16_rn(x);
+        yh[o] = h;
+        yl[o] = __float2bfloat16_rn(x - __bfloat162float(h));
+      }
     }
   }
 }
@@ -1450,6 +1466,7 @@ __global__ void __launch_bounds__(256) rows_reduce_kernel(const float4 *__restri
                                                           const float *__restrict__ norm, float s,
                                                           float *__restrict__ out, long long ldo) {
   __shared__ float tile[kBM][33];
+  __shared__ float coef[kBM];   // s c_row of the block's rows (dB)
   const int tm = blockIdx.x;
   const int mt = tm / nchunks, nc = tm - mt * nchunks;
   const long long ub = (static_cast<long long>(mt) * nchunks + nc) * sk.kbtot;
@@ -1463,12 +1480,19 @@ __global__ void __launch_bounds__(256) rows_reduce_kernel(const float4 *__restri
   float4 acc[4];
 #pragma unroll
   for (int k = 0; k < 4; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (!trans && threadIdx.x < kBM) {
+    const long long row = row0 + threadIdx.x;
+    coef[threadIdx.x] = row < M ? s * norm_grad_coef(g, d_mag, norm, row) : 0.0f;
+  }
   if (4 * cg < ncol) {
-    for (int j = 0; j < nseg; ++j) {
-      float4 o[4];
+    // parts in order, two parts' loads in flight per round
+    auto part4 = [&](int j, float4 (&o)[4]) {
 #pragma unroll
       for (int k = 0; k < 4; ++k)
-        o[k] = row0 + 32 * k + lane < M ? __ldcg(src + j * slot + 32 * k) : make_float4(0.f, 0.f, 0.f, 0.f);
+        o[k] = (j < nseg && row0 + 32 * k + lane < M) ? __ldcg(src + j * slot + 32 * k)
+                                                      : make_float4(0.f, 0.f, 0.f, 0.f);
+    };
+    auto add4 = [&](const float4 (&o)[4]) {
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         acc[k].x += o[k].x;
@@ -1476,6 +1500,13 @@ __global__ void __launch_bounds__(256) rows_reduce_kernel(const float4 *__restri
         acc[k].z += o[k].z;
         acc[k].w += o[k].w;
       }
+    };
+    for (int j = 0; j < nseg; j += 2) {
+      float4 o0[4], o1[4];
+      part4(j, o0);
+      part4(j + 1, o1);
+      add4(o0);
+      if (j + 1 < nseg) add4(o1);
     }
   }
   if (trans) {
@@ -1503,7 +1534,7 @@ __global__ void __launch_bounds__(256) rows_reduce_kernel(const float4 *__restri
   for (int rr = warp; rr < kBM; rr += 8) {
     const long long row = row0 + rr;
     if (row < M && col < ncol)
-      out[row * ldo + static_cast<long long>(nc) * NC + col] = (s * norm_grad_coef(g, d_mag, norm, row)) * tile[rr][lane];
+      out[row * ldo + static_cast<long long>(nc) * NC + col] = coef[rr] * tile[rr][lane];
   }
 }
 
@@ -2748,7 +2779,7 @@ extern "C" dora_status dora_norm_factored_bwd(const float *W0, const float *A, c
     ldb = rp;
   }
   bs_split_kernel<<<dim3(static_cast<unsigned>(dora::ceil_div(out8, 32)),
-                               static_cast<unsigned>(dora::ceil_div(r, 32))),
+                               static_cast<unsigned>(dora::ceil_div(r, kBsCols))),
                           dim3(32, 8), 0, cs>>>(B, out, static_cast<int>(r), out8, g, d_mag, norm, s, y_h, y_l);
   ++launches;
 

@@ -22,6 +22,7 @@ import torch
 
 import oracle
 import parameter_efficient_fine_gb300 as dora
+from parameter_efficient_fine_gb300 import workloads as wl
 
 DEV = torch.device("cuda:0")
 BF16_REL = 2.0 ** -7
@@ -119,3 +120,41 @@ def dmag_bound(dy, base, lora, n, s):
     T = dy.shape[0]
     mag = np.sum(np.abs(dy) * (np.abs(base) + s * np.abs(lora)), axis=0) / np.abs(n)
     return 2.0 ** -24 * (T + 16) * mag + 1e-30
+
+
+def weights_dev(d):
+    return tuple(f32_dev(d[k]) for k in ("W0", "A", "B", "m"))
+
+
+def full_check(sh, seed, bwd=True):
+    """Norm, forward and (optionally) backward of one module, all elements."""
+    d = wl.make_module(sh, seed)
+    s = d["s"]
+    W0, A, B, m = weights_dev(d)
+    norm, g = run_norm(W0, A, B, m, s)
+    n_ref, g_ref = oracle.weight_norm(d["W0"], d["A"], d["B"], d["m"], s)
+    check_rel("norm", to_f64(norm), n_ref)
+    check_rel("g", to_f64(g), g_ref)
+
+    base, lora, dy = (act_to_dev(d[k]) for k in ("base", "lora", "dy"))
+    b64, l64, d64 = (act_to_f64(d[k]) for k in ("base", "lora", "dy"))
+    y = run_fwd(base, lora, g, s)
+    y_ref = oracle.compose_fwd(b64, l64, g_ref, s)
+    if sh.act == "bf16":
+        check_bf16_rule("y", to_f64(y), y_ref)
+    else:
+        bound = 2.0 ** -21 * (np.abs(b64) + np.abs(g_ref) * s * np.abs(l64)) + 1.1e-5 * np.abs(y_ref)
+        check_bound("y", to_f64(y), y_ref, bound)
+    if bwd:
+        db, dl, dm = run_bwd(dy, base, lora, g, norm, s)
+        db_ref, dl_ref, dm_ref = oracle.compose_bwd(d64, b64, l64, g_ref, n_ref, s)
+        if sh.act == "bf16":
+            check_bf16_rule("d_base", to_f64(db), db_ref)
+            check_bf16_rule("d_lora", to_f64(dl), dl_ref)
+        else:
+            gb = np.abs(g_ref)[None, :] * np.abs(d64)
+            check_bound("d_base", to_f64(db), db_ref, 2.0 ** -22 * gb + 1.1e-5 * np.abs(db_ref))
+            check_bound("d_lora", to_f64(dl), dl_ref, 2.0 ** -22 * gb * (1 + s) + 1.1e-5 * np.abs(dl_ref))
+        check_bf16_rule("d_mag", to_f64(dm), dm_ref)
+        check_bound("d_mag", to_f64(dm), dm_ref, dmag_bound(d64, b64, l64, n_ref, s) + 1.1e-5 * np.abs(dm_ref))
+    assert_no_device_error()

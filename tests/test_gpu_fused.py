@@ -100,6 +100,26 @@ def test_linear_form(T, inp, out, r, layout):
     _check("y (linear form)", y, ref)
 
 
+def _drawn(k):
+    # a seeded draw over the accepted shapes (out, r and in multiples of 8)
+    rng = np.random.default_rng(20261204 + k)
+    return (int(rng.integers(1, 700)), 8 * int(rng.integers(1, 161)), 8 * int(rng.integers(1, 201)),
+            8 * int(rng.integers(1, 97)))
+
+
+@pytest.mark.parametrize("k", range(12))
+def test_drawn_shapes_both_forms(k, layout):
+    T, inp, out, r = _drawn(k)
+    d = _layer(T, inp, out, r, 9800 + k)
+    y = run_lora(d)
+    assert_no_device_error()
+    _check("y (lora form)", y, oracle.compose_lora_fwd(_f64(d["base"]), _f64(d["xa"]), d["B"], d["g"], d["s"]))
+    y = run_linear(d)
+    assert_no_device_error()
+    _check("y (linear form)", y,
+           oracle.linear_fwd(_f64(d["x"]), _f64(d["W0"]), _f64(d["xa"]), d["B"], d["g"], d["s"]))
+
+
 def test_bitwise_reproducible(layout):
     d = _layer(300, 264, 520, 40, 9700)
     assert torch.equal(run_linear(d), run_linear(d))

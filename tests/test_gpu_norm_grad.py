@@ -117,6 +117,15 @@ def test_norm_grad_shapes(out, inp, r):
     _run_and_check(d, d_mag)
 
 
+@pytest.mark.parametrize("k", range(10))
+def test_norm_grad_drawn_shapes(k):
+    # a seeded draw over the accepted shapes (in a multiple of 4, any r and out)
+    rng = np.random.default_rng(20261205 + k)
+    out, inp, r = int(rng.integers(1, 1300)), 4 * int(rng.integers(1, 326)), int(rng.integers(1, 801))
+    d, d_mag = _case(out, inp, r, 9900 + k)
+    _run_and_check(d, d_mag)
+
+
 def test_norm_grad_is_bitwise_reproducible():
     d, d_mag = _case(1000, 1040, 384, 9201)
     s = d["s"]

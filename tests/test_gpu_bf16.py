@@ -65,6 +65,14 @@ def test_bf16_norm_matches_oracle(out, inp, r):
     assert_no_device_error()
 
 
+@pytest.mark.parametrize("k", range(10))
+def test_bf16_norm_drawn_shapes(k):
+    # a seeded draw over the accepted shapes (in a multiple of 8, any r and out)
+    rng = np.random.default_rng(20261206 + k)
+    out, inp, r = int(rng.integers(1, 1600)), 8 * int(rng.integers(1, 201)), int(rng.integers(1, 801))
+    test_bf16_norm_matches_oracle(out, inp, r)
+
+
 def test_bf16_zero_adapter_gives_unit_g():
     sh = wl.shape("high_rank", out=512, inp=1024, r=32, T=8)
     w, (w0b, ab, bb), (w0, a, b) = _module(sh, 5)

@@ -524,7 +524,8 @@ fused_compose_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_const
           }
         }
         if (j == kQPW - 1 && !freed) {
-          // a quarter that was not live: the accumulator is not read
+          // the warp's last quarter was not live, so the release after its
+          // last tensor-memory load did not run: every load it made is done
           tc_fence_before();
           __syncwarp();
           if (lane == 0) {

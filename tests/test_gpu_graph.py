@@ -2,7 +2,7 @@
 point outside capture (which sets up the device and caches the plans and
 tensor maps for those buffers), a training step captured with
 torch.cuda.graph -- the factored norm, the compose forward and backward, the
-norm gradient and the fused lora form -- replays to the same bits as the same
+norm gradient and both fused forms -- replays to the same bits as the same
 calls launched one by one, on new input values written into the captured
 buffers.  The eager results themselves are checked against the fp64 oracle by
 the other parity tests; here they are also checked against the oracle once,
@@ -30,14 +30,16 @@ def test_step_replays_bitwise_in_a_cuda_graph():
     W0, A, B, m = (f32_dev(d0[k]) for k in ("W0", "A", "B", "m"))
     base, lora, dy = (act_to_dev(d0[k]) for k in ("base", "lora", "dy"))
     xa = act_to_dev(d0["base"][:, : sh.r].copy())
+    x = act_to_dev(d0["dy"][:, : sh.inp].copy())          # any bf16 [T, in] serves as x
+    W0b = W0.to(torch.bfloat16)
     norm, g, dm = (torch.empty(sh.out, device=DEV) for _ in range(3))
-    y, db, dl, yl = (torch.empty_like(base) for _ in range(4))
+    y, db, dl, yl, yx = (torch.empty_like(base) for _ in range(5))
     dA, dB = torch.empty_like(A), torch.empty_like(B)
     ws_n = torch.empty(dora.dora_norm_factored_workspace(sh.out, sh.inp, sh.r), dtype=torch.uint8, device=DEV)
     ws_b = torch.empty(dora.dora_compose_bwd_workspace(sh.T, sh.out), dtype=torch.uint8, device=DEV)
     ws_g = torch.empty(dora.dora_norm_factored_bwd_workspace(sh.out, sh.inp, sh.r), dtype=torch.uint8, device=DEV)
     ws_f = torch.empty(dora.dora_compose_fused_workspace(sh.out, sh.r), dtype=torch.uint8, device=DEV)
-    outs = (norm, g, y, db, dl, dm, dA, dB, yl)
+    outs = (norm, g, y, db, dl, dm, dA, dB, yl, yx)
 
     def step():
         st = torch.cuda.current_stream()
@@ -46,6 +48,7 @@ def test_step_replays_bitwise_in_a_cuda_graph():
         dora.dora_compose_bwd(dy, base, lora, g, norm, s, db, dl, dm, ws_b, st)
         dora.dora_norm_factored_bwd(W0, A, B, norm, g, dm, s, dA, dB, ws_g, st)
         dora.dora_compose_lora_fwd(base, xa, B, g, s, yl, ws_f, st)
+        dora.dora_linear_fwd(x, W0b, xa, B, g, s, yx, ws_f, st)
 
     # one eager call of each (set-up and caches), then the reference results
     # for the second input set, computed eagerly
@@ -58,6 +61,8 @@ def test_step_replays_bitwise_in_a_cuda_graph():
         for t, k in ((base, "base"), (lora, "lora"), (dy, "dy")):
             t.copy_(act_to_dev(dd[k]))
         xa.copy_(act_to_dev(dd["base"][:, : sh.r].copy()))
+        x.copy_(act_to_dev(dd["dy"][:, : sh.inp].copy()))
+        W0b.copy_(W0.to(torch.bfloat16))
 
     load(d1)
     step()
@@ -90,7 +95,7 @@ def test_step_replays_bitwise_in_a_cuda_graph():
     assert_no_device_error()
     # replays launch from the graph, not through the host entry points
     assert dora.dora_kernel_launches() - launches0 == captured
-    names = ("norm", "g", "y", "d_base", "d_lora", "d_mag", "dA", "dB", "lora-form y")
+    names = ("norm", "g", "y", "d_base", "d_lora", "d_mag", "dA", "dB", "lora-form y", "linear-form y")
     for name, a, b in zip(names, outs, eager):
         assert torch.equal(a.view(torch.int16) if a.dtype == torch.bfloat16 else a.view(torch.int32),
                            b.view(torch.int16) if b.dtype == torch.bfloat16 else b.view(torch.int32)), name

@@ -565,7 +565,7 @@ constexpr int kFwdBox = 32;                      // K indices of one raw M-side 
 constexpr int kFwdBoxBytes = kBM * kFwdBox * 4;  // 16 KB
 constexpr int kFwdMaxX = 16;
 constexpr int kFwdMaxS = 8;
-constexpr int kGramPieces = 16;                  // CTAs (K pieces) per Gram tile, at most
+constexpr int kGramPieces = 8;                   // CTAs (K pieces) per Gram tile, at most (16 was 3-4% slower at r = 256)
 
 // one phase's work list and N-side geometry
 struct FwdPhase {

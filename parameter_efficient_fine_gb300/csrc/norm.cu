@@ -2197,7 +2197,9 @@ bool plan_fwd(int64_t out, int64_t in, int64_t r, int max_ctas, FwdPlan *fp, boo
   const int nsub = (fg.NC + 31) / 32;
   const double t_gram =
       fg.kbtot / static_cast<double>(P) * 0.75 * kscale + 1.2 + 1.6 * ((nsub * nsub + P - 1) / P);
-  const double t_seg = 1.0 + 12.5 * fn.NC / 384.0;
+  // (with 64-wide K blocks 3 us more: without it, at r = 64 and 128 the
+  // CTAs with two segments ended their MMA loops 2.3-2.9 us after the others)
+  const double t_seg = 1.0 + 12.5 * fn.NC / 384.0 + (fbk == 64 ? 3.0 : 0.0);
   if (with_split) balance_split(fn.units, fn.kbtot, p.ctas, fg.ctas, t_norm, t_seg, t_gram, p.ub);
 
   p.nsync = 1 + fg.tiles;

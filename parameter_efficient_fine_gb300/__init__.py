@@ -104,6 +104,10 @@ def _ptr(x) -> int:
         return 0
     if isinstance(x, int):
         return x
+    # every pointer of the C ABI is a device pointer: a host tensor would hand
+    # a host address to the kernels
+    if not getattr(x, "is_cuda", False):
+        raise ValueError(f"libdora takes CUDA tensors (device memory); got one on {getattr(x, 'device', type(x))}")
     return x.data_ptr()
 
 

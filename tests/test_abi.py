@@ -1,7 +1,6 @@
 """Host-side checks of the C ABI: the library loads, exports every symbol the
 header declares, sizes workspaces, and rejects bad arguments before touching
 the GPU.  CPU only (no compute call is made)."""
-import ctypes
 import os
 import re
 

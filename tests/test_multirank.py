@@ -4,8 +4,6 @@ throughput is the aggregate of both replicas.  No GPU."""
 import os
 import socket
 
-import pytest
-import torch
 import torch.distributed as dist
 import torch.multiprocessing as mp
 

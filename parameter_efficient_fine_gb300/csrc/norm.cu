@@ -2117,10 +2117,15 @@ void balance_split(long long U, int kbtot, int C, int g, double t_unit, double t
 
 // with_split = false: the geometry and workspace only (no CTA ranges);
 // fbk: K indices per K block (32 or 64; 0 = 64 where at least three 64-wide
-// stages fit into tensor and shared memory, else 32)
+// stages fit into tensor and shared memory, or two when N is cut into
+// several chunks, else 32).  Measured: with N in two chunks of 256 (r = 512)
+// 64-wide blocks on two stages take 168 against 172 us; with one chunk of
+// 256 (r = 256) 94 against 93
 bool plan_fwd(int64_t out, int64_t in, int64_t r, int max_ctas, FwdPlan *fp, bool with_split = true, int fbk = 0) {
   if (fbk == 0) {
-    if (plan_fwd(out, in, r, max_ctas, fp, with_split, 64) && fp->p.S >= 3) return true;
+    if (plan_fwd(out, in, r, max_ctas, fp, with_split, 64) &&
+        (fp->p.S >= 3 || (fp->p.S == 2 && fp->p.ph[1].nchunks > 1)))
+      return true;
     return plan_fwd(out, in, r, max_ctas, fp, with_split, 32);
   }
   FwdParams &p = fp->p;

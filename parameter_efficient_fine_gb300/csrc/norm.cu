@@ -37,7 +37,11 @@
 // global memory.
 //
 // The gradient through the norm (dora_norm_factored_bwd) runs the same
-// scheme in tc_gemm_kernel, four passes of separate launches.
+// scheme in tc_gemm_kernel for its two large products (dB and dA, each one
+// pass over W0).  Its first launch, grad_prep_kernel, splits the passes' N
+// operands and, for r <= kSgMaxR, forms the Gram products G and s H on the
+// CUDA cores as fp32 partials that sg_fin_kernel sums; for larger r those are
+// two more tc_gemm_kernel passes with their reductions.
 //
 // tc_gemm structure (one CTA per SM, persistent, 192 threads):
 //   warp 0      TMA producer: loads the raw M-side box [128 x 32 fp32] and the
@@ -1272,14 +1276,12 @@ fwd_norm_kernel(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
 //   h [rows, cols8] bf16: x rounded to bf16 (nearest even)
 //   l [rows, cols8] bf16: x - h rounded to bf16;  zero past cols
 // (cols8 = cols rounded up to 8, a 16-byte row).  One thread per group of 4.
-__global__ void __launch_bounds__(256) split_hl_kernel(const float *__restrict__ x, long long rows, int cols,
-                                                       int cols8, __nv_bfloat16 *__restrict__ h,
-                                                       __nv_bfloat16 *__restrict__ l, int *__restrict__ cnt,
-                                                       int ncnt) {
-  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < ncnt; i += gridDim.x * blockDim.x) cnt[i] = 0;
+__device__ __forceinline__ void split_hl_range(const float *__restrict__ x, long long rows, int cols, int cols8,
+                                               __nv_bfloat16 *__restrict__ h, __nv_bfloat16 *__restrict__ l,
+                                               long long first, long long step) {
   const int g4 = cols8 / 4;
   const long long n = rows * g4;
-  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
+  for (long long i = first; i < n; i += step) {
     const long long row = i / g4;
     const int k = static_cast<int>(i - row * g4) * 4;
     float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -1290,6 +1292,15 @@ __global__ void __launch_bounds__(256) split_hl_kernel(const float *__restrict__
     *reinterpret_cast<uint2 *>(h + row * cols8 + k) = make_uint2(h01, h23);
     *reinterpret_cast<uint2 *>(l + row * cols8 + k) = make_uint2(l01, l23);
   }
+}
+
+__global__ void __launch_bounds__(256) split_hl_kernel(const float *__restrict__ x, long long rows, int cols,
+                                                       int cols8, __nv_bfloat16 *__restrict__ h,
+                                                       __nv_bfloat16 *__restrict__ l, int *__restrict__ cnt,
+                                                       int ncnt) {
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < ncnt; i += gridDim.x * blockDim.x) cnt[i] = 0;
+  split_hl_range(x, rows, cols, cols8, h, l, static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x,
+                 static_cast<long long>(gridDim.x) * blockDim.x);
 }
 
 // B [out, r] -> Bp [out, rp] with zero columns r..rp-1 (rp = r rounded up to 4)
@@ -1402,21 +1413,21 @@ __global__ void __launch_bounds__(256) gram_reduce_kernel(const float *__restric
 // ---------------------------------------------------------------------------
 
 // Y = (s c (.) B)^T [r, out8], columns out..out8-1 zero, split for the N side
-// like split_hl_kernel: h and l [r, out8] bf16.  A block transposes 32 rows of
-// B by 128 of its columns (four 32 x 32 tiles through shared memory, all
-// sixteen loads of a thread in flight together); the rows' coefficients
-// s c_i are formed once per block.
-constexpr int kBsCols = 128;   // columns of B (rows of Y) per bs_split_kernel block
-__global__ void __launch_bounds__(256) bs_split_kernel(const float *__restrict__ B, long long out, int r,
-                                                       long long out8, const float *__restrict__ g,
-                                                       const float *__restrict__ d_mag,
-                                                       const float *__restrict__ norm, float s,
-                                                       __nv_bfloat16 *__restrict__ yh, __nv_bfloat16 *__restrict__ yl) {
-  __shared__ float tile[kBsCols / 32][32][33];
-  __shared__ float coef[32];
-  const long long i0 = static_cast<long long>(blockIdx.x) * 32;
-  const int n0 = static_cast<int>(blockIdx.y) * kBsCols;
-  const int tx = threadIdx.x, ty = threadIdx.y;
+// like split_hl_kernel: h and l [r, out8] bf16.  One block (bx, by) of 256
+// threads transposes 32 rows of B by 128 of its columns (four 32 x 32 tiles
+// through shared memory, all sixteen loads of a thread in flight together);
+// the rows' coefficients s c_i are formed once per block.
+constexpr int kBsCols = 128;   // columns of B (rows of Y) per block
+__device__ __forceinline__ void bs_split_block(long long bx, int by, const float *__restrict__ B, long long out,
+                                               int r, long long out8, const float *__restrict__ g,
+                                               const float *__restrict__ d_mag, const float *__restrict__ norm,
+                                               float s, __nv_bfloat16 *__restrict__ yh,
+                                               __nv_bfloat16 *__restrict__ yl, float *smem) {
+  float(*tile)[32][33] = reinterpret_cast<float(*)[32][33]>(smem);   // [kBsCols / 32][32][33]
+  float *coef = smem + (kBsCols / 32) * 32 * 33;                      // [32]
+  const long long i0 = bx * 32;
+  const int n0 = by * kBsCols;
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
   if (ty == 0) {
     const long long i = i0 + tx;
     coef[tx] = i < out ? s * norm_grad_coef(g, d_mag, norm, i) : 0.0f;
@@ -1449,6 +1460,288 @@ __global__ void __launch_bounds__(256) bs_split_kernel(const float *__restrict__
         yl[o] = __float2bfloat16_rn(x - __bfloat162float(h));
       }
     }
+  }
+}
+
+// ---- the Gram products on the CUDA cores (r <= kSgMaxR)
+//
+// At small r, G = A A^T (K = in) and s H = B^T (s c (.) B) (K = out) are a few
+// hundred MFLOP; as tensor-core passes of their own they are bound by the
+// latency of one CTA's K loop and by four launches.  Here a block of the
+// gradient's first launch forms one fp32 partial of a T x T tile of the upper
+// triangle over one K slice, and the next launch sums the slices of each entry
+// in a fixed order.  T (16, 32 or 64, the smallest that covers r up to 64) keeps
+// the FMAs on entries below r.  In a block, each thread holds a 4 x 4 block of
+// the tile; the (T/4)^2 threads that cover the tile form a K group, and the
+// 256 / (T/4)^2 groups take equal parts of each chunk of KC K indices staged
+// K-major in shared memory (the next chunk's loads in flight during the FMAs).
+// The groups' tiles are added in group order at the end.
+constexpr int kSgMaxSlices = 128;   // K slices per tile at most (bounds the partials)
+constexpr int kSgMaxR = 256;        // largest r that takes this path
+constexpr int kSgSmemFloats = 4672; // staging (and group sums) of a block, floats
+
+template <int T>
+struct SgShape {
+  static constexpr int kTT = T / 4;                      // threads per tile side
+  static constexpr int kGroup = kTT * kTT;               // threads per K group
+  static constexpr int kGroups = 256 / kGroup;           // K groups per block
+  static constexpr int kKC = T == 64 ? 32 : 64;          // K indices per chunk
+  static constexpr int kLd = T + 4;                      // row stride of a K-major chunk (16-byte rows)
+  static constexpr int kKK = kKC / kGroups;              // K indices of a chunk per group
+  static constexpr int kSlice = T == 16 ? 64 : 128;      // K indices per slice (at most kSgMaxSlices)
+  static_assert(kGroups * kGroup == 256 && kKK * kGroups == kKC, "K groups");
+  static_assert(2 * kKC * kLd + kKC <= kSgSmemFloats && kGroups * T * T <= kSgSmemFloats, "shared memory");
+};
+
+struct SgDims {
+  int T;            // tile side (16, 32 or 64); 0: no Gram part
+  int nt1;          // tiles per side, ceil(r / T)
+  int ntiles;       // upper-triangular tiles, nt1 (nt1 + 1) / 2
+  int nsG, nsH;     // K slices of G (K = in) and of H (K = out)
+  int ksG, ksH;     // K indices per slice (multiples of the chunk)
+};
+
+__host__ __device__ __forceinline__ void sg_tile(int t, int nt1, int *ti, int *tj) {
+  int i = 0;
+  while (t >= nt1 - i) {
+    t -= nt1 - i;
+    ++i;
+  }
+  *ti = i;
+  *tj = i + t;
+}
+
+// Partial q of the Gram part: q < ntiles * nsG is G's (tile q / nsG, slice
+// q % nsG), the rest are H's.  part[q] is the T x T tile, row-major, entries
+// past r zero.  A is [r, in] with 16-byte rows (in % 4 == 0), B is [out, r].
+template <int T>
+__device__ __forceinline__ void sg_part_block(int q, const SgDims &d, const float *__restrict__ A, int r,
+                                              long long in, const float *__restrict__ B, long long out,
+                                              const float *__restrict__ g, const float *__restrict__ d_mag,
+                                              const float *__restrict__ norm, float s, float *__restrict__ part,
+                                              float *smem) {
+  using S = SgShape<T>;
+  constexpr int KC = S::kKC, LD = S::kLd;
+  constexpr int NQ = T * KC / 4 / 256;   // float4s of an A chunk per thread and operand (G)
+  constexpr int NE = T * KC / 256;       // entries of a B chunk per thread and operand (H)
+  const bool isG = q < d.ntiles * d.nsG;
+  const int qq = isG ? q : q - d.ntiles * d.nsG;
+  const int ns = isG ? d.nsG : d.nsH;
+  const int t = qq / ns, z = qq - t * ns;
+  int ti, tj;
+  sg_tile(t, d.nt1, &ti, &tj);
+  const int i0 = ti * T, j0 = tj * T;
+  const long long K = isG ? in : out;
+  const long long k0 = static_cast<long long>(z) * (isG ? d.ksG : d.ksH);
+  const long long kend = min(K, k0 + (isG ? d.ksG : d.ksH));
+  const int nch = static_cast<int>((kend - k0 + KC - 1) / KC);
+  float(*xi)[LD] = reinterpret_cast<float(*)[LD]>(smem);
+  float(*xj)[LD] = (isG && ti == tj) ? xi : reinterpret_cast<float(*)[LD]>(smem + KC * LD);
+  float *coef = smem + 2 * KC * LD;   // s c_k of the chunk's rows of B (H)
+  const int tid = threadIdx.x;
+  const int grp = tid / S::kGroup, loc = tid - grp * S::kGroup;
+  const int ty = loc / S::kTT, tx = loc - ty * S::kTT;
+  // a chunk's loads, held in registers until staged:
+  //   G: NQ quads of A rows per operand, KC / 4 lanes along a row piece
+  //   H: NE entries of B per operand, T lanes along a row of B; the first KC
+  //      threads also fetch the inputs of one row's coefficient
+  float vi[4 * NQ > NE ? 4 * NQ : NE], vj[4 * NQ > NE ? 4 * NQ : NE];
+  float cg = 0.0f, cd = 0.0f, cn = 1.0f;
+  auto load = [&](long long kc) {
+    if (isG) {
+#pragma unroll
+      for (int e = 0; e < NQ; ++e) {
+        const int f = tid + 256 * e;
+        const int row = f / (KC / 4), kq = (f - row * (KC / 4)) * 4;
+        const long long k = kc + kq;
+        float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
+        if (k < kend) {
+          if (i0 + row < r) a = __ldg(reinterpret_cast<const float4 *>(A + (i0 + row) * in + k));
+          if (ti != tj && j0 + row < r) b = __ldg(reinterpret_cast<const float4 *>(A + (j0 + row) * in + k));
+        }
+        vi[4 * e] = a.x, vi[4 * e + 1] = a.y, vi[4 * e + 2] = a.z, vi[4 * e + 3] = a.w;
+        vj[4 * e] = b.x, vj[4 * e + 1] = b.y, vj[4 * e + 2] = b.z, vj[4 * e + 3] = b.w;
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < NE; ++e) {
+        const int f = tid + 256 * e;
+        const int kk = f / T, col = f - kk * T;
+        const long long k = kc + kk;
+        float a = 0.0f, b = 0.0f;
+        if (k < kend) {
+          if (i0 + col < r) a = B[k * r + i0 + col];
+          if (j0 + col < r) b = B[k * r + j0 + col];
+        }
+        vi[e] = a;
+        vj[e] = b;
+      }
+      if (tid < KC && kc + tid < kend) {
+        cg = g[kc + tid];
+        cd = d_mag[kc + tid];
+        cn = norm[kc + tid];
+      }
+    }
+  };
+  auto stage = [&]() {
+    if (isG) {
+#pragma unroll
+      for (int e = 0; e < NQ; ++e) {
+        const int f = tid + 256 * e;
+        const int row = f / (KC / 4), kq = (f - row * (KC / 4)) * 4;
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          xi[kq + m][row] = vi[4 * e + m];
+          if (ti != tj) xj[kq + m][row] = vj[4 * e + m];
+        }
+      }
+    } else {
+      // the coefficients first (rows past K get 0: their B entries are 0)
+      if (tid < KC) coef[tid] = s * (-(cg * cd) / cn);
+      __syncthreads();
+#pragma unroll
+      for (int e = 0; e < NE; ++e) {
+        const int f = tid + 256 * e;
+        const int kk = f / T, col = f - kk * T;
+        xi[kk][col] = vi[e];
+        xj[kk][col] = coef[kk] * vj[e];
+      }
+    }
+  };
+  float acc[4][4];
+#pragma unroll
+  for (int a = 0; a < 4; ++a)
+#pragma unroll
+    for (int b = 0; b < 4; ++b) acc[a][b] = 0.0f;
+  load(k0);
+  for (int c = 0; c < nch; ++c) {
+    __syncthreads();
+    stage();
+    __syncthreads();
+    if (c + 1 < nch) {
+      cg = 0.0f, cd = 0.0f, cn = 1.0f;
+      load(k0 + static_cast<long long>(c + 1) * KC);
+    }
+#pragma unroll 8
+    for (int u0 = 0; u0 < S::kKK; ++u0) {
+      const int kk = grp * S::kKK + u0;
+      const float4 a = *reinterpret_cast<const float4 *>(&xi[kk][4 * ty]);
+      const float4 b = *reinterpret_cast<const float4 *>(&xj[kk][4 * tx]);
+      const float av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int v = 0; v < 4; ++v) acc[u][v] = fmaf(av[u], bv[v], acc[u][v]);
+    }
+  }
+  float *pp = part + static_cast<size_t>(q) * T * T;
+  if constexpr (S::kGroups == 1) {
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      *reinterpret_cast<float4 *>(pp + (4 * ty + u) * T + 4 * tx) =
+          make_float4(acc[u][0], acc[u][1], acc[u][2], acc[u][3]);
+    return;
+  }
+  // the groups' tiles side by side in shared memory, then added in group order
+  __syncthreads();
+  float *gs = smem + grp * T * T;
+#pragma unroll
+  for (int u = 0; u < 4; ++u)
+    *reinterpret_cast<float4 *>(gs + (4 * ty + u) * T + 4 * tx) =
+        make_float4(acc[u][0], acc[u][1], acc[u][2], acc[u][3]);
+  __syncthreads();
+  for (int e = tid; e < T * T; e += 256) {
+    float v = smem[e];
+#pragma unroll
+    for (int k = 1; k < S::kGroups; ++k) v += smem[k * T * T + e];
+    pp[e] = v;
+  }
+}
+
+// The gradient's first launch: blocks [0, nb_sg) are Gram partials (T > 0
+// only), the next nb_bs the split of (s c (.) B)^T (bs_bx per row of blocks),
+// the last nb_split the split of A (split_hl_kernel's work, grid stride).
+// The three parts read only the call's inputs, so they run side by side; the
+// Gram blocks, the longest, come first.
+struct GradPrep {
+  SgDims sg;
+  int nb_sg, nb_bs, bs_bx, nb_split;
+  const float *A;
+  int r, in, in8;
+  __nv_bfloat16 *a_h, *a_l;
+  const float *B;
+  long long out, out8;
+  const float *g, *d_mag, *norm;
+  float s;
+  __nv_bfloat16 *y_h, *y_l;
+  float *sg_part;
+};
+static_assert(kSgSmemFloats >= (kBsCols / 32) * 32 * 33 + 32, "prep shared memory holds the bs_split tiles");
+
+template <int T>
+__global__ void __launch_bounds__(256, 3) grad_prep_kernel(const GradPrep p) {
+  __shared__ __align__(16) float smem[T > 0 ? kSgSmemFloats : (kBsCols / 32) * 32 * 33 + 32];
+  int b = static_cast<int>(blockIdx.x);
+  if constexpr (T > 0) {
+    if (b < p.nb_sg) {
+      sg_part_block<T>(b, p.sg, p.A, p.r, p.in, p.B, p.out, p.g, p.d_mag, p.norm, p.s, p.sg_part, smem);
+      return;
+    }
+    b -= p.nb_sg;
+  }
+  if (b < p.nb_bs) {
+    bs_split_block(b % p.bs_bx, b / p.bs_bx, p.B, p.out, p.r, p.out8, p.g, p.d_mag, p.norm, p.s, p.y_h, p.y_l, smem);
+    return;
+  }
+  b -= p.nb_bs;
+  split_hl_range(p.A, p.r, p.in, p.in8, p.a_h, p.a_l, static_cast<long long>(b) * blockDim.x + threadIdx.x,
+                 static_cast<long long>(p.nb_split) * blockDim.x);
+}
+
+// Sum of the Gram partials: warp w adds slices w, w + 8, ... in turn, then the
+// 8 warp sums are added in warp order; times s (s G from G, s^2 H from s H),
+// written split into the bf16 h / l [npad, npad] the passes read, mirrored
+// below the diagonal (zero past r, as the partials are).  blockIdx.x =
+// (product * ntiles + tile) * (T^2 / 64) + entry group; a block covers 64
+// consecutive entries of a tile (row-major), two per lane.
+__global__ void __launch_bounds__(256) sg_fin_kernel(const float *__restrict__ part, const SgDims d, int npad,
+                                                     float s, __nv_bfloat16 *__restrict__ gh,
+                                                     __nv_bfloat16 *__restrict__ gl, __nv_bfloat16 *__restrict__ hh,
+                                                     __nv_bfloat16 *__restrict__ hl) {
+  __shared__ float wsum[8][2][33];
+  const int T = d.T, tt = T * T, per = tt / 64;
+  int b = static_cast<int>(blockIdx.x);
+  const int eg = b % per;
+  b /= per;
+  const bool isG = b < d.ntiles;
+  const int t = isG ? b : b - d.ntiles;
+  const int ns = isG ? d.nsG : d.nsH;
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const float *p0 = part + ((isG ? 0 : static_cast<size_t>(d.ntiles) * d.nsG) + static_cast<size_t>(t) * ns) * tt +
+                    eg * 64 + lane;
+  float acc[2] = {0.0f, 0.0f};
+#pragma unroll 8
+  for (int z = w; z < ns; z += 8) {
+    const float *pz = p0 + static_cast<size_t>(z) * tt;
+    acc[0] += __ldcg(pz);
+    acc[1] += __ldcg(pz + 32);
+  }
+  wsum[w][0][lane] = acc[0];
+  wsum[w][1][lane] = acc[1];
+  __syncthreads();
+  if (threadIdx.x < 64) {
+    const int a = threadIdx.x >> 5;
+    float v = 0.0f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) v += wsum[k][a][lane];
+    v *= s;
+    int ti, tj;
+    sg_tile(t, d.nt1, &ti, &tj);
+    const int e = eg * 64 + a * 32 + lane;
+    const int row = ti * T + e / T, col = tj * T + e % T;
+    __nv_bfloat16 *oh = isG ? gh : hh, *ol = isG ? gl : hl;
+    store_gs_hl(row, col, v, npad, oh, ol);
+    if (ti != tj) store_gs_hl(col, row, v, npad, oh, ol);
   }
 }
 
@@ -2281,7 +2574,19 @@ struct BwdPlans {
   GemmPlan gh;   // s H = B^T (s c (.) B) partial tiles (K = out; B read transposed)
   GemmPlan gb;   // dB rows (M = out, K = in + r)
   GemmPlan ga;   // dA^T rows (M = in, K = out + r; W0 and A read transposed)
+  bool small;    // r <= kSgMaxR: G and s H on the CUDA cores (sg) instead of gg, gh
+  SgDims sg;
 };
+
+// K slices of one Gram product on the CUDA cores: slices of `slice` K indices,
+// or longer ones (multiples of the chunk kc) when K would need more than
+// `most` of them
+void sg_slices(int64_t K, int slice, int kc, int most, int *ns, int *ks) {
+  const int64_t n = std::min<int64_t>(dora::ceil_div(K, slice), most);
+  const int64_t k = dora::round_up(dora::ceil_div(K, n), kc);
+  *ks = static_cast<int>(k);
+  *ns = static_cast<int>(dora::ceil_div(K, k));
+}
 // the N-side operands of the four passes, each a bf16 h / l pair
 struct BwdLayout {
   size_t a_h, a_l, y_h, y_l, g_h, g_l, h_h, h_l, part_t, part_r, b_pad, total;
@@ -2297,6 +2602,22 @@ bool plan_bwd(int64_t out, int64_t in, int64_t r, int sms, BwdPlans *P, BwdLayou
   P->ga.xt = true;
   P->gb.p.chain = kChainK / kBK;
   P->ga.p.chain = kChainK / kBK;
+  P->small = r <= kSgMaxR;
+  SgDims &sg = P->sg;
+  std::memset(&sg, 0, sizeof(sg));
+  if (P->small) {
+    sg.T = r <= 16 ? 16 : r <= 32 ? 32 : 64;
+    const int kc = sg.T == 16 ? SgShape<16>::kKC : sg.T == 32 ? SgShape<32>::kKC : SgShape<64>::kKC;
+    const int slice = sg.T == 16 ? SgShape<16>::kSlice : sg.T == 32 ? SgShape<32>::kSlice : SgShape<64>::kSlice;
+    sg.nt1 = static_cast<int>(dora::ceil_div(r, sg.T));
+    sg.ntiles = sg.nt1 * (sg.nt1 + 1) / 2;
+    // slices per tile: at most kSgMaxSlices, and no more than the Gram blocks
+    // of about one wave (three blocks per SM) need; this also bounds the
+    // partials to about 3 * sms tiles
+    const int most = std::max(1, std::min(kSgMaxSlices, 3 * sms / (2 * sg.ntiles)));
+    sg_slices(in, slice, kc, most, &sg.nsG, &sg.ksG);
+    sg_slices(out, slice, kc, most, &sg.nsH, &sg.ksH);
+  }
   int npad, nchunks, NC;
   plan_n(ri, &npad, &nchunks, &NC);
   const size_t out8 = static_cast<size_t>(dora::round_up(out, 8));
@@ -2315,7 +2636,9 @@ bool plan_bwd(int64_t out, int64_t in, int64_t r, int sms, BwdPlans *P, BwdLayou
   L->g_l = take(static_cast<size_t>(npad) * npad * 2);
   L->h_h = take(static_cast<size_t>(npad) * npad * 2); // s^2 H: bf16 [npad, npad] each
   L->h_l = take(static_cast<size_t>(npad) * npad * 2);
-  L->part_t = take(P->gg.part_bytes > P->gh.part_bytes ? P->gg.part_bytes : P->gh.part_bytes);
+  // Gram partials: the CUDA-core slices (small r) or the tensor-core passes' tiles
+  L->part_t = take(P->small ? static_cast<size_t>(sg.ntiles) * (sg.nsG + sg.nsH) * sg.T * sg.T * 4
+                            : std::max(P->gg.part_bytes, P->gh.part_bytes));
   L->part_r = take(P->gb.part_bytes > P->ga.part_bytes ? P->gb.part_bytes : P->ga.part_bytes);
   L->b_pad = (r % 4) ? take(static_cast<size_t>(out) * dora::round_up(r, 4) * 4) : 0;
   L->total = off;
@@ -2770,11 +3093,9 @@ extern "C" dora_status dora_norm_factored_bwd(const float *W0, const float *A, c
     return DORA_ERR_CUDA;
   };
 
-  // 1. N-side split of A; B padded to a TMA-legal row stride when r % 4 != 0;
-  //    the N-side split of (s c B)^T
-  split_hl_kernel<<<grid_for(r * in8 / 4, sms), 256, 0, cs>>>(A, r, static_cast<int>(in), static_cast<int>(in8), a_h,
-                                                               a_l, nullptr, 0);
-  ++launches;
+  // 1. B padded to a TMA-legal row stride when r % 4 != 0; then one launch:
+  //    the N-side splits of A and of (s c B)^T and, for r <= kSgMaxR, the
+  //    partials of G and s H
   const float *Bk = B;
   int64_t ldb = r;
   if (r % 4) {
@@ -2785,23 +3106,45 @@ extern "C" dora_status dora_norm_factored_bwd(const float *W0, const float *A, c
     Bk = bp;
     ldb = rp;
   }
-  bs_split_kernel<<<dim3(static_cast<unsigned>(dora::ceil_div(out8, 32)),
-                               static_cast<unsigned>(dora::ceil_div(r, kBsCols))),
-                          dim3(32, 8), 0, cs>>>(B, out, static_cast<int>(r), out8, g, d_mag, norm, s, y_h, y_l);
-  ++launches;
+  {
+    GradPrep gp;
+    gp.sg = P.sg;
+    gp.nb_sg = P.small ? P.sg.ntiles * (P.sg.nsG + P.sg.nsH) : 0;
+    gp.bs_bx = static_cast<int>(dora::ceil_div(out8, 32));
+    gp.nb_bs = gp.bs_bx * static_cast<int>(dora::ceil_div(r, kBsCols));
+    gp.nb_split = grid_for(r * in8 / 4, sms);
+    gp.A = A;
+    gp.r = static_cast<int>(r);
+    gp.in = static_cast<int>(in);
+    gp.in8 = static_cast<int>(in8);
+    gp.a_h = a_h;
+    gp.a_l = a_l;
+    gp.B = B;
+    gp.out = out;
+    gp.out8 = out8;
+    gp.g = g;
+    gp.d_mag = d_mag;
+    gp.norm = norm;
+    gp.s = s;
+    gp.y_h = y_h;
+    gp.y_l = y_l;
+    gp.sg_part = part_t;
+    const unsigned nblk = static_cast<unsigned>(gp.nb_sg + gp.nb_bs + gp.nb_split);
+    switch (P.sg.T) {
+      case 16: grad_prep_kernel<16><<<nblk, 256, 0, cs>>>(gp); break;
+      case 32: grad_prep_kernel<32><<<nblk, 256, 0, cs>>>(gp); break;
+      case 64: grad_prep_kernel<64><<<nblk, 256, 0, cs>>>(gp); break;
+      default: grad_prep_kernel<0><<<nblk, 256, 0, cs>>>(gp); break;
+    }
+    ++launches;
+  }
 
   // tensor maps: the raw fp32 M-side boxes (one K block of 32 by 128 rows) and
   // the bf16 N-side boxes (64-byte rows of 32 K indices)
   const GemmPlan &gg = P.gg, &gh = P.gh, &gb = P.gb, &ga = P.ga;
   const int rb = 4 * kBK, nb = 2 * kBK;
   CUtensorMap mA, mAh_g, mAl_g, mBt, mYh_h, mYl_h, mW0, mB, mAh_b, mAl_b, mGh, mGl, mW0t, mAt, mYh_a, mYl_a, mHh, mHl;
-  bool ok = make_map(&mA, A, false, r, in, in, kBM, rb) &&
-            make_map(&mAh_g, a_h, true, r, in8, in8, gg.p.nbox, nb) &&
-            make_map(&mAl_g, a_l, true, r, in8, in8, gg.p.nbox, nb) &&
-            make_map_t(&mBt, Bk, out, r, ldb, kBK) &&
-            make_map(&mYh_h, y_h, true, r, out8, out8, gh.p.nbox, nb) &&
-            make_map(&mYl_h, y_l, true, r, out8, out8, gh.p.nbox, nb) &&
-            make_map(&mW0, W0, false, out, in, in, kBM, rb) && make_map(&mB, Bk, false, out, ldb, ldb, kBM, rb) &&
+  bool ok = make_map(&mW0, W0, false, out, in, in, kBM, rb) && make_map(&mB, Bk, false, out, ldb, ldb, kBM, rb) &&
             make_map(&mAh_b, a_h, true, r, in8, in8, gb.p.nbox, nb) &&
             make_map(&mAl_b, a_l, true, r, in8, in8, gb.p.nbox, nb) &&
             make_map(&mGh, g_h, true, npad, npad, npad, gb.p.nbox, nb) &&
@@ -2811,35 +3154,47 @@ extern "C" dora_status dora_norm_factored_bwd(const float *W0, const float *A, c
             make_map(&mYl_a, y_l, true, r, out8, out8, ga.p.nbox, nb) &&
             make_map(&mHh, h_h, true, npad, npad, npad, ga.p.nbox, nb) &&
             make_map(&mHl, h_l, true, npad, npad, npad, ga.p.nbox, nb);
+  if (ok && !P.small)
+    ok = make_map(&mA, A, false, r, in, in, kBM, rb) && make_map(&mAh_g, a_h, true, r, in8, in8, gg.p.nbox, nb) &&
+         make_map(&mAl_g, a_l, true, r, in8, in8, gg.p.nbox, nb) && make_map_t(&mBt, Bk, out, r, ldb, kBK) &&
+         make_map(&mYh_h, y_h, true, r, out8, out8, gh.p.nbox, nb) &&
+         make_map(&mYl_h, y_l, true, r, out8, out8, gh.p.nbox, nb);
   if (!ok) return fail();
 
-  // 2. s G = s A A^T (partial tiles, fixed-order reduction, split)
-  GemmPlan pg = gg;
-  pg.p.part = part_t;
-  pg.p.err = errp;
-  if (launch_gemm(pg, cs, mA, mA, mAh_g, mAl_g, mAh_g, mAl_g) != cudaSuccess) return fail();
-  ++launches;
-  {
-    const StreamK sk{pg.p.units, pg.p.ncl, pg.p.kbtot, pg.p.maxseg};
-    const int nsub = (pg.p.NC + 31) / 32;
-    gram_reduce_kernel<<<dim3(static_cast<unsigned>(pg.p.tiles), static_cast<unsigned>(nsub * nsub)),
-                               dim3(32, 8), 0, cs>>>(part_t, sk, pg.p.nchunks, pg.p.NC, static_cast<int>(r), npad, s,
-                                                     g_h, g_l);
+  if (P.small) {
+    // 2-3. s G and s^2 H from the partials (fixed-order sums, split)
+    sg_fin_kernel<<<2 * P.sg.ntiles * (P.sg.T * P.sg.T / 64), 256, 0, cs>>>(part_t, P.sg, npad, s, g_h, g_l, h_h,
+                                                                              h_l);
     ++launches;
-  }
-  // 3. s^2 H = s (B^T (s c (.) B)), B read transposed
-  GemmPlan ph = gh;
-  ph.p.part = part_t;
-  ph.p.err = errp;
-  if (launch_gemm(ph, cs, mBt, mBt, mYh_h, mYl_h, mYh_h, mYl_h) != cudaSuccess) return fail();
-  ++launches;
-  {
-    const StreamK sk{ph.p.units, ph.p.ncl, ph.p.kbtot, ph.p.maxseg};
-    const int nsub = (ph.p.NC + 31) / 32;
-    gram_reduce_kernel<<<dim3(static_cast<unsigned>(ph.p.tiles), static_cast<unsigned>(nsub * nsub)),
-                               dim3(32, 8), 0, cs>>>(part_t, sk, ph.p.nchunks, ph.p.NC, static_cast<int>(r), npad, s,
-                                                     h_h, h_l);
+  } else {
+    // 2. s G = s A A^T (partial tiles, fixed-order reduction, split)
+    GemmPlan pg = gg;
+    pg.p.part = part_t;
+    pg.p.err = errp;
+    if (launch_gemm(pg, cs, mA, mA, mAh_g, mAl_g, mAh_g, mAl_g) != cudaSuccess) return fail();
     ++launches;
+    {
+      const StreamK sk{pg.p.units, pg.p.ncl, pg.p.kbtot, pg.p.maxseg};
+      const int nsub = (pg.p.NC + 31) / 32;
+      gram_reduce_kernel<<<dim3(static_cast<unsigned>(pg.p.tiles), static_cast<unsigned>(nsub * nsub)),
+                                 dim3(32, 8), 0, cs>>>(part_t, sk, pg.p.nchunks, pg.p.NC, static_cast<int>(r), npad,
+                                                       s, g_h, g_l);
+      ++launches;
+    }
+    // 3. s^2 H = s (B^T (s c (.) B)), B read transposed
+    GemmPlan ph = gh;
+    ph.p.part = part_t;
+    ph.p.err = errp;
+    if (launch_gemm(ph, cs, mBt, mBt, mYh_h, mYl_h, mYh_h, mYl_h) != cudaSuccess) return fail();
+    ++launches;
+    {
+      const StreamK sk{ph.p.units, ph.p.ncl, ph.p.kbtot, ph.p.maxseg};
+      const int nsub = (ph.p.NC + 31) / 32;
+      gram_reduce_kernel<<<dim3(static_cast<unsigned>(ph.p.tiles), static_cast<unsigned>(nsub * nsub)),
+                                 dim3(32, 8), 0, cs>>>(part_t, sk, ph.p.nchunks, ph.p.NC, static_cast<int>(r), npad,
+                                                       s, h_h, h_l);
+      ++launches;
+    }
   }
   // 4. dB = s c (.) ([W0 | B] x [A | s G]^T): partial rows, then their sum
   GemmPlan pb = gb;

@@ -10,8 +10,10 @@ Tolerance, derived from the arithmetic.  Every output element is a sum of
 products evaluated with the bf16 three-product split (x = h + l with h =
 bf16(x), l = bf16(x - h); per product the dropped l l term and the residuals
 are <= 3 * 2^-18 of its magnitude, see dora_norm_factored) and fp32
-accumulation; dA also carries the error of s^2 H, itself such a sum.  With |.| the same expressions over
-absolute values (abs_ref), a rigorous elementwise bound is
+accumulation; dA also carries the error of s^2 H, itself such a sum.  (For
+r <= 256, s G and s^2 H are fp32 FMA sums on the CUDA cores, whose error
+lies within the same bound.)  With |.| the same expressions over absolute
+values (abs_ref), a rigorous elementwise bound is
     |err| <= (2^-16 + 2^-23 (K + 64)) * abs_ref,   K = out + in + 2 r
 (2^-23 per addition allows for an accumulator that truncates).  Because that
 bound grows with K, the normwise error is also held to the norm's own
@@ -111,6 +113,10 @@ def _run_and_check(d, d_mag):
     (300, 1040, 128),     # N = 128: 32-wide K blocks
     (260, 200, 129),      # N = 144
     (1030, 136, 64),      # out (the K of the dA pass) ragged against every K block width
+    (200, 136, 32),       # CUDA-core Gram products: the largest r of 32 x 32 tiles
+    (200, 136, 33),       # the smallest r of 64 x 64 tiles
+    (2000, 4104, 256),    # the largest r of the CUDA-core Gram; slices longer than 128 (one wave)
+    (300, 520, 257),      # the smallest r of the tensor-core Gram passes
 ])
 def test_norm_grad_shapes(out, inp, r):
     d, d_mag = _case(out, inp, r, 9100 + out + r)

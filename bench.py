@@ -825,6 +825,15 @@ def run_report(args):
         Bs16 = (sh.s * B).bfloat16()
         t_lora = _time_ms(lambda: dora.dora_compose_lora_fwd(base, xa, B, g, sh.s, y, ws, stream), 20, stream)
         t_lin = _time_ms(lambda: dora.dora_linear_fwd(x, W0, xa, B, g, sh.s, y, ws, stream), 10, stream)
+        # the lora form for an adapter kept in bf16 (one product, no split)
+        B16 = B.bfloat16()
+        t_lb = _time_ms(lambda: dora.dora_compose_lora_fwd_bf16(base, xa, B16, g, sh.s, y, stream), 20, stream)
+
+        def unfused_lora_bf16():
+            lora = torch.matmul(xa, B16.t())
+            dora.dora_compose_fwd(base, lora, g, sh.s, y, stream)
+
+        t_lb_u = _time_ms(unfused_lora_bf16, 20, stream)
 
         def unfused_lora():
             lora = torch.matmul(xa, Bs16.t())
@@ -839,10 +848,13 @@ def run_report(args):
         t_lin_u = _time_ms(unfused_linear, 10, stream)
         t_gemm = _time_ms(lambda: torch.matmul(x, W0.t()), 10, stream)
         lora_bytes = 2 * T * out * 2 + T * r * 2 + 2 * out * r * 2      # base, y, xa, the two bf16 halves of s B
+        lb_bytes = 2 * T * out * 2 + T * r * 2 + out * r * 2            # base, y, xa, B
         flops = 2 * T * out * (inp + r)
         print(json.dumps({"report": "fused", "T": T, "in": inp, "out": out, "r": r,
                           "lora_form_us": t_lora * 1e3, "lora_form_gbs": lora_bytes / (t_lora * 1e-3) / 1e9,
                           "unfused_lora_matmul_plus_compose_us": t_lora_u * 1e3,
+                          "lora_form_bf16_b_us": t_lb * 1e3, "lora_form_bf16_b_gbs": lb_bytes / (t_lb * 1e-3) / 1e9,
+                          "unfused_lora_bf16_b_matmul_plus_compose_us": t_lb_u * 1e3,
                           "linear_form_us": t_lin * 1e3,
                           "linear_form_tflops_algorithmic": flops / (t_lin * 1e-3) / 1e12,
                           "unfused_two_matmuls_plus_compose_us": t_lin_u * 1e3,

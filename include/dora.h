@@ -344,6 +344,27 @@ dora_status dora_compose_lora_fwd(const void *base, const void *xa, const float 
                                   dora_stream_t stream);
 
 /*
+ * The same lora up-projection form for a bf16 B (adapters kept in bf16):
+ * y = base + (g-1)*base + g*(s*acc) with acc = xa B^T, B used as it is as the
+ * tensor-core operand (every product exact in fp32, fp32 accumulation), s
+ * applied to the accumulator in the epilogue, y rounded once to bf16
+ * (P1 ¶第二个创新是"融合Triton内核"技术, the stable form).  One product instead
+ * of the fp32-B form's two, and no split of B: one launch, no workspace.
+ *
+ *   base  bf16 [T, out]   xa  bf16 [T, r]   B  bf16 [out, r]   y  bf16 [T, out]
+ *   g  float32 [out]; all five 16-byte aligned
+ *   Sizes: T, out >= 0 (either 0 is a no-op), r >= 1; out % 8 == 0 and
+ *   r % 8 == 0.
+ * One launch (an ordinary one: it reads base from its first instruction), as
+ * clusters of two CTAs where the device holds them, else single CTAs.
+ * Results are bitwise reproducible for a given shape and device.
+ */
+dora_status dora_compose_lora_fwd_bf16(const void *base, const void *xa, const void *B,
+                                       const float *g, float s,
+                                       int64_t T, int64_t out, int64_t r, void *y,
+                                       dora_stream_t stream);
+
+/*
  * The whole layer output y = g*(x W0^T + s xa B^T) as ONE tensor-core GEMM
  * over K = in + r ([x | xa] times [W0 | s B]^T), with the compose in its
  * epilogue: neither base nor lora is formed.  x [T, in] and W0 [out, in] are

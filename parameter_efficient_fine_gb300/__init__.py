@@ -26,6 +26,7 @@ __all__ = [
     "dora_compose_fwd",
     "dora_compose_fused_workspace",
     "dora_compose_lora_fwd",
+    "dora_compose_lora_fwd_bf16",
     "dora_linear_fwd",
     "dora_compose_bwd_workspace",
     "dora_compose_bwd",
@@ -63,6 +64,7 @@ _SIGNATURES = {
     "dora_compose_fwd": (_int, [_int, _vp, _vp, _vp, _f32, _i64, _i64, _vp, _vp]),
     "dora_compose_fused_workspace": (_sz, [_i64, _i64]),
     "dora_compose_lora_fwd": (_int, [_vp, _vp, _vp, _vp, _f32, _i64, _i64, _i64, _vp, _vp, _sz, _vp]),
+    "dora_compose_lora_fwd_bf16": (_int, [_vp, _vp, _vp, _vp, _f32, _i64, _i64, _i64, _vp, _vp]),
     "dora_linear_fwd": (_int, [_vp, _vp, _vp, _vp, _vp, _f32, _i64, _i64, _i64, _i64, _vp, _vp, _sz, _vp]),
     "dora_compose_bwd_workspace": (_sz, [_i64, _i64]),
     "dora_compose_bwd": (_int, [_int, _vp, _vp, _vp, _vp, _vp, _f32, _i64, _i64, _vp, _vp, _vp, _vp, _sz, _vp]),
@@ -209,6 +211,16 @@ def dora_compose_lora_fwd(base, xa, B, g, s: float, y, workspace, stream=None) -
         _ptr(base), _ptr(xa), _ptr(B), _ptr(g), float(s), T, out, r, _ptr(y),
         _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
     _check("dora_compose_lora_fwd", st)
+
+
+def dora_compose_lora_fwd_bf16(base, xa, B, g, s: float, y, stream=None) -> None:
+    """y = base + (g-1) base + g s (xa B^T) for a bf16 B: one product, s applied to
+    the accumulator (see include/dora.h)."""
+    T, out = base.shape
+    r = xa.shape[1]
+    st = load_library().dora_compose_lora_fwd_bf16(
+        _ptr(base), _ptr(xa), _ptr(B), _ptr(g), float(s), T, out, r, _ptr(y), _stream(stream))
+    _check("dora_compose_lora_fwd_bf16", st)
 
 
 def dora_linear_fwd(x, W0, xa, B, g, s: float, y, workspace, stream=None) -> None:

@@ -15,11 +15,15 @@
 //   dora_linear_fwd        (both products, one K-concatenated GEMM):
 //       acc = [x | xa] [W0 | s B]^T            K = in + r
 //       y   = g acc                            neither base nor lora is stored
+//   dora_compose_lora_fwd_bf16  (the up-projection with a bf16 B):
+//       acc = xa B^T                           K = r, one product
+//       y   = base + (g - 1) base + g (s acc)  s applied in the epilogue
 //
 // Operands are bf16, so every product is exact in fp32; the fp32 B is scaled
 // by s and split into bf16 hi + lo (|lo| <= 2^-9 |hi|, residual <= 2^-17 of
 // s B), and xa multiplies both (the xa segment of K is taken twice, against
-// hi and against lo).  Accumulation is fp32 in tensor memory; y is rounded once
+// hi and against lo).  A bf16 B is taken as it is, as the linear form takes
+// W0 (its first K segment), and s scales the accumulator.  Accumulation is fp32 in tensor memory; y is rounded once
 // to bf16.
 //
 // Kernel structure (persistent, one CTA per SM, 320 threads for the linear
@@ -54,8 +58,8 @@
 //               accumulator right after its last tensor-memory load of the
 //               tile, before computing y.  The epilogue warps never wait
 //               for one another
-// A call is two launches: split_sb_kernel (s B into hi and lo), then this
-// kernel as a programmatic dependent launch on it: its prologue and the
+// A call with an fp32 B is two launches: split_sb_kernel (s B into hi and
+// lo), then this kernel as a programmatic dependent launch on it: its prologue and the
 // epilogue's first base loads overlap the split, and only the producer,
 // which loads hi and lo, waits for the split to complete.
 // Every wait on a shared-memory barrier is bounded; a wait that gives up
@@ -101,6 +105,7 @@ struct FusedParams {
   int nslots;           // staging slots per epilogue warp: one per quarter with base, else one
   int groupm;           // M tiles per tile-order group (tile_mn)
   int has_base;
+  float acc_scale;      // SC kernels: the accumulator's factor in the epilogue (s)
   const float *g;
   int *err;
   const int *stall;                      // test hook: the producer withholds its loads
@@ -148,7 +153,9 @@ __device__ __forceinline__ bool fwait(uint32_t bar, uint32_t parity, SharedCtl *
 // K block instead of 48.  Both CTAs' copies of a stage complete on the even
 // CTA's stage barrier; the even CTA's lane issues the MMAs and signals both
 // CTAs' stage-free and accumulator barriers.
-template <bool PAIR, int EPI>
+// SC: the accumulator is multiplied by p.acc_scale in the epilogue (the bf16-B
+// lora form, whose weight operand is B itself rather than s B)
+template <bool PAIR, int EPI, bool SC = false>
 __global__ void __launch_bounds__(fthreads(EPI), 1)
 fused_compose_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUtensorMap mA1,
                      const __grid_constant__ CUtensorMap mB0, const __grid_constant__ CUtensorMap mB1,
@@ -208,7 +215,7 @@ fused_compose_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_const
     prefetch_map(&mB1);
     prefetch_map(&mB2);
     prefetch_map(&mY);
-    if (p.nseg == 3) {
+    if (p.kb[0] > 0) {
       prefetch_map(&mA0);
       prefetch_map(&mB0);
     }
@@ -498,8 +505,10 @@ fused_compose_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_const
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                   const float2 b2 = __bfloat1622float2(bb[e]);
-                  yv[2 * e] = b2.x + fmaf(gv[2 * e] - 1.0f, b2.x, gv[2 * e] * a[2 * e]);
-                  yv[2 * e + 1] = b2.y + fmaf(gv[2 * e + 1] - 1.0f, b2.y, gv[2 * e + 1] * a[2 * e + 1]);
+                  const float a0 = SC ? p.acc_scale * a[2 * e] : a[2 * e];
+                  const float a1 = SC ? p.acc_scale * a[2 * e + 1] : a[2 * e + 1];
+                  yv[2 * e] = b2.x + fmaf(gv[2 * e] - 1.0f, b2.x, gv[2 * e] * a0);
+                  yv[2 * e + 1] = b2.y + fmaf(gv[2 * e + 1] - 1.0f, b2.y, gv[2 * e + 1] * a1);
                 }
               } else {
 #pragma unroll
@@ -593,8 +602,10 @@ struct FusedPlan {
 };
 
 // max_units: CTAs (one per SM) or, for pairs, the pairs that can be resident at once
+// bf16_b: the lora form with a bf16 B, one K segment of r (xa, B) like the
+// linear form's (x, W0)
 bool plan_fused(int64_t T, int64_t in, int64_t out, int64_t r, bool has_base, bool pair, int max_units,
-                FusedPlan *fp) {
+                FusedPlan *fp, bool bf16_b = false) {
   FusedParams &p = fp->p;
   p = FusedParams{};
   fp->pair = pair;
@@ -603,11 +614,13 @@ bool plan_fused(int64_t T, int64_t in, int64_t out, int64_t r, bool has_base, bo
   fp->epi = has_base ? 16 : 8;
   p.T = static_cast<int>(T);
   p.out = static_cast<int>(out);
-  p.nseg = has_base ? 2 : 3;
+  p.nseg = bf16_b ? 1 : has_base ? 2 : 3;
   // K blocks (stages) per segment: single CTA (x, W0), (xa, s B hi), (xa, s B
-  // lo), 64 K each; a pair (x, W0) by 128 K, then (xa; s B hi, s B lo) by 64 K
-  p.kb[0] = has_base ? 0 : static_cast<int>(dora::ceil_div(in, pair ? 2 * kFK : kFK));
-  p.kb[1] = static_cast<int>(dora::ceil_div(r, kFK));
+  // lo), 64 K each; a pair (x, W0) by 128 K, then (xa; s B hi, s B lo) by 64 K.
+  // A bf16 B: only the first segment, (xa, B) over K = r
+  const int64_t k0 = bf16_b ? r : has_base ? 0 : in;
+  p.kb[0] = static_cast<int>(dora::ceil_div(k0, pair ? 2 * kFK : kFK));
+  p.kb[1] = bf16_b ? 0 : static_cast<int>(dora::ceil_div(r, kFK));
   p.kb[2] = pair ? 0 : p.kb[1];
   p.kbtot = p.kb[0] + p.kb[1] + p.kb[2];
   p.mtiles = static_cast<int>(dora::ceil_div(T, pair ? 2 * kFM : kFM));
@@ -626,7 +639,7 @@ bool plan_fused(int64_t T, int64_t in, int64_t out, int64_t r, bool has_base, bo
   // a pair: two token-side boxes per stage for the linear form's (x, W0)
   // segment, one for the lora form; two half weight boxes.  A single CTA: one
   // token-side box and one weight box
-  p.na = (pair && !has_base) ? 2 : 1;
+  p.na = (pair && p.kb[0] > 0) ? 2 : 1;
   const size_t stage_bytes = static_cast<size_t>(p.na) * kABytes + kBBytes;
   p.stage_bytes = static_cast<unsigned>(stage_bytes);
   p.stages = static_cast<int>((kFSmemMax - fixed) / stage_bytes);
@@ -684,7 +697,9 @@ dora_status fused_init(int device, int sms, int **errp) {
     if (cudaFuncSetAttribute(fused_compose_kernel<false, 8>, a, kFSmemMax) != cudaSuccess ||
         cudaFuncSetAttribute(fused_compose_kernel<true, 8>, a, kFSmemMax) != cudaSuccess ||
         cudaFuncSetAttribute(fused_compose_kernel<false, 16>, a, kFSmemMax) != cudaSuccess ||
-        cudaFuncSetAttribute(fused_compose_kernel<true, 16>, a, kFSmemMax) != cudaSuccess)
+        cudaFuncSetAttribute(fused_compose_kernel<true, 16>, a, kFSmemMax) != cudaSuccess ||
+        cudaFuncSetAttribute(fused_compose_kernel<false, 16, true>, a, kFSmemMax) != cudaSuccess ||
+        cudaFuncSetAttribute(fused_compose_kernel<true, 16, true>, a, kFSmemMax) != cudaSuccess)
       return DORA_ERR_CUDA;
     // pairs resident at once with the largest shared-memory footprint (one CTA per SM)
     cudaLaunchConfig_t cfg = {};
@@ -792,6 +807,57 @@ dora_status fused_run(const void *x, const void *W0, const void *base, const voi
   return dora::launch_status();
 }
 
+// the lora form with a bf16 B: one launch, no split (B is the MMA operand as
+// it is; s scales the accumulator)
+dora_status fused_run_bf16b(const void *base, const void *xa, const void *B, const float *g, float s, int64_t T,
+                            int64_t out, int64_t r, void *y, dora_stream_t stream) {
+  dora::DeviceInfo info;
+  int device = 0;
+  dora_status st = dora::current_device(&info, &device);
+  if (st != DORA_OK) return st;
+  const int sms = info.sms < kFMaxCtas ? info.sms : kFMaxCtas;
+  int *errp = nullptr;
+  st = fused_init(device, sms, &errp);
+  if (st != DORA_OK) return st;
+  const int max_pairs = g_max_pairs[device];
+  const bool pair = max_pairs > 0 && g_pairs_allowed.load() != 0;
+  FusedPlan fp;
+  if (!plan_fused(T, 0, out, r, true, pair, pair ? max_pairs : sms, &fp, true)) return DORA_ERR_SHAPE;
+  fp.p.g = g;
+  fp.p.acc_scale = s;
+  fp.p.err = errp;
+  fp.p.stall = g_stall_ptr[device];
+  fp.p.limit_ns = g_limit_ptr[device];
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  uint64_t launches = 0;
+  const int brows = pair ? kFN / 2 : kFN;
+  CUtensorMap mA0, mB0, mC, mY;
+  const bool ok = map_bf16(&mA0, xa, T, r, r, kFM) && map_bf16(&mB0, B, out, r, r, brows) &&
+                  map_bf16(&mC, base, T, out, out, 32) && map_bf16(&mY, y, T, out, out, 32);
+  if (!ok) return DORA_ERR_CUDA;
+  // an ordinary launch: the epilogue reads base from the first instruction, so
+  // the kernel may not start before the launch that wrote it has completed
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  cudaError_t e;
+  if (pair) {
+    pair_config(&cfg, attr, static_cast<unsigned>(fp.ctas), fthreads(16), fp.smem_bytes, cs);
+    e = cudaLaunchKernelEx(&cfg, fused_compose_kernel<true, 16, true>, mA0, mA0, mB0, mB0, mB0, mC, mY, fp.p);
+  } else {
+    cfg.gridDim = dim3(static_cast<unsigned>(fp.ctas));
+    cfg.blockDim = dim3(static_cast<unsigned>(fthreads(16)));
+    cfg.dynamicSmemBytes = fp.smem_bytes;
+    cfg.stream = cs;
+    cfg.attrs = attr;
+    cfg.numAttrs = 0;
+    e = cudaLaunchKernelEx(&cfg, fused_compose_kernel<false, 16, true>, mA0, mA0, mB0, mB0, mB0, mC, mY, fp.p);
+  }
+  if (e != cudaSuccess) return DORA_ERR_CUDA;
+  ++launches;
+  dora::count_launches(launches);
+  return dora::launch_status();
+}
+
 }  // namespace
 
 extern "C" size_t dora_compose_fused_workspace(int64_t out, int64_t r) {
@@ -840,6 +906,20 @@ extern "C" dora_status dora_linear_fwd(const void *x, const void *W0, const void
   if (st != DORA_OK) return st;
   if (in % 8 != 0 || !dora::aligned(x, 16) || !dora::aligned(W0, 16)) return DORA_ERR_ALIGN;
   return fused_run(x, W0, nullptr, xa, B, g, s, T, in, out, r, y, workspace, workspace_bytes, stream);
+}
+
+extern "C" dora_status dora_compose_lora_fwd_bf16(const void *base, const void *xa, const void *B, const float *g,
+                                                  float s, int64_t T, int64_t out, int64_t r, void *y,
+                                                  dora_stream_t stream) {
+  if (T < 0 || out < 0 || r < 1 || T >= (1ll << 31) || out >= (1ll << 31) || r >= (1ll << 20)) return DORA_ERR_SHAPE;
+  if (T == 0 || out == 0) return DORA_OK;
+  if (!base || !xa || !B || !g || !y) return DORA_ERR_NULL;
+  // TMA: 16-byte aligned bases and row strides (bf16 rows of out and r elements)
+  if (out % 8 != 0 || r % 8 != 0) return DORA_ERR_ALIGN;
+  if (!dora::aligned(base, 16) || !dora::aligned(xa, 16) || !dora::aligned(B, 16) || !dora::aligned(y, 16) ||
+      !dora::aligned(g, 16))
+    return DORA_ERR_ALIGN;
+  return fused_run_bf16b(base, xa, B, g, s, T, out, r, y, stream);
 }
 
 extern "C" dora_status dora_test_fused_pairs(int allow) {

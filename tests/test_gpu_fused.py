@@ -1,6 +1,7 @@
 """GPU parity of the compose folded into its adjacent products
-(dora_compose_lora_fwd, dora_linear_fwd) against the fp64 oracle, through the
-C ABI.  Tolerance: the bf16 rule of tests/gpu_util.py (|err| <= 2^-7 |ref| +
+(dora_compose_lora_fwd, dora_compose_lora_fwd_bf16, dora_linear_fwd) against
+the fp64 oracle, through the C ABI.  The bf16-B form gets B rounded to bf16,
+and the oracle the same bf16 values.  Tolerance: the bf16 rule of tests/gpu_util.py (|err| <= 2^-7 |ref| +
 1e-3 elementwise, cosine >= 0.99999).  The fraction of outputs equal to the
 correctly rounded bf16 of the exact result is also checked: y is rounded once
 from an fp32 accumulator whose error is far below half a bf16 ulp, so almost
@@ -47,6 +48,21 @@ def run_lora(d):
     return y
 
 
+def run_lora_bf16(d):
+    """The lora form for a bf16 B (B rounded to bf16 by the seeded generator's
+    rounding; the oracle receives the same values)."""
+    base, xa = act_to_dev(d["base"]), act_to_dev(d["xa"])
+    Bb, g = act_to_dev(wl.f32_to_bf16_bits(d["B"])), f32_dev(d["g"])
+    y = torch.full_like(base, float("nan"))
+    dora.dora_compose_lora_fwd_bf16(base, xa, Bb, g, d["s"], y)
+    return y
+
+
+def ref_lora_bf16(d, rows=slice(None)):
+    return oracle.compose_lora_fwd(_f64(d["base"][rows]), _f64(d["xa"][rows]), _f64(wl.f32_to_bf16_bits(d["B"])),
+                                   d["g"], d["s"])
+
+
 def run_linear(d):
     x, W0, xa = act_to_dev(d["x"]), act_to_dev(d["W0"]), act_to_dev(d["xa"])
     B, g = f32_dev(d["B"]), f32_dev(d["g"])
@@ -84,6 +100,21 @@ def test_lora_form(T, out, r, layout):
     _check("y (lora form)", y, ref)
 
 
+@pytest.mark.parametrize("T,out,r", [
+    (300, 520, 40),      # ragged tokens and outputs; K below one 64-block
+    (128, 256, 8),       # one tile exactly
+    (1000, 1032, 384),   # several tiles, ragged output tile; K = 3 x 128 on pairs
+    (77, 8, 16),         # one partial tile
+    (513, 4096, 776),    # many output tiles; K ragged against the 128-wide pair stages
+    (1, 264, 64),        # one token
+])
+def test_lora_form_bf16_b(T, out, r, layout):
+    d = _layer(T, 16, out, r, 9550 + T + out + r)
+    y = run_lora_bf16(d)
+    assert_no_device_error()
+    _check("y (lora form, bf16 B)", y, ref_lora_bf16(d))
+
+
 @pytest.mark.parametrize("T,inp,out,r", [
     (300, 264, 520, 40),     # ragged everything; K = 264 + 2 x 40
     (257, 1032, 776, 128),   # K blocks ragged in the x segment
@@ -118,12 +149,16 @@ def test_drawn_shapes_both_forms(k, layout):
     assert_no_device_error()
     _check("y (linear form)", y,
            oracle.linear_fwd(_f64(d["x"]), _f64(d["W0"]), _f64(d["xa"]), d["B"], d["g"], d["s"]))
+    y = run_lora_bf16(d)
+    assert_no_device_error()
+    _check("y (lora form, bf16 B)", y, ref_lora_bf16(d))
 
 
 def test_bitwise_reproducible(layout):
     d = _layer(300, 264, 520, 40, 9700)
     assert torch.equal(run_linear(d), run_linear(d))
     assert torch.equal(run_lora(d), run_lora(d))
+    assert torch.equal(run_lora_bf16(d), run_lora_bf16(d))
 
 
 def test_g_one_and_zero_adapter_lora_form_returns_base():
@@ -133,6 +168,7 @@ def test_g_one_and_zero_adapter_lora_form_returns_base():
     d["g"] = np.ones_like(d["g"])
     y = run_lora(d)
     assert torch.equal(y, act_to_dev(d["base"]))
+    assert torch.equal(run_lora_bf16(d), act_to_dev(d["base"]))
 
 
 def test_full_size_sampled():
@@ -145,8 +181,11 @@ def test_full_size_sampled():
     ref_lin = oracle.linear_fwd(_f64(d["x"][rows]), _f64(d["W0"]), _f64(d["xa"][rows]), d["B"], d["g"], d["s"])
     y_lora = to_f64(run_lora(d))[rows]
     ref_lora = oracle.compose_lora_fwd(_f64(d["base"][rows]), _f64(d["xa"][rows]), d["B"], d["g"], d["s"])
+    y_lb = to_f64(run_lora_bf16(d))[rows]
+    ref_lb = ref_lora_bf16(d, rows)
     assert_no_device_error()
-    for name, got, ref in (("y (linear form)", y_lin, ref_lin), ("y (lora form)", y_lora, ref_lora)):
+    for name, got, ref in (("y (linear form)", y_lin, ref_lin), ("y (lora form)", y_lora, ref_lora),
+                           ("y (lora form, bf16 B)", y_lb, ref_lb)):
         check_bf16_rule(name, got, ref)
         cr = float(np.mean(got == oracle.bf16_bits_to_f64(oracle.f64_to_bf16_bits(ref))))
         assert cr >= CR_MIN, f"{name}: only {cr:.4f} of outputs correctly rounded"

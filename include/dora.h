@@ -312,8 +312,9 @@ dora_status dora_compose_bwd_noalloc(dora_dtype act, const void *grad_out, const
 /* (d) the compose folded into its adjacent products                         */
 /* ------------------------------------------------------------------------ */
 
-/* Bytes of workspace the two entry points below need (host arithmetic; 0 for
- * an invalid shape): s B split into two bf16 [out, r] matrices. */
+/* Bytes of workspace dora_compose_lora_fwd and dora_linear_fwd need (host
+ * arithmetic; 0 for an invalid shape): s B split into two bf16 [out, r]
+ * matrices.  dora_compose_lora_fwd_bf16 needs none. */
 size_t dora_compose_fused_workspace(int64_t out, int64_t r);
 
 /*

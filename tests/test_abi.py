@@ -245,3 +245,19 @@ def test_fused_forward_workspace_and_argument_errors(lib):
     assert call_l(inp=12) == 3
     assert call_l(x=FAKE + 4) == 3
     assert call_l(wsb=16) == 5
+    lb = lib.dora_compose_lora_fwd_bf16
+    okb = dict(base=FAKE, xa=FAKE, B=FAKE, g=FAKE, s=1.0, T=64, out=256, r=16, y=FAKE, stream=None)
+
+    def call_b(**kw):
+        a = dict(okb, **kw)
+        return lb(a["base"], a["xa"], a["B"], a["g"], a["s"], a["T"], a["out"], a["r"], a["y"], a["stream"])
+
+    assert call_b(T=-1) == 2
+    assert call_b(r=0) == 2
+    assert call_b(T=0) == 0 and call_b(out=0) == 0       # empty: no-op
+    assert call_b(B=None) == 1
+    assert call_b(g=None) == 1
+    assert call_b(out=260) == 3
+    assert call_b(r=12) == 3
+    assert call_b(B=FAKE + 8) == 3                       # bf16 B is a TMA operand: 16-byte aligned
+    assert call_b(g=FAKE + 4) == 3

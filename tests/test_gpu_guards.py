@@ -112,13 +112,16 @@ def test_fused_forward_writes_stay_in_bounds(T, inp, out, r):
     d = wl.make_layer(sh, 33)
     x, W0, xa, base = (act_to_dev(d[k]) for k in ("x", "W0", "xa", "base"))
     B, g = f32_dev(d["B"]), f32_dev(d["g"])
+    B16 = act_to_dev(wl.f32_to_bf16_bits(d["B"]))
     nbytes = dora.dora_compose_fused_workspace(out, r)
-    for form in ("lora", "linear"):
+    for form in ("lora", "lora_bf16", "linear"):
         y_b, ws_b = Guarded(T * out * 2), Guarded(nbytes)
         y = y_b.view(torch.bfloat16, (T, out))
         ws = ws_b.view(torch.uint8, (nbytes,))
         if form == "lora":
             dora.dora_compose_lora_fwd(base, xa, B, g, d["s"], y, ws)
+        elif form == "lora_bf16":
+            dora.dora_compose_lora_fwd_bf16(base, xa, B16, g, d["s"], y)
         else:
             dora.dora_linear_fwd(x, W0, xa, B, g, d["s"], y, ws)
         torch.cuda.synchronize()

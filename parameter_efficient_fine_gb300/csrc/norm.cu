@@ -593,6 +593,10 @@ struct FwdParams {
   int M;            // out (rows of the norm phase)
   int r, npad;
   int NT;           // N-side rows of a stage (the larger phase's)
+  // NT <= 64: h_x h_y and h_x l_y as ONE MMA of N = 2 NT over the stage's h
+  // and l rows together (accumulator columns [0, NT) and [NT, 2 NT), added in
+  // the epilogue), then l_x h_y: two MMAs per K = 16 step instead of three
+  int dbl;
   int tmem_cols, slot0;
   int S;            // N-side stages = tensor-memory operand slots
   int SX;           // raw M-side box slots
@@ -693,7 +697,9 @@ __device__ __forceinline__ void store_gs3(__nv_bfloat16 *gh, __nv_bfloat16 *gl, 
   gl[i] = __float2bfloat16_rn(v - __bfloat162float(h));
 }
 
-template <int FBK>
+// DBL: the plan's dbl (two MMAs per K = 16 step, N-side rows <= 64), a
+// separate instance so that the other ranks' code is unchanged
+template <int FBK, bool DBL = false>
 __global__ void __launch_bounds__(kFwdThreads, 1)
 fwd_norm_kernel(const __grid_constant__ CUtensorMap mA, const __grid_constant__ CUtensorMap mW0,
                 const __grid_constant__ CUtensorMap mB, const __grid_constant__ CUtensorMap mAh_g,
@@ -858,6 +864,8 @@ fwd_norm_kernel(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
       uint32_t sph = 0;
       uint32_t aphase = 0;
       bool ok = true;
+      constexpr bool dbl = DBL;
+      const uint32_t icd = dbl ? idesc_bf16(2 * p.NT) : 0u;
       for (int ph = 0; ph < 2 && ok; ++ph) {
         const FwdPhase &f = p.ph[ph];
         const uint32_t ic0 = idesc_bf16(f.nmma0);
@@ -893,9 +901,14 @@ fwd_norm_kernel(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
               const uint32_t ah = sh + 8u * k, al = sl + 8u * k;
               {
                 const uint64_t bh = sdesc<kFwdBK / 2>(yh + ko), bl = sdesc<kFwdBK / 2>(yl + ko);
-                mma_bf16_ta(tmem, ah, bh, ic0, acc0);
-                mma_bf16_ta(tmem, al, bh, ic0, 1u);
-                mma_bf16_ta(tmem, ah, bl, ic0, 1u);
+                if constexpr (dbl) {
+                  mma_bf16_ta(tmem, ah, bh, icd, acc0);   // rows [h; l] of the stage: h_x h_y | h_x l_y
+                  mma_bf16_ta(tmem, al, bh, ic0, 1u);
+                } else {
+                  mma_bf16_ta(tmem, ah, bh, ic0, acc0);
+                  mma_bf16_ta(tmem, al, bh, ic0, 1u);
+                  mma_bf16_ta(tmem, ah, bl, ic0, 1u);
+                }
               }
               if (f.nmma1 > 0) {
                 const uint32_t no = 256u * kFwdNRow;
@@ -926,6 +939,18 @@ fwd_norm_kernel(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
     const int row = quad * 32 + lane;
     const int ct = threadIdx.x - 64;   // 0..127 over the four converter warps
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+    // accumulator columns [c, c + 32) of this warp's rows; with p.dbl the
+    // h_x l_y half (NT columns on) is added in
+    const int nt_cols = p.NT;
+    auto acc_ld32 = [&](int c, float (&v)[32]) {
+      tmem_ld32(lane_addr + static_cast<uint32_t>(c), v);
+      if constexpr (DBL) {
+        float w[32];
+        tmem_ld32(lane_addr + static_cast<uint32_t>(nt_cols + c), w);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) v[e] += w[e];
+      }
+    };
     int xs = 0, ss = 0;
     uint32_t xph = 0, sph = 0;
     uint32_t aphase = 0;
@@ -1056,7 +1081,7 @@ fwd_norm_kernel(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
             const uint8_t *rw = smem + quad * nchk * 4096 + lane * 128;
             for (int ci = 0; ci < nchk; ++ci) {
               float v[32];
-              tmem_ld32(lane_addr + static_cast<uint32_t>(32 * ci), v);
+              acc_ld32(32 * ci, v);
               // columns past the chunk's last valid one: neither B (the box may
               // reach into the next chunk) nor the accumulator (past N it was
               // never written) may enter the sum
@@ -1089,7 +1114,7 @@ fwd_norm_kernel(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
           for (int ci = 0; ci < nchk; ++ci) {
             ldb8(ci + 2, b2);
             float v[32];
-            tmem_ld32(lane_addr + static_cast<uint32_t>(32 * ci), v);
+            acc_ld32(32 * ci, v);
             // accumulator columns past the chunk's valid ones (past N they
             // were never written) stay out of the sum
 #pragma unroll
@@ -1150,7 +1175,7 @@ fwd_norm_kernel(const __grid_constant__ CUtensorMap mA, const __grid_constant__ 
           float *dst = f.part + (static_cast<size_t>(cl) * kBM + row) * f.NC;
           for (int c = 0; c < f.NC; c += 32) {
             float v[32];
-            tmem_ld32(lane_addr + static_cast<uint32_t>(c), v);
+            acc_ld32(c, v);
 #pragma unroll
             for (int j = 0; j < 32; j += 4) {
               if (c + j < f.NC) *reinterpret_cast<float4 *>(dst + c + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
@@ -2437,7 +2462,11 @@ bool plan_fwd(int64_t out, int64_t in, int64_t r, int max_ctas, FwdPlan *fp, boo
   plan_n(ri, &p.npad, &nch, &NCn);
   const int nt_g = fg.nb * fg.nbox, nt_n = fn.nb * fn.nbox;
   p.NT = nt_g > nt_n ? nt_g : nt_n;
-  const int acc_cols = static_cast<int>(dora::round_up(fn.nmma1 > 0 ? 256 + fn.nmma1 : fn.nmma0, 32));
+  p.dbl = (fbk == 64 && fn.nmma1 == 0 && fg.nmma1 == 0 && p.NT <= 64) ? 1 : 0;   // fwd_norm_kernel<64, true>
+  // with p.dbl the epilogue reads 32-column chunks at NT on as well
+  const int acc_cols = static_cast<int>(
+      p.dbl ? dora::round_up(p.NT + dora::round_up(p.NT, 32), 32)
+            : dora::round_up(fn.nmma1 > 0 ? 256 + fn.nmma1 : fn.nmma0, 32));
   p.slot0 = acc_cols;
   p.y_bytes = static_cast<unsigned>(p.NT * 2 * nrow);
   // shared memory: as many N-side stages as tensor memory and shared memory
@@ -2528,6 +2557,9 @@ cudaError_t launch_fwd(const FwdPlan &fp, cudaStream_t cs, const CUtensorMap &mA
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  if (fp.p.fbk == 64 && fp.p.dbl)
+    return cudaLaunchKernelEx(&cfg, fwd_norm_kernel<64, true>, mA, mW0, mB, mAh_g, mAl_g, mAh_n, mAl_n, mGh, mGl, mBs,
+                              fp.p);
   if (fp.p.fbk == 64)
     return cudaLaunchKernelEx(&cfg, fwd_norm_kernel<64>, mA, mW0, mB, mAh_g, mAl_g, mAh_n, mAl_n, mGh, mGl, mBs, fp.p);
   return cudaLaunchKernelEx(&cfg, fwd_norm_kernel<32>, mA, mW0, mB, mAh_g, mAl_g, mAh_n, mAl_n, mGh, mGl, mBs, fp.p);
@@ -2789,6 +2821,7 @@ dora_status device_init(int device, int **errp) {
         cudaFuncSetAttribute(tc_gemm_kernel<true>, a, kSmemMax) != cudaSuccess ||
         cudaFuncSetAttribute(fwd_norm_kernel<32>, a, kSmemMax) != cudaSuccess ||
         cudaFuncSetAttribute(fwd_norm_kernel<64>, a, kSmemMax) != cudaSuccess ||
+        cudaFuncSetAttribute(fwd_norm_kernel<64, true>, a, kSmemMax) != cudaSuccess ||
         cudaFuncSetAttribute(tc16_kernel<32>, a, kSmemMax) != cudaSuccess ||
         cudaFuncSetAttribute(tc16_kernel<64>, a, kSmemMax) != cudaSuccess)
       return DORA_ERR_CUDA;

@@ -126,6 +126,10 @@ struct TcParams {
   int nb;           // N-side boxes per stage (per h / l operand)
   int NT;           // N-side rows in shared memory per stage (nb * nbox >= NC)
   int nmma0, nmma1; // N of the first / second MMA instruction of a chunk
+  // NT <= 64 (ROWS passes): h_x h_y and h_x l_y as one MMA of N = 2 NT over
+  // the stage's h and l rows together (accumulator columns [0, NT) and
+  // [NT, 2 NT), added in the epilogue): tc_gemm_kernel<XT, true>
+  int dbl;
   int tmem_cols;
   int slot0;        // first tensor-memory column of the M-side operand slots (one slot per stage)
   int stages;
@@ -209,7 +213,7 @@ __device__ void wait_drain(uint32_t bar, uint32_t parity) { wait_drain_ns(bar, p
 // loads an unswizzled [BK x 128] box and the converters read it column-wise
 // (lane = M row, conflict-free), the rest is unchanged.
 // ---------------------------------------------------------------------------
-template <bool XT>
+template <bool XT, bool DBL = false>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_gemm_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ CUtensorMap mX2,
                const __grid_constant__ CUtensorMap mY1h, const __grid_constant__ CUtensorMap mY1l,
@@ -336,6 +340,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ 
       bool ok = true;
       const uint32_t ic0 = idesc_bf16(p.nmma0);
       const uint32_t ic1 = p.nmma1 > 0 ? idesc_bf16(p.nmma1) : 0u;
+      const uint32_t icd = DBL ? idesc_bf16(2 * p.NT) : 0u;
       for (long long u = u_begin; u < u_end && ok;) {
         const int t = static_cast<int>(u / p.kbtot);
         const int kb0 = static_cast<int>(u - static_cast<long long>(t) * p.kbtot);
@@ -365,9 +370,15 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ 
             const uint32_t ah = sh + 8u * k, al = sl + 8u * k;
             {
               const uint64_t bh = sdesc<BK / 2>(yh + ko), bl = sdesc<BK / 2>(yl + ko);
-              mma_bf16_ta(tmem, ah, bh, ic0, acc0);
-              mma_bf16_ta(tmem, al, bh, ic0, 1u);
-              mma_bf16_ta(tmem, ah, bl, ic0, 1u);
+              if constexpr (DBL) {
+                mma_bf16_ta(tmem, ah, bh, icd, acc0);   // rows [h; l] of the stage: h_x h_y | h_x l_y
+                mma_bf16_ta(tmem, al, bh, ic0, 1u);
+                (void)bl;
+              } else {
+                mma_bf16_ta(tmem, ah, bh, ic0, acc0);
+                mma_bf16_ta(tmem, al, bh, ic0, 1u);
+                mma_bf16_ta(tmem, ah, bl, ic0, 1u);
+              }
             }
             if (p.nmma1 > 0) {
               const uint32_t no = 256u * kNRowBytes;
@@ -397,6 +408,18 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ 
     const int quad = warp & 3;            // tensor-memory lane group of this warp
     const int row = quad * 32 + lane;     // row within the M tile
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+    // accumulator columns [c, c + 32) of this warp's rows; with DBL the
+    // h_x l_y half (NT columns on) is added in
+    const int nt_cols = p.NT;
+    auto acc_ld32 = [&](int c, float (&v)[32]) {
+      tmem_ld32(lane_addr + static_cast<uint32_t>(c), v);
+      if constexpr (DBL) {
+        float w[32];
+        tmem_ld32(lane_addr + static_cast<uint32_t>(nt_cols + c), w);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) v[e] += w[e];
+      }
+    };
     int stage = 0;
     uint32_t phase = 0;
     uint32_t aphase = 0;
@@ -480,7 +503,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ 
         float *dst = p.part + ((tm * p.maxseg + seg) * kBM + row) * p.NC;
         for (int c = 0; c < p.NC; c += 32) {
           float v[32];
-          tmem_ld32(lane_addr + static_cast<uint32_t>(c), v);
+          acc_ld32(c, v);
           if (valid) {
 #pragma unroll
             for (int j = 0; j < 32; j += 4) {
@@ -499,7 +522,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ 
         float4 *mine = reinterpret_cast<float4 *>(p.part) + (tm * p.maxseg + seg) * slot_f4 + row;
         for (int c = 0; c < p.NC; c += 32) {
           float v[32];
-          tmem_ld32(lane_addr + static_cast<uint32_t>(c), v);
+          acc_ld32(c, v);
           if (valid) {
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
@@ -2328,9 +2351,12 @@ bool plan_gemm(int mode, int M, int64_t in, int r, int max_ctas, GemmPlan *gp) {
   p.NT = p.nb * p.nbox;
   p.nmma0 = p.NC <= 256 ? p.NC : 256;
   p.nmma1 = p.NC - p.nmma0;
-  // tensor memory: the accumulator (nmma0 columns at 0, nmma1 at 256), then one
+  p.dbl = (mode == kRows && p.nmma1 == 0 && p.NT <= 64) ? 1 : 0;
+  // tensor memory: the accumulator (nmma0 columns at 0, nmma1 at 256; with
+  // dbl the epilogue also reads 32-column chunks from NT on), then one
   // M-side operand slot per stage (kBK columns: bf16 h pairs, then l pairs)
-  const int acc_cols = static_cast<int>(dora::round_up(p.nmma1 > 0 ? 256 + p.nmma1 : p.nmma0, 32));
+  const int acc_cols = static_cast<int>(p.dbl ? dora::round_up(p.NT + dora::round_up(p.NT, 32), 32)
+                                              : dora::round_up(p.nmma1 > 0 ? 256 + p.nmma1 : p.nmma0, 32));
   const int slot_cols = kBK;
   p.slot0 = acc_cols;
   // a stage in shared memory: the raw M-side box, then the two N-side tiles
@@ -2695,9 +2721,11 @@ cudaError_t launch_gemm(const GemmPlan &gp, cudaStream_t cs, const CUtensorMap &
                         const CUtensorMap &y2l) {
   const dim3 grid(static_cast<unsigned>(gp.p.ctas)), block(kThreads);
   if (gp.xt)
-    tc_gemm_kernel<true><<<grid, block, gp.smem_bytes, cs>>>(x1, x2, y1h, y1l, y2h, y2l, gp.p);
+    gp.p.dbl ? tc_gemm_kernel<true, true><<<grid, block, gp.smem_bytes, cs>>>(x1, x2, y1h, y1l, y2h, y2l, gp.p)
+             : tc_gemm_kernel<true><<<grid, block, gp.smem_bytes, cs>>>(x1, x2, y1h, y1l, y2h, y2l, gp.p);
   else
-    tc_gemm_kernel<false><<<grid, block, gp.smem_bytes, cs>>>(x1, x2, y1h, y1l, y2h, y2l, gp.p);
+    gp.p.dbl ? tc_gemm_kernel<false, true><<<grid, block, gp.smem_bytes, cs>>>(x1, x2, y1h, y1l, y2h, y2l, gp.p)
+             : tc_gemm_kernel<false><<<grid, block, gp.smem_bytes, cs>>>(x1, x2, y1h, y1l, y2h, y2l, gp.p);
   return cudaGetLastError();
 }
 
@@ -2819,6 +2847,8 @@ dora_status device_init(int device, int **errp) {
     const cudaFuncAttribute a = cudaFuncAttributeMaxDynamicSharedMemorySize;
     if (cudaFuncSetAttribute(tc_gemm_kernel<false>, a, kSmemMax) != cudaSuccess ||
         cudaFuncSetAttribute(tc_gemm_kernel<true>, a, kSmemMax) != cudaSuccess ||
+        cudaFuncSetAttribute(tc_gemm_kernel<false, true>, a, kSmemMax) != cudaSuccess ||
+        cudaFuncSetAttribute(tc_gemm_kernel<true, true>, a, kSmemMax) != cudaSuccess ||
         cudaFuncSetAttribute(fwd_norm_kernel<32>, a, kSmemMax) != cudaSuccess ||
         cudaFuncSetAttribute(fwd_norm_kernel<64>, a, kSmemMax) != cudaSuccess ||
         cudaFuncSetAttribute(fwd_norm_kernel<64, true>, a, kSmemMax) != cudaSuccess ||

@@ -126,7 +126,7 @@ struct TcParams {
   int nb;           // N-side boxes per stage (per h / l operand)
   int NT;           // N-side rows in shared memory per stage (nb * nbox >= NC)
   int nmma0, nmma1; // N of the first / second MMA instruction of a chunk
-  // NT <= 64 (ROWS passes): h_x h_y and h_x l_y as one MMA of N = 2 NT over
+  // NT <= 128 (ROWS passes): h_x h_y and h_x l_y as one MMA of N = 2 NT over
   // the stage's h and l rows together (accumulator columns [0, NT) and
   // [NT, 2 NT), added in the epilogue): tc_gemm_kernel<XT, true>
   int dbl;
@@ -2351,7 +2351,7 @@ bool plan_gemm(int mode, int M, int64_t in, int r, int max_ctas, GemmPlan *gp) {
   p.NT = p.nb * p.nbox;
   p.nmma0 = p.NC <= 256 ? p.NC : 256;
   p.nmma1 = p.NC - p.nmma0;
-  p.dbl = (mode == kRows && p.nmma1 == 0 && p.NT <= 64) ? 1 : 0;
+  p.dbl = (mode == kRows && p.nmma1 == 0 && p.NT <= 128) ? 1 : 0;
   // tensor memory: the accumulator (nmma0 columns at 0, nmma1 at 256; with
   // dbl the epilogue also reads 32-column chunks from NT on), then one
   // M-side operand slot per stage (kBK columns: bf16 h pairs, then l pairs)

@@ -117,6 +117,8 @@ def _run_and_check(d, d_mag):
     (200, 136, 33),       # the smallest r of 64 x 64 tiles
     (2000, 4104, 256),    # the largest r of the CUDA-core Gram; slices longer than 128 (one wave)
     (300, 520, 257),      # the smallest r of the tensor-core Gram passes
+    (400, 520, 100),      # N-side tile of 112 rows: one MMA over the stacked h and l rows (N = 224)
+    (260, 200, 113),      # N-side tile of 128 rows, the largest so taken (N = 256)
 ])
 def test_norm_grad_shapes(out, inp, r):
     d, d_mag = _case(out, inp, r, 9100 + out + r)

@@ -213,14 +213,19 @@ __device__ void wait_drain(uint32_t bar, uint32_t parity) { wait_drain_ns(bar, p
 // loads an unswizzled [BK x 128] box and the converters read it column-wise
 // (lane = M row, conflict-free), the rest is unchanged.
 // ---------------------------------------------------------------------------
-template <bool XT, bool DBL = false>
+// BKT: K indices per K block, 32 (one 128-byte fp32 box row) or 64 (two
+// 128-byte-swizzled boxes side by side; XT: a [64 x 128] box), with N-side
+// rows of 64 or 128 bytes
+template <bool XT, bool DBL = false, int BKT = kBK>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_gemm_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ CUtensorMap mX2,
                const __grid_constant__ CUtensorMap mY1h, const __grid_constant__ CUtensorMap mY1l,
                const __grid_constant__ CUtensorMap mY2h, const __grid_constant__ CUtensorMap mY2l,
                const TcParams p) {
-  constexpr int BK = kBK;
-  constexpr int kRowBytes = BK * 4;    // one swizzle span of the raw fp32 M-side box
+  constexpr int BK = BKT;
+  static_assert(BK == 32 || BK == 64, "K blocks of 32 or 64");
+  constexpr int kRowBytes = BK * 4;    // the raw fp32 M-side block's row (XT: column)
+  constexpr int kBoxBytes = kBM * 128; // one 128-byte-swizzled raw box [128 rows x 32 fp32]
   constexpr int kNRowBytes = BK * 2;   // one N-side row of BK bf16 (h or l)
   constexpr int kSlotCols = BK;        // tensor-memory columns of one M-side operand slot (h, then l)
   extern __shared__ uint8_t smem_raw[];
@@ -300,8 +305,13 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ 
           const uint32_t yl = yh + static_cast<uint32_t>(p.NT) * kNRowBytes;
           const bool seg1 = kb < p.kb1;
           const int kx = (seg1 ? kb : kb - p.kb1) * BK;    // first K index of the block
-          if (XT) tma_load_2d(xs, seg1 ? &mX1 : &mX2, mt * kBM, kx, fb);
-          else tma_load_2d(xs, seg1 ? &mX1 : &mX2, kx, mt * kBM, fb);
+          if (XT) {
+            tma_load_2d(xs, seg1 ? &mX1 : &mX2, mt * kBM, kx, fb);
+          } else {
+#pragma unroll
+            for (int bx = 0; bx < BK / 32; ++bx)
+              tma_load_2d(xs + bx * kBoxBytes, seg1 ? &mX1 : &mX2, kx + 32 * bx, mt * kBM, fb);
+          }
           // the N-side tile of the chunk: the bf16 h and l operands
           for (int i = 0; i < p.nb; ++i) {
             const int ro = i * p.nbox;
@@ -443,7 +453,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ 
         // (swz_chunk); one K = 16 step at a time, split into the stage's
         // tensor-memory operand slot: 8 columns of h pairs and 8 of l pairs
         const uint8_t *xbox = smem + static_cast<size_t>(stage) * p.stage_bytes;
-        const float4 *xr = reinterpret_cast<const float4 *>(xbox + row * kRowBytes);
+        const float4 *xr = reinterpret_cast<const float4 *>(xbox + row * 128);   // row `row` of raw box 0
         const float *xc = reinterpret_cast<const float *>(xbox) + row;   // XT: column `row` of [BK][128]
         const uint32_t slot = lane_addr + static_cast<uint32_t>(p.slot0 + stage * kSlotCols);
         auto load8 = [&](int q, float (&v)[8]) {
@@ -451,7 +461,9 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mX1, const __grid_constant__ 
 #pragma unroll
             for (int e = 0; e < 8; ++e) v[e] = xc[(8 * q + e) * kBM];
           } else {
-            const float4 a = xr[swz_chunk<BK>(2 * q, row)], b = xr[swz_chunk<BK>(2 * q + 1, row)];
+            // K indices 8q .. 8q + 7: chunks 2q, 2q + 1 of raw box q / 4
+            const float4 *xq = xr + (q >> 2) * (kBoxBytes / 16);
+            const float4 a = xq[swz_chunk<32>((2 * q) & 7, row)], b = xq[swz_chunk<32>((2 * q + 1) & 7, row)];
             v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
             v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
           }
@@ -2308,6 +2320,7 @@ __global__ void __launch_bounds__(256) gram_reduce3_kernel(const float *__restri
 struct GemmPlan {
   TcParams p;
   bool xt;  // M-side operand stored transposed (the kernel instance)
+  int bk;   // K indices per K block (the kernel instance): 32 or 64
   size_t smem_bytes;
   size_t part_bytes;
 };
@@ -2326,10 +2339,11 @@ void plan_n(int r, int *npad, int *nchunks, int *NC) {
 }
 
 // K = in (+ r for the norm and row passes); at most max_ctas CTAs
-bool plan_gemm(int mode, int M, int64_t in, int r, int max_ctas, GemmPlan *gp) {
+bool plan_gemm(int mode, int M, int64_t in, int r, int max_ctas, GemmPlan *gp, int bk = kBK) {
   TcParams &p = gp->p;
   std::memset(&p, 0, sizeof(p));
   gp->xt = false;
+  gp->bk = bk;
   p.mode = mode;
   p.M = M;
   int npad;
@@ -2340,10 +2354,10 @@ bool plan_gemm(int mode, int M, int64_t in, int r, int max_ctas, GemmPlan *gp) {
     p.nchunks = static_cast<int>(dora::ceil_div(npad, p.NC));
     p.sym = 1;
   }
-  const int row_bytes = kBK * 4;    // the raw fp32 M-side box
-  const int nrow_bytes = kBK * 2;   // each bf16 N-side operand
-  p.kb1 = static_cast<int>(dora::ceil_div(in, kBK));
-  p.kbtot = p.kb1 + (mode != kGram ? static_cast<int>(dora::ceil_div(r, kBK)) : 0);
+  const int row_bytes = bk * 4;    // the raw fp32 M-side block
+  const int nrow_bytes = bk * 2;   // each bf16 N-side operand
+  p.kb1 = static_cast<int>(dora::ceil_div(in, bk));
+  p.kbtot = p.kb1 + (mode != kGram ? static_cast<int>(dora::ceil_div(r, bk)) : 0);
   // the N-side tile in nb boxes of nbox rows (a multiple of 8, so every box
   // starts on a swizzle-pattern boundary; at most 256, the box limit)
   p.nb = static_cast<int>(dora::ceil_div(p.NC, 256));
@@ -2354,10 +2368,10 @@ bool plan_gemm(int mode, int M, int64_t in, int r, int max_ctas, GemmPlan *gp) {
   p.dbl = (mode == kRows && p.nmma1 == 0 && p.NT <= 128) ? 1 : 0;
   // tensor memory: the accumulator (nmma0 columns at 0, nmma1 at 256; with
   // dbl the epilogue also reads 32-column chunks from NT on), then one
-  // M-side operand slot per stage (kBK columns: bf16 h pairs, then l pairs)
+  // M-side operand slot per stage (bk columns: bf16 h pairs, then l pairs)
   const int acc_cols = static_cast<int>(p.dbl ? dora::round_up(p.NT + dora::round_up(p.NT, 32), 32)
                                               : dora::round_up(p.nmma1 > 0 ? 256 + p.nmma1 : p.nmma0, 32));
-  const int slot_cols = kBK;
+  const int slot_cols = bk;
   p.slot0 = acc_cols;
   // a stage in shared memory: the raw M-side box, then the two N-side tiles
   p.stage_bytes = static_cast<unsigned>(kBM * row_bytes + 2 * p.NT * nrow_bytes);
@@ -2654,12 +2668,18 @@ bool plan_bwd(int64_t out, int64_t in, int64_t r, int sms, BwdPlans *P, BwdLayou
   const int ri = static_cast<int>(r);
   if (!plan_gemm(kGram, ri, in, ri, sms, &P->gg)) return false;
   if (!plan_gemm(kGram, ri, out, ri, sms, &P->gh)) return false;
-  if (!plan_gemm(kRows, static_cast<int>(out), in, ri, sms, &P->gb)) return false;
-  if (!plan_gemm(kRows, static_cast<int>(in), out, ri, sms, &P->ga)) return false;
+  // the W0 passes: 64-wide K blocks where four stages fit (with three, at
+  // r = 128, they measured 4% slower than 32-wide ones), else 32-wide
+  auto rows_plan = [&](int M, int64_t K, GemmPlan *gp) {
+    if (plan_gemm(kRows, M, K, ri, sms, gp, 64) && gp->p.stages >= 4) return true;
+    return plan_gemm(kRows, M, K, ri, sms, gp, 32);
+  };
+  if (!rows_plan(static_cast<int>(out), in, &P->gb)) return false;
+  if (!rows_plan(static_cast<int>(in), out, &P->ga)) return false;
   P->gh.xt = true;
   P->ga.xt = true;
-  P->gb.p.chain = kChainK / kBK;
-  P->ga.p.chain = kChainK / kBK;
+  P->gb.p.chain = kChainK / P->gb.bk;
+  P->ga.p.chain = kChainK / P->ga.bk;
   P->small = r <= kSgMaxR;
   SgDims &sg = P->sg;
   std::memset(&sg, 0, sizeof(sg));
@@ -2720,12 +2740,18 @@ cudaError_t launch_gemm(const GemmPlan &gp, cudaStream_t cs, const CUtensorMap &
                         const CUtensorMap &y1h, const CUtensorMap &y1l, const CUtensorMap &y2h,
                         const CUtensorMap &y2l) {
   const dim3 grid(static_cast<unsigned>(gp.p.ctas)), block(kThreads);
-  if (gp.xt)
-    gp.p.dbl ? tc_gemm_kernel<true, true><<<grid, block, gp.smem_bytes, cs>>>(x1, x2, y1h, y1l, y2h, y2l, gp.p)
-             : tc_gemm_kernel<true><<<grid, block, gp.smem_bytes, cs>>>(x1, x2, y1h, y1l, y2h, y2l, gp.p);
-  else
-    gp.p.dbl ? tc_gemm_kernel<false, true><<<grid, block, gp.smem_bytes, cs>>>(x1, x2, y1h, y1l, y2h, y2l, gp.p)
-             : tc_gemm_kernel<false><<<grid, block, gp.smem_bytes, cs>>>(x1, x2, y1h, y1l, y2h, y2l, gp.p);
+  const size_t sm = gp.smem_bytes;
+#define DORA_TC_LAUNCH(XT_, DBL_, BK_) \
+  tc_gemm_kernel<XT_, DBL_, BK_><<<grid, block, sm, cs>>>(x1, x2, y1h, y1l, y2h, y2l, gp.p)
+  const bool d = gp.p.dbl != 0;
+  if (gp.bk == 64) {
+    if (gp.xt) d ? DORA_TC_LAUNCH(true, true, 64) : DORA_TC_LAUNCH(true, false, 64);
+    else d ? DORA_TC_LAUNCH(false, true, 64) : DORA_TC_LAUNCH(false, false, 64);
+  } else {
+    if (gp.xt) d ? DORA_TC_LAUNCH(true, true, 32) : DORA_TC_LAUNCH(true, false, 32);
+    else d ? DORA_TC_LAUNCH(false, true, 32) : DORA_TC_LAUNCH(false, false, 32);
+  }
+#undef DORA_TC_LAUNCH
   return cudaGetLastError();
 }
 
@@ -2849,6 +2875,10 @@ dora_status device_init(int device, int **errp) {
         cudaFuncSetAttribute(tc_gemm_kernel<true>, a, kSmemMax) != cudaSuccess ||
         cudaFuncSetAttribute(tc_gemm_kernel<false, true>, a, kSmemMax) != cudaSuccess ||
         cudaFuncSetAttribute(tc_gemm_kernel<true, true>, a, kSmemMax) != cudaSuccess ||
+        cudaFuncSetAttribute(tc_gemm_kernel<false, false, 64>, a, kSmemMax) != cudaSuccess ||
+        cudaFuncSetAttribute(tc_gemm_kernel<true, false, 64>, a, kSmemMax) != cudaSuccess ||
+        cudaFuncSetAttribute(tc_gemm_kernel<false, true, 64>, a, kSmemMax) != cudaSuccess ||
+        cudaFuncSetAttribute(tc_gemm_kernel<true, true, 64>, a, kSmemMax) != cudaSuccess ||
         cudaFuncSetAttribute(fwd_norm_kernel<32>, a, kSmemMax) != cudaSuccess ||
         cudaFuncSetAttribute(fwd_norm_kernel<64>, a, kSmemMax) != cudaSuccess ||
         cudaFuncSetAttribute(fwd_norm_kernel<64, true>, a, kSmemMax) != cudaSuccess ||
@@ -3205,18 +3235,19 @@ extern "C" dora_status dora_norm_factored_bwd(const float *W0, const float *A, c
   // tensor maps: the raw fp32 M-side boxes (one K block of 32 by 128 rows) and
   // the bf16 N-side boxes (64-byte rows of 32 K indices)
   const GemmPlan &gg = P.gg, &gh = P.gh, &gb = P.gb, &ga = P.ga;
-  const int rb = 4 * kBK, nb = 2 * kBK;
+  // raw fp32 boxes of 32 K (128-byte rows); N-side rows of each pass's K block
+  const int rb = 4 * kBK, nb = 2 * kBK, nbb = 2 * gb.bk, nba = 2 * ga.bk;
   CUtensorMap mA, mAh_g, mAl_g, mBt, mYh_h, mYl_h, mW0, mB, mAh_b, mAl_b, mGh, mGl, mW0t, mAt, mYh_a, mYl_a, mHh, mHl;
   bool ok = make_map(&mW0, W0, false, out, in, in, kBM, rb) && make_map(&mB, Bk, false, out, ldb, ldb, kBM, rb) &&
-            make_map(&mAh_b, a_h, true, r, in8, in8, gb.p.nbox, nb) &&
-            make_map(&mAl_b, a_l, true, r, in8, in8, gb.p.nbox, nb) &&
-            make_map(&mGh, g_h, true, npad, npad, npad, gb.p.nbox, nb) &&
-            make_map(&mGl, g_l, true, npad, npad, npad, gb.p.nbox, nb) &&
-            make_map_t(&mW0t, W0, out, in, in, kBK) && make_map_t(&mAt, A, r, in, in, kBK) &&
-            make_map(&mYh_a, y_h, true, r, out8, out8, ga.p.nbox, nb) &&
-            make_map(&mYl_a, y_l, true, r, out8, out8, ga.p.nbox, nb) &&
-            make_map(&mHh, h_h, true, npad, npad, npad, ga.p.nbox, nb) &&
-            make_map(&mHl, h_l, true, npad, npad, npad, ga.p.nbox, nb);
+            make_map(&mAh_b, a_h, true, r, in8, in8, gb.p.nbox, nbb) &&
+            make_map(&mAl_b, a_l, true, r, in8, in8, gb.p.nbox, nbb) &&
+            make_map(&mGh, g_h, true, npad, npad, npad, gb.p.nbox, nbb) &&
+            make_map(&mGl, g_l, true, npad, npad, npad, gb.p.nbox, nbb) &&
+            make_map_t(&mW0t, W0, out, in, in, ga.bk) && make_map_t(&mAt, A, r, in, in, ga.bk) &&
+            make_map(&mYh_a, y_h, true, r, out8, out8, ga.p.nbox, nba) &&
+            make_map(&mYl_a, y_l, true, r, out8, out8, ga.p.nbox, nba) &&
+            make_map(&mHh, h_h, true, npad, npad, npad, ga.p.nbox, nba) &&
+            make_map(&mHl, h_l, true, npad, npad, npad, ga.p.nbox, nba);
   if (ok && !P.small)
     ok = make_map(&mA, A, false, r, in, in, kBM, rb) && make_map(&mAh_g, a_h, true, r, in8, in8, gg.p.nbox, nb) &&
          make_map(&mAl_g, a_l, true, r, in8, in8, gg.p.nbox, nb) && make_map_t(&mBt, Bk, out, r, ldb, kBK) &&

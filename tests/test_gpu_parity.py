@@ -39,6 +39,8 @@ def test_attention_projection_reduced_tokens():
     (64, 8, 1024, 5),          # the largest rank: 36 Gram tiles of one K piece each, more Gram tiles than
                                # norm units per CTA, three N chunks of 352
     (2048, 64, 1024, 12),      # the largest rank with 152 CTAs, 36 of them Gram CTAs
+    (700, 1000, 64, 20),       # N-side tile of 64 rows, the largest with h_x [h_y; l_y] as one MMA (N = 128)
+    (700, 1000, 65, 20),       # 80 rows: three MMAs per K step again
 ])
 def test_shapes_span_tiles_and_ragged_tails(out, inp, r, T):
     sh = wl.shape("high_rank", out=out, inp=inp, r=r, T=T)
